@@ -1,0 +1,223 @@
+/*
+ * dqmoe.h — C ABI of the block-quantized GEMV / sparse-MoE library for one
+ * GB300 GPU (sm_103a).
+ *
+ * What is computed.  Three offloading inference engines describe the same
+ * data-parallel decode hot path: weight matrices stored as llama.cpp-style
+ * quantized super-blocks (Q4_K, Q6_K, Q8_0) multiplied by activations, and a
+ * sparse mixture-of-experts layer that activates a few experts per token.
+ *   - Titan Engine: trillion-parameter inference on consumer hardware
+ *     (zingnex.cn), sections "MoE 专家流式加载" (only 2 of 8 experts are
+ *     active per forward pass) and "激进量化策略" (Q4_K weights).
+ *   - KTransformers (news.fishai.com.cn/news/2715575), section "支持的量化格式"
+ *     (Q4_K_M, Q6_K, Q8_0) and "技术原理" (sparse MoE matrices, CUDA Graph:
+ *     one graph launch per decode step).
+ *   - NTransformer, Show HN: Llama 3.1 70B on a single RTX 3090
+ *     (hn.213312.xyz/article/47104667), section "量化支持" (Q4_0/Q8_0/Q4_K_M/
+ *     Q5_K/Q6_K/F16/F32) and "核心性能" (decode speed follows resident bytes).
+ * The pages name the formats but print no byte layout.  This library reads
+ * them as the GGUF/llama.cpp layouts spelled out below (byte for byte).
+ *
+ * Conventions shared by every entry point.
+ *   - Every pointer argument named "device" is a CUDA device pointer owned by
+ *     the caller; the library never frees it and never keeps it after the call
+ *     returns (calls are asynchronous on `stream`; the caller keeps buffers
+ *     alive until the stream has passed the call).
+ *   - `stream` is a cudaStream_t passed as void*; NULL means the legacy default
+ *     stream.  No entry point synchronises the stream or the device, and no
+ *     entry point allocates device memory: scratch is passed in by the caller.
+ *     So a sequence of calls can be captured in a CUDA graph.
+ *   - Return value: DQ_OK (0) or a negative dq_status.  Arguments are checked
+ *     before anything is launched: on an argument error nothing is enqueued.
+ *     DQ_ERR_CUDA means a launch reported an error (cudaGetLastError); the
+ *     stream state is then whatever CUDA left it in.
+ *   - No C++ exception crosses this boundary.  Kernels never trap: a device-
+ *     side wait that runs past its time limit records DQ_ERR_DEVICE_TIMEOUT in
+ *     a device status word (see dq_device_status) and returns.
+ *
+ * Layouts.
+ *   - Quantized matrix W with N rows and K columns: row n is the K/QK blocks
+ *     of that row, consecutive, starting at byte n * row_bytes where
+ *     row_bytes = (K/QK) * block_bytes.  Rows are consecutive.  W must be
+ *     16-byte aligned and row_bytes a multiple of 16 (true for every shape
+ *     with K a multiple of 256 for Q4_K and Q8_0, of 2048 for Q6_K).
+ *   - Activations x: [batch][K] row-major in x_dtype.  Outputs y: [batch][N]
+ *     row-major, always fp32 (MoE activations reach ~1e7, beyond fp16).
+ */
+#ifndef DQMOE_H
+#define DQMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------------------ */
+/* Block formats.                                                           */
+/*                                                                          */
+/* Q4_K super-block, 256 weights in 144 bytes:                              */
+/*   bytes 0-1   d     fp16 super-block scale                               */
+/*   bytes 2-3   dmin  fp16 super-block min scale                           */
+/*   bytes 4-15  12 bytes holding eight 6-bit (sc_j, m_j) pairs, j = 0..7:  */
+/*               j<4 : sc_j = s[j] & 63,  m_j = s[j+4] & 63                 */
+/*               j>=4: sc_j = (s[j+4] & 15) | ((s[j-4] >> 6) << 4)          */
+/*                     m_j  = (s[j+4] >> 4) | ((s[j]   >> 6) << 4)          */
+/*   bytes 16-143 qs[128]: four 32-byte groups c = 0..3; byte l of group c  */
+/*               holds weight 64c+l in its low nibble (sub-block 2c) and    */
+/*               weight 64c+32+l in its high nibble (sub-block 2c+1).       */
+/*   weight i of sub-block j: w = d*sc_j*q - dmin*m_j, q in [0,15].         */
+/* Q6_K super-block, 256 weights in 210 bytes:                              */
+/*   bytes 0-127 ql[128], 128-191 qh[64], 192-207 int8 scales[16],          */
+/*   208-209 fp16 d.  Half h (0,1) uses ql[64h..], qh[32h..]; for l=0..31:  */
+/*     weight 128h+l    : low nibble of ql[64h+l],    qh bits 0-1          */
+/*     weight 128h+l+32 : low nibble of ql[64h+l+32], qh bits 2-3          */
+/*     weight 128h+l+64 : high nibble of ql[64h+l],   qh bits 4-5          */
+/*     weight 128h+l+96 : high nibble of ql[64h+l+32],qh bits 6-7          */
+/*   (qh byte is qh[32h+l], its two bits are the high bits of the 6-bit q). */
+/*   weight i: w = d * scales[i/16] * (q - 32), q in [0,63].                */
+/* Q8_0 block, 32 weights in 34 bytes: fp16 d, int8 qs[32]; w = d*q.        */
+/* ------------------------------------------------------------------------ */
+typedef enum { DQ_Q4_K = 1, DQ_Q6_K = 2, DQ_Q8_0 = 3 } dq_fmt;
+
+/* Activation element types accepted by the entry points. */
+typedef enum { DQ_F32 = 0, DQ_F16 = 1, DQ_BF16 = 2 } dq_dtype;
+
+typedef enum {
+  DQ_OK = 0,
+  DQ_ERR_ARG = -1,          /* null pointer, bad size, K not a multiple of QK, batch out of range */
+  DQ_ERR_ALIGN = -2,        /* a pointer or a row stride is not 16-byte aligned */
+  DQ_ERR_UNSUPPORTED = -3,  /* format / dtype / shape this build does not handle */
+  DQ_ERR_WORKSPACE = -4,    /* workspace pointer null or smaller than dq_moe_workspace_size */
+  DQ_ERR_CUDA = -5,         /* a CUDA runtime call or launch failed */
+  DQ_ERR_DEVICE_TIMEOUT = -6 /* a kernel's bounded wait ran out (read via dq_device_status) */
+} dq_status;
+
+#define DQ_QK_K 256         /* weights per Q4_K / Q6_K super-block */
+#define DQ_QK8_0 32         /* weights per Q8_0 block */
+#define DQ_Q4_K_BYTES 144
+#define DQ_Q6_K_BYTES 210
+#define DQ_Q8_0_BYTES 34
+#define DQ_MAX_BATCH 8      /* activation columns per dq_qgemv call */
+
+/* Weights per block and bytes per block of `fmt`.  Host-only, no CUDA.
+ * Returns DQ_ERR_ARG for an unknown format or null outputs. */
+int dq_block_geometry(int fmt, int* weights_per_block, int* bytes_per_block);
+
+/* dq_dequant — decode `n_weights` weights (a whole number of blocks) of format
+ * `fmt` into fp32.  Step "block decode" of the path; exposed so the decoded
+ * values can be compared bit for bit (every closed form above is exact in
+ * fp32 up to the final rounding of the Q4_K subtraction).
+ *   blocks : device, n_weights/QK consecutive blocks, 16-byte aligned for
+ *            Q4_K; 2-byte aligned for Q6_K/Q8_0 (their blocks are 210/34 B).
+ *   out    : device fp32 [n_weights], 4-byte aligned.
+ * Errors: DQ_ERR_ARG (null, n_weights <= 0 or not a multiple of QK),
+ *         DQ_ERR_ALIGN, DQ_ERR_CUDA. */
+int dq_dequant(int fmt, const void* blocks, int64_t n_weights, float* out,
+               void* stream);
+
+/* dq_qgemv — y[b][n] = sum_k W[n][k] * x[b][k] for b < batch, fp32 accumulate,
+ * W decoded inside the kernel (never materialised).  The decode linear of the
+ * engines above ([NTransformer, §核心性能]: decode rate is set by the bytes of
+ * the resident quantized weights; [Titan Engine, §性能表现]).
+ *   W      : device, N rows of K/QK blocks (layout above), 16-byte aligned.
+ *   x      : device [batch][K] of x_dtype, 16-byte aligned.
+ *   y      : device fp32 [batch][N], 16-byte aligned; fully overwritten.
+ *   batch  : 1..DQ_MAX_BATCH.
+ * fp16/bf16 activations run on the tensor-core path (weights decoded to fp16
+ * in registers); fp32 activations run on an fp32 CUDA-core path (decode and
+ * products in fp32).
+ * Errors: DQ_ERR_ARG (null, N/K <= 0, K % QK != 0, batch outside 1..8),
+ *         DQ_ERR_ALIGN (W, x, y not 16-B aligned; Q6_K needs K % 2048 == 0
+ *         so that rows stay 16-B aligned), DQ_ERR_CUDA. */
+int dq_qgemv(int fmt, const void* W, int64_t N, int64_t K, const void* x,
+             int x_dtype, int batch, float* y, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Sparse MoE layer.                                                         */
+/*   logits[t][e] = sum_h router_W[e][h] * x[t][h]            (fp32)         */
+/*   sel(t)       = the top_k largest logits, lowest index first on ties     */
+/*   gate[t][i]   = exp(l_i - l_max) / sum_{j in sel} exp(l_j - l_max)       */
+/*                  (softmax over all E, renormalised over the selection)    */
+/*   FFN_e(v)     = W_down_e * ( silu(W_gate_e v) (.) (W_up_e v) ),          */
+/*                  silu(g) = g / (1 + exp(-g))                              */
+/*   y[t]         = sum_i gate[t][i] * FFN_{sel_i}(x_t) + sum_s FFN_shared_s(x_t) */
+/* [Titan Engine, §MoE 专家流式加载] (activate 2 of 8 experts per forward);  */
+/* [KTransformers, §技术原理] (sparse MoE matrices).  The pages give no      */
+/* router or FFN formula: softmax top-k renormalised with SwiGLU experts is */
+/* the Mixtral / DeepSeek-V3 (plain softmax routing) reading.                */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+  int32_t E;          /* routed experts, 1..256 */
+  int32_t top_k;      /* experts per token, 1..min(E, 8) */
+  int32_t hidden;     /* H: length of x rows, rows of W_down */
+  int32_t ffn;        /* F: rows of W_gate / W_up, columns of W_down */
+  int32_t n_shared;   /* always-on shared experts, 0..4, weight 1 each */
+  int32_t fmt;        /* dq_fmt of every expert matrix */
+  const float* router_W; /* device fp32 [E][H] */
+  const void* w_gate; /* device, E stacked [F rows][H/QK blocks] matrices */
+  const void* w_up;   /* device, E stacked [F][H/QK] */
+  const void* w_down; /* device, E stacked [H rows][F/QK blocks] */
+  const void* sh_gate; /* device, n_shared stacked [F][H/QK]; NULL if n_shared == 0 */
+  const void* sh_up;   /* device, n_shared stacked [F][H/QK] */
+  const void* sh_down; /* device, n_shared stacked [H][F/QK] */
+} dq_moe_desc;
+
+/* Bytes of scratch dq_moe_forward needs for T tokens (host-only, no CUDA).
+ * Errors: DQ_ERR_ARG on a malformed descriptor or T <= 0,
+ *         DQ_ERR_UNSUPPORTED on shapes outside the limits above. */
+int dq_moe_workspace_size(const dq_moe_desc* desc, int T, size_t* bytes);
+
+/* dq_moe_router — steps "router" and "top-k + gates" alone.
+ *   router_W : device fp32 [E][H];  x : device [T][H] of x_dtype.
+ *   logits   : device fp32 [T][E] (nullable).
+ *   topk_idx : device int32 [T][top_k], slot order = descending logit,
+ *              lowest expert index first among equal logits.
+ *   topk_gate: device fp32 [T][top_k], renormalised softmax weights.
+ * Errors: DQ_ERR_ARG, DQ_ERR_ALIGN (x, router_W not 16-B aligned),
+ *         DQ_ERR_UNSUPPORTED (E > 256 or top_k > 8), DQ_ERR_CUDA. */
+int dq_moe_router(const float* router_W, int E, int H, const void* x,
+                  int x_dtype, int T, int top_k, float* logits,
+                  int32_t* topk_idx, float* topk_gate, void* stream);
+
+/* dq_moe_permute — step "token -> expert permute" alone.  The T*top_k
+ * (token, slot) pairs p = t*top_k + slot are ordered by (expert, p):
+ *   offsets : device int32 [E+1], offsets[e] = number of pairs routed to
+ *             experts < e (exclusive prefix sum of the per-expert counts).
+ *   sorted  : device int32 [T*top_k], the pair ids p in that order (stable).
+ * Errors: DQ_ERR_ARG, DQ_ERR_UNSUPPORTED (E > 256, T*top_k > 65536),
+ *         DQ_ERR_CUDA.  Expert ids outside [0, E) are out of contract. */
+int dq_moe_permute(const int32_t* topk_idx, int T, int top_k, int E,
+                   int32_t* offsets, int32_t* sorted, void* stream);
+
+/* dq_moe_forward — the whole layer for T tokens (router, top-k, permute,
+ * grouped gate/up with SwiGLU, grouped down, weighted combine + shared).
+ *   x        : device [T][H] of x_dtype, 16-byte aligned.
+ *   y        : device fp32 [T][H], fully overwritten.
+ *   ws       : device scratch of at least dq_moe_workspace_size bytes,
+ *              256-byte aligned; contents on entry are ignored.
+ *   topk_idx, topk_gate, logits : optional device outputs as in
+ *              dq_moe_router (NULL to skip).
+ * All launches go on `stream` with no host synchronisation, so the layer is
+ * capturable in one CUDA graph ([KTransformers, §技术原理]: one graph call
+ * per decode step).
+ * Errors: DQ_ERR_ARG, DQ_ERR_ALIGN, DQ_ERR_UNSUPPORTED, DQ_ERR_WORKSPACE,
+ *         DQ_ERR_CUDA. */
+int dq_moe_forward(const dq_moe_desc* desc, const void* x, int x_dtype, int T,
+                   float* y, void* ws, size_t ws_bytes, int32_t* topk_idx,
+                   float* topk_gate, float* logits, void* stream);
+
+/* Human-readable name of a dq_status value (static string, never NULL). */
+const char* dq_status_string(int status);
+
+/* Reads and clears the device status word of the current device: DQ_OK, or
+ * DQ_ERR_DEVICE_TIMEOUT if a kernel gave up a bounded wait since the last
+ * read.  Synchronous (waits for the device).  Errors: DQ_ERR_ARG, DQ_ERR_CUDA. */
+int dq_device_status(int* status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DQMOE_H */
