@@ -1,0 +1,504 @@
+"""Benchmark: qGEMV weight GB/s (% of HBM peak) and MoE-layer tokens/s on GB300.
+
+One step = the seven Q4_K linears of a Llama-3-8B decode layer (q, k, v, o,
+gate, up, down; fp16 activations, batch 1), each a dq_qgemv call, replayed as
+one CUDA graph per step (one graph launch per decode step, the way the
+KTransformers page runs decode).  value = algorithmic weight bytes streamed
+per step / device time per step.  Inputs are resident in HBM before timing;
+L2 is defeated by rotating 4 copies of the layer's weights (491 MB > 3x L2).
+The same run also times the 70B-shaped batch-1 Q4_K gate GEMV (the north-star
+shape) and the two MoE layers (tokens/s), and the CPU oracle on a bounded
+sample of the same work.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "qGEMV weight GB/s (% of HBM peak); MoE-layer tokens/s at 1 GB300"
+Q4_K = 1
+ROTATE = 4
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-moe", action="store_true", help="skip the MoE-layer lines")
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return float(m["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def weight_bytes(fmt, N, K):
+    qk, nb = synth.BLOCK[fmt]
+    return N * (K // qk) * nb
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for nme, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nme)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only: each rank runs its own copy)
+# ---------------------------------------------------------------------------
+def dist_setup(ngpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world <= 1:
+        return 0, 1, 0, None
+    import torch.distributed as dist
+    rank = int(os.environ["RANK"])
+    local = int(os.environ.get("LOCAL_RANK", rank))
+    backend = "nccl"
+    dist.init_process_group(backend=backend)
+    return rank, world, local, dist
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, v):
+    if dist is None:
+        return v
+    import torch
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline (bounded sample of the same work)
+# ---------------------------------------------------------------------------
+def oracle_sample(budget_s=12.0, seed=synth.BASE_SEED + 1):
+    import oracle
+    g = synth.streams(seed, 2)
+    x = synth.activations(g[1], (1, 14336), 1)
+    threads = oracle.default_threads()
+    total_bytes, total_t, rows_done = 0, 0.0, 0
+    rng = np.random.default_rng(0)
+    mats = {}
+    for name, N, K in synth.LLAMA8B_LINEARS:
+        key = (N, K)
+        if key not in mats:
+            mats[key] = synth.quant_matrix(g[0], Q4_K, 512, K)   # 512 sampled rows
+    t_end = time.time() + budget_s
+    while time.time() < t_end:
+        for name, N, K in synth.LLAMA8B_LINEARS:
+            W = mats[(N, K)]
+            rows = np.sort(rng.choice(512, 256, replace=False)).astype(np.int64)
+            t0 = time.perf_counter()
+            oracle.qgemv(Q4_K, W, 512, K, x[:, :K], 1, 1, rows=rows, nthreads=threads)
+            total_t += time.perf_counter() - t0
+            total_bytes += weight_bytes(Q4_K, len(rows), K)
+            rows_done += len(rows)
+    return {"value": total_bytes / total_t / 1e9, "unit": "GB/s", "cores": threads,
+            "kind": "oracle",
+            "sample": "%d rows of the 7 Llama-3-8B linears (256-row random samples), batch 1, "
+                      "fp16 x, %.1f s of CPU time" % (rows_done, total_t)}
+
+
+def run_reference(args):
+    rank, world, local, dist = dist_setup(args.gpus)
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        oracle_sample(budget_s=1.0)
+    budget = max(5.0, min(20.0, 2.0 * args.steps / 10.0))
+    t0 = time.time()
+    r = oracle_sample(budget_s=budget)
+    wall = time.time() - t0
+    line = {"metric": METRIC, "impl": "reference", "value": r["value"], "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "llama3-8b decode-layer linears, Q4_K, fp16 x, batch 1 "
+                                   "(oracle on sampled rows)"},
+            "cpu_baseline": r,
+            "e2e": {"value": r["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "wall_s": round(wall, 2)}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def _traffic_record(kernel):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source
+    it was taken on is unchanged."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    r = rec.get(kernel)
+    if not r:
+        return None
+    if r.get("src_sha1") != csrc_hash():
+        return None
+    return r
+
+
+def csrc_hash():
+    h = hashlib.sha1()
+    d = os.path.join(ROOT, "dequant_gemv_moe_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode())
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def make_event(torch, external):
+    if external:
+        try:
+            return torch.cuda.Event(enable_timing=True, external=True)
+        except TypeError:
+            return None
+    return torch.cuda.Event(enable_timing=True)
+
+
+def bench_layer(torch, dq, args):
+    """The headline: 7 Llama-3-8B linears per step, one CUDA graph per step."""
+    g = synth.streams(synth.BASE_SEED + 1, 3)
+    lin = synth.LLAMA8B_LINEARS
+    # weights: ROTATE copies of the layer
+    Ws = [[torch.from_numpy(synth.quant_matrix(g[0], Q4_K, N, K)).cuda() for (_, N, K) in lin]
+          for _ in range(ROTATE)]
+    xs = [torch.from_numpy(synth.activations(g[1], (1, K), 1)).cuda() for (_, N, K) in lin]
+    ys = [torch.empty(1, N, dtype=torch.float32, device="cuda") for (_, N, K) in lin]
+    wbytes = sum(weight_bytes(Q4_K, N, K) for (_, N, K) in lin)
+    abytes = sum(K * 2 + N * 4 for (_, N, K) in lin)
+
+    def step(r, evs=None):
+        for i, (_, N, K) in enumerate(lin):
+            if evs is not None:
+                evs[i].record()
+            dq.qgemv(Q4_K, Ws[r][i], N, K, xs[i], y=ys[i])
+        if evs is not None:
+            evs[len(lin)].record()
+
+    # warm up (also sets kernel attributes before capture)
+    for r in range(ROTATE):
+        step(r)
+    torch.cuda.synchronize()
+    K = args.steps
+    ext_ok = make_event(torch, True) is not None
+    graphs, evsets = [], []
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for i in range(K + args.warmup):
+            evs = [make_event(torch, True) for _ in range(len(lin) + 1)] if ext_ok else None
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=s):
+                step(i % ROTATE, evs)
+            graphs.append(gr)
+            evsets.append(evs)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    for i in range(args.warmup):
+        graphs[i].replay()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        start.record()
+        for i in range(args.warmup, args.warmup + K):
+            graphs[i].replay()
+        end.record()
+        torch.cuda.synchronize()
+    ms = start.elapsed_time(end)
+    # per-launch kernel durations from the events inside each step's graph
+    kern_ms, kern_src = None, "graph_step_time/7"
+    if ext_ok:
+        tot = 0.0
+        for i in range(args.warmup, args.warmup + K):
+            e = evsets[i]
+            tot += sum(e[j].elapsed_time(e[j + 1]) for j in range(len(lin)))
+        kern_ms = tot / (K * len(lin))
+        kern_src = "cuda events around each launch inside the step graphs"
+    else:
+        kern_ms = ms / (K * len(lin))
+    del graphs
+    res = {"ms_per_step": ms / K, "weight_bytes": wbytes, "act_bytes": abytes,
+           "value": wbytes * K / (ms / 1e3) / 1e9, "kern_ms": kern_ms, "kern_src": kern_src,
+           "clocks": clk.summary(), "launches": K * len(lin)}
+
+    # e2e: the same step through the public call with host buffers — pinned
+    # x uploaded and y read back every step inside the timed region
+    hx = [torch.from_numpy(synth.activations(g[2], (1, K_), 1)).pin_memory() for (_, N_, K_) in lin]
+    hy = [torch.empty(1, N_, dtype=torch.float32).pin_memory() for (_, N_, K_) in lin]
+    h2d = sum(t.numel() * 2 for t in hx)
+    d2h = sum(t.numel() * 4 for t in hy)
+
+    def e2e_step(r):
+        for i, (_, N_, K_) in enumerate(lin):
+            xs[i].copy_(hx[i], non_blocking=True)
+        step(r)
+        for i in range(len(lin)):
+            hy[i].copy_(ys[i], non_blocking=True)
+
+    egr = []
+    with torch.cuda.stream(s):
+        for r in range(ROTATE):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=s):
+                e2e_step(r)
+            egr.append(gr)
+    torch.cuda.synchronize()
+    for i in range(args.warmup):
+        egr[i % ROTATE].replay()
+    torch.cuda.synchronize()
+    start.record()
+    for i in range(K):
+        egr[i % ROTATE].replay()
+    end.record()
+    torch.cuda.synchronize()
+    ems = start.elapsed_time(end)
+    res["e2e"] = {"value": wbytes * K / (ems / 1e3) / 1e9, "unit": "GB/s",
+                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                  "ms_per_step": ems / K,
+                  "note": "x uploaded from pinned host memory and y read back in every step, "
+                          "captured with the seven dq_qgemv calls in one graph per step"}
+    del egr, Ws
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_gemv_70b(torch, dq, reps=50):
+    """North-star shape: batch-1 Q4_K 28672 x 8192 gate GEMV, 4 rotating copies."""
+    g = synth.streams(synth.BASE_SEED + 2, 2)
+    N, K = 28672, 8192
+    Ws = [torch.from_numpy(synth.quant_matrix(g[0], Q4_K, N, K)).cuda() for _ in range(ROTATE)]
+    x = torch.from_numpy(synth.activations(g[1], (1, K), 1)).cuda()
+    y = torch.empty(1, N, dtype=torch.float32, device="cuda")
+    for r in range(ROTATE):
+        dq.qgemv(Q4_K, Ws[r], N, K, x, y=y)
+    torch.cuda.synchronize()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * reps)]
+    for i in range(reps):
+        evs[2 * i].record()
+        dq.qgemv(Q4_K, Ws[i % ROTATE], N, K, x, y=y)
+        evs[2 * i + 1].record()
+    torch.cuda.synchronize()
+    t = [evs[2 * i].elapsed_time(evs[2 * i + 1]) for i in range(reps)]
+    wb = weight_bytes(Q4_K, N, K)
+    us = float(np.median(t)) * 1e3
+    del Ws
+    torch.cuda.empty_cache()
+    return {"shape": "28672x8192 Q4_K batch 1 fp16", "us_median": us,
+            "us_p10": float(np.percentile(t, 10)) * 1e3, "us_p90": float(np.percentile(t, 90)) * 1e3,
+            "weight_GBps": wb / (us / 1e6) / 1e9, "bytes": wb + K * 2 + N * 4}
+
+
+def bench_moe(torch, dq, cfg, T, reps=20):
+    w = synth.moe_weights(synth.BASE_SEED + (3 if cfg is synth.MOE_MIXTRAL else 4), cfg["E"],
+                          cfg["H"], cfg["F"], cfg["n_shared"], cfg["fmt"])
+    dev = {k: (torch.from_numpy(v).cuda() if v is not None else None) for k, v in w.items()}
+    del w
+    desc = dq.ops.make_desc(cfg["E"], cfg["top_k"], cfg["H"], cfg["F"], cfg["n_shared"], cfg["fmt"],
+                            dev["router_W"], dev["w_gate"], dev["w_up"], dev["w_down"],
+                            dev["sh_gate"], dev["sh_up"], dev["sh_down"])
+    g = synth.streams(synth.BASE_SEED + 50 + T, ROTATE)
+    xs = []
+    for r in range(ROTATE):
+        a = synth.activations(g[r], (T, cfg["H"]), cfg["xdt"])
+        t = torch.from_numpy(a.view(np.int16) if cfg["xdt"] == 2 else a).cuda()
+        xs.append(t.view(torch.bfloat16) if cfg["xdt"] == 2 else t)
+    ws = torch.empty(dq.moe_workspace_size(desc, T), dtype=torch.uint8, device="cuda")
+    y = torch.empty(T, cfg["H"], dtype=torch.float32, device="cuda")
+    idx = torch.empty(T, cfg["top_k"], dtype=torch.int32, device="cuda")
+    gate = torch.empty(T, cfg["top_k"], dtype=torch.float32, device="cuda")
+    import ctypes
+
+    def fwd(r):
+        rc = dq.lib.dq_moe_forward(ctypes.byref(desc), ctypes.c_void_p(xs[r].data_ptr()),
+                                   cfg["xdt"], T, ctypes.c_void_p(y.data_ptr()),
+                                   ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+                                   ctypes.c_void_p(idx.data_ptr()),
+                                   ctypes.c_void_p(gate.data_ptr()), None,
+                                   ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        assert rc == 0, rc
+
+    touched = []
+    for r in range(ROTATE):
+        fwd(r)
+        torch.cuda.synchronize()
+        touched.append(len(np.unique(idx.cpu().numpy())))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graphs = []
+    with torch.cuda.stream(s):
+        for r in range(ROTATE):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=s):
+                fwd(r)
+            graphs.append(gr)
+    torch.cuda.synchronize()
+    for r in range(ROTATE):
+        graphs[r].replay()
+    torch.cuda.synchronize()
+    st, en = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    st.record()
+    for i in range(reps):
+        graphs[i % ROTATE].replay()
+    en.record()
+    torch.cuda.synchronize()
+    ms = st.elapsed_time(en) / reps
+    qk, nb = synth.BLOCK[cfg["fmt"]]
+    per_expert = 3 * cfg["F"] * (cfg["H"] // qk) * nb
+    exp_bytes = (np.mean(touched) + cfg["n_shared"]) * per_expert
+    alg = exp_bytes + cfg["E"] * cfg["H"] * 4 + T * cfg["H"] * (2 + 4)
+    del graphs, dev
+    torch.cuda.empty_cache()
+    return {"T": T, "ms": ms, "tokens_per_s": T / (ms / 1e3),
+            "experts_touched": float(np.mean(touched)), "alg_bytes": alg,
+            "GBps": alg / (ms / 1e3) / 1e9}
+
+
+def run_ours(args):
+    import torch
+    rank, world, local, dist = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    import dequant_gemv_moe_gb300 as dq
+
+    peak, peak_src = peaks()
+    barrier(dist)
+    torch.cuda.synchronize()
+    lay = bench_layer(torch, dq, args)
+    barrier(dist)
+    ms = max_over_ranks(dist, lay["ms_per_step"])
+    value = world * lay["weight_bytes"] * 1e3 / ms / 1e9
+    extra = {}
+    if rank == 0:
+        extra["gemv_70b_gate_b1"] = bench_gemv_70b(torch, dq)
+        extra["gemv_70b_gate_b1"]["frac_of_hbm"] = extra["gemv_70b_gate_b1"]["weight_GBps"] / peak
+        if not args.no_moe:
+            moe = {}
+            moe["mixtral_T16"] = bench_moe(torch, dq, synth.MOE_MIXTRAL, 16)
+            for T in synth.MOE_DEEPSEEK["T"]:
+                moe["deepseek_v3_T%d" % T] = bench_moe(torch, dq, synth.MOE_DEEPSEEK, T)
+            for v in moe.values():
+                v["frac_of_hbm"] = v["GBps"] / peak
+            extra["moe"] = moe
+        cpu = oracle_sample()
+    if rank != 0:
+        return
+    kern_bytes = (lay["weight_bytes"] + lay["act_bytes"]) / 7.0
+    achieved = kern_bytes / (lay["kern_ms"] / 1e3) / 1e9
+    tr = _traffic_record("qgemv_mma_kernel<Q4_K>")
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic",
+        "config": {"workload": "llama3-8b decode-layer linears: q,k,v,o,gate,up,down Q4_K "
+                               "(122.7 MB), fp16 x, batch 1, one CUDA graph per step",
+                   "l2": "4 rotating weight copies, 491 MB > 3x L2",
+                   "frac_of_hbm": round(value / world / peak, 4),
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "roofline": {"bound": "hbm", "kernel": "qgemv_mma_kernel<Q4_K>",
+                     "achieved": round(achieved, 1), "peak": peak,
+                     "peak_source": peak_src + " hbm_gbs (MEASURED_PEAKS.json)",
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": tr["dram_bytes_per_launch"] if tr else None,
+                     "launch_time_source": lay["kern_src"],
+                     "alg_bytes_per_launch": kern_bytes},
+        "cpu_baseline": cpu,
+        "e2e": lay["e2e"],
+        "gpu_launches": lay["launches"],
+        "clocks": lay["clocks"],
+    }
+    line.update(extra)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

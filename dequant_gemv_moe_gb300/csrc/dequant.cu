@@ -1,0 +1,82 @@
+// dequant.cu — step "block decode" on its own: packed blocks -> fp32.
+//
+// The pages name the formats (Titan Engine §激进量化策略: Q4_K; KTransformers
+// §支持的量化格式: Q4_K_M, Q6_K, Q8_0; NTransformer §量化支持: Q80, Q6K) but
+// print no layout; the GGUF/llama.cpp layouts declared in dqmoe.h are used.
+// Each output is the exact closed form rounded once to fp32: every product
+// below is exact in fp32 and the Q4_K difference is formed by one fused
+// multiply-add, so the result is bit-identical to any exact evaluation.
+//
+// One thread per output weight (coalesced fp32 stores); the block's few
+// header bytes are re-read by its threads through L1.  This kernel is for
+// bit-exact checking, not for speed: the GEMV kernels never materialise W.
+#include "common.cuh"
+
+namespace dqmoe {
+
+__device__ __forceinline__ float h16(const uint8_t* p) {
+  return __half2float(__ushort_as_half((unsigned short)(p[0] | (p[1] << 8))));
+}
+
+__global__ void dequant_q4k_kernel(const uint8_t* __restrict__ blocks, int64_t nblk,
+                                   float* __restrict__ out) {
+  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t blk = gid >> 8;
+  if (blk >= nblk) return;
+  const int i = (int)(gid & 255);
+  const uint8_t* b = blocks + blk * 144;
+  const float d = h16(b), dmin = h16(b + 2);
+  const uint8_t* s = b + 4;
+  const int j = i >> 5;            // sub-block: 32 weights
+  int sc, m;
+  if (j < 4) {
+    sc = s[j] & 63;
+    m = s[j + 4] & 63;
+  } else {
+    sc = (s[j + 4] & 15) | ((s[j - 4] >> 6) << 4);
+    m = (s[j + 4] >> 4) | ((s[j] >> 6) << 4);
+  }
+  const int c = i >> 6, l = i & 31;  // 32-byte group c; low nibble first half
+  const uint8_t byte = b[16 + 32 * c + l];
+  const int q = (i & 32) ? (byte >> 4) : (byte & 15);
+  out[gid] = __fmaf_rn(d * (float)sc, (float)q, -(dmin * (float)m));
+}
+
+__global__ void dequant_q6k_kernel(const uint8_t* __restrict__ blocks, int64_t nblk,
+                                   float* __restrict__ out) {
+  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t blk = gid >> 8;
+  if (blk >= nblk) return;
+  const int i = (int)(gid & 255);
+  const uint8_t* b = blocks + blk * 210;
+  const int h = i >> 7, r = (i >> 5) & 3, l = i & 31;   // i = 128h + 32r + l
+  const uint8_t qlb = b[64 * h + l + ((r & 1) ? 32 : 0)];
+  const uint8_t qhb = b[128 + 32 * h + l];
+  const int lo = (r & 2) ? (qlb >> 4) : (qlb & 15);
+  const int hi = (qhb >> (2 * r)) & 3;
+  const int q = lo | (hi << 4);
+  const int sc = (int)(int8_t)b[192 + (i >> 4)];
+  const float d = h16(b + 208);
+  out[gid] = d * (float)sc * (float)(q - 32);
+}
+
+__global__ void dequant_q80_kernel(const uint8_t* __restrict__ blocks, int64_t nblk,
+                                   float* __restrict__ out) {
+  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t blk = gid >> 5;
+  if (blk >= nblk) return;
+  const uint8_t* b = blocks + blk * 34;
+  out[gid] = h16(b) * (float)(int8_t)b[2 + (gid & 31)];
+}
+
+int launch_dequant(int fmt, const void* blocks, int64_t n, float* out, cudaStream_t s) {
+  const int threads = 256;
+  const int64_t grid = (n + threads - 1) / threads;
+  const uint8_t* b = (const uint8_t*)blocks;
+  if (fmt == DQ_Q4_K) dequant_q4k_kernel<<<(unsigned)grid, threads, 0, s>>>(b, n / 256, out);
+  else if (fmt == DQ_Q6_K) dequant_q6k_kernel<<<(unsigned)grid, threads, 0, s>>>(b, n / 256, out);
+  else dequant_q80_kernel<<<(unsigned)grid, threads, 0, s>>>(b, n / 32, out);
+  return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
+}
+
+}  // namespace dqmoe

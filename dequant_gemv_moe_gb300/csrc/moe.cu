@@ -1,0 +1,617 @@
+// moe.cu — the sparse MoE layer on one GPU, as a sequence of launches on one
+// stream with no host synchronisation (capturable in one CUDA graph, as
+// [KTransformers, §技术原理] runs one graph per decode step):
+//   1. router_logits_kernel : logits = x W_r^T, fp32, tiled over (experts,
+//      tokens) and split over the hidden dimension into partial sums.
+//   2. topk_kernel          : one warp per token sums the partials in a fixed
+//      order, picks the top_k logits (lowest index first on ties) and the
+//      renormalised softmax gates.
+//   3. permute_kernel       : one CTA counts pairs per expert, prefix-sums the
+//      counts and scatters the (token, slot) pairs stably by expert; it also
+//      emits the work list: (expert, first position, <= 8 columns) groups.
+//   4. grouped_kernel<gate/up> : persistent; each unit is 32 rows of W_gate
+//      and the same 32 rows of W_up of one expert times that group's tokens
+//      (gathered rows of x); epilogue h = silu(g) * u in fp32.
+//   5. grouped_kernel<down>    : persistent; 64 rows of W_down times h.
+//   6. combine_kernel       : y[t] = sum_i gate[t][i] * y_e(t,i) + shared.
+// [Titan Engine, §MoE 专家流式加载]: only a few experts per token are active,
+// so only the touched experts' packed weights are streamed from HBM.
+#include <algorithm>
+
+#include "moe_plan.h"
+#include "qgemv_mma.cuh"
+
+namespace dqmoe {
+
+// ===========================================================================
+// workspace plan
+// ===========================================================================
+static size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+MoePlan moe_plan(const dq_moe_desc& d, int T) {
+  MoePlan p;
+  const int tiles = ((d.E + 63) / 64) * ((T + 31) / 32);
+  p.KS = std::max(1, std::min(d.hidden / 256, (320 + tiles - 1) / tiles));
+  p.P = (int64_t)T * d.top_k;
+  p.NP = p.P + (int64_t)d.n_shared * T;
+  p.G_max = (int)((p.P + 7) / 8 + std::min<int64_t>(d.E, p.P) + (int64_t)d.n_shared * ((T + 7) / 8));
+  size_t o = 0;
+  p.off_part = o;    o = align256(o + (size_t)p.KS * T * d.E * 4);
+  p.off_logits = o;  o = align256(o + (size_t)T * d.E * 4);
+  p.off_idx = o;     o = align256(o + (size_t)p.P * 4);
+  p.off_gate = o;    o = align256(o + (size_t)p.P * 4);
+  p.off_offsets = o; o = align256(o + (size_t)(d.E + 1) * 4);
+  p.off_sorted = o;  o = align256(o + (size_t)p.P * 4);
+  p.off_inv = o;     o = align256(o + (size_t)p.P * 4);
+  p.off_tok = o;     o = align256(o + (size_t)p.NP * 4);
+  p.off_groups = o;  o = align256(o + (size_t)p.G_max * 16);
+  p.off_ngroups = o; o = align256(o + 16);
+  p.off_h = o;       o = align256(o + (size_t)p.NP * d.ffn * 4);
+  p.off_ypos = o;    o = align256(o + (size_t)p.NP * d.hidden * 4);
+  p.total = o;
+  return p;
+}
+
+// ===========================================================================
+// 1. router logits (fp32 SIMT tile 64 experts x 32 tokens, 4x4 per thread)
+// ===========================================================================
+__device__ __forceinline__ float act_f32(const void* x, int dtype, int64_t i) {
+  if (dtype == DQ_F32) return __ldg((const float*)x + i);
+  const unsigned short u = __ldg((const unsigned short*)x + i);
+  if (dtype == DQ_BF16) return __uint_as_float((uint32_t)u << 16);
+  return __half2float(__ushort_as_half(u));
+}
+
+__global__ void __launch_bounds__(128) router_logits_kernel(const float* __restrict__ Wr, int E,
+                                                            int H, const void* __restrict__ x,
+                                                            int xdt, int T, int KS,
+                                                            float* __restrict__ part) {
+  __shared__ __align__(16) float Ws[32][64 + 4];
+  __shared__ __align__(16) float Xs[32][32 + 4];
+  const int e0 = blockIdx.x * 64, t0 = blockIdx.y * 32, ks = blockIdx.z;
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const int nch = H / 32;
+  const int c_begin = (int)((int64_t)nch * ks / KS), c_end = (int)((int64_t)nch * (ks + 1) / KS);
+  float acc[4][4] = {};
+  for (int c = c_begin; c < c_end; ++c) {
+    const int h0 = c * 32;
+    for (int i = tid; i < 64 * 32; i += 128) {
+      const int e = i >> 5, hh = i & 31;
+      Ws[hh][e] = (e0 + e < E) ? __ldg(Wr + (int64_t)(e0 + e) * H + h0 + hh) : 0.f;
+    }
+    for (int i = tid; i < 32 * 32; i += 128) {
+      const int t = i >> 5, hh = i & 31;
+      Xs[hh][t] = (t0 + t < T) ? act_f32(x, xdt, (int64_t)(t0 + t) * H + h0 + hh) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int hh = 0; hh < 32; ++hh) {
+      const float4 xv = *(const float4*)&Xs[hh][ty * 4];
+      const float4 wv = *(const float4*)&Ws[hh][tx * 4];
+      const float xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(xa[a], wa[b], acc[a][b]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int t = t0 + ty * 4 + a;
+    if (t >= T) continue;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int e = e0 + tx * 4 + b;
+      if (e < E) part[((int64_t)ks * T + t) * E + e] = acc[a][b];
+    }
+  }
+}
+
+// ===========================================================================
+// 2. top-k + gates: one warp per token
+// ===========================================================================
+__device__ __forceinline__ bool better(float a, int ia, float b, int ib) {
+  return a > b || (a == b && ia < ib);
+}
+
+__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ part, int KS, int T,
+                                                   int E, int k, float* __restrict__ logits,
+                                                   int32_t* __restrict__ idx,
+                                                   float* __restrict__ gate) {
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  float v[8];
+  int id[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int e = lane + 32 * j;
+    id[j] = e;
+    if (e < E) {
+      float s = 0.f;
+      for (int q = 0; q < KS; ++q) s += part[((int64_t)q * T + t) * E + e];   // fixed order
+      v[j] = s;
+      if (logits) logits[(int64_t)t * E + e] = s;
+    } else {
+      v[j] = -INFINITY;
+      id[j] = 0x7fffffff;
+    }
+  }
+  float sv[8];
+  int si[8];
+  for (int i = 0; i < k; ++i) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (better(v[j], id[j], bv, bi)) {
+        bv = v[j];
+        bi = id[j];
+      }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (better(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    sv[i] = bv;
+    si[i] = bi;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (id[j] == bi) {   // remove the winner from further rounds
+        v[j] = -INFINITY;
+        id[j] = 0x7fffffff;
+      }
+  }
+  if (lane == 0) {
+    // softmax over all E renormalised over the selection
+    float z = 0.f;
+    for (int i = 0; i < k; ++i) z += expf(sv[i] - sv[0]);
+    for (int i = 0; i < k; ++i) {
+      idx[(int64_t)t * k + i] = si[i];
+      gate[(int64_t)t * k + i] = expf(sv[i] - sv[0]) / z;
+    }
+  }
+}
+
+// ===========================================================================
+// 3. stable permute + work groups: one CTA of 1024 threads
+// ===========================================================================
+__global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict__ idx, int T,
+                                                       int k, int E, int n_shared,
+                                                       int32_t* __restrict__ offsets,
+                                                       int32_t* __restrict__ sorted,
+                                                       int32_t* __restrict__ inv,
+                                                       int32_t* __restrict__ tok,
+                                                       int4* __restrict__ groups,
+                                                       int32_t* __restrict__ n_groups) {
+  __shared__ int cnt[256];
+  __shared__ int off[257];
+  __shared__ int run[256];
+  __shared__ int cntw[32][256];
+  __shared__ int gsc[257];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int P = T * k;
+  if (tid < 256) cnt[tid] = 0;
+  __syncthreads();
+  for (int p = tid; p < P; p += 1024) atomicAdd(&cnt[idx[p]], 1);
+  __syncthreads();
+  // exclusive scan of counts (E <= 256), Hillis-Steele on off[1..E]
+  if (tid < 256) off[tid + 1] = (tid < E) ? cnt[tid] : 0;
+  if (tid == 0) off[0] = 0;
+  __syncthreads();
+  for (int d = 1; d < 256; d <<= 1) {
+    int v = 0;
+    if (tid < 256 && tid + 1 > d) v = off[tid + 1 - d];
+    __syncthreads();
+    if (tid < 256) off[tid + 1] += v;
+    __syncthreads();
+  }
+  if (tid <= E && offsets) offsets[tid] = off[tid];
+  if (tid < E) run[tid] = off[tid];
+  __syncthreads();
+  // stable scatter, 1024 pairs per round: rank inside the warp by match_any,
+  // warps ordered through per-warp counts
+  for (int base = 0; base < P; base += 1024) {
+    for (int i = tid; i < 32 * 256; i += 1024) (&cntw[0][0])[i] = 0;
+    __syncthreads();
+    const int p = base + tid;
+    const int e = (p < P) ? idx[p] : 256;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    if (p < P && rank == 0) cntw[warp][e] = __popc(peers);
+    __syncthreads();
+    if (tid < E) {
+      int s = run[tid];
+      for (int w = 0; w < 32; ++w) {
+        const int c = cntw[w][tid];
+        cntw[w][tid] = s;
+        s += c;
+      }
+      run[tid] = s;
+    }
+    __syncthreads();
+    if (p < P) {
+      const int pos = cntw[warp][e] + rank;
+      sorted[pos] = p;
+      if (inv) inv[p] = pos;
+      if (tok) tok[pos] = p / k;
+    }
+    __syncthreads();
+  }
+  if (!groups) return;
+  // shared-expert positions follow the routed ones: P + s*T + t
+  for (int i = tid; i < n_shared * T; i += 1024) tok[P + i] = i % T;
+  // groups of <= 8 columns per expert, experts in order, then shared experts
+  if (tid < 256) gsc[tid + 1] = (tid < E) ? (cnt[tid] + 7) / 8 : 0;
+  if (tid == 0) gsc[0] = 0;
+  __syncthreads();
+  for (int d = 1; d < 256; d <<= 1) {
+    int v = 0;
+    if (tid < 256 && tid + 1 > d) v = gsc[tid + 1 - d];
+    __syncthreads();
+    if (tid < 256) gsc[tid + 1] += v;
+    __syncthreads();
+  }
+  if (tid < E) {
+    const int n = cnt[tid];
+    for (int j = 0; j * 8 < n; ++j)
+      groups[gsc[tid] + j] = make_int4(tid, off[tid] + 8 * j, min(8, n - 8 * j), 0);
+  }
+  const int nr = gsc[E];
+  const int per = (T + 7) / 8;
+  for (int i = tid; i < n_shared * per; i += 1024) {
+    const int s = i / per, j = i % per;
+    groups[nr + i] = make_int4(E + s, P + s * T + 8 * j, min(8, T - 8 * j), 0);
+  }
+  if (tid == 0) *n_groups = nr + n_shared * per;
+}
+
+// ===========================================================================
+// 4/5. persistent grouped streaming GEMV (gate/up with SwiGLU, or down)
+// ===========================================================================
+struct GroupedParams {
+  const uint8_t* Wa;   // routed: W_gate (gate/up) or W_down (down), E stacked
+  const uint8_t* Wb;   // routed: W_up (gate/up only)
+  const uint8_t* Sa;   // shared experts, same roles
+  const uint8_t* Sb;
+  int64_t mat_bytes;   // bytes of one expert matrix
+  int64_t row_bytes;
+  int nsb;             // super-blocks per row (K / 256)
+  int E;
+  const int4* groups;
+  const int* n_groups;
+  const int* tok;      // position -> token (gate/up gather)
+  const void* xbase;   // gate/up: x [T][H]; down: h [NP][F]
+  int xdt;
+  int64_t xstride;     // elements per x / h row
+  float* out;          // gate/up: h [NP][F]; down: ypos [NP][H]
+  int64_t out_stride;
+  int tiles;           // tiles per group
+  int nstage;
+};
+
+template <int FMT, bool GATEUP>
+__global__ void __launch_bounds__(kThreads) grouped_kernel(const GroupedParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  using L = Layout<FMT>;
+  const SmemPlan plan = make_plan<FMT>(p.nstage, 8, 1);
+  uint64_t* full = (uint64_t*)(smem + plan.off_bar);
+  uint64_t* empty = full + plan.nstage;
+  uint8_t* wbuf = smem + plan.off_w;
+  uint8_t* xbuf = smem + plan.off_x;
+  float* xinv = (float*)(smem + plan.off_xinv);
+  float* ex = (float*)(smem + plan.off_red);   // [64][8] gate/up exchange
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_units = __ldg(p.n_groups) * p.tiles;
+  const int nchunk = (p.nsb + L::C - 1) / L::C;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < plan.nstage; ++s) {
+      mbar_init(&full[s], 32);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    // ------------------------------ loader ------------------------------
+    const uint64_t pol = l2_evict_first_policy();
+    int gc = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      const int4 grp = __ldg(p.groups + u / p.tiles);
+      const int tile = u % p.tiles;
+      const bool shared = grp.x >= p.E;
+      const int eid = shared ? grp.x - p.E : grp.x;
+      // two weight rows per lane: r = lane and lane + 32
+      const uint8_t* rowp[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int r = lane + 32 * h;
+        const uint8_t* m;
+        int row;
+        if (GATEUP) {
+          m = (h == 0) ? (shared ? p.Sa : p.Wa) : (shared ? p.Sb : p.Wb);
+          row = tile * 32 + lane;
+        } else {
+          m = shared ? p.Sa : p.Wa;
+          row = tile * 64 + r;
+        }
+        rowp[h] = m + (int64_t)eid * p.mat_bytes + (int64_t)row * p.row_bytes;
+      }
+      XSrc xs;
+      xs.dtype = p.xdt;
+      xs.col_stride = p.xstride;
+      if (GATEUP) {
+        xs.base = p.xbase;
+        xs.rows = p.tok + grp.y;
+      } else {
+        xs.base = (const float*)p.xbase + (int64_t)grp.y * p.xstride;
+        xs.rows = nullptr;
+      }
+      for (int c = 0; c < nchunk && ok; ++c, ++gc) {
+        const int s = gc % plan.nstage, round = gc / plan.nstage;
+        if (round > 0) ok = mbar_wait(&empty[s], (round - 1) & 1);
+        if (!ok) break;
+        const int c0 = c * L::C;
+        const int ncs = min(L::C, p.nsb - c0);
+        const int64_t a_raw = (int64_t)c0 * L::SBB, b_raw = (int64_t)(c0 + ncs) * L::SBB;
+        const int64_t a = a_raw & ~(int64_t)15, b = (b_raw + 15) & ~(int64_t)15;
+        const uint32_t bytes = (uint32_t)(b - a);
+        if (lane == 0) mbar_expect_tx(&full[s], bytes * kTileRows);
+        __syncwarp();
+        uint8_t* wst = wbuf + s * L::W_STAGE;
+        bulk_g2s(wst + lane * L::ROW_PITCH, rowp[0] + a, bytes, &full[s], pol);
+        bulk_g2s(wst + (lane + 32) * L::ROW_PITCH, rowp[1] + a, bytes, &full[s], pol);
+        convert_x_stage<FMT>(xs, grp.z, (int64_t)c0 * 256, ncs, xbuf + s * 8 * L::XCOL,
+                             xinv + s * 8, lane);
+        mbar_arrive(&full[s]);
+      }
+    }
+  } else {
+    // ----------------------------- consumers -----------------------------
+    const int cw = warp - 1;
+    const int g = lane >> 2, t = lane & 3;
+    int gc = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+      const int4 grp = __ldg(p.groups + u / p.tiles);
+      const int tile = u % p.tiles;
+      const int ncols = grp.z;
+      const bool xon = g < ncols;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int c = 0; c < nchunk; ++c, ++gc) {
+        const int s = gc % plan.nstage, round = gc / plan.nstage;
+        // after a timed-out wait the warp keeps walking the same units (no
+        // further waits, no reads) so every warp still meets the barriers
+        ok = ok && mbar_wait(&full[s], round & 1);
+        if (!ok) continue;
+        const int c0 = c * L::C;
+        const int ncs = min(L::C, p.nsb - c0);
+        const int delta = (int)(((int64_t)c0 * L::SBB) & 15);
+        const uint32_t wst =
+            smem_u32(wbuf + s * L::W_STAGE) + (16 * cw + g) * L::ROW_PITCH + delta;
+        const uint32_t xcol = smem_u32(xbuf + (s * 8 + (xon ? g : 0)) * L::XCOL);
+        float part[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int j = 0; j < ncs; ++j)
+          SBDot<FMT>::run(wst + j * L::SBB, 8 * L::ROW_PITCH, xcol, j * 256, t, xon, part);
+        const float inv0 = xinv[s * 8 + 2 * t], inv1 = xinv[s * 8 + 2 * t + 1];
+        acc[0] = fmaf(part[0], inv0, acc[0]);
+        acc[1] = fmaf(part[1], inv1, acc[1]);
+        acc[2] = fmaf(part[2], inv0, acc[2]);
+        acc[3] = fmaf(part[3], inv1, acc[3]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+      }
+      const int c0 = 2 * t, c1 = 2 * t + 1;
+      if (!GATEUP) {
+        const int ra = tile * 64 + 16 * cw + g, rb = ra + 8;
+        float* o = p.out + (int64_t)grp.y * p.out_stride;
+        if (c0 < ncols) {
+          o[(int64_t)c0 * p.out_stride + ra] = acc[0];
+          o[(int64_t)c0 * p.out_stride + rb] = acc[2];
+        }
+        if (c1 < ncols) {
+          o[(int64_t)c1 * p.out_stride + ra] = acc[1];
+          o[(int64_t)c1 * p.out_stride + rb] = acc[3];
+        }
+      } else {
+        // rows 0..31 hold gate, rows 32..63 the matching up rows
+        const int ra = 16 * cw + g, rb = ra + 8;
+        ex[ra * 8 + c0] = acc[0];
+        ex[ra * 8 + c1] = acc[1];
+        ex[rb * 8 + c0] = acc[2];
+        ex[rb * 8 + c1] = acc[3];
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        const int ct = threadIdx.x - 32;
+        for (int i = ct; i < 32 * ncols; i += 128) {
+          const int r = i & 31, col = i >> 5;
+          const float gv = ex[r * 8 + col], uv = ex[(32 + r) * 8 + col];
+          // silu(g) = g / (1 + exp(-g)); for g < -88 exp overflows to inf and
+          // the quotient is -0, never NaN
+          const float h = gv / (1.f + expf(-gv)) * uv;
+          p.out[(int64_t)(grp.y + col) * p.out_stride + tile * 32 + r] = h;
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+      }
+    }
+  }
+}
+
+// ===========================================================================
+// 6. combine: y[t] = sum_i gate[t][i] * ypos[pos(t,i)] + sum_s ypos[P + sT + t]
+// ===========================================================================
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ ypos,
+                                                      const int32_t* __restrict__ inv,
+                                                      const float* __restrict__ gate, int T,
+                                                      int k, int H, int n_shared,
+                                                      float* __restrict__ y) {
+  const int H4 = H / 4;
+  const int64_t total = (int64_t)T * H4;
+  const int64_t P = (int64_t)T * k;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int t = (int)(i / H4), h4 = (int)(i % H4);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < k; ++s) {
+      const int pos = __ldg(inv + (int64_t)t * k + s);
+      const float g = __ldg(gate + (int64_t)t * k + s);
+      const float4 v = __ldg((const float4*)(ypos + (int64_t)pos * H) + h4);
+      acc.x = fmaf(g, v.x, acc.x);
+      acc.y = fmaf(g, v.y, acc.y);
+      acc.z = fmaf(g, v.z, acc.z);
+      acc.w = fmaf(g, v.w, acc.w);
+    }
+    for (int s = 0; s < n_shared; ++s) {
+      const float4 v = __ldg((const float4*)(ypos + (P + (int64_t)s * T + t) * H) + h4);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    ((float4*)y)[i] = acc;
+  }
+}
+
+// ===========================================================================
+// host side
+// ===========================================================================
+namespace {
+
+int sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return sms;
+}
+
+int qk(int fmt) { return fmt == DQ_Q8_0 ? 32 : 256; }
+int blk_bytes(int fmt) { return fmt == DQ_Q4_K ? 144 : fmt == DQ_Q6_K ? 210 : 34; }
+
+template <int FMT, bool GATEUP>
+int launch_grouped(const GroupedParams& gp_in, int units_max, cudaStream_t s) {
+  GroupedParams gp = gp_in;
+  int nstage = 6;
+  while (nstage > 3 && make_plan<FMT>(nstage, 8, 1).total + 2048 > 113 * 1024) --nstage;
+  gp.nstage = nstage;
+  const int smem = make_plan<FMT>(nstage, 8, 1).total + 2048;
+  static bool attr[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 64 || !attr[dev]) {
+    if (cudaFuncSetAttribute(grouped_kernel<FMT, GATEUP>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) != cudaSuccess)
+      return DQ_ERR_CUDA;
+    if (dev < 64) attr[dev] = true;
+  }
+  const int sms = sm_count();
+  if (sms <= 0) return DQ_ERR_CUDA;
+  const int grid = std::max(1, std::min(units_max, 2 * sms));
+  grouped_kernel<FMT, GATEUP><<<grid, kThreads, smem, s>>>(gp);
+  return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
+}
+
+template <bool GATEUP>
+int launch_grouped_fmt(int fmt, const GroupedParams& gp, int units_max, cudaStream_t s) {
+  if (fmt == DQ_Q4_K) return launch_grouped<DQ_Q4_K, GATEUP>(gp, units_max, s);
+  if (fmt == DQ_Q6_K) return launch_grouped<DQ_Q6_K, GATEUP>(gp, units_max, s);
+  return launch_grouped<DQ_Q8_0, GATEUP>(gp, units_max, s);
+}
+
+}  // namespace
+
+int launch_router(const float* Wr, int E, int H, const void* x, int xdt, int T, int top_k,
+                  int KS, float* part, float* logits, int32_t* idx, float* gate, cudaStream_t s) {
+  dim3 g1((unsigned)((E + 63) / 64), (unsigned)((T + 31) / 32), (unsigned)KS);
+  router_logits_kernel<<<g1, 128, 0, s>>>(Wr, E, H, x, xdt, T, KS, part);
+  if (cudaGetLastError() != cudaSuccess) return DQ_ERR_CUDA;
+  topk_kernel<<<(unsigned)((T + 7) / 8), 256, 0, s>>>(part, KS, T, E, top_k, logits, idx, gate);
+  return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
+}
+
+int launch_permute(const int32_t* idx, int T, int k, int E, int32_t* offsets, int32_t* sorted,
+                   cudaStream_t s) {
+  permute_kernel<<<1, 1024, 0, s>>>(idx, T, k, E, 0, offsets, sorted, nullptr, nullptr, nullptr,
+                                    nullptr);
+  return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
+}
+
+int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, float* y, void* ws,
+                       int32_t* topk_idx, float* topk_gate, float* logits, cudaStream_t s) {
+  const MoePlan pl = moe_plan(d, T);
+  uint8_t* w = (uint8_t*)ws;
+  float* part = (float*)(w + pl.off_part);
+  float* lg = logits ? logits : (float*)(w + pl.off_logits);
+  int32_t* idx = topk_idx ? topk_idx : (int32_t*)(w + pl.off_idx);
+  float* gate = topk_gate ? topk_gate : (float*)(w + pl.off_gate);
+  int32_t* offsets = (int32_t*)(w + pl.off_offsets);
+  int32_t* sorted = (int32_t*)(w + pl.off_sorted);
+  int32_t* inv = (int32_t*)(w + pl.off_inv);
+  int32_t* tok = (int32_t*)(w + pl.off_tok);
+  int4* groups = (int4*)(w + pl.off_groups);
+  int32_t* ngroups = (int32_t*)(w + pl.off_ngroups);
+  float* h = (float*)(w + pl.off_h);
+  float* ypos = (float*)(w + pl.off_ypos);
+
+  int rc = launch_router(d.router_W, d.E, d.hidden, x, xdt, T, d.top_k, pl.KS, part, lg, idx,
+                         gate, s);
+  if (rc != DQ_OK) return rc;
+  permute_kernel<<<1, 1024, 0, s>>>(idx, T, d.top_k, d.E, d.n_shared, offsets, sorted, inv, tok,
+                                    groups, ngroups);
+  if (cudaGetLastError() != cudaSuccess) return DQ_ERR_CUDA;
+
+  const int q = qk(d.fmt), bb = blk_bytes(d.fmt);
+  GroupedParams gu = {};
+  gu.Wa = (const uint8_t*)d.w_gate;
+  gu.Wb = (const uint8_t*)d.w_up;
+  gu.Sa = (const uint8_t*)d.sh_gate;
+  gu.Sb = (const uint8_t*)d.sh_up;
+  gu.row_bytes = (int64_t)(d.hidden / q) * bb;
+  gu.mat_bytes = gu.row_bytes * d.ffn;
+  gu.nsb = d.hidden / 256;
+  gu.E = d.E;
+  gu.groups = groups;
+  gu.n_groups = ngroups;
+  gu.tok = tok;
+  gu.xbase = x;
+  gu.xdt = xdt;
+  gu.xstride = d.hidden;
+  gu.out = h;
+  gu.out_stride = d.ffn;
+  gu.tiles = d.ffn / 32;
+  rc = launch_grouped_fmt<true>(d.fmt, gu, pl.G_max * gu.tiles, s);
+  if (rc != DQ_OK) return rc;
+
+  GroupedParams dn = {};
+  dn.Wa = (const uint8_t*)d.w_down;
+  dn.Sa = (const uint8_t*)d.sh_down;
+  dn.row_bytes = (int64_t)(d.ffn / q) * bb;
+  dn.mat_bytes = dn.row_bytes * d.hidden;
+  dn.nsb = d.ffn / 256;
+  dn.E = d.E;
+  dn.groups = groups;
+  dn.n_groups = ngroups;
+  dn.tok = nullptr;
+  dn.xbase = h;
+  dn.xdt = DQ_F32;
+  dn.xstride = d.ffn;
+  dn.out = ypos;
+  dn.out_stride = d.hidden;
+  dn.tiles = d.hidden / 64;
+  rc = launch_grouped_fmt<false>(d.fmt, dn, pl.G_max * dn.tiles, s);
+  if (rc != DQ_OK) return rc;
+
+  const int64_t n4 = (int64_t)T * d.hidden / 4;
+  const int cgrid = (int)std::min<int64_t>((n4 + 255) / 256, 4096);
+  combine_kernel<<<cgrid, 256, 0, s>>>(ypos, inv, gate, T, d.top_k, d.hidden, d.n_shared, y);
+  return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
+}
+
+}  // namespace dqmoe

@@ -1,0 +1,23 @@
+// moe_plan.h — workspace layout of dq_moe_forward (host side, shared by the
+// C-ABI validation in api.cu and the launch sequence in moe.cu).
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/dqmoe.h"
+
+namespace dqmoe {
+
+struct MoePlan {
+  int KS;           // router hidden-dimension split
+  int64_t P;        // routed (token, slot) pairs = T * top_k
+  int64_t NP;       // positions: P routed + n_shared * T shared
+  int G_max;        // upper bound of work groups
+  size_t off_part, off_logits, off_idx, off_gate, off_offsets, off_sorted, off_inv, off_tok,
+      off_groups, off_ngroups, off_h, off_ypos, total;
+};
+
+MoePlan moe_plan(const dq_moe_desc& d, int T);
+
+}  // namespace dqmoe

@@ -1,0 +1,242 @@
+// qgemv_mma.cu — dq_qgemv for 16-bit activations (and the scaled path for
+// bf16): the streaming GEMV of qgemv_mma.cuh over a grid of 64-row tiles,
+// optionally split along K over a thread-block cluster whose partial sums are
+// reduced through distributed shared memory (split-K for small N, without a
+// second pass and without scratch memory).
+#include <algorithm>
+
+#include "qgemv_mma.cuh"
+
+namespace dqmoe {
+
+struct GemvParams {
+  const uint8_t* W;
+  int64_t row_bytes;
+  int N;
+  int nsb;          // super-blocks (256 weights) per row
+  XSrc x;           // [batch][K]
+  int batch;
+  float* y;         // [batch][N]
+  int nstage;
+};
+
+template <int FMT>
+__global__ void __launch_bounds__(kThreads) qgemv_mma_kernel(const GemvParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  using L = Layout<FMT>;
+  const int ksplit = (int)cluster_nctarank();
+  const int rank = (int)cluster_ctarank();
+  const SmemPlan plan = make_plan<FMT>(p.nstage, p.batch, ksplit);
+  uint64_t* full = (uint64_t*)(smem + plan.off_bar);
+  uint64_t* empty = full + plan.nstage;
+  uint64_t* red_full = empty + plan.nstage;
+  uint8_t* wbuf = smem + plan.off_w;
+  uint8_t* xbuf = smem + plan.off_x;
+  float* xinv = (float*)(smem + plan.off_xinv);
+  float* red = (float*)(smem + plan.off_red);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile = blockIdx.y;
+  const int row0 = tile * kTileRows;
+  const int rows_valid = min(kTileRows, p.N - row0);
+
+  // this CTA's super-block range [sb0, sb1)
+  const int sb0 = (int)((int64_t)p.nsb * rank / ksplit);
+  const int sb1 = (int)((int64_t)p.nsb * (rank + 1) / ksplit);
+  const int nchunk = (sb1 - sb0 + L::C - 1) / L::C;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < plan.nstage; ++s) {
+      mbar_init(&full[s], 32);                 // 32 loader lanes (+ tx bytes)
+      mbar_init(&empty[s], kConsumerWarps);    // one per consumer warp
+    }
+    if (ksplit > 1) mbar_init(red_full, (ksplit - 1) * kConsumerWarps * 32);
+    fence_barrier_init();
+  }
+  if (ksplit > 1) cluster_sync_all();
+  else __syncthreads();
+
+  if (warp == 0) {
+    // ------------------------------ loader ------------------------------
+    const uint64_t pol = l2_evict_first_policy();
+    bool ok = true;
+    for (int c = 0; c < nchunk && ok; ++c) {
+      const int s = c % plan.nstage, round = c / plan.nstage;
+      if (round > 0) ok = mbar_wait(&empty[s], (round - 1) & 1);
+      if (!ok) break;
+      const int c0 = sb0 + c * L::C;
+      const int ncs = min(L::C, sb1 - c0);
+      // byte range of each row: [a, b) rounded to 16 bytes (Q6_K blocks are
+      // 210 bytes; the row start itself is 16-byte aligned)
+      const int64_t a_raw = (int64_t)c0 * L::SBB, b_raw = (int64_t)(c0 + ncs) * L::SBB;
+      const int64_t a = a_raw & ~(int64_t)15, b = (b_raw + 15) & ~(int64_t)15;
+      const uint32_t bytes = (uint32_t)(b - a);
+      if (lane == 0) mbar_expect_tx(&full[s], bytes * rows_valid);
+      __syncwarp();
+      uint8_t* wst = wbuf + s * L::W_STAGE;
+      for (int r = lane; r < rows_valid; r += 32)
+        bulk_g2s(wst + r * L::ROW_PITCH, p.W + (int64_t)(row0 + r) * p.row_bytes + a, bytes,
+                 &full[s], pol);
+      convert_x_stage<FMT>(p.x, p.batch, (int64_t)c0 * 256, ncs,
+                           xbuf + s * p.batch * L::XCOL, xinv + s * 8, lane);
+      mbar_arrive(&full[s]);
+    }
+  } else {
+    // ----------------------------- consumers -----------------------------
+    const int cw = warp - 1;
+    const int g = lane >> 2, t = lane & 3;
+    const bool xon = g < p.batch;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    bool ok = true;
+    for (int c = 0; c < nchunk; ++c) {
+      const int s = c % plan.nstage, round = c / plan.nstage;
+      ok = ok && mbar_wait(&full[s], round & 1);
+      if (!ok) continue;
+      const int c0 = sb0 + c * L::C;
+      const int ncs = min(L::C, sb1 - c0);
+      const int delta = (int)(((int64_t)c0 * L::SBB) & 15);
+      const uint32_t wst = smem_u32(wbuf + s * L::W_STAGE) + (16 * cw + g) * L::ROW_PITCH + delta;
+      const uint32_t xcol = smem_u32(xbuf + (s * p.batch + (xon ? g : 0)) * L::XCOL);
+      float part[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int j = 0; j < ncs; ++j)
+        SBDot<FMT>::run(wst + j * L::SBB, 8 * L::ROW_PITCH, xcol, j * 256, t, xon, part);
+      const float inv0 = xinv[s * 8 + ((2 * t) & 7)], inv1 = xinv[s * 8 + ((2 * t + 1) & 7)];
+      acc[0] = fmaf(part[0], inv0, acc[0]);
+      acc[1] = fmaf(part[1], inv1, acc[1]);
+      acc[2] = fmaf(part[2], inv0, acc[2]);
+      acc[3] = fmaf(part[3], inv1, acc[3]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+
+    // ------------------------ split-K reduction -------------------------
+    if (ksplit > 1) {
+      if (rank != 0) {
+        float* slot = red + (((rank - 1) * kConsumerWarps + cw) * 32 + lane) * 4;
+        st_cluster_f32x4(slot, 0, acc[0], acc[1], acc[2], acc[3]);
+        mbar_arrive_cluster(red_full, 0);
+      } else {
+        if (mbar_wait_cluster(red_full, 0)) {
+          for (int r = 1; r < ksplit; ++r) {   // fixed order: deterministic
+            const float4 v = *(const float4*)(red + (((r - 1) * kConsumerWarps + cw) * 32 + lane) * 4);
+            acc[0] += v.x;
+            acc[1] += v.y;
+            acc[2] += v.z;
+            acc[3] += v.w;
+          }
+        }
+      }
+    }
+    if (rank == 0) {
+      const int ra = row0 + 16 * cw + g, rb = ra + 8;
+      const int c0 = 2 * t, c1 = 2 * t + 1;
+      if (ra < p.N) {
+        if (c0 < p.batch) p.y[(int64_t)c0 * p.N + ra] = acc[0];
+        if (c1 < p.batch) p.y[(int64_t)c1 * p.N + ra] = acc[1];
+      }
+      if (rb < p.N) {
+        if (c0 < p.batch) p.y[(int64_t)c0 * p.N + rb] = acc[2];
+        if (c1 < p.batch) p.y[(int64_t)c1 * p.N + rb] = acc[3];
+      }
+    }
+  }
+}
+
+namespace {
+
+int device_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev < 64 && cached[dev]) return cached[dev];
+  int sms = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (dev < 64) cached[dev] = sms;
+  return sms;
+}
+
+// Pick the K-split (cluster size, 1..8) that best fills the GPU: balance of
+// the CTA waves times balance of the super-blocks inside a cluster.
+int choose_ksplit(int tiles, int nsb, int slots) {
+  int best = 1;
+  double best_eff = -1.0;
+  for (int s = 1; s <= 8; ++s) {
+    if (nsb / s < 1) break;
+    const double waves = (double)tiles * s / slots;
+    const double eff_w = waves / std::ceil(waves);
+    const double per = (double)nsb / s;
+    const double eff_k = per / std::ceil(per);
+    // small penalty for very short K slices (pipeline fill per CTA)
+    const double eff_fill = per / (per + 0.5);
+    const double eff = eff_w * eff_k * eff_fill;
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best = s;
+    }
+  }
+  return best;
+}
+
+}  // namespace
+
+template <int FMT>
+int launch_qgemv_mma_fmt(const void* W, int64_t N, int64_t K, const void* x, int xdt, int batch,
+                         float* y, cudaStream_t stream, int force_ksplit) {
+  using L = Layout<FMT>;
+  GemvParams p;
+  p.W = (const uint8_t*)W;
+  p.nsb = (int)(K / 256);
+  p.row_bytes = (int64_t)p.nsb * L::SBB;
+  p.N = (int)N;
+  p.x.base = x;
+  p.x.dtype = xdt;
+  p.x.col_stride = K;
+  p.x.rows = nullptr;
+  p.batch = batch;
+  p.y = y;
+  const int tiles = (int)((N + kTileRows - 1) / kTileRows);
+  const int sms = device_sms();
+  if (sms <= 0) return DQ_ERR_CUDA;
+  int ks = force_ksplit > 0 ? force_ksplit : choose_ksplit(tiles, p.nsb, 2 * sms);
+  ks = std::max(1, std::min(ks, std::min(8, p.nsb)));
+  // stages: as many as fit two CTAs per SM (<= 113 KB each), at least 3
+  int nstage = 6;
+  while (nstage > 3 && make_plan<FMT>(nstage, batch, ks).total > 113 * 1024) --nstage;
+  p.nstage = nstage;
+  const SmemPlan plan = make_plan<FMT>(nstage, batch, ks);
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 64 || !attr_set[dev]) {
+    if (cudaFuncSetAttribute(qgemv_mma_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             200 * 1024) != cudaSuccess)
+      return DQ_ERR_CUDA;
+    if (cudaFuncSetAttribute(qgemv_mma_kernel<FMT>, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                             1) != cudaSuccess)
+      return DQ_ERR_CUDA;
+    if (dev < 64) attr_set[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ks, (unsigned)tiles, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)plan.total;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)ks;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, qgemv_mma_kernel<FMT>, p) != cudaSuccess) return DQ_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
+}
+
+int launch_qgemv_mma(int fmt, const void* W, int64_t N, int64_t K, const void* x, int xdt,
+                     int batch, float* y, cudaStream_t s, int force_ksplit) {
+  if (fmt == DQ_Q4_K) return launch_qgemv_mma_fmt<DQ_Q4_K>(W, N, K, x, xdt, batch, y, s, force_ksplit);
+  if (fmt == DQ_Q6_K) return launch_qgemv_mma_fmt<DQ_Q6_K>(W, N, K, x, xdt, batch, y, s, force_ksplit);
+  return launch_qgemv_mma_fmt<DQ_Q8_0>(W, N, K, x, xdt, batch, y, s, force_ksplit);
+}
+
+}  // namespace dqmoe

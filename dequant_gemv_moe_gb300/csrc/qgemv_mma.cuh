@@ -1,0 +1,386 @@
+// qgemv_mma.cuh — the streaming quantized GEMV core for 16-bit-operand
+// tensor-core products, shared by dq_qgemv and the grouped MoE kernels.
+//
+// What it computes: for a 64-row tile of a quantized matrix W (N x K, blocks
+// of dqmoe.h) and up to 8 activation columns, acc[row][col] = sum_k W x, fp32
+// accumulate — the decode linear of [NTransformer, §核心性能] and the expert
+// projections of [Titan Engine, §MoE 专家流式加载].
+//
+// How (sm_103a):
+//   * warp 0 is the loader.  Per pipeline stage it issues one 1-D bulk copy
+//     (TMA engine, L2 evict-first) per weight row of C super-blocks into a
+//     padded shared-memory row, and converts the activation chunk of the stage
+//     into fp16 (with a per-column power-of-two scale for bf16/fp32 inputs, so
+//     no value overflows fp16), writing it in a bank-skewed layout.
+//   * warps 1..4 are consumers, 16 rows each.  Lane (g = lane/4, t = lane%4)
+//     owns 64 weights of every super-block of rows g and g+8: it decodes them
+//     in registers to fp16 (magic-number nibble unpack, exact integer, then one
+//     fused scale/min per pair) straight into the A fragment of
+//     mma.m16n8k16 (rows = weights, k = 16 weights, n = 8 activation columns).
+//     Scales are folded into A, so the k order inside an mma is free; the
+//     activation B fragment is read in natural k order.
+//   * fp32 accumulators per stage are scaled by the column's inverse scale and
+//     summed into the running accumulator.
+//   * stages flow through full/empty mbarriers with bounded waits.
+// Arithmetic per weight: ~1.6 integer/half2 instructions (Q4_K); the tensor
+// core does the multiply-accumulate, so the loop stays HBM-bound at batch 1..8.
+#pragma once
+
+#include "common.cuh"
+
+namespace dqmoe {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kTileRows = 16 * kConsumerWarps;   // 64
+constexpr int kThreads = 32 * (kConsumerWarps + 1);
+
+// fp16 element offset of activation k inside a stage column: 4 halves of
+// padding after every 64 so that the 4 lanes of a quad hit distinct banks.
+__host__ __device__ constexpr int xoff(int k) { return k + 4 * (k >> 6); }
+
+template <int FMT>
+struct Layout {
+  static constexpr int SBB = Fmt<FMT>::SB_BYTES;
+  // super-blocks (256 weights) per pipeline stage per row: ~300 bytes per row
+  static constexpr int C = (FMT == DQ_Q4_K) ? 2 : 1;
+  // bytes reserved per weight row per stage (Q6_K stages start off 16 B).
+  static constexpr int ROW_RAW = C * SBB + (FMT == DQ_Q6_K ? 32 : 0);
+  static constexpr int ROW_A16 = (ROW_RAW + 15) / 16 * 16;
+  // pitch = 16 (mod 32) bytes: rows g and g+1 land on different bank halves
+  static constexpr int ROW_PITCH = (ROW_A16 % 32 == 16) ? ROW_A16 : ROW_A16 + 16;
+  static constexpr int W_STAGE = kTileRows * ROW_PITCH;
+  // activation column pitch: 32 (mod 128) bytes
+  static constexpr int XCOL_RAW = xoff(C * 256) * 2;
+  static constexpr int XCOL = XCOL_RAW + ((32 - XCOL_RAW % 128) + 128) % 128;
+};
+
+// Dynamic shared memory layout of one CTA (offsets in bytes).
+struct SmemPlan {
+  int nstage, batch, ksplit;
+  int off_bar, off_w, off_x, off_xinv, off_red, total;
+};
+
+template <int FMT>
+__host__ __device__ inline SmemPlan make_plan(int nstage, int batch, int ksplit) {
+  SmemPlan p;
+  p.nstage = nstage;
+  p.batch = batch;
+  p.ksplit = ksplit;
+  p.off_bar = 0;                                       // full[ns], empty[ns], red
+  p.off_w = 1024;
+  p.off_x = p.off_w + nstage * Layout<FMT>::W_STAGE;
+  p.off_xinv = p.off_x + nstage * batch * Layout<FMT>::XCOL;
+  p.off_red = p.off_xinv + nstage * 8 * 4;
+  p.off_red = (p.off_red + 15) / 16 * 16;
+  p.total = p.off_red + (ksplit > 1 ? (ksplit - 1) * kConsumerWarps * 32 * 16 : 0);
+  return p;
+}
+
+// ---------------------------------------------------------------------------
+// Activation sources: the loader converts a column chunk of 8 values.
+// ---------------------------------------------------------------------------
+struct XSrc {
+  const void* base;   // element 0 of row 0
+  int dtype;          // DQ_F16 / DQ_BF16 / DQ_F32
+  int64_t col_stride; // elements between rows
+  const int* rows;    // column c reads row rows[c] (gather); nullptr: row c
+};
+
+__device__ __forceinline__ int64_t xrow(const XSrc& xs, int c) {
+  return xs.rows ? (int64_t)__ldg(xs.rows + c) : (int64_t)c;
+}
+
+__device__ __forceinline__ void load8_f32(const XSrc& xs, int col, int64_t k, float (&v)[8]) {
+  if (xs.dtype == DQ_F32) {
+    const float4* p = (const float4*)((const float*)xs.base + xrow(xs, col) * xs.col_stride + k);
+    const float4 a = __ldg(p), b = __ldg(p + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  } else {
+    const uint4 u = __ldg((const uint4*)((const uint16_t*)xs.base + xrow(xs, col) * xs.col_stride + k));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    if (xs.dtype == DQ_BF16) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __half22float2(u32_as_h2(w[i]));
+        v[2 * i] = f.x;
+        v[2 * i + 1] = f.y;
+      }
+    }
+  }
+}
+
+// scale = 2^(14 - e) where max|x| in [2^e, 2^(e+1)): scaled values < 2^15.
+__device__ __forceinline__ void pow2_scale(float amax, float& scale, float& inv) {
+  const uint32_t bits = __float_as_uint(amax);
+  int e = (int)((bits >> 23) & 255) - 127;
+  if (amax == 0.f || e == 128) {   // zero column (or non-finite: out of contract)
+    scale = 1.f;
+    inv = 1.f;
+    return;
+  }
+  if (e < -126) e = -126;
+  int se = 14 - e;                 // in [-113, 140]
+  if (se > 126) se = 126;          // keep both 2^se and 2^-se normal
+  scale = __uint_as_float((uint32_t)(127 + se) << 23);
+  inv = __uint_as_float((uint32_t)(127 - se) << 23);
+}
+
+// Loader: convert columns of one stage (nsb_stage super-blocks starting at
+// activation index k0) into fp16 at xdst (column pitch XCOL bytes).
+template <int FMT>
+__device__ __forceinline__ void convert_x_stage(const XSrc& xs, int ncols, int64_t k0, int nsb_stage,
+                                                uint8_t* xdst, float* xinv, int lane) {
+  for (int c = 0; c < ncols; ++c) {
+    uint8_t* col = xdst + c * Layout<FMT>::XCOL;
+    if (xs.dtype == DQ_F16) {
+      const int64_t rowoff = xrow(xs, c) * xs.col_stride;
+      for (int j = 0; j < nsb_stage; ++j) {
+        const int k = j * 256 + 8 * lane;
+        const uint4 u = __ldg((const uint4*)((const uint16_t*)xs.base + rowoff + k0 + k));
+        uint2* d = (uint2*)(col + 2 * xoff(k));
+        d[0] = make_uint2(u.x, u.y);
+        d[1] = make_uint2(u.z, u.w);
+      }
+      if (lane == 0) xinv[c] = 1.f;
+    } else {
+      constexpr int C = Layout<FMT>::C;
+      float v[C][8];
+      float amax = 0.f;
+#pragma unroll
+      for (int j = 0; j < C; ++j) {
+        if (j < nsb_stage) {
+          load8_f32(xs, c, k0 + j * 256 + 8 * lane, v[j]);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[j][i]));
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      float sc, inv;
+      pow2_scale(amax, sc, inv);
+#pragma unroll
+      for (int j = 0; j < C; ++j) {
+        if (j < nsb_stage) {
+          uint32_t h[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            h[i] = h2_as_u32(__floats2half2_rn(v[j][2 * i] * sc, v[j][2 * i + 1] * sc));
+          uint2* d = (uint2*)(col + 2 * xoff(j * 256 + 8 * lane));
+          d[0] = make_uint2(h[0], h[1]);
+          d[1] = make_uint2(h[2], h[3]);
+        }
+      }
+      if (lane == 0) xinv[c] = inv;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Consumer: one super-block of 16 rows (rows g, g+8 of lane) x 256 weights.
+// wrow: shared address of row g's super-block; pitch: bytes to row g+8.
+// xcol: shared address of this lane's activation column, at the stage start;
+// kb: k offset of the super-block inside the stage (j*256).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void ldx(uint32_t xcol, int k, bool on, uint32_t& b0, uint32_t& b1) {
+  if (on) {
+    const uint2 v = lds_u64(xcol + 2 * xoff(k));
+    b0 = v.x;
+    b1 = v.y;
+  } else {
+    b0 = 0u;
+    b1 = 0u;
+  }
+}
+
+template <int FMT>
+struct SBDot;
+
+// Q4_K: lane t owns qs group t (bytes 32t..32t+31): sub-blocks 2t (low
+// nibbles) and 2t+1 (high nibbles), weights 64t + [0,64).
+template <>
+struct SBDot<DQ_Q4_K> {
+  __device__ __forceinline__ static void scales(uint4 hd, int t, __half2& slo, __half2& olo,
+                                                __half2& shi, __half2& ohi) {
+    const int jj = 2 * (t & 1);
+    const uint32_t sel = (uint32_t)jj | (4u << 4) | ((uint32_t)(jj + 1) << 8) | (4u << 12);
+    const uint32_t hy = __byte_perm(hd.y, 0, sel);
+    const uint32_t hz = __byte_perm(hd.z, 0, sel);
+    const uint32_t hw = __byte_perm(hd.w, 0, sel);
+    uint32_t sc, mn;
+    if (t < 2) {
+      sc = hy & 0x003F003Fu;
+      mn = hz & 0x003F003Fu;
+    } else {
+      sc = (hw & 0x000F000Fu) | ((hy >> 2) & 0x00300030u);
+      mn = ((hw >> 4) & 0x000F000Fu) | ((hz >> 2) & 0x00300030u);
+    }
+    const __half2 magic = u32_as_h2(0x64006400u);
+    const __half2 sch = __hsub2(u32_as_h2(sc | 0x64006400u), magic);   // exact ints
+    const __half2 mnh = __hsub2(u32_as_h2(mn | 0x64006400u), magic);
+    const __half2 d2 = __half2half2(__ushort_as_half((unsigned short)(hd.x & 0xFFFF)));
+    const __half2 dm2 = __half2half2(__hneg(__ushort_as_half((unsigned short)(hd.x >> 16))));
+    const __half2 s = __hmul2(d2, sch);      // (d*sc_lo, d*sc_hi)
+    const __half2 o = __hmul2(dm2, mnh);     // (-dmin*m_lo, -dmin*m_hi)
+    slo = __low2half2(s);
+    olo = __low2half2(o);
+    shi = __hmul2(__high2half2(s), __float2half2_rn(0.0625f));   // high nibbles carry x16
+    ohi = __high2half2(o);
+  }
+
+  __device__ __forceinline__ static void run(uint32_t wrow, int pitch8, uint32_t xcol, int kb,
+                                             int t, bool xon, float (&acc)[4]) {
+    const uint32_t r0 = wrow, r8 = wrow + pitch8;
+    const uint4 h0 = lds_u128(r0), h8 = lds_u128(r8);
+    __half2 s0l, o0l, s0h, o0h, s8l, o8l, s8h, o8h;
+    scales(h0, t, s0l, o0l, s0h, o0h);
+    scales(h8, t, s8l, o8l, s8h, o8h);
+    const uint4 qa0 = lds_u128(r0 + 16 + 32 * t), qb0 = lds_u128(r0 + 32 + 32 * t);
+    const uint4 qa8 = lds_u128(r8 + 16 + 32 * t), qb8 = lds_u128(r8 + 32 + 32 * t);
+    const uint32_t q0[8] = {qa0.x, qa0.y, qa0.z, qa0.w, qb0.x, qb0.y, qb0.z, qb0.w};
+    const uint32_t q8[8] = {qa8.x, qa8.y, qa8.z, qa8.w, qb8.x, qb8.y, qb8.z, qb8.w};
+    const __half2 magic = u32_as_h2(0x64006400u);
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      // bytes (b0 b1 b2 b3) -> (b0 b2 b1 b3): 16-bit lanes hold weights k, k+1
+      const uint32_t p0 = __byte_perm(q0[s], 0, 0x3120), p8 = __byte_perm(q8[s], 0, 0x3120);
+      const uint32_t p0s = p0 >> 8, p8s = p8 >> 8;
+      const int k = kb + 64 * t + 4 * s;
+      uint32_t b0, b1;
+      // low nibbles: weights k..k+3 (sub-block 2t)
+      ldx(xcol, k, xon, b0, b1);
+      {
+        const uint32_t a0 = h2_as_u32(__hfma2(__hsub2(u32_as_h2(lop3_and_or(p0, 0x000F000Fu, 0x64006400u)), magic), s0l, o0l));
+        const uint32_t a1 = h2_as_u32(__hfma2(__hsub2(u32_as_h2(lop3_and_or(p8, 0x000F000Fu, 0x64006400u)), magic), s8l, o8l));
+        const uint32_t a2 = h2_as_u32(__hfma2(__hsub2(u32_as_h2(lop3_and_or(p0s, 0x000F000Fu, 0x64006400u)), magic), s0l, o0l));
+        const uint32_t a3 = h2_as_u32(__hfma2(__hsub2(u32_as_h2(lop3_and_or(p8s, 0x000F000Fu, 0x64006400u)), magic), s8l, o8l));
+        mma_16816(acc, a0, a1, a2, a3, b0, b1);
+      }
+      // high nibbles: weights k+32..k+35 (sub-block 2t+1), value 16*q
+      ldx(xcol, k + 32, xon, b0, b1);
+      {
+        const uint32_t a0 = h2_as_u32(__hfma2(__hsub2(u32_as_h2(lop3_and_or(p0, 0x00F000F0u, 0x64006400u)), magic), s0h, o0h));
+        const uint32_t a1 = h2_as_u32(__hfma2(__hsub2(u32_as_h2(lop3_and_or(p8, 0x00F000F0u, 0x64006400u)), magic), s8h, o8h));
+        const uint32_t a2 = h2_as_u32(__hfma2(__hsub2(u32_as_h2(lop3_and_or(p0s, 0x00F000F0u, 0x64006400u)), magic), s0h, o0h));
+        const uint32_t a3 = h2_as_u32(__hfma2(__hsub2(u32_as_h2(lop3_and_or(p8s, 0x00F000F0u, 0x64006400u)), magic), s8h, o8h));
+        mma_16816(acc, a0, a1, a2, a3, b0, b1);
+      }
+    }
+  }
+};
+
+// Q6_K: lane t owns, in each half h, positions l in [8t, 8t+8) of the four
+// 32-weight runs r = 0..3: weights 128h + 32r + l, scale index 8h + 2r + t/2.
+// Blocks are 210 bytes, so every other block is only 2-byte aligned.
+template <>
+struct SBDot<DQ_Q6_K> {
+  __device__ __forceinline__ static uint32_t q6_pair(uint32_t nib, uint32_t hq) {
+    // nib: 4-bit values in bits 0-3 of each 16-bit lane; hq: 2-bit values
+    // already in bits 4-5.  Returns fp16 pair of (q - 32), exact.
+    const uint32_t v = (nib & 0x000F000Fu) | (hq & 0x00300030u) | 0x64006400u;
+    return h2_as_u32(__hsub2(u32_as_h2(v), u32_as_h2(0x64206420u)));   // 1024+q - 1056
+  }
+
+  __device__ __forceinline__ static void run(uint32_t wrow, int pitch8, uint32_t xcol, int kb,
+                                             int t, bool xon, float (&acc)[4]) {
+    const uint32_t rows[2] = {wrow, wrow + pitch8};
+    // d and this lane's 8 scales per row: sc[8h + 2r + t/2], h = 0..1, r = 0..3
+    __half2 scl[2][8];
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      const uint32_t rb = rows[rr];
+      const __half d = __ushort_as_half((unsigned short)lds_u16(rb + 208));
+      const uint32_t s0 = lds_u32_a2(rb + 192), s1 = lds_u32_a2(rb + 196);
+      const uint32_t s2 = lds_u32_a2(rb + 200), s3 = lds_u32_a2(rb + 204);
+      const uint32_t sw[4] = {s0, s1, s2, s3};
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int idx = 8 * h + 2 * r;    // + t/2
+          const uint32_t word = sw[idx >> 2];
+          const int byte = (idx & 3) + (t >> 1);
+          const int sc = (int)(int8_t)((word >> (8 * byte)) & 0xFF);
+          scl[rr][4 * h + r] = __half2half2(__hmul(d, __int2half_rn(sc)));
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        uint32_t A[2], B[2], H[2];
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+          const uint32_t rb = rows[rr];
+          A[rr] = __byte_perm(lds_u32_a2(rb + 64 * h + 8 * t + 4 * p), 0, 0x3120);
+          B[rr] = __byte_perm(lds_u32_a2(rb + 64 * h + 32 + 8 * t + 4 * p), 0, 0x3120);
+          H[rr] = __byte_perm(lds_u32_a2(rb + 128 + 32 * h + 8 * t + 4 * p), 0, 0x3120);
+        }
+        const int kbase = kb + 128 * h + 8 * t + 4 * p;
+        // run r: nibble source and the shift that brings qh bits 2r..2r+1 to 4..5
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          uint32_t a[4];
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr) {
+            const uint32_t src = (r & 1) ? B[rr] : A[rr];
+            const uint32_t nlo = (r & 2) ? (src >> 4) : src;            // weights k, k+1
+            const uint32_t nhi = (r & 2) ? (src >> 12) : (src >> 8);    // weights k+2, k+3
+            // qh bits 2r..2r+1 of each byte moved to bits 4..5 of its 16-bit lane
+            const uint32_t hq = H[rr], hs = H[rr] >> 8;
+            const uint32_t hlo = (r <= 2) ? (hq << (4 - 2 * r)) : (hq >> (2 * r - 4));
+            const uint32_t hhi = (r <= 2) ? (hs << (4 - 2 * r)) : (hs >> (2 * r - 4));
+            const __half2 sc = scl[rr][4 * h + r];
+            a[rr] = h2_as_u32(__hmul2(u32_as_h2(q6_pair(nlo, hlo)), sc));
+            a[2 + rr] = h2_as_u32(__hmul2(u32_as_h2(q6_pair(nhi, hhi)), sc));
+          }
+          uint32_t b0, b1;
+          ldx(xcol, kbase + 32 * r, xon, b0, b1);
+          mma_16816(acc, a[0], a[1], a[2], a[3], b0, b1);
+        }
+      }
+    }
+  }
+};
+
+// Q8_0: 8 blocks of 34 bytes per 256 weights; block s is step s; lane t owns
+// quants 8t..8t+7 of each block.
+template <>
+struct SBDot<DQ_Q8_0> {
+  __device__ __forceinline__ static void run(uint32_t wrow, int pitch8, uint32_t xcol, int kb,
+                                             int t, bool xon, float (&acc)[4]) {
+    const __half2 bias = __float2half2_rn(1152.f);   // 1024 + 128
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      uint32_t a[2][4];
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        const uint32_t blk = wrow + (rr ? pitch8 : 0) + 34 * s;
+        const __half2 d2 = __half2half2(__ushort_as_half((unsigned short)lds_u16(blk)));
+        const uint32_t w0 = lds_u32_a2(blk + 2 + 8 * t) ^ 0x80808080u;   // q + 128, unsigned
+        const uint32_t w1 = lds_u32_a2(blk + 6 + 8 * t) ^ 0x80808080u;
+        const uint32_t ws[2] = {w0, w1};
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          const uint32_t lo = __byte_perm(ws[m], 0x64646464u, 0x4140);   // bytes 0,1
+          const uint32_t hi = __byte_perm(ws[m], 0x64646464u, 0x4342);   // bytes 2,3
+          a[m][rr] = h2_as_u32(__hmul2(__hsub2(u32_as_h2(lo), bias), d2));
+          a[m][2 + rr] = h2_as_u32(__hmul2(__hsub2(u32_as_h2(hi), bias), d2));
+        }
+      }
+      uint32_t b0, b1;
+      ldx(xcol, kb + 32 * s + 8 * t, xon, b0, b1);
+      mma_16816(acc, a[0][0], a[0][1], a[0][2], a[0][3], b0, b1);
+      ldx(xcol, kb + 32 * s + 8 * t + 4, xon, b0, b1);
+      mma_16816(acc, a[1][0], a[1][1], a[1][2], a[1][3], b0, b1);
+    }
+  }
+};
+
+}  // namespace dqmoe

@@ -1,0 +1,123 @@
+"""torch-facing wrappers of the C ABI (marshalling only; see include/dqmoe.h)."""
+import ctypes
+
+import torch
+
+from ._lib import F16, F32, BF16, DqError, MoeDesc, lib
+
+_DT = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _call(name, *args):
+    rc = getattr(lib, name)(*args)
+    if rc != 0:
+        raise DqError(name, rc)
+
+
+def _dtype_code(x):
+    if x.dtype not in _DT:
+        raise TypeError("activation dtype must be float32, float16 or bfloat16, got %s" % x.dtype)
+    return _DT[x.dtype]
+
+
+def block_geometry(fmt):
+    qk, nb = ctypes.c_int(), ctypes.c_int()
+    _call("dq_block_geometry", fmt, ctypes.byref(qk), ctypes.byref(nb))
+    return qk.value, nb.value
+
+
+def dequant(fmt, blocks, n_weights, out=None):
+    """Decode n_weights weights of packed blocks (uint8 CUDA tensor) to fp32."""
+    if out is None:
+        out = torch.empty(n_weights, dtype=torch.float32, device=blocks.device)
+    _call("dq_dequant", fmt, _ptr(blocks), n_weights, _ptr(out), _stream())
+    return out
+
+
+def qgemv(fmt, W, N, K, x, y=None, ksplit=None):
+    """y[b][n] = sum_k W[n][k] x[b][k]; x is [batch][K] (float32/float16/bfloat16)."""
+    x = x.reshape(-1, K)
+    batch = x.shape[0]
+    if y is None:
+        y = torch.empty(batch, N, dtype=torch.float32, device=x.device)
+    if ksplit is None:
+        _call("dq_qgemv", fmt, _ptr(W), N, K, _ptr(x), _dtype_code(x), batch, _ptr(y), _stream())
+    else:
+        _call("dq_qgemv_ksplit", fmt, _ptr(W), N, K, _ptr(x), _dtype_code(x), batch, _ptr(y),
+              int(ksplit), _stream())
+    return y
+
+
+def device_status():
+    v = ctypes.c_int()
+    _call("dq_device_status", ctypes.byref(v))
+    return v.value
+
+
+# ---------------------------------------------------------------- MoE layer
+def make_desc(E, top_k, hidden, ffn, n_shared, fmt, router_W, w_gate, w_up, w_down,
+              sh_gate=None, sh_up=None, sh_down=None):
+    d = MoeDesc()
+    d.E, d.top_k, d.hidden, d.ffn, d.n_shared, d.fmt = E, top_k, hidden, ffn, n_shared, fmt
+    d.router_W, d.w_gate, d.w_up, d.w_down = (router_W.data_ptr(), w_gate.data_ptr(),
+                                              w_up.data_ptr(), w_down.data_ptr())
+    d.sh_gate = sh_gate.data_ptr() if sh_gate is not None else None
+    d.sh_up = sh_up.data_ptr() if sh_up is not None else None
+    d.sh_down = sh_down.data_ptr() if sh_down is not None else None
+    return d
+
+
+def moe_workspace_size(desc, T):
+    n = ctypes.c_size_t()
+    _call("dq_moe_workspace_size", ctypes.byref(desc), T, ctypes.byref(n))
+    return n.value
+
+
+def moe_router(router_W, E, H, x, top_k, logits=None, want_logits=True):
+    T = x.shape[0]
+    dev = x.device
+    if logits is None and want_logits:
+        logits = torch.empty(T, E, dtype=torch.float32, device=dev)
+    idx = torch.empty(T, top_k, dtype=torch.int32, device=dev)
+    gate = torch.empty(T, top_k, dtype=torch.float32, device=dev)
+    _call("dq_moe_router", _ptr(router_W), E, H, _ptr(x), _dtype_code(x), T, top_k, _ptr(logits),
+          _ptr(idx), _ptr(gate), _stream())
+    return logits, idx, gate
+
+
+def moe_permute(topk_idx, E):
+    T, k = topk_idx.shape
+    dev = topk_idx.device
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    sorted_ = torch.empty(T * k, dtype=torch.int32, device=dev)
+    _call("dq_moe_permute", _ptr(topk_idx), T, k, E, _ptr(offsets), _ptr(sorted_), _stream())
+    return offsets, sorted_
+
+
+def moe_forward(desc, x, y=None, ws=None, want_routing=False):
+    """The whole MoE layer.  Returns y (and idx, gate, logits if want_routing)."""
+    T = x.shape[0]
+    dev = x.device
+    if y is None:
+        y = torch.empty(T, desc.hidden, dtype=torch.float32, device=dev)
+    need = moe_workspace_size(desc, T)
+    if ws is None:
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    idx = gate = logits = None
+    if want_routing:
+        idx = torch.empty(T, desc.top_k, dtype=torch.int32, device=dev)
+        gate = torch.empty(T, desc.top_k, dtype=torch.float32, device=dev)
+        logits = torch.empty(T, desc.E, dtype=torch.float32, device=dev)
+    _call("dq_moe_forward", ctypes.byref(desc), _ptr(x), _dtype_code(x), T, _ptr(y), _ptr(ws),
+          ws.numel(), _ptr(idx), _ptr(gate), _ptr(logits), _stream())
+    if want_routing:
+        return y, idx, gate, logits
+    return y

@@ -123,16 +123,27 @@ int dq_dequant(int fmt, const void* blocks, int64_t n_weights, float* out,
  * the resident quantized weights; [Titan Engine, §性能表现]).
  *   W      : device, N rows of K/QK blocks (layout above), 16-byte aligned.
  *   x      : device [batch][K] of x_dtype, 16-byte aligned.
- *   y      : device fp32 [batch][N], 16-byte aligned; fully overwritten.
+ *   y      : device fp32 [batch][N], 4-byte aligned; fully overwritten.
  *   batch  : 1..DQ_MAX_BATCH.
  * fp16/bf16 activations run on the tensor-core path (weights decoded to fp16
  * in registers); fp32 activations run on an fp32 CUDA-core path (decode and
  * products in fp32).
- * Errors: DQ_ERR_ARG (null, N/K <= 0, K % QK != 0, batch outside 1..8),
- *         DQ_ERR_ALIGN (W, x, y not 16-B aligned; Q6_K needs K % 2048 == 0
- *         so that rows stay 16-B aligned), DQ_ERR_CUDA. */
+ * Errors: DQ_ERR_ARG (null, N/K <= 0, K % 256 != 0 — every format is
+ *         streamed in 256-weight units —, batch outside 1..8),
+ *         DQ_ERR_ALIGN (W, x not 16-B aligned, y not 4-B aligned; Q6_K needs
+ *         K % 2048 == 0 so that its 210-byte-block rows stay 16-B aligned),
+ *         DQ_ERR_UNSUPPORTED (N > 65535*64), DQ_ERR_CUDA. */
 int dq_qgemv(int fmt, const void* W, int64_t N, int64_t K, const void* x,
              int x_dtype, int batch, float* y, void* stream);
+
+/* dq_qgemv with the K split chosen by the caller (tuning and tests): the 16-bit
+ * activation path splits the K/256 super-blocks of every 64-row tile over a
+ * thread-block cluster of `ksplit` CTAs (1..8, clamped to K/256) and sums the
+ * partial results through distributed shared memory in a fixed order.
+ * ksplit = 0 lets the library choose (what dq_qgemv does).  Ignored for fp32
+ * activations.  Errors: as dq_qgemv, plus DQ_ERR_ARG for ksplit outside 0..8. */
+int dq_qgemv_ksplit(int fmt, const void* W, int64_t N, int64_t K, const void* x,
+                    int x_dtype, int batch, float* y, int ksplit, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Sparse MoE layer.                                                         */

@@ -1,0 +1,66 @@
+"""The C-ABI library loads and exports every symbol include/dqmoe.h declares
+(CPU only: no compute call without a GPU), and host-side validation rejects
+bad arguments before anything is launched."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "dqmoe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dq_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def so():
+    import importlib.util
+    path = os.path.join(ROOT, "dequant_gemv_moe_gb300", "build.py")
+    spec = importlib.util.spec_from_file_location("_dqmoe_build", path)
+    b = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(b)
+    return ctypes.CDLL(b.build())
+
+
+def test_header_symbols_exported(so):
+    names = _declared()
+    assert "dq_qgemv" in names and "dq_moe_forward" in names and "dq_dequant" in names
+    for n in names:
+        assert hasattr(so, n), n
+
+
+def test_status_strings(so):
+    so.dq_status_string.restype = ctypes.c_char_p
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert so.dq_status_string(code)
+    assert so.dq_status_string(12345) == b"unknown status"
+
+
+def test_qgemv_argument_errors_without_launch(so):
+    f = so.dq_qgemv
+    P, I, L = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    f.argtypes = [I, P, L, L, P, I, I, P, P]
+    a = P(4096)                # fake, aligned; never dereferenced on the error paths
+    assert f(9, a, 64, 256, a, 1, 1, a, None) == -1            # bad format
+    assert f(1, None, 64, 256, a, 1, 1, a, None) == -1         # null W
+    assert f(1, a, 64, 100, a, 1, 1, a, None) == -1            # K % 256
+    assert f(1, a, 64, 256, a, 1, 0, a, None) == -1            # batch 0
+    assert f(1, a, 64, 256, a, 1, 9, a, None) == -1            # batch 9
+    assert f(1, a, 64, 256, a, 7, 1, a, None) == -1            # bad dtype
+    assert f(1, P(4097), 64, 256, a, 1, 1, a, None) == -2      # misaligned W
+    assert f(2, a, 64, 1024, a, 1, 1, a, None) == -2           # Q6_K needs K % 2048
+    assert f(1, a, 0, 256, a, 1, 1, a, None) == -1             # N = 0
+
+
+def test_dequant_argument_errors(so):
+    f = so.dq_dequant
+    P = ctypes.c_void_p
+    f.argtypes = [ctypes.c_int, P, ctypes.c_int64, P, P]
+    a = P(4096)
+    assert f(1, a, 100, a, None) == -1
+    assert f(3, a, 0, a, None) == -1
+    assert f(3, P(4097), 32, a, None) == -2

@@ -1,0 +1,159 @@
+"""GPU parity of the MoE steps and the whole layer against the CPU oracle (-m gpu).
+
+Router logits: within the fp32 summation bound (gamma_n * sum |W x|).
+Top-k indices: bit-exact against the oracle's stable sort applied to the GPU's
+own logits; against the oracle's own (double) logits every disagreement must
+be a near-tie (gap below twice the bound).  Permute: bit-exact.  Layer output:
+max|y - y_ref| / max|y_ref| <= 2e-3 (16-bit operands on the tensor cores).
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from gpu_util import dev_act, dev_bytes, rel_err
+
+pytestmark = pytest.mark.gpu
+
+Q4_K, Q6_K, Q8_0 = 1, 2, 3
+MOE_TOL = 2e-3
+
+
+@pytest.fixture(scope="module")
+def dq():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import dequant_gemv_moe_gb300 as dq
+    return dq
+
+
+def _fp32_bound(Wr, xf, H):
+    # |fl(sum) - sum| <= gamma_n * sum |terms|, gamma_n = n u / (1 - n u), n = H + splits
+    u = 2.0 ** -24
+    n = H + 64
+    gam = n * u / (1 - n * u)
+    return gam * (np.abs(xf) @ np.abs(Wr.astype(np.float64)).T)
+
+
+def _check_router(orc, Wr, x, xdt, E, H, T, k, logits, idx, gate):
+    xf = orc.act_to_f64(xdt, x).reshape(T, H)
+    L_ref = orc.router_logits(Wr, E, H, x, xdt, T)
+    bound = _fp32_bound(Wr, xf, H)
+    assert np.all(np.abs(logits.astype(np.float64) - L_ref) <= bound)
+    # (ii) selection and tie-break exactly as the stable sort of the GPU's logits
+    idx_g, gate_g = orc.topk(logits.astype(np.float64), k)
+    np.testing.assert_array_equal(idx, idx_g)
+    np.testing.assert_allclose(gate, gate_g, rtol=2e-6, atol=1e-7)
+    # (iii) against the exact logits: only near-ties may differ
+    idx_r, _ = orc.topk(L_ref, k)
+    bad = np.nonzero(np.any(idx != idx_r, axis=1))[0]
+    for t in bad:
+        srt = np.sort(L_ref[t])[::-1]
+        gap = np.min(np.abs(np.diff(srt[max(0, k - 2):k + 1])))
+        assert gap <= 2 * bound[t].max(), (t, gap)
+    return len(bad)
+
+
+@pytest.mark.parametrize("E,k,H,T,xdt", [(8, 2, 4096, 16, 1), (256, 8, 7168, 8, 2),
+                                         (256, 8, 7168, 1, 2), (64, 6, 1024, 37, 0),
+                                         (3, 3, 256, 5, 1)])
+def test_router_topk(dq, orc, E, k, H, T, xdt):
+    g = synth.streams(900 + E + T, 2)
+    Wr = synth.router_weights(g[0], E, H)
+    x = synth.activations(g[1], (T, H), xdt)
+    logits, idx, gate = dq.moe_router(torch.from_numpy(Wr).cuda(), E, H, dev_act(x, xdt), k)
+    _check_router(orc, Wr, x, xdt, E, H, T, k, logits.cpu().numpy(), idx.cpu().numpy(),
+                  gate.cpu().numpy())
+
+
+def test_topk_ties_lowest_index(dq):
+    # zero router weights: every logit is 0, the selection is experts 0..k-1
+    E, k, H, T = 32, 4, 256, 3
+    Wr = torch.zeros(E, H, dtype=torch.float32, device="cuda")
+    x = torch.randn(T, H, device="cuda").half()
+    logits, idx, gate = dq.moe_router(Wr, E, H, x, k)
+    assert idx.cpu().numpy().tolist() == [[0, 1, 2, 3]] * T
+    np.testing.assert_allclose(gate.cpu().numpy(), 0.25, rtol=1e-7)
+
+
+@pytest.mark.parametrize("T,k,E", [(16, 2, 8), (8, 8, 256), (256, 8, 256), (1, 1, 1),
+                                   (1000, 4, 60)])
+def test_permute_bit_exact(dq, orc, T, k, E):
+    rng = np.random.default_rng(T * 31 + E)
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    offs, srt = dq.moe_permute(torch.from_numpy(idx).cuda(), E)
+    counts, offsets, sorted_ = orc.permute(idx, E)
+    np.testing.assert_array_equal(offs.cpu().numpy(), offsets)
+    np.testing.assert_array_equal(srt.cpu().numpy(), sorted_)
+
+
+def _moe_case(dq, orc, fmt, E, k, H, F, ns, T, xdt, seed, tokens=None):
+    w = synth.moe_weights(seed, E, H, F, ns, fmt)
+    x = synth.activations(synth.streams(seed + 1, 1)[0], (T, H), xdt)
+    dev = {kk: (dev_bytes(v) if v is not None and v.dtype == np.uint8 else
+                (torch.from_numpy(v).cuda() if v is not None else None)) for kk, v in w.items()}
+    desc = dq.ops.make_desc(E, k, H, F, ns, fmt, dev["router_W"], dev["w_gate"], dev["w_up"],
+                            dev["w_down"], dev["sh_gate"], dev["sh_up"], dev["sh_down"])
+    y, idx, gate, logits = dq.moe_forward(desc, dev_act(x, xdt), want_routing=True)
+    y = y.cpu().numpy()
+    assert dq.device_status() == 0
+    assert np.isfinite(y).all()
+    nb = _check_router(orc, w["router_W"], x, xdt, E, H, T, k, logits.cpu().numpy(),
+                       idx.cpu().numpy(), gate.cpu().numpy())
+    y_ref, idx_ref, _, _ = orc.moe_forward(fmt, E, k, H, F, ns, w["router_W"], w["w_gate"],
+                                           w["w_up"], w["w_down"], w["sh_gate"], w["sh_up"],
+                                           w["sh_down"], x, xdt, T, tokens=tokens)
+    rows = np.arange(T) if tokens is None else np.asarray(tokens)
+    # compare only tokens whose selection agrees with the exact one (near-ties
+    # legitimately route differently)
+    same = np.all(idx.cpu().numpy()[rows] == idx_ref[rows], axis=1)
+    assert same.sum() >= max(1, len(rows) - 1)
+    err = rel_err(y[rows][same], y_ref[same])
+    del dev
+    torch.cuda.empty_cache()
+    return err, nb
+
+
+@pytest.mark.parametrize("fmt,E,k,H,F,ns,T,xdt", [
+    (Q4_K, 8, 2, 512, 1024, 0, 5, 1),
+    (Q4_K, 8, 2, 512, 1024, 1, 16, 2),
+    (Q4_K, 16, 4, 1024, 512, 2, 33, 1),     # > 8 tokens on some experts: several groups
+    (Q8_0, 8, 3, 768, 512, 1, 9, 2),
+    (Q6_K, 4, 2, 2048, 2048, 1, 7, 1),
+    (Q4_K, 4, 4, 256, 256, 0, 3, 0),        # every expert active, fp32 activations
+    (Q4_K, 1, 1, 256, 512, 0, 1, 1),        # one expert, one token
+])
+def test_moe_forward_small(dq, orc, fmt, E, k, H, F, ns, T, xdt):
+    err, _ = _moe_case(dq, orc, fmt, E, k, H, F, ns, T, xdt, seed=3000 + E * 7 + T)
+    assert err <= MOE_TOL, err
+
+
+def test_moe_mixtral_config(dq, orc):
+    c = synth.MOE_MIXTRAL
+    err, nb = _moe_case(dq, orc, c["fmt"], c["E"], c["top_k"], c["H"], c["F"], c["n_shared"],
+                        16, c["xdt"], seed=synth.BASE_SEED + 3, tokens=[0, 5, 10, 15])
+    assert err <= MOE_TOL, err
+
+
+@pytest.mark.parametrize("T,tokens", [(1, None), (8, [0, 3, 7]), (256, [0, 101, 255])])
+def test_moe_deepseek_config(dq, orc, T, tokens):
+    c = synth.MOE_DEEPSEEK
+    err, nb = _moe_case(dq, orc, c["fmt"], c["E"], c["top_k"], c["H"], c["F"], c["n_shared"], T,
+                        c["xdt"], seed=synth.BASE_SEED + 4, tokens=tokens)
+    assert err <= MOE_TOL, err
+
+
+def test_moe_workspace_errors(dq):
+    import ctypes
+    E, k, H, F = 8, 2, 256, 256
+    d = dq.ops.make_desc(E, k, H, F, 0, 1, torch.zeros(E, H, device="cuda"),
+                         torch.zeros(E * F * 144, dtype=torch.uint8, device="cuda"),
+                         torch.zeros(E * F * 144, dtype=torch.uint8, device="cuda"),
+                         torch.zeros(E * H * 144, dtype=torch.uint8, device="cuda"))
+    need = dq.moe_workspace_size(d, 4)
+    x = torch.zeros(4, H, dtype=torch.float16, device="cuda")
+    y = torch.empty(4, H, device="cuda")
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    rc = dq.lib.dq_moe_forward(ctypes.byref(d), ctypes.c_void_p(x.data_ptr()), 1, 4,
+                               ctypes.c_void_p(y.data_ptr()), ctypes.c_void_p(ws.data_ptr()),
+                               need - 1, None, None, None, None)
+    assert rc == -4
