@@ -36,11 +36,32 @@ ROTATE = 4
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-moe", action="store_true", help="skip the MoE-layer lines")
+    ap.add_argument("--case", default=None,
+                    help="profiling aid: run only one workload a few times and exit "
+                         "(gemv70b | layer8b | mixtral | deepseek1 | deepseek8 | deepseek256)")
     return ap.parse_args()
+
+
+def run_case(args):
+    """Run one workload `--steps` times (for ncu captures); prints timings only."""
+    import torch
+    import dequant_gemv_moe_gb300 as dq
+    torch.cuda.set_device(0)
+    if args.case == "gemv70b":
+        print(json.dumps(bench_gemv_70b(torch, dq, reps=max(1, args.steps))))
+    elif args.case == "layer8b":
+        print(json.dumps({k: v for k, v in bench_layer(torch, dq, args).items() if k != "e2e"}))
+    elif args.case == "mixtral":
+        print(json.dumps(bench_moe(torch, dq, synth.MOE_MIXTRAL, 16, reps=max(1, args.steps))))
+    elif args.case.startswith("deepseek"):
+        T = int(args.case[len("deepseek"):])
+        print(json.dumps(bench_moe(torch, dq, synth.MOE_DEEPSEEK, T, reps=max(1, args.steps))))
+    else:
+        raise SystemExit("unknown case " + args.case)
 
 
 def peaks():
@@ -61,7 +82,7 @@ def weight_bytes(fmt, N, K):
 # clocks during the timed region
 # ---------------------------------------------------------------------------
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -74,7 +95,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -94,12 +115,27 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
-    def summary(self):
+    @staticmethod
+    def _ts(txt):
+        import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(txt, fmt).timestamp()
+            except ValueError:
+                pass
+        return None
+
+    def summary(self, t0=None, t1=None):
+        """Median SM clock and active throttle reasons of the samples taken
+        inside [t0, t1] (host wall-clock seconds; all samples if None)."""
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
+                continue
+            ts = self._ts(parts[0])
+            if t0 is not None and ts is not None and not (t0 - 0.06 <= ts <= t1 + 0.06):
                 continue
             try:
                 sm.append(float(parts[1]))
@@ -263,11 +299,13 @@ def bench_layer(torch, dq, args):
     torch.cuda.synchronize()
     K = args.steps
     ext_ok = make_event(torch, True) is not None
+    G = min(K + args.warmup, 400)
+    G = max(ROTATE, G - G % ROTATE)
     graphs, evsets = [], []
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
-        for i in range(K + args.warmup):
+        for i in range(G):
             evs = [make_event(torch, True) for _ in range(len(lin) + 1)] if ext_ok else None
             gr = torch.cuda.CUDAGraph()
             with torch.cuda.graph(gr, stream=s):
@@ -276,32 +314,36 @@ def bench_layer(torch, dq, args):
             evsets.append(evs)
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
-    for i in range(args.warmup):
-        graphs[i].replay()
-    torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(torch.cuda.current_device()) as clk:
+        time.sleep(0.3)   # let the sampler start
+        for i in range(args.warmup):
+            graphs[i % G].replay()
+        torch.cuda.synchronize()
+        t0 = time.time()
         start.record()
         for i in range(args.warmup, args.warmup + K):
-            graphs[i].replay()
+            graphs[i % G].replay()
         end.record()
         torch.cuda.synchronize()
+        t1 = time.time()
+        time.sleep(0.1)
     ms = start.elapsed_time(end)
-    # per-launch kernel durations from the events inside each step's graph
+    # per-launch kernel durations from the events inside each step's graph: the
+    # events of the last G timed steps (every graph's last replay is timed)
     kern_ms, kern_src = None, "graph_step_time/7"
-    if ext_ok:
+    if ext_ok and K >= G:
         tot = 0.0
-        for i in range(args.warmup, args.warmup + K):
-            e = evsets[i]
+        for e in evsets:
             tot += sum(e[j].elapsed_time(e[j + 1]) for j in range(len(lin)))
-        kern_ms = tot / (K * len(lin))
-        kern_src = "cuda events around each launch inside the step graphs"
+        kern_ms = tot / (G * len(lin))
+        kern_src = "cuda events around each launch inside the step graphs (last %d timed steps)" % G
     else:
         kern_ms = ms / (K * len(lin))
     del graphs
     res = {"ms_per_step": ms / K, "weight_bytes": wbytes, "act_bytes": abytes,
            "value": wbytes * K / (ms / 1e3) / 1e9, "kern_ms": kern_ms, "kern_src": kern_src,
-           "clocks": clk.summary(), "launches": K * len(lin)}
+           "clocks": clk.summary(t0, t1), "launches": K * len(lin)}
 
     # e2e: the same step through the public call with host buffers — pinned
     # x uploaded and y read back every step inside the timed region
@@ -494,7 +536,9 @@ def run_ours(args):
 
 def main():
     args = parse()
-    if args.impl == "reference":
+    if args.case:
+        run_case(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
