@@ -17,9 +17,11 @@
 // [Titan Engine, §MoE 专家流式加载]: only a few experts per token are active,
 // so only the touched experts' packed weights are streamed from HBM.
 #include <algorithm>
+#include <cstring>
 
 #include "moe_plan.h"
 #include "qgemv_mma.cuh"
+#include "tmap.h"
 
 namespace dqmoe {
 
@@ -275,6 +277,11 @@ __global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict
 // 4/5. persistent grouped streaming GEMV (gate/up with SwiGLU, or down)
 // ===========================================================================
 struct GroupedParams {
+  // TMA maps over the stacked matrices as [experts*rows][row_bytes/2]:
+  // routed a (gate or down), routed b (up), shared a, shared b.  Boxes are
+  // BOX x 32 rows (gate/up) or BOX x 64 rows (down).
+  CUtensorMap map_a, map_b, map_sa, map_sb;
+  int rows_per_expert; // F (gate/up) or H (down)
   const uint8_t* Wa;   // routed: W_gate (gate/up) or W_down (down), E stacked
   const uint8_t* Wb;   // routed: W_up (gate/up only)
   const uint8_t* Sa;   // shared experts, same roles
@@ -296,7 +303,7 @@ struct GroupedParams {
 };
 
 template <int FMT, bool GATEUP>
-__global__ void __launch_bounds__(kThreads) grouped_kernel(const GroupedParams p) {
+__global__ void __launch_bounds__(kThreads) grouped_kernel(const __grid_constant__ GroupedParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   using L = Layout<FMT>;
   const SmemPlan plan = make_plan<FMT>(p.nstage, 8, 1);
@@ -313,11 +320,12 @@ __global__ void __launch_bounds__(kThreads) grouped_kernel(const GroupedParams p
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < plan.nstage; ++s) {
-      mbar_init(&full[s], 32);
+      mbar_init(&full[s], 64);
       mbar_init(&empty[s], kConsumerWarps);
     }
     fence_barrier_init();
   }
+  init_xinv(xinv, plan.nstage, p.xdt);
   __syncthreads();
 
   if (warp == 0) {
@@ -330,22 +338,10 @@ __global__ void __launch_bounds__(kThreads) grouped_kernel(const GroupedParams p
       const int tile = u % p.tiles;
       const bool shared = grp.x >= p.E;
       const int eid = shared ? grp.x - p.E : grp.x;
-      // two weight rows per lane: r = lane and lane + 32
-      const uint8_t* rowp[2];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int r = lane + 32 * h;
-        const uint8_t* m;
-        int row;
-        if (GATEUP) {
-          m = (h == 0) ? (shared ? p.Sa : p.Wa) : (shared ? p.Sb : p.Wb);
-          row = tile * 32 + lane;
-        } else {
-          m = shared ? p.Sa : p.Wa;
-          row = tile * 64 + r;
-        }
-        rowp[h] = m + (int64_t)eid * p.mat_bytes + (int64_t)row * p.row_bytes;
-      }
+      // first stacked row of the tile: gate/up -> 32 gate rows then the same 32 up rows
+      const int grow = eid * p.rows_per_expert + (GATEUP ? tile * 32 : tile * 64);
+      const CUtensorMap* ma = shared ? &p.map_sa : &p.map_a;
+      const CUtensorMap* mb = shared ? &p.map_sb : &p.map_b;
       XSrc xs;
       xs.dtype = p.xdt;
       xs.col_stride = p.xstride;
@@ -362,17 +358,19 @@ __global__ void __launch_bounds__(kThreads) grouped_kernel(const GroupedParams p
         if (!ok) break;
         const int c0 = c * L::C;
         const int ncs = min(L::C, p.nsb - c0);
-        const int64_t a_raw = (int64_t)c0 * L::SBB, b_raw = (int64_t)(c0 + ncs) * L::SBB;
-        const int64_t a = a_raw & ~(int64_t)15, b = (b_raw + 15) & ~(int64_t)15;
-        const uint32_t bytes = (uint32_t)(b - a);
-        if (lane == 0) mbar_expect_tx(&full[s], bytes * kTileRows);
-        __syncwarp();
-        uint8_t* wst = wbuf + s * L::W_STAGE;
-        bulk_g2s(wst + lane * L::ROW_PITCH, rowp[0] + a, bytes, &full[s], pol);
-        bulk_g2s(wst + (lane + 32) * L::ROW_PITCH, rowp[1] + a, bytes, &full[s], pol);
-        convert_x_stage<FMT>(xs, grp.z, (int64_t)c0 * 256, ncs, xbuf + s * 8 * L::XCOL,
-                             xinv + s * 8, lane);
-        mbar_arrive(&full[s]);
+        const int64_t a = ((int64_t)c0 * L::SBB) & ~(int64_t)15;
+        if (lane == 0) {
+          uint8_t* wst = wbuf + s * L::W_STAGE;
+          mbar_expect_tx(&full[s], L::W_STAGE);
+          if (GATEUP) {
+            tma_load_2d(wst, ma, (int)(a >> 1), grow, &full[s], pol);
+            tma_load_2d(wst + 32 * L::ROW_PITCH, mb, (int)(a >> 1), grow, &full[s], pol);
+          } else {
+            tma_load_2d(wst, ma, (int)(a >> 1), grow, &full[s], pol);
+          }
+        }
+        stage_x<FMT>(xs, grp.z, (int64_t)c0 * 256, ncs, xbuf + s * 8 * L::XCOL, xinv + s * 8,
+                     lane, &full[s]);
       }
     }
   } else {
@@ -399,14 +397,14 @@ __global__ void __launch_bounds__(kThreads) grouped_kernel(const GroupedParams p
         const uint32_t wst =
             smem_u32(wbuf + s * L::W_STAGE) + (16 * cw + g) * L::ROW_PITCH + delta;
         const uint32_t xcol = smem_u32(xbuf + (s * 8 + (xon ? g : 0)) * L::XCOL);
-        float part[4] = {0.f, 0.f, 0.f, 0.f};
+        float part[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         for (int j = 0; j < ncs; ++j)
           SBDot<FMT>::run(wst + j * L::SBB, 8 * L::ROW_PITCH, xcol, j * 256, t, xon, part);
         const float inv0 = xinv[s * 8 + 2 * t], inv1 = xinv[s * 8 + 2 * t + 1];
-        acc[0] = fmaf(part[0], inv0, acc[0]);
-        acc[1] = fmaf(part[1], inv1, acc[1]);
-        acc[2] = fmaf(part[2], inv0, acc[2]);
-        acc[3] = fmaf(part[3], inv1, acc[3]);
+        acc[0] = fmaf(part[0][0] + part[1][0], inv0, acc[0]);
+        acc[1] = fmaf(part[0][1] + part[1][1], inv1, acc[1]);
+        acc[2] = fmaf(part[0][2] + part[1][2], inv0, acc[2]);
+        acc[3] = fmaf(part[0][3] + part[1][3], inv1, acc[3]);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
       }
@@ -496,9 +494,21 @@ int qk(int fmt) { return fmt == DQ_Q8_0 ? 32 : 256; }
 int blk_bytes(int fmt) { return fmt == DQ_Q4_K ? 144 : fmt == DQ_Q6_K ? 210 : 34; }
 
 template <int FMT, bool GATEUP>
-int launch_grouped(const GroupedParams& gp_in, int units_max, cudaStream_t s) {
+int launch_grouped(const GroupedParams& gp_in, int units_max, cudaStream_t s, int E, int n_shared) {
+  using L = Layout<FMT>;
   GroupedParams gp = gp_in;
-  int nstage = 6;
+  const uint32_t box_rows = GATEUP ? 32 : 64;
+  const uint64_t rpe = (uint64_t)gp.rows_per_expert;
+  if (!make_weight_tmap(&gp.map_a, gp.Wa, rpe * E, gp.row_bytes, L::BOX, box_rows)) return DQ_ERR_CUDA;
+  if (GATEUP && !make_weight_tmap(&gp.map_b, gp.Wb, rpe * E, gp.row_bytes, L::BOX, box_rows))
+    return DQ_ERR_CUDA;
+  if (n_shared > 0) {
+    if (!make_weight_tmap(&gp.map_sa, gp.Sa, rpe * n_shared, gp.row_bytes, L::BOX, box_rows))
+      return DQ_ERR_CUDA;
+    if (GATEUP && !make_weight_tmap(&gp.map_sb, gp.Sb, rpe * n_shared, gp.row_bytes, L::BOX, box_rows))
+      return DQ_ERR_CUDA;
+  }
+  int nstage = 12;
   while (nstage > 3 && make_plan<FMT>(nstage, 8, 1).total + 2048 > 113 * 1024) --nstage;
   gp.nstage = nstage;
   const int smem = make_plan<FMT>(nstage, 8, 1).total + 2048;
@@ -519,10 +529,11 @@ int launch_grouped(const GroupedParams& gp_in, int units_max, cudaStream_t s) {
 }
 
 template <bool GATEUP>
-int launch_grouped_fmt(int fmt, const GroupedParams& gp, int units_max, cudaStream_t s) {
-  if (fmt == DQ_Q4_K) return launch_grouped<DQ_Q4_K, GATEUP>(gp, units_max, s);
-  if (fmt == DQ_Q6_K) return launch_grouped<DQ_Q6_K, GATEUP>(gp, units_max, s);
-  return launch_grouped<DQ_Q8_0, GATEUP>(gp, units_max, s);
+int launch_grouped_fmt(int fmt, const GroupedParams& gp, int units_max, cudaStream_t s, int E,
+                       int n_shared) {
+  if (fmt == DQ_Q4_K) return launch_grouped<DQ_Q4_K, GATEUP>(gp, units_max, s, E, n_shared);
+  if (fmt == DQ_Q6_K) return launch_grouped<DQ_Q6_K, GATEUP>(gp, units_max, s, E, n_shared);
+  return launch_grouped<DQ_Q8_0, GATEUP>(gp, units_max, s, E, n_shared);
 }
 
 }  // namespace
@@ -568,7 +579,8 @@ int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, floa
   if (cudaGetLastError() != cudaSuccess) return DQ_ERR_CUDA;
 
   const int q = qk(d.fmt), bb = blk_bytes(d.fmt);
-  GroupedParams gu = {};
+  GroupedParams gu;
+  memset(&gu, 0, sizeof(gu));
   gu.Wa = (const uint8_t*)d.w_gate;
   gu.Wb = (const uint8_t*)d.w_up;
   gu.Sa = (const uint8_t*)d.sh_gate;
@@ -586,10 +598,12 @@ int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, floa
   gu.out = h;
   gu.out_stride = d.ffn;
   gu.tiles = d.ffn / 32;
-  rc = launch_grouped_fmt<true>(d.fmt, gu, pl.G_max * gu.tiles, s);
+  gu.rows_per_expert = d.ffn;
+  rc = launch_grouped_fmt<true>(d.fmt, gu, pl.G_max * gu.tiles, s, d.E, d.n_shared);
   if (rc != DQ_OK) return rc;
 
-  GroupedParams dn = {};
+  GroupedParams dn;
+  memset(&dn, 0, sizeof(dn));
   dn.Wa = (const uint8_t*)d.w_down;
   dn.Sa = (const uint8_t*)d.sh_down;
   dn.row_bytes = (int64_t)(d.ffn / q) * bb;
@@ -605,7 +619,8 @@ int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, floa
   dn.out = ypos;
   dn.out_stride = d.hidden;
   dn.tiles = d.hidden / 64;
-  rc = launch_grouped_fmt<false>(d.fmt, dn, pl.G_max * dn.tiles, s);
+  dn.rows_per_expert = d.hidden;
+  rc = launch_grouped_fmt<false>(d.fmt, dn, pl.G_max * dn.tiles, s, d.E, d.n_shared);
   if (rc != DQ_OK) return rc;
 
   const int64_t n4 = (int64_t)T * d.hidden / 4;

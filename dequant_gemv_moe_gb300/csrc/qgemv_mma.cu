@@ -6,10 +6,12 @@
 #include <algorithm>
 
 #include "qgemv_mma.cuh"
+#include "tmap.h"
 
 namespace dqmoe {
 
 struct GemvParams {
+  CUtensorMap tmap;  // W as [N rows][row_bytes/2] 16-bit elements, box BOX x 64 rows
   const uint8_t* W;
   int64_t row_bytes;
   int N;
@@ -21,7 +23,7 @@ struct GemvParams {
 };
 
 template <int FMT>
-__global__ void __launch_bounds__(kThreads) qgemv_mma_kernel(const GemvParams p) {
+__global__ void __launch_bounds__(kThreads) qgemv_mma_kernel(const __grid_constant__ GemvParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   using L = Layout<FMT>;
   const int ksplit = (int)cluster_nctarank();
@@ -38,7 +40,6 @@ __global__ void __launch_bounds__(kThreads) qgemv_mma_kernel(const GemvParams p)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile = blockIdx.y;
   const int row0 = tile * kTileRows;
-  const int rows_valid = min(kTileRows, p.N - row0);
 
   // this CTA's super-block range [sb0, sb1)
   const int sb0 = (int)((int64_t)p.nsb * rank / ksplit);
@@ -47,18 +48,20 @@ __global__ void __launch_bounds__(kThreads) qgemv_mma_kernel(const GemvParams p)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < plan.nstage; ++s) {
-      mbar_init(&full[s], 32);                 // 32 loader lanes (+ tx bytes)
+      mbar_init(&full[s], 64);                 // 32 loader lanes x (copies landed, stores done)
       mbar_init(&empty[s], kConsumerWarps);    // one per consumer warp
     }
     if (ksplit > 1) mbar_init(red_full, (ksplit - 1) * kConsumerWarps * 32);
     fence_barrier_init();
   }
+  init_xinv(xinv, plan.nstage, p.x.dtype);
   if (ksplit > 1) cluster_sync_all();
   else __syncthreads();
 
   if (warp == 0) {
     // ------------------------------ loader ------------------------------
     const uint64_t pol = l2_evict_first_policy();
+    if (lane == 0) prefetch_tmap(&p.tmap);
     bool ok = true;
     for (int c = 0; c < nchunk && ok; ++c) {
       const int s = c % plan.nstage, round = c / plan.nstage;
@@ -66,20 +69,15 @@ __global__ void __launch_bounds__(kThreads) qgemv_mma_kernel(const GemvParams p)
       if (!ok) break;
       const int c0 = sb0 + c * L::C;
       const int ncs = min(L::C, sb1 - c0);
-      // byte range of each row: [a, b) rounded to 16 bytes (Q6_K blocks are
-      // 210 bytes; the row start itself is 16-byte aligned)
-      const int64_t a_raw = (int64_t)c0 * L::SBB, b_raw = (int64_t)(c0 + ncs) * L::SBB;
-      const int64_t a = a_raw & ~(int64_t)15, b = (b_raw + 15) & ~(int64_t)15;
-      const uint32_t bytes = (uint32_t)(b - a);
-      if (lane == 0) mbar_expect_tx(&full[s], bytes * rows_valid);
-      __syncwarp();
-      uint8_t* wst = wbuf + s * L::W_STAGE;
-      for (int r = lane; r < rows_valid; r += 32)
-        bulk_g2s(wst + r * L::ROW_PITCH, p.W + (int64_t)(row0 + r) * p.row_bytes + a, bytes,
-                 &full[s], pol);
-      convert_x_stage<FMT>(p.x, p.batch, (int64_t)c0 * 256, ncs,
-                           xbuf + s * p.batch * L::XCOL, xinv + s * 8, lane);
-      mbar_arrive(&full[s]);
+      // box start: the super-block's first byte rounded down to 16 bytes
+      // (Q6_K blocks are 210 bytes; row starts are 16-byte aligned)
+      const int64_t a = ((int64_t)c0 * L::SBB) & ~(int64_t)15;
+      if (lane == 0) {
+        mbar_expect_tx(&full[s], L::W_STAGE);   // rows past N are zero-filled, still counted
+        tma_load_2d(wbuf + s * L::W_STAGE, &p.tmap, (int)(a >> 1), row0, &full[s], pol);
+      }
+      stage_x<FMT>(p.x, p.batch, (int64_t)c0 * 256, ncs, xbuf + s * p.batch * L::XCOL,
+                   xinv + s * 8, lane, &full[s]);
     }
   } else {
     // ----------------------------- consumers -----------------------------
@@ -97,14 +95,14 @@ __global__ void __launch_bounds__(kThreads) qgemv_mma_kernel(const GemvParams p)
       const int delta = (int)(((int64_t)c0 * L::SBB) & 15);
       const uint32_t wst = smem_u32(wbuf + s * L::W_STAGE) + (16 * cw + g) * L::ROW_PITCH + delta;
       const uint32_t xcol = smem_u32(xbuf + (s * p.batch + (xon ? g : 0)) * L::XCOL);
-      float part[4] = {0.f, 0.f, 0.f, 0.f};
+      float part[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
       for (int j = 0; j < ncs; ++j)
         SBDot<FMT>::run(wst + j * L::SBB, 8 * L::ROW_PITCH, xcol, j * 256, t, xon, part);
       const float inv0 = xinv[s * 8 + ((2 * t) & 7)], inv1 = xinv[s * 8 + ((2 * t + 1) & 7)];
-      acc[0] = fmaf(part[0], inv0, acc[0]);
-      acc[1] = fmaf(part[1], inv1, acc[1]);
-      acc[2] = fmaf(part[2], inv0, acc[2]);
-      acc[3] = fmaf(part[3], inv1, acc[3]);
+      acc[0] = fmaf(part[0][0] + part[1][0], inv0, acc[0]);
+      acc[1] = fmaf(part[0][1] + part[1][1], inv1, acc[1]);
+      acc[2] = fmaf(part[0][2] + part[1][2], inv0, acc[2]);
+      acc[3] = fmaf(part[0][3] + part[1][3], inv1, acc[3]);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
@@ -187,6 +185,8 @@ int launch_qgemv_mma_fmt(const void* W, int64_t N, int64_t K, const void* x, int
   p.W = (const uint8_t*)W;
   p.nsb = (int)(K / 256);
   p.row_bytes = (int64_t)p.nsb * L::SBB;
+  if (!make_weight_tmap(&p.tmap, W, (uint64_t)N, (uint64_t)p.row_bytes, L::BOX, kTileRows))
+    return DQ_ERR_CUDA;
   p.N = (int)N;
   p.x.base = x;
   p.x.dtype = xdt;
@@ -200,7 +200,7 @@ int launch_qgemv_mma_fmt(const void* W, int64_t N, int64_t K, const void* x, int
   int ks = force_ksplit > 0 ? force_ksplit : choose_ksplit(tiles, p.nsb, 2 * sms);
   ks = std::max(1, std::min(ks, std::min(8, p.nsb)));
   // stages: as many as fit two CTAs per SM (<= 113 KB each), at least 3
-  int nstage = 6;
+  int nstage = 12;
   while (nstage > 3 && make_plan<FMT>(nstage, batch, ks).total > 113 * 1024) --nstage;
   p.nstage = nstage;
   const SmemPlan plan = make_plan<FMT>(nstage, batch, ks);

@@ -34,20 +34,22 @@ constexpr int kConsumerWarps = 4;
 constexpr int kTileRows = 16 * kConsumerWarps;   // 64
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
 
-// fp16 element offset of activation k inside a stage column: 4 halves of
-// padding after every 64 so that the 4 lanes of a quad hit distinct banks.
-__host__ __device__ constexpr int xoff(int k) { return k + 4 * (k >> 6); }
+// fp16 element offset of activation k inside a stage column: 8 halves (16 B)
+// of padding after every 64 so that the 4 lanes of a quad, which read 64
+// elements apart, hit distinct banks; 8-element runs stay 16-byte aligned.
+__host__ __device__ constexpr int xoff(int k) { return k + 8 * (k >> 6); }
 
 template <int FMT>
 struct Layout {
   static constexpr int SBB = Fmt<FMT>::SB_BYTES;
-  // super-blocks (256 weights) per pipeline stage per row: ~300 bytes per row
-  static constexpr int C = (FMT == DQ_Q4_K) ? 2 : 1;
-  // bytes reserved per weight row per stage (Q6_K stages start off 16 B).
-  static constexpr int ROW_RAW = C * SBB + (FMT == DQ_Q6_K ? 32 : 0);
-  static constexpr int ROW_A16 = (ROW_RAW + 15) / 16 * 16;
-  // pitch = 16 (mod 32) bytes: rows g and g+1 land on different bank halves
-  static constexpr int ROW_PITCH = (ROW_A16 % 32 == 16) ? ROW_A16 : ROW_A16 + 16;
+  // one super-block (256 weights) per row per pipeline stage
+  static constexpr int C = 1;
+  // bytes of a row's TMA box per stage: the super-block, for Q6_K a 16-byte
+  // aligned superset of its 210 bytes (starts up to 14 bytes early)
+  static constexpr int BOX = (FMT == DQ_Q4_K) ? 144 : (FMT == DQ_Q6_K) ? 240 : 272;
+  // TMA writes box rows densely: pitch = BOX; BOX/16 is odd for every format,
+  // so rows g and g+1 fall on different bank halves for 16-byte reads
+  static constexpr int ROW_PITCH = BOX;
   static constexpr int W_STAGE = kTileRows * ROW_PITCH;
   // activation column pitch: 32 (mod 128) bytes
   static constexpr int XCOL_RAW = xoff(C * 256) * 2;
@@ -67,7 +69,7 @@ __host__ __device__ inline SmemPlan make_plan(int nstage, int batch, int ksplit)
   p.batch = batch;
   p.ksplit = ksplit;
   p.off_bar = 0;                                       // full[ns], empty[ns], red
-  p.off_w = 1024;
+  p.off_w = 1024;                                      // 128-byte aligned TMA stages
   p.off_x = p.off_w + nstage * Layout<FMT>::W_STAGE;
   p.off_xinv = p.off_x + nstage * batch * Layout<FMT>::XCOL;
   p.off_red = p.off_xinv + nstage * 8 * 4;
@@ -132,54 +134,67 @@ __device__ __forceinline__ void pow2_scale(float amax, float& scale, float& inv)
   inv = __uint_as_float((uint32_t)(127 - se) << 23);
 }
 
-// Loader: convert columns of one stage (nsb_stage super-blocks starting at
-// activation index k0) into fp16 at xdst (column pitch XCOL bytes).
+// fp16 activations need no scale: every stage's column scale is 1.
+__device__ __forceinline__ void init_xinv(float* xinv, int nstage, int dtype) {
+  if (dtype == DQ_F16)
+    for (int i = threadIdx.x; i < nstage * 8; i += blockDim.x) xinv[i] = 1.f;
+}
+
+// Loader: stage the activation columns of one stage (nsb_stage super-blocks
+// starting at activation index k0) as fp16 at xdst (column pitch XCOL bytes)
+// and arrive on `full` for this lane twice: once asynchronously when all of
+// the lane's cp.async copies of the stage (weights and fp16 activations) have
+// landed, once after its own shared-memory stores.  fp16 input is copied
+// asynchronously; bf16 / fp32 input is converted with a per-column
+// power-of-two scale.
 template <int FMT>
-__device__ __forceinline__ void convert_x_stage(const XSrc& xs, int ncols, int64_t k0, int nsb_stage,
-                                                uint8_t* xdst, float* xinv, int lane) {
-  for (int c = 0; c < ncols; ++c) {
-    uint8_t* col = xdst + c * Layout<FMT>::XCOL;
-    if (xs.dtype == DQ_F16) {
-      const int64_t rowoff = xrow(xs, c) * xs.col_stride;
+__device__ __forceinline__ void stage_x(const XSrc& xs, int ncols, int64_t k0, int nsb_stage,
+                                        uint8_t* xdst, float* xinv, int lane, uint64_t* full) {
+  if (xs.dtype == DQ_F16) {
+    for (int c = 0; c < ncols; ++c) {
+      uint8_t* col = xdst + c * Layout<FMT>::XCOL;
+      const uint16_t* src = (const uint16_t*)xs.base + xrow(xs, c) * xs.col_stride + k0;
       for (int j = 0; j < nsb_stage; ++j) {
         const int k = j * 256 + 8 * lane;
-        const uint4 u = __ldg((const uint4*)((const uint16_t*)xs.base + rowoff + k0 + k));
-        uint2* d = (uint2*)(col + 2 * xoff(k));
-        d[0] = make_uint2(u.x, u.y);
-        d[1] = make_uint2(u.z, u.w);
+        cp_async16(col + 2 * xoff(k), src + k);
       }
-      if (lane == 0) xinv[c] = 1.f;
-    } else {
-      constexpr int C = Layout<FMT>::C;
-      float v[C][8];
-      float amax = 0.f;
-#pragma unroll
-      for (int j = 0; j < C; ++j) {
-        if (j < nsb_stage) {
-          load8_f32(xs, c, k0 + j * 256 + 8 * lane, v[j]);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[j][i]));
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      float sc, inv;
-      pow2_scale(amax, sc, inv);
-#pragma unroll
-      for (int j = 0; j < C; ++j) {
-        if (j < nsb_stage) {
-          uint32_t h[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            h[i] = h2_as_u32(__floats2half2_rn(v[j][2 * i] * sc, v[j][2 * i + 1] * sc));
-          uint2* d = (uint2*)(col + 2 * xoff(j * 256 + 8 * lane));
-          d[0] = make_uint2(h[0], h[1]);
-          d[1] = make_uint2(h[2], h[3]);
-        }
-      }
-      if (lane == 0) xinv[c] = inv;
     }
+    // xinv stays 1 for fp16 input: set once per CTA before the pipeline starts
+    cp_async_arrive_noinc(full);
+    mbar_arrive(full);
+    return;
   }
+  for (int c = 0; c < ncols; ++c) {
+    uint8_t* col = xdst + c * Layout<FMT>::XCOL;
+    constexpr int C = Layout<FMT>::C;
+    float v[C][8];
+    float amax = 0.f;
+#pragma unroll
+    for (int j = 0; j < C; ++j) {
+      if (j < nsb_stage) {
+        load8_f32(xs, c, k0 + j * 256 + 8 * lane, v[j]);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[j][i]));
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    float sc, inv;
+    pow2_scale(amax, sc, inv);
+#pragma unroll
+    for (int j = 0; j < C; ++j) {
+      if (j < nsb_stage) {
+        uint32_t h[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          h[i] = h2_as_u32(__floats2half2_rn(v[j][2 * i] * sc, v[j][2 * i + 1] * sc));
+        *(uint4*)(col + 2 * xoff(j * 256 + 8 * lane)) = make_uint4(h[0], h[1], h[2], h[3]);
+      }
+    }
+    if (lane == 0) xinv[c] = inv;
+  }
+  cp_async_arrive_noinc(full);
+  mbar_arrive(full);
 }
 
 // ---------------------------------------------------------------------------
@@ -235,7 +250,7 @@ struct SBDot<DQ_Q4_K> {
   }
 
   __device__ __forceinline__ static void run(uint32_t wrow, int pitch8, uint32_t xcol, int kb,
-                                             int t, bool xon, float (&acc)[4]) {
+                                             int t, bool xon, float (&acc)[2][4]) {
     const uint32_t r0 = wrow, r8 = wrow + pitch8;
     const uint4 h0 = lds_u128(r0), h8 = lds_u128(r8);
     __half2 s0l, o0l, s0h, o0h, s8l, o8l, s8h, o8h;
@@ -260,7 +275,7 @@ struct SBDot<DQ_Q4_K> {
         const uint32_t a1 = h2_as_u32(__hfma2(__hsub2(u32_as_h2(lop3_and_or(p8, 0x000F000Fu, 0x64006400u)), magic), s8l, o8l));
         const uint32_t a2 = h2_as_u32(__hfma2(__hsub2(u32_as_h2(lop3_and_or(p0s, 0x000F000Fu, 0x64006400u)), magic), s0l, o0l));
         const uint32_t a3 = h2_as_u32(__hfma2(__hsub2(u32_as_h2(lop3_and_or(p8s, 0x000F000Fu, 0x64006400u)), magic), s8l, o8l));
-        mma_16816(acc, a0, a1, a2, a3, b0, b1);
+        mma_16816(acc[0], a0, a1, a2, a3, b0, b1);
       }
       // high nibbles: weights k+32..k+35 (sub-block 2t+1), value 16*q
       ldx(xcol, k + 32, xon, b0, b1);
@@ -269,7 +284,7 @@ struct SBDot<DQ_Q4_K> {
         const uint32_t a1 = h2_as_u32(__hfma2(__hsub2(u32_as_h2(lop3_and_or(p8, 0x00F000F0u, 0x64006400u)), magic), s8h, o8h));
         const uint32_t a2 = h2_as_u32(__hfma2(__hsub2(u32_as_h2(lop3_and_or(p0s, 0x00F000F0u, 0x64006400u)), magic), s0h, o0h));
         const uint32_t a3 = h2_as_u32(__hfma2(__hsub2(u32_as_h2(lop3_and_or(p8s, 0x00F000F0u, 0x64006400u)), magic), s8h, o8h));
-        mma_16816(acc, a0, a1, a2, a3, b0, b1);
+        mma_16816(acc[1], a0, a1, a2, a3, b0, b1);
       }
     }
   }
@@ -288,7 +303,7 @@ struct SBDot<DQ_Q6_K> {
   }
 
   __device__ __forceinline__ static void run(uint32_t wrow, int pitch8, uint32_t xcol, int kb,
-                                             int t, bool xon, float (&acc)[4]) {
+                                             int t, bool xon, float (&acc)[2][4]) {
     const uint32_t rows[2] = {wrow, wrow + pitch8};
     // d and this lane's 8 scales per row: sc[8h + 2r + t/2], h = 0..1, r = 0..3
     __half2 scl[2][8];
@@ -342,7 +357,7 @@ struct SBDot<DQ_Q6_K> {
           }
           uint32_t b0, b1;
           ldx(xcol, kbase + 32 * r, xon, b0, b1);
-          mma_16816(acc, a[0], a[1], a[2], a[3], b0, b1);
+          mma_16816(acc[r & 1], a[0], a[1], a[2], a[3], b0, b1);
         }
       }
     }
@@ -354,7 +369,7 @@ struct SBDot<DQ_Q6_K> {
 template <>
 struct SBDot<DQ_Q8_0> {
   __device__ __forceinline__ static void run(uint32_t wrow, int pitch8, uint32_t xcol, int kb,
-                                             int t, bool xon, float (&acc)[4]) {
+                                             int t, bool xon, float (&acc)[2][4]) {
     const __half2 bias = __float2half2_rn(1152.f);   // 1024 + 128
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
@@ -376,9 +391,9 @@ struct SBDot<DQ_Q8_0> {
       }
       uint32_t b0, b1;
       ldx(xcol, kb + 32 * s + 8 * t, xon, b0, b1);
-      mma_16816(acc, a[0][0], a[0][1], a[0][2], a[0][3], b0, b1);
+      mma_16816(acc[0], a[0][0], a[0][1], a[0][2], a[0][3], b0, b1);
       ldx(xcol, kb + 32 * s + 8 * t + 4, xon, b0, b1);
-      mma_16816(acc, a[1][0], a[1][1], a[1][2], a[1][3], b0, b1);
+      mma_16816(acc[1], a[1][0], a[1][1], a[1][2], a[1][3], b0, b1);
     }
   }
 };
