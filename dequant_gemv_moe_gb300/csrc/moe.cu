@@ -383,7 +383,8 @@ __global__ void __launch_bounds__(kThreads) grouped_kernel(const __grid_constant
       const int4 grp = __ldg(p.groups + u / p.tiles);
       const int tile = u % p.tiles;
       const int ncols = grp.z;
-      const bool xon = g < ncols;
+      const int xc = g < ncols ? g : 0;      // this lane's activation column
+      const bool f16 = p.xdt == DQ_F16;      // fp16 input carries no scale
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
       for (int c = 0; c < nchunk; ++c, ++gc) {
         const int s = gc % plan.nstage, round = gc / plan.nstage;
@@ -396,15 +397,19 @@ __global__ void __launch_bounds__(kThreads) grouped_kernel(const __grid_constant
         const int delta = (int)(((int64_t)c0 * L::SBB) & 15);
         const uint32_t wst =
             smem_u32(wbuf + s * L::W_STAGE) + (16 * cw + g) * L::ROW_PITCH + delta;
-        const uint32_t xcol = smem_u32(xbuf + (s * 8 + (xon ? g : 0)) * L::XCOL);
+        const uint32_t xcol = smem_u32(xbuf + (s * 8 + xc) * L::XCOL);
         float part[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         for (int j = 0; j < ncs; ++j)
-          SBDot<FMT>::run(wst + j * L::SBB, 8 * L::ROW_PITCH, xcol, j * 256, t, xon, part);
-        const float inv0 = xinv[s * 8 + 2 * t], inv1 = xinv[s * 8 + 2 * t + 1];
-        acc[0] = fmaf(part[0][0] + part[1][0], inv0, acc[0]);
-        acc[1] = fmaf(part[0][1] + part[1][1], inv1, acc[1]);
-        acc[2] = fmaf(part[0][2] + part[1][2], inv0, acc[2]);
-        acc[3] = fmaf(part[0][3] + part[1][3], inv1, acc[3]);
+          SBDot<FMT>::run(wst + j * L::SBB, 8 * L::ROW_PITCH, xcol, j * 256, t, part);
+        if (f16) {
+          for (int i = 0; i < 4; ++i) acc[i] += part[0][i] + part[1][i];
+        } else {
+          const float inv0 = xinv[s * 8 + 2 * t], inv1 = xinv[s * 8 + 2 * t + 1];
+          acc[0] = fmaf(part[0][0] + part[1][0], inv0, acc[0]);
+          acc[1] = fmaf(part[0][1] + part[1][1], inv1, acc[1]);
+          acc[2] = fmaf(part[0][2] + part[1][2], inv0, acc[2]);
+          acc[3] = fmaf(part[0][3] + part[1][3], inv1, acc[3]);
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
       }
@@ -509,7 +514,7 @@ int launch_grouped(const GroupedParams& gp_in, int units_max, cudaStream_t s, in
       return DQ_ERR_CUDA;
   }
   int nstage = 12;
-  while (nstage > 3 && make_plan<FMT>(nstage, 8, 1).total + 2048 > 113 * 1024) --nstage;
+  while (nstage > 3 && make_plan<FMT>(nstage, 8, 1).total + 2048 > 56 * 1024) --nstage;
   gp.nstage = nstage;
   const int smem = make_plan<FMT>(nstage, 8, 1).total + 2048;
   static bool attr[64] = {false};
@@ -523,7 +528,11 @@ int launch_grouped(const GroupedParams& gp_in, int units_max, cudaStream_t s, in
   }
   const int sms = sm_count();
   if (sms <= 0) return DQ_ERR_CUDA;
-  const int grid = std::max(1, std::min(units_max, 2 * sms));
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, grouped_kernel<FMT, GATEUP>, kThreads,
+                                                    smem) != cudaSuccess || occ < 1)
+    occ = 1;
+  const int grid = std::max(1, std::min(units_max, occ * sms));
   grouped_kernel<FMT, GATEUP><<<grid, kThreads, smem, s>>>(gp);
   return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
 }

@@ -83,7 +83,8 @@ __global__ void __launch_bounds__(kThreads) qgemv_mma_kernel(const __grid_consta
     // ----------------------------- consumers -----------------------------
     const int cw = warp - 1;
     const int g = lane >> 2, t = lane & 3;
-    const bool xon = g < p.batch;
+    const int xc = g < p.batch ? g : 0;      // this lane's activation column
+    const bool f16 = p.x.dtype == DQ_F16;    // fp16 input carries no scale
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     bool ok = true;
     for (int c = 0; c < nchunk; ++c) {
@@ -94,15 +95,19 @@ __global__ void __launch_bounds__(kThreads) qgemv_mma_kernel(const __grid_consta
       const int ncs = min(L::C, sb1 - c0);
       const int delta = (int)(((int64_t)c0 * L::SBB) & 15);
       const uint32_t wst = smem_u32(wbuf + s * L::W_STAGE) + (16 * cw + g) * L::ROW_PITCH + delta;
-      const uint32_t xcol = smem_u32(xbuf + (s * p.batch + (xon ? g : 0)) * L::XCOL);
+      const uint32_t xcol = smem_u32(xbuf + (s * p.batch + xc) * L::XCOL);
       float part[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
       for (int j = 0; j < ncs; ++j)
-        SBDot<FMT>::run(wst + j * L::SBB, 8 * L::ROW_PITCH, xcol, j * 256, t, xon, part);
-      const float inv0 = xinv[s * 8 + ((2 * t) & 7)], inv1 = xinv[s * 8 + ((2 * t + 1) & 7)];
-      acc[0] = fmaf(part[0][0] + part[1][0], inv0, acc[0]);
-      acc[1] = fmaf(part[0][1] + part[1][1], inv1, acc[1]);
-      acc[2] = fmaf(part[0][2] + part[1][2], inv0, acc[2]);
-      acc[3] = fmaf(part[0][3] + part[1][3], inv1, acc[3]);
+        SBDot<FMT>::run(wst + j * L::SBB, 8 * L::ROW_PITCH, xcol, j * 256, t, part);
+      if (f16) {
+        for (int i = 0; i < 4; ++i) acc[i] += part[0][i] + part[1][i];
+      } else {
+        const float inv0 = xinv[s * 8 + ((2 * t) & 7)], inv1 = xinv[s * 8 + ((2 * t + 1) & 7)];
+        acc[0] = fmaf(part[0][0] + part[1][0], inv0, acc[0]);
+        acc[1] = fmaf(part[0][1] + part[1][1], inv1, acc[1]);
+        acc[2] = fmaf(part[0][2] + part[1][2], inv0, acc[2]);
+        acc[3] = fmaf(part[0][3] + part[1][3], inv1, acc[3]);
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
@@ -197,11 +202,12 @@ int launch_qgemv_mma_fmt(const void* W, int64_t N, int64_t K, const void* x, int
   const int tiles = (int)((N + kTileRows - 1) / kTileRows);
   const int sms = device_sms();
   if (sms <= 0) return DQ_ERR_CUDA;
-  int ks = force_ksplit > 0 ? force_ksplit : choose_ksplit(tiles, p.nsb, 2 * sms);
+  // shared memory per CTA <= 56 KB so that four CTAs (20 warps) share an SM
+  constexpr int kSmemBudget = 56 * 1024;
+  int ks = force_ksplit > 0 ? force_ksplit : choose_ksplit(tiles, p.nsb, 4 * sms);
   ks = std::max(1, std::min(ks, std::min(8, p.nsb)));
-  // stages: as many as fit two CTAs per SM (<= 113 KB each), at least 3
   int nstage = 12;
-  while (nstage > 3 && make_plan<FMT>(nstage, batch, ks).total > 113 * 1024) --nstage;
+  while (nstage > 3 && make_plan<FMT>(nstage, batch, ks).total > kSmemBudget) --nstage;
   p.nstage = nstage;
   const SmemPlan plan = make_plan<FMT>(nstage, batch, ks);
   static bool attr_set[64] = {false};

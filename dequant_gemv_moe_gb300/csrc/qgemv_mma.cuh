@@ -200,18 +200,17 @@ __device__ __forceinline__ void stage_x(const XSrc& xs, int ncols, int64_t k0, i
 // ---------------------------------------------------------------------------
 // Consumer: one super-block of 16 rows (rows g, g+8 of lane) x 256 weights.
 // wrow: shared address of row g's super-block; pitch: bytes to row g+8.
-// xcol: shared address of this lane's activation column, at the stage start;
+// xcol: shared address of this lane's activation column, at the stage start
+// (column 0 for lanes past the batch);
 // kb: k offset of the super-block inside the stage (j*256).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void ldx(uint32_t xcol, int k, bool on, uint32_t& b0, uint32_t& b1) {
-  if (on) {
-    const uint2 v = lds_u64(xcol + 2 * xoff(k));
-    b0 = v.x;
-    b1 = v.y;
-  } else {
-    b0 = 0u;
-    b1 = 0u;
-  }
+// B fragment (k, k+1 | k+2, k+3) of this lane's activation column.  Lanes
+// whose column is past the batch read column 0: their output column is never
+// stored, and an mma output column depends only on its own B column.
+__device__ __forceinline__ void ldx(uint32_t xcol, int k, uint32_t& b0, uint32_t& b1) {
+  const uint2 v = lds_u64(xcol + 2 * xoff(k));
+  b0 = v.x;
+  b1 = v.y;
 }
 
 template <int FMT>
@@ -250,7 +249,7 @@ struct SBDot<DQ_Q4_K> {
   }
 
   __device__ __forceinline__ static void run(uint32_t wrow, int pitch8, uint32_t xcol, int kb,
-                                             int t, bool xon, float (&acc)[2][4]) {
+                                             int t, float (&acc)[2][4]) {
     const uint32_t r0 = wrow, r8 = wrow + pitch8;
     const uint4 h0 = lds_u128(r0), h8 = lds_u128(r8);
     __half2 s0l, o0l, s0h, o0h, s8l, o8l, s8h, o8h;
@@ -269,7 +268,7 @@ struct SBDot<DQ_Q4_K> {
       const int k = kb + 64 * t + 4 * s;
       uint32_t b0, b1;
       // low nibbles: weights k..k+3 (sub-block 2t)
-      ldx(xcol, k, xon, b0, b1);
+      ldx(xcol, k, b0, b1);
       {
         const uint32_t a0 = h2_as_u32(__hfma2(__hsub2(u32_as_h2(lop3_and_or(p0, 0x000F000Fu, 0x64006400u)), magic), s0l, o0l));
         const uint32_t a1 = h2_as_u32(__hfma2(__hsub2(u32_as_h2(lop3_and_or(p8, 0x000F000Fu, 0x64006400u)), magic), s8l, o8l));
@@ -278,7 +277,7 @@ struct SBDot<DQ_Q4_K> {
         mma_16816(acc[0], a0, a1, a2, a3, b0, b1);
       }
       // high nibbles: weights k+32..k+35 (sub-block 2t+1), value 16*q
-      ldx(xcol, k + 32, xon, b0, b1);
+      ldx(xcol, k + 32, b0, b1);
       {
         const uint32_t a0 = h2_as_u32(__hfma2(__hsub2(u32_as_h2(lop3_and_or(p0, 0x00F000F0u, 0x64006400u)), magic), s0h, o0h));
         const uint32_t a1 = h2_as_u32(__hfma2(__hsub2(u32_as_h2(lop3_and_or(p8, 0x00F000F0u, 0x64006400u)), magic), s8h, o8h));
@@ -303,7 +302,7 @@ struct SBDot<DQ_Q6_K> {
   }
 
   __device__ __forceinline__ static void run(uint32_t wrow, int pitch8, uint32_t xcol, int kb,
-                                             int t, bool xon, float (&acc)[2][4]) {
+                                             int t, float (&acc)[2][4]) {
     const uint32_t rows[2] = {wrow, wrow + pitch8};
     // d and this lane's 8 scales per row: sc[8h + 2r + t/2], h = 0..1, r = 0..3
     __half2 scl[2][8];
@@ -356,7 +355,7 @@ struct SBDot<DQ_Q6_K> {
             a[2 + rr] = h2_as_u32(__hmul2(u32_as_h2(q6_pair(nhi, hhi)), sc));
           }
           uint32_t b0, b1;
-          ldx(xcol, kbase + 32 * r, xon, b0, b1);
+          ldx(xcol, kbase + 32 * r, b0, b1);
           mma_16816(acc[r & 1], a[0], a[1], a[2], a[3], b0, b1);
         }
       }
@@ -369,7 +368,7 @@ struct SBDot<DQ_Q6_K> {
 template <>
 struct SBDot<DQ_Q8_0> {
   __device__ __forceinline__ static void run(uint32_t wrow, int pitch8, uint32_t xcol, int kb,
-                                             int t, bool xon, float (&acc)[2][4]) {
+                                             int t, float (&acc)[2][4]) {
     const __half2 bias = __float2half2_rn(1152.f);   // 1024 + 128
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
@@ -390,9 +389,9 @@ struct SBDot<DQ_Q8_0> {
         }
       }
       uint32_t b0, b1;
-      ldx(xcol, kb + 32 * s + 8 * t, xon, b0, b1);
+      ldx(xcol, kb + 32 * s + 8 * t, b0, b1);
       mma_16816(acc[0], a[0][0], a[0][1], a[0][2], a[0][3], b0, b1);
-      ldx(xcol, kb + 32 * s + 8 * t + 4, xon, b0, b1);
+      ldx(xcol, kb + 32 * s + 8 * t + 4, b0, b1);
       mma_16816(acc[1], a[1][0], a[1][1], a[1][2], a[1][3], b0, b1);
     }
   }
