@@ -36,7 +36,13 @@ MoePlan moe_plan(const dq_moe_desc& d, int T) {
   p.KS = std::max(1, std::min(d.hidden / 256, (320 + tiles - 1) / tiles));
   p.P = (int64_t)T * d.top_k;
   p.NP = p.P + (int64_t)d.n_shared * T;
-  p.G_max = (int)((p.P + 7) / 8 + std::min<int64_t>(d.E, p.P) + (int64_t)d.n_shared * ((T + 7) / 8));
+  // group width from the expected tokens per routed expert (uniform routing):
+  // wider groups stream an expert's weights once for more tokens
+  const double per_expert = (double)p.P / d.E;
+  p.NT = per_expert <= 6.0 ? 1 : per_expert <= 14.0 ? 2 : 4;
+  p.GW = 8 * p.NT;
+  p.G_max = (int)((p.P + p.GW - 1) / p.GW + std::min<int64_t>(d.E, p.P) +
+                  (int64_t)d.n_shared * ((T + p.GW - 1) / p.GW));
   size_t o = 0;
   p.off_part = o;    o = align256(o + (size_t)p.KS * T * d.E * 4);
   p.off_logits = o;  o = align256(o + (size_t)T * d.E * 4);
@@ -184,7 +190,7 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ par
 // 3. stable permute + work groups: one CTA of 1024 threads
 // ===========================================================================
 __global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict__ idx, int T,
-                                                       int k, int E, int n_shared,
+                                                       int k, int E, int n_shared, int gw,
                                                        int32_t* __restrict__ offsets,
                                                        int32_t* __restrict__ sorted,
                                                        int32_t* __restrict__ inv,
@@ -248,8 +254,8 @@ __global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict
   if (!groups) return;
   // shared-expert positions follow the routed ones: P + s*T + t
   for (int i = tid; i < n_shared * T; i += 1024) tok[P + i] = i % T;
-  // groups of <= 8 columns per expert, experts in order, then shared experts
-  if (tid < 256) gsc[tid + 1] = (tid < E) ? (cnt[tid] + 7) / 8 : 0;
+  // groups of <= gw columns per expert, experts in order, then shared experts
+  if (tid < 256) gsc[tid + 1] = (tid < E) ? (cnt[tid] + gw - 1) / gw : 0;
   if (tid == 0) gsc[0] = 0;
   __syncthreads();
   for (int d = 1; d < 256; d <<= 1) {
@@ -261,14 +267,14 @@ __global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict
   }
   if (tid < E) {
     const int n = cnt[tid];
-    for (int j = 0; j * 8 < n; ++j)
-      groups[gsc[tid] + j] = make_int4(tid, off[tid] + 8 * j, min(8, n - 8 * j), 0);
+    for (int j = 0; j * gw < n; ++j)
+      groups[gsc[tid] + j] = make_int4(tid, off[tid] + gw * j, min(gw, n - gw * j), 0);
   }
   const int nr = gsc[E];
-  const int per = (T + 7) / 8;
+  const int per = (T + gw - 1) / gw;
   for (int i = tid; i < n_shared * per; i += 1024) {
     const int s = i / per, j = i % per;
-    groups[nr + i] = make_int4(E + s, P + s * T + 8 * j, min(8, T - 8 * j), 0);
+    groups[nr + i] = make_int4(E + s, P + s * T + gw * j, min(gw, T - gw * j), 0);
   }
   if (tid == 0) *n_groups = nr + n_shared * per;
 }
@@ -302,17 +308,19 @@ struct GroupedParams {
   int nstage;
 };
 
-template <int FMT, bool GATEUP>
+// NT: activation tiles of 8 columns per unit (groups hold <= 8*NT columns).
+template <int FMT, bool GATEUP, int NT>
 __global__ void __launch_bounds__(kThreads) grouped_kernel(const __grid_constant__ GroupedParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   using L = Layout<FMT>;
-  const SmemPlan plan = make_plan<FMT>(p.nstage, 8, 1);
+  constexpr int NC = 8 * NT;
+  const SmemPlan plan = make_plan<FMT>(p.nstage, NC, 1);
   uint64_t* full = (uint64_t*)(smem + plan.off_bar);
   uint64_t* empty = full + plan.nstage;
   uint8_t* wbuf = smem + plan.off_w;
   uint8_t* xbuf = smem + plan.off_x;
   float* xinv = (float*)(smem + plan.off_xinv);
-  float* ex = (float*)(smem + plan.off_red);   // [64][8] gate/up exchange
+  float* ex = (float*)(smem + plan.off_red);   // [64][NC] gate/up exchange
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_units = __ldg(p.n_groups) * p.tiles;
@@ -325,7 +333,7 @@ __global__ void __launch_bounds__(kThreads) grouped_kernel(const __grid_constant
     }
     fence_barrier_init();
   }
-  init_xinv(xinv, plan.nstage, p.xdt);
+  init_xinv(xinv, plan.nstage * NC, p.xdt);
   __syncthreads();
 
   if (warp == 0) {
@@ -369,7 +377,7 @@ __global__ void __launch_bounds__(kThreads) grouped_kernel(const __grid_constant
             tma_load_2d(wst, ma, (int)(a >> 1), grow, &full[s], pol);
           }
         }
-        stage_x<FMT>(xs, grp.z, (int64_t)c0 * 256, ncs, xbuf + s * 8 * L::XCOL, xinv + s * 8,
+        stage_x<FMT>(xs, grp.z, (int64_t)c0 * 256, ncs, xbuf + s * NC * L::XCOL, xinv + s * NC,
                      lane, &full[s]);
       }
     }
@@ -383,9 +391,8 @@ __global__ void __launch_bounds__(kThreads) grouped_kernel(const __grid_constant
       const int4 grp = __ldg(p.groups + u / p.tiles);
       const int tile = u % p.tiles;
       const int ncols = grp.z;
-      const int xc = g < ncols ? g : 0;      // this lane's activation column
       const bool f16 = p.xdt == DQ_F16;      // fp16 input carries no scale
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      float acc[NT][4] = {};
       for (int c = 0; c < nchunk; ++c, ++gc) {
         const int s = gc % plan.nstage, round = gc / plan.nstage;
         // after a timed-out wait the warp keeps walking the same units (no
@@ -397,46 +404,64 @@ __global__ void __launch_bounds__(kThreads) grouped_kernel(const __grid_constant
         const int delta = (int)(((int64_t)c0 * L::SBB) & 15);
         const uint32_t wst =
             smem_u32(wbuf + s * L::W_STAGE) + (16 * cw + g) * L::ROW_PITCH + delta;
-        const uint32_t xcol = smem_u32(xbuf + (s * 8 + xc) * L::XCOL);
-        float part[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        // this lane's activation column in each 8-column tile (column 0 past the group)
+        uint32_t xcol[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const int col = 8 * nt + g;
+          xcol[nt] = smem_u32(xbuf + (s * NC + (col < ncols ? col : 0)) * L::XCOL);
+        }
+        float part[NT][2][4] = {};
         for (int j = 0; j < ncs; ++j)
-          SBDot<FMT>::run(wst + j * L::SBB, 8 * L::ROW_PITCH, xcol, j * 256, t, part);
-        if (f16) {
-          for (int i = 0; i < 4; ++i) acc[i] += part[0][i] + part[1][i];
-        } else {
-          const float inv0 = xinv[s * 8 + 2 * t], inv1 = xinv[s * 8 + 2 * t + 1];
-          acc[0] = fmaf(part[0][0] + part[1][0], inv0, acc[0]);
-          acc[1] = fmaf(part[0][1] + part[1][1], inv1, acc[1]);
-          acc[2] = fmaf(part[0][2] + part[1][2], inv0, acc[2]);
-          acc[3] = fmaf(part[0][3] + part[1][3], inv1, acc[3]);
+          SBDot<FMT>::template run<NT>(wst + j * L::SBB, 8 * L::ROW_PITCH, xcol, j * 256, t, part);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          if (f16) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[nt][i] += part[nt][0][i] + part[nt][1][i];
+          } else {
+            const float inv0 = xinv[s * NC + 8 * nt + 2 * t];
+            const float inv1 = xinv[s * NC + 8 * nt + 2 * t + 1];
+            acc[nt][0] = fmaf(part[nt][0][0] + part[nt][1][0], inv0, acc[nt][0]);
+            acc[nt][1] = fmaf(part[nt][0][1] + part[nt][1][1], inv1, acc[nt][1]);
+            acc[nt][2] = fmaf(part[nt][0][2] + part[nt][1][2], inv0, acc[nt][2]);
+            acc[nt][3] = fmaf(part[nt][0][3] + part[nt][1][3], inv1, acc[nt][3]);
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
       }
-      const int c0 = 2 * t, c1 = 2 * t + 1;
       if (!GATEUP) {
         const int ra = tile * 64 + 16 * cw + g, rb = ra + 8;
         float* o = p.out + (int64_t)grp.y * p.out_stride;
-        if (c0 < ncols) {
-          o[(int64_t)c0 * p.out_stride + ra] = acc[0];
-          o[(int64_t)c0 * p.out_stride + rb] = acc[2];
-        }
-        if (c1 < ncols) {
-          o[(int64_t)c1 * p.out_stride + ra] = acc[1];
-          o[(int64_t)c1 * p.out_stride + rb] = acc[3];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const int c0 = 8 * nt + 2 * t, c1 = c0 + 1;
+          if (c0 < ncols) {
+            o[(int64_t)c0 * p.out_stride + ra] = acc[nt][0];
+            o[(int64_t)c0 * p.out_stride + rb] = acc[nt][2];
+          }
+          if (c1 < ncols) {
+            o[(int64_t)c1 * p.out_stride + ra] = acc[nt][1];
+            o[(int64_t)c1 * p.out_stride + rb] = acc[nt][3];
+          }
         }
       } else {
         // rows 0..31 hold gate, rows 32..63 the matching up rows
         const int ra = 16 * cw + g, rb = ra + 8;
-        ex[ra * 8 + c0] = acc[0];
-        ex[ra * 8 + c1] = acc[1];
-        ex[rb * 8 + c0] = acc[2];
-        ex[rb * 8 + c1] = acc[3];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const int c0 = 8 * nt + 2 * t, c1 = c0 + 1;
+          ex[ra * NC + c0] = acc[nt][0];
+          ex[ra * NC + c1] = acc[nt][1];
+          ex[rb * NC + c0] = acc[nt][2];
+          ex[rb * NC + c1] = acc[nt][3];
+        }
         asm volatile("bar.sync 1, 128;" ::: "memory");
         const int ct = threadIdx.x - 32;
         for (int i = ct; i < 32 * ncols; i += 128) {
           const int r = i & 31, col = i >> 5;
-          const float gv = ex[r * 8 + col], uv = ex[(32 + r) * 8 + col];
+          const float gv = ex[r * NC + col], uv = ex[(32 + r) * NC + col];
           // silu(g) = g / (1 + exp(-g)); for g < -88 exp overflows to inf and
           // the quotient is -0, never NaN
           const float h = gv / (1.f + expf(-gv)) * uv;
@@ -498,7 +523,7 @@ int sm_count() {
 int qk(int fmt) { return fmt == DQ_Q8_0 ? 32 : 256; }
 int blk_bytes(int fmt) { return fmt == DQ_Q4_K ? 144 : fmt == DQ_Q6_K ? 210 : 34; }
 
-template <int FMT, bool GATEUP>
+template <int FMT, bool GATEUP, int NT>
 int launch_grouped(const GroupedParams& gp_in, int units_max, cudaStream_t s, int E, int n_shared) {
   using L = Layout<FMT>;
   GroupedParams gp = gp_in;
@@ -513,15 +538,16 @@ int launch_grouped(const GroupedParams& gp_in, int units_max, cudaStream_t s, in
     if (GATEUP && !make_weight_tmap(&gp.map_sb, gp.Sb, rpe * n_shared, gp.row_bytes, L::BOX, box_rows))
       return DQ_ERR_CUDA;
   }
+  const int ex_bytes = 64 * 8 * NT * 4;
   int nstage = 12;
-  while (nstage > 3 && make_plan<FMT>(nstage, 8, 1).total + 2048 > 56 * 1024) --nstage;
+  while (nstage > 3 && make_plan<FMT>(nstage, 8 * NT, 1).total + ex_bytes > 56 * 1024) --nstage;
   gp.nstage = nstage;
-  const int smem = make_plan<FMT>(nstage, 8, 1).total + 2048;
+  const int smem = make_plan<FMT>(nstage, 8 * NT, 1).total + ex_bytes;
   static bool attr[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 64 || !attr[dev]) {
-    if (cudaFuncSetAttribute(grouped_kernel<FMT, GATEUP>,
+    if (cudaFuncSetAttribute(grouped_kernel<FMT, GATEUP, NT>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) != cudaSuccess)
       return DQ_ERR_CUDA;
     if (dev < 64) attr[dev] = true;
@@ -529,20 +555,24 @@ int launch_grouped(const GroupedParams& gp_in, int units_max, cudaStream_t s, in
   const int sms = sm_count();
   if (sms <= 0) return DQ_ERR_CUDA;
   int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, grouped_kernel<FMT, GATEUP>, kThreads,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, grouped_kernel<FMT, GATEUP, NT>, kThreads,
                                                     smem) != cudaSuccess || occ < 1)
     occ = 1;
   const int grid = std::max(1, std::min(units_max, occ * sms));
-  grouped_kernel<FMT, GATEUP><<<grid, kThreads, smem, s>>>(gp);
+  grouped_kernel<FMT, GATEUP, NT><<<grid, kThreads, smem, s>>>(gp);
   return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
 }
 
 template <bool GATEUP>
-int launch_grouped_fmt(int fmt, const GroupedParams& gp, int units_max, cudaStream_t s, int E,
-                       int n_shared) {
-  if (fmt == DQ_Q4_K) return launch_grouped<DQ_Q4_K, GATEUP>(gp, units_max, s, E, n_shared);
-  if (fmt == DQ_Q6_K) return launch_grouped<DQ_Q6_K, GATEUP>(gp, units_max, s, E, n_shared);
-  return launch_grouped<DQ_Q8_0, GATEUP>(gp, units_max, s, E, n_shared);
+int launch_grouped_fmt(int fmt, int nt, const GroupedParams& gp, int units_max, cudaStream_t s,
+                       int E, int n_shared) {
+#define DQ_GROUPED(F, N) \
+  if (fmt == F && nt == N) return launch_grouped<F, GATEUP, N>(gp, units_max, s, E, n_shared);
+  DQ_GROUPED(DQ_Q4_K, 1) DQ_GROUPED(DQ_Q4_K, 2) DQ_GROUPED(DQ_Q4_K, 4)
+  DQ_GROUPED(DQ_Q6_K, 1) DQ_GROUPED(DQ_Q6_K, 2) DQ_GROUPED(DQ_Q6_K, 4)
+  DQ_GROUPED(DQ_Q8_0, 1) DQ_GROUPED(DQ_Q8_0, 2) DQ_GROUPED(DQ_Q8_0, 4)
+#undef DQ_GROUPED
+  return DQ_ERR_UNSUPPORTED;
 }
 
 }  // namespace
@@ -558,8 +588,8 @@ int launch_router(const float* Wr, int E, int H, const void* x, int xdt, int T, 
 
 int launch_permute(const int32_t* idx, int T, int k, int E, int32_t* offsets, int32_t* sorted,
                    cudaStream_t s) {
-  permute_kernel<<<1, 1024, 0, s>>>(idx, T, k, E, 0, offsets, sorted, nullptr, nullptr, nullptr,
-                                    nullptr);
+  permute_kernel<<<1, 1024, 0, s>>>(idx, T, k, E, 0, 8, offsets, sorted, nullptr, nullptr,
+                                    nullptr, nullptr);
   return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
 }
 
@@ -583,8 +613,8 @@ int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, floa
   int rc = launch_router(d.router_W, d.E, d.hidden, x, xdt, T, d.top_k, pl.KS, part, lg, idx,
                          gate, s);
   if (rc != DQ_OK) return rc;
-  permute_kernel<<<1, 1024, 0, s>>>(idx, T, d.top_k, d.E, d.n_shared, offsets, sorted, inv, tok,
-                                    groups, ngroups);
+  permute_kernel<<<1, 1024, 0, s>>>(idx, T, d.top_k, d.E, d.n_shared, pl.GW, offsets, sorted,
+                                    inv, tok, groups, ngroups);
   if (cudaGetLastError() != cudaSuccess) return DQ_ERR_CUDA;
 
   const int q = qk(d.fmt), bb = blk_bytes(d.fmt);
@@ -608,7 +638,7 @@ int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, floa
   gu.out_stride = d.ffn;
   gu.tiles = d.ffn / 32;
   gu.rows_per_expert = d.ffn;
-  rc = launch_grouped_fmt<true>(d.fmt, gu, pl.G_max * gu.tiles, s, d.E, d.n_shared);
+  rc = launch_grouped_fmt<true>(d.fmt, pl.NT, gu, pl.G_max * gu.tiles, s, d.E, d.n_shared);
   if (rc != DQ_OK) return rc;
 
   GroupedParams dn;
@@ -629,7 +659,7 @@ int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, floa
   dn.out_stride = d.hidden;
   dn.tiles = d.hidden / 64;
   dn.rows_per_expert = d.hidden;
-  rc = launch_grouped_fmt<false>(d.fmt, dn, pl.G_max * dn.tiles, s, d.E, d.n_shared);
+  rc = launch_grouped_fmt<false>(d.fmt, pl.NT, dn, pl.G_max * dn.tiles, s, d.E, d.n_shared);
   if (rc != DQ_OK) return rc;
 
   const int64_t n4 = (int64_t)T * d.hidden / 4;

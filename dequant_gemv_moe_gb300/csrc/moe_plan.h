@@ -13,6 +13,8 @@ struct MoePlan {
   int KS;           // router hidden-dimension split
   int64_t P;        // routed (token, slot) pairs = T * top_k
   int64_t NP;       // positions: P routed + n_shared * T shared
+  int NT;           // 8-column activation tiles per grouped-GEMV unit (1, 2, 4)
+  int GW;           // group width = 8 * NT columns
   int G_max;        // upper bound of work groups
   size_t off_part, off_logits, off_idx, off_gate, off_offsets, off_sorted, off_inv, off_tok,
       off_groups, off_ngroups, off_h, off_ypos, total;

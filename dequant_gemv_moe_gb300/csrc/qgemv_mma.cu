@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(kThreads) qgemv_mma_kernel(const __grid_consta
     if (ksplit > 1) mbar_init(red_full, (ksplit - 1) * kConsumerWarps * 32);
     fence_barrier_init();
   }
-  init_xinv(xinv, plan.nstage, p.x.dtype);
+  init_xinv(xinv, plan.nstage * 8, p.x.dtype);
   if (ksplit > 1) cluster_sync_all();
   else __syncthreads();
 
@@ -95,10 +95,11 @@ __global__ void __launch_bounds__(kThreads) qgemv_mma_kernel(const __grid_consta
       const int ncs = min(L::C, sb1 - c0);
       const int delta = (int)(((int64_t)c0 * L::SBB) & 15);
       const uint32_t wst = smem_u32(wbuf + s * L::W_STAGE) + (16 * cw + g) * L::ROW_PITCH + delta;
-      const uint32_t xcol = smem_u32(xbuf + (s * p.batch + xc) * L::XCOL);
-      float part[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      const uint32_t xcol[1] = {smem_u32(xbuf + (s * p.batch + xc) * L::XCOL)};
+      float pt[1][2][4] = {};
       for (int j = 0; j < ncs; ++j)
-        SBDot<FMT>::run(wst + j * L::SBB, 8 * L::ROW_PITCH, xcol, j * 256, t, part);
+        SBDot<FMT>::template run<1>(wst + j * L::SBB, 8 * L::ROW_PITCH, xcol, j * 256, t, pt);
+      float (&part)[2][4] = pt[0];
       if (f16) {
         for (int i = 0; i < 4; ++i) acc[i] += part[0][i] + part[1][i];
       } else {

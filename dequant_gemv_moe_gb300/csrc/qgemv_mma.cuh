@@ -56,6 +56,9 @@ struct Layout {
   static constexpr int XCOL = XCOL_RAW + ((32 - XCOL_RAW % 128) + 128) % 128;
 };
 
+// Per-stage column-scale slots: 8 per 8 activation columns.
+__host__ __device__ constexpr int xinv_stride(int cols) { return 8 * ((cols + 7) / 8); }
+
 // Dynamic shared memory layout of one CTA (offsets in bytes).
 struct SmemPlan {
   int nstage, batch, ksplit;
@@ -72,7 +75,7 @@ __host__ __device__ inline SmemPlan make_plan(int nstage, int batch, int ksplit)
   p.off_w = 1024;                                      // 128-byte aligned TMA stages
   p.off_x = p.off_w + nstage * Layout<FMT>::W_STAGE;
   p.off_xinv = p.off_x + nstage * batch * Layout<FMT>::XCOL;
-  p.off_red = p.off_xinv + nstage * 8 * 4;
+  p.off_red = p.off_xinv + nstage * xinv_stride(batch) * 4;
   p.off_red = (p.off_red + 15) / 16 * 16;
   p.total = p.off_red + (ksplit > 1 ? (ksplit - 1) * kConsumerWarps * 32 * 16 : 0);
   return p;
@@ -135,9 +138,9 @@ __device__ __forceinline__ void pow2_scale(float amax, float& scale, float& inv)
 }
 
 // fp16 activations need no scale: every stage's column scale is 1.
-__device__ __forceinline__ void init_xinv(float* xinv, int nstage, int dtype) {
+__device__ __forceinline__ void init_xinv(float* xinv, int n, int dtype) {
   if (dtype == DQ_F16)
-    for (int i = threadIdx.x; i < nstage * 8; i += blockDim.x) xinv[i] = 1.f;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) xinv[i] = 1.f;
 }
 
 // Loader: stage the activation columns of one stage (nsb_stage super-blocks
@@ -213,6 +216,20 @@ __device__ __forceinline__ void ldx(uint32_t xcol, int k, uint32_t& b0, uint32_t
   b1 = v.y;
 }
 
+// One A fragment times NT activation tiles of 8 columns: NT mma into the
+// accumulator chain `ch` of each tile.
+template <int NT>
+__device__ __forceinline__ void mma_x(float (&acc)[NT][2][4], int ch, uint32_t a0, uint32_t a1,
+                                      uint32_t a2, uint32_t a3, const uint32_t (&xcol)[NT],
+                                      int k) {
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    uint32_t b0, b1;
+    ldx(xcol[nt], k, b0, b1);
+    mma_16816(acc[nt][ch], a0, a1, a2, a3, b0, b1);
+  }
+}
+
 template <int FMT>
 struct SBDot;
 
@@ -248,8 +265,10 @@ struct SBDot<DQ_Q4_K> {
     ohi = __high2half2(o);
   }
 
-  __device__ __forceinline__ static void run(uint32_t wrow, int pitch8, uint32_t xcol, int kb,
-                                             int t, float (&acc)[2][4]) {
+  template <int NT>
+  __device__ __forceinline__ static void run(uint32_t wrow, int pitch8,
+                                             const uint32_t (&xcol)[NT], int kb, int t,
+                                             float (&acc)[NT][2][4]) {
     const uint32_t r0 = wrow, r8 = wrow + pitch8;
     const uint4 h0 = lds_u128(r0), h8 = lds_u128(r8);
     __half2 s0l, o0l, s0h, o0h, s8l, o8l, s8h, o8h;
@@ -266,24 +285,21 @@ struct SBDot<DQ_Q4_K> {
       const uint32_t p0 = __byte_perm(q0[s], 0, 0x3120), p8 = __byte_perm(q8[s], 0, 0x3120);
       const uint32_t p0s = p0 >> 8, p8s = p8 >> 8;
       const int k = kb + 64 * t + 4 * s;
-      uint32_t b0, b1;
       // low nibbles: weights k..k+3 (sub-block 2t)
-      ldx(xcol, k, b0, b1);
       {
         const uint32_t a0 = h2_as_u32(__hfma2(__hsub2(u32_as_h2(lop3_and_or(p0, 0x000F000Fu, 0x64006400u)), magic), s0l, o0l));
         const uint32_t a1 = h2_as_u32(__hfma2(__hsub2(u32_as_h2(lop3_and_or(p8, 0x000F000Fu, 0x64006400u)), magic), s8l, o8l));
         const uint32_t a2 = h2_as_u32(__hfma2(__hsub2(u32_as_h2(lop3_and_or(p0s, 0x000F000Fu, 0x64006400u)), magic), s0l, o0l));
         const uint32_t a3 = h2_as_u32(__hfma2(__hsub2(u32_as_h2(lop3_and_or(p8s, 0x000F000Fu, 0x64006400u)), magic), s8l, o8l));
-        mma_16816(acc[0], a0, a1, a2, a3, b0, b1);
+        mma_x<NT>(acc, 0, a0, a1, a2, a3, xcol, k);
       }
       // high nibbles: weights k+32..k+35 (sub-block 2t+1), value 16*q
-      ldx(xcol, k + 32, b0, b1);
       {
         const uint32_t a0 = h2_as_u32(__hfma2(__hsub2(u32_as_h2(lop3_and_or(p0, 0x00F000F0u, 0x64006400u)), magic), s0h, o0h));
         const uint32_t a1 = h2_as_u32(__hfma2(__hsub2(u32_as_h2(lop3_and_or(p8, 0x00F000F0u, 0x64006400u)), magic), s8h, o8h));
         const uint32_t a2 = h2_as_u32(__hfma2(__hsub2(u32_as_h2(lop3_and_or(p0s, 0x00F000F0u, 0x64006400u)), magic), s0h, o0h));
         const uint32_t a3 = h2_as_u32(__hfma2(__hsub2(u32_as_h2(lop3_and_or(p8s, 0x00F000F0u, 0x64006400u)), magic), s8h, o8h));
-        mma_16816(acc[1], a0, a1, a2, a3, b0, b1);
+        mma_x<NT>(acc, 1, a0, a1, a2, a3, xcol, k + 32);
       }
     }
   }
@@ -301,8 +317,10 @@ struct SBDot<DQ_Q6_K> {
     return h2_as_u32(__hsub2(u32_as_h2(v), u32_as_h2(0x64206420u)));   // 1024+q - 1056
   }
 
-  __device__ __forceinline__ static void run(uint32_t wrow, int pitch8, uint32_t xcol, int kb,
-                                             int t, float (&acc)[2][4]) {
+  template <int NT>
+  __device__ __forceinline__ static void run(uint32_t wrow, int pitch8,
+                                             const uint32_t (&xcol)[NT], int kb, int t,
+                                             float (&acc)[NT][2][4]) {
     const uint32_t rows[2] = {wrow, wrow + pitch8};
     // d and this lane's 8 scales per row: sc[8h + 2r + t/2], h = 0..1, r = 0..3
     __half2 scl[2][8];
@@ -354,9 +372,7 @@ struct SBDot<DQ_Q6_K> {
             a[rr] = h2_as_u32(__hmul2(u32_as_h2(q6_pair(nlo, hlo)), sc));
             a[2 + rr] = h2_as_u32(__hmul2(u32_as_h2(q6_pair(nhi, hhi)), sc));
           }
-          uint32_t b0, b1;
-          ldx(xcol, kbase + 32 * r, b0, b1);
-          mma_16816(acc[r & 1], a[0], a[1], a[2], a[3], b0, b1);
+          mma_x<NT>(acc, r & 1, a[0], a[1], a[2], a[3], xcol, kbase + 32 * r);
         }
       }
     }
@@ -367,8 +383,10 @@ struct SBDot<DQ_Q6_K> {
 // quants 8t..8t+7 of each block.
 template <>
 struct SBDot<DQ_Q8_0> {
-  __device__ __forceinline__ static void run(uint32_t wrow, int pitch8, uint32_t xcol, int kb,
-                                             int t, float (&acc)[2][4]) {
+  template <int NT>
+  __device__ __forceinline__ static void run(uint32_t wrow, int pitch8,
+                                             const uint32_t (&xcol)[NT], int kb, int t,
+                                             float (&acc)[NT][2][4]) {
     const __half2 bias = __float2half2_rn(1152.f);   // 1024 + 128
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
@@ -388,11 +406,8 @@ struct SBDot<DQ_Q8_0> {
           a[m][2 + rr] = h2_as_u32(__hmul2(__hsub2(u32_as_h2(hi), bias), d2));
         }
       }
-      uint32_t b0, b1;
-      ldx(xcol, kb + 32 * s + 8 * t, b0, b1);
-      mma_16816(acc[0], a[0][0], a[0][1], a[0][2], a[0][3], b0, b1);
-      ldx(xcol, kb + 32 * s + 8 * t + 4, b0, b1);
-      mma_16816(acc[1], a[1][0], a[1][1], a[1][2], a[1][3], b0, b1);
+      mma_x<NT>(acc, 0, a[0][0], a[0][1], a[0][2], a[0][3], xcol, kb + 32 * s + 8 * t);
+      mma_x<NT>(acc, 1, a[1][0], a[1][1], a[1][2], a[1][3], xcol, kb + 32 * s + 8 * t + 4);
     }
   }
 };

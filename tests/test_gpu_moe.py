@@ -121,6 +121,8 @@ def _moe_case(dq, orc, fmt, E, k, H, F, ns, T, xdt, seed, tokens=None):
     (Q6_K, 4, 2, 2048, 2048, 1, 7, 1),
     (Q4_K, 4, 4, 256, 256, 0, 3, 0),        # every expert active, fp32 activations
     (Q4_K, 1, 1, 256, 512, 0, 1, 1),        # one expert, one token
+    (Q4_K, 4, 2, 512, 512, 1, 40, 1),       # ~20 tokens per expert: 32-column groups
+    (Q8_0, 4, 2, 256, 512, 0, 64, 2),       # ~32 tokens per expert: some groups split
 ])
 def test_moe_forward_small(dq, orc, fmt, E, k, H, F, ns, T, xdt):
     err, _ = _moe_case(dq, orc, fmt, E, k, H, F, ns, T, xdt, seed=3000 + E * 7 + T)
