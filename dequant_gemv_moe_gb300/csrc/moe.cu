@@ -30,6 +30,9 @@ namespace dqmoe {
 // ===========================================================================
 static size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
+// an expert with more than kWide tokens is computed by the tcgen05 GEMM
+constexpr int kWide = 32;
+
 MoePlan moe_plan(const dq_moe_desc& d, int T) {
   MoePlan p;
   const int tiles = ((d.E + 63) / 64) * ((T + 31) / 32);
@@ -43,6 +46,12 @@ MoePlan moe_plan(const dq_moe_desc& d, int T) {
   p.GW = 8 * p.NT;
   p.G_max = (int)((p.P + p.GW - 1) / p.GW + std::min<int64_t>(d.E, p.P) +
                   (int64_t)d.n_shared * ((T + p.GW - 1) / p.GW));
+  // experts with more than kWide tokens go to the tensor-core GEMM in units of
+  // <= 128 tokens: at most P/(kWide+1) such experts
+  p.wide = T > kWide;
+  p.U_max = p.wide ? (int)(p.P / 128 + p.P / (kWide + 1) + 1 +
+                           (int64_t)d.n_shared * ((T + 127) / 128))
+                   : 0;
   size_t o = 0;
   p.off_part = o;    o = align256(o + (size_t)p.KS * T * d.E * 4);
   p.off_logits = o;  o = align256(o + (size_t)T * d.E * 4);
@@ -56,6 +65,18 @@ MoePlan moe_plan(const dq_moe_desc& d, int T) {
   p.off_ngroups = o; o = align256(o + 16);
   p.off_h = o;       o = align256(o + (size_t)p.NP * d.ffn * 4);
   p.off_ypos = o;    o = align256(o + (size_t)p.NP * d.hidden * 4);
+  p.off_units = o;   o = align256(o + (size_t)std::max(p.U_max, 1) * 16);
+  p.off_nunits = o;  o = align256(o + 16);
+  // fp16 copies of the activations the streaming kernels read
+  p.off_x16t = o;    o = align256(o + (size_t)T * d.hidden * 2);   // per token (bf16/fp32 x)
+  p.off_xinvt = o;   o = align256(o + (size_t)T * 4);
+  p.off_h16 = o;     o = align256(o + (size_t)p.NP * d.ffn * 2);   // per position
+  p.off_hinv = o;    o = align256(o + (size_t)p.NP * 4);
+  const size_t npw = p.wide ? (size_t)p.NP : 0;   // wide-path buffers only when possible
+  p.off_x16 = o;     o = align256(o + npw * d.hidden * 2);
+  p.off_xinv = o;    o = align256(o + npw * 4);
+  p.off_g = o;       o = align256(o + npw * d.ffn * 4);
+  p.off_u = o;       o = align256(o + npw * d.ffn * 4);
   p.total = o;
   return p;
 }
@@ -196,12 +217,15 @@ __global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict
                                                        int32_t* __restrict__ inv,
                                                        int32_t* __restrict__ tok,
                                                        int4* __restrict__ groups,
-                                                       int32_t* __restrict__ n_groups) {
+                                                       int32_t* __restrict__ n_groups,
+                                                       int4* __restrict__ units,
+                                                       int32_t* __restrict__ n_units) {
   __shared__ int cnt[256];
   __shared__ int off[257];
   __shared__ int run[256];
   __shared__ int cntw[32][256];
   __shared__ int gsc[257];
+  __shared__ int usc[257];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int P = T * k;
   if (tid < 256) cnt[tid] = 0;
@@ -254,29 +278,58 @@ __global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict
   if (!groups) return;
   // shared-expert positions follow the routed ones: P + s*T + t
   for (int i = tid; i < n_shared * T; i += 1024) tok[P + i] = i % T;
-  // groups of <= gw columns per expert, experts in order, then shared experts
-  if (tid < 256) gsc[tid + 1] = (tid < E) ? (cnt[tid] + gw - 1) / gw : 0;
-  if (tid == 0) gsc[0] = 0;
+  // narrow groups of <= gw columns per expert (experts with <= kWide tokens),
+  // wide units of <= 128 columns (more tokens); experts in order, then the
+  // shared experts (all T tokens)
+  const bool wide_ok = units != nullptr;
+  if (tid < 256) {
+    const int n = (tid < E) ? cnt[tid] : 0;
+    const bool w = wide_ok && n > kWide;
+    gsc[tid + 1] = w ? 0 : (n + gw - 1) / gw;
+    usc[tid + 1] = w ? (n + 127) / 128 : 0;
+  }
+  if (tid == 0) {
+    gsc[0] = 0;
+    usc[0] = 0;
+  }
   __syncthreads();
   for (int d = 1; d < 256; d <<= 1) {
-    int v = 0;
-    if (tid < 256 && tid + 1 > d) v = gsc[tid + 1 - d];
+    int v = 0, w = 0;
+    if (tid < 256 && tid + 1 > d) {
+      v = gsc[tid + 1 - d];
+      w = usc[tid + 1 - d];
+    }
     __syncthreads();
-    if (tid < 256) gsc[tid + 1] += v;
+    if (tid < 256) {
+      gsc[tid + 1] += v;
+      usc[tid + 1] += w;
+    }
     __syncthreads();
   }
   if (tid < E) {
     const int n = cnt[tid];
-    for (int j = 0; j * gw < n; ++j)
-      groups[gsc[tid] + j] = make_int4(tid, off[tid] + gw * j, min(gw, n - gw * j), 0);
+    if (wide_ok && n > kWide) {
+      for (int j = 0; j * 128 < n; ++j)
+        units[usc[tid] + j] = make_int4(tid, off[tid] + 128 * j, min(128, n - 128 * j), 0);
+    } else {
+      for (int j = 0; j * gw < n; ++j)
+        groups[gsc[tid] + j] = make_int4(tid, off[tid] + gw * j, min(gw, n - gw * j), 0);
+    }
   }
-  const int nr = gsc[E];
-  const int per = (T + gw - 1) / gw;
+  const int nr = gsc[E], ur = usc[E];
+  const bool sh_wide = wide_ok && T > kWide;
+  const int per = sh_wide ? (T + 127) / 128 : (T + gw - 1) / gw;
+  const int width = sh_wide ? 128 : gw;
   for (int i = tid; i < n_shared * per; i += 1024) {
     const int s = i / per, j = i % per;
-    groups[nr + i] = make_int4(E + s, P + s * T + gw * j, min(gw, T - gw * j), 0);
+    const int4 g = make_int4(E + s, P + s * T + width * j, min(width, T - width * j), 0);
+    if (sh_wide) units[ur + i] = g;
+    else groups[nr + i] = g;
   }
-  if (tid == 0) *n_groups = nr + n_shared * per;
+  if (tid == 0) {
+    *n_groups = nr + (sh_wide ? 0 : n_shared * per);
+    if (wide_ok) *n_units = ur + (sh_wide ? n_shared * per : 0);
+  }
 }
 
 // ===========================================================================
@@ -304,6 +357,8 @@ struct GroupedParams {
   int64_t xstride;     // elements per x / h row
   float* out;          // gate/up: h [NP][F]; down: ypos [NP][H]
   int64_t out_stride;
+  const float* colinv; // 1/scale of each column's fp16 activations (nullable: 1)
+  const int* coltok;   // colinv index of position pos: coltok[pos] (nullable: pos)
   int tiles;           // tiles per group
   int nstage;
 };
@@ -357,7 +412,7 @@ __global__ void __launch_bounds__(kThreads) grouped_kernel(const __grid_constant
         xs.base = p.xbase;
         xs.rows = p.tok + grp.y;
       } else {
-        xs.base = (const float*)p.xbase + (int64_t)grp.y * p.xstride;
+        xs.base = (const __half*)p.xbase + (int64_t)grp.y * p.xstride;
         xs.rows = nullptr;
       }
       for (int c = 0; c < nchunk && ok; ++c, ++gc) {
@@ -430,6 +485,20 @@ __global__ void __launch_bounds__(kThreads) grouped_kernel(const __grid_constant
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
+      }
+      // undo the activation scale of each column
+      if (p.colinv) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const int c0 = 8 * nt + 2 * t;
+          const int p0 = grp.y + min(c0, ncols - 1), p1 = grp.y + min(c0 + 1, ncols - 1);
+          const float i0 = __ldg(p.colinv + (p.coltok ? __ldg(p.coltok + p0) : p0));
+          const float i1 = __ldg(p.colinv + (p.coltok ? __ldg(p.coltok + p1) : p1));
+          acc[nt][0] *= i0;
+          acc[nt][1] *= i1;
+          acc[nt][2] *= i0;
+          acc[nt][3] *= i1;
+        }
       }
       if (!GATEUP) {
         const int ra = tile * 64 + 16 * cw + g, rb = ra + 8;
@@ -577,6 +646,18 @@ int launch_grouped_fmt(int fmt, int nt, const GroupedParams& gp, int units_max, 
 
 }  // namespace
 
+int launch_tc_gemm(int fmt, const void* W, const void* Wsh, int E, int n_shared,
+                   int rows_per_expert, int K, const int4* units, const int* n_units,
+                   int max_units, const __half* X16, int64_t npos, const float* xinv, float* out,
+                   int64_t out_stride, cudaStream_t s);
+int launch_x16_rows(const void* x, int xdt, int rows, int K, __half* out, float* inv,
+                    cudaStream_t s);
+int launch_gather_x16(const int4* units, const int* n_units, int max_units, const int32_t* tok,
+                      const __half* x16, const float* tinv, int K, __half* X16, float* xinv,
+                      cudaStream_t s);
+int launch_swiglu_wide(const int4* units, const int* n_units, int max_units, const float* G,
+                       const float* U, int F, float* h, cudaStream_t s);
+
 int launch_router(const float* Wr, int E, int H, const void* x, int xdt, int T, int top_k,
                   int KS, float* part, float* logits, int32_t* idx, float* gate, cudaStream_t s) {
   dim3 g1((unsigned)((E + 63) / 64), (unsigned)((T + 31) / 32), (unsigned)KS);
@@ -589,7 +670,7 @@ int launch_router(const float* Wr, int E, int H, const void* x, int xdt, int T, 
 int launch_permute(const int32_t* idx, int T, int k, int E, int32_t* offsets, int32_t* sorted,
                    cudaStream_t s) {
   permute_kernel<<<1, 1024, 0, s>>>(idx, T, k, E, 0, 8, offsets, sorted, nullptr, nullptr,
-                                    nullptr, nullptr);
+                                    nullptr, nullptr, nullptr, nullptr);
   return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
 }
 
@@ -613,11 +694,33 @@ int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, floa
   int rc = launch_router(d.router_W, d.E, d.hidden, x, xdt, T, d.top_k, pl.KS, part, lg, idx,
                          gate, s);
   if (rc != DQ_OK) return rc;
+  int4* units = (int4*)(w + pl.off_units);
+  int32_t* nunits = (int32_t*)(w + pl.off_nunits);
   permute_kernel<<<1, 1024, 0, s>>>(idx, T, d.top_k, d.E, d.n_shared, pl.GW, offsets, sorted,
-                                    inv, tok, groups, ngroups);
+                                    inv, tok, groups, ngroups, pl.wide ? units : nullptr,
+                                    nunits);
   if (cudaGetLastError() != cudaSuccess) return DQ_ERR_CUDA;
 
   const int q = qk(d.fmt), bb = blk_bytes(d.fmt);
+  __half* x16t = (__half*)(w + pl.off_x16t);
+  float* xinvt = (float*)(w + pl.off_xinvt);
+  __half* h16 = (__half*)(w + pl.off_h16);
+  float* hinv = (float*)(w + pl.off_hinv);
+  __half* x16 = (__half*)(w + pl.off_x16);
+  float* xinv = (float*)(w + pl.off_xinv);
+  float* G = (float*)(w + pl.off_g);
+  float* U = (float*)(w + pl.off_u);
+
+  // fp16 activations for the streaming kernels (fp16 input is used as is)
+  const __half* xh = (const __half*)x;
+  const float* xh_inv = nullptr;
+  if (xdt != DQ_F16) {
+    rc = launch_x16_rows(x, xdt, T, d.hidden, x16t, xinvt, s);
+    if (rc != DQ_OK) return rc;
+    xh = x16t;
+    xh_inv = xinvt;
+  }
+
   GroupedParams gu;
   memset(&gu, 0, sizeof(gu));
   gu.Wa = (const uint8_t*)d.w_gate;
@@ -631,14 +734,34 @@ int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, floa
   gu.groups = groups;
   gu.n_groups = ngroups;
   gu.tok = tok;
-  gu.xbase = x;
-  gu.xdt = xdt;
+  gu.xbase = xh;
+  gu.xdt = DQ_F16;
   gu.xstride = d.hidden;
   gu.out = h;
   gu.out_stride = d.ffn;
+  gu.colinv = xh_inv;
+  gu.coltok = tok;
   gu.tiles = d.ffn / 32;
   gu.rows_per_expert = d.ffn;
   rc = launch_grouped_fmt<true>(d.fmt, pl.NT, gu, pl.G_max * gu.tiles, s, d.E, d.n_shared);
+  if (rc != DQ_OK) return rc;
+
+  // wide units: gathered fp16 rows, tensor-core gate and up GEMMs, SwiGLU
+  if (pl.wide) {
+    rc = launch_gather_x16(units, nunits, pl.U_max, tok, xh, xh_inv, d.hidden, x16, xinv, s);
+    if (rc != DQ_OK) return rc;
+    rc = launch_tc_gemm(d.fmt, d.w_gate, d.sh_gate, d.E, d.n_shared, d.ffn, d.hidden, units,
+                        nunits, pl.U_max, x16, pl.NP, xinv, G, d.ffn, s);
+    if (rc != DQ_OK) return rc;
+    rc = launch_tc_gemm(d.fmt, d.w_up, d.sh_up, d.E, d.n_shared, d.ffn, d.hidden, units, nunits,
+                        pl.U_max, x16, pl.NP, xinv, U, d.ffn, s);
+    if (rc != DQ_OK) return rc;
+    rc = launch_swiglu_wide(units, nunits, pl.U_max, G, U, d.ffn, h, s);
+    if (rc != DQ_OK) return rc;
+  }
+
+  // h -> fp16 with a power-of-two scale per position (all positions)
+  rc = launch_x16_rows(h, DQ_F32, (int)pl.NP, d.ffn, h16, hinv, s);
   if (rc != DQ_OK) return rc;
 
   GroupedParams dn;
@@ -652,15 +775,22 @@ int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, floa
   dn.groups = groups;
   dn.n_groups = ngroups;
   dn.tok = nullptr;
-  dn.xbase = h;
-  dn.xdt = DQ_F32;
+  dn.xbase = h16;
+  dn.xdt = DQ_F16;
   dn.xstride = d.ffn;
   dn.out = ypos;
   dn.out_stride = d.hidden;
+  dn.colinv = hinv;
+  dn.coltok = nullptr;
   dn.tiles = d.hidden / 64;
   dn.rows_per_expert = d.hidden;
   rc = launch_grouped_fmt<false>(d.fmt, pl.NT, dn, pl.G_max * dn.tiles, s, d.E, d.n_shared);
   if (rc != DQ_OK) return rc;
+  if (pl.wide) {
+    rc = launch_tc_gemm(d.fmt, d.w_down, d.sh_down, d.E, d.n_shared, d.hidden, d.ffn, units,
+                        nunits, pl.U_max, h16, pl.NP, hinv, ypos, d.hidden, s);
+    if (rc != DQ_OK) return rc;
+  }
 
   const int64_t n4 = (int64_t)T * d.hidden / 4;
   const int cgrid = (int)std::min<int64_t>((n4 + 255) / 256, 4096);

@@ -1,0 +1,105 @@
+// moe_prep.cu — activation preparation for the MoE layer's streaming kernels.
+//
+// The grouped expert kernels read 16-bit activations straight into shared
+// memory with asynchronous copies, so every activation they read is fp16:
+//   * x16_tokens_kernel : bf16 / fp32 x -> fp16 rows with one power-of-two
+//     scale per token (max|x| * scale in [2^14, 2^15): no overflow);
+//   * h16_kernel        : the fp32 SwiGLU output h -> fp16 rows with one
+//     power-of-two scale per position;
+//   * gather_x16_kernel : the wide (tensor-core) units' activation rows,
+//     gathered by token into position order for TMA;
+//   * swiglu_wide_kernel: h = silu(g) * u for the wide units.
+// The kernels consuming these undo the scale on their fp32 results.
+#include "qgemv_mma.cuh"
+
+namespace dqmoe {
+
+namespace {
+__device__ __forceinline__ float wmax(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float act(const void* x, int xdt, int64_t i) {
+  if (xdt == DQ_F32) return __ldg((const float*)x + i);
+  if (xdt == DQ_BF16) return __uint_as_float((uint32_t)__ldg((const unsigned short*)x + i) << 16);
+  return __half2float(__ldg((const __half*)x + i));
+}
+}  // namespace
+
+// one warp per row: out[row][k] = fp16(in[row][k] * 2^e), inv[row] = 2^-e
+__global__ void __launch_bounds__(256) x16_tokens_kernel(const void* __restrict__ x, int xdt,
+                                                         int rows, int K, __half* __restrict__ out,
+                                                         float* __restrict__ inv) {
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const int64_t base = (int64_t)row * K;
+  float amax = 0.f;
+  for (int k = lane; k < K; k += 32) amax = fmaxf(amax, fabsf(act(x, xdt, base + k)));
+  amax = wmax(amax);
+  float sc, iv;
+  pow2_scale(amax, sc, iv);
+  for (int k = lane; k < K; k += 32) out[base + k] = __float2half_rn(act(x, xdt, base + k) * sc);
+  if (lane == 0) inv[row] = iv;
+}
+
+// X16[pos] = x16[tok[pos]], xinv[pos] = tinv[tok[pos]] (tinv null: 1) for the
+// positions of the wide units; one CTA per unit
+__global__ void __launch_bounds__(256) gather_x16_kernel(const int4* __restrict__ units,
+                                                         const int* __restrict__ n_units,
+                                                         const int32_t* __restrict__ tok,
+                                                         const __half* __restrict__ x16,
+                                                         const float* __restrict__ tinv, int K,
+                                                         __half* __restrict__ X16,
+                                                         float* __restrict__ xinv) {
+  if ((int)blockIdx.x >= __ldg(n_units)) return;
+  const int4 u = __ldg(units + blockIdx.x);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int n = warp; n < u.z; n += 8) {
+    const int pos = u.y + n;
+    const int t = __ldg(tok + pos);
+    const uint4* src = (const uint4*)(x16 + (int64_t)t * K);
+    uint4* dst = (uint4*)(X16 + (int64_t)pos * K);
+    for (int k = lane; k < K / 8; k += 32) dst[k] = __ldg(src + k);
+    if (lane == 0) xinv[pos] = tinv ? __ldg(tinv + t) : 1.f;
+  }
+}
+
+// h = silu(G) * U for the wide units' positions; silu(g) = g / (1 + exp(-g))
+// (-0 for g < -88: exp overflows to inf, never NaN)
+__global__ void __launch_bounds__(256) swiglu_wide_kernel(const int4* __restrict__ units,
+                                                          const int* __restrict__ n_units,
+                                                          const float* __restrict__ G,
+                                                          const float* __restrict__ U, int F,
+                                                          float* __restrict__ h) {
+  if ((int)blockIdx.x >= __ldg(n_units)) return;
+  const int4 u = __ldg(units + blockIdx.x);
+  const int64_t base = (int64_t)u.y * F, n = (int64_t)u.z * F;
+  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
+    const float g = G[base + i];
+    h[base + i] = g / (1.f + expf(-g)) * U[base + i];
+  }
+}
+
+int launch_x16_rows(const void* x, int xdt, int rows, int K, __half* out, float* inv,
+                    cudaStream_t s) {
+  x16_tokens_kernel<<<(rows + 7) / 8, 256, 0, s>>>(x, xdt, rows, K, out, inv);
+  return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
+}
+
+int launch_gather_x16(const int4* units, const int* n_units, int max_units, const int32_t* tok,
+                      const __half* x16, const float* tinv, int K, __half* X16, float* xinv,
+                      cudaStream_t s) {
+  gather_x16_kernel<<<max_units > 0 ? max_units : 1, 256, 0, s>>>(units, n_units, tok, x16, tinv,
+                                                                  K, X16, xinv);
+  return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
+}
+
+int launch_swiglu_wide(const int4* units, const int* n_units, int max_units, const float* G,
+                       const float* U, int F, float* h, cudaStream_t s) {
+  swiglu_wide_kernel<<<max_units > 0 ? max_units : 1, 256, 0, s>>>(units, n_units, G, U, F, h);
+  return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
+}
+
+}  // namespace dqmoe

@@ -167,34 +167,38 @@ __device__ __forceinline__ void stage_x(const XSrc& xs, int ncols, int64_t k0, i
     mbar_arrive(full);
     return;
   }
-  for (int c = 0; c < ncols; ++c) {
-    uint8_t* col = xdst + c * Layout<FMT>::XCOL;
-    constexpr int C = Layout<FMT>::C;
-    float v[C][8];
-    float amax = 0.f;
+  // four columns at a time: their global loads are in flight together
+  static_assert(Layout<FMT>::C == 1, "one super-block per stage");
+  for (int c0 = 0; c0 < ncols; c0 += 4) {
+    float v[4][8];
+    float amax[4];
 #pragma unroll
-    for (int j = 0; j < C; ++j) {
-      if (j < nsb_stage) {
-        load8_f32(xs, c, k0 + j * 256 + 8 * lane, v[j]);
+    for (int j = 0; j < 4; ++j) {
+      amax[j] = 0.f;
+      if (c0 + j < ncols && nsb_stage > 0) {
+        load8_f32(xs, c0 + j, k0 + 8 * lane, v[j]);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[j][i]));
+        for (int i = 0; i < 8; ++i) amax[j] = fmaxf(amax[j], fabsf(v[j][i]));
       }
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    float sc, inv;
-    pow2_scale(amax, sc, inv);
+    for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
-    for (int j = 0; j < C; ++j) {
-      if (j < nsb_stage) {
+      for (int j = 0; j < 4; ++j) amax[j] = fmaxf(amax[j], __shfl_xor_sync(0xffffffffu, amax[j], o));
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (c0 + j < ncols && nsb_stage > 0) {
+        float sc, inv;
+        pow2_scale(amax[j], sc, inv);
         uint32_t h[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
           h[i] = h2_as_u32(__floats2half2_rn(v[j][2 * i] * sc, v[j][2 * i + 1] * sc));
-        *(uint4*)(col + 2 * xoff(j * 256 + 8 * lane)) = make_uint4(h[0], h[1], h[2], h[3]);
+        *(uint4*)(xdst + (c0 + j) * Layout<FMT>::XCOL + 2 * xoff(8 * lane)) =
+            make_uint4(h[0], h[1], h[2], h[3]);
+        if (lane == 0) xinv[c0 + j] = inv;
       }
     }
-    if (lane == 0) xinv[c] = inv;
   }
   cp_async_arrive_noinc(full);
   mbar_arrive(full);

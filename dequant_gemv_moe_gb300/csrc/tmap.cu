@@ -39,4 +39,18 @@ bool make_weight_tmap(CUtensorMap* map, const void* base, uint64_t rows, uint64_
   return r == CUDA_SUCCESS;
 }
 
+bool make_act_tmap_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t K) {
+  auto fn = encode_fn();
+  if (!fn || (K * 2) % 16 || ((uintptr_t)base & 15) || rows == 0) return false;
+  const cuuint64_t dims[2] = {K, rows};
+  const cuuint64_t strides[1] = {K * 2};
+  const cuuint32_t box[2] = {64, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace dqmoe

@@ -13,4 +13,8 @@ namespace dqmoe {
 bool make_weight_tmap(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_bytes,
                       uint32_t box_bytes, uint32_t box_rows);
 
+// fp16 activations [rows][K] (K contiguous): boxes of 64 elements (128 B) x 32
+// rows, written to shared memory in the 128-byte swizzled layout.
+bool make_act_tmap_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t K);
+
 }  // namespace dqmoe

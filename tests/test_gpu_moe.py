@@ -123,6 +123,10 @@ def _moe_case(dq, orc, fmt, E, k, H, F, ns, T, xdt, seed, tokens=None):
     (Q4_K, 1, 1, 256, 512, 0, 1, 1),        # one expert, one token
     (Q4_K, 4, 2, 512, 512, 1, 40, 1),       # ~20 tokens per expert: 32-column groups
     (Q8_0, 4, 2, 256, 512, 0, 64, 2),       # ~32 tokens per expert: some groups split
+    # more than 32 tokens on an expert: the tcgen05 grouped GEMM (units of <= 128)
+    (Q4_K, 4, 2, 512, 512, 1, 64, 1),
+    (Q6_K, 2, 1, 2048, 2048, 0, 100, 2),
+    (Q8_0, 2, 2, 256, 256, 1, 300, 0),
 ])
 def test_moe_forward_small(dq, orc, fmt, E, k, H, F, ns, T, xdt):
     err, _ = _moe_case(dq, orc, fmt, E, k, H, F, ns, T, xdt, seed=3000 + E * 7 + T)
