@@ -14,8 +14,8 @@ pytestmark = pytest.mark.gpu
 
 @pytest.mark.parametrize("fmt,E,k,H,F,ns,T,xdt", [
     (Q4_K, 1, 1, 256, 256, 0, 33, 1),       # one unit of 33 tokens: N = 48, 2 boxes
-    (Q4_K, 1, 1, 512, 384, 1, 40, 2),       # shared expert too; 3 row tiles
-    (Q8_0, 2, 1, 256, 256, 0, 130, 1),      # > 128 tokens: two units per expert
+    (Q4_K, 1, 1, 512, 512, 1, 40, 2),       # shared expert too; 4 row tiles
+    (Q8_0, 1, 1, 256, 256, 0, 130, 1),      # > 128 tokens: two units (128 + 2)
     (Q6_K, 1, 1, 2048, 2048, 0, 64, 0),     # Q6_K rows, fp32 activations
 ])
 def test_tc_wide_units(dq, orc, fmt, E, k, H, F, ns, T, xdt):
