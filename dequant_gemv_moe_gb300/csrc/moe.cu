@@ -383,7 +383,7 @@ __global__ void __launch_bounds__(kThreads) grouped_kernel(const __grid_constant
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < plan.nstage; ++s) {
-      mbar_init(&full[s], 64);
+      mbar_init(&full[s], full_arrivals(p.xdt));
       mbar_init(&empty[s], kConsumerWarps);
     }
     fence_barrier_init();
@@ -424,7 +424,7 @@ __global__ void __launch_bounds__(kThreads) grouped_kernel(const __grid_constant
         const int64_t a = ((int64_t)c0 * L::SBB) & ~(int64_t)15;
         if (lane == 0) {
           uint8_t* wst = wbuf + s * L::W_STAGE;
-          mbar_expect_tx(&full[s], L::W_STAGE);
+          mbar_arrive_expect_tx(&full[s], L::W_STAGE);
           if (GATEUP) {
             tma_load_2d(wst, ma, (int)(a >> 1), grow, &full[s], pol);
             tma_load_2d(wst + 32 * L::ROW_PITCH, mb, (int)(a >> 1), grow, &full[s], pol);

@@ -28,20 +28,26 @@ __device__ __forceinline__ float act(const void* x, int xdt, int64_t i) {
 }
 }  // namespace
 
-// one warp per row: out[row][k] = fp16(in[row][k] * 2^e), inv[row] = 2^-e
+// one CTA (256 threads) per row: out[row][k] = fp16(in[row][k] * 2^e),
+// inv[row] = 2^-e, with max|in[row]| * 2^e in [2^14, 2^15)
 __global__ void __launch_bounds__(256) x16_tokens_kernel(const void* __restrict__ x, int xdt,
                                                          int rows, int K, __half* __restrict__ out,
                                                          float* __restrict__ inv) {
-  const int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (row >= rows) return;
+  __shared__ float red[8];
+  const int row = blockIdx.x;
   const int64_t base = (int64_t)row * K;
   float amax = 0.f;
-  for (int k = lane; k < K; k += 32) amax = fmaxf(amax, fabsf(act(x, xdt, base + k)));
+  for (int k = threadIdx.x; k < K; k += 256) amax = fmaxf(amax, fabsf(act(x, xdt, base + k)));
   amax = wmax(amax);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = red[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
   float sc, iv;
   pow2_scale(amax, sc, iv);
-  for (int k = lane; k < K; k += 32) out[base + k] = __float2half_rn(act(x, xdt, base + k) * sc);
-  if (lane == 0) inv[row] = iv;
+  for (int k = threadIdx.x; k < K; k += 256) out[base + k] = __float2half_rn(act(x, xdt, base + k) * sc);
+  if (threadIdx.x == 0) inv[row] = iv;
 }
 
 // X16[pos] = x16[tok[pos]], xinv[pos] = tinv[tok[pos]] (tinv null: 1) for the
@@ -84,7 +90,7 @@ __global__ void __launch_bounds__(256) swiglu_wide_kernel(const int4* __restrict
 
 int launch_x16_rows(const void* x, int xdt, int rows, int K, __half* out, float* inv,
                     cudaStream_t s) {
-  x16_tokens_kernel<<<(rows + 7) / 8, 256, 0, s>>>(x, xdt, rows, K, out, inv);
+  x16_tokens_kernel<<<rows, 256, 0, s>>>(x, xdt, rows, K, out, inv);
   return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
 }
 

@@ -48,7 +48,7 @@ __global__ void __launch_bounds__(kThreads) qgemv_mma_kernel(const __grid_consta
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < plan.nstage; ++s) {
-      mbar_init(&full[s], 64);                 // 32 loader lanes x (copies landed, stores done)
+      mbar_init(&full[s], full_arrivals(p.x.dtype));
       mbar_init(&empty[s], kConsumerWarps);    // one per consumer warp
     }
     if (ksplit > 1) mbar_init(red_full, (ksplit - 1) * kConsumerWarps * 32);
@@ -73,7 +73,7 @@ __global__ void __launch_bounds__(kThreads) qgemv_mma_kernel(const __grid_consta
       // (Q6_K blocks are 210 bytes; row starts are 16-byte aligned)
       const int64_t a = ((int64_t)c0 * L::SBB) & ~(int64_t)15;
       if (lane == 0) {
-        mbar_expect_tx(&full[s], L::W_STAGE);   // rows past N are zero-filled, still counted
+        mbar_arrive_expect_tx(&full[s], L::W_STAGE);   // rows past N are zero-filled, still counted
         tma_load_2d(wbuf + s * L::W_STAGE, &p.tmap, (int)(a >> 1), row0, &full[s], pol);
       }
       stage_x<FMT>(p.x, p.batch, (int64_t)c0 * 256, ncs, xbuf + s * p.batch * L::XCOL,

@@ -137,6 +137,11 @@ __device__ __forceinline__ void pow2_scale(float amax, float& scale, float& inv)
   inv = __uint_as_float((uint32_t)(127 - se) << 23);
 }
 
+// Arrivals per phase of a stage's full barrier: the loader's lane 0 with the
+// TMA byte count, one cp.async arrival per loader lane, and for converted
+// (bf16 / fp32) activations one more arrival per lane after its stores.
+__host__ __device__ constexpr int full_arrivals(int dtype) { return dtype == DQ_F16 ? 33 : 65; }
+
 // fp16 activations need no scale: every stage's column scale is 1.
 __device__ __forceinline__ void init_xinv(float* xinv, int n, int dtype) {
   if (dtype == DQ_F16)
@@ -145,11 +150,11 @@ __device__ __forceinline__ void init_xinv(float* xinv, int n, int dtype) {
 
 // Loader: stage the activation columns of one stage (nsb_stage super-blocks
 // starting at activation index k0) as fp16 at xdst (column pitch XCOL bytes)
-// and arrive on `full` for this lane twice: once asynchronously when all of
-// the lane's cp.async copies of the stage (weights and fp16 activations) have
-// landed, once after its own shared-memory stores.  fp16 input is copied
-// asynchronously; bf16 / fp32 input is converted with a per-column
-// power-of-two scale.
+// and arrive on `full` for this lane: asynchronously once its cp.async copies
+// of the stage have landed, and (bf16 / fp32 input only) once more after its
+// own shared-memory stores.  fp16 input is copied asynchronously; bf16 / fp32
+// input is converted with a per-column power-of-two scale.  The full barrier
+// therefore expects full_arrivals(dtype) arrivals per phase.
 template <int FMT>
 __device__ __forceinline__ void stage_x(const XSrc& xs, int ncols, int64_t k0, int nsb_stage,
                                         uint8_t* xdst, float* xinv, int lane, uint64_t* full) {
@@ -164,7 +169,6 @@ __device__ __forceinline__ void stage_x(const XSrc& xs, int ncols, int64_t k0, i
     }
     // xinv stays 1 for fp16 input: set once per CTA before the pipeline starts
     cp_async_arrive_noinc(full);
-    mbar_arrive(full);
     return;
   }
   // four columns at a time: their global loads are in flight together
