@@ -394,7 +394,8 @@ __global__ void __launch_bounds__(kThreads) grouped_kernel(const __grid_constant
   if (warp == 0) {
     // ------------------------------ loader ------------------------------
     const uint64_t pol = l2_evict_first_policy();
-    int gc = 0;
+    int gc = 0, ls = 0;
+    uint32_t lph = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
       const int4 grp = __ldg(p.groups + u / p.tiles);
@@ -416,9 +417,13 @@ __global__ void __launch_bounds__(kThreads) grouped_kernel(const __grid_constant
         xs.rows = nullptr;
       }
       for (int c = 0; c < nchunk && ok; ++c, ++gc) {
-        const int s = gc % plan.nstage, round = gc / plan.nstage;
-        if (round > 0) ok = mbar_wait(&empty[s], (round - 1) & 1);
+        if (gc >= plan.nstage) ok = mbar_wait(&empty[ls], lph ^ 1);
         if (!ok) break;
+        const int s = ls;
+        if (++ls == plan.nstage) {
+          ls = 0;
+          lph ^= 1;
+        }
         const int c0 = c * L::C;
         const int ncs = min(L::C, p.nsb - c0);
         const int64_t a = ((int64_t)c0 * L::SBB) & ~(int64_t)15;
@@ -440,7 +445,8 @@ __global__ void __launch_bounds__(kThreads) grouped_kernel(const __grid_constant
     // ----------------------------- consumers -----------------------------
     const int cw = warp - 1;
     const int g = lane >> 2, t = lane & 3;
-    int gc = 0;
+    int cs = 0;
+    uint32_t cph = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
       const int4 grp = __ldg(p.groups + u / p.tiles);
@@ -448,11 +454,17 @@ __global__ void __launch_bounds__(kThreads) grouped_kernel(const __grid_constant
       const int ncols = grp.z;
       const bool f16 = p.xdt == DQ_F16;      // fp16 input carries no scale
       float acc[NT][4] = {};
-      for (int c = 0; c < nchunk; ++c, ++gc) {
-        const int s = gc % plan.nstage, round = gc / plan.nstage;
+      float accs[NT][2][4] = {};             // fp16 input: running accumulator pairs
+      for (int c = 0; c < nchunk; ++c) {
+        const int s = cs;
+        const uint32_t par = cph;
+        if (++cs == plan.nstage) {
+          cs = 0;
+          cph ^= 1;
+        }
         // after a timed-out wait the warp keeps walking the same units (no
         // further waits, no reads) so every warp still meets the barriers
-        ok = ok && mbar_wait(&full[s], round & 1);
+        ok = ok && mbar_wait(&full[s], par);
         if (!ok) continue;
         const int c0 = c * L::C;
         const int ncs = min(L::C, p.nsb - c0);
@@ -466,15 +478,15 @@ __global__ void __launch_bounds__(kThreads) grouped_kernel(const __grid_constant
           const int col = 8 * nt + g;
           xcol[nt] = smem_u32(xbuf + (s * NC + (col < ncols ? col : 0)) * L::XCOL);
         }
-        float part[NT][2][4] = {};
-        for (int j = 0; j < ncs; ++j)
-          SBDot<FMT>::template run<NT>(wst + j * L::SBB, 8 * L::ROW_PITCH, xcol, j * 256, t, part);
+        if (f16) {
+          for (int j = 0; j < ncs; ++j)
+            SBDot<FMT>::template run<NT>(wst + j * L::SBB, 8 * L::ROW_PITCH, xcol, j * 256, t, accs);
+        } else {
+          float part[NT][2][4] = {};
+          for (int j = 0; j < ncs; ++j)
+            SBDot<FMT>::template run<NT>(wst + j * L::SBB, 8 * L::ROW_PITCH, xcol, j * 256, t, part);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          if (f16) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) acc[nt][i] += part[nt][0][i] + part[nt][1][i];
-          } else {
+          for (int nt = 0; nt < NT; ++nt) {
             const float inv0 = xinv[s * NC + 8 * nt + 2 * t];
             const float inv1 = xinv[s * NC + 8 * nt + 2 * t + 1];
             acc[nt][0] = fmaf(part[nt][0][0] + part[nt][1][0], inv0, acc[nt][0]);
@@ -485,6 +497,12 @@ __global__ void __launch_bounds__(kThreads) grouped_kernel(const __grid_constant
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
+      }
+      if (f16) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[nt][i] = accs[nt][0][i] + accs[nt][1][i];
       }
       // undo the activation scale of each column
       if (p.colinv) {

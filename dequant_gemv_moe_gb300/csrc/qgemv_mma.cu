@@ -63,9 +63,10 @@ __global__ void __launch_bounds__(kThreads) qgemv_mma_kernel(const __grid_consta
     const uint64_t pol = l2_evict_first_policy();
     if (lane == 0) prefetch_tmap(&p.tmap);
     bool ok = true;
+    int s = 0;
+    uint32_t ph = 0;            // phase parity of stage s in the current round
     for (int c = 0; c < nchunk && ok; ++c) {
-      const int s = c % plan.nstage, round = c / plan.nstage;
-      if (round > 0) ok = mbar_wait(&empty[s], (round - 1) & 1);
+      if (c >= plan.nstage) ok = mbar_wait(&empty[s], ph ^ 1);
       if (!ok) break;
       const int c0 = sb0 + c * L::C;
       const int ncs = min(L::C, sb1 - c0);
@@ -78,6 +79,10 @@ __global__ void __launch_bounds__(kThreads) qgemv_mma_kernel(const __grid_consta
       }
       stage_x<FMT>(p.x, p.batch, (int64_t)c0 * 256, ncs, xbuf + s * p.batch * L::XCOL,
                    xinv + s * 8, lane, &full[s]);
+      if (++s == plan.nstage) {
+        s = 0;
+        ph ^= 1;
+      }
     }
   } else {
     // ----------------------------- consumers -----------------------------
@@ -86,32 +91,42 @@ __global__ void __launch_bounds__(kThreads) qgemv_mma_kernel(const __grid_consta
     const int xc = g < p.batch ? g : 0;      // this lane's activation column
     const bool f16 = p.x.dtype == DQ_F16;    // fp16 input carries no scale
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float accs[1][2][4] = {};               // fp16 input: one running accumulator pair
+    const uint32_t wrow = smem_u32(wbuf) + (16 * cw + g) * L::ROW_PITCH;
+    const uint32_t xcol0 = smem_u32(xbuf) + xc * L::XCOL;
     bool ok = true;
+    int s = 0;
+    uint32_t ph = 0;
     for (int c = 0; c < nchunk; ++c) {
-      const int s = c % plan.nstage, round = c / plan.nstage;
-      ok = ok && mbar_wait(&full[s], round & 1);
-      if (!ok) continue;
-      const int c0 = sb0 + c * L::C;
-      const int ncs = min(L::C, sb1 - c0);
-      const int delta = (int)(((int64_t)c0 * L::SBB) & 15);
-      const uint32_t wst = smem_u32(wbuf + s * L::W_STAGE) + (16 * cw + g) * L::ROW_PITCH + delta;
-      const uint32_t xcol[1] = {smem_u32(xbuf + (s * p.batch + xc) * L::XCOL)};
-      float pt[1][2][4] = {};
-      for (int j = 0; j < ncs; ++j)
-        SBDot<FMT>::template run<1>(wst + j * L::SBB, 8 * L::ROW_PITCH, xcol, j * 256, t, pt);
-      float (&part)[2][4] = pt[0];
-      if (f16) {
-        for (int i = 0; i < 4; ++i) acc[i] += part[0][i] + part[1][i];
-      } else {
-        const float inv0 = xinv[s * 8 + ((2 * t) & 7)], inv1 = xinv[s * 8 + ((2 * t + 1) & 7)];
-        acc[0] = fmaf(part[0][0] + part[1][0], inv0, acc[0]);
-        acc[1] = fmaf(part[0][1] + part[1][1], inv1, acc[1]);
-        acc[2] = fmaf(part[0][2] + part[1][2], inv0, acc[2]);
-        acc[3] = fmaf(part[0][3] + part[1][3], inv1, acc[3]);
+      ok = ok && mbar_wait(&full[s], ph);
+      if (ok) {
+        const int c0 = sb0 + c * L::C;
+        const int ncs = min(L::C, sb1 - c0);
+        const uint32_t wst = wrow + s * L::W_STAGE + (uint32_t)(((int64_t)c0 * L::SBB) & 15);
+        const uint32_t xcol[1] = {xcol0 + s * p.batch * L::XCOL};
+        if (f16) {
+          for (int j = 0; j < ncs; ++j)
+            SBDot<FMT>::template run<1>(wst + j * L::SBB, 8 * L::ROW_PITCH, xcol, j * 256, t, accs);
+        } else {
+          float pt[1][2][4] = {};
+          for (int j = 0; j < ncs; ++j)
+            SBDot<FMT>::template run<1>(wst + j * L::SBB, 8 * L::ROW_PITCH, xcol, j * 256, t, pt);
+          const float inv0 = xinv[s * 8 + ((2 * t) & 7)], inv1 = xinv[s * 8 + ((2 * t + 1) & 7)];
+          acc[0] = fmaf(pt[0][0][0] + pt[0][1][0], inv0, acc[0]);
+          acc[1] = fmaf(pt[0][0][1] + pt[0][1][1], inv1, acc[1]);
+          acc[2] = fmaf(pt[0][0][2] + pt[0][1][2], inv0, acc[2]);
+          acc[3] = fmaf(pt[0][0][3] + pt[0][1][3], inv1, acc[3]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
+      if (++s == plan.nstage) {
+        s = 0;
+        ph ^= 1;
+      }
     }
+    if (f16)
+      for (int i = 0; i < 4; ++i) acc[i] = accs[0][0][i] + accs[0][1][i];
 
     // ------------------------ split-K reduction -------------------------
     if (ksplit > 1) {
