@@ -45,6 +45,7 @@ _OPTIONAL_SIGS = {
     "dq_moe_router": [_P, _I, _I, _P, _I, _I, _I, _P, _P, _P, _P],
     "dq_moe_permute": [_P, _I, _I, _I, _P, _P, _P],
     "dq_moe_forward": [ctypes.POINTER(MoeDesc), _P, _I, _I, _P, _P, _SZ, _P, _P, _P, _P],
+    "dq_moe_forward_noalloc": [ctypes.POINTER(MoeDesc), _P, _I, _I, _P, _P, _P, _P, _P],
 }
 
 

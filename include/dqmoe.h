@@ -219,6 +219,30 @@ int dq_moe_forward(const dq_moe_desc* desc, const void* x, int x_dtype, int T,
                    float* y, void* ws, size_t ws_bytes, int32_t* topk_idx,
                    float* topk_gate, float* logits, void* stream);
 
+/* dq_moe_forward_noalloc — dq_moe_forward for callers that cannot allocate
+ * device memory, so cannot provide the `ws` scratch buffer: code running
+ * under a host framework that owns all device memory and gives no workspace
+ * hook (plugins, custom-op shims), or decode loops that must not allocate on
+ * the hot path.  The inference engines this library follows have no
+ * counterpart; it exists for such callers only.
+ * Scratch comes from one fixed array of DQ_NOALLOC_SCRATCH_BYTES (32 MiB)
+ * inside the library: every GPU that loads the library keeps that much
+ * device memory until the process exits.  No call allocates or frees memory.
+ * The first call on a device (with that device current) looks up the array's
+ * device address once (cudaGetSymbolAddress); make that first call before any
+ * stream capture.  All calls on a device share the one array and each call
+ * overwrites it, so calls that may overlap on the GPU (different streams
+ * without ordering) race: order them.  Nothing needs to be zero on entry.
+ * Arguments and outputs as dq_moe_forward (without ws / ws_bytes).
+ * Errors: as dq_moe_forward; DQ_ERR_WORKSPACE when
+ * dq_moe_workspace_size(desc, T) exceeds DQ_NOALLOC_SCRATCH_BYTES (decode-
+ * sized T fits: e.g. 8 tokens of the 256-expert layer, 16 of the 8-expert one);
+ * DQ_ERR_CUDA if the array's address cannot be obtained. */
+#define DQ_NOALLOC_SCRATCH_BYTES (32u << 20)
+int dq_moe_forward_noalloc(const dq_moe_desc* desc, const void* x, int x_dtype, int T,
+                           float* y, int32_t* topk_idx, float* topk_gate, float* logits,
+                           void* stream);
+
 /* Human-readable name of a dq_status value (static string, never NULL). */
 const char* dq_status_string(int status);
 
