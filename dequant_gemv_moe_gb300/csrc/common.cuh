@@ -56,8 +56,9 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
 }
 
 // Arrive once and add `bytes` to the transaction count of the current phase.
+// Relaxed: what the phase waits for (the TMA bytes) is tracked by the count.
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+  asm volatile("mbarrier.arrive.expect_tx.relaxed.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
                    smem_u32(bar)),
                "r"(bytes)
                : "memory");
@@ -78,6 +79,17 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint64_t* bar, uint32_t rank
       "mapa.shared::cluster.u32 ra, %0, %1;\n\t"
       "mbarrier.arrive.release.cluster.shared::cluster.b64 _, [ra];\n\t}" ::"r"(smem_u32(bar)),
       "r"(rank)
+      : "memory");
+}
+
+// Relaxed arrival: for a consumer releasing a stage it has finished reading.
+// Every shared-memory load of the stage has returned its data (each result
+// was consumed by an instruction earlier in program order), so no fence is
+// needed before the producer's next asynchronous overwrite.
+__device__ __forceinline__ void mbar_arrive_relaxed(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.relaxed.cta.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar))
       : "memory");
 }
 

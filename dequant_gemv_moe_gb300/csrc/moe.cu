@@ -496,7 +496,7 @@ __global__ void __launch_bounds__(kThreads) grouped_kernel(const __grid_constant
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
+        if (lane == 0) mbar_arrive_relaxed(&empty[s]);
       }
       if (f16) {
 #pragma unroll

@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(kThreads) qgemv_mma_kernel(const __grid_consta
           acc[3] = fmaf(pt[0][0][3] + pt[0][1][3], inv1, acc[3]);
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
+        if (lane == 0) mbar_arrive_relaxed(&empty[s]);
       }
       if (++s == plan.nstage) {
         s = 0;
