@@ -10,6 +10,8 @@
 //     gathered by token into position order for TMA;
 //   * swiglu_wide_kernel: h = silu(g) * u for the wide units.
 // The kernels consuming these undo the scale on their fp32 results.
+#include <algorithm>
+
 #include "qgemv_mma.cuh"
 
 namespace dqmoe {
@@ -73,16 +75,17 @@ __global__ void __launch_bounds__(256) gather_x16_kernel(const int4* __restrict_
 }
 
 // h = silu(G) * U for the wide units' positions; silu(g) = g / (1 + exp(-g))
-// (-0 for g < -88: exp overflows to inf, never NaN)
+// (-0 for g < -88: exp overflows to inf, never NaN).  Grid: (chunks, units).
 __global__ void __launch_bounds__(256) swiglu_wide_kernel(const int4* __restrict__ units,
                                                           const int* __restrict__ n_units,
                                                           const float* __restrict__ G,
                                                           const float* __restrict__ U, int F,
                                                           float* __restrict__ h) {
-  if ((int)blockIdx.x >= __ldg(n_units)) return;
-  const int4 u = __ldg(units + blockIdx.x);
+  if ((int)blockIdx.y >= __ldg(n_units)) return;
+  const int4 u = __ldg(units + blockIdx.y);
   const int64_t base = (int64_t)u.y * F, n = (int64_t)u.z * F;
-  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
     const float g = G[base + i];
     h[base + i] = g / (1.f + expf(-g)) * U[base + i];
   }
@@ -104,7 +107,9 @@ int launch_gather_x16(const int4* units, const int* n_units, int max_units, cons
 
 int launch_swiglu_wide(const int4* units, const int* n_units, int max_units, const float* G,
                        const float* U, int F, float* h, cudaStream_t s) {
-  swiglu_wide_kernel<<<max_units > 0 ? max_units : 1, 256, 0, s>>>(units, n_units, G, U, F, h);
+  const int chunks = (int)std::min<int64_t>(((int64_t)128 * F + 2047) / 2048, 256);
+  swiglu_wide_kernel<<<dim3(chunks, max_units > 0 ? max_units : 1), 256, 0, s>>>(units, n_units,
+                                                                               G, U, F, h);
   return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
 }
 
