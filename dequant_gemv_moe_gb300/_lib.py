@@ -38,6 +38,7 @@ _SIGS = {
     "dq_dequant": [_I, _P, _I64, _P, _P],
     "dq_qgemv": [_I, _P, _I64, _I64, _P, _I, _I, _P, _P],
     "dq_qgemv_ksplit": [_I, _P, _I64, _I64, _P, _I, _I, _P, _I, _P],
+    "dq_qgemv_ex": [_I, _P, _I64, _I64, _P, _I, _I, _P, _I, ctypes.c_uint, _P],
     "dq_device_status": [_P],
 }
 _OPTIONAL_SIGS = {

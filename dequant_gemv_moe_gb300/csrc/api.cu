@@ -12,7 +12,7 @@ int launch_dequant(int fmt, const void* blocks, int64_t n, float* out, cudaStrea
 int launch_qgemv_f32(int fmt, const void* W, int64_t N, int64_t K, const float* x, int batch,
                      float* y, cudaStream_t s);
 int launch_qgemv_mma(int fmt, const void* W, int64_t N, int64_t K, const void* x, int xdt,
-                     int batch, float* y, cudaStream_t s, int force_ksplit);
+                     int batch, float* y, cudaStream_t s, int force_ksplit, bool w_early);
 int launch_router(const float* Wr, int E, int H, const void* x, int xdt, int T, int top_k,
                   int KS, float* part, float* logits, int32_t* idx, float* gate, cudaStream_t s);
 int launch_permute(const int32_t* idx, int T, int k, int E, int32_t* offsets, int32_t* sorted,
@@ -92,12 +92,19 @@ int dq_qgemv(int fmt, const void* W, int64_t N, int64_t K, const void* x, int x_
 
 int dq_qgemv_ksplit(int fmt, const void* W, int64_t N, int64_t K, const void* x, int x_dtype,
                     int batch, float* y, int ksplit, void* stream) {
+  return dq_qgemv_ex(fmt, W, N, K, x, x_dtype, batch, y, ksplit, 0u, stream);
+}
+
+int dq_qgemv_ex(int fmt, const void* W, int64_t N, int64_t K, const void* x, int x_dtype,
+                int batch, float* y, int ksplit, unsigned flags, void* stream) {
   const int rc = check_qgemv(fmt, W, N, K, x, x_dtype, batch, y);
   if (rc != DQ_OK) return rc;
   if (ksplit < 0 || ksplit > 8) return DQ_ERR_ARG;
+  if (flags & ~DQ_QGEMV_WEIGHTS_EARLY) return DQ_ERR_ARG;
   if (x_dtype == DQ_F32)
     return launch_qgemv_f32(fmt, W, N, K, (const float*)x, batch, y, (cudaStream_t)stream);
-  return launch_qgemv_mma(fmt, W, N, K, x, x_dtype, batch, y, (cudaStream_t)stream, ksplit);
+  return launch_qgemv_mma(fmt, W, N, K, x, x_dtype, batch, y, (cudaStream_t)stream, ksplit,
+                          (flags & DQ_QGEMV_WEIGHTS_EARLY) != 0);
 }
 
 int dq_moe_workspace_size(const dq_moe_desc* desc, int T, size_t* bytes) {

@@ -7,7 +7,10 @@
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
+#include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <utility>
 
 #include "../../include/dqmoe.h"
 
@@ -283,4 +286,47 @@ __device__ __forceinline__ uint32_t lds_u32_a2(uint32_t addr) {
   return __funnelshift_r(lo, hi, 16);
 }
 
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// programmatic stream serialization: it may be scheduled while the kernel
+// before it in the stream is still finishing.  pdl_wait() blocks the calling
+// thread until that kernel has completed and its memory is visible (it returns
+// at once when there is none), so every thread calls it before its first read
+// of data another kernel may produce and before its first global write.
+// pdl_trigger() lets the next kernel be scheduled; issued once every CTA of
+// this grid is resident, it only shortens the gap between kernels.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch with programmatic stream serialization and, for cluster > 0, a
+// thread-block cluster of `cluster` CTAs along x.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, int cluster, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster > 0) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = (unsigned)cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = (unsigned)n;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 }  // namespace dqmoe
+

@@ -20,6 +20,8 @@ __device__ __forceinline__ float h16(const uint8_t* p) {
 
 __global__ void dequant_q4k_kernel(const uint8_t* __restrict__ blocks, int64_t nblk,
                                    float* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t blk = gid >> 8;
   if (blk >= nblk) return;
@@ -44,6 +46,8 @@ __global__ void dequant_q4k_kernel(const uint8_t* __restrict__ blocks, int64_t n
 
 __global__ void dequant_q6k_kernel(const uint8_t* __restrict__ blocks, int64_t nblk,
                                    float* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t blk = gid >> 8;
   if (blk >= nblk) return;
@@ -62,6 +66,8 @@ __global__ void dequant_q6k_kernel(const uint8_t* __restrict__ blocks, int64_t n
 
 __global__ void dequant_q80_kernel(const uint8_t* __restrict__ blocks, int64_t nblk,
                                    float* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t blk = gid >> 5;
   if (blk >= nblk) return;
@@ -73,9 +79,9 @@ int launch_dequant(int fmt, const void* blocks, int64_t n, float* out, cudaStrea
   const int threads = 256;
   const int64_t grid = (n + threads - 1) / threads;
   const uint8_t* b = (const uint8_t*)blocks;
-  if (fmt == DQ_Q4_K) dequant_q4k_kernel<<<(unsigned)grid, threads, 0, s>>>(b, n / 256, out);
-  else if (fmt == DQ_Q6_K) dequant_q6k_kernel<<<(unsigned)grid, threads, 0, s>>>(b, n / 256, out);
-  else dequant_q80_kernel<<<(unsigned)grid, threads, 0, s>>>(b, n / 32, out);
+  if (fmt == DQ_Q4_K) launch_pdl(dequant_q4k_kernel, dim3((unsigned)grid), dim3(threads), 0, s, 0, b, n / 256, out);
+  else if (fmt == DQ_Q6_K) launch_pdl(dequant_q6k_kernel, dim3((unsigned)grid), dim3(threads), 0, s, 0, b, n / 256, out);
+  else launch_pdl(dequant_q80_kernel, dim3((unsigned)grid), dim3(threads), 0, s, 0, b, n / 32, out);
   return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
 }
 

@@ -95,6 +95,8 @@ __global__ void __launch_bounds__(128) router_logits_kernel(const float* __restr
                                                             int H, const void* __restrict__ x,
                                                             int xdt, int T, int KS,
                                                             float* __restrict__ part) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ __align__(16) float Ws[32][64 + 4];
   __shared__ __align__(16) float Xs[32][32 + 4];
   const int e0 = blockIdx.x * 64, t0 = blockIdx.y * 32, ks = blockIdx.z;
@@ -148,6 +150,8 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ par
                                                    int E, int k, float* __restrict__ logits,
                                                    int32_t* __restrict__ idx,
                                                    float* __restrict__ gate) {
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -220,6 +224,8 @@ __global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict
                                                        int32_t* __restrict__ n_groups,
                                                        int4* __restrict__ units,
                                                        int32_t* __restrict__ n_units) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int cnt[256];
   __shared__ int off[257];
   __shared__ int run[256];
@@ -367,6 +373,8 @@ struct GroupedParams {
 template <int FMT, bool GATEUP, int NT>
 __global__ void __launch_bounds__(kThreads) grouped_kernel(const __grid_constant__ GroupedParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
+  pdl_wait();
+  pdl_trigger();
   using L = Layout<FMT>;
   constexpr int NC = 8 * NT;
   const SmemPlan plan = make_plan<FMT>(p.nstage, NC, 1);
@@ -478,7 +486,20 @@ __global__ void __launch_bounds__(kThreads) grouped_kernel(const __grid_constant
           const int col = 8 * nt + g;
           xcol[nt] = smem_u32(xbuf + (s * NC + (col < ncols ? col : 0)) * L::XCOL);
         }
-        if (f16) {
+        if constexpr (SBDot<FMT>::kRowScale) {
+          for (int j = 0; j < ncs; ++j) {
+            float d[NT][2][4] = {};
+            float r0, r8;
+            SBDot<FMT>::template run<NT>(wst + j * L::SBB, 8 * L::ROW_PITCH, xcol, j * 256, t, d,
+                                         r0, r8);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              const float c0 = f16 ? 1.f : xinv[s * NC + 8 * nt + 2 * t];
+              const float c1 = f16 ? 1.f : xinv[s * NC + 8 * nt + 2 * t + 1];
+              fold_tile(acc[nt], d[nt], r0, r8, c0, c1);
+            }
+          }
+        } else if (f16) {
           for (int j = 0; j < ncs; ++j)
             SBDot<FMT>::template run<NT>(wst + j * L::SBB, 8 * L::ROW_PITCH, xcol, j * 256, t, accs);
         } else {
@@ -486,19 +507,14 @@ __global__ void __launch_bounds__(kThreads) grouped_kernel(const __grid_constant
           for (int j = 0; j < ncs; ++j)
             SBDot<FMT>::template run<NT>(wst + j * L::SBB, 8 * L::ROW_PITCH, xcol, j * 256, t, part);
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            const float inv0 = xinv[s * NC + 8 * nt + 2 * t];
-            const float inv1 = xinv[s * NC + 8 * nt + 2 * t + 1];
-            acc[nt][0] = fmaf(part[nt][0][0] + part[nt][1][0], inv0, acc[nt][0]);
-            acc[nt][1] = fmaf(part[nt][0][1] + part[nt][1][1], inv1, acc[nt][1]);
-            acc[nt][2] = fmaf(part[nt][0][2] + part[nt][1][2], inv0, acc[nt][2]);
-            acc[nt][3] = fmaf(part[nt][0][3] + part[nt][1][3], inv1, acc[nt][3]);
-          }
+          for (int nt = 0; nt < NT; ++nt)
+            fold_tile(acc[nt], part[nt], 1.f, 1.f, xinv[s * NC + 8 * nt + 2 * t],
+                      xinv[s * NC + 8 * nt + 2 * t + 1]);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive_relaxed(&empty[s]);
       }
-      if (f16) {
+      if (!SBDot<FMT>::kRowScale && f16) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -568,6 +584,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       const float* __restrict__ gate, int T,
                                                       int k, int H, int n_shared,
                                                       float* __restrict__ y) {
+  pdl_wait();
+  pdl_trigger();
   const int H4 = H / 4;
   const int64_t total = (int64_t)T * H4;
   const int64_t P = (int64_t)T * k;
@@ -646,7 +664,9 @@ int launch_grouped(const GroupedParams& gp_in, int units_max, cudaStream_t s, in
                                                     smem) != cudaSuccess || occ < 1)
     occ = 1;
   const int grid = std::max(1, std::min(units_max, occ * sms));
-  grouped_kernel<FMT, GATEUP, NT><<<grid, kThreads, smem, s>>>(gp);
+  if (launch_pdl(grouped_kernel<FMT, GATEUP, NT>, dim3(grid), dim3(kThreads), smem, s, 0, gp) !=
+      cudaSuccess)
+    return DQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
 }
 
@@ -679,15 +699,15 @@ int launch_swiglu_wide(const int4* units, const int* n_units, int max_units, con
 int launch_router(const float* Wr, int E, int H, const void* x, int xdt, int T, int top_k,
                   int KS, float* part, float* logits, int32_t* idx, float* gate, cudaStream_t s) {
   dim3 g1((unsigned)((E + 63) / 64), (unsigned)((T + 31) / 32), (unsigned)KS);
-  router_logits_kernel<<<g1, 128, 0, s>>>(Wr, E, H, x, xdt, T, KS, part);
+  launch_pdl(router_logits_kernel, dim3(g1), dim3(128), 0, s, 0, Wr, E, H, x, xdt, T, KS, part);
   if (cudaGetLastError() != cudaSuccess) return DQ_ERR_CUDA;
-  topk_kernel<<<(unsigned)((T + 7) / 8), 256, 0, s>>>(part, KS, T, E, top_k, logits, idx, gate);
+  launch_pdl(topk_kernel, dim3((unsigned)((T + 7) / 8)), dim3(256), 0, s, 0, part, KS, T, E, top_k, logits, idx, gate);
   return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
 }
 
 int launch_permute(const int32_t* idx, int T, int k, int E, int32_t* offsets, int32_t* sorted,
                    cudaStream_t s) {
-  permute_kernel<<<1, 1024, 0, s>>>(idx, T, k, E, 0, 8, offsets, sorted, nullptr, nullptr,
+  launch_pdl(permute_kernel, dim3(1), dim3(1024), 0, s, 0, idx, T, k, E, 0, 8, offsets, sorted, nullptr, nullptr,
                                     nullptr, nullptr, nullptr, nullptr);
   return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
 }
@@ -714,7 +734,7 @@ int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, floa
   if (rc != DQ_OK) return rc;
   int4* units = (int4*)(w + pl.off_units);
   int32_t* nunits = (int32_t*)(w + pl.off_nunits);
-  permute_kernel<<<1, 1024, 0, s>>>(idx, T, d.top_k, d.E, d.n_shared, pl.GW, offsets, sorted,
+  launch_pdl(permute_kernel, dim3(1), dim3(1024), 0, s, 0, idx, T, d.top_k, d.E, d.n_shared, pl.GW, offsets, sorted,
                                     inv, tok, groups, ngroups, pl.wide ? units : nullptr,
                                     nunits);
   if (cudaGetLastError() != cudaSuccess) return DQ_ERR_CUDA;
@@ -812,7 +832,7 @@ int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, floa
 
   const int64_t n4 = (int64_t)T * d.hidden / 4;
   const int cgrid = (int)std::min<int64_t>((n4 + 255) / 256, 4096);
-  combine_kernel<<<cgrid, 256, 0, s>>>(ypos, inv, gate, T, d.top_k, d.hidden, d.n_shared, y);
+  launch_pdl(combine_kernel, dim3(cgrid), dim3(256), 0, s, 0, ypos, inv, gate, T, d.top_k, d.hidden, d.n_shared, y);
   return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
 }
 

@@ -35,6 +35,8 @@ __device__ __forceinline__ float act(const void* x, int xdt, int64_t i) {
 __global__ void __launch_bounds__(256) x16_tokens_kernel(const void* __restrict__ x, int xdt,
                                                          int rows, int K, __half* __restrict__ out,
                                                          float* __restrict__ inv) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[8];
   const int row = blockIdx.x;
   const int64_t base = (int64_t)row * K;
@@ -61,6 +63,8 @@ __global__ void __launch_bounds__(256) gather_x16_kernel(const int4* __restrict_
                                                          const float* __restrict__ tinv, int K,
                                                          __half* __restrict__ X16,
                                                          float* __restrict__ xinv) {
+  pdl_wait();
+  pdl_trigger();
   if ((int)blockIdx.x >= __ldg(n_units)) return;
   const int4 u = __ldg(units + blockIdx.x);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -81,6 +85,8 @@ __global__ void __launch_bounds__(256) swiglu_wide_kernel(const int4* __restrict
                                                           const float* __restrict__ G,
                                                           const float* __restrict__ U, int F,
                                                           float* __restrict__ h) {
+  pdl_wait();
+  pdl_trigger();
   if ((int)blockIdx.y >= __ldg(n_units)) return;
   const int4 u = __ldg(units + blockIdx.y);
   const int64_t base = (int64_t)u.y * F, n = (int64_t)u.z * F;
@@ -93,23 +99,29 @@ __global__ void __launch_bounds__(256) swiglu_wide_kernel(const int4* __restrict
 
 int launch_x16_rows(const void* x, int xdt, int rows, int K, __half* out, float* inv,
                     cudaStream_t s) {
-  x16_tokens_kernel<<<rows, 256, 0, s>>>(x, xdt, rows, K, out, inv);
+  if (launch_pdl(x16_tokens_kernel, dim3(rows), dim3(256), 0, s, 0, x, xdt, rows, K, out, inv) !=
+      cudaSuccess)
+    return DQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
 }
 
 int launch_gather_x16(const int4* units, const int* n_units, int max_units, const int32_t* tok,
                       const __half* x16, const float* tinv, int K, __half* X16, float* xinv,
                       cudaStream_t s) {
-  gather_x16_kernel<<<max_units > 0 ? max_units : 1, 256, 0, s>>>(units, n_units, tok, x16, tinv,
-                                                                  K, X16, xinv);
+  const unsigned grid = (unsigned)(max_units > 0 ? max_units : 1);
+  if (launch_pdl(gather_x16_kernel, dim3(grid), dim3(256), 0, s, 0, units, n_units, tok, x16, tinv,
+                 K, X16, xinv) != cudaSuccess)
+    return DQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
 }
 
 int launch_swiglu_wide(const int4* units, const int* n_units, int max_units, const float* G,
                        const float* U, int F, float* h, cudaStream_t s) {
   const int chunks = (int)std::min<int64_t>(((int64_t)128 * F + 2047) / 2048, 256);
-  swiglu_wide_kernel<<<dim3(chunks, max_units > 0 ? max_units : 1), 256, 0, s>>>(units, n_units,
-                                                                               G, U, F, h);
+  const dim3 grid((unsigned)chunks, (unsigned)(max_units > 0 ? max_units : 1));
+  if (launch_pdl(swiglu_wide_kernel, grid, dim3(256), 0, s, 0, units, n_units, G, U, F, h) !=
+      cudaSuccess)
+    return DQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
 }
 

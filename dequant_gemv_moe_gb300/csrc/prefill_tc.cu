@@ -57,7 +57,7 @@ struct SlabDecode<DQ_Q4_K> {
   __device__ __forceinline__ static void run(uint32_t rb, int q, uint4 (&out)[8]) {
     const uint4 hd = lds_u128(rb);
     __half2 slo, olo, shi, ohi;
-    SBDot<DQ_Q4_K>::scales(hd, q, slo, olo, shi, ohi);   // sub-blocks 2q (low), 2q+1 (high)
+    SBDot<DQ_Q4_K>::scales_abs(hd, q, slo, olo, shi, ohi);   // sub-blocks 2q (low), 2q+1 (high)
     const uint4 qa = lds_u128(rb + 16 + 32 * q), qb = lds_u128(rb + 32 + 32 * q);
     const uint32_t w[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
     const __half2 magic = u32_as_h2(0x64006400u);
@@ -151,6 +151,8 @@ struct TcParams {
 template <int FMT>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
+  pdl_wait();
+  pdl_trigger();
   using TL = TcLayout<FMT>;
   const int unit = blockIdx.y;
   if (unit >= __ldg(p.n_units)) return;            // uniform for the whole CTA
@@ -338,7 +340,8 @@ int launch_tc_fmt(const void* W, const void* Wsh, int E, int n_shared, int rows_
     if (dev < 64) attr[dev] = true;
   }
   dim3 grid((unsigned)(rows_per_expert / kTcRows), (unsigned)std::max(1, max_units));
-  tc_gemm_kernel<FMT><<<grid, kTcThreads, TL::TOTAL, s>>>(p);
+  if (launch_pdl(tc_gemm_kernel<FMT>, grid, dim3(kTcThreads), TL::TOTAL, s, 0, p) != cudaSuccess)
+    return DQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
 }
 

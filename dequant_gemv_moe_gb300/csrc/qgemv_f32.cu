@@ -88,6 +88,8 @@ __global__ void __launch_bounds__(256) qgemv_f32_kernel(const uint8_t* __restric
                                                         int64_t N, int64_t nsb,
                                                         const float* __restrict__ x,
                                                         int64_t K, float* __restrict__ y) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= N) return;
@@ -121,13 +123,17 @@ int launch_f32_fmt(const void* W, int64_t N, int64_t K, const float* x, int batc
   const int64_t nsb = K / 256;
   const unsigned grid = (unsigned)((N + 7) / 8);
   const uint8_t* w = (const uint8_t*)W;
+  cudaError_t rc = cudaSuccess;
   switch (batch) {
 #define DQ_CASE(BB) \
-  case BB: qgemv_f32_kernel<FMT, BB><<<grid, 256, 0, s>>>(w, N, nsb, x, K, y); break;
+  case BB:                                                                               \
+    rc = launch_pdl(qgemv_f32_kernel<FMT, BB>, dim3(grid), dim3(256), 0, s, 0, w, N, nsb, x, K, y); \
+    break;
     DQ_CASE(1) DQ_CASE(2) DQ_CASE(3) DQ_CASE(4) DQ_CASE(5) DQ_CASE(6) DQ_CASE(7) DQ_CASE(8)
 #undef DQ_CASE
     default: return DQ_ERR_ARG;
   }
+  if (rc != cudaSuccess) return DQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
 }
 

@@ -20,6 +20,7 @@ struct GemvParams {
   int batch;
   float* y;         // [batch][N]
   int nstage;
+  int w_early;      // 1: issue the first stages' weight copies before pdl_wait
 };
 
 template <int FMT>
@@ -44,7 +45,7 @@ __global__ void __launch_bounds__(kThreads) qgemv_mma_kernel(const __grid_consta
   // this CTA's super-block range [sb0, sb1)
   const int sb0 = (int)((int64_t)p.nsb * rank / ksplit);
   const int sb1 = (int)((int64_t)p.nsb * (rank + 1) / ksplit);
-  const int nchunk = (sb1 - sb0 + L::C - 1) / L::C;
+  const int nchunk = sb1 - sb0;   // one super-block per stage
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < plan.nstage; ++s) {
@@ -58,26 +59,37 @@ __global__ void __launch_bounds__(kThreads) qgemv_mma_kernel(const __grid_consta
   if (ksplit > 1) cluster_sync_all();
   else __syncthreads();
 
+  pdl_trigger();
+
   if (warp == 0) {
     // ------------------------------ loader ------------------------------
     const uint64_t pol = l2_evict_first_policy();
     if (lane == 0) prefetch_tmap(&p.tmap);
+    // weights are read-only inputs: with w_early their first stages stream in
+    // while the previous kernel in the stream finishes
+    const int early = p.w_early ? min(plan.nstage, nchunk) : 0;
+    if (lane == 0)
+      for (int c = 0; c < early; ++c) {
+        const int64_t a = ((int64_t)(sb0 + c) * L::SBB) & ~(int64_t)15;
+        mbar_arrive_expect_tx(&full[c], L::W_STAGE);
+        tma_load_2d(wbuf + c * L::W_STAGE, &p.tmap, (int)(a >> 1), row0, &full[c], pol);
+      }
+    pdl_wait();
     bool ok = true;
     int s = 0;
     uint32_t ph = 0;            // phase parity of stage s in the current round
     for (int c = 0; c < nchunk && ok; ++c) {
       if (c >= plan.nstage) ok = mbar_wait(&empty[s], ph ^ 1);
       if (!ok) break;
-      const int c0 = sb0 + c * L::C;
-      const int ncs = min(L::C, sb1 - c0);
+      const int c0 = sb0 + c;
       // box start: the super-block's first byte rounded down to 16 bytes
       // (Q6_K blocks are 210 bytes; row starts are 16-byte aligned)
       const int64_t a = ((int64_t)c0 * L::SBB) & ~(int64_t)15;
-      if (lane == 0) {
+      if (lane == 0 && c >= early) {
         mbar_arrive_expect_tx(&full[s], L::W_STAGE);   // rows past N are zero-filled, still counted
         tma_load_2d(wbuf + s * L::W_STAGE, &p.tmap, (int)(a >> 1), row0, &full[s], pol);
       }
-      stage_x<FMT>(p.x, p.batch, (int64_t)c0 * 256, ncs, xbuf + s * p.batch * L::XCOL,
+      stage_x<FMT>(p.x, p.batch, (int64_t)c0 * 256, 1, xbuf + s * p.batch * L::XCOL,
                    xinv + s * 8, lane, &full[s]);
       if (++s == plan.nstage) {
         s = 0;
@@ -86,6 +98,7 @@ __global__ void __launch_bounds__(kThreads) qgemv_mma_kernel(const __grid_consta
     }
   } else {
     // ----------------------------- consumers -----------------------------
+    pdl_wait();
     const int cw = warp - 1;
     const int g = lane >> 2, t = lane & 3;
     const int xc = g < p.batch ? g : 0;      // this lane's activation column
@@ -100,22 +113,23 @@ __global__ void __launch_bounds__(kThreads) qgemv_mma_kernel(const __grid_consta
     for (int c = 0; c < nchunk; ++c) {
       ok = ok && mbar_wait(&full[s], ph);
       if (ok) {
-        const int c0 = sb0 + c * L::C;
-        const int ncs = min(L::C, sb1 - c0);
+        const int c0 = sb0 + c;
         const uint32_t wst = wrow + s * L::W_STAGE + (uint32_t)(((int64_t)c0 * L::SBB) & 15);
         const uint32_t xcol[1] = {xcol0 + s * p.batch * L::XCOL};
-        if (f16) {
-          for (int j = 0; j < ncs; ++j)
-            SBDot<FMT>::template run<1>(wst + j * L::SBB, 8 * L::ROW_PITCH, xcol, j * 256, t, accs);
+        if constexpr (SBDot<FMT>::kRowScale) {
+          float d[1][2][4] = {};
+          float r0, r8;
+          SBDot<FMT>::template run<1>(wst, 8 * L::ROW_PITCH, xcol, 0, t, d, r0, r8);
+          const float c0 = f16 ? 1.f : xinv[s * 8 + ((2 * t) & 7)];
+          const float c1 = f16 ? 1.f : xinv[s * 8 + ((2 * t + 1) & 7)];
+          fold_tile(acc, d[0], r0, r8, c0, c1);
+        } else if (f16) {
+          SBDot<FMT>::template run<1>(wst, 8 * L::ROW_PITCH, xcol, 0, t, accs);
         } else {
           float pt[1][2][4] = {};
-          for (int j = 0; j < ncs; ++j)
-            SBDot<FMT>::template run<1>(wst + j * L::SBB, 8 * L::ROW_PITCH, xcol, j * 256, t, pt);
+          SBDot<FMT>::template run<1>(wst, 8 * L::ROW_PITCH, xcol, 0, t, pt);
           const float inv0 = xinv[s * 8 + ((2 * t) & 7)], inv1 = xinv[s * 8 + ((2 * t + 1) & 7)];
-          acc[0] = fmaf(pt[0][0][0] + pt[0][1][0], inv0, acc[0]);
-          acc[1] = fmaf(pt[0][0][1] + pt[0][1][1], inv1, acc[1]);
-          acc[2] = fmaf(pt[0][0][2] + pt[0][1][2], inv0, acc[2]);
-          acc[3] = fmaf(pt[0][0][3] + pt[0][1][3], inv1, acc[3]);
+          fold_tile(acc, pt[0], 1.f, 1.f, inv0, inv1);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive_relaxed(&empty[s]);
@@ -125,7 +139,7 @@ __global__ void __launch_bounds__(kThreads) qgemv_mma_kernel(const __grid_consta
         ph ^= 1;
       }
     }
-    if (f16)
+    if (!SBDot<FMT>::kRowScale && f16)
       for (int i = 0; i < 4; ++i) acc[i] = accs[0][0][i] + accs[0][1][i];
 
     // ------------------------ split-K reduction -------------------------
@@ -174,22 +188,20 @@ int device_sms() {
   return sms;
 }
 
-// Pick the K-split (cluster size, 1..8) that best fills the GPU: balance of
-// the CTA waves times balance of the super-blocks inside a cluster.
-int choose_ksplit(int tiles, int nsb, int slots) {
+// Pick the K-split (cluster size, 1..8).  Model: about three 64-row CTAs per
+// SM keep HBM busy; a CTA costs its super-blocks plus a fixed pipeline fill
+// and drain of about two super-blocks; CTAs beyond three per SM run in another
+// round.  Splitting only pays when the tiles alone leave SMs idle (measured on
+// GB300: the 28672 x 8192 matrix runs best unsplit, 14336 x 4096 split in 2).
+int choose_ksplit(int tiles, int nsb, int sms) {
   int best = 1;
-  double best_eff = -1.0;
-  for (int s = 1; s <= 8; ++s) {
-    if (nsb / s < 1) break;
-    const double waves = (double)tiles * s / slots;
-    const double eff_w = waves / std::ceil(waves);
-    const double per = (double)nsb / s;
-    const double eff_k = per / std::ceil(per);
-    // small penalty for very short K slices (pipeline fill per CTA)
-    const double eff_fill = per / (per + 0.5);
-    const double eff = eff_w * eff_k * eff_fill;
-    if (eff > best_eff + 1e-9) {
-      best_eff = eff;
+  long best_cost = -1;
+  for (int s = 1; s <= 8 && s <= nsb; ++s) {
+    const long ctas = (long)tiles * s;
+    const long rounds = (ctas + 3L * sms - 1) / (3L * sms);
+    const long cost = rounds * ((nsb + s - 1) / s + 2);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
       best = s;
     }
   }
@@ -200,7 +212,7 @@ int choose_ksplit(int tiles, int nsb, int slots) {
 
 template <int FMT>
 int launch_qgemv_mma_fmt(const void* W, int64_t N, int64_t K, const void* x, int xdt, int batch,
-                         float* y, cudaStream_t stream, int force_ksplit) {
+                         float* y, cudaStream_t stream, int force_ksplit, bool w_early) {
   using L = Layout<FMT>;
   GemvParams p;
   p.W = (const uint8_t*)W;
@@ -215,12 +227,13 @@ int launch_qgemv_mma_fmt(const void* W, int64_t N, int64_t K, const void* x, int
   p.x.rows = nullptr;
   p.batch = batch;
   p.y = y;
+  p.w_early = w_early ? 1 : 0;
   const int tiles = (int)((N + kTileRows - 1) / kTileRows);
   const int sms = device_sms();
   if (sms <= 0) return DQ_ERR_CUDA;
   // shared memory per CTA <= 56 KB so that four CTAs (20 warps) share an SM
   constexpr int kSmemBudget = 56 * 1024;
-  int ks = force_ksplit > 0 ? force_ksplit : choose_ksplit(tiles, p.nsb, 4 * sms);
+  int ks = force_ksplit > 0 ? force_ksplit : choose_ksplit(tiles, p.nsb, sms);
   ks = std::max(1, std::min(ks, std::min(8, p.nsb)));
   int nstage = 12;
   while (nstage > 3 && make_plan<FMT>(nstage, batch, ks).total > kSmemBudget) --nstage;
@@ -238,27 +251,19 @@ int launch_qgemv_mma_fmt(const void* W, int64_t N, int64_t K, const void* x, int
       return DQ_ERR_CUDA;
     if (dev < 64) attr_set[dev] = true;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)ks, (unsigned)tiles, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = (size_t)plan.total;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)ks;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, qgemv_mma_kernel<FMT>, p) != cudaSuccess) return DQ_ERR_CUDA;
+  if (launch_pdl(qgemv_mma_kernel<FMT>, dim3((unsigned)ks, (unsigned)tiles, 1), dim3(kThreads),
+                 (size_t)plan.total, stream, ks, p) != cudaSuccess)
+    return DQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
 }
 
 int launch_qgemv_mma(int fmt, const void* W, int64_t N, int64_t K, const void* x, int xdt,
-                     int batch, float* y, cudaStream_t s, int force_ksplit) {
-  if (fmt == DQ_Q4_K) return launch_qgemv_mma_fmt<DQ_Q4_K>(W, N, K, x, xdt, batch, y, s, force_ksplit);
-  if (fmt == DQ_Q6_K) return launch_qgemv_mma_fmt<DQ_Q6_K>(W, N, K, x, xdt, batch, y, s, force_ksplit);
-  return launch_qgemv_mma_fmt<DQ_Q8_0>(W, N, K, x, xdt, batch, y, s, force_ksplit);
+                     int batch, float* y, cudaStream_t s, int force_ksplit, bool w_early) {
+  if (fmt == DQ_Q4_K)
+    return launch_qgemv_mma_fmt<DQ_Q4_K>(W, N, K, x, xdt, batch, y, s, force_ksplit, w_early);
+  if (fmt == DQ_Q6_K)
+    return launch_qgemv_mma_fmt<DQ_Q6_K>(W, N, K, x, xdt, batch, y, s, force_ksplit, w_early);
+  return launch_qgemv_mma_fmt<DQ_Q8_0>(W, N, K, x, xdt, batch, y, s, force_ksplit, w_early);
 }
 
 }  // namespace dqmoe

@@ -14,16 +14,16 @@
 //     no value overflows fp16), writing it in a bank-skewed layout.
 //   * warps 1..4 are consumers, 16 rows each.  Lane (g = lane/4, t = lane%4)
 //     owns 64 weights of every super-block of rows g and g+8: it decodes them
-//     in registers to fp16 (magic-number nibble unpack, exact integer, then one
-//     fused scale/min per pair) straight into the A fragment of
+//     in registers to fp16 (exact integer unpack, then one fused scale/min per
+//     pair; Q4_K in per-row power-of-two units) straight into the A fragment of
 //     mma.m16n8k16 (rows = weights, k = 16 weights, n = 8 activation columns).
 //     Scales are folded into A, so the k order inside an mma is free; the
 //     activation B fragment is read in natural k order.
 //   * fp32 accumulators per stage are scaled by the column's inverse scale and
 //     summed into the running accumulator.
 //   * stages flow through full/empty mbarriers with bounded waits.
-// Arithmetic per weight: ~1.6 integer/half2 instructions (Q4_K); the tensor
-// core does the multiply-accumulate, so the loop stays HBM-bound at batch 1..8.
+// Arithmetic per weight: ~1.3 integer/half2 instructions (Q4_K); the tensor
+// core does the multiply-accumulate.
 #pragma once
 
 #include "common.cuh"
@@ -241,12 +241,33 @@ __device__ __forceinline__ void mma_x(float (&acc)[NT][2][4], int ch, uint32_t a
 template <int FMT>
 struct SBDot;
 
+// acc += (D0 + D1) * row scale * column scale for one 8-column tile: D0, D1
+// are the two accumulator chains of a super-block in row-scaled units (r0 for
+// row g, r8 for row g+8); c0, c1 undo the activation scale of columns 2t, 2t+1.
+__device__ __forceinline__ void fold_tile(float (&acc)[4], const float (&d)[2][4], float r0,
+                                          float r8, float c0, float c1) {
+  acc[0] = fmaf(d[0][0] + d[1][0], r0 * c0, acc[0]);
+  acc[1] = fmaf(d[0][1] + d[1][1], r0 * c1, acc[1]);
+  acc[2] = fmaf(d[0][2] + d[1][2], r8 * c0, acc[2]);
+  acc[3] = fmaf(d[0][3] + d[1][3], r8 * c1, acc[3]);
+}
+
 // Q4_K: lane t owns qs group t (bytes 32t..32t+31): sub-blocks 2t (low
 // nibbles) and 2t+1 (high nibbles), weights 64t + [0,64).
+//
+// Decode: a masked nibble pair, read as two fp16 bit patterns, is the exact
+// subnormal pair (q * 2^-24); one fp16 FMA then gives q * S + O with
+// S = sc * d * F and O = -m * dmin * F * 2^-24, F = 2^(24 - e) for e the larger
+// exponent field of d and dmin.  The A operand is therefore the weight times
+// the power of two 2^-e, normal and within fp16 range for any d, dmin, and the
+// fp32 result of the super-block is multiplied back by 2^e (rinv).  One integer
+// AND and one FMA per weight pair, no magic-number subtraction.
 template <>
 struct SBDot<DQ_Q4_K> {
+  static constexpr bool kRowScale = true;
+
   __device__ __forceinline__ static void scales(uint4 hd, int t, __half2& slo, __half2& olo,
-                                                __half2& shi, __half2& ohi) {
+                                                __half2& shi, __half2& ohi, float& rinv) {
     const int jj = 2 * (t & 1);
     const uint32_t sel = (uint32_t)jj | (4u << 4) | ((uint32_t)(jj + 1) << 8) | (4u << 12);
     const uint32_t hy = __byte_perm(hd.y, 0, sel);
@@ -262,31 +283,70 @@ struct SBDot<DQ_Q4_K> {
     }
     const __half2 magic = u32_as_h2(0x64006400u);
     const __half2 sch = __hsub2(u32_as_h2(sc | 0x64006400u), magic);   // exact ints
-    const __half2 mnh = __hsub2(u32_as_h2(mn | 0x64006400u), magic);
-    const __half2 d2 = __half2half2(__ushort_as_half((unsigned short)(hd.x & 0xFFFF)));
-    const __half2 dm2 = __half2half2(__hneg(__ushort_as_half((unsigned short)(hd.x >> 16))));
-    const __half2 s = __hmul2(d2, sch);      // (d*sc_lo, d*sc_hi)
-    const __half2 o = __hmul2(dm2, mnh);     // (-dmin*m_lo, -dmin*m_hi)
+    const float2 mnf = __half22float2(__hsub2(u32_as_h2(mn | 0x64006400u), magic));
+    // e: larger biased exponent field of d and dmin (0 when both are
+    // subnormal or zero: then F = 2^24 maps d = k * 2^-24 to the integer k)
+    const uint32_t e = max(hd.x & 0x7C00u, (hd.x >> 16) & 0x7C00u) >> 10;
+    const float F = __uint_as_float((151u - e) << 23);     // 2^(24 - e)
+    const float Fm = __uint_as_float((127u - e) << 23);    // 2^-e = F * 2^-24
+    rinv = __uint_as_float((127u + e) << 23);              // 2^e
+    // d * F < 1024: exact in fp16; sc * d * F <= 63 * 1023.5 < 65504
+    const float df = __half2float(__ushort_as_half((unsigned short)(hd.x & 0xFFFF))) * F;
+    const float dm = -__half2float(__ushort_as_half((unsigned short)(hd.x >> 16))) * Fm;
+    const __half2 s = __hmul2(__float2half2_rn(df), sch);   // (S_lo, S_hi)
+    const __half2 o = __floats2half2_rn(mnf.x * dm, mnf.y * dm);
     slo = __low2half2(s);
     olo = __low2half2(o);
     shi = __hmul2(__high2half2(s), __float2half2_rn(0.0625f));   // high nibbles carry x16
     ohi = __high2half2(o);
   }
 
+  // Absolute scales for decoding real fp16 weights (the tensor-core prefill
+  // tiles, whose K runs across super-blocks): (d*sc, -dmin*m) of sub-blocks
+  // 2t (lo) and 2t+1 (hi, with the x16 of high nibbles folded in).
+  __device__ __forceinline__ static void scales_abs(uint4 hd, int t, __half2& slo, __half2& olo,
+                                                    __half2& shi, __half2& ohi) {
+    const int jj = 2 * (t & 1);
+    const uint32_t sel = (uint32_t)jj | (4u << 4) | ((uint32_t)(jj + 1) << 8) | (4u << 12);
+    const uint32_t hy = __byte_perm(hd.y, 0, sel);
+    const uint32_t hz = __byte_perm(hd.z, 0, sel);
+    const uint32_t hw = __byte_perm(hd.w, 0, sel);
+    uint32_t sc, mn;
+    if (t < 2) {
+      sc = hy & 0x003F003Fu;
+      mn = hz & 0x003F003Fu;
+    } else {
+      sc = (hw & 0x000F000Fu) | ((hy >> 2) & 0x00300030u);
+      mn = ((hw >> 4) & 0x000F000Fu) | ((hz >> 2) & 0x00300030u);
+    }
+    const __half2 magic = u32_as_h2(0x64006400u);
+    const __half2 sch = __hsub2(u32_as_h2(sc | 0x64006400u), magic);
+    const __half2 mnh = __hsub2(u32_as_h2(mn | 0x64006400u), magic);
+    const __half2 d2 = __half2half2(__ushort_as_half((unsigned short)(hd.x & 0xFFFF)));
+    const __half2 dm2 = __half2half2(__hneg(__ushort_as_half((unsigned short)(hd.x >> 16))));
+    const __half2 s = __hmul2(d2, sch);
+    const __half2 o = __hmul2(dm2, mnh);
+    slo = __low2half2(s);
+    olo = __low2half2(o);
+    shi = __hmul2(__high2half2(s), __float2half2_rn(0.0625f));
+    ohi = __high2half2(o);
+  }
+
+  // acc: this super-block's products in units of 2^-e per row (rows g and
+  // g+8: r0, r8 = 2^e of each row's super-block).
   template <int NT>
   __device__ __forceinline__ static void run(uint32_t wrow, int pitch8,
                                              const uint32_t (&xcol)[NT], int kb, int t,
-                                             float (&acc)[NT][2][4]) {
-    const uint32_t r0 = wrow, r8 = wrow + pitch8;
-    const uint4 h0 = lds_u128(r0), h8 = lds_u128(r8);
+                                             float (&acc)[NT][2][4], float& r0, float& r8) {
+    const uint32_t ra = wrow, rb = wrow + pitch8;
+    const uint4 h0 = lds_u128(ra), h8 = lds_u128(rb);
     __half2 s0l, o0l, s0h, o0h, s8l, o8l, s8h, o8h;
-    scales(h0, t, s0l, o0l, s0h, o0h);
-    scales(h8, t, s8l, o8l, s8h, o8h);
-    const uint4 qa0 = lds_u128(r0 + 16 + 32 * t), qb0 = lds_u128(r0 + 32 + 32 * t);
-    const uint4 qa8 = lds_u128(r8 + 16 + 32 * t), qb8 = lds_u128(r8 + 32 + 32 * t);
+    scales(h0, t, s0l, o0l, s0h, o0h, r0);
+    scales(h8, t, s8l, o8l, s8h, o8h, r8);
+    const uint4 qa0 = lds_u128(ra + 16 + 32 * t), qb0 = lds_u128(ra + 32 + 32 * t);
+    const uint4 qa8 = lds_u128(rb + 16 + 32 * t), qb8 = lds_u128(rb + 32 + 32 * t);
     const uint32_t q0[8] = {qa0.x, qa0.y, qa0.z, qa0.w, qb0.x, qb0.y, qb0.z, qb0.w};
     const uint32_t q8[8] = {qa8.x, qa8.y, qa8.z, qa8.w, qb8.x, qb8.y, qb8.z, qb8.w};
-    const __half2 magic = u32_as_h2(0x64006400u);
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
       // bytes (b0 b1 b2 b3) -> (b0 b2 b1 b3): 16-bit lanes hold weights k, k+1
@@ -295,18 +355,18 @@ struct SBDot<DQ_Q4_K> {
       const int k = kb + 64 * t + 4 * s;
       // low nibbles: weights k..k+3 (sub-block 2t)
       {
-        const uint32_t a0 = h2_as_u32(__hfma2(__hsub2(u32_as_h2(lop3_and_or(p0, 0x000F000Fu, 0x64006400u)), magic), s0l, o0l));
-        const uint32_t a1 = h2_as_u32(__hfma2(__hsub2(u32_as_h2(lop3_and_or(p8, 0x000F000Fu, 0x64006400u)), magic), s8l, o8l));
-        const uint32_t a2 = h2_as_u32(__hfma2(__hsub2(u32_as_h2(lop3_and_or(p0s, 0x000F000Fu, 0x64006400u)), magic), s0l, o0l));
-        const uint32_t a3 = h2_as_u32(__hfma2(__hsub2(u32_as_h2(lop3_and_or(p8s, 0x000F000Fu, 0x64006400u)), magic), s8l, o8l));
+        const uint32_t a0 = h2_as_u32(__hfma2(u32_as_h2(p0 & 0x000F000Fu), s0l, o0l));
+        const uint32_t a1 = h2_as_u32(__hfma2(u32_as_h2(p8 & 0x000F000Fu), s8l, o8l));
+        const uint32_t a2 = h2_as_u32(__hfma2(u32_as_h2(p0s & 0x000F000Fu), s0l, o0l));
+        const uint32_t a3 = h2_as_u32(__hfma2(u32_as_h2(p8s & 0x000F000Fu), s8l, o8l));
         mma_x<NT>(acc, 0, a0, a1, a2, a3, xcol, k);
       }
       // high nibbles: weights k+32..k+35 (sub-block 2t+1), value 16*q
       {
-        const uint32_t a0 = h2_as_u32(__hfma2(__hsub2(u32_as_h2(lop3_and_or(p0, 0x00F000F0u, 0x64006400u)), magic), s0h, o0h));
-        const uint32_t a1 = h2_as_u32(__hfma2(__hsub2(u32_as_h2(lop3_and_or(p8, 0x00F000F0u, 0x64006400u)), magic), s8h, o8h));
-        const uint32_t a2 = h2_as_u32(__hfma2(__hsub2(u32_as_h2(lop3_and_or(p0s, 0x00F000F0u, 0x64006400u)), magic), s0h, o0h));
-        const uint32_t a3 = h2_as_u32(__hfma2(__hsub2(u32_as_h2(lop3_and_or(p8s, 0x00F000F0u, 0x64006400u)), magic), s8h, o8h));
+        const uint32_t a0 = h2_as_u32(__hfma2(u32_as_h2(p0 & 0x00F000F0u), s0h, o0h));
+        const uint32_t a1 = h2_as_u32(__hfma2(u32_as_h2(p8 & 0x00F000F0u), s8h, o8h));
+        const uint32_t a2 = h2_as_u32(__hfma2(u32_as_h2(p0s & 0x00F000F0u), s0h, o0h));
+        const uint32_t a3 = h2_as_u32(__hfma2(u32_as_h2(p8s & 0x00F000F0u), s8h, o8h));
         mma_x<NT>(acc, 1, a0, a1, a2, a3, xcol, k + 32);
       }
     }
@@ -318,6 +378,7 @@ struct SBDot<DQ_Q4_K> {
 // Blocks are 210 bytes, so every other block is only 2-byte aligned.
 template <>
 struct SBDot<DQ_Q6_K> {
+  static constexpr bool kRowScale = false;
   __device__ __forceinline__ static uint32_t q6_pair(uint32_t nib, uint32_t hq) {
     // nib: 4-bit values in bits 0-3 of each 16-bit lane; hq: 2-bit values
     // already in bits 4-5.  Returns fp16 pair of (q - 32), exact.
@@ -391,6 +452,7 @@ struct SBDot<DQ_Q6_K> {
 // quants 8t..8t+7 of each block.
 template <>
 struct SBDot<DQ_Q8_0> {
+  static constexpr bool kRowScale = false;
   template <int NT>
   __device__ __forceinline__ static void run(uint32_t wrow, int pitch8,
                                              const uint32_t (&xcol)[NT], int kb, int t,

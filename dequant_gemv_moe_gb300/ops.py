@@ -42,13 +42,24 @@ def dequant(fmt, blocks, n_weights, out=None):
     return out
 
 
-def qgemv(fmt, W, N, K, x, y=None, ksplit=None):
-    """y[b][n] = sum_k W[n][k] x[b][k]; x is [batch][K] (float32/float16/bfloat16)."""
+QGEMV_WEIGHTS_EARLY = 1
+
+
+def qgemv(fmt, W, N, K, x, y=None, ksplit=None, weights_early=False):
+    """y[b][n] = sum_k W[n][k] x[b][k]; x is [batch][K] (float32/float16/bfloat16).
+
+    weights_early: W is not written by the kernel issued just before on the
+    stream, so its first stages may stream in while that kernel drains
+    (dq_qgemv_ex with DQ_QGEMV_WEIGHTS_EARLY).
+    """
     x = x.reshape(-1, K)
     batch = x.shape[0]
     if y is None:
         y = torch.empty(batch, N, dtype=torch.float32, device=x.device)
-    if ksplit is None:
+    if weights_early:
+        _call("dq_qgemv_ex", fmt, _ptr(W), N, K, _ptr(x), _dtype_code(x), batch, _ptr(y),
+              int(ksplit or 0), QGEMV_WEIGHTS_EARLY, _stream())
+    elif ksplit is None:
         _call("dq_qgemv", fmt, _ptr(W), N, K, _ptr(x), _dtype_code(x), batch, _ptr(y), _stream())
     else:
         _call("dq_qgemv_ksplit", fmt, _ptr(W), N, K, _ptr(x), _dtype_code(x), batch, _ptr(y),

@@ -145,6 +145,26 @@ int dq_qgemv(int fmt, const void* W, int64_t N, int64_t K, const void* x,
 int dq_qgemv_ksplit(int fmt, const void* W, int64_t N, int64_t K, const void* x,
                     int x_dtype, int batch, float* y, int ksplit, void* stream);
 
+/* Flags of dq_qgemv_ex. */
+#define DQ_QGEMV_WEIGHTS_EARLY 1u
+/* dq_qgemv_ex — dq_qgemv with the K split (0 = library's choice, as
+ * dq_qgemv_ksplit) and flags.
+ *   DQ_QGEMV_WEIGHTS_EARLY: the caller guarantees that W is not written by
+ *     the kernel issued just before this call on `stream` (weights are
+ *     loaded once and stay read-only, as in decode).  The kernel then starts
+ *     streaming its first weight stages while that kernel is still finishing
+ *     (programmatic dependent launch), hiding the start-up latency of a chain
+ *     of GEMVs.  x and y are still ordered after the previous kernel.
+ *     Ignored for fp32 activations.
+ * Every kernel of this library is launched as a programmatic dependent
+ * launch: it may be scheduled while the previous kernel in the stream drains,
+ * and waits for that kernel's completion before it reads any input other than
+ * W under DQ_QGEMV_WEIGHTS_EARLY, or writes any output.
+ * Errors: as dq_qgemv_ksplit, plus DQ_ERR_ARG for unknown flag bits. */
+int dq_qgemv_ex(int fmt, const void* W, int64_t N, int64_t K, const void* x,
+                int x_dtype, int batch, float* y, int ksplit, unsigned flags,
+                void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Sparse MoE layer.                                                         */
 /*   logits[t][e] = sum_h router_W[e][h] * x[t][h]            (fp32)         */

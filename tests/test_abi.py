@@ -56,6 +56,17 @@ def test_qgemv_argument_errors_without_launch(so):
     assert f(1, a, 0, 256, a, 1, 1, a, None) == -1             # N = 0
 
 
+def test_qgemv_ex_argument_errors_without_launch(so):
+    f = so.dq_qgemv_ex
+    P, I, L, U = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint
+    f.argtypes = [I, P, L, L, P, I, I, P, I, U, P]
+    a = P(4096)
+    assert f(1, a, 64, 256, a, 1, 1, a, 0, 2, None) == -1      # unknown flag bit
+    assert f(1, a, 64, 256, a, 1, 1, a, 9, 1, None) == -1      # ksplit > 8
+    assert f(1, a, 64, 256, a, 1, 1, a, -1, 0, None) == -1     # ksplit < 0
+    assert f(1, P(4097), 64, 256, a, 1, 1, a, 0, 1, None) == -2  # misaligned W
+
+
 def test_dequant_argument_errors(so):
     f = so.dq_dequant
     P = ctypes.c_void_p

@@ -120,3 +120,66 @@ def test_llama70b_linears(dq, orc, fmt, name, N, K, B):
     err = _case(dq, orc, fmt, N, K, B, 1, seed=synth.BASE_SEED + 2, rows=rows)
     assert err <= TOL[1], err
     torch.cuda.empty_cache()
+
+
+def _set_q4k_scales(W, N, K, d, dmin):
+    """Overwrite d and dmin of every Q4_K super-block of row r with d[r], dmin[r]."""
+    blocks = W.reshape(N, K // 256, 144)
+    dh = np.asarray(d, dtype=np.float16).view(np.uint8).reshape(N, 1, 2)
+    mh = np.asarray(dmin, dtype=np.float16).view(np.uint8).reshape(N, 1, 2)
+    blocks[:, :, 0:2] = dh
+    blocks[:, :, 2:4] = mh
+    return blocks.reshape(-1)
+
+
+@pytest.mark.parametrize("xdt", [1, 2])
+def test_q4k_scale_regimes(dq, orc, xdt):
+    # the tensor-core path normalises each super-block by a power of two taken
+    # from the exponents of d and dmin: every regime of the two fp16 scales
+    # (subnormal, zero, negative, near the fp16 maximum, very unequal) must
+    # keep every row within its own error bound
+    regimes = [(1e-2, 1e-2), (2.0 ** -24, 0.0), (3e-6, 5e-6), (0.0, 1e-3), (1e-3, 0.0),
+               (6.0e4, 6.0e4), (-1e-2, 1e-2), (1e-4, 10.0), (10.0, 1e-7), (0.0, 0.0)]
+    per = 13
+    N, K, B = per * len(regimes), 2048, 3
+    d = np.repeat([r[0] for r in regimes], per)
+    dmin = np.repeat([r[1] for r in regimes], per)
+    g = synth.streams(4242 + xdt, 2)
+    W = _set_q4k_scales(synth.quant_matrix(g[0], Q4_K, N, K), N, K, d, dmin)
+    x = synth.activations(g[1], (B, K), xdt)
+    y = dq.qgemv(Q4_K, dev_bytes(W), N, K, dev_act(x, xdt)).cpu().numpy().astype(np.float64)
+    assert dq.device_status() == 0
+    ref = orc.qgemv(Q4_K, W, N, K, x, xdt, B)
+    wabs = np.abs(orc.dequant(Q4_K, W, N * K).reshape(N, K).astype(np.float64))
+    xabs = np.abs(orc.act_to_f64(xdt, x).reshape(B, K))
+    scale = xabs @ wabs.T                     # sum_k |w x| per output
+    zero = scale == 0
+    assert np.all(y[zero] == 0)
+    rel = np.abs(y - ref)[~zero] / scale[~zero]
+    assert rel.max() <= 1e-3, rel.max()
+
+
+def test_qgemv_weights_early_and_chains(dq, orc):
+    # DQ_QGEMV_WEIGHTS_EARLY: same result; and every kernel orders its reads
+    # of x after the kernel before it, whether that is one of this library's
+    # kernels (fp32 path reading y1) or a PyTorch kernel (the fp16 cast)
+    g = synth.streams(9090, 4)
+    N1, K1, N2 = 512, 4096, 200
+    W1 = synth.quant_matrix(g[0], Q4_K, N1, K1)
+    W2 = synth.quant_matrix(g[1], Q4_K, N2, N1)
+    W3 = synth.quant_matrix(g[2], Q8_0, N2, N1)
+    x1 = synth.activations(g[3], (2, K1), 1)
+    dW1, dW2, dW3 = dev_bytes(W1), dev_bytes(W2), dev_bytes(W3)
+    dx1 = dev_act(x1, 1)
+    for early in (False, True):
+        y1 = dq.qgemv(Q4_K, dW1, N1, K1, dx1, weights_early=early)
+        y2 = dq.qgemv(Q4_K, dW2, N2, N1, y1, weights_early=early)             # fp32 path
+        x3 = y1.half()
+        y3 = dq.qgemv(Q8_0, dW3, N2, N1, x3, weights_early=early)             # fp16 path
+        torch.cuda.synchronize()
+        assert dq.device_status() == 0
+        y1h = y1.cpu().numpy()
+        assert rel_err(y1h, orc.qgemv(Q4_K, W1, N1, K1, x1, 1, 2)) <= TOL[1]
+        assert rel_err(y2.cpu().numpy(), orc.qgemv(Q4_K, W2, N2, N1, y1h, 0, 2)) <= TOL[0]
+        x3h = x3.cpu().numpy()
+        assert rel_err(y3.cpu().numpy(), orc.qgemv(Q8_0, W3, N2, N1, x3h, 1, 2)) <= TOL[1]
