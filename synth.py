@@ -82,6 +82,11 @@ def router_weights(rng, E, H):
 LLAMA8B_LINEARS = [("q", 4096, 4096), ("k", 1024, 4096), ("v", 1024, 4096),
                    ("o", 4096, 4096), ("gate", 14336, 4096), ("up", 14336, 4096),
                    ("down", 4096, 14336)]
+# the same matrices as inference engines store them: q, k, v stacked into one
+# [6144 x 4096] matrix and gate, up into one [28672 x 4096] matrix (identical
+# bytes and products; four GEMV launches per layer instead of seven)
+LLAMA8B_MERGED = [("qkv", 6144, 4096), ("o", 4096, 4096), ("gate_up", 28672, 4096),
+                  ("down", 4096, 14336)]
 LLAMA70B_LINEARS = [("gate", 28672, 8192), ("up", 28672, 8192),
                     ("down", 8192, 28672), ("q", 8192, 8192)]
 
