@@ -60,6 +60,12 @@ def run_case(args):
                                                         with_e2e=False).items()}))
     elif args.case == "mixtral":
         print(json.dumps(bench_moe(torch, dq, synth.MOE_MIXTRAL, 16, reps=max(1, args.steps))))
+    elif args.case == "prefill32":
+        # DeepSeek-V3 expert shapes with 32 routed experts (+1 shared), T = 256:
+        # ~64 tokens per expert, every expert on the tcgen05 grouped GEMM; 0.8 GB
+        # of weights (a small case for full ncu captures of that kernel)
+        cfg = dict(synth.MOE_DEEPSEEK, E=32)
+        print(json.dumps(bench_moe(torch, dq, cfg, 256, reps=max(1, args.steps))))
     elif args.case.startswith("deepseek"):
         T = int(args.case[len("deepseek"):])
         print(json.dumps(bench_moe(torch, dq, synth.MOE_DEEPSEEK, T, reps=max(1, args.steps))))
