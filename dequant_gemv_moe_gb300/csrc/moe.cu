@@ -33,10 +33,16 @@ static size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 // an expert with more than kWide tokens is computed by the tcgen05 GEMM
 constexpr int kWide = 32;
 
+// up to kRouterStreamT tokens the router streams W_r in hidden chunks of
+// kRouterChunk (one warp per expert row and chunk); beyond, it tiles
+constexpr int kRouterStreamT = 8;
+constexpr int kRouterChunk = 1024;
+
 MoePlan moe_plan(const dq_moe_desc& d, int T) {
   MoePlan p;
   const int tiles = ((d.E + 63) / 64) * ((T + 31) / 32);
-  p.KS = std::max(1, std::min(d.hidden / 256, (320 + tiles - 1) / tiles));
+  p.KS = T <= kRouterStreamT ? (d.hidden + kRouterChunk - 1) / kRouterChunk
+                             : std::max(1, std::min(d.hidden / 256, (320 + tiles - 1) / tiles));
   p.P = (int64_t)T * d.top_k;
   p.NP = p.P + (int64_t)d.n_shared * T;
   // group width from the expected tokens per routed expert (uniform routing):
@@ -135,6 +141,54 @@ __global__ void __launch_bounds__(128) router_logits_kernel(const float* __restr
     for (int b = 0; b < 4; ++b) {
       const int e = e0 + tx * 4 + b;
       if (e < E) part[((int64_t)ks * T + t) * E + e] = acc[a][b];
+    }
+  }
+}
+
+// Few tokens (T <= 8): the router is a GEMV over the 7.3 MB of W_r (DeepSeek);
+// warp w of CTA (b, ks) streams expert row 8b + w over hidden chunk ks with
+// 16-byte loads against the chunk of every token's x, staged once per CTA in
+// shared memory, and writes part[ks][t][e] like the tiled kernel.
+__global__ void __launch_bounds__(256) router_stream_kernel(const float* __restrict__ Wr, int E,
+                                                            int H, const void* __restrict__ x,
+                                                            int xdt, int T,
+                                                            float* __restrict__ part) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ __align__(16) float xs[kRouterStreamT][kRouterChunk];
+  const int ks = blockIdx.y, h0 = ks * kRouterChunk;
+  const int n = min(kRouterChunk, H - h0);          // multiple of 32
+  for (int i = threadIdx.x; i < T * n; i += blockDim.x) {
+    const int t = i / n, h = i - t * n;
+    xs[t][h] = act_f32(x, xdt, (int64_t)t * H + h0 + h);
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 8 + warp;
+  if (e >= E) return;
+  const float4* w = (const float4*)(Wr + (int64_t)e * H + h0);
+  float acc[kRouterStreamT] = {};
+#pragma unroll 4
+  for (int j = lane; j < n / 4; j += 32) {
+    const float4 wv = __ldcs(w + j);
+#pragma unroll
+    for (int t = 0; t < kRouterStreamT; ++t) {
+      if (t < T) {
+        const float4 xv = *(const float4*)&xs[t][4 * j];
+        acc[t] = fmaf(wv.x, xv.x, acc[t]);
+        acc[t] = fmaf(wv.y, xv.y, acc[t]);
+        acc[t] = fmaf(wv.z, xv.z, acc[t]);
+        acc[t] = fmaf(wv.w, xv.w, acc[t]);
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < kRouterStreamT; ++t) {
+    if (t < T) {
+      float v = acc[t];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0) part[((int64_t)ks * T + t) * E + e] = v;
     }
   }
 }
@@ -490,8 +544,8 @@ __global__ void __launch_bounds__(kThreads) grouped_kernel(const __grid_constant
           for (int j = 0; j < ncs; ++j) {
             float d[NT][2][4] = {};
             float r0, r8;
-            SBDot<FMT>::template run<NT>(wst + j * L::SBB, 8 * L::ROW_PITCH, xcol, j * 256, t, d,
-                                         r0, r8);
+            SBDot<FMT>::template run<NT, true>(wst + j * L::SBB, 8 * L::ROW_PITCH, xcol, j * 256,
+                                               t, d, r0, r8);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
               const float c0 = f16 ? 1.f : xinv[s * NC + 8 * nt + 2 * t];
@@ -698,8 +752,14 @@ int launch_swiglu_wide(const int4* units, const int* n_units, int max_units, con
 
 int launch_router(const float* Wr, int E, int H, const void* x, int xdt, int T, int top_k,
                   int KS, float* part, float* logits, int32_t* idx, float* gate, cudaStream_t s) {
-  dim3 g1((unsigned)((E + 63) / 64), (unsigned)((T + 31) / 32), (unsigned)KS);
-  launch_pdl(router_logits_kernel, dim3(g1), dim3(128), 0, s, 0, Wr, E, H, x, xdt, T, KS, part);
+  if (T <= kRouterStreamT && KS == (H + kRouterChunk - 1) / kRouterChunk && KS > 1 &&
+      ((uintptr_t)Wr & 15) == 0 && H % 4 == 0) {
+    const dim3 g((unsigned)((E + 7) / 8), (unsigned)KS);
+    launch_pdl(router_stream_kernel, g, dim3(256), 0, s, 0, Wr, E, H, x, xdt, T, part);
+  } else {
+    dim3 g1((unsigned)((E + 63) / 64), (unsigned)((T + 31) / 32), (unsigned)KS);
+    launch_pdl(router_logits_kernel, dim3(g1), dim3(128), 0, s, 0, Wr, E, H, x, xdt, T, KS, part);
+  }
   if (cudaGetLastError() != cudaSuccess) return DQ_ERR_CUDA;
   launch_pdl(topk_kernel, dim3((unsigned)((T + 7) / 8)), dim3(256), 0, s, 0, part, KS, T, E, top_k, logits, idx, gate);
   return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;

@@ -333,8 +333,10 @@ struct SBDot<DQ_Q4_K> {
   }
 
   // acc: this super-block's products in units of 2^-e per row (rows g and
-  // g+8: r0, r8 = 2^e of each row's super-block).
-  template <int NT>
+  // g+8: r0, r8 = 2^e of each row's super-block).  PAIRX: fetch the B
+  // fragments of two consecutive steps with one 16-byte load (faster in the
+  // grouped kernel, slower in the single-matrix one, measured on GB300).
+  template <int NT, bool PAIRX = false>
   __device__ __forceinline__ static void run(uint32_t wrow, int pitch8,
                                              const uint32_t (&xcol)[NT], int kb, int t,
                                              float (&acc)[NT][2][4], float& r0, float& r8) {
@@ -343,31 +345,78 @@ struct SBDot<DQ_Q4_K> {
     __half2 s0l, o0l, s0h, o0h, s8l, o8l, s8h, o8h;
     scales(h0, t, s0l, o0l, s0h, o0h, r0);
     scales(h8, t, s8l, o8l, s8h, o8h, r8);
-    const uint4 qa0 = lds_u128(ra + 16 + 32 * t), qb0 = lds_u128(ra + 32 + 32 * t);
-    const uint4 qa8 = lds_u128(rb + 16 + 32 * t), qb8 = lds_u128(rb + 32 + 32 * t);
+    const uint32_t qa = ra + 16 + 32 * t;      // this lane's 32 quant bytes of row g
+    const uint4 qa0 = lds_u128(qa), qb0 = lds_u128(qa + 16);
+    const uint4 qa8 = lds_u128(qa + pitch8), qb8 = lds_u128(qa + pitch8 + 16);
     const uint32_t q0[8] = {qa0.x, qa0.y, qa0.z, qa0.w, qb0.x, qb0.y, qb0.z, qb0.w};
     const uint32_t q8[8] = {qa8.x, qa8.y, qa8.z, qa8.w, qb8.x, qb8.y, qb8.z, qb8.w};
+    if constexpr (PAIRX) {
+      // activation kb + 64t + c (c < 64) of a tile sits at xb + 2c: the B
+      // fragments of two consecutive steps come from one 16-byte load
+      uint32_t xb[NT];
 #pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      // bytes (b0 b1 b2 b3) -> (b0 b2 b1 b3): 16-bit lanes hold weights k, k+1
-      const uint32_t p0 = __byte_perm(q0[s], 0, 0x3120), p8 = __byte_perm(q8[s], 0, 0x3120);
-      const uint32_t p0s = p0 >> 8, p8s = p8 >> 8;
-      const int k = kb + 64 * t + 4 * s;
-      // low nibbles: weights k..k+3 (sub-block 2t)
-      {
-        const uint32_t a0 = h2_as_u32(__hfma2(u32_as_h2(p0 & 0x000F000Fu), s0l, o0l));
-        const uint32_t a1 = h2_as_u32(__hfma2(u32_as_h2(p8 & 0x000F000Fu), s8l, o8l));
-        const uint32_t a2 = h2_as_u32(__hfma2(u32_as_h2(p0s & 0x000F000Fu), s0l, o0l));
-        const uint32_t a3 = h2_as_u32(__hfma2(u32_as_h2(p8s & 0x000F000Fu), s8l, o8l));
-        mma_x<NT>(acc, 0, a0, a1, a2, a3, xcol, k);
+      for (int nt = 0; nt < NT; ++nt) xb[nt] = xcol[nt] + 2 * xoff(kb + 64 * t);
+#pragma unroll
+      for (int sp = 0; sp < 4; ++sp) {
+        uint4 xl[NT], xh[NT];                      // steps 2sp, 2sp+1: low / high nibbles
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          xl[nt] = lds_u128(xb[nt] + 16 * sp);
+          xh[nt] = lds_u128(xb[nt] + 16 * sp + 64);
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int s = 2 * sp + h;
+          // bytes (b0 b1 b2 b3) -> (b0 b2 b1 b3): 16-bit lanes hold weights k, k+1
+          const uint32_t p0 = __byte_perm(q0[s], 0, 0x3120), p8 = __byte_perm(q8[s], 0, 0x3120);
+          const uint32_t p0s = p0 >> 8, p8s = p8 >> 8;
+          // low nibbles: weights kb + 64t + 4s + 0..3 (sub-block 2t)
+          {
+            const uint32_t a0 = h2_as_u32(__hfma2(u32_as_h2(p0 & 0x000F000Fu), s0l, o0l));
+            const uint32_t a1 = h2_as_u32(__hfma2(u32_as_h2(p8 & 0x000F000Fu), s8l, o8l));
+            const uint32_t a2 = h2_as_u32(__hfma2(u32_as_h2(p0s & 0x000F000Fu), s0l, o0l));
+            const uint32_t a3 = h2_as_u32(__hfma2(u32_as_h2(p8s & 0x000F000Fu), s8l, o8l));
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              mma_16816(acc[nt][0], a0, a1, a2, a3, h ? xl[nt].z : xl[nt].x,
+                        h ? xl[nt].w : xl[nt].y);
+          }
+          // high nibbles: 32 weights further (sub-block 2t+1), value 16*q
+          {
+            const uint32_t a0 = h2_as_u32(__hfma2(u32_as_h2(p0 & 0x00F000F0u), s0h, o0h));
+            const uint32_t a1 = h2_as_u32(__hfma2(u32_as_h2(p8 & 0x00F000F0u), s8h, o8h));
+            const uint32_t a2 = h2_as_u32(__hfma2(u32_as_h2(p0s & 0x00F000F0u), s0h, o0h));
+            const uint32_t a3 = h2_as_u32(__hfma2(u32_as_h2(p8s & 0x00F000F0u), s8h, o8h));
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              mma_16816(acc[nt][1], a0, a1, a2, a3, h ? xh[nt].z : xh[nt].x,
+                        h ? xh[nt].w : xh[nt].y);
+          }
+        }
       }
-      // high nibbles: weights k+32..k+35 (sub-block 2t+1), value 16*q
-      {
-        const uint32_t a0 = h2_as_u32(__hfma2(u32_as_h2(p0 & 0x00F000F0u), s0h, o0h));
-        const uint32_t a1 = h2_as_u32(__hfma2(u32_as_h2(p8 & 0x00F000F0u), s8h, o8h));
-        const uint32_t a2 = h2_as_u32(__hfma2(u32_as_h2(p0s & 0x00F000F0u), s0h, o0h));
-        const uint32_t a3 = h2_as_u32(__hfma2(u32_as_h2(p8s & 0x00F000F0u), s8h, o8h));
-        mma_x<NT>(acc, 1, a0, a1, a2, a3, xcol, k + 32);
+    } else {
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        // bytes (b0 b1 b2 b3) -> (b0 b2 b1 b3): 16-bit lanes hold weights k, k+1
+        const uint32_t p0 = __byte_perm(q0[s], 0, 0x3120), p8 = __byte_perm(q8[s], 0, 0x3120);
+        const uint32_t p0s = p0 >> 8, p8s = p8 >> 8;
+        const int k = kb + 64 * t + 4 * s;
+        // low nibbles: weights k..k+3 (sub-block 2t)
+        {
+          const uint32_t a0 = h2_as_u32(__hfma2(u32_as_h2(p0 & 0x000F000Fu), s0l, o0l));
+          const uint32_t a1 = h2_as_u32(__hfma2(u32_as_h2(p8 & 0x000F000Fu), s8l, o8l));
+          const uint32_t a2 = h2_as_u32(__hfma2(u32_as_h2(p0s & 0x000F000Fu), s0l, o0l));
+          const uint32_t a3 = h2_as_u32(__hfma2(u32_as_h2(p8s & 0x000F000Fu), s8l, o8l));
+          mma_x<NT>(acc, 0, a0, a1, a2, a3, xcol, k);
+        }
+        // high nibbles: weights k+32..k+35 (sub-block 2t+1), value 16*q
+        {
+          const uint32_t a0 = h2_as_u32(__hfma2(u32_as_h2(p0 & 0x00F000F0u), s0h, o0h));
+          const uint32_t a1 = h2_as_u32(__hfma2(u32_as_h2(p8 & 0x00F000F0u), s8h, o8h));
+          const uint32_t a2 = h2_as_u32(__hfma2(u32_as_h2(p0s & 0x00F000F0u), s0h, o0h));
+          const uint32_t a3 = h2_as_u32(__hfma2(u32_as_h2(p8s & 0x00F000F0u), s8h, o8h));
+          mma_x<NT>(acc, 1, a0, a1, a2, a3, xcol, k + 32);
+        }
       }
     }
   }
