@@ -332,6 +332,33 @@ struct SBDot<DQ_Q4_K> {
     ohi = __high2half2(o);
   }
 
+  // A fragments of one step: words w0 (row g) and w8 (row g+8) hold bytes
+  // b0..b3 = weights 4s..4s+3 of sub-block 2t (low nibbles) and 2t+1 (high).
+  // lo / hi: the fragments of the low / high nibbles, weights in k order.
+  // s*h is the high sub-block's S/16 (the scale of 16*q).
+  __device__ __forceinline__ static void frags(uint32_t w0, uint32_t w8, __half2 s0l, __half2 o0l,
+                                               __half2 s0h, __half2 o0h, __half2 s8l,
+                                               __half2 o8l, __half2 s8h, __half2 o8h,
+                                               uint32_t (&lo)[4], uint32_t (&hi)[4]) {
+    // whole bytes in 16-bit lanes: (b0, b1) and (b2, b3), each the exact
+    // subnormal (lo + 16 hi) * 2^-24.  The low term is one AND and one HFMA2;
+    // the high term s_h * (b - lo) + o_h takes two HFMA2 and no mask, which
+    // moves work from the integer pipe (the busier one) to the fp16 pipe.
+    const uint32_t r0 = __byte_perm(w0, 0, 0x4140), r0s = __byte_perm(w0, 0, 0x4342);
+    const uint32_t r8 = __byte_perm(w8, 0, 0x4140), r8s = __byte_perm(w8, 0, 0x4342);
+    const uint32_t l0 = r0 & 0x000F000Fu, l0s = r0s & 0x000F000Fu;
+    const uint32_t l8 = r8 & 0x000F000Fu, l8s = r8s & 0x000F000Fu;
+    lo[0] = h2_as_u32(__hfma2(u32_as_h2(l0), s0l, o0l));
+    lo[1] = h2_as_u32(__hfma2(u32_as_h2(l8), s8l, o8l));
+    lo[2] = h2_as_u32(__hfma2(u32_as_h2(l0s), s0l, o0l));
+    lo[3] = h2_as_u32(__hfma2(u32_as_h2(l8s), s8l, o8l));
+    const __half2 n0h = __hneg2(s0h), n8h = __hneg2(s8h);
+    hi[0] = h2_as_u32(__hfma2(u32_as_h2(r0), s0h, __hfma2(u32_as_h2(l0), n0h, o0h)));
+    hi[1] = h2_as_u32(__hfma2(u32_as_h2(r8), s8h, __hfma2(u32_as_h2(l8), n8h, o8h)));
+    hi[2] = h2_as_u32(__hfma2(u32_as_h2(r0s), s0h, __hfma2(u32_as_h2(l0s), n0h, o0h)));
+    hi[3] = h2_as_u32(__hfma2(u32_as_h2(r8s), s8h, __hfma2(u32_as_h2(l8s), n8h, o8h)));
+  }
+
   // acc: this super-block's products in units of 2^-e per row (rows g and
   // g+8: r0, r8 = 2^e of each row's super-block).  PAIRX: fetch the B
   // fragments of two consecutive steps with one 16-byte load (faster in the
@@ -367,56 +394,26 @@ struct SBDot<DQ_Q4_K> {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int s = 2 * sp + h;
-          // bytes (b0 b1 b2 b3) -> (b0 b2 b1 b3): 16-bit lanes hold weights k, k+1
-          const uint32_t p0 = __byte_perm(q0[s], 0, 0x3120), p8 = __byte_perm(q8[s], 0, 0x3120);
-          const uint32_t p0s = p0 >> 8, p8s = p8 >> 8;
-          // low nibbles: weights kb + 64t + 4s + 0..3 (sub-block 2t)
-          {
-            const uint32_t a0 = h2_as_u32(__hfma2(u32_as_h2(p0 & 0x000F000Fu), s0l, o0l));
-            const uint32_t a1 = h2_as_u32(__hfma2(u32_as_h2(p8 & 0x000F000Fu), s8l, o8l));
-            const uint32_t a2 = h2_as_u32(__hfma2(u32_as_h2(p0s & 0x000F000Fu), s0l, o0l));
-            const uint32_t a3 = h2_as_u32(__hfma2(u32_as_h2(p8s & 0x000F000Fu), s8l, o8l));
+          uint32_t lo[4], hi[4];
+          frags(q0[s], q8[s], s0l, o0l, s0h, o0h, s8l, o8l, s8h, o8h, lo, hi);
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-              mma_16816(acc[nt][0], a0, a1, a2, a3, h ? xl[nt].z : xl[nt].x,
-                        h ? xl[nt].w : xl[nt].y);
-          }
-          // high nibbles: 32 weights further (sub-block 2t+1), value 16*q
-          {
-            const uint32_t a0 = h2_as_u32(__hfma2(u32_as_h2(p0 & 0x00F000F0u), s0h, o0h));
-            const uint32_t a1 = h2_as_u32(__hfma2(u32_as_h2(p8 & 0x00F000F0u), s8h, o8h));
-            const uint32_t a2 = h2_as_u32(__hfma2(u32_as_h2(p0s & 0x00F000F0u), s0h, o0h));
-            const uint32_t a3 = h2_as_u32(__hfma2(u32_as_h2(p8s & 0x00F000F0u), s8h, o8h));
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-              mma_16816(acc[nt][1], a0, a1, a2, a3, h ? xh[nt].z : xh[nt].x,
-                        h ? xh[nt].w : xh[nt].y);
+          for (int nt = 0; nt < NT; ++nt) {
+            mma_16816(acc[nt][0], lo[0], lo[1], lo[2], lo[3], h ? xl[nt].z : xl[nt].x,
+                      h ? xl[nt].w : xl[nt].y);
+            mma_16816(acc[nt][1], hi[0], hi[1], hi[2], hi[3], h ? xh[nt].z : xh[nt].x,
+                      h ? xh[nt].w : xh[nt].y);
           }
         }
       }
     } else {
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
-        // bytes (b0 b1 b2 b3) -> (b0 b2 b1 b3): 16-bit lanes hold weights k, k+1
-        const uint32_t p0 = __byte_perm(q0[s], 0, 0x3120), p8 = __byte_perm(q8[s], 0, 0x3120);
-        const uint32_t p0s = p0 >> 8, p8s = p8 >> 8;
+        // weights kb + 64t + 4s + 0..3 (low nibbles), 32 further (high)
         const int k = kb + 64 * t + 4 * s;
-        // low nibbles: weights k..k+3 (sub-block 2t)
-        {
-          const uint32_t a0 = h2_as_u32(__hfma2(u32_as_h2(p0 & 0x000F000Fu), s0l, o0l));
-          const uint32_t a1 = h2_as_u32(__hfma2(u32_as_h2(p8 & 0x000F000Fu), s8l, o8l));
-          const uint32_t a2 = h2_as_u32(__hfma2(u32_as_h2(p0s & 0x000F000Fu), s0l, o0l));
-          const uint32_t a3 = h2_as_u32(__hfma2(u32_as_h2(p8s & 0x000F000Fu), s8l, o8l));
-          mma_x<NT>(acc, 0, a0, a1, a2, a3, xcol, k);
-        }
-        // high nibbles: weights k+32..k+35 (sub-block 2t+1), value 16*q
-        {
-          const uint32_t a0 = h2_as_u32(__hfma2(u32_as_h2(p0 & 0x00F000F0u), s0h, o0h));
-          const uint32_t a1 = h2_as_u32(__hfma2(u32_as_h2(p8 & 0x00F000F0u), s8h, o8h));
-          const uint32_t a2 = h2_as_u32(__hfma2(u32_as_h2(p0s & 0x00F000F0u), s0h, o0h));
-          const uint32_t a3 = h2_as_u32(__hfma2(u32_as_h2(p8s & 0x00F000F0u), s8h, o8h));
-          mma_x<NT>(acc, 1, a0, a1, a2, a3, xcol, k + 32);
-        }
+        uint32_t lo[4], hi[4];
+        frags(q0[s], q8[s], s0l, o0l, s0h, o0h, s8l, o8l, s8h, o8h, lo, hi);
+        mma_x<NT>(acc, 0, lo[0], lo[1], lo[2], lo[3], xcol, k);
+        mma_x<NT>(acc, 1, hi[0], hi[1], hi[2], hi[3], xcol, k + 32);
       }
     }
   }
