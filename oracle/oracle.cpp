@@ -127,11 +127,48 @@ void decode_q80(const uint8_t* b, double* w) {
   for (int i = 0; i < 32; ++i) w[i] = d * q[i];
 }
 
+// Q4_0: fp16 d, 16 bytes of 4-bit quants; byte j holds weight j (low nibble)
+// and weight j+16 (high nibble).  w = d*(q - 8).
+void decode_q40(const uint8_t* b, double* w) {
+  const double d = half_to_f64(rd16(b));
+  const uint8_t* qs = b + 2;
+  for (int j = 0; j < 16; ++j) {
+    w[j] = d * ((qs[j] & 15) - 8);
+    w[j + 16] = d * ((qs[j] >> 4) - 8);
+  }
+}
+
+// Q5_K: d, dmin fp16; 12 bytes of eight 6-bit (sc, m) pairs packed as in
+// Q4_K; 32 bytes qh of fifth bits; 128 bytes of low 4-bit quants in four
+// 32-byte groups.  Group c: weight 64c+l takes the low nibble of qs[32c+l] and
+// bit 2c of qh[l]; weight 64c+32+l the high nibble and bit 2c+1.
+// q in [0, 31]; w = d*sc_j*q - dmin*m_j.
+void decode_q5k(const uint8_t* b, double* w) {
+  const double d = half_to_f64(rd16(b));
+  const double dmin = half_to_f64(rd16(b + 2));
+  const uint8_t* s = b + 4;
+  const uint8_t* qh = b + 16;
+  const uint8_t* qs = b + 48;
+  for (int c = 0; c < 4; ++c) {
+    int sc_lo, m_lo, sc_hi, m_hi;
+    q4k_scale_min(2 * c, s, &sc_lo, &m_lo);
+    q4k_scale_min(2 * c + 1, s, &sc_hi, &m_hi);
+    for (int l = 0; l < 32; ++l) {
+      const int q_lo = (qs[32 * c + l] & 15) | (((qh[l] >> (2 * c)) & 1) << 4);
+      const int q_hi = (qs[32 * c + l] >> 4) | (((qh[l] >> (2 * c + 1)) & 1) << 4);
+      w[64 * c + l] = d * sc_lo * q_lo - dmin * m_lo;
+      w[64 * c + 32 + l] = d * sc_hi * q_hi - dmin * m_hi;
+    }
+  }
+}
+
 bool geometry(int fmt, int* qk, int* bytes) {
   switch (fmt) {
     case OR_Q4_K: *qk = 256; *bytes = 144; return true;
     case OR_Q6_K: *qk = 256; *bytes = 210; return true;
     case OR_Q8_0: *qk = 32; *bytes = 34; return true;
+    case OR_Q4_0: *qk = 32; *bytes = 18; return true;
+    case OR_Q5_K: *qk = 256; *bytes = 176; return true;
     default: return false;
   }
 }
@@ -139,7 +176,9 @@ bool geometry(int fmt, int* qk, int* bytes) {
 void decode_block(int fmt, const uint8_t* b, double* w) {
   if (fmt == OR_Q4_K) decode_q4k(b, w);
   else if (fmt == OR_Q6_K) decode_q6k(b, w);
-  else decode_q80(b, w);
+  else if (fmt == OR_Q8_0) decode_q80(b, w);
+  else if (fmt == OR_Q4_0) decode_q40(b, w);
+  else decode_q5k(b, w);
 }
 
 // Split [0, n) into nthreads contiguous ranges and run fn(lo, hi) on each.

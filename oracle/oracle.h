@@ -12,6 +12,7 @@
  *   [Titan Engine, §MoE 专家流式加载]  sparse activation, 2 of 8 experts
  *   [KTransformers, §支持的量化格式]  Q4_K_M / Q6_K / Q8_0
  *   [NTransformer (Show HN), §量化支持]  Q8_0 / Q4_K_M / Q6_K
+ *   [KTransformers, §支持的量化格式]  Q4_0 / Q5_K (the other GGUF blocks)
  *
  * All functions return 0 on success, -1 on a bad argument.
  */
@@ -26,7 +27,7 @@ extern "C" {
 
 /* format ids and activation dtype ids, same numbering as the public ABI but
  * declared independently */
-enum { OR_Q4_K = 1, OR_Q6_K = 2, OR_Q8_0 = 3 };
+enum { OR_Q4_K = 1, OR_Q6_K = 2, OR_Q8_0 = 3, OR_Q4_0 = 4, OR_Q5_K = 5 };
 enum { OR_F32 = 0, OR_F16 = 1, OR_BF16 = 2 };
 
 /* weights per block / bytes per block */

@@ -12,13 +12,15 @@ Recipe (the pages name no dataset; everything is synthetic):
     128 quant bytes uniform over 0..255 (so every 6-bit field is uniform).
   * Q6_K: ql, qh and the 16 int8 scale bytes uniform over 0..255; d as Q4_K.
   * Q8_0: d as Q4_K; the 32 int8 quants uniform over -127..127.
+  * Q4_0: d as Q4_K; the 16 quant bytes uniform.  Q5_K: as Q4_K, plus the
+    32 fifth-bit bytes uniform.
   * activations N(0,1), drawn in fp32 and rounded to nearest-even into the
     activation dtype; router weights N(0, 0.02) fp32.
 """
 import numpy as np
 
-BLOCK = {1: (256, 144), 2: (256, 210), 3: (32, 34)}  # fmt -> (weights, bytes)
-FMT_NAMES = {"q4_k": 1, "q6_k": 2, "q8_0": 3}
+BLOCK = {1: (256, 144), 2: (256, 210), 3: (32, 34), 4: (32, 18), 5: (256, 176)}  # fmt -> (weights, bytes)
+FMT_NAMES = {"q4_k": 1, "q6_k": 2, "q8_0": 3, "q4_0": 4, "q5_k": 5}
 DT_NAMES = {"f32": 0, "f16": 1, "bf16": 2}
 BASE_SEED = 20261202
 
@@ -45,9 +47,14 @@ def quant_matrix(rng, fmt, rows, cols):
         blk[:, 2:4] = _scale_f16(rng, nblk).view(np.uint8).reshape(nblk, 2)
     elif fmt == 2:      # Q6_K: d at 208
         blk[:, 208:210] = _scale_f16(rng, nblk).view(np.uint8).reshape(nblk, 2)
-    else:               # Q8_0: d at 0, quants -127..127
+    elif fmt == 3:      # Q8_0: d at 0, quants -127..127
         blk[:, 0:2] = _scale_f16(rng, nblk).view(np.uint8).reshape(nblk, 2)
         blk[:, 2:34] = rng.integers(-127, 128, size=(nblk, 32), dtype=np.int8).view(np.uint8)
+    elif fmt == 4:      # Q4_0: d at 0
+        blk[:, 0:2] = _scale_f16(rng, nblk).view(np.uint8).reshape(nblk, 2)
+    else:               # Q5_K: d at 0, dmin at 2 (as Q4_K)
+        blk[:, 0:2] = _scale_f16(rng, nblk).view(np.uint8).reshape(nblk, 2)
+        blk[:, 2:4] = _scale_f16(rng, nblk).view(np.uint8).reshape(nblk, 2)
     return raw
 
 

@@ -21,7 +21,7 @@ from scipy.special import softmax
 import synth
 from golden_io import read_block_cases
 
-Q4_K, Q6_K, Q8_0 = 1, 2, 3
+Q4_K, Q6_K, Q8_0, Q4_0, Q5_K = 1, 2, 3, 4, 5
 
 
 # ---------------------------------------------------------------------------
@@ -141,9 +141,79 @@ def test_synth_bf16_rounding_is_nearest_even():
 
 
 # ---------------------------------------------------------------------------
+# Q4_0 and Q5_K: reductions to the pinned formats, and bit walks
+# ---------------------------------------------------------------------------
+def test_q40_equals_q80_with_shifted_quants(orc):
+    # a Q4_0 block is a Q8_0 block whose int8 quants are the nibbles minus 8,
+    # low nibbles first (weights 0..15), then high nibbles (16..31)
+    rng = np.random.default_rng(404)
+    nblk = 64
+    q40 = np.frombuffer(rng.bytes(nblk * 18), dtype=np.uint8).copy().reshape(nblk, 18)
+    q40[:, 0:2] = (np.abs(rng.standard_normal(nblk)) * 0.01).astype(np.float16).view(np.uint8).reshape(nblk, 2)
+    q80 = np.zeros((nblk, 34), dtype=np.uint8)
+    q80[:, 0:2] = q40[:, 0:2]
+    nib = q40[:, 2:18]
+    q80[:, 2:18] = ((nib & 15).astype(np.int16) - 8).astype(np.int8).view(np.uint8)
+    q80[:, 18:34] = ((nib >> 4).astype(np.int16) - 8).astype(np.int8).view(np.uint8)
+    a = orc.dequant(Q4_0, q40.reshape(-1), nblk * 32)
+    b = orc.dequant(Q8_0, q80.reshape(-1), nblk * 32)
+    np.testing.assert_array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_q40_nibble_walk(orc):
+    # d = 0.5, every nibble 8 (weight 0); raising one nibble to 11 gives 1.5 at
+    # exactly one position: low nibble of byte j -> weight j, high -> j + 16
+    base = np.zeros(18, dtype=np.uint8)
+    base[0:2] = np.array([0.5], dtype=np.float16).view(np.uint8)
+    base[2:18] = 0x88
+    assert np.all(orc.dequant(Q4_0, base, 32) == 0.0)
+    for j in range(16):
+        for hi in (0, 1):
+            b = base.copy()
+            b[2 + j] = 0x8B if hi == 0 else 0xB8
+            w = orc.dequant(Q4_0, b, 32)
+            want = np.zeros(32, dtype=np.float32)
+            want[j + 16 * hi] = 1.5
+            np.testing.assert_array_equal(w, want)
+
+
+def test_q5k_without_fifth_bits_is_q4k(orc):
+    # with every qh byte zero a Q5_K block decodes as the Q4_K block made of
+    # the same d, dmin, scale bytes and low quants
+    rng = np.random.default_rng(505)
+    q4 = synth.quant_matrix(rng, Q4_K, 8, 1024).reshape(-1, 144)
+    q5 = np.zeros((q4.shape[0], 176), dtype=np.uint8)
+    q5[:, 0:16] = q4[:, 0:16]
+    q5[:, 48:176] = q4[:, 16:144]
+    n = q4.shape[0] * 256
+    a = orc.dequant(Q5_K, q5.reshape(-1), n)
+    b = orc.dequant(Q4_K, q4.reshape(-1), n)
+    np.testing.assert_array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_q5k_fifth_bit_walk(orc):
+    # d = 1, dmin = 0, every 6-bit scale 1 and min 0, low quants 0: all weights
+    # 0.  Setting bit i of qh[l] must add 16 to exactly one weight:
+    # 64*(i//2) + l for even i, 64*(i//2) + 32 + l for odd i.
+    base = np.zeros(176, dtype=np.uint8)
+    base[0:2] = np.array([1.0], dtype=np.float16).view(np.uint8)
+    base[4:8] = 1          # sc_0..3 = 1 (m_0..3 = 0 from bytes 8..11)
+    base[12:16] = 0x01     # sc_4..7 = 1, m_4..7 = 0
+    assert np.all(orc.dequant(Q5_K, base, 256) == 0.0)
+    for i in range(8):
+        for l in (0, 1, 17, 31):
+            b = base.copy()
+            b[16 + l] = 1 << i
+            w = orc.dequant(Q5_K, b, 256)
+            want = np.zeros(256, dtype=np.float32)
+            want[64 * (i // 2) + 32 * (i % 2) + l] = 16.0
+            np.testing.assert_array_equal(w, want)
+
+
+# ---------------------------------------------------------------------------
 # qGEMV: brute force against numpy on tiny shapes; an exact integer case
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("fmt", [Q4_K, Q6_K, Q8_0])
+@pytest.mark.parametrize("fmt", [Q4_K, Q6_K, Q8_0, Q4_0, Q5_K])
 @pytest.mark.parametrize("xdt", [0, 1, 2])
 def test_qgemv_brute_force(orc, fmt, xdt):
     g = synth.streams(100 + fmt * 10 + xdt, 4)
