@@ -25,11 +25,23 @@ using namespace dqmoe;
 
 namespace {
 
-bool fmt_ok(int fmt) { return fmt == DQ_Q4_K || fmt == DQ_Q6_K || fmt == DQ_Q8_0; }
+bool fmt_ok(int fmt) { return fmt >= DQ_Q4_K && fmt <= DQ_Q5_K; }
+// formats of the MoE layer's expert matrices
+bool moe_fmt_ok(int fmt) { return fmt == DQ_Q4_K || fmt == DQ_Q6_K || fmt == DQ_Q8_0; }
 bool dtype_ok(int dt) { return dt == DQ_F32 || dt == DQ_F16 || dt == DQ_BF16; }
 bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
 
-int qk_of(int fmt) { return fmt == DQ_Q8_0 ? DQ_QK8_0 : DQ_QK_K; }
+int qk_of(int fmt) { return (fmt == DQ_Q8_0 || fmt == DQ_Q4_0) ? DQ_QK8_0 : DQ_QK_K; }
+
+int block_bytes(int fmt) {
+  switch (fmt) {
+    case DQ_Q4_K: return DQ_Q4_K_BYTES;
+    case DQ_Q6_K: return DQ_Q6_K_BYTES;
+    case DQ_Q8_0: return DQ_Q8_0_BYTES;
+    case DQ_Q4_0: return DQ_Q4_0_BYTES;
+    default: return DQ_Q5_K_BYTES;
+  }
+}
 
 int check_qgemv(int fmt, const void* W, int64_t N, int64_t K, const void* x, int xdt, int batch,
                 const float* y) {
@@ -48,6 +60,7 @@ int check_qgemv(int fmt, const void* W, int64_t N, int64_t K, const void* x, int
 int check_desc(const dq_moe_desc* d, int T) {
   if (!d || T <= 0) return DQ_ERR_ARG;
   if (!fmt_ok(d->fmt)) return DQ_ERR_ARG;
+  if (!moe_fmt_ok(d->fmt)) return DQ_ERR_UNSUPPORTED;
   if (d->E <= 0 || d->top_k <= 0 || d->top_k > d->E || d->hidden <= 0 || d->ffn <= 0 ||
       d->n_shared < 0)
     return DQ_ERR_ARG;
@@ -73,7 +86,7 @@ extern "C" {
 int dq_block_geometry(int fmt, int* weights_per_block, int* bytes_per_block) {
   if (!weights_per_block || !bytes_per_block || !fmt_ok(fmt)) return DQ_ERR_ARG;
   *weights_per_block = qk_of(fmt);
-  *bytes_per_block = fmt == DQ_Q4_K ? DQ_Q4_K_BYTES : fmt == DQ_Q6_K ? DQ_Q6_K_BYTES : DQ_Q8_0_BYTES;
+  *bytes_per_block = block_bytes(fmt);
   return DQ_OK;
 }
 

@@ -17,11 +17,13 @@
 namespace dqmoe {
 
 // Bytes of one 256-weight "super-block row unit" per format.  Q8_0 stores 8
-// blocks of 34 bytes per 256 weights.
+// blocks of 34 bytes per 256 weights, Q4_0 8 blocks of 18.
 template <int FMT> struct Fmt;
 template <> struct Fmt<DQ_Q4_K> { static constexpr int SB_BYTES = 144; };
 template <> struct Fmt<DQ_Q6_K> { static constexpr int SB_BYTES = 210; };
 template <> struct Fmt<DQ_Q8_0> { static constexpr int SB_BYTES = 272; };
+template <> struct Fmt<DQ_Q4_0> { static constexpr int SB_BYTES = 144; };   // 8 blocks of 18
+template <> struct Fmt<DQ_Q5_K> { static constexpr int SB_BYTES = 176; };
 
 // Device status word: a kernel whose bounded wait runs out sets it to
 // DQ_ERR_DEVICE_TIMEOUT and returns instead of hanging.  Read by

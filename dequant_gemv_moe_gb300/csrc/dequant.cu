@@ -1,7 +1,7 @@
 // dequant.cu — step "block decode" on its own: packed blocks -> fp32.
 //
 // The pages name the formats (Titan Engine §激进量化策略: Q4_K; KTransformers
-// §支持的量化格式: Q4_K_M, Q6_K, Q8_0; NTransformer §量化支持: Q80, Q6K) but
+// §支持的量化格式: Q4_K_M, Q6_K, Q8_0, Q4_0, Q5_K; NTransformer §量化支持: Q80, Q6K) but
 // print no layout; the GGUF/llama.cpp layouts declared in dqmoe.h are used.
 // Each output is the exact closed form rounded once to fp32: every product
 // below is exact in fp32 and the Q4_K difference is formed by one fused
@@ -75,13 +75,58 @@ __global__ void dequant_q80_kernel(const uint8_t* __restrict__ blocks, int64_t n
   out[gid] = h16(b) * (float)(int8_t)b[2 + (gid & 31)];
 }
 
+// Q4_0: w = d*(q - 8); byte j of qs: weight j (low nibble), j+16 (high).
+__global__ void dequant_q40_kernel(const uint8_t* __restrict__ blocks, int64_t nblk,
+                                   float* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t blk = gid >> 5;
+  if (blk >= nblk) return;
+  const int i = (int)(gid & 31);
+  const uint8_t* b = blocks + blk * 18;
+  const uint8_t byte = b[2 + (i & 15)];
+  const int q = (i & 16) ? (byte >> 4) : (byte & 15);
+  out[gid] = h16(b) * (float)(q - 8);
+}
+
+// Q5_K: Q4_K's closed form with a 5-bit q (qh bit 2c or 2c+1 as bit 4).
+__global__ void dequant_q5k_kernel(const uint8_t* __restrict__ blocks, int64_t nblk,
+                                   float* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t blk = gid >> 8;
+  if (blk >= nblk) return;
+  const int i = (int)(gid & 255);
+  const uint8_t* b = blocks + blk * 176;
+  const float d = h16(b), dmin = h16(b + 2);
+  const uint8_t* s = b + 4;
+  const int j = i >> 5;            // sub-block: 32 weights
+  int sc, m;
+  if (j < 4) {
+    sc = s[j] & 63;
+    m = s[j + 4] & 63;
+  } else {
+    sc = (s[j + 4] & 15) | ((s[j - 4] >> 6) << 4);
+    m = (s[j + 4] >> 4) | ((s[j] >> 6) << 4);
+  }
+  const int c = i >> 6, l = i & 31;
+  const uint8_t byte = b[48 + 32 * c + l];
+  const int hb = (b[16 + l] >> j) & 1;   // bit 2c (low half) or 2c+1 (high half) = bit j
+  const int q = ((i & 32) ? (byte >> 4) : (byte & 15)) | (hb << 4);
+  out[gid] = __fmaf_rn(d * (float)sc, (float)q, -(dmin * (float)m));
+}
+
 int launch_dequant(int fmt, const void* blocks, int64_t n, float* out, cudaStream_t s) {
   const int threads = 256;
   const int64_t grid = (n + threads - 1) / threads;
   const uint8_t* b = (const uint8_t*)blocks;
   if (fmt == DQ_Q4_K) launch_pdl(dequant_q4k_kernel, dim3((unsigned)grid), dim3(threads), 0, s, 0, b, n / 256, out);
   else if (fmt == DQ_Q6_K) launch_pdl(dequant_q6k_kernel, dim3((unsigned)grid), dim3(threads), 0, s, 0, b, n / 256, out);
-  else launch_pdl(dequant_q80_kernel, dim3((unsigned)grid), dim3(threads), 0, s, 0, b, n / 32, out);
+  else if (fmt == DQ_Q8_0) launch_pdl(dequant_q80_kernel, dim3((unsigned)grid), dim3(threads), 0, s, 0, b, n / 32, out);
+  else if (fmt == DQ_Q4_0) launch_pdl(dequant_q40_kernel, dim3((unsigned)grid), dim3(threads), 0, s, 0, b, n / 32, out);
+  else launch_pdl(dequant_q5k_kernel, dim3((unsigned)grid), dim3(threads), 0, s, 0, b, n / 256, out);
   return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
 }
 

@@ -83,6 +83,54 @@ __device__ __forceinline__ void lane_weights<DQ_Q8_0>(const uint8_t* b, int l, f
   }
 }
 
+template <>
+__device__ __forceinline__ void lane_weights<DQ_Q4_0>(const uint8_t* b, int l, float (&w)[8],
+                                                      int (&k)[8]) {
+  // 8 blocks of 18 bytes; lane l: block l/4, bytes 4*(l%4)..+3 (weights j, j+16)
+  const uint8_t* blk = b + 18 * (l >> 2);
+  const float d = h16g(blk);
+  const int o = (l & 3) * 4;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint8_t q = blk[2 + o + i];
+    w[i] = d * (float)((q & 15) - 8);
+    k[i] = 32 * (l >> 2) + o + i;
+    w[4 + i] = d * (float)((q >> 4) - 8);
+    k[4 + i] = 32 * (l >> 2) + 16 + o + i;
+  }
+}
+
+template <>
+__device__ __forceinline__ void lane_weights<DQ_Q5_K>(const uint8_t* b, int l, float (&w)[8],
+                                                      int (&k)[8]) {
+  const float d = h16g(b), dmin = h16g(b + 2);
+  const uint8_t* s = b + 4;
+  const int c = l >> 3, o = (l & 7) * 4;       // group c, bytes o..o+3
+  int sc[2], m[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int j = 2 * c + h;
+    if (j < 4) {
+      sc[h] = s[j] & 63;
+      m[h] = s[j + 4] & 63;
+    } else {
+      sc[h] = (s[j + 4] & 15) | ((s[j - 4] >> 6) << 4);
+      m[h] = (s[j + 4] >> 4) | ((s[j] >> 6) << 4);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint8_t q = b[48 + 32 * c + o + i];
+    const uint8_t h = b[16 + o + i];
+    const int q0 = (q & 15) | (((h >> (2 * c)) & 1) << 4);
+    const int q1 = (q >> 4) | (((h >> (2 * c + 1)) & 1) << 4);
+    w[i] = __fmaf_rn(d * (float)sc[0], (float)q0, -(dmin * (float)m[0]));
+    k[i] = 64 * c + o + i;
+    w[4 + i] = __fmaf_rn(d * (float)sc[1], (float)q1, -(dmin * (float)m[1]));
+    k[4 + i] = 64 * c + 32 + o + i;
+  }
+}
+
 template <int FMT, int B>
 __global__ void __launch_bounds__(256) qgemv_f32_kernel(const uint8_t* __restrict__ W,
                                                         int64_t N, int64_t nsb,
@@ -143,7 +191,9 @@ int launch_qgemv_f32(int fmt, const void* W, int64_t N, int64_t K, const float* 
                      float* y, cudaStream_t s) {
   if (fmt == DQ_Q4_K) return launch_f32_fmt<DQ_Q4_K>(W, N, K, x, batch, y, s);
   if (fmt == DQ_Q6_K) return launch_f32_fmt<DQ_Q6_K>(W, N, K, x, batch, y, s);
-  return launch_f32_fmt<DQ_Q8_0>(W, N, K, x, batch, y, s);
+  if (fmt == DQ_Q8_0) return launch_f32_fmt<DQ_Q8_0>(W, N, K, x, batch, y, s);
+  if (fmt == DQ_Q4_0) return launch_f32_fmt<DQ_Q4_0>(W, N, K, x, batch, y, s);
+  return launch_f32_fmt<DQ_Q5_K>(W, N, K, x, batch, y, s);
 }
 
 }  // namespace dqmoe

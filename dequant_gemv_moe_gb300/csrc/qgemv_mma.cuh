@@ -46,7 +46,10 @@ struct Layout {
   static constexpr int C = 1;
   // bytes of a row's TMA box per stage: the super-block, for Q6_K a 16-byte
   // aligned superset of its 210 bytes (starts up to 14 bytes early)
-  static constexpr int BOX = (FMT == DQ_Q4_K) ? 144 : (FMT == DQ_Q6_K) ? 240 : 272;
+  static constexpr int BOX = (FMT == DQ_Q4_K || FMT == DQ_Q4_0) ? 144
+                             : (FMT == DQ_Q6_K)                   ? 240
+                             : (FMT == DQ_Q5_K)                   ? 176
+                                                                  : 272;
   // TMA writes box rows densely: pitch = BOX; BOX/16 is odd for every format,
   // so rows g and g+1 fall on different bank halves for 16-byte reads
   static constexpr int ROW_PITCH = BOX;
@@ -524,6 +527,96 @@ struct SBDot<DQ_Q8_0> {
       }
       mma_x<NT>(acc, 0, a[0][0], a[0][1], a[0][2], a[0][3], xcol, kb + 32 * s + 8 * t);
       mma_x<NT>(acc, 1, a[1][0], a[1][1], a[1][2], a[1][3], xcol, kb + 32 * s + 8 * t + 4);
+    }
+  }
+};
+
+// Q5_K: Q4_K's scales and nibble layout plus a fifth bit per weight (qh[l]
+// bit 2t for the low nibble of byte l of group t, bit 2t+1 for the high one).
+// Lane t owns group t as in Q4_K; the fifth bits are merged into the masked
+// nibbles before the same one-HFMA2 decode (q up to 31: still an exact fp16
+// subnormal).
+template <>
+struct SBDot<DQ_Q5_K> {
+  static constexpr bool kRowScale = true;
+
+  template <int NT, bool PAIRX = false>
+  __device__ __forceinline__ static void run(uint32_t wrow, int pitch8,
+                                             const uint32_t (&xcol)[NT], int kb, int t,
+                                             float (&acc)[NT][2][4], float& r0, float& r8) {
+    const uint32_t ra = wrow, rb = wrow + pitch8;
+    const uint4 h0 = lds_u128(ra), h8 = lds_u128(rb);
+    __half2 s0l, o0l, s0h, o0h, s8l, o8l, s8h, o8h;
+    SBDot<DQ_Q4_K>::scales(h0, t, s0l, o0l, s0h, o0h, r0);
+    SBDot<DQ_Q4_K>::scales(h8, t, s8l, o8l, s8h, o8h, r8);
+    const uint32_t qa = ra + 48 + 32 * t;      // this lane's 32 low-quant bytes of row g
+    const uint4 qa0 = lds_u128(qa), qb0 = lds_u128(qa + 16);
+    const uint4 qa8 = lds_u128(qa + pitch8), qb8 = lds_u128(qa + pitch8 + 16);
+    const uint4 ea0 = lds_u128(ra + 16), eb0 = lds_u128(ra + 32);   // qh[0..31] of row g
+    const uint4 ea8 = lds_u128(rb + 16), eb8 = lds_u128(rb + 32);
+    const uint32_t q0[8] = {qa0.x, qa0.y, qa0.z, qa0.w, qb0.x, qb0.y, qb0.z, qb0.w};
+    const uint32_t q8[8] = {qa8.x, qa8.y, qa8.z, qa8.w, qb8.x, qb8.y, qb8.z, qb8.w};
+    const uint32_t e0[8] = {ea0.x, ea0.y, ea0.z, ea0.w, eb0.x, eb0.y, eb0.z, eb0.w};
+    const uint32_t e8[8] = {ea8.x, ea8.y, ea8.z, ea8.w, eb8.x, eb8.y, eb8.z, eb8.w};
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      // bytes (b0 b1 b2 b3) -> (b0 b2 b1 b3): 16-bit lanes hold weights k, k+1;
+      // the qh bytes follow the same permutation, shifted so that bit 2t of
+      // each byte is bit 0 of its lane and bit 2t+1 is bit 1
+      const uint32_t p0 = __byte_perm(q0[s], 0, 0x3120), p8 = __byte_perm(q8[s], 0, 0x3120);
+      const uint32_t f0 = __byte_perm(e0[s], 0, 0x3120) >> (2 * t);
+      const uint32_t f8 = __byte_perm(e8[s], 0, 0x3120) >> (2 * t);
+      const uint32_t pv[4] = {p0, p8, p0 >> 8, p8 >> 8};
+      const uint32_t fv[4] = {f0, f8, f0 >> 8, f8 >> 8};
+      const int k = kb + 64 * t + 4 * s;
+      uint32_t lo[4], hi[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __half2 sl = (i & 1) ? s8l : s0l, ol = (i & 1) ? o8l : o0l;
+        const __half2 sh = (i & 1) ? s8h : s0h, oh = (i & 1) ? o8h : o0h;
+        // q * 2^-24 with q = nibble | fifth bit << 4; high nibbles as 16 * q
+        const uint32_t ql = (pv[i] & 0x000F000Fu) | ((fv[i] << 4) & 0x00100010u);
+        const uint32_t qh = (pv[i] & 0x00F000F0u) | ((fv[i] << 7) & 0x01000100u);
+        lo[i] = h2_as_u32(__hfma2(u32_as_h2(ql), sl, ol));
+        hi[i] = h2_as_u32(__hfma2(u32_as_h2(qh), sh, oh));
+      }
+      mma_x<NT>(acc, 0, lo[0], lo[1], lo[2], lo[3], xcol, k);
+      mma_x<NT>(acc, 1, hi[0], hi[1], hi[2], hi[3], xcol, k + 32);
+    }
+  }
+};
+
+// Q4_0: 8 blocks of 18 bytes per 256 weights; block s is step s.  Lane t owns
+// quant bytes 4t..4t+3 of each block: weights 4t..4t+3 (low nibbles) and
+// 16+4t..16+4t+3 (high nibbles).  Absolute fp16 weights (q - 8 exact by the
+// 1024 magic, one multiply by d).
+template <>
+struct SBDot<DQ_Q4_0> {
+  static constexpr bool kRowScale = false;
+  template <int NT, bool PAIRX = false>
+  __device__ __forceinline__ static void run(uint32_t wrow, int pitch8,
+                                             const uint32_t (&xcol)[NT], int kb, int t,
+                                             float (&acc)[NT][2][4]) {
+    const __half2 bias = __float2half2_rn(1032.f);   // 1024 + 8
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      uint32_t lo[4], hi[4];
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        const uint32_t blk = wrow + (rr ? pitch8 : 0) + 18 * s;
+        const __half2 d2 = __half2half2(__ushort_as_half((unsigned short)lds_u16(blk)));
+        const uint32_t p = __byte_perm(lds_u32_a2(blk + 2 + 4 * t), 0, 0x3120);
+        const uint32_t pv[2] = {p, p >> 8};
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          const uint32_t l = lop3_and_or(pv[m], 0x000F000Fu, 0x64006400u);
+          const uint32_t h = lop3_and_or(pv[m] >> 4, 0x000F000Fu, 0x64006400u);
+          lo[2 * m + rr] = h2_as_u32(__hmul2(__hsub2(u32_as_h2(l), bias), d2));
+          hi[2 * m + rr] = h2_as_u32(__hmul2(__hsub2(u32_as_h2(h), bias), d2));
+        }
+      }
+      mma_x<NT>(acc, 0, lo[0], lo[1], lo[2], lo[3], xcol, kb + 32 * s + 4 * t);
+      mma_x<NT>(acc, 1, hi[0], hi[1], hi[2], hi[3], xcol, kb + 32 * s + 16 + 4 * t);
     }
   }
 };

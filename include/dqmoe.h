@@ -40,7 +40,8 @@
  *     of that row, consecutive, starting at byte n * row_bytes where
  *     row_bytes = (K/QK) * block_bytes.  Rows are consecutive.  W must be
  *     16-byte aligned and row_bytes a multiple of 16 (true for every shape
- *     with K a multiple of 256 for Q4_K and Q8_0, of 2048 for Q6_K).
+ *     with K a multiple of 256 for Q4_K, Q8_0, Q4_0 and Q5_K, of 2048 for
+ *     Q6_K).
  *   - Activations x: [batch][K] row-major in x_dtype.  Outputs y: [batch][N]
  *     row-major, always fp32 (MoE activations reach ~1e7, beyond fp16).
  */
@@ -78,8 +79,18 @@ extern "C" {
 /*   (qh byte is qh[32h+l], its two bits are the high bits of the 6-bit q). */
 /*   weight i: w = d * scales[i/16] * (q - 32), q in [0,63].                */
 /* Q8_0 block, 32 weights in 34 bytes: fp16 d, int8 qs[32]; w = d*q.        */
+/* Q4_0 block, 32 weights in 18 bytes: fp16 d, qs[16]; byte j holds weight j */
+/*   in its low nibble and weight j+16 in its high nibble; w = d*(q - 8).   */
+/* Q5_K super-block, 256 weights in 176 bytes:                              */
+/*   bytes 0-15 as Q4_K (d, dmin, the 12 scale/min bytes), bytes 16-47      */
+/*   qh[32], bytes 48-175 qs[128] as Q4_K's.  Weight 64c+l (c = 0..3,       */
+/*   l = 0..31) takes the low nibble of qs[32c+l] plus bit 2c of qh[l] as   */
+/*   bit 4; weight 64c+32+l the high nibble plus bit 2c+1.  q in [0,31];    */
+/*   w = d*sc_j*q - dmin*m_j as Q4_K.  Both are the other GGUF blocks the   */
+/*   [KTransformers, §支持的量化格式] list names beside Q4_K, Q6_K, Q8_0;    */
+/*   dq_dequant and dq_qgemv take them, the MoE layer does not.             */
 /* ------------------------------------------------------------------------ */
-typedef enum { DQ_Q4_K = 1, DQ_Q6_K = 2, DQ_Q8_0 = 3 } dq_fmt;
+typedef enum { DQ_Q4_K = 1, DQ_Q6_K = 2, DQ_Q8_0 = 3, DQ_Q4_0 = 4, DQ_Q5_K = 5 } dq_fmt;
 
 /* Activation element types accepted by the entry points. */
 typedef enum { DQ_F32 = 0, DQ_F16 = 1, DQ_BF16 = 2 } dq_dtype;
@@ -99,6 +110,9 @@ typedef enum {
 #define DQ_Q4_K_BYTES 144
 #define DQ_Q6_K_BYTES 210
 #define DQ_Q8_0_BYTES 34
+#define DQ_QK4_0 32         /* weights per Q4_0 block */
+#define DQ_Q4_0_BYTES 18
+#define DQ_Q5_K_BYTES 176
 #define DQ_MAX_BATCH 8      /* activation columns per dq_qgemv call */
 
 /* Weights per block and bytes per block of `fmt`.  Host-only, no CUDA.
@@ -110,7 +124,8 @@ int dq_block_geometry(int fmt, int* weights_per_block, int* bytes_per_block);
  * values can be compared bit for bit (every closed form above is exact in
  * fp32 up to the final rounding of the Q4_K subtraction).
  *   blocks : device, n_weights/QK consecutive blocks, 16-byte aligned for
- *            Q4_K; 2-byte aligned for Q6_K/Q8_0 (their blocks are 210/34 B).
+ *            Q4_K and Q5_K; 2-byte aligned for Q6_K/Q8_0/Q4_0 (their blocks
+ *            are 210/34/18 B).
  *   out    : device fp32 [n_weights], 4-byte aligned.
  * Errors: DQ_ERR_ARG (null, n_weights <= 0 or not a multiple of QK),
  *         DQ_ERR_ALIGN, DQ_ERR_CUDA. */

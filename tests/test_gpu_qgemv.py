@@ -13,7 +13,7 @@ from gpu_util import TOL, dev_act, dev_bytes, rel_err
 
 pytestmark = pytest.mark.gpu
 
-Q4_K, Q6_K, Q8_0 = 1, 2, 3
+Q4_K, Q6_K, Q8_0, Q4_0, Q5_K = 1, 2, 3, 4, 5
 
 
 @pytest.fixture(scope="module")
@@ -23,7 +23,8 @@ def dq():
     return dq
 
 
-@pytest.mark.parametrize("fmt,qk", [(Q4_K, 256), (Q6_K, 256), (Q8_0, 32)])
+@pytest.mark.parametrize("fmt,qk", [(Q4_K, 256), (Q6_K, 256), (Q8_0, 32), (Q4_0, 32),
+                                    (Q5_K, 256)])
 def test_dequant_bit_exact_random(dq, orc, fmt, qk):
     g = synth.streams(31 + fmt, 1)[0]
     raw = synth.quant_matrix(g, fmt, 37, 4096)
@@ -63,7 +64,7 @@ def _case(dq, orc, fmt, N, K, B, xdt, seed, ksplit=None, rows=None, xscale=1.0):
     return rel_err(got, ref)
 
 
-@pytest.mark.parametrize("fmt", [Q4_K, Q6_K, Q8_0])
+@pytest.mark.parametrize("fmt", [Q4_K, Q6_K, Q8_0, Q4_0, Q5_K])
 @pytest.mark.parametrize("xdt", [0, 1, 2])
 @pytest.mark.parametrize("B", [1, 3, 8])
 def test_qgemv_small_ragged(dq, orc, fmt, xdt, B):
@@ -73,7 +74,7 @@ def test_qgemv_small_ragged(dq, orc, fmt, xdt, B):
     assert err <= TOL[xdt], err
 
 
-@pytest.mark.parametrize("fmt", [Q4_K, Q6_K, Q8_0])
+@pytest.mark.parametrize("fmt", [Q4_K, Q6_K, Q8_0, Q4_0, Q5_K])
 @pytest.mark.parametrize("ks", [1, 2, 3, 5, 8])
 def test_qgemv_cluster_ksplit(dq, orc, fmt, ks):
     N, K = 130, 8192
@@ -183,3 +184,31 @@ def test_qgemv_weights_early_and_chains(dq, orc):
         assert rel_err(y2.cpu().numpy(), orc.qgemv(Q4_K, W2, N2, N1, y1h, 0, 2)) <= TOL[0]
         x3h = x3.cpu().numpy()
         assert rel_err(y3.cpu().numpy(), orc.qgemv(Q8_0, W3, N2, N1, x3h, 1, 2)) <= TOL[1]
+
+
+# ---------------------------------------------------------- Q4_0 and Q5_K
+@pytest.mark.parametrize("fmt", [Q4_0, Q5_K])
+@pytest.mark.parametrize("B", [1, 8])
+def test_gemv_only_formats_70b_shape(dq, orc, fmt, B):
+    # the 70B gate shape in the two qGEMV-only formats, sampled rows
+    N, K = 28672, 8192
+    rows = np.unique(np.concatenate([[0, N - 1], np.random.default_rng(fmt + B).integers(0, N, 64)]))
+    err = _case(dq, orc, fmt, N, K, B, 1, seed=9100 + fmt * 10 + B, rows=rows)
+    assert err <= TOL[1], err
+
+
+def test_q5k_fifth_bits_matter_on_gpu(dq, orc):
+    # the same bytes with and without the qh bits differ, and each matches the
+    # oracle: the GPU decode reads the fifth bits
+    g = synth.streams(9200, 2)
+    N, K = 128, 2048
+    W = synth.quant_matrix(g[0], Q5_K, N, K)
+    W0 = W.reshape(-1, 176).copy()
+    W0[:, 16:48] = 0
+    W0 = W0.reshape(-1)
+    x = synth.activations(g[1], (2, K), 1)
+    ys = [dq.qgemv(Q5_K, dev_bytes(w), N, K, dev_act(x, 1)).cpu().numpy() for w in (W, W0)]
+    refs = [orc.qgemv(Q5_K, w, N, K, x, 1, 2) for w in (W, W0)]
+    for y, r in zip(ys, refs):
+        assert rel_err(y, r) <= TOL[1]
+    assert rel_err(ys[0], refs[1]) > 10 * TOL[1]
