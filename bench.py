@@ -60,6 +60,8 @@ def run_case(args):
                                                         with_e2e=False).items()}))
     elif args.case == "mixtral":
         print(json.dumps(bench_moe(torch, dq, synth.MOE_MIXTRAL, 16, reps=max(1, args.steps))))
+    elif args.case == "formats70b":
+        print(json.dumps(bench_gemv_70b_formats(torch, dq, reps=max(1, args.steps))))
     elif args.case == "prefill32":
         # DeepSeek-V3 expert shapes with 32 routed experts (+1 shared), T = 256:
         # ~64 tokens per expert, every expert on the tcgen05 grouped GEMM; 0.8 GB
@@ -469,6 +471,38 @@ def bench_gemv_70b(torch, dq, reps=50):
                     "in graphs of 8 (4 rotating weight copies, 528 MB > L2)"}
 
 
+def bench_gemv_70b_formats(torch, dq, reps=30):
+    """The 70B-shaped linears (gate 28672x8192, down 8192x28672, q 8192x8192) in
+    Q4_K / Q6_K / Q8_0 at batch 1 and 8: one launch between two events, 4
+    rotating weight copies."""
+    out = {}
+    g = synth.streams(synth.BASE_SEED + 7, 2)
+    for fmt, fname in ((Q4_K, "q4_k"), (2, "q6_k"), (3, "q8_0")):
+        for name, N, K in synth.LLAMA70B_LINEARS[1:]:       # up (= gate shape), down, q
+            W0 = torch.from_numpy(synth.quant_matrix(g[0], fmt, N, K)).cuda()
+            Ws = [W0] + [W0.clone() for _ in range(ROTATE - 1)]
+            wb = weight_bytes(fmt, N, K)
+            for B in (1, 8):
+                x = torch.from_numpy(synth.activations(g[1], (B, K), 1)).cuda()
+                y = torch.empty(B, N, dtype=torch.float32, device="cuda")
+                for r in range(ROTATE):
+                    dq.qgemv(fmt, Ws[r], N, K, x, y=y)
+                torch.cuda.synchronize()
+                evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * reps)]
+                for i in range(reps):
+                    evs[2 * i].record()
+                    dq.qgemv(fmt, Ws[i % ROTATE], N, K, x, y=y)
+                    evs[2 * i + 1].record()
+                torch.cuda.synchronize()
+                us = float(np.median([evs[2 * i].elapsed_time(evs[2 * i + 1])
+                                      for i in range(reps)])) * 1e3
+                out["%s_%s_%dx%d_b%d" % (fname, "gate" if name == "up" else name, N, K, B)] = {
+                    "us": round(us, 2), "weight_GBps": round(wb / (us / 1e6) / 1e9, 1)}
+            del Ws, W0
+            torch.cuda.empty_cache()
+    return out
+
+
 def bench_moe(torch, dq, cfg, T, reps=20):
     w = synth.moe_weights(synth.BASE_SEED + (3 if cfg is synth.MOE_MIXTRAL else 4), cfg["E"],
                           cfg["H"], cfg["F"], cfg["n_shared"], cfg["fmt"])
@@ -553,6 +587,10 @@ def run_ours(args):
         g70 = extra["gemv_70b_gate_b1"]
         g70["frac_of_hbm"] = g70["weight_GBps"] / peak
         g70["frac_of_hbm_back_to_back"] = g70["weight_GBps_back_to_back"] / peak
+        f70 = bench_gemv_70b_formats(torch, dq)
+        for v in f70.values():
+            v["frac_of_hbm"] = round(v["weight_GBps"] / peak, 4)
+        extra["gemv_70b_formats"] = f70
         if not args.no_moe:
             moe = {}
             moe["mixtral_T16"] = bench_moe(torch, dq, synth.MOE_MIXTRAL, 16)
