@@ -162,6 +162,37 @@ void decode_q5k(const uint8_t* b, double* w) {
   }
 }
 
+// E2M1 (FP4): sign, 2-bit exponent (bias 1), 1-bit mantissa; exponent 0 is
+// subnormal (0 or 0.5).  Magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6.
+double e2m1_to_f64(int c) {
+  const int e = (c >> 1) & 3, m = c & 1;
+  const double mag = e == 0 ? 0.5 * m : std::ldexp(1.0 + 0.5 * m, e - 1);
+  return (c & 8) ? -mag : mag;
+}
+
+// E4M3 (FP8): sign, 4-bit exponent (bias 7), 3-bit mantissa; exponent 0 is
+// subnormal (m/8 * 2^-6); S.1111.111 is NaN, there is no infinity.
+double e4m3_to_f64(int b) {
+  const int e = (b >> 3) & 15, m = b & 7;
+  double mag;
+  if (e == 15 && m == 7) mag = NAN;
+  else if (e == 0) mag = std::ldexp((double)m, -9);
+  else mag = std::ldexp(1.0 + m / 8.0, e - 7);
+  return (b & 128) ? -mag : mag;
+}
+
+// NVFP4 super-block (this library's layout: the pages name the format but
+// print no layout): 256 weights in 144 bytes, bytes 0-15 the E4M3 scales of
+// the sixteen 16-weight blocks, bytes 16-143 the E2M1 codes, two per byte,
+// weight 2i in the low nibble of byte 16+i and 2i+1 in the high nibble.
+// w = e2m1(code) * e4m3(scale[i/16]); a per-tensor scale is the caller's.
+void decode_nvfp4(const uint8_t* b, double* w) {
+  for (int i = 0; i < 256; ++i) {
+    const int code = (b[16 + i / 2] >> (4 * (i & 1))) & 15;
+    w[i] = e2m1_to_f64(code) * e4m3_to_f64(b[i / 16]);
+  }
+}
+
 bool geometry(int fmt, int* qk, int* bytes) {
   switch (fmt) {
     case OR_Q4_K: *qk = 256; *bytes = 144; return true;
@@ -169,6 +200,7 @@ bool geometry(int fmt, int* qk, int* bytes) {
     case OR_Q8_0: *qk = 32; *bytes = 34; return true;
     case OR_Q4_0: *qk = 32; *bytes = 18; return true;
     case OR_Q5_K: *qk = 256; *bytes = 176; return true;
+    case OR_NVFP4: *qk = 256; *bytes = 144; return true;
     default: return false;
   }
 }
@@ -178,7 +210,8 @@ void decode_block(int fmt, const uint8_t* b, double* w) {
   else if (fmt == OR_Q6_K) decode_q6k(b, w);
   else if (fmt == OR_Q8_0) decode_q80(b, w);
   else if (fmt == OR_Q4_0) decode_q40(b, w);
-  else decode_q5k(b, w);
+  else if (fmt == OR_Q5_K) decode_q5k(b, w);
+  else decode_nvfp4(b, w);
 }
 
 // Split [0, n) into nthreads contiguous ranges and run fn(lo, hi) on each.

@@ -13,6 +13,8 @@
  *   [KTransformers, §支持的量化格式]  Q4_K_M / Q6_K / Q8_0
  *   [NTransformer (Show HN), §量化支持]  Q8_0 / Q4_K_M / Q6_K
  *   [KTransformers, §支持的量化格式]  Q4_0 / Q5_K (the other GGUF blocks)
+ *   [Titan Engine, §激进量化策略 / §模型格式支持]  NVIDIA FP4 (Blackwell's
+ *       native 4-bit float): E2M1 values with E4M3 scales per 16 weights
  *
  * All functions return 0 on success, -1 on a bad argument.
  */
@@ -27,7 +29,7 @@ extern "C" {
 
 /* format ids and activation dtype ids, same numbering as the public ABI but
  * declared independently */
-enum { OR_Q4_K = 1, OR_Q6_K = 2, OR_Q8_0 = 3, OR_Q4_0 = 4, OR_Q5_K = 5 };
+enum { OR_Q4_K = 1, OR_Q6_K = 2, OR_Q8_0 = 3, OR_Q4_0 = 4, OR_Q5_K = 5, OR_NVFP4 = 6 };
 enum { OR_F32 = 0, OR_F16 = 1, OR_BF16 = 2 };
 
 /* weights per block / bytes per block */

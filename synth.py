@@ -14,13 +14,17 @@ Recipe (the pages name no dataset; everything is synthetic):
   * Q8_0: d as Q4_K; the 32 int8 quants uniform over -127..127.
   * Q4_0: d as Q4_K; the 16 quant bytes uniform.  Q5_K: as Q4_K, plus the
     32 fifth-bit bytes uniform.
+  * NVFP4: the 128 code bytes uniform; the 16 E4M3 scale bytes positive with
+    exponent field uniform over 1..6 and mantissa field uniform (scales
+    2^-6 .. 2^-1 * 1.875: weights within +-0.7, the range of Q4_K's).
   * activations N(0,1), drawn in fp32 and rounded to nearest-even into the
     activation dtype; router weights N(0, 0.02) fp32.
 """
 import numpy as np
 
-BLOCK = {1: (256, 144), 2: (256, 210), 3: (32, 34), 4: (32, 18), 5: (256, 176)}  # fmt -> (weights, bytes)
-FMT_NAMES = {"q4_k": 1, "q6_k": 2, "q8_0": 3, "q4_0": 4, "q5_k": 5}
+BLOCK = {1: (256, 144), 2: (256, 210), 3: (32, 34), 4: (32, 18), 5: (256, 176),
+         6: (256, 144)}  # fmt -> (weights, bytes)
+FMT_NAMES = {"q4_k": 1, "q6_k": 2, "q8_0": 3, "q4_0": 4, "q5_k": 5, "nvfp4": 6}
 DT_NAMES = {"f32": 0, "f16": 1, "bf16": 2}
 BASE_SEED = 20261202
 
@@ -52,9 +56,13 @@ def quant_matrix(rng, fmt, rows, cols):
         blk[:, 2:34] = rng.integers(-127, 128, size=(nblk, 32), dtype=np.int8).view(np.uint8)
     elif fmt == 4:      # Q4_0: d at 0
         blk[:, 0:2] = _scale_f16(rng, nblk).view(np.uint8).reshape(nblk, 2)
-    else:               # Q5_K: d at 0, dmin at 2 (as Q4_K)
+    elif fmt == 5:      # Q5_K: d at 0, dmin at 2 (as Q4_K)
         blk[:, 0:2] = _scale_f16(rng, nblk).view(np.uint8).reshape(nblk, 2)
         blk[:, 2:4] = _scale_f16(rng, nblk).view(np.uint8).reshape(nblk, 2)
+    else:               # NVFP4: 16 positive E4M3 scale bytes with exponent field 1..6
+        ef = rng.integers(1, 7, size=(nblk, 16), dtype=np.uint8)
+        mf = rng.integers(0, 8, size=(nblk, 16), dtype=np.uint8)
+        blk[:, 0:16] = (ef << 3) | mf
     return raw
 
 

@@ -21,7 +21,7 @@ from scipy.special import softmax
 import synth
 from golden_io import read_block_cases
 
-Q4_K, Q6_K, Q8_0, Q4_0, Q5_K = 1, 2, 3, 4, 5
+Q4_K, Q6_K, Q8_0, Q4_0, Q5_K, NVFP4 = 1, 2, 3, 4, 5, 6
 
 
 # ---------------------------------------------------------------------------
@@ -211,9 +211,82 @@ def test_q5k_fifth_bit_walk(orc):
 
 
 # ---------------------------------------------------------------------------
+# NVFP4: the E2M1 and E4M3 value tables, a reduction to Q8_0, placement walks
+# ---------------------------------------------------------------------------
+E2M1_TABLE = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0,
+              -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0]   # codes 0..15
+
+
+def _nvfp4_block(scales, codes):
+    b = np.zeros(144, dtype=np.uint8)
+    b[0:16] = scales
+    c = np.asarray(codes, dtype=np.uint8)
+    b[16:144] = c[0::2] | (c[1::2] << 4)
+    return b
+
+
+def test_nvfp4_e2m1_table(orc):
+    # scale 0x38 = 1.0: weight i shows the code's E2M1 value
+    codes = np.arange(256) % 16
+    w = orc.dequant(NVFP4, _nvfp4_block(np.full(16, 0x38), codes), 256)
+    np.testing.assert_array_equal(w, np.array([E2M1_TABLE[c] for c in codes], dtype=np.float32))
+    assert np.signbit(w[8])                       # code 8 is -0
+
+
+def test_nvfp4_e4m3_scale_values(orc):
+    # code 2 (= 1.0) times the block's scale: E4M3 values of the FP8 definition
+    # (bias 7; exponent 0 subnormal m/8 * 2^-6; max 448)
+    cases = {0x38: 1.0, 0x30: 0.5, 0x3F: 1.875, 0x40: 2.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9,
+             0x08: 2.0 ** -6, 0x7E: 448.0, 0xC0: -2.0, 0x00: 0.0, 0x5C: 24.0}
+    items = list(cases.items())
+    for i in range(0, len(items), 16):
+        chunk = items[i:i + 16]
+        scales = np.full(16, 0x38, dtype=np.uint8)
+        for j, (byte, _) in enumerate(chunk):
+            scales[j] = byte
+        w = orc.dequant(NVFP4, _nvfp4_block(scales, np.full(256, 2)), 256)
+        for j, (byte, val) in enumerate(chunk):
+            np.testing.assert_array_equal(w[16 * j:16 * j + 16], np.float32(val), err_msg=hex(byte))
+
+
+def test_nvfp4_equals_q80_at_unit_scale(orc):
+    # with every scale 1.0 an NVFP4 super-block is eight Q8_0 blocks with
+    # d = 0.5 and q = 2 * the E2M1 value (integers 0, +-1, .., +-12)
+    rng = np.random.default_rng(606)
+    codes = rng.integers(0, 16, size=256)
+    a = orc.dequant(NVFP4, _nvfp4_block(np.full(16, 0x38), codes), 256)
+    q80 = np.zeros((8, 34), dtype=np.uint8)
+    q80[:, 0:2] = np.array([0.5], dtype=np.float16).view(np.uint8)
+    q = np.array([int(2 * E2M1_TABLE[c]) for c in codes], dtype=np.int8).reshape(8, 32)
+    q80[:, 2:34] = q.view(np.uint8)
+    b = orc.dequant(Q8_0, q80.reshape(-1), 256)
+    np.testing.assert_array_equal(np.abs(a), np.abs(b))
+    np.testing.assert_array_equal(a[a != 0], b[a != 0])
+
+
+def test_nvfp4_placement_walk(orc):
+    # one scale byte doubled -> exactly its 16 weights double; one code set ->
+    # exactly weight 2i (low nibble of byte i) or 2i+1 (high nibble)
+    for blk in range(16):
+        scales = np.full(16, 0x38, dtype=np.uint8)
+        scales[blk] = 0x40
+        w = orc.dequant(NVFP4, _nvfp4_block(scales, np.full(256, 2)), 256)
+        want = np.ones(256, dtype=np.float32)
+        want[16 * blk:16 * blk + 16] = 2.0
+        np.testing.assert_array_equal(w, want)
+    for i in (0, 1, 2, 127, 128, 254, 255):
+        codes = np.zeros(256, dtype=np.int64)
+        codes[i] = 7
+        w = orc.dequant(NVFP4, _nvfp4_block(np.full(16, 0x38), codes), 256)
+        want = np.zeros(256, dtype=np.float32)
+        want[i] = 6.0
+        np.testing.assert_array_equal(w, want)
+
+
+# ---------------------------------------------------------------------------
 # qGEMV: brute force against numpy on tiny shapes; an exact integer case
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("fmt", [Q4_K, Q6_K, Q8_0, Q4_0, Q5_K])
+@pytest.mark.parametrize("fmt", [Q4_K, Q6_K, Q8_0, Q4_0, Q5_K, NVFP4])
 @pytest.mark.parametrize("xdt", [0, 1, 2])
 def test_qgemv_brute_force(orc, fmt, xdt):
     g = synth.streams(100 + fmt * 10 + xdt, 4)
