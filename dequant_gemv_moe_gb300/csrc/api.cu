@@ -25,7 +25,7 @@ using namespace dqmoe;
 
 namespace {
 
-bool fmt_ok(int fmt) { return fmt >= DQ_Q4_K && fmt <= DQ_Q5_K; }
+bool fmt_ok(int fmt) { return fmt >= DQ_Q4_K && fmt <= DQ_NVFP4; }
 // formats of the MoE layer's expert matrices
 bool moe_fmt_ok(int fmt) { return fmt == DQ_Q4_K || fmt == DQ_Q6_K || fmt == DQ_Q8_0; }
 bool dtype_ok(int dt) { return dt == DQ_F32 || dt == DQ_F16 || dt == DQ_BF16; }
@@ -39,7 +39,8 @@ int block_bytes(int fmt) {
     case DQ_Q6_K: return DQ_Q6_K_BYTES;
     case DQ_Q8_0: return DQ_Q8_0_BYTES;
     case DQ_Q4_0: return DQ_Q4_0_BYTES;
-    default: return DQ_Q5_K_BYTES;
+    case DQ_Q5_K: return DQ_Q5_K_BYTES;
+    default: return DQ_NVFP4_BYTES;
   }
 }
 

@@ -24,6 +24,26 @@ template <> struct Fmt<DQ_Q6_K> { static constexpr int SB_BYTES = 210; };
 template <> struct Fmt<DQ_Q8_0> { static constexpr int SB_BYTES = 272; };
 template <> struct Fmt<DQ_Q4_0> { static constexpr int SB_BYTES = 144; };   // 8 blocks of 18
 template <> struct Fmt<DQ_Q5_K> { static constexpr int SB_BYTES = 176; };
+template <> struct Fmt<DQ_NVFP4> { static constexpr int SB_BYTES = 144; };
+
+// Hardware FP4/FP8 -> fp16 conversions (exact).  e2m1x8: the 8 E2M1 codes of
+// a word (byte j: codes 2j low nibble, 2j+1 high nibble) as 4 fp16 pairs in
+// code order; e4m3x2: two E4M3 bytes (low byte first) as one fp16 pair.
+__device__ __forceinline__ void e2m1x8_to_h2x4(uint32_t w, uint32_t (&h)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
+}
+__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint16_t v) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+  return r;
+}
 
 // Device status word: a kernel whose bounded wait runs out sets it to
 // DQ_ERR_DEVICE_TIMEOUT and returns instead of hanging.  Read by

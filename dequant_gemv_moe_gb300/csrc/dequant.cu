@@ -118,6 +118,32 @@ __global__ void dequant_q5k_kernel(const uint8_t* __restrict__ blocks, int64_t n
   out[gid] = __fmaf_rn(d * (float)sc, (float)q, -(dmin * (float)m));
 }
 
+// NVFP4: w = e2m1(code) * e4m3(scale of the 16-weight block); both
+// conversions by the hardware (exact), the product exact in fp32.  One thread
+// per 8 weights (one code word).
+__global__ void dequant_nvfp4_kernel(const uint8_t* __restrict__ blocks, int64_t nblk,
+                                     float* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t blk = gid >> 5;
+  if (blk >= nblk) return;
+  const int j = (int)(gid & 31);                   // weights 8j..8j+7
+  const uint8_t* b = blocks + blk * 144;
+  const uint32_t w = (uint32_t)b[16 + 4 * j] | ((uint32_t)b[17 + 4 * j] << 8) |
+                     ((uint32_t)b[18 + 4 * j] << 16) | ((uint32_t)b[19 + 4 * j] << 24);
+  uint32_t h[4];
+  e2m1x8_to_h2x4(w, h);
+  const float s = __low2float(u32_as_h2(e4m3x2_to_h2((uint16_t)b[j >> 1])));
+  float* o = out + blk * 256 + 8 * j;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 v = __half22float2(u32_as_h2(h[i]));
+    o[2 * i] = v.x * s;
+    o[2 * i + 1] = v.y * s;
+  }
+}
+
 int launch_dequant(int fmt, const void* blocks, int64_t n, float* out, cudaStream_t s) {
   const int threads = 256;
   const int64_t grid = (n + threads - 1) / threads;
@@ -126,7 +152,8 @@ int launch_dequant(int fmt, const void* blocks, int64_t n, float* out, cudaStrea
   else if (fmt == DQ_Q6_K) launch_pdl(dequant_q6k_kernel, dim3((unsigned)grid), dim3(threads), 0, s, 0, b, n / 256, out);
   else if (fmt == DQ_Q8_0) launch_pdl(dequant_q80_kernel, dim3((unsigned)grid), dim3(threads), 0, s, 0, b, n / 32, out);
   else if (fmt == DQ_Q4_0) launch_pdl(dequant_q40_kernel, dim3((unsigned)grid), dim3(threads), 0, s, 0, b, n / 32, out);
-  else launch_pdl(dequant_q5k_kernel, dim3((unsigned)grid), dim3(threads), 0, s, 0, b, n / 256, out);
+  else if (fmt == DQ_Q5_K) launch_pdl(dequant_q5k_kernel, dim3((unsigned)grid), dim3(threads), 0, s, 0, b, n / 256, out);
+  else launch_pdl(dequant_nvfp4_kernel, dim3((unsigned)((n / 8 + threads - 1) / threads)), dim3(threads), 0, s, 0, b, n / 256, out);
   return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
 }
 

@@ -131,6 +131,25 @@ __device__ __forceinline__ void lane_weights<DQ_Q5_K>(const uint8_t* b, int l, f
   }
 }
 
+template <>
+__device__ __forceinline__ void lane_weights<DQ_NVFP4>(const uint8_t* b, int l, float (&w)[8],
+                                                       int (&k)[8]) {
+  // lane l: weights 8l..8l+7 (code bytes 16+4l..+3), block scale l/2
+  const uint32_t word = (uint32_t)b[16 + 4 * l] | ((uint32_t)b[17 + 4 * l] << 8) |
+                        ((uint32_t)b[18 + 4 * l] << 16) | ((uint32_t)b[19 + 4 * l] << 24);
+  uint32_t h[4];
+  e2m1x8_to_h2x4(word, h);
+  const float s = __low2float(u32_as_h2(e4m3x2_to_h2((uint16_t)b[l >> 1])));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 v = __half22float2(u32_as_h2(h[i]));
+    w[2 * i] = v.x * s;
+    w[2 * i + 1] = v.y * s;
+    k[2 * i] = 8 * l + 2 * i;
+    k[2 * i + 1] = 8 * l + 2 * i + 1;
+  }
+}
+
 template <int FMT, int B>
 __global__ void __launch_bounds__(256) qgemv_f32_kernel(const uint8_t* __restrict__ W,
                                                         int64_t N, int64_t nsb,
@@ -193,7 +212,8 @@ int launch_qgemv_f32(int fmt, const void* W, int64_t N, int64_t K, const float* 
   if (fmt == DQ_Q6_K) return launch_f32_fmt<DQ_Q6_K>(W, N, K, x, batch, y, s);
   if (fmt == DQ_Q8_0) return launch_f32_fmt<DQ_Q8_0>(W, N, K, x, batch, y, s);
   if (fmt == DQ_Q4_0) return launch_f32_fmt<DQ_Q4_0>(W, N, K, x, batch, y, s);
-  return launch_f32_fmt<DQ_Q5_K>(W, N, K, x, batch, y, s);
+  if (fmt == DQ_Q5_K) return launch_f32_fmt<DQ_Q5_K>(W, N, K, x, batch, y, s);
+  return launch_f32_fmt<DQ_NVFP4>(W, N, K, x, batch, y, s);
 }
 
 }  // namespace dqmoe

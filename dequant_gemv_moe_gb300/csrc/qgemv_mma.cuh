@@ -46,7 +46,7 @@ struct Layout {
   static constexpr int C = 1;
   // bytes of a row's TMA box per stage: the super-block, for Q6_K a 16-byte
   // aligned superset of its 210 bytes (starts up to 14 bytes early)
-  static constexpr int BOX = (FMT == DQ_Q4_K || FMT == DQ_Q4_0) ? 144
+  static constexpr int BOX = (FMT == DQ_Q4_K || FMT == DQ_Q4_0 || FMT == DQ_NVFP4) ? 144
                              : (FMT == DQ_Q6_K)                   ? 240
                              : (FMT == DQ_Q5_K)                   ? 176
                                                                   : 272;
@@ -617,6 +617,54 @@ struct SBDot<DQ_Q4_0> {
       }
       mma_x<NT>(acc, 0, lo[0], lo[1], lo[2], lo[3], xcol, kb + 32 * s + 4 * t);
       mma_x<NT>(acc, 1, hi[0], hi[1], hi[2], hi[3], xcol, kb + 32 * s + 16 + 4 * t);
+    }
+  }
+};
+
+// NVFP4: lane t owns the four 16-weight blocks 4t..4t+3 (weights 64t..64t+63,
+// code bytes 32t..32t+31) and their scales (scale bytes 4t..4t+3).  Step m
+// (0..15) takes weights 64t+4m..+3: the hardware converts two code bytes to
+// two fp16 pairs (exact) and one HMUL2 applies the block's E4M3 scale
+// (exact: the products keep <= 6 significant bits and stay within
+// 2^-10..2688).  Absolute fp16 weights.
+template <>
+struct SBDot<DQ_NVFP4> {
+  static constexpr bool kRowScale = false;
+  template <int NT, bool PAIRX = false>
+  __device__ __forceinline__ static void run(uint32_t wrow, int pitch8,
+                                             const uint32_t (&xcol)[NT], int kb, int t,
+                                             float (&acc)[NT][2][4]) {
+    const uint32_t rows[2] = {wrow, wrow + pitch8};
+    uint32_t cw[2][8];
+    __half2 sc[2][4];
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      const uint4 a = lds_u128(rows[rr] + 16 + 32 * t), b = lds_u128(rows[rr] + 32 + 32 * t);
+      cw[rr][0] = a.x; cw[rr][1] = a.y; cw[rr][2] = a.z; cw[rr][3] = a.w;
+      cw[rr][4] = b.x; cw[rr][5] = b.y; cw[rr][6] = b.z; cw[rr][7] = b.w;
+      const uint32_t sw = lds_u32(rows[rr] + 4 * t);            // scales of blocks 4t..4t+3
+      const __half2 s01 = u32_as_h2(e4m3x2_to_h2((uint16_t)(sw & 0xFFFF)));
+      const __half2 s23 = u32_as_h2(e4m3x2_to_h2((uint16_t)(sw >> 16)));
+      sc[rr][0] = __low2half2(s01);
+      sc[rr][1] = __high2half2(s01);
+      sc[rr][2] = __low2half2(s23);
+      sc[rr][3] = __high2half2(s23);
+    }
+#pragma unroll
+    for (int wv = 0; wv < 8; ++wv) {                 // code word wv: steps 2wv, 2wv+1
+      uint32_t h0[4], h8[4];
+      e2m1x8_to_h2x4(cw[0][wv], h0);
+      e2m1x8_to_h2x4(cw[1][wv], h8);
+      const __half2 s0 = sc[0][wv >> 1], s8 = sc[1][wv >> 1];
+#pragma unroll
+      for (int hm = 0; hm < 2; ++hm) {
+        const int m = 2 * wv + hm;
+        const uint32_t a0 = h2_as_u32(__hmul2(u32_as_h2(h0[2 * hm]), s0));
+        const uint32_t a1 = h2_as_u32(__hmul2(u32_as_h2(h8[2 * hm]), s8));
+        const uint32_t a2 = h2_as_u32(__hmul2(u32_as_h2(h0[2 * hm + 1]), s0));
+        const uint32_t a3 = h2_as_u32(__hmul2(u32_as_h2(h8[2 * hm + 1]), s8));
+        mma_x<NT>(acc, m & 1, a0, a1, a2, a3, xcol, kb + 64 * t + 4 * m);
+      }
     }
   }
 };

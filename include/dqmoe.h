@@ -40,8 +40,8 @@
  *     of that row, consecutive, starting at byte n * row_bytes where
  *     row_bytes = (K/QK) * block_bytes.  Rows are consecutive.  W must be
  *     16-byte aligned and row_bytes a multiple of 16 (true for every shape
- *     with K a multiple of 256 for Q4_K, Q8_0, Q4_0 and Q5_K, of 2048 for
- *     Q6_K).
+ *     with K a multiple of 256 for Q4_K, Q8_0, Q4_0, Q5_K and NVFP4, of 2048
+ *     for Q6_K).
  *   - Activations x: [batch][K] row-major in x_dtype.  Outputs y: [batch][N]
  *     row-major, always fp32 (MoE activations reach ~1e7, beyond fp16).
  */
@@ -89,8 +89,18 @@ extern "C" {
 /*   w = d*sc_j*q - dmin*m_j as Q4_K.  Both are the other GGUF blocks the   */
 /*   [KTransformers, §支持的量化格式] list names beside Q4_K, Q6_K, Q8_0;    */
 /*   dq_dequant and dq_qgemv take them, the MoE layer does not.             */
+/* NVFP4 super-block, 256 weights in 144 bytes (the pages name NVIDIA's FP4 */
+/*   as Blackwell's native 4-bit float, [Titan Engine, §激进量化策略], and    */
+/*   print no layout; this is the library's):                               */
+/*   bytes 0-15   E4M3 scales of the sixteen 16-weight blocks               */
+/*   bytes 16-143 E2M1 codes, weight 2i in the low nibble of byte 16+i,     */
+/*                weight 2i+1 in its high nibble                            */
+/*   w = e2m1(code) * e4m3(scale[i/16]); a per-tensor scale, where a model  */
+/*   has one, is the caller's (it commutes with the product).  NaN scale    */
+/*   bytes are out of contract.  dq_dequant and dq_qgemv only.              */
 /* ------------------------------------------------------------------------ */
-typedef enum { DQ_Q4_K = 1, DQ_Q6_K = 2, DQ_Q8_0 = 3, DQ_Q4_0 = 4, DQ_Q5_K = 5 } dq_fmt;
+typedef enum { DQ_Q4_K = 1, DQ_Q6_K = 2, DQ_Q8_0 = 3, DQ_Q4_0 = 4, DQ_Q5_K = 5,
+               DQ_NVFP4 = 6 } dq_fmt;
 
 /* Activation element types accepted by the entry points. */
 typedef enum { DQ_F32 = 0, DQ_F16 = 1, DQ_BF16 = 2 } dq_dtype;
@@ -113,6 +123,7 @@ typedef enum {
 #define DQ_QK4_0 32         /* weights per Q4_0 block */
 #define DQ_Q4_0_BYTES 18
 #define DQ_Q5_K_BYTES 176
+#define DQ_NVFP4_BYTES 144  /* per 256-weight super-block */
 #define DQ_MAX_BATCH 8      /* activation columns per dq_qgemv call */
 
 /* Weights per block and bytes per block of `fmt`.  Host-only, no CUDA.

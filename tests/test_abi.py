@@ -82,16 +82,16 @@ def test_block_geometry_all_formats(so):
     qk, nb = ctypes.c_int(), ctypes.c_int()
     # Q4_K, Q6_K, Q8_0, Q4_0, Q5_K: the GGUF block sizes
     for fmt, want in [(1, (256, 144)), (2, (256, 210)), (3, (32, 34)), (4, (32, 18)),
-                      (5, (256, 176))]:
+                      (5, (256, 176)), (6, (256, 144))]:
         assert f(fmt, ctypes.byref(qk), ctypes.byref(nb)) == 0
         assert (qk.value, nb.value) == want
-    assert f(6, ctypes.byref(qk), ctypes.byref(nb)) == -1
+    assert f(7, ctypes.byref(qk), ctypes.byref(nb)) == -1
     assert f(0, ctypes.byref(qk), ctypes.byref(nb)) == -1
 
 
 def test_moe_rejects_gemv_only_formats(so):
-    # the MoE layer takes Q4_K / Q6_K / Q8_0 experts; Q4_0 and Q5_K are
-    # dequant / qGEMV formats: refused before anything is launched
+    # the MoE layer takes Q4_K / Q6_K / Q8_0 experts; Q4_0, Q5_K and NVFP4
+    # are dequant / qGEMV formats: refused before anything is launched
     class Desc(ctypes.Structure):
         _fields_ = [("E", ctypes.c_int32), ("top_k", ctypes.c_int32), ("hidden", ctypes.c_int32),
                     ("ffn", ctypes.c_int32), ("n_shared", ctypes.c_int32), ("fmt", ctypes.c_int32),
@@ -103,6 +103,6 @@ def test_moe_rejects_gemv_only_formats(so):
     n = ctypes.c_size_t()
     f = so.dq_moe_workspace_size
     f.argtypes = [ctypes.POINTER(Desc), ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]
-    for fmt, rc in [(1, 0), (4, -3), (5, -3)]:
+    for fmt, rc in [(1, 0), (4, -3), (5, -3), (6, -3)]:
         d = Desc(8, 2, 512, 512, 0, fmt, a, a, a, a, None, None, None)
         assert f(ctypes.byref(d), 4, ctypes.byref(n)) == rc, fmt

@@ -13,7 +13,7 @@ from gpu_util import TOL, dev_act, dev_bytes, rel_err
 
 pytestmark = pytest.mark.gpu
 
-Q4_K, Q6_K, Q8_0, Q4_0, Q5_K = 1, 2, 3, 4, 5
+Q4_K, Q6_K, Q8_0, Q4_0, Q5_K, NVFP4 = 1, 2, 3, 4, 5, 6
 
 
 @pytest.fixture(scope="module")
@@ -24,7 +24,7 @@ def dq():
 
 
 @pytest.mark.parametrize("fmt,qk", [(Q4_K, 256), (Q6_K, 256), (Q8_0, 32), (Q4_0, 32),
-                                    (Q5_K, 256)])
+                                    (Q5_K, 256), (NVFP4, 256)])
 def test_dequant_bit_exact_random(dq, orc, fmt, qk):
     g = synth.streams(31 + fmt, 1)[0]
     raw = synth.quant_matrix(g, fmt, 37, 4096)
@@ -64,7 +64,7 @@ def _case(dq, orc, fmt, N, K, B, xdt, seed, ksplit=None, rows=None, xscale=1.0):
     return rel_err(got, ref)
 
 
-@pytest.mark.parametrize("fmt", [Q4_K, Q6_K, Q8_0, Q4_0, Q5_K])
+@pytest.mark.parametrize("fmt", [Q4_K, Q6_K, Q8_0, Q4_0, Q5_K, NVFP4])
 @pytest.mark.parametrize("xdt", [0, 1, 2])
 @pytest.mark.parametrize("B", [1, 3, 8])
 def test_qgemv_small_ragged(dq, orc, fmt, xdt, B):
@@ -74,7 +74,7 @@ def test_qgemv_small_ragged(dq, orc, fmt, xdt, B):
     assert err <= TOL[xdt], err
 
 
-@pytest.mark.parametrize("fmt", [Q4_K, Q6_K, Q8_0, Q4_0, Q5_K])
+@pytest.mark.parametrize("fmt", [Q4_K, Q6_K, Q8_0, Q4_0, Q5_K, NVFP4])
 @pytest.mark.parametrize("ks", [1, 2, 3, 5, 8])
 def test_qgemv_cluster_ksplit(dq, orc, fmt, ks):
     N, K = 130, 8192
@@ -187,7 +187,7 @@ def test_qgemv_weights_early_and_chains(dq, orc):
 
 
 # ---------------------------------------------------------- Q4_0 and Q5_K
-@pytest.mark.parametrize("fmt", [Q4_0, Q5_K])
+@pytest.mark.parametrize("fmt", [Q4_0, Q5_K, NVFP4])
 @pytest.mark.parametrize("B", [1, 8])
 def test_gemv_only_formats_70b_shape(dq, orc, fmt, B):
     # the 70B gate shape in the two qGEMV-only formats, sampled rows
@@ -212,3 +212,21 @@ def test_q5k_fifth_bits_matter_on_gpu(dq, orc):
     for y, r in zip(ys, refs):
         assert rel_err(y, r) <= TOL[1]
     assert rel_err(ys[0], refs[1]) > 10 * TOL[1]
+
+
+def test_nvfp4_every_code_and_scale_on_gpu(dq, orc):
+    # all 16 E2M1 codes against every positive finite E4M3 scale byte (and a
+    # few negative ones): the hardware conversions, the code order within a
+    # byte and the scale order must all match the oracle bit for bit
+    scales = np.array([b for b in range(0, 0x7F)] + [0x80, 0xB8, 0xC0, 0xFE], dtype=np.uint8)
+    nsb = (len(scales) + 15) // 16
+    blocks = np.zeros((nsb, 144), dtype=np.uint8)
+    flat = np.full(nsb * 16, 0x38, dtype=np.uint8)
+    flat[:len(scales)] = scales
+    blocks[:, 0:16] = flat.reshape(nsb, 16)
+    codes = np.arange(256) % 16
+    blocks[:, 16:144] = (codes[0::2] | (codes[1::2] << 4)).astype(np.uint8)
+    raw = blocks.reshape(-1)
+    got = dq.dequant(NVFP4, dev_bytes(raw), nsb * 256).cpu().numpy()
+    ref = orc.dequant(NVFP4, raw, nsb * 256)
+    assert got.view(np.uint32).tolist() == ref.view(np.uint32).tolist()
