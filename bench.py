@@ -471,14 +471,15 @@ def bench_gemv_70b(torch, dq, reps=50):
                     "in graphs of 8 (4 rotating weight copies, 528 MB > L2)"}
 
 
-def bench_gemv_70b_formats(torch, dq, reps=30):
+def bench_gemv_70b_formats(torch, dq, reps=30, fmts=((Q4_K, "q4_k"), (2, "q6_k"), (3, "q8_0")),
+                           shapes=None):
     """The 70B-shaped linears (gate 28672x8192, down 8192x28672, q 8192x8192) in
     Q4_K / Q6_K / Q8_0 at batch 1 and 8: one launch between two events, 4
     rotating weight copies."""
     out = {}
     g = synth.streams(synth.BASE_SEED + 7, 2)
-    for fmt, fname in ((Q4_K, "q4_k"), (2, "q6_k"), (3, "q8_0")):
-        for name, N, K in synth.LLAMA70B_LINEARS[1:]:       # up (= gate shape), down, q
+    for fmt, fname in fmts:
+        for name, N, K in (shapes or synth.LLAMA70B_LINEARS[1:]):   # up (= gate shape), down, q
             W0 = torch.from_numpy(synth.quant_matrix(g[0], fmt, N, K)).cuda()
             Ws = [W0] + [W0.clone() for _ in range(ROTATE - 1)]
             wb = weight_bytes(fmt, N, K)
@@ -591,6 +592,12 @@ def run_ours(args):
         for v in f70.values():
             v["frac_of_hbm"] = round(v["weight_GBps"] / peak, 4)
         extra["gemv_70b_formats"] = f70
+        # the further block formats (Q4_0, Q5_K, NVFP4) on the gate shape
+        fx = bench_gemv_70b_formats(torch, dq, fmts=((4, "q4_0"), (5, "q5_k"), (6, "nvfp4")),
+                                    shapes=[("up", 28672, 8192)])
+        for v in fx.values():
+            v["frac_of_hbm"] = round(v["weight_GBps"] / peak, 4)
+        extra["gemv_70b_more_formats"] = fx
         if not args.no_moe:
             moe = {}
             moe["mixtral_T16"] = bench_moe(torch, dq, synth.MOE_MIXTRAL, 16)

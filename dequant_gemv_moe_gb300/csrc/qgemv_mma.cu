@@ -188,24 +188,22 @@ int device_sms() {
   return sms;
 }
 
-// Pick the K-split (cluster size, 1..8).  Model: about three 64-row CTAs per
-// SM keep HBM busy; a CTA costs its super-blocks plus a fixed pipeline fill
-// and drain of about two super-blocks; CTAs beyond three per SM run in another
-// round.  Splitting only pays when the tiles alone leave SMs idle (measured on
-// GB300: the 28672 x 8192 matrix runs best unsplit, 14336 x 4096 split in 2).
+// Pick the K-split (cluster size).  Measured on GB300 (graphs of back-to-back
+// launches): with two or more 64-row tiles per SM the unsplit grid (or a split
+// in two for long rows) is within a few percent of the best; with fewer, the
+// best split is the largest power of
+// two whose CTAs all fit at once (four per SM, the 56 KB shared-memory
+// budget).  Odd cluster sizes (3, 5, 6, 7) measured slower than the
+// neighbouring powers of two on every shape tried: a cluster's CTAs share one
+// GPC, and odd sizes leave SMs of it idle.
 int choose_ksplit(int tiles, int nsb, int sms) {
-  int best = 1;
-  long best_cost = -1;
-  for (int s = 1; s <= 8 && s <= nsb; ++s) {
-    const long ctas = (long)tiles * s;
-    const long rounds = (ctas + 3L * sms - 1) / (3L * sms);
-    const long cost = rounds * ((nsb + s - 1) / s + 2);
-    if (best_cost < 0 || cost < best_cost) {
-      best_cost = cost;
-      best = s;
-    }
-  }
-  return best;
+  // many tiles: unsplit, except long rows (>= 32 super-blocks), where halving
+  // each CTA's range measured 6-11% faster (28672 x 8192; at 28672 x 4096 the
+  // split gained nothing)
+  if (tiles >= 2 * sms) return (nsb >= 32 && (long)tiles * 2 <= 8L * sms) ? 2 : 1;
+  int s = 1;
+  while (2 * s <= 8 && 2 * s <= nsb && (long)tiles * 2 * s <= 4L * sms) s *= 2;
+  return s;
 }
 
 }  // namespace
