@@ -194,11 +194,11 @@ def max_over_ranks(dist, v):
 # ---------------------------------------------------------------------------
 # CPU oracle baseline (bounded sample of the same work)
 # ---------------------------------------------------------------------------
-def oracle_sample(budget_s=12.0, seed=synth.BASE_SEED + 1):
+def oracle_sample(budget_s=12.0, seed=synth.BASE_SEED + 1, threads=None):
     import oracle
     g = synth.streams(seed, 2)
     x = synth.activations(g[1], (1, 14336), 1)
-    threads = oracle.default_threads()
+    threads = threads or oracle.default_threads()
     total_bytes, total_t, rows_done = 0, 0.0, 0
     rng = np.random.default_rng(0)
     mats = {}
@@ -613,6 +613,9 @@ def run_ours(args):
             "note": "the same layer with q, k, v, gate, up as five separate matrices: "
                     "seven dq_qgemv launches per step"}
         cpu = oracle_sample()
+        one = oracle_sample(budget_s=4.0, threads=1)
+        cpu["value_1_thread"] = one["value"]
+        cpu["sample_1_thread"] = one["sample"]
     if rank != 0:
         return
     kern_bytes = (lay["weight_bytes"] + lay["act_bytes"]) / lay["n_linears"]
