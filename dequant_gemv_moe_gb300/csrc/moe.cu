@@ -168,8 +168,8 @@ __global__ void __launch_bounds__(256) router_stream_kernel(const float* __restr
   if (e >= E) return;
   const float4* w = (const float4*)(Wr + (int64_t)e * H + h0);
   float acc[kRouterStreamT] = {};
-#pragma unroll 4
-  for (int j = lane; j < n / 4; j += 32) {
+#pragma unroll 8
+  for (int j = lane; j < n / 4; j += 32) {   // a full chunk: 8 loads in flight per lane
     const float4 wv = __ldcs(w + j);
 #pragma unroll
     for (int t = 0; t < kRouterStreamT; ++t) {
@@ -211,15 +211,28 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ par
   if (t >= T) return;
   float v[8];
   int id[8];
+  // sum the KS partials of this lane's 8 experts in a fixed order (q
+  // ascending); the 8 experts' loads of one q are independent and in flight
+  // together, so KS rounds of memory latency rather than 8 * KS
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[j] = 0.f;
+  for (int q = 0; q < KS; ++q) {
+    const float* pq = part + ((int64_t)q * T + t) * E;
+    float a[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int e = lane + 32 * j;
+      a[j] = e < E ? __ldg(pq + e) : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] += a[j];
+  }
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const int e = lane + 32 * j;
     id[j] = e;
     if (e < E) {
-      float s = 0.f;
-      for (int q = 0; q < KS; ++q) s += part[((int64_t)q * T + t) * E + e];   // fixed order
-      v[j] = s;
-      if (logits) logits[(int64_t)t * E + e] = s;
+      if (logits) logits[(int64_t)t * E + e] = v[j];
     } else {
       v[j] = -INFINITY;
       id[j] = 0x7fffffff;
@@ -227,7 +240,11 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ par
   }
   float sv[8];
   int si[8];
-  for (int i = 0; i < k; ++i) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {             // k <= 8 rounds, registers only
+    sv[i] = -INFINITY;
+    si[i] = 0;
+    if (i >= k) continue;
     float bv = -INFINITY;
     int bi = 0x7fffffff;
 #pragma unroll
@@ -257,17 +274,78 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ par
   if (lane == 0) {
     // softmax over all E renormalised over the selection
     float z = 0.f;
-    for (int i = 0; i < k; ++i) z += expf(sv[i] - sv[0]);
-    for (int i = 0; i < k; ++i) {
-      idx[(int64_t)t * k + i] = si[i];
-      gate[(int64_t)t * k + i] = expf(sv[i] - sv[0]) / z;
-    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (i < k) z += expf(sv[i] - sv[0]);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (i < k) {
+        idx[(int64_t)t * k + i] = si[i];
+        gate[(int64_t)t * k + i] = expf(sv[i] - sv[0]) / z;
+      }
   }
 }
 
 // ===========================================================================
 // 3. stable permute + work groups: one CTA of 1024 threads
 // ===========================================================================
+// Exclusive scan of v over threads 0..255 of the CTA (warp shuffles, then the
+// eight warp totals): returns the sum of v over lower threads; *total gets the
+// sum over all 256.  Every thread of the CTA calls it (two barriers).
+__device__ __forceinline__ int block_scan256(int v, int* wsum, int* total) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int inc = tid < 256 ? v : 0;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += n;
+  }
+  if (tid < 256 && lane == 31) wsum[warp] = inc;
+  __syncthreads();
+  int before = 0, all = 0;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const int c = wsum[w];
+    if (w < warp) before += c;
+    all += c;
+  }
+  __syncthreads();   // wsum may be reused by the next call
+  *total = all;
+  return tid < 256 ? before + inc - v : 0;
+}
+
+// Few tokens: the permute CTA also converts x to fp16 with a power-of-two
+// scale per token (the x16 prep of the expert kernels), saving a launch on
+// the decode path.  Rows of at most 8192 values.
+__device__ __forceinline__ void x16_rows_cta(const void* x, int xdt, int T, int K, __half* out,
+                                             float* inv, float* red) {
+  for (int row = 0; row < T; ++row) {
+    const int64_t base = (int64_t)row * K;
+    float v[8];
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {                  // K <= 8192
+      const int k = threadIdx.x + 1024 * i;
+      v[i] = k < K ? act_f32(x, xdt, base + k) : 0.f;
+      amax = fmaxf(amax, fabsf(v[i]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+    __syncthreads();
+    amax = 0.f;
+    for (int w = 0; w < 32; ++w) amax = fmaxf(amax, red[w]);
+    __syncthreads();
+    float sc, iv;
+    pow2_scale(amax, sc, iv);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int k = threadIdx.x + 1024 * i;
+      if (k < K) out[base + k] = __float2half_rn(v[i] * sc);
+    }
+    if (threadIdx.x == 0) inv[row] = iv;
+  }
+}
 __global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict__ idx, int T,
                                                        int k, int E, int n_shared, int gw,
                                                        int32_t* __restrict__ offsets,
@@ -277,9 +355,15 @@ __global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict
                                                        int4* __restrict__ groups,
                                                        int32_t* __restrict__ n_groups,
                                                        int4* __restrict__ units,
-                                                       int32_t* __restrict__ n_units) {
+                                                       int32_t* __restrict__ n_units,
+                                                       const void* __restrict__ cx, int cxdt,
+                                                       int cK, __half* __restrict__ cx16,
+                                                       float* __restrict__ cxinv) {
   pdl_wait();
   pdl_trigger();
+  __shared__ float red[32];
+  __shared__ int wsum[8];
+  if (cx16) x16_rows_cta(cx, cxdt, T, cK, cx16, cxinv, red);
   __shared__ int cnt[256];
   __shared__ int off[257];
   __shared__ int run[256];
@@ -292,15 +376,12 @@ __global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict
   __syncthreads();
   for (int p = tid; p < P; p += 1024) atomicAdd(&cnt[idx[p]], 1);
   __syncthreads();
-  // exclusive scan of counts (E <= 256), Hillis-Steele on off[1..E]
-  if (tid < 256) off[tid + 1] = (tid < E) ? cnt[tid] : 0;
-  if (tid == 0) off[0] = 0;
-  __syncthreads();
-  for (int d = 1; d < 256; d <<= 1) {
-    int v = 0;
-    if (tid < 256 && tid + 1 > d) v = off[tid + 1 - d];
-    __syncthreads();
-    if (tid < 256) off[tid + 1] += v;
+  // exclusive scan of counts (E <= 256)
+  {
+    int total;
+    const int ex = block_scan256(tid < E ? cnt[tid] : 0, wsum, &total);
+    if (tid < 256) off[tid] = ex;
+    if (tid == 0) off[256] = total;
     __syncthreads();
   }
   if (tid <= E && offsets) offsets[tid] = off[tid];
@@ -342,27 +423,19 @@ __global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict
   // wide units of <= 128 columns (more tokens); experts in order, then the
   // shared experts (all T tokens)
   const bool wide_ok = units != nullptr;
-  if (tid < 256) {
+  {
     const int n = (tid < E) ? cnt[tid] : 0;
     const bool w = wide_ok && n > kWide;
-    gsc[tid + 1] = w ? 0 : (n + gw - 1) / gw;
-    usc[tid + 1] = w ? (n + 127) / 128 : 0;
-  }
-  if (tid == 0) {
-    gsc[0] = 0;
-    usc[0] = 0;
-  }
-  __syncthreads();
-  for (int d = 1; d < 256; d <<= 1) {
-    int v = 0, w = 0;
-    if (tid < 256 && tid + 1 > d) {
-      v = gsc[tid + 1 - d];
-      w = usc[tid + 1 - d];
-    }
-    __syncthreads();
+    int gtot, utot;
+    const int gex = block_scan256(w ? 0 : (n + gw - 1) / gw, wsum, &gtot);
+    const int uex = block_scan256(w ? (n + 127) / 128 : 0, wsum, &utot);
     if (tid < 256) {
-      gsc[tid + 1] += v;
-      usc[tid + 1] += w;
+      gsc[tid] = gex;
+      usc[tid] = uex;
+    }
+    if (tid == 0) {
+      gsc[256] = gtot;
+      usc[256] = utot;
     }
     __syncthreads();
   }
@@ -767,8 +840,9 @@ int launch_router(const float* Wr, int E, int H, const void* x, int xdt, int T, 
 
 int launch_permute(const int32_t* idx, int T, int k, int E, int32_t* offsets, int32_t* sorted,
                    cudaStream_t s) {
-  launch_pdl(permute_kernel, dim3(1), dim3(1024), 0, s, 0, idx, T, k, E, 0, 8, offsets, sorted, nullptr, nullptr,
-                                    nullptr, nullptr, nullptr, nullptr);
+  launch_pdl(permute_kernel, dim3(1), dim3(1024), 0, s, 0, idx, T, k, E, 0, 8, offsets, sorted,
+             nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, 0, 0, nullptr,
+             nullptr);
   return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
 }
 
@@ -794,14 +868,18 @@ int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, floa
   if (rc != DQ_OK) return rc;
   int4* units = (int4*)(w + pl.off_units);
   int32_t* nunits = (int32_t*)(w + pl.off_nunits);
-  launch_pdl(permute_kernel, dim3(1), dim3(1024), 0, s, 0, idx, T, d.top_k, d.E, d.n_shared, pl.GW, offsets, sorted,
-                                    inv, tok, groups, ngroups, pl.wide ? units : nullptr,
-                                    nunits);
+  __half* x16t = (__half*)(w + pl.off_x16t);
+  float* xinvt = (float*)(w + pl.off_xinvt);
+  // one or two tokens of bf16/fp32 x: the permute CTA also makes their fp16
+  // copy (measured: one launch less at T=1; at T=8 eight CTAs are faster)
+  const bool fuse_x16 = xdt != DQ_F16 && T <= 2 && d.hidden <= 8192;
+  launch_pdl(permute_kernel, dim3(1), dim3(1024), 0, s, 0, idx, T, d.top_k, d.E, d.n_shared,
+             pl.GW, offsets, sorted, inv, tok, groups, ngroups, pl.wide ? units : nullptr, nunits,
+             fuse_x16 ? x : nullptr, xdt, d.hidden, fuse_x16 ? x16t : nullptr,
+             fuse_x16 ? xinvt : nullptr);
   if (cudaGetLastError() != cudaSuccess) return DQ_ERR_CUDA;
 
   const int q = qk(d.fmt), bb = blk_bytes(d.fmt);
-  __half* x16t = (__half*)(w + pl.off_x16t);
-  float* xinvt = (float*)(w + pl.off_xinvt);
   __half* h16 = (__half*)(w + pl.off_h16);
   float* hinv = (float*)(w + pl.off_hinv);
   __half* x16 = (__half*)(w + pl.off_x16);
@@ -813,8 +891,10 @@ int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, floa
   const __half* xh = (const __half*)x;
   const float* xh_inv = nullptr;
   if (xdt != DQ_F16) {
-    rc = launch_x16_rows(x, xdt, T, d.hidden, x16t, xinvt, s);
-    if (rc != DQ_OK) return rc;
+    if (!fuse_x16) {
+      rc = launch_x16_rows(x, xdt, T, d.hidden, x16t, xinvt, s);
+      if (rc != DQ_OK) return rc;
+    }
     xh = x16t;
     xh_inv = xinvt;
   }

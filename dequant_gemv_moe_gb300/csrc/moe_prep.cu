@@ -38,10 +38,33 @@ __global__ void __launch_bounds__(256) x16_tokens_kernel(const void* __restrict_
   pdl_wait();
   pdl_trigger();
   __shared__ float red[8];
+  constexpr int R = 32;                 // values kept in registers per thread
   const int row = blockIdx.x;
   const int64_t base = (int64_t)row * K;
+  const bool in_regs = K <= 256 * R;
+  float v[R];
   float amax = 0.f;
-  for (int k = threadIdx.x; k < K; k += 256) amax = fmaxf(amax, fabsf(act(x, xdt, base + k)));
+  if (in_regs) {
+    // every load of the row is issued before any is used
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      const int k = threadIdx.x + 256 * i;
+      v[i] = k < K ? act(x, xdt, base + k) : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < R; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  } else {
+    for (int k0 = threadIdx.x; k0 < K; k0 += 256 * 8) {
+      float a[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int k = k0 + 256 * i;
+        a[i] = k < K ? act(x, xdt, base + k) : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(a[i]));
+    }
+  }
   amax = wmax(amax);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
   __syncthreads();
@@ -50,7 +73,27 @@ __global__ void __launch_bounds__(256) x16_tokens_kernel(const void* __restrict_
   for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
   float sc, iv;
   pow2_scale(amax, sc, iv);
-  for (int k = threadIdx.x; k < K; k += 256) out[base + k] = __float2half_rn(act(x, xdt, base + k) * sc);
+  if (in_regs) {
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      const int k = threadIdx.x + 256 * i;
+      if (k < K) out[base + k] = __float2half_rn(v[i] * sc);
+    }
+  } else {
+    for (int k0 = threadIdx.x; k0 < K; k0 += 256 * 8) {
+      float a[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int k = k0 + 256 * i;
+        a[i] = k < K ? act(x, xdt, base + k) : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int k = k0 + 256 * i;
+        if (k < K) out[base + k] = __float2half_rn(a[i] * sc);
+      }
+    }
+  }
   if (threadIdx.x == 0) inv[row] = iv;
 }
 
