@@ -62,6 +62,12 @@ def run_case(args):
         print(json.dumps(bench_moe(torch, dq, synth.MOE_MIXTRAL, 16, reps=max(1, args.steps))))
     elif args.case == "formats70b":
         print(json.dumps(bench_gemv_70b_formats(torch, dq, reps=max(1, args.steps))))
+    elif args.case == "ds64":
+        # DeepSeek-V3 expert shapes, 64 routed experts (+1 shared), T = 64: ~8
+        # tokens per expert as at T=256 of the full layer (16-column groups);
+        # 1.6 GB of weights (a small case for full captures of that kernel)
+        cfg = dict(synth.MOE_DEEPSEEK, E=64)
+        print(json.dumps(bench_moe(torch, dq, cfg, 64, reps=max(1, args.steps))))
     elif args.case == "prefill32":
         # DeepSeek-V3 expert shapes with 32 routed experts (+1 shared), T = 256:
         # ~64 tokens per expert, every expert on the tcgen05 grouped GEMM; 0.8 GB
