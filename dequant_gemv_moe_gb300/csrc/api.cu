@@ -27,7 +27,9 @@ namespace {
 
 bool fmt_ok(int fmt) { return fmt >= DQ_Q4_K && fmt <= DQ_NVFP4; }
 // formats of the MoE layer's expert matrices
-bool moe_fmt_ok(int fmt) { return fmt == DQ_Q4_K || fmt == DQ_Q6_K || fmt == DQ_Q8_0; }
+bool moe_fmt_ok(int fmt) {
+  return fmt == DQ_Q4_K || fmt == DQ_Q6_K || fmt == DQ_Q8_0 || fmt == DQ_NVFP4;
+}
 bool dtype_ok(int dt) { return dt == DQ_F32 || dt == DQ_F16 || dt == DQ_BF16; }
 bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
 

@@ -753,7 +753,9 @@ int sm_count() {
 }
 
 int qk(int fmt) { return fmt == DQ_Q8_0 ? 32 : 256; }
-int blk_bytes(int fmt) { return fmt == DQ_Q4_K ? 144 : fmt == DQ_Q6_K ? 210 : 34; }
+int blk_bytes(int fmt) {
+  return (fmt == DQ_Q4_K || fmt == DQ_NVFP4) ? 144 : fmt == DQ_Q6_K ? 210 : 34;
+}
 
 template <int FMT, bool GATEUP, int NT>
 int launch_grouped(const GroupedParams& gp_in, int units_max, cudaStream_t s, int E, int n_shared) {
@@ -805,6 +807,7 @@ int launch_grouped_fmt(int fmt, int nt, const GroupedParams& gp, int units_max, 
   DQ_GROUPED(DQ_Q4_K, 1) DQ_GROUPED(DQ_Q4_K, 2) DQ_GROUPED(DQ_Q4_K, 4)
   DQ_GROUPED(DQ_Q6_K, 1) DQ_GROUPED(DQ_Q6_K, 2) DQ_GROUPED(DQ_Q6_K, 4)
   DQ_GROUPED(DQ_Q8_0, 1) DQ_GROUPED(DQ_Q8_0, 2) DQ_GROUPED(DQ_Q8_0, 4)
+  DQ_GROUPED(DQ_NVFP4, 1) DQ_GROUPED(DQ_NVFP4, 2) DQ_GROUPED(DQ_NVFP4, 4)
 #undef DQ_GROUPED
   return DQ_ERR_UNSUPPORTED;
 }

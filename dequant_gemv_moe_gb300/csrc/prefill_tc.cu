@@ -131,6 +131,31 @@ struct SlabDecode<DQ_Q8_0> {
   }
 };
 
+// NVFP4: slab q = weights 64q..64q+63 = code bytes 32q..32q+31 of the codes
+// and the scales of blocks 4q..4q+3; exact fp16 weights from the hardware
+// conversions times the block scale.
+template <>
+struct SlabDecode<DQ_NVFP4> {
+  __device__ __forceinline__ static void run(uint32_t rb, int q, uint4 (&out)[8]) {
+    const uint32_t sw = lds_u32(rb + 4 * q);
+    const __half2 s01 = u32_as_h2(e4m3x2_to_h2((uint16_t)(sw & 0xFFFF)));
+    const __half2 s23 = u32_as_h2(e4m3x2_to_h2((uint16_t)(sw >> 16)));
+    const __half2 sc[4] = {__low2half2(s01), __high2half2(s01), __low2half2(s23),
+                           __high2half2(s23)};
+    const uint4 a = lds_u128(rb + 16 + 32 * q), b = lds_u128(rb + 32 + 32 * q);
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {                     // weights 64q+8c..+7: block 4q + c/2
+      uint32_t h[4];
+      e2m1x8_to_h2x4(w[c], h);
+      uint32_t r[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) r[i] = h2_as_u32(__hmul2(u32_as_h2(h[i]), sc[c >> 1]));
+      out[c] = make_uint4(r[0], r[1], r[2], r[3]);
+    }
+  }
+};
+
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
@@ -313,7 +338,7 @@ int launch_tc_fmt(const void* W, const void* Wsh, int E, int n_shared, int rows_
   TcParams p;
   memset(&p, 0, sizeof(p));
   const int qk = FMT == DQ_Q8_0 ? 32 : 256;
-  const int bb = FMT == DQ_Q4_K ? 144 : FMT == DQ_Q6_K ? 210 : 34;
+  const int bb = Layout<FMT>::SBB * qk / 256;   // bytes per quantisation block
   const uint64_t row_bytes = (uint64_t)(K / qk) * bb;
   if (!make_weight_tmap(&p.wmap, W, (uint64_t)rows_per_expert * E, row_bytes, TL::BOX, kTcRows))
     return DQ_ERR_CUDA;
@@ -356,8 +381,11 @@ int launch_tc_gemm(int fmt, const void* W, const void* Wsh, int E, int n_shared,
   if (fmt == DQ_Q6_K)
     return launch_tc_fmt<DQ_Q6_K>(W, Wsh, E, n_shared, rows_per_expert, K, units, n_units,
                                   max_units, X16, npos, xinv, out, out_stride, s);
-  return launch_tc_fmt<DQ_Q8_0>(W, Wsh, E, n_shared, rows_per_expert, K, units, n_units,
-                                max_units, X16, npos, xinv, out, out_stride, s);
+  if (fmt == DQ_Q8_0)
+    return launch_tc_fmt<DQ_Q8_0>(W, Wsh, E, n_shared, rows_per_expert, K, units, n_units,
+                                  max_units, X16, npos, xinv, out, out_stride, s);
+  return launch_tc_fmt<DQ_NVFP4>(W, Wsh, E, n_shared, rows_per_expert, K, units, n_units,
+                                 max_units, X16, npos, xinv, out, out_stride, s);
 }
 
 }  // namespace dqmoe

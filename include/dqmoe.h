@@ -211,7 +211,8 @@ typedef struct {
   int32_t hidden;     /* H: length of x rows, rows of W_down */
   int32_t ffn;        /* F: rows of W_gate / W_up, columns of W_down */
   int32_t n_shared;   /* always-on shared experts, 0..4, weight 1 each */
-  int32_t fmt;        /* dq_fmt of every expert matrix */
+  int32_t fmt;        /* dq_fmt of every expert matrix: DQ_Q4_K, DQ_Q6_K,
+                         DQ_Q8_0 or DQ_NVFP4 (others: DQ_ERR_UNSUPPORTED) */
   const float* router_W; /* device fp32 [E][H] */
   const void* w_gate; /* device, E stacked [F rows][H/QK blocks] matrices */
   const void* w_up;   /* device, E stacked [F][H/QK] */

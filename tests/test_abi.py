@@ -90,7 +90,7 @@ def test_block_geometry_all_formats(so):
 
 
 def test_moe_rejects_gemv_only_formats(so):
-    # the MoE layer takes Q4_K / Q6_K / Q8_0 experts; Q4_0, Q5_K and NVFP4
+    # the MoE layer takes Q4_K / Q6_K / Q8_0 / NVFP4 experts; Q4_0 and Q5_K
     # are dequant / qGEMV formats: refused before anything is launched
     class Desc(ctypes.Structure):
         _fields_ = [("E", ctypes.c_int32), ("top_k", ctypes.c_int32), ("hidden", ctypes.c_int32),
@@ -103,6 +103,6 @@ def test_moe_rejects_gemv_only_formats(so):
     n = ctypes.c_size_t()
     f = so.dq_moe_workspace_size
     f.argtypes = [ctypes.POINTER(Desc), ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]
-    for fmt, rc in [(1, 0), (4, -3), (5, -3), (6, -3)]:
+    for fmt, rc in [(1, 0), (6, 0), (4, -3), (5, -3)]:
         d = Desc(8, 2, 512, 512, 0, fmt, a, a, a, a, None, None, None)
         assert f(ctypes.byref(d), 4, ctypes.byref(n)) == rc, fmt

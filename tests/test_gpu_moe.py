@@ -15,7 +15,7 @@ from gpu_util import dev_act, dev_bytes, rel_err
 
 pytestmark = pytest.mark.gpu
 
-Q4_K, Q6_K, Q8_0 = 1, 2, 3
+Q4_K, Q6_K, Q8_0, NVFP4 = 1, 2, 3, 6
 MOE_TOL = 2e-3
 
 
@@ -127,6 +127,12 @@ def _moe_case(dq, orc, fmt, E, k, H, F, ns, T, xdt, seed, tokens=None):
     (Q4_K, 4, 2, 512, 512, 1, 64, 1),
     (Q6_K, 2, 1, 2048, 2048, 0, 100, 2),
     (Q8_0, 2, 2, 256, 256, 1, 300, 0),
+    # NVFP4 experts: one-token decode, 16-column groups, 32-column groups,
+    # and the tcgen05 path
+    (NVFP4, 8, 2, 512, 1024, 1, 1, 2),
+    (NVFP4, 8, 2, 512, 512, 0, 30, 1),
+    (NVFP4, 4, 2, 768, 512, 1, 50, 0),
+    (NVFP4, 2, 2, 512, 256, 1, 90, 1),
 ])
 def test_moe_forward_small(dq, orc, fmt, E, k, H, F, ns, T, xdt):
     err, _ = _moe_case(dq, orc, fmt, E, k, H, F, ns, T, xdt, seed=3000 + E * 7 + T)

@@ -7,7 +7,7 @@ tile, 33 tokens) upwards, and compare the whole layer with the CPU oracle.
 """
 import pytest
 
-from test_gpu_moe import MOE_TOL, Q4_K, Q6_K, Q8_0, _moe_case, dq  # noqa: F401
+from test_gpu_moe import MOE_TOL, NVFP4, Q4_K, Q6_K, Q8_0, _moe_case, dq  # noqa: F401
 
 pytestmark = pytest.mark.gpu
 
@@ -17,6 +17,7 @@ pytestmark = pytest.mark.gpu
     (Q4_K, 1, 1, 512, 512, 1, 40, 2),       # shared expert too; 4 row tiles
     (Q8_0, 1, 1, 256, 256, 0, 130, 1),      # > 128 tokens: two units (128 + 2)
     (Q6_K, 1, 1, 2048, 2048, 0, 64, 0),     # Q6_K rows, fp32 activations
+    (NVFP4, 1, 1, 512, 256, 1, 150, 2),     # NVFP4 rows: two units, shared expert
 ])
 def test_tc_wide_units(dq, orc, fmt, E, k, H, F, ns, T, xdt):
     err, _ = _moe_case(dq, orc, fmt, E, k, H, F, ns, T, xdt, seed=7000 + T + E)
