@@ -175,6 +175,236 @@ __global__ void __launch_bounds__(kThreads) qgemv_mma_kernel(const __grid_consta
   }
 }
 
+// ---------------------------------------------------------------------------
+// Q4_K, one activation column: the block-diagonal core (Q4KB1).  Each stage
+// carries one super-block of 64 weight rows (TMA) and its 256 activations,
+// staged by the loader warp: fp16 values (bf16 input scaled by a power of two
+// per stage), the negated sum of each 32-value sub-block, and the stage's
+// inverse scale.  The loader keeps the activation loads of the next
+// kB1Prefetch stages in flight in registers.
+// ---------------------------------------------------------------------------
+constexpr int kB1Prefetch = 4;
+
+struct B1Plan {
+  int nstage, off_w, off_x, off_sx, off_inv, off_z, off_red, total;
+};
+
+__host__ __device__ inline B1Plan b1_plan(int nstage, int ksplit) {
+  B1Plan p;
+  p.nstage = nstage;
+  p.off_w = 1024;                                             // barriers below
+  p.off_x = p.off_w + nstage * Layout<DQ_Q4_K>::W_STAGE;      // 128-byte aligned
+  p.off_sx = p.off_x + nstage * Q4KB1::kStageX;
+  p.off_inv = p.off_sx + nstage * 32;
+  p.off_z = (p.off_inv + nstage * 4 + 127) / 128 * 128;       // 16 zero bytes at +0
+  p.off_red = p.off_z + 128;
+  p.total = p.off_red + (ksplit > 1 ? (ksplit - 1) * kConsumerWarps * 32 * 16 : 0);
+  return p;
+}
+
+struct B1Params {
+  CUtensorMap tmap;  // W as [N rows][row_bytes/2] 16-bit elements, box 144 B x 64 rows
+  int N;
+  int nsb;           // super-blocks per row
+  const void* x;     // [K], fp16 or bf16
+  float* y;          // [N]
+  int nstage;
+  int w_early;
+};
+
+// PAIR: each consumer iteration takes two stages (more independent work per
+// warp, more registers: three CTAs per SM instead of four).
+template <bool BF16, bool PAIR>
+__global__ void __launch_bounds__(kThreads, PAIR ? 3 : 4)
+    qgemv_q4k_b1_kernel(const __grid_constant__ B1Params p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  using L = Layout<DQ_Q4_K>;
+  const int ksplit = (int)cluster_nctarank();
+  const int rank = (int)cluster_ctarank();
+  const B1Plan plan = b1_plan(p.nstage, ksplit);
+  uint64_t* full = (uint64_t*)smem;
+  uint64_t* empty = full + plan.nstage;
+  uint64_t* red_full = empty + plan.nstage;
+  uint8_t* wbuf = smem + plan.off_w;
+  float* red = (float*)(smem + plan.off_red);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row0 = blockIdx.y * kTileRows;
+  const int sb0 = (int)((int64_t)p.nsb * rank / ksplit);
+  const int sb1 = (int)((int64_t)p.nsb * (rank + 1) / ksplit);
+  const int nsbl = sb1 - sb0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < plan.nstage; ++s) {
+      mbar_init(&full[s], 33);          // TMA bytes + one arrival per loader lane
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    if (ksplit > 1) mbar_init(red_full, (ksplit - 1) * kConsumerWarps * 32);
+    fence_barrier_init();
+  }
+  if (threadIdx.x < 32) ((uint32_t*)(smem + plan.off_z))[threadIdx.x] = 0u;
+  if (ksplit > 1) cluster_sync_all();
+  else __syncthreads();
+  pdl_trigger();
+
+  if (warp == 0) {
+    // ------------------------------- loader --------------------------------
+    const uint64_t pol = l2_evict_first_policy();
+    auto issue = [&](int c, int s) {
+      mbar_arrive_expect_tx(&full[s], L::W_STAGE);   // rows past N are zero-filled, still counted
+      tma_load_2d(wbuf + s * L::W_STAGE, &p.tmap, (int)(((int64_t)(sb0 + c) * L::SBB) >> 1),
+                  row0, &full[s], pol);
+    };
+    const int early = p.w_early ? min(plan.nstage, nsbl) : 0;
+    if (lane == 0) {
+      prefetch_tmap(&p.tmap);
+      // weights are read-only: stream them in while the previous kernel ends
+      for (int c = 0; c < early; ++c) issue(c, c);
+    }
+    pdl_wait();
+    // lane covers activations 8*lane .. 8*lane+7 of a stage; sub-block = lane/4
+    const uint4* xsrc = (const uint4*)((const uint16_t*)p.x + (int64_t)sb0 * 256) + lane;
+    uint4 xr[kB1Prefetch];
+#pragma unroll
+    for (int u = 0; u < kB1Prefetch; ++u)
+      if (u < nsbl) xr[u] = __ldg(xsrc + 32 * u);
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int c0 = 0; c0 < nsbl && ok; c0 += kB1Prefetch) {
+#pragma unroll
+      for (int u = 0; u < kB1Prefetch; ++u) {
+        const int c = c0 + u;
+        // warp-uniform: every lane leaves together after a timed-out wait
+        if (ok && c < nsbl && c >= plan.nstage)
+          ok = __all_sync(0xffffffffu, mbar_wait(&empty[s], ph ^ 1));
+        if (!ok || c >= nsbl) continue;
+        if (lane == 0 && c >= early) issue(c, s);
+        uint32_t h[4] = {xr[u].x, xr[u].y, xr[u].z, xr[u].w};
+        if (c + kB1Prefetch < nsbl) xr[u] = __ldg(xsrc + 32 * (c + kB1Prefetch));
+        float inv = 1.f;
+        if constexpr (BF16) {
+          float amax = 0.f;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(h[j] << 16)),
+                                     fabsf(__uint_as_float(h[j] & 0xFFFF0000u))));
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+          float scale;
+          pow2_scale(amax, scale, inv);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            h[j] = h2_as_u32(__floats2half2_rn(__uint_as_float(h[j] << 16) * scale,
+                                               __uint_as_float(h[j] & 0xFFFF0000u) * scale));
+        }
+        uint8_t* xst = smem + plan.off_x + s * Q4KB1::kStageX;
+        *(uint4*)(xst + 16 * lane) = make_uint4(h[0], h[1], h[2], h[3]);
+        if (lane & 4)   // odd sub-block: its negation too
+          *(uint4*)(xst + 512 + 16 * lane) = make_uint4(h[0] ^ 0x80008000u, h[1] ^ 0x80008000u,
+                                                        h[2] ^ 0x80008000u, h[3] ^ 0x80008000u);
+        float sum = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 f = __half22float2(u32_as_h2(h[j]));
+          sum += f.x;
+          sum += f.y;
+        }
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        if ((lane & 3) == 0) ((float*)(smem + plan.off_sx + s * 32))[lane >> 2] = -sum;
+        if (lane == 0) ((float*)(smem + plan.off_inv))[s] = inv;
+        mbar_arrive(&full[s]);
+        if (++s == plan.nstage) {
+          s = 0;
+          ph ^= 1;
+        }
+      }
+    }
+  } else {
+    // ------------------------------ consumers ------------------------------
+    const int cw = warp - 1, g = lane >> 2, t = lane & 3;
+    // mma row g is weight row rg (and rg + 8) of the warp's 16: rows 0,2,4,6
+    // in the first half-warp, 1,3,5,7 in the second, so that the 8-byte quant
+    // loads of a half-warp fall on 32 distinct banks (row pitch 144 bytes)
+    const int rg = 2 * (g & 3) + (g >> 2);
+    const Q4KB1::Lane lc = Q4KB1::lane_consts(g, t);
+    const uint32_t wrow = smem_u32(wbuf) + (16 * cw + rg) * L::ROW_PITCH;
+    const uint32_t xg = smem_u32(smem + plan.off_x) + 64 * g + 16 * t;
+    const uint32_t sx = smem_u32(smem + plan.off_sx) + 8 * t;
+    const uint32_t zb = smem_u32(smem + plan.off_z);
+    const float* invs = (const float*)(smem + plan.off_inv);
+    float2 accp0 = make_float2(0.f, 0.f), accp8 = make_float2(0.f, 0.f);
+    float2 accq0 = make_float2(0.f, 0.f), accq8 = make_float2(0.f, 0.f);
+    int s = 0;
+    uint32_t ph = 0;
+    auto stage = [&](int st, uint32_t o, float2& a0, float2& a8) {
+      Q4KB1::run(wrow + st * L::W_STAGE + o, 8 * L::ROW_PITCH, xg + Q4KB1::kStageX * st + o, zb,
+                 sx + 32 * st + o, BF16 ? invs[st] : 1.f, lc, a0, a8);
+    };
+    auto advance = [&]() {
+      if (++s == plan.nstage) {
+        s = 0;
+        ph ^= 1;
+      }
+    };
+    // two stages per iteration: independent work for the scheduler to interleave
+    int c = 0;
+    bool ok = true;
+    for (; PAIR && c + 1 < nsbl; c += 2) {
+      const int s0 = s;
+      if (!mbar_wait(&full[s], ph)) { ok = false; break; }
+      advance();
+      const int s1 = s;
+      if (!mbar_wait(&full[s], ph)) { ok = false; break; }
+      advance();
+      const uint32_t o = order_after_wait(0u);
+      stage(s0, o, accp0, accp8);
+      stage(s1, o, accq0, accq8);
+      keep_before_release(accp0.x, accp0.y, accp8.x, accp8.y);
+      keep_before_release(accq0.x, accq0.y, accq8.x, accq8.y);
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_relaxed(&empty[s0]);
+        mbar_arrive_relaxed(&empty[s1]);
+      }
+    }
+    for (; ok && c < nsbl; ++c) {
+      if (!mbar_wait(&full[s], ph)) break;
+      const uint32_t o = order_after_wait(0u);
+      stage(s, o, accp0, accp8);
+      keep_before_release(accp0.x, accp0.y, accp8.x, accp8.y);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_relaxed(&empty[s]);
+      advance();
+    }
+    float acc0 = (accp0.x + accp0.y) + (accq0.x + accq0.y);
+    float acc8 = (accp8.x + accp8.y) + (accq8.x + accq8.y);
+    // the four lanes of a quad hold sub-blocks (2t, 2t+1): fixed-order sum
+    acc0 += __shfl_xor_sync(0xffffffffu, acc0, 1);
+    acc8 += __shfl_xor_sync(0xffffffffu, acc8, 1);
+    acc0 += __shfl_xor_sync(0xffffffffu, acc0, 2);
+    acc8 += __shfl_xor_sync(0xffffffffu, acc8, 2);
+    if (ksplit > 1) {
+      if (rank != 0) {
+        float* slot = red + (((rank - 1) * kConsumerWarps + cw) * 32 + lane) * 4;
+        st_cluster_f32x4(slot, 0, acc0, acc8, 0.f, 0.f);
+        mbar_arrive_cluster(red_full, 0);
+      } else if (mbar_wait_cluster(red_full, 0)) {
+        for (int r = 1; r < ksplit; ++r) {   // fixed order: deterministic
+          const float4 v = *(const float4*)(red + (((r - 1) * kConsumerWarps + cw) * 32 + lane) * 4);
+          acc0 += v.x;
+          acc8 += v.y;
+        }
+      }
+    }
+    if (rank == 0 && t == 0) {
+      const int ra = row0 + 16 * cw + rg, rb = ra + 8;
+      if (ra < p.N) p.y[ra] = acc0;
+      if (rb < p.N) p.y[rb] = acc8;
+    }
+  }
+}
+
 namespace {
 
 int device_sms() {
@@ -255,8 +485,61 @@ int launch_qgemv_mma_fmt(const void* W, int64_t N, int64_t K, const void* x, int
   return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
 }
 
+// One fp16 / bf16 column of Q4_K: the block-diagonal kernel.
+int launch_qgemv_q4k_b1(const void* W, int64_t N, int64_t K, const void* x, int xdt, float* y,
+                        cudaStream_t stream, int force_ksplit, bool w_early) {
+  using L = Layout<DQ_Q4_K>;
+  B1Params p;
+  p.nsb = (int)(K / 256);
+  const int tiles = (int)((N + kTileRows - 1) / kTileRows);
+  const int sms = device_sms();
+  if (sms <= 0) return DQ_ERR_CUDA;
+  // with two or more tiles per SM the unsplit grid measured best for this
+  // kernel (28672 x 8192: 29.0 us unsplit, 29.3 us split in two)
+  int ks = force_ksplit > 0 ? force_ksplit
+                            : (tiles >= 2 * sms ? 1 : choose_ksplit(tiles, p.nsb, sms));
+  ks = std::max(1, std::min(ks, std::min(8, p.nsb)));
+  // grids that fit three CTAs per SM take the paired kernel with deeper rings
+  // (28672 x 8192: 23.8 us against 28.2 us); larger ones four CTAs per SM
+  const bool pair = (long)tiles * ks <= 3L * sms;
+  const int budget = pair ? 74 * 1024 : 56 * 1024;
+  int nstage = 12;
+  while (nstage > 3 && b1_plan(nstage, ks).total > budget) --nstage;
+  const B1Plan plan = b1_plan(nstage, ks);
+  if (!make_weight_tmap(&p.tmap, W, (uint64_t)N, (uint64_t)p.nsb * L::SBB, L::BOX, kTileRows))
+    return DQ_ERR_CUDA;
+  p.N = (int)N;
+  p.x = x;
+  p.y = y;
+  p.nstage = nstage;
+  p.w_early = w_early ? 1 : 0;
+  auto kern = xdt == DQ_BF16 ? (pair ? qgemv_q4k_b1_kernel<true, true>
+                                     : qgemv_q4k_b1_kernel<true, false>)
+                             : (pair ? qgemv_q4k_b1_kernel<false, true>
+                                     : qgemv_q4k_b1_kernel<false, false>);
+  static bool attr_set[4][64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int v = (xdt == DQ_BF16 ? 1 : 0) + (pair ? 2 : 0);
+  if (dev >= 64 || !attr_set[v][dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) !=
+        cudaSuccess)
+      return DQ_ERR_CUDA;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+        cudaSuccess)
+      return DQ_ERR_CUDA;
+    if (dev < 64) attr_set[v][dev] = true;
+  }
+  if (launch_pdl(kern, dim3((unsigned)ks, (unsigned)tiles, 1), dim3(kThreads), (size_t)plan.total,
+                 stream, ks, p) != cudaSuccess)
+    return DQ_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
+}
+
 int launch_qgemv_mma(int fmt, const void* W, int64_t N, int64_t K, const void* x, int xdt,
                      int batch, float* y, cudaStream_t s, int force_ksplit, bool w_early) {
+  if (fmt == DQ_Q4_K && batch == 1)
+    return launch_qgemv_q4k_b1(W, N, K, x, xdt, y, s, force_ksplit, w_early);
   if (fmt == DQ_Q4_K)
     return launch_qgemv_mma_fmt<DQ_Q4_K>(W, N, K, x, xdt, batch, y, s, force_ksplit, w_early);
   if (fmt == DQ_Q6_K)

@@ -669,4 +669,136 @@ struct SBDot<DQ_NVFP4> {
   }
 };
 
+// ---------------------------------------------------------------------------
+// Q4_K with one activation column (decode at batch 1).
+//
+// With a single column, the 8 columns of mma.m16n8k16 are free to carry the 8
+// sub-blocks of a super-block instead: B is block-diagonal (column j holds the
+// activations of sub-block j, zeros elsewhere), so one accumulator keeps the 8
+// per-sub-block dot products apart, and every scale and min is applied once per
+// sub-block, in fp32, after the products:
+//   y_row += d sc_j (sum_k q_k x_k) - dmin m_j (sum_k x_k)      (Q4_K, j = 0..7)
+// with the sub-block sums of x computed once per activation vector.
+//
+// A holds quant bytes spread into 16-bit lanes, read as exact fp16
+// subnormals: b * 2^-24 for a whole byte b = lo + 16 hi, lo * 2^-24 for its
+// low nibble.  Byte j of qs group c carries weight j of sub-block 2c (low
+// nibble) and of sub-block 2c+1 (high nibble), so with
+//   mma 1:  A = b,   B column 2c+1 = +x(2c+1)
+//   mma 2:  A = lo,  B column 2c = +x(2c),  column 2c+1 = -x(2c+1)
+// column 2c gets sum lo x and column 2c+1 gets 16 sum hi x: the high nibble
+// never needs its own mask.
+//
+// Lane (g, t) supplies rows g and g+8 and weights 8t..8t+7 of every
+// sub-block; its B fragment is real only for sub-block g (16 bytes of x, or
+// of -x for the second product of an odd sub-block) and reads zero bytes
+// otherwise.  Its accumulator ends with sub-blocks 2t and 2t+1 of both rows.
+// ---------------------------------------------------------------------------
+struct Q4KB1 {
+  // Per-lane constants, set once per kernel.
+  struct Lane {
+    int t;
+    uint32_t sel_a;    // byte selector: scale bytes 2(t&1), +1 of hd.y (t < 2) or hd.w (t >= 2)
+    uint32_t sel_b;    // the same bytes of the first source, zeros above them
+    uint32_t sh_m;     // mins of sub-blocks 4..7 sit in the high nibbles: shift 4
+    uint32_t mask_a;   // 6 (t < 2) or 4 (t >= 2) low bits per 16-bit lane
+    uint32_t mask_b;   // bits 4-5 of each lane from the top 2 bits (t >= 2 only)
+    uint32_t real[4];  // 1 for qs group c == g/2 (the group holding sub-block g), else 0
+    uint32_t odd;      // g odd: this lane's sub-block is a high-nibble one
+  };
+  __device__ __forceinline__ static Lane lane_consts(int g, int t) {
+    Lane L;
+    L.t = t;
+    const uint32_t jj = 2u * (uint32_t)(t & 1);
+    const uint32_t hiw = t >= 2 ? 4u : 0u;   // PRMT indices 4-7 address the second source
+    // bytes 1 and 3 of each result are don't-care (cleared by the masks)
+    L.sel_a = (jj + hiw) | ((jj + 1 + hiw) << 8);
+    L.sel_b = jj | (4u << 4) | ((jj + 1) << 8) | (4u << 12);
+    L.sh_m = t >= 2 ? 4u : 0u;
+    L.mask_a = t >= 2 ? 0x000F000Fu : 0x003F003Fu;
+    L.mask_b = t >= 2 ? 0x00300030u : 0u;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) L.real[c] = (c == (g >> 1)) ? 1u : 0u;
+    L.odd = (uint32_t)(g & 1);
+    return L;
+  }
+
+  // Stage activations: [0, 512) fp16 x of sub-blocks 0..7 (16 bytes per lane
+  // t at 64 j + 16 t); [512, 1024) -x of the odd sub-blocks at the same offsets.
+  static constexpr int kStageX = 1024;
+
+  // 6-bit scales and mins of sub-blocks 2t (x) and 2t+1 (y) as exact floats.
+  // Sub-blocks 0-3: low 6 bits of scales[j] / scales[j+4]; 4-7: low / high
+  // nibble of scales[j+4] with the top 2 bits of scales[j-4] / scales[j].
+  __device__ __forceinline__ static void sub_scales(uint4 hd, const Lane& L, float2& sc,
+                                                    float2& mn) {
+    const uint32_t as = __byte_perm(hd.y, hd.w, L.sel_a);
+    const uint32_t am = __byte_perm(hd.z, hd.w, L.sel_a) >> L.sh_m;
+    const uint32_t bs = (__byte_perm(hd.y, 0, L.sel_b) >> 2) & L.mask_b;
+    const uint32_t bm = (__byte_perm(hd.z, 0, L.sel_b) >> 2) & L.mask_b;
+    const uint32_t s = (as & L.mask_a) | bs | 0x64006400u;
+    const uint32_t m = (am & L.mask_a) | bm | 0x64006400u;
+    const __half2 magic = u32_as_h2(0x64006400u);
+    sc = __half22float2(__hsub2(u32_as_h2(s), magic));
+    mn = __half22float2(__hsub2(u32_as_h2(m), magic));
+  }
+
+  // Shared addresses (wrow, xg, nsx) must come through order_after_wait() of
+  // the stage's full barrier; acc must pass keep_before_release() before the
+  // stage is released (the loads themselves are freely scheduled).
+  // wrow: shared address of row g's super-block, row g+8 at wrow + pitch8.
+  // xst: the stage's activations; xg = xst + 64 g + 16 t (this lane's x).
+  // z: 16 zero bytes on banks 0-3 (no real lane of a quarter-warp reads them).
+  // nsx: shared address of (-sum x of sub-block 2t, -sum of 2t+1).
+  // inv: the activations' inverse power-of-two scale.
+  // acc0 / acc8: rows g / g+8, as (sub-block 2t, 2t+1) pairs summed at the end.
+  __device__ __forceinline__ static void run(uint32_t wrow, int pitch8, uint32_t xg, uint32_t z,
+                                             uint32_t nsx, float inv, const Lane& L,
+                                             float2& acc0, float2& acc8) {
+    const uint4 h0 = lds_u128_nv(wrow), h8 = lds_u128_nv(wrow + pitch8);
+    // first product: x of an odd sub-block; second: x (even) or -x (odd)
+    const uint32_t d1 = L.odd * (xg - z), d2 = xg + L.odd * 512u - z;
+    float D[4][4] = {};   // one chain per qs group
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint2 w0 = lds_u64_nv(wrow + 16 + 32 * c + 8 * L.t);
+      const uint2 w8 = lds_u64_nv(wrow + pitch8 + 16 + 32 * c + 8 * L.t);
+      const uint4 x1 = lds_u128_nv(z + L.real[c] * d1);
+      const uint4 x2 = lds_u128_nv(z + L.real[c] * d2);
+      const uint32_t b0[4] = {__byte_perm(w0.x, 0, 0x4140), __byte_perm(w0.x, 0, 0x4342),
+                              __byte_perm(w0.y, 0, 0x4140), __byte_perm(w0.y, 0, 0x4342)};
+      const uint32_t b8[4] = {__byte_perm(w8.x, 0, 0x4140), __byte_perm(w8.x, 0, 0x4342),
+                              __byte_perm(w8.y, 0, 0x4140), __byte_perm(w8.y, 0, 0x4342)};
+      // k slots (2t, 2t+1 | 2t+8, 2t+9) = weights (8t, 8t+1 | 8t+2, 8t+3), then +4
+      mma_16816_nv(D[c], b0[0], b8[0], b0[1], b8[1], x1.x, x1.y);
+      mma_16816_nv(D[c], b0[2], b8[2], b0[3], b8[3], x1.z, x1.w);
+      mma_16816_nv(D[c], b0[0] & 0x000F000Fu, b8[0] & 0x000F000Fu, b0[1] & 0x000F000Fu,
+                b8[1] & 0x000F000Fu, x2.x, x2.y);
+      mma_16816_nv(D[c], b0[2] & 0x000F000Fu, b8[2] & 0x000F000Fu, b0[3] & 0x000F000Fu,
+                b8[3] & 0x000F000Fu, x2.z, x2.w);
+    }
+    const uint2 nsu = lds_u64_nv(nsx);
+    const float2 ns = make_float2(__uint_as_float(nsu.x), __uint_as_float(nsu.y));
+    float2 sc0, mn0, sc8, mn8;
+    sub_scales(h0, L, sc0, mn0);
+    sub_scales(h8, L, sc8, mn8);
+    // (d, dmin) of each row; with the activation scale undone
+    float2 dm0 = __half22float2(u32_as_h2(h0.x)), dm8 = __half22float2(u32_as_h2(h8.x));
+    dm0 = fmul2(dm0, make_float2(inv, inv));
+    dm8 = fmul2(dm8, make_float2(inv, inv));
+    // column 2t: low nibbles in units of 2^-24; column 2t+1: high, 16 * 2^-24
+    const float2 unit = make_float2(16777216.f, 1048576.f);
+    const float2 c0 = fmul2(fmul2(sc0, unit), make_float2(dm0.x, dm0.x));
+    const float2 c8 = fmul2(fmul2(sc8, unit), make_float2(dm8.x, dm8.x));
+    const float2 k0 = fmul2(mn0, make_float2(dm0.y, dm0.y));
+    const float2 k8 = fmul2(mn8, make_float2(dm8.y, dm8.y));
+    const float2 s0 = fadd2(fadd2(make_float2(D[0][0], D[0][1]), make_float2(D[1][0], D[1][1])),
+                            fadd2(make_float2(D[2][0], D[2][1]), make_float2(D[3][0], D[3][1])));
+    const float2 s8 = fadd2(fadd2(make_float2(D[0][2], D[0][3]), make_float2(D[1][2], D[1][3])),
+                            fadd2(make_float2(D[2][2], D[2][3]), make_float2(D[3][2], D[3][3])));
+    acc0 = ffma2(ns, k0, ffma2(s0, c0, acc0));
+    acc8 = ffma2(ns, k8, ffma2(s8, c8, acc8));
+  }
+};
+
 }  // namespace dqmoe

@@ -87,8 +87,9 @@ def test_qgemv_edge_shapes(dq, orc):
     for fmt, N, K in [(Q4_K, 1, 256), (Q8_0, 1, 256), (Q6_K, 1, 2048), (Q4_K, 65, 256),
                       (Q8_0, 63, 512)]:
         for xdt in (0, 1, 2):
-            err = _case(dq, orc, fmt, N, K, 5, xdt, seed=N + K + xdt)
-            assert err <= TOL[xdt], (fmt, N, K, xdt, err)
+            for B in (5, 1):
+                err = _case(dq, orc, fmt, N, K, B, xdt, seed=N + K + xdt + B)
+                assert err <= TOL[xdt], (fmt, N, K, xdt, B, err)
 
 
 def test_qgemv_bf16_large_values(dq, orc):
@@ -158,6 +159,61 @@ def test_q4k_scale_regimes(dq, orc, xdt):
     assert np.all(y[zero] == 0)
     rel = np.abs(y - ref)[~zero] / scale[~zero]
     assert rel.max() <= 1e-3, rel.max()
+
+
+@pytest.mark.parametrize("xdt", [1, 2])
+def test_q4k_batch1_scale_regimes(dq, orc, xdt):
+    # one activation column takes the block-diagonal kernel, which applies d,
+    # dmin, the 6-bit scales and mins in fp32 after the products: the same
+    # regimes of d and dmin as above, each row within its own error bound
+    regimes = [(1e-2, 1e-2), (2.0 ** -24, 0.0), (3e-6, 5e-6), (0.0, 1e-3), (1e-3, 0.0),
+               (6.0e4, 6.0e4), (-1e-2, 1e-2), (1e-4, 10.0), (10.0, 1e-7), (0.0, 0.0)]
+    per = 13
+    N, K = per * len(regimes), 2048
+    d = np.repeat([r[0] for r in regimes], per)
+    dmin = np.repeat([r[1] for r in regimes], per)
+    g = synth.streams(4343 + xdt, 2)
+    W = _set_q4k_scales(synth.quant_matrix(g[0], Q4_K, N, K), N, K, d, dmin)
+    x = synth.activations(g[1], (1, K), xdt)
+    y = dq.qgemv(Q4_K, dev_bytes(W), N, K, dev_act(x, xdt)).cpu().numpy().astype(np.float64)
+    assert dq.device_status() == 0
+    ref = orc.qgemv(Q4_K, W, N, K, x, xdt, 1)
+    wabs = np.abs(orc.dequant(Q4_K, W, N * K).reshape(N, K).astype(np.float64))
+    xabs = np.abs(orc.act_to_f64(xdt, x).reshape(1, K))
+    scale = xabs @ wabs.T
+    zero = scale == 0
+    assert np.all(y[zero] == 0)
+    rel = np.abs(y - ref)[~zero] / scale[~zero]
+    assert rel.max() <= 1e-3, rel.max()
+
+
+@pytest.mark.parametrize("xdt", [1, 2])
+@pytest.mark.parametrize("ks", [1, 2, 3, 5, 8])
+def test_q4k_batch1_ksplit(dq, orc, xdt, ks):
+    # batch-1 kernel under every cluster split (uneven super-block ranges),
+    # ragged rows, rows of 32 and 64 super-blocks
+    for N, K in [(130, 8192), (70, 16384)]:
+        err = _case(dq, orc, Q4_K, N, K, 1, xdt, seed=600 + ks * 10 + xdt + K, ksplit=ks)
+        assert err <= TOL[xdt], (N, K, err)
+
+
+@pytest.mark.parametrize("xdt", [1, 2])
+def test_q4k_batch1_activation_extremes(dq, orc, xdt):
+    # activations near the top of the fp16 range, tiny ones, and exact zeros in
+    # whole sub-blocks (bf16 input far above fp16: one power-of-two scale)
+    N, K = 96, 4096
+    g = synth.streams(4545 + xdt, 3)
+    W = synth.quant_matrix(g[0], Q4_K, N, K)
+    x = synth.activations(g[1], (1, K), 0)
+    x[0, :256] *= np.float32(1.0e4 if xdt == 1 else 3.0e6)
+    x[0, 256:512] *= np.float32(1e-5)
+    x[0, 512:544] = 0.0
+    x = x.astype(np.float16) if xdt == 1 else synth.f32_to_bf16_bits(x)
+    y = dq.qgemv(Q4_K, dev_bytes(W), N, K, dev_act(x, xdt)).cpu().numpy()
+    assert dq.device_status() == 0
+    ref = orc.qgemv(Q4_K, W, N, K, x, xdt, 1)
+    assert np.isfinite(y).all()
+    assert rel_err(y, ref) <= TOL[xdt]
 
 
 def test_qgemv_weights_early_and_chains(dq, orc):
