@@ -97,7 +97,7 @@ extern "C" {
 /*                weight 2i+1 in its high nibble                            */
 /*   w = e2m1(code) * e4m3(scale[i/16]); a per-tensor scale, where a model  */
 /*   has one, is the caller's (it commutes with the product).  NaN scale    */
-/*   bytes are out of contract.  dq_dequant and dq_qgemv only.              */
+/*   bytes are out of contract.  dq_dequant, dq_qgemv and MoE experts.      */
 /* ------------------------------------------------------------------------ */
 typedef enum { DQ_Q4_K = 1, DQ_Q6_K = 2, DQ_Q8_0 = 3, DQ_Q4_0 = 4, DQ_Q5_K = 5,
                DQ_NVFP4 = 6 } dq_fmt;
