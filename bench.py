@@ -33,6 +33,7 @@ import synth  # noqa: E402
 METRIC = "qGEMV weight GB/s (% of HBM peak); MoE-layer tokens/s at 1 GB300"
 Q4_K = 1
 ROTATE = 4
+LAYERS_PER_GRAPH = 8   # layer passes per captured graph (a decode step spans the layers)
 
 
 def parse():
@@ -290,6 +291,23 @@ def make_event(torch, external):
     return torch.cuda.Event(enable_timing=True)
 
 
+def layer_graphs(torch, s, step, K):
+    """Capture LAYERS_PER_GRAPH consecutive steps (weight copy i % ROTATE for
+    the i-th) as one graph, and the K % LAYERS_PER_GRAPH remaining steps as a
+    second one (None when K is a multiple)."""
+    def capture(n):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(gr, stream=s):
+                for i in range(n):
+                    step(i % ROTATE)
+        return gr
+    s.wait_stream(torch.cuda.current_stream())
+    full = [capture(LAYERS_PER_GRAPH)]
+    rem = K % LAYERS_PER_GRAPH
+    return full, (capture(rem) if rem else None)
+
+
 def bench_layer(torch, dq, args, lin, with_e2e=True):
     """One Llama-3-8B decode layer's linears per step (the matrices in `lin`),
     one CUDA graph launch per step."""
@@ -320,33 +338,31 @@ def bench_layer(torch, dq, args, lin, with_e2e=True):
     K = args.steps
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
-    # timed region 1 (the value): one graph per weight copy, the launches back
-    # to back with nothing between them
-    graphs = []
-    with torch.cuda.stream(s):
-        for r in range(ROTATE):
-            gr = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gr, stream=s):
-                step(r)
-            graphs.append(gr)
+    # timed region 1 (the value): LAYERS_PER_GRAPH layer passes per CUDA graph,
+    # as one graph per decode step spans a model's layers, the launches back
+    # to back with nothing between them; each pass reads the next of the
+    # ROTATE weight copies
+    graphs, rem = layer_graphs(torch, s, step, K)
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(torch.cuda.current_device()) as clk:
         time.sleep(0.3)   # let the sampler start
-        for i in range(args.warmup):
-            graphs[i % ROTATE].replay()
+        for i in range(-(-args.warmup // LAYERS_PER_GRAPH)):
+            graphs[0].replay()
         torch.cuda.synchronize()
         t0 = time.time()
         start.record()
-        for i in range(args.warmup, args.warmup + K):
-            graphs[i % ROTATE].replay()
+        for i in range(K // LAYERS_PER_GRAPH):
+            graphs[0].replay()
+        if rem is not None:
+            rem.replay()
         end.record()
         torch.cuda.synchronize()
         t1 = time.time()
         time.sleep(0.1)
     ms = start.elapsed_time(end)
-    del graphs
+    del graphs, rem
     # timed region 2 (per-launch durations for the roofline): the same steps
     # with an event before and after every launch, one graph per step so that
     # every event keeps its own timestamp.  Events between launches serialise
@@ -401,20 +417,16 @@ def bench_layer(torch, dq, args, lin, with_e2e=True):
         for i in range(len(lin)):
             hy[i].copy_(ys[i], non_blocking=True)
 
-    egr = []
-    with torch.cuda.stream(s):
-        for r in range(ROTATE):
-            gr = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gr, stream=s):
-                e2e_step(r)
-            egr.append(gr)
+    egr, erem = layer_graphs(torch, s, e2e_step, K)
     torch.cuda.synchronize()
-    for i in range(args.warmup):
-        egr[i % ROTATE].replay()
+    for i in range(-(-args.warmup // LAYERS_PER_GRAPH)):
+        egr[0].replay()
     torch.cuda.synchronize()
     start.record()
-    for i in range(K):
-        egr[i % ROTATE].replay()
+    for i in range(K // LAYERS_PER_GRAPH):
+        egr[0].replay()
+    if erem is not None:
+        erem.replay()
     end.record()
     torch.cuda.synchronize()
     ems = start.elapsed_time(end)
@@ -422,8 +434,9 @@ def bench_layer(torch, dq, args, lin, with_e2e=True):
                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                   "ms_per_step": ems / K,
                   "note": "x uploaded from pinned host memory and y read back in every step, "
-                          "captured with the step's %d dq_qgemv calls in one graph per step" % nl}
-    del egr, Ws
+                          "captured with the step's %d dq_qgemv calls, %d steps per graph"
+                          % (nl, LAYERS_PER_GRAPH)}
+    del egr, erem, Ws
     torch.cuda.empty_cache()
     return res
 
@@ -633,9 +646,11 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic",
         "config": {"workload": "llama3-8b decode-layer linears: q,k,v,o,gate,up,down Q4_K "
-                               "(122.7 MB), fp16 x, batch 1, one CUDA graph per step, "
-                               "q|k|v and gate|up stored as merged matrices (4 dq_qgemv "
-                               "launches), weights read-only (early weight streaming)",
+                               "(122.7 MB), fp16 x, batch 1, q|k|v and gate|up stored as "
+                               "merged matrices (4 dq_qgemv launches per layer), weights "
+                               "read-only (early weight streaming); 8 layer passes per CUDA "
+                               "graph over 4 rotating weight copies, as a decode step's graph "
+                               "spans the model's layers",
                    "l2": "4 rotating weight copies, 491 MB > 3x L2",
                    "frac_of_hbm": round(value / world / peak, 4),
                    "parallelism": "replicas" if world > 1 else "single"},

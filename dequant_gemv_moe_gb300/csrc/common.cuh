@@ -345,12 +345,36 @@ __device__ __forceinline__ uint4 lds_u128_nv(uint32_t addr) {
       : "r"(addr));
   return v;
 }
+__device__ __forceinline__ uint32_t lds_u32_nv(uint32_t addr) {
+  uint32_t v;
+  asm("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds_u16_nv(uint32_t addr) {
+  unsigned short v;
+  asm("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+// 32-bit load from a 2-byte aligned shared address.
+__device__ __forceinline__ uint32_t lds_u32_a2_nv(uint32_t addr) {
+  const uint32_t base = addr & ~3u;
+  const uint32_t lo = lds_u32_nv(base);
+  if ((addr & 2u) == 0) return lo;
+  const uint32_t hi = lds_u32_nv(base + 4);
+  return __funnelshift_r(lo, hi, 16);
+}
 __device__ __forceinline__ uint32_t order_after_wait(uint32_t v) {
   asm volatile("mov.b32 %0, %1;" : "=r"(v) : "r"(v) : "memory");
   return v;
 }
 __device__ __forceinline__ void keep_before_release(float a, float b, float c, float d) {
   asm volatile("" ::"f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+// every element of a float array whose size is a multiple of 4
+template <int N>
+__device__ __forceinline__ void keep_before_release(const float* a) {
+#pragma unroll
+  for (int i = 0; i < N; i += 4) keep_before_release(a[i], a[i + 1], a[i + 2], a[i + 3]);
 }
 __device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
   unsigned short v;

@@ -601,17 +601,18 @@ __global__ void __launch_bounds__(kThreads) grouped_kernel(const __grid_constant
         // further waits, no reads) so every warp still meets the barriers
         ok = ok && mbar_wait(&full[s], par);
         if (!ok) continue;
+        const uint32_t o = order_after_wait(0u);   // stage reads follow the wait
         const int c0 = c * L::C;
         const int ncs = min(L::C, p.nsb - c0);
         const int delta = (int)(((int64_t)c0 * L::SBB) & 15);
         const uint32_t wst =
-            smem_u32(wbuf + s * L::W_STAGE) + (16 * cw + g) * L::ROW_PITCH + delta;
+            smem_u32(wbuf + s * L::W_STAGE) + (16 * cw + g) * L::ROW_PITCH + delta + o;
         // this lane's activation column in each 8-column tile (column 0 past the group)
         uint32_t xcol[NT];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           const int col = 8 * nt + g;
-          xcol[nt] = smem_u32(xbuf + (s * NC + (col < ncols ? col : 0)) * L::XCOL);
+          xcol[nt] = smem_u32(xbuf + (s * NC + (col < ncols ? col : 0)) * L::XCOL) + o;
         }
         if constexpr (SBDot<FMT>::kRowScale) {
           for (int j = 0; j < ncs; ++j) {
@@ -638,6 +639,8 @@ __global__ void __launch_bounds__(kThreads) grouped_kernel(const __grid_constant
             fold_tile(acc[nt], part[nt], 1.f, 1.f, xinv[s * NC + 8 * nt + 2 * t],
                       xinv[s * NC + 8 * nt + 2 * t + 1]);
         }
+        keep_before_release<NT * 4>(&acc[0][0]);    // ... and finish before its release
+        keep_before_release<NT * 8>(&accs[0][0][0]);
         __syncwarp();
         if (lane == 0) mbar_arrive_relaxed(&empty[s]);
       }

@@ -113,9 +113,10 @@ __global__ void __launch_bounds__(kThreads) qgemv_mma_kernel(const __grid_consta
     for (int c = 0; c < nchunk; ++c) {
       ok = ok && mbar_wait(&full[s], ph);
       if (ok) {
+        const uint32_t o = order_after_wait(0u);   // stage reads follow the wait
         const int c0 = sb0 + c;
-        const uint32_t wst = wrow + s * L::W_STAGE + (uint32_t)(((int64_t)c0 * L::SBB) & 15);
-        const uint32_t xcol[1] = {xcol0 + s * p.batch * L::XCOL};
+        const uint32_t wst = wrow + s * L::W_STAGE + (uint32_t)(((int64_t)c0 * L::SBB) & 15) + o;
+        const uint32_t xcol[1] = {xcol0 + s * p.batch * L::XCOL + o};
         if constexpr (SBDot<FMT>::kRowScale) {
           float d[1][2][4] = {};
           float r0, r8;
@@ -131,6 +132,8 @@ __global__ void __launch_bounds__(kThreads) qgemv_mma_kernel(const __grid_consta
           const float inv0 = xinv[s * 8 + ((2 * t) & 7)], inv1 = xinv[s * 8 + ((2 * t + 1) & 7)];
           fold_tile(acc, pt[0], 1.f, 1.f, inv0, inv1);
         }
+        keep_before_release<4>(acc);                // ... and finish before its release
+        keep_before_release<8>(&accs[0][0][0]);
         __syncwarp();
         if (lane == 0) mbar_arrive_relaxed(&empty[s]);
       }
@@ -233,6 +236,7 @@ __global__ void __launch_bounds__(kThreads, PAIR ? 3 : 4)
   const int sb1 = (int)((int64_t)p.nsb * (rank + 1) / ksplit);
   const int nsbl = sb1 - sb0;
 
+  pdl_trigger();
   if (threadIdx.x == 0) {
     for (int s = 0; s < plan.nstage; ++s) {
       mbar_init(&full[s], 33);          // TMA bytes + one arrival per loader lane
@@ -242,24 +246,26 @@ __global__ void __launch_bounds__(kThreads, PAIR ? 3 : 4)
     fence_barrier_init();
   }
   if (threadIdx.x < 32) ((uint32_t*)(smem + plan.off_z))[threadIdx.x] = 0u;
+  __syncthreads();
+  const uint64_t pol = l2_evict_first_policy();
+  auto issue = [&](int c, int s) {
+    mbar_arrive_expect_tx(&full[s], L::W_STAGE);   // rows past N are zero-filled, still counted
+    tma_load_2d(wbuf + s * L::W_STAGE, &p.tmap, (int)(((int64_t)(sb0 + c) * L::SBB) >> 1), row0,
+                &full[s], pol);
+  };
+  const int early = p.w_early ? min(plan.nstage, nsbl) : 0;
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&p.tmap);
+    // weights are read-only: stream them in while the previous kernel ends
+    // (and while the cluster forms)
+    for (int c = 0; c < early; ++c) issue(c, c);
+  }
+  // the cluster's reduction barrier must be initialised before any peer
+  // arrives on it, at the end of the kernel
   if (ksplit > 1) cluster_sync_all();
-  else __syncthreads();
-  pdl_trigger();
 
   if (warp == 0) {
     // ------------------------------- loader --------------------------------
-    const uint64_t pol = l2_evict_first_policy();
-    auto issue = [&](int c, int s) {
-      mbar_arrive_expect_tx(&full[s], L::W_STAGE);   // rows past N are zero-filled, still counted
-      tma_load_2d(wbuf + s * L::W_STAGE, &p.tmap, (int)(((int64_t)(sb0 + c) * L::SBB) >> 1),
-                  row0, &full[s], pol);
-    };
-    const int early = p.w_early ? min(plan.nstage, nsbl) : 0;
-    if (lane == 0) {
-      prefetch_tmap(&p.tmap);
-      // weights are read-only: stream them in while the previous kernel ends
-      for (int c = 0; c < early; ++c) issue(c, c);
-    }
     pdl_wait();
     // lane covers activations 8*lane .. 8*lane+7 of a stage; sub-block = lane/4
     const uint4* xsrc = (const uint4*)((const uint16_t*)p.x + (int64_t)sb0 * 256) + lane;

@@ -218,11 +218,16 @@ __device__ __forceinline__ void stage_x(const XSrc& xs, int ncols, int64_t k0, i
 // (column 0 for lanes past the batch);
 // kb: k offset of the super-block inside the stage (j*256).
 // ---------------------------------------------------------------------------
+// The decode cores below read shared memory with plain (schedulable) loads:
+// callers pass addresses derived from order_after_wait() of the stage's full
+// barrier and pass the accumulators through keep_before_release() before the
+// stage is released.
+//
 // B fragment (k, k+1 | k+2, k+3) of this lane's activation column.  Lanes
 // whose column is past the batch read column 0: their output column is never
 // stored, and an mma output column depends only on its own B column.
 __device__ __forceinline__ void ldx(uint32_t xcol, int k, uint32_t& b0, uint32_t& b1) {
-  const uint2 v = lds_u64(xcol + 2 * xoff(k));
+  const uint2 v = lds_u64_nv(xcol + 2 * xoff(k));
   b0 = v.x;
   b1 = v.y;
 }
@@ -237,7 +242,7 @@ __device__ __forceinline__ void mma_x(float (&acc)[NT][2][4], int ch, uint32_t a
   for (int nt = 0; nt < NT; ++nt) {
     uint32_t b0, b1;
     ldx(xcol[nt], k, b0, b1);
-    mma_16816(acc[nt][ch], a0, a1, a2, a3, b0, b1);
+    mma_16816_nv(acc[nt][ch], a0, a1, a2, a3, b0, b1);
   }
 }
 
@@ -371,13 +376,13 @@ struct SBDot<DQ_Q4_K> {
                                              const uint32_t (&xcol)[NT], int kb, int t,
                                              float (&acc)[NT][2][4], float& r0, float& r8) {
     const uint32_t ra = wrow, rb = wrow + pitch8;
-    const uint4 h0 = lds_u128(ra), h8 = lds_u128(rb);
+    const uint4 h0 = lds_u128_nv(ra), h8 = lds_u128_nv(rb);
     __half2 s0l, o0l, s0h, o0h, s8l, o8l, s8h, o8h;
     scales(h0, t, s0l, o0l, s0h, o0h, r0);
     scales(h8, t, s8l, o8l, s8h, o8h, r8);
     const uint32_t qa = ra + 16 + 32 * t;      // this lane's 32 quant bytes of row g
-    const uint4 qa0 = lds_u128(qa), qb0 = lds_u128(qa + 16);
-    const uint4 qa8 = lds_u128(qa + pitch8), qb8 = lds_u128(qa + pitch8 + 16);
+    const uint4 qa0 = lds_u128_nv(qa), qb0 = lds_u128_nv(qa + 16);
+    const uint4 qa8 = lds_u128_nv(qa + pitch8), qb8 = lds_u128_nv(qa + pitch8 + 16);
     const uint32_t q0[8] = {qa0.x, qa0.y, qa0.z, qa0.w, qb0.x, qb0.y, qb0.z, qb0.w};
     const uint32_t q8[8] = {qa8.x, qa8.y, qa8.z, qa8.w, qb8.x, qb8.y, qb8.z, qb8.w};
     if constexpr (PAIRX) {
@@ -391,8 +396,8 @@ struct SBDot<DQ_Q4_K> {
         uint4 xl[NT], xh[NT];                      // steps 2sp, 2sp+1: low / high nibbles
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          xl[nt] = lds_u128(xb[nt] + 16 * sp);
-          xh[nt] = lds_u128(xb[nt] + 16 * sp + 64);
+          xl[nt] = lds_u128_nv(xb[nt] + 16 * sp);
+          xh[nt] = lds_u128_nv(xb[nt] + 16 * sp + 64);
         }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -401,9 +406,9 @@ struct SBDot<DQ_Q4_K> {
           frags(q0[s], q8[s], s0l, o0l, s0h, o0h, s8l, o8l, s8h, o8h, lo, hi);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            mma_16816(acc[nt][0], lo[0], lo[1], lo[2], lo[3], h ? xl[nt].z : xl[nt].x,
+            mma_16816_nv(acc[nt][0], lo[0], lo[1], lo[2], lo[3], h ? xl[nt].z : xl[nt].x,
                       h ? xl[nt].w : xl[nt].y);
-            mma_16816(acc[nt][1], hi[0], hi[1], hi[2], hi[3], h ? xh[nt].z : xh[nt].x,
+            mma_16816_nv(acc[nt][1], hi[0], hi[1], hi[2], hi[3], h ? xh[nt].z : xh[nt].x,
                       h ? xh[nt].w : xh[nt].y);
           }
         }
@@ -445,9 +450,9 @@ struct SBDot<DQ_Q6_K> {
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
       const uint32_t rb = rows[rr];
-      const __half d = __ushort_as_half((unsigned short)lds_u16(rb + 208));
-      const uint32_t s0 = lds_u32_a2(rb + 192), s1 = lds_u32_a2(rb + 196);
-      const uint32_t s2 = lds_u32_a2(rb + 200), s3 = lds_u32_a2(rb + 204);
+      const __half d = __ushort_as_half((unsigned short)lds_u16_nv(rb + 208));
+      const uint32_t s0 = lds_u32_a2_nv(rb + 192), s1 = lds_u32_a2_nv(rb + 196);
+      const uint32_t s2 = lds_u32_a2_nv(rb + 200), s3 = lds_u32_a2_nv(rb + 204);
       const uint32_t sw[4] = {s0, s1, s2, s3};
 #pragma unroll
       for (int h = 0; h < 2; ++h)
@@ -468,9 +473,9 @@ struct SBDot<DQ_Q6_K> {
 #pragma unroll
         for (int rr = 0; rr < 2; ++rr) {
           const uint32_t rb = rows[rr];
-          A[rr] = __byte_perm(lds_u32_a2(rb + 64 * h + 8 * t + 4 * p), 0, 0x3120);
-          B[rr] = __byte_perm(lds_u32_a2(rb + 64 * h + 32 + 8 * t + 4 * p), 0, 0x3120);
-          H[rr] = __byte_perm(lds_u32_a2(rb + 128 + 32 * h + 8 * t + 4 * p), 0, 0x3120);
+          A[rr] = __byte_perm(lds_u32_a2_nv(rb + 64 * h + 8 * t + 4 * p), 0, 0x3120);
+          B[rr] = __byte_perm(lds_u32_a2_nv(rb + 64 * h + 32 + 8 * t + 4 * p), 0, 0x3120);
+          H[rr] = __byte_perm(lds_u32_a2_nv(rb + 128 + 32 * h + 8 * t + 4 * p), 0, 0x3120);
         }
         const int kbase = kb + 128 * h + 8 * t + 4 * p;
         // run r: nibble source and the shift that brings qh bits 2r..2r+1 to 4..5
@@ -513,9 +518,9 @@ struct SBDot<DQ_Q8_0> {
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
         const uint32_t blk = wrow + (rr ? pitch8 : 0) + 34 * s;
-        const __half2 d2 = __half2half2(__ushort_as_half((unsigned short)lds_u16(blk)));
-        const uint32_t w0 = lds_u32_a2(blk + 2 + 8 * t) ^ 0x80808080u;   // q + 128, unsigned
-        const uint32_t w1 = lds_u32_a2(blk + 6 + 8 * t) ^ 0x80808080u;
+        const __half2 d2 = __half2half2(__ushort_as_half((unsigned short)lds_u16_nv(blk)));
+        const uint32_t w0 = lds_u32_a2_nv(blk + 2 + 8 * t) ^ 0x80808080u;   // q + 128, unsigned
+        const uint32_t w1 = lds_u32_a2_nv(blk + 6 + 8 * t) ^ 0x80808080u;
         const uint32_t ws[2] = {w0, w1};
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
@@ -545,15 +550,15 @@ struct SBDot<DQ_Q5_K> {
                                              const uint32_t (&xcol)[NT], int kb, int t,
                                              float (&acc)[NT][2][4], float& r0, float& r8) {
     const uint32_t ra = wrow, rb = wrow + pitch8;
-    const uint4 h0 = lds_u128(ra), h8 = lds_u128(rb);
+    const uint4 h0 = lds_u128_nv(ra), h8 = lds_u128_nv(rb);
     __half2 s0l, o0l, s0h, o0h, s8l, o8l, s8h, o8h;
     SBDot<DQ_Q4_K>::scales(h0, t, s0l, o0l, s0h, o0h, r0);
     SBDot<DQ_Q4_K>::scales(h8, t, s8l, o8l, s8h, o8h, r8);
     const uint32_t qa = ra + 48 + 32 * t;      // this lane's 32 low-quant bytes of row g
-    const uint4 qa0 = lds_u128(qa), qb0 = lds_u128(qa + 16);
-    const uint4 qa8 = lds_u128(qa + pitch8), qb8 = lds_u128(qa + pitch8 + 16);
-    const uint4 ea0 = lds_u128(ra + 16), eb0 = lds_u128(ra + 32);   // qh[0..31] of row g
-    const uint4 ea8 = lds_u128(rb + 16), eb8 = lds_u128(rb + 32);
+    const uint4 qa0 = lds_u128_nv(qa), qb0 = lds_u128_nv(qa + 16);
+    const uint4 qa8 = lds_u128_nv(qa + pitch8), qb8 = lds_u128_nv(qa + pitch8 + 16);
+    const uint4 ea0 = lds_u128_nv(ra + 16), eb0 = lds_u128_nv(ra + 32);   // qh[0..31] of row g
+    const uint4 ea8 = lds_u128_nv(rb + 16), eb8 = lds_u128_nv(rb + 32);
     const uint32_t q0[8] = {qa0.x, qa0.y, qa0.z, qa0.w, qb0.x, qb0.y, qb0.z, qb0.w};
     const uint32_t q8[8] = {qa8.x, qa8.y, qa8.z, qa8.w, qb8.x, qb8.y, qb8.z, qb8.w};
     const uint32_t e0[8] = {ea0.x, ea0.y, ea0.z, ea0.w, eb0.x, eb0.y, eb0.z, eb0.w};
@@ -604,8 +609,8 @@ struct SBDot<DQ_Q4_0> {
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
         const uint32_t blk = wrow + (rr ? pitch8 : 0) + 18 * s;
-        const __half2 d2 = __half2half2(__ushort_as_half((unsigned short)lds_u16(blk)));
-        const uint32_t p = __byte_perm(lds_u32_a2(blk + 2 + 4 * t), 0, 0x3120);
+        const __half2 d2 = __half2half2(__ushort_as_half((unsigned short)lds_u16_nv(blk)));
+        const uint32_t p = __byte_perm(lds_u32_a2_nv(blk + 2 + 4 * t), 0, 0x3120);
         const uint32_t pv[2] = {p, p >> 8};
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
@@ -639,10 +644,10 @@ struct SBDot<DQ_NVFP4> {
     __half2 sc[2][4];
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
-      const uint4 a = lds_u128(rows[rr] + 16 + 32 * t), b = lds_u128(rows[rr] + 32 + 32 * t);
+      const uint4 a = lds_u128_nv(rows[rr] + 16 + 32 * t), b = lds_u128_nv(rows[rr] + 32 + 32 * t);
       cw[rr][0] = a.x; cw[rr][1] = a.y; cw[rr][2] = a.z; cw[rr][3] = a.w;
       cw[rr][4] = b.x; cw[rr][5] = b.y; cw[rr][6] = b.z; cw[rr][7] = b.w;
-      const uint32_t sw = lds_u32(rows[rr] + 4 * t);            // scales of blocks 4t..4t+3
+      const uint32_t sw = lds_u32_nv(rows[rr] + 4 * t);            // scales of blocks 4t..4t+3
       const __half2 s01 = u32_as_h2(e4m3x2_to_h2((uint16_t)(sw & 0xFFFF)));
       const __half2 s23 = u32_as_h2(e4m3x2_to_h2((uint16_t)(sw >> 16)));
       sc[rr][0] = __low2half2(s01);
