@@ -127,6 +127,9 @@ def _moe_case(dq, orc, fmt, E, k, H, F, ns, T, xdt, seed, tokens=None):
     (Q4_K, 4, 2, 512, 512, 1, 64, 1),
     (Q6_K, 2, 1, 2048, 2048, 0, 100, 2),
     (Q8_0, 2, 2, 256, 256, 1, 300, 0),
+    # many one-token experts beside a 3-token shared expert
+    (Q4_K, 64, 2, 1024, 512, 1, 3, 2),
+    (Q4_K, 32, 8, 2048, 1024, 0, 2, 1),
     # NVFP4 experts: one-token decode, 16-column groups, 32-column groups,
     # and the tcgen05 path
     (NVFP4, 8, 2, 512, 1024, 1, 1, 2),
