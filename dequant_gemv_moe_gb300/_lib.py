@@ -47,6 +47,11 @@ _OPTIONAL_SIGS = {
     "dq_moe_permute": [_P, _I, _I, _I, _P, _P, _P],
     "dq_moe_forward": [ctypes.POINTER(MoeDesc), _P, _I, _I, _P, _P, _SZ, _P, _P, _P, _P],
     "dq_moe_forward_noalloc": [ctypes.POINTER(MoeDesc), _P, _I, _I, _P, _P, _P, _P, _P],
+    "dq_expert_cache_create": [ctypes.POINTER(MoeDesc), _I, _P, _P, _P, _I, _I, _P],
+    "dq_expert_cache_workspace_size": [_P, _I, _P],
+    "dq_moe_forward_streamed": [_P, _P, _I, _I, _P, _P, _SZ, _P, _P],
+    "dq_expert_cache_stats": [_P, _P, _P, _P],
+    "dq_expert_cache_destroy": [_P],
 }
 
 

@@ -2,8 +2,12 @@
 // dispatch on format / activation dtype, status strings, device status word.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <new>
+
 #include "common.cuh"
 #include "moe_plan.h"
+#include "stream_cache.h"
 
 namespace dqmoe {
 __device__ int g_device_status = 0;
@@ -17,8 +21,7 @@ int launch_router(const float* Wr, int E, int H, const void* x, int xdt, int T, 
                   int KS, float* part, float* logits, int32_t* idx, float* gate, cudaStream_t s);
 int launch_permute(const int32_t* idx, int T, int k, int E, int32_t* offsets, int32_t* sorted,
                    cudaStream_t s);
-int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, float* y, void* ws,
-                       int32_t* topk_idx, float* topk_gate, float* logits, cudaStream_t s);
+
 }  // namespace dqmoe
 
 using namespace dqmoe;
@@ -166,6 +169,82 @@ int dq_moe_forward(const dq_moe_desc* desc, const void* x, int x_dtype, int T, f
   if (ws_bytes < moe_plan(*desc, T).total) return DQ_ERR_WORKSPACE;
   return launch_moe_forward(*desc, x, x_dtype, T, y, ws, topk_idx, topk_gate, logits,
                             (cudaStream_t)stream);
+}
+
+int dq_expert_cache_create(const dq_moe_desc* d, int slots, void* slot_gate, void* slot_up,
+                           void* slot_down, int max_tokens, int phases, dq_expert_cache** cache) {
+  if (!cache) return DQ_ERR_ARG;
+  *cache = nullptr;
+  if (max_tokens <= 0) return DQ_ERR_ARG;
+  const int rc = check_desc(d, max_tokens);
+  if (rc != DQ_OK) return rc;
+  if (phases < 1 || phases > dqmoe::kMaxStreamPhases) return DQ_ERR_ARG;
+  const long long need = std::min<long long>(d->E, (long long)max_tokens * d->top_k);
+  if (slots < need || slots > d->E) return DQ_ERR_ARG;
+  if (!slot_gate || !slot_up || !slot_down) return DQ_ERR_ARG;
+  if (!aligned(slot_gate, 16) || !aligned(slot_up, 16) || !aligned(slot_down, 16))
+    return DQ_ERR_ALIGN;
+  // the routed experts must be page-locked host memory (asynchronous copies)
+  const void* hp[3] = {d->w_gate, d->w_up, d->w_down};
+  for (const void* ptr : hp) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+      cudaGetLastError();
+      return DQ_ERR_ARG;
+    }
+    if (a.type != cudaMemoryTypeHost) return DQ_ERR_ARG;
+  }
+  const int q = qk_of(d->fmt), bb = block_bytes(d->fmt);
+  const int64_t gu_bytes = (int64_t)d->ffn * (d->hidden / q) * bb;
+  const int64_t dn_bytes = (int64_t)d->hidden * (d->ffn / q) * bb;
+  dq_expert_cache* c = new (std::nothrow) dq_expert_cache;
+  if (!c) return DQ_ERR_CUDA;
+  const int irc = dqmoe::stream_cache_init(c, *d, slots, slot_gate, slot_up, slot_down,
+                                           max_tokens, phases, gu_bytes, dn_bytes);
+  if (irc != DQ_OK) {
+    dqmoe::stream_cache_release(c);
+    delete c;
+    return irc;
+  }
+  *cache = c;
+  return DQ_OK;
+}
+
+int dq_expert_cache_workspace_size(const dq_expert_cache* cache, int T, size_t* bytes) {
+  if (!cache || !bytes || T <= 0 || T > cache->max_tokens) return DQ_ERR_ARG;
+  size_t a, b;
+  *bytes = dqmoe::stream_workspace(*cache, T, &a, &b);
+  return DQ_OK;
+}
+
+int dq_moe_forward_streamed(dq_expert_cache* cache, const void* x, int x_dtype, int T, float* y,
+                            void* ws, size_t ws_bytes, void* stream, void* copy_stream) {
+  if (!cache || !x || !y || !dtype_ok(x_dtype) || T <= 0 || T > cache->max_tokens)
+    return DQ_ERR_ARG;
+  if (stream == copy_stream) return DQ_ERR_ARG;
+  if (!aligned(x, 16) || !aligned(y, 16)) return DQ_ERR_ALIGN;
+  if (!ws) return DQ_ERR_WORKSPACE;
+  if (!aligned(ws, 256)) return DQ_ERR_ALIGN;
+  size_t a, b;
+  if (ws_bytes < dqmoe::stream_workspace(*cache, T, &a, &b)) return DQ_ERR_WORKSPACE;
+  return dqmoe::stream_forward(cache, x, x_dtype, T, y, ws, (cudaStream_t)stream,
+                               (cudaStream_t)copy_stream);
+}
+
+int dq_expert_cache_stats(const dq_expert_cache* cache, long long* hits, long long* misses,
+                          long long* bytes_copied) {
+  if (!cache || !hits || !misses || !bytes_copied) return DQ_ERR_ARG;
+  *hits = cache->hits;
+  *misses = cache->misses;
+  *bytes_copied = cache->bytes_copied;
+  return DQ_OK;
+}
+
+int dq_expert_cache_destroy(dq_expert_cache* cache) {
+  if (!cache) return DQ_ERR_ARG;
+  dqmoe::stream_cache_release(cache);
+  delete cache;
+  return DQ_OK;
 }
 
 const char* dq_status_string(int status) {

@@ -38,7 +38,7 @@ constexpr int kWide = 32;
 constexpr int kRouterStreamT = 8;
 constexpr int kRouterChunk = 1024;
 
-MoePlan moe_plan(const dq_moe_desc& d, int T) {
+MoePlan moe_plan(const dq_moe_desc& d, int T, bool allow_wide) {
   MoePlan p;
   const int tiles = ((d.E + 63) / 64) * ((T + 31) / 32);
   p.KS = T <= kRouterStreamT ? (d.hidden + kRouterChunk - 1) / kRouterChunk
@@ -54,7 +54,7 @@ MoePlan moe_plan(const dq_moe_desc& d, int T) {
                   (int64_t)d.n_shared * ((T + p.GW - 1) / p.GW));
   // experts with more than kWide tokens go to the tensor-core GEMM in units of
   // <= 128 tokens: at most P/(kWide+1) such experts
-  p.wide = T > kWide;
+  p.wide = allow_wide && T > kWide;
   p.U_max = p.wide ? (int)(p.P / 128 + p.P / (kWide + 1) + 1 +
                            (int64_t)d.n_shared * ((T + 127) / 128))
                    : 0;
@@ -494,7 +494,25 @@ struct GroupedParams {
   const int* coltok;   // colinv index of position pos: coltok[pos] (nullable: pos)
   int tiles;           // tiles per group
   int nstage;
+  // expert streaming (both nullable): routed expert e's matrices sit in slot
+  // slot_of[e] of the stacked maps; only units of experts with
+  // phase_of[e] == phase run (shared experts run in phase 0)
+  const int* slot_of;
+  const int8_t* phase_of;
+  int phase;
 };
+
+// Whether a unit of group grp runs in this launch, and its matrix index in
+// the routed or shared maps.
+__device__ __forceinline__ bool unit_in_phase(const GroupedParams& p, int4 grp, int& mat) {
+  const bool shared = grp.x >= p.E;
+  if (shared) {
+    mat = grp.x - p.E;
+    return p.phase_of == nullptr || p.phase == 0;
+  }
+  mat = p.slot_of ? __ldg(p.slot_of + grp.x) : grp.x;
+  return p.phase_of == nullptr || __ldg(p.phase_of + grp.x) == p.phase;
+}
 
 // NT: activation tiles of 8 columns per unit (groups hold <= 8*NT columns).
 template <int FMT, bool GATEUP, int NT>
@@ -536,7 +554,8 @@ __global__ void __launch_bounds__(kThreads) grouped_kernel(const __grid_constant
       const int4 grp = __ldg(p.groups + u / p.tiles);
       const int tile = u % p.tiles;
       const bool shared = grp.x >= p.E;
-      const int eid = shared ? grp.x - p.E : grp.x;
+      int eid;
+      if (!unit_in_phase(p, grp, eid)) continue;
       // first stacked row of the tile: gate/up -> 32 gate rows then the same 32 up rows
       const int grow = eid * p.rows_per_expert + (GATEUP ? tile * 32 : tile * 64);
       const CUtensorMap* ma = shared ? &p.map_sa : &p.map_a;
@@ -587,6 +606,8 @@ __global__ void __launch_bounds__(kThreads) grouped_kernel(const __grid_constant
       const int4 grp = __ldg(p.groups + u / p.tiles);
       const int tile = u % p.tiles;
       const int ncols = grp.z;
+      int mat_unused;
+      if (!unit_in_phase(p, grp, mat_unused)) continue;   // the loader skips it too
       const bool f16 = p.xdt == DQ_F16;      // fp16 input carries no scale
       float acc[NT][4] = {};
       float accs[NT][2][4] = {};             // fp16 input: running accumulator pairs
@@ -761,13 +782,15 @@ int blk_bytes(int fmt) {
 }
 
 template <int FMT, bool GATEUP, int NT>
-int launch_grouped(const GroupedParams& gp_in, int units_max, cudaStream_t s, int E, int n_shared) {
+int launch_grouped(const GroupedParams& gp_in, int units_max, cudaStream_t s, int E_map,
+                   int n_shared) {
   using L = Layout<FMT>;
   GroupedParams gp = gp_in;
   const uint32_t box_rows = GATEUP ? 32 : 64;
   const uint64_t rpe = (uint64_t)gp.rows_per_expert;
-  if (!make_weight_tmap(&gp.map_a, gp.Wa, rpe * E, gp.row_bytes, L::BOX, box_rows)) return DQ_ERR_CUDA;
-  if (GATEUP && !make_weight_tmap(&gp.map_b, gp.Wb, rpe * E, gp.row_bytes, L::BOX, box_rows))
+  if (!make_weight_tmap(&gp.map_a, gp.Wa, rpe * E_map, gp.row_bytes, L::BOX, box_rows))
+    return DQ_ERR_CUDA;
+  if (GATEUP && !make_weight_tmap(&gp.map_b, gp.Wb, rpe * E_map, gp.row_bytes, L::BOX, box_rows))
     return DQ_ERR_CUDA;
   if (n_shared > 0) {
     if (!make_weight_tmap(&gp.map_sa, gp.Sa, rpe * n_shared, gp.row_bytes, L::BOX, box_rows))
@@ -852,9 +875,12 @@ int launch_permute(const int32_t* idx, int T, int k, int E, int32_t* offsets, in
   return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
 }
 
+// stages: 1 = router and top-k, 2 = the rest (permute, experts, combine), 3 = both.
+// ms (nullable): the streamed layer's slot cache and copy/compute phases.
 int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, float* y, void* ws,
-                       int32_t* topk_idx, float* topk_gate, float* logits, cudaStream_t s) {
-  const MoePlan pl = moe_plan(d, T);
+                       int32_t* topk_idx, float* topk_gate, float* logits, cudaStream_t s,
+                       const MoeStream* ms, int stages) {
+  const MoePlan pl = moe_plan(d, T, ms == nullptr);
   uint8_t* w = (uint8_t*)ws;
   float* part = (float*)(w + pl.off_part);
   float* lg = logits ? logits : (float*)(w + pl.off_logits);
@@ -869,9 +895,13 @@ int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, floa
   float* h = (float*)(w + pl.off_h);
   float* ypos = (float*)(w + pl.off_ypos);
 
-  int rc = launch_router(d.router_W, d.E, d.hidden, x, xdt, T, d.top_k, pl.KS, part, lg, idx,
-                         gate, s);
-  if (rc != DQ_OK) return rc;
+  int rc = DQ_OK;
+  if (stages & 1) {
+    rc = launch_router(d.router_W, d.E, d.hidden, x, xdt, T, d.top_k, pl.KS, part, lg, idx, gate,
+                       s);
+    if (rc != DQ_OK) return rc;
+  }
+  if (!(stages & 2)) return DQ_OK;
   int4* units = (int4*)(w + pl.off_units);
   int32_t* nunits = (int32_t*)(w + pl.off_nunits);
   __half* x16t = (__half*)(w + pl.off_x16t);
@@ -927,8 +957,25 @@ int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, floa
   gu.coltok = tok;
   gu.tiles = d.ffn / 32;
   gu.rows_per_expert = d.ffn;
-  rc = launch_grouped_fmt<true>(d.fmt, pl.NT, gu, pl.G_max * gu.tiles, s, d.E, d.n_shared);
-  if (rc != DQ_OK) return rc;
+  if (!ms) {
+    rc = launch_grouped_fmt<true>(d.fmt, pl.NT, gu, pl.G_max * gu.tiles, s, d.E, d.n_shared);
+    if (rc != DQ_OK) return rc;
+  } else {
+    // streamed: routed matrices from the slot cache, one launch per phase
+    // once that phase's copies have landed
+    gu.Wa = (const uint8_t*)ms->slot_gate;
+    gu.Wb = (const uint8_t*)ms->slot_up;
+    gu.slot_of = ms->slot_of;
+    gu.phase_of = ms->phase_of;
+    for (int ph = 0; ph < ms->nphase; ++ph) {
+      if (ms->gu_ready[ph] && cudaStreamWaitEvent(s, ms->gu_ready[ph], 0) != cudaSuccess)
+        return DQ_ERR_CUDA;
+      gu.phase = ph;
+      rc = launch_grouped_fmt<true>(d.fmt, pl.NT, gu, pl.G_max * gu.tiles, s, ms->slots,
+                                    d.n_shared);
+      if (rc != DQ_OK) return rc;
+    }
+  }
 
   // wide units: gathered fp16 rows, tensor-core gate and up GEMMs, SwiGLU
   if (pl.wide) {
@@ -968,8 +1015,22 @@ int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, floa
   dn.coltok = nullptr;
   dn.tiles = d.hidden / 64;
   dn.rows_per_expert = d.hidden;
-  rc = launch_grouped_fmt<false>(d.fmt, pl.NT, dn, pl.G_max * dn.tiles, s, d.E, d.n_shared);
-  if (rc != DQ_OK) return rc;
+  if (!ms) {
+    rc = launch_grouped_fmt<false>(d.fmt, pl.NT, dn, pl.G_max * dn.tiles, s, d.E, d.n_shared);
+    if (rc != DQ_OK) return rc;
+  } else {
+    dn.Wa = (const uint8_t*)ms->slot_down;
+    dn.slot_of = ms->slot_of;
+    dn.phase_of = ms->phase_of;
+    for (int ph = 0; ph < ms->nphase; ++ph) {
+      if (ms->dn_ready[ph] && cudaStreamWaitEvent(s, ms->dn_ready[ph], 0) != cudaSuccess)
+        return DQ_ERR_CUDA;
+      dn.phase = ph;
+      rc = launch_grouped_fmt<false>(d.fmt, pl.NT, dn, pl.G_max * dn.tiles, s, ms->slots,
+                                     d.n_shared);
+      if (rc != DQ_OK) return rc;
+    }
+  }
   if (pl.wide) {
     rc = launch_tc_gemm(d.fmt, d.w_down, d.sh_down, d.E, d.n_shared, d.hidden, d.ffn, units,
                         nunits, pl.U_max, h16, pl.NP, hinv, ypos, d.hidden, s);

@@ -2,6 +2,7 @@
 // C-ABI validation in api.cu and the launch sequence in moe.cu).
 #pragma once
 
+#include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
 
@@ -23,6 +24,39 @@ struct MoePlan {
       off_x16, off_xinv, off_g, off_u, off_h16, off_hinv, total;
 };
 
-MoePlan moe_plan(const dq_moe_desc& d, int T);
+// allow_wide = false keeps every expert on the grouped mma.sync kernel (the
+// streamed layer, whose experts live in a slot cache).
+MoePlan moe_plan(const dq_moe_desc& d, int T, bool allow_wide = true);
 
+// The streamed layer's expert cache as the launch sequence sees it: routed
+// expert e's gate/up/down sit in slot slot_of[e] of the slot buffers, and its
+// units run in copy/compute phase phase_of[e] (both device arrays of E).
+constexpr int kMaxStreamPhases = 8;
+struct MoeStream {
+  const int* slot_of;
+  const int8_t* phase_of;
+  int nphase;
+  cudaEvent_t gu_ready[kMaxStreamPhases];   // gate/up of the phase copied (null: none)
+  cudaEvent_t dn_ready[kMaxStreamPhases];   // down of the phase copied (null: none)
+  const void* slot_gate;
+  const void* slot_up;
+  const void* slot_down;
+  int slots;
+};
+
+int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, float* y, void* ws,
+                       int32_t* topk_idx, float* topk_gate, float* logits, cudaStream_t s,
+                       const MoeStream* ms = nullptr, int stages = 3);
+
+}  // namespace dqmoe
+
+struct dq_expert_cache;   // the streamed layer's state (csrc/stream.cu)
+
+namespace dqmoe {
+size_t stream_workspace(const ::dq_expert_cache& c, int T, size_t* off_slot, size_t* off_phase);
+int stream_cache_init(::dq_expert_cache* c, const dq_moe_desc& d, int slots, void* sg, void* su,
+                      void* sd, int max_tokens, int phases, int64_t gu_bytes, int64_t dn_bytes);
+void stream_cache_release(::dq_expert_cache* c);
+int stream_forward(::dq_expert_cache* c, const void* x, int xdt, int T, float* y, void* ws,
+                   cudaStream_t s, cudaStream_t cs);
 }  // namespace dqmoe

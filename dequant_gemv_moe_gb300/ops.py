@@ -132,3 +132,69 @@ def moe_forward(desc, x, y=None, ws=None, want_routing=False):
     if want_routing:
         return y, idx, gate, logits
     return y
+
+
+# ------------------------------------------------------- expert streaming
+class ExpertCache:
+    """A device cache of `slots` experts for a layer whose routed experts live
+    in page-locked host memory (dq_expert_cache_*; marshalling only).
+
+    host_w_gate / host_w_up / host_w_down: pinned CPU uint8 tensors of all E
+    experts; router_W and the shared experts (optional) are CUDA tensors.  The
+    slot buffers are allocated here as CUDA tensors and kept by this object.
+    """
+
+    def __init__(self, E, top_k, hidden, ffn, n_shared, fmt, router_W, host_w_gate, host_w_up,
+                 host_w_down, sh_gate=None, sh_up=None, sh_down=None, slots=None,
+                 max_tokens=1, phases=2):
+        self.desc = make_desc(E, top_k, hidden, ffn, n_shared, fmt, router_W, host_w_gate,
+                              host_w_up, host_w_down, sh_gate, sh_up, sh_down)
+        self._keep = (router_W, host_w_gate, host_w_up, host_w_down, sh_gate, sh_up, sh_down)
+        if slots is None:
+            slots = min(E, max_tokens * top_k)
+        dev = router_W.device
+        gu = host_w_gate.numel() // E
+        dn = host_w_down.numel() // E
+        self.slot_gate = torch.empty(slots * gu, dtype=torch.uint8, device=dev)
+        self.slot_up = torch.empty(slots * gu, dtype=torch.uint8, device=dev)
+        self.slot_down = torch.empty(slots * dn, dtype=torch.uint8, device=dev)
+        self.max_tokens = max_tokens
+        h = ctypes.c_void_p()
+        _call("dq_expert_cache_create", ctypes.byref(self.desc), slots, _ptr(self.slot_gate),
+              _ptr(self.slot_up), _ptr(self.slot_down), max_tokens, phases, ctypes.byref(h))
+        self.handle = h
+        self.copy_stream = torch.cuda.Stream(device=dev)
+
+    def workspace_size(self, T):
+        n = ctypes.c_size_t()
+        _call("dq_expert_cache_workspace_size", self.handle, T, ctypes.byref(n))
+        return n.value
+
+    def forward(self, x, y=None, ws=None):
+        """The layer for x [T][hidden] on the current stream (copies on this
+        cache's copy stream)."""
+        T = x.shape[0]
+        if y is None:
+            y = torch.empty(T, self.desc.hidden, dtype=torch.float32, device=x.device)
+        if ws is None:
+            ws = torch.empty(self.workspace_size(T), dtype=torch.uint8, device=x.device)
+        _call("dq_moe_forward_streamed", self.handle, _ptr(x), _dtype_code(x), T, _ptr(y),
+              _ptr(ws), ws.numel(), _stream(), ctypes.c_void_p(self.copy_stream.cuda_stream))
+        return y
+
+    def stats(self):
+        h, m, b = ctypes.c_longlong(), ctypes.c_longlong(), ctypes.c_longlong()
+        _call("dq_expert_cache_stats", self.handle, ctypes.byref(h), ctypes.byref(m),
+              ctypes.byref(b))
+        return {"hits": h.value, "misses": m.value, "bytes_copied": b.value}
+
+    def close(self):
+        if self.handle:
+            _call("dq_expert_cache_destroy", self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

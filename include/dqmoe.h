@@ -290,6 +290,68 @@ int dq_moe_forward_noalloc(const dq_moe_desc* desc, const void* x, int x_dtype, 
                            float* y, int32_t* topk_idx, float* topk_gate, float* logits,
                            void* stream);
 
+/* ------------------------------------------------------------------------ */
+/* Expert streaming: the routed experts in page-locked host memory, a device */
+/* cache of expert slots ([Titan Engine, §MoE 专家流式加载]: experts loaded   */
+/* on demand, an LRU cache of hot experts, asynchronous loads hiding the     */
+/* transfer; [NTransformer, §核心技术] SLEP: a double-buffered pipeline that  */
+/* overlaps transfers with GPU compute).                                     */
+/*                                                                          */
+/* Each dq_moe_forward_streamed call runs the router and top-k on `stream`,  */
+/* reads the routing back (one host synchronisation of `stream`), keeps the  */
+/* cache least-recently-used, copies the missing experts on `copy_stream` in */
+/* up to phases-1 chunks (one cudaMemcpyAsync per matrix), and runs the      */
+/* grouped expert kernels chunk by chunk on `stream`, each after its chunk's */
+/* copies: the cached experts (and the shared ones) first, with no wait.     */
+/* Its result equals dq_moe_forward's on the same experts bit for bit when   */
+/* no expert receives more than 32 tokens (beyond that, the streamed layer   */
+/* keeps every expert on the grouped mma.sync kernel).  Not capturable in a  */
+/* CUDA graph (the host reads the routing).  A cache is used by one host     */
+/* thread at a time.                                                         */
+/* ------------------------------------------------------------------------ */
+typedef struct dq_expert_cache dq_expert_cache;
+
+/* dq_expert_cache_create
+ *   host_experts : a descriptor as for dq_moe_forward, except that w_gate,
+ *                  w_up and w_down point to page-locked host memory holding
+ *                  all E experts (same stacked layout; 16-byte aligned);
+ *                  router_W and the shared experts are device memory.
+ *   slots        : experts the device cache holds, at least
+ *                  min(E, max_tokens * top_k).
+ *   slot_gate, slot_up : device, slots * ffn rows each (one expert's
+ *                  gate / up matrix per slot); slot_down: slots * hidden
+ *                  rows.  16-byte aligned, owned by the caller, kept until
+ *                  the cache is destroyed.
+ *   max_tokens   : the largest T of a call (1..65536).
+ *   phases       : 1..8 copy/compute chunks per call (1: all copies first).
+ *   *cache       : receives the handle.
+ * Allocates host memory (page-locked staging, events), no device memory.
+ * Errors: DQ_ERR_ARG (including host expert memory that is not page-locked),
+ *         DQ_ERR_ALIGN, DQ_ERR_UNSUPPORTED, DQ_ERR_CUDA. */
+int dq_expert_cache_create(const dq_moe_desc* host_experts, int slots, void* slot_gate,
+                           void* slot_up, void* slot_down, int max_tokens, int phases,
+                           dq_expert_cache** cache);
+
+/* Bytes of device scratch dq_moe_forward_streamed needs for T tokens. */
+int dq_expert_cache_workspace_size(const dq_expert_cache* cache, int T, size_t* bytes);
+
+/* dq_moe_forward_streamed — the layer for T <= max_tokens tokens.
+ *   x, y, x_dtype, ws, ws_bytes : as dq_moe_forward (ws of at least
+ *                  dq_expert_cache_workspace_size bytes, 256-byte aligned).
+ *   stream       : compute stream; copy_stream: the copies (a different
+ *                  stream; NULL is the legacy default stream).
+ * Returns once the work is enqueued (after the routing read-back).
+ * Errors: DQ_ERR_ARG, DQ_ERR_ALIGN, DQ_ERR_WORKSPACE, DQ_ERR_CUDA. */
+int dq_moe_forward_streamed(dq_expert_cache* cache, const void* x, int x_dtype, int T, float* y,
+                            void* ws, size_t ws_bytes, void* stream, void* copy_stream);
+
+/* Cumulative counts: experts found in the cache, experts copied, bytes copied. */
+int dq_expert_cache_stats(const dq_expert_cache* cache, long long* hits, long long* misses,
+                          long long* bytes_copied);
+
+/* Releases the host resources of the cache (not the caller's slot buffers). */
+int dq_expert_cache_destroy(dq_expert_cache* cache);
+
 /* Human-readable name of a dq_status value (static string, never NULL). */
 const char* dq_status_string(int status);
 

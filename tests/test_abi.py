@@ -106,3 +106,43 @@ def test_moe_rejects_gemv_only_formats(so):
     for fmt, rc in [(1, 0), (6, 0), (4, -3), (5, -3)]:
         d = Desc(8, 2, 512, 512, 0, fmt, a, a, a, a, None, None, None)
         assert f(ctypes.byref(d), 4, ctypes.byref(n)) == rc, fmt
+
+
+def test_expert_cache_argument_errors(so):
+    # checks that fail before any CUDA call: no cache pointer, tokens, phases,
+    # too few slots; null handles everywhere else
+    class Desc(ctypes.Structure):
+        _fields_ = [("E", ctypes.c_int32), ("top_k", ctypes.c_int32), ("hidden", ctypes.c_int32),
+                    ("ffn", ctypes.c_int32), ("n_shared", ctypes.c_int32), ("fmt", ctypes.c_int32),
+                    ("router_W", ctypes.c_void_p), ("w_gate", ctypes.c_void_p),
+                    ("w_up", ctypes.c_void_p), ("w_down", ctypes.c_void_p),
+                    ("sh_gate", ctypes.c_void_p), ("sh_up", ctypes.c_void_p),
+                    ("sh_down", ctypes.c_void_p)]
+    a = ctypes.c_void_p(4096)
+    d = Desc(8, 2, 512, 512, 0, 1, a, a, a, a, None, None, None)
+    f = so.dq_expert_cache_create
+    f.argtypes = [ctypes.POINTER(Desc), ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    h = ctypes.c_void_p()
+    assert f(ctypes.byref(d), 4, a, a, a, 2, 2, None) == -1             # no handle pointer
+    assert f(ctypes.byref(d), 4, a, a, a, 0, 2, ctypes.byref(h)) == -1  # max_tokens
+    assert f(ctypes.byref(d), 4, a, a, a, 2, 0, ctypes.byref(h)) == -1  # phases
+    assert f(ctypes.byref(d), 4, a, a, a, 2, 9, ctypes.byref(h)) == -1
+    assert f(ctypes.byref(d), 3, a, a, a, 2, 2, ctypes.byref(h)) == -1  # slots < 2 * 2
+    assert f(ctypes.byref(d), 9, a, a, a, 2, 2, ctypes.byref(h)) == -1  # slots > E
+    assert f(ctypes.byref(d), 4, None, a, a, 2, 2, ctypes.byref(h)) == -1
+    assert f(ctypes.byref(d), 4, ctypes.c_void_p(4100), a, a, 2, 2, ctypes.byref(h)) == -2
+    d.fmt = 4   # Q4_0 experts are not supported by the layer
+    assert f(ctypes.byref(d), 4, a, a, a, 2, 2, ctypes.byref(h)) == -3
+    assert h.value is None
+    g = so.dq_moe_forward_streamed
+    g.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]
+    assert g(None, a, 1, 1, a, a, 1 << 20, None, a) == -1
+    so.dq_expert_cache_stats.argtypes = [ctypes.c_void_p] * 4
+    assert so.dq_expert_cache_stats(None, a, a, a) == -1
+    so.dq_expert_cache_destroy.argtypes = [ctypes.c_void_p]
+    assert so.dq_expert_cache_destroy(None) == -1
+    so.dq_expert_cache_workspace_size.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
+    n = ctypes.c_size_t()
+    assert so.dq_expert_cache_workspace_size(None, 1, ctypes.byref(n)) == -1
