@@ -75,6 +75,8 @@ def run_case(args):
         # of weights (a small case for full ncu captures of that kernel)
         cfg = dict(synth.MOE_DEEPSEEK, E=32)
         print(json.dumps(bench_moe(torch, dq, cfg, 256, reps=max(1, args.steps))))
+    elif args.case == "streamed":
+        print(json.dumps(bench_moe_streamed(torch, dq, synth.MOE_DEEPSEEK, 8, reps=max(3, args.steps))))
     elif args.case.startswith("deepseek"):
         T = int(args.case[len("deepseek"):])
         print(json.dumps(bench_moe(torch, dq, synth.MOE_DEEPSEEK, T, reps=max(1, args.steps))))
@@ -588,6 +590,74 @@ def bench_moe(torch, dq, cfg, T, reps=20):
             "GBps": alg / (ms / 1e3) / 1e9}
 
 
+def h2d_peak(torch, nbytes=1 << 30, reps=5):
+    """Page-locked host -> device copy bandwidth (GB/s, best of reps)."""
+    src = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    dst = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    best = 0.0
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        dst.copy_(src, non_blocking=True)
+        b.record()
+        torch.cuda.synchronize()
+        best = max(best, nbytes / (a.elapsed_time(b) / 1e3) / 1e9)
+    del src, dst
+    torch.cuda.empty_cache()
+    return best
+
+
+def bench_moe_streamed(torch, dq, cfg, T, reps=20, slots=64, phases=4, rotate=8):
+    """The DeepSeek-V3-shaped layer with its 256 routed experts in page-locked
+    host memory and a device cache of `slots` experts: every call routes on
+    the device, copies the missing experts over the host link in chunks and
+    computes each chunk as it lands (dq_moe_forward_streamed)."""
+    w = synth.moe_weights(synth.BASE_SEED + 4, cfg["E"], cfg["H"], cfg["F"], cfg["n_shared"],
+                          cfg["fmt"])
+    host = {k: torch.from_numpy(w[k]).pin_memory() for k in ("w_gate", "w_up", "w_down")}
+    dev = {k: (torch.from_numpy(w[k]).cuda() if w[k] is not None else None)
+           for k in ("router_W", "sh_gate", "sh_up", "sh_down")}
+    del w
+    cache = dq.ExpertCache(cfg["E"], cfg["top_k"], cfg["H"], cfg["F"], cfg["n_shared"],
+                           cfg["fmt"], dev["router_W"], host["w_gate"], host["w_up"],
+                           host["w_down"], dev["sh_gate"], dev["sh_up"], dev["sh_down"],
+                           slots=slots, max_tokens=T, phases=phases)
+    g = synth.streams(synth.BASE_SEED + 40, rotate)
+    xs = []
+    for i in range(rotate):
+        a = synth.activations(g[i], (T, cfg["H"]), cfg["xdt"])
+        t = torch.from_numpy(a.view(np.int16) if cfg["xdt"] == 2 else a).cuda()
+        xs.append(t.view(torch.bfloat16) if cfg["xdt"] == 2 else t)
+    ws = torch.empty(cache.workspace_size(T), dtype=torch.uint8, device="cuda")
+    y = torch.empty(T, cfg["H"], dtype=torch.float32, device="cuda")
+    for i in range(3):
+        cache.forward(xs[i % rotate], y=y, ws=ws)
+    torch.cuda.synchronize()
+    s0 = cache.stats()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for i in range(reps):
+        cache.forward(xs[(i + 3) % rotate], y=y, ws=ws)
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / reps
+    s1 = cache.stats()
+    copied = (s1["bytes_copied"] - s0["bytes_copied"]) / reps
+    hits, misses = s1["hits"] - s0["hits"], s1["misses"] - s0["misses"]
+    cache.close()
+    del cache, host, dev, xs, ws
+    torch.cuda.empty_cache()
+    peak = h2d_peak(torch)
+    achieved = copied / (ms / 1e3) / 1e9
+    return {"T": T, "ms": ms, "tokens_per_s": T / (ms / 1e3), "slots": slots, "phases": phases,
+            "experts_host_GB": round(3 * cfg["E"] * cfg["F"] * cfg["H"] * 0.5625 / 1e9, 2),
+            "hit_rate": hits / max(1, hits + misses), "bytes_copied_per_call": copied,
+            "h2d_GBps": achieved, "h2d_peak_GBps": peak, "frac_of_h2d": achieved / peak,
+            "note": "routing varies over 8 activation sets; each call's time includes the "
+                    "routing read-back (host synchronisation) and the copies of the experts "
+                    "not in the cache; h2d_peak is a 1 GiB page-locked copy on this box"}
+
+
 def run_ours(args):
     import torch
     rank, world, local, dist = dist_setup(args.gpus)
@@ -625,6 +695,9 @@ def run_ours(args):
             for v in moe.values():
                 v["frac_of_hbm"] = v["GBps"] / peak
             extra["moe"] = moe
+            # the same layer with its routed experts streamed from host memory
+            extra["moe_streamed"] = {"deepseek_v3_T8_64slots": bench_moe_streamed(
+                torch, dq, synth.MOE_DEEPSEEK, 8, reps=20)}
         sep = bench_layer(torch, dq, args, synth.LLAMA8B_LINEARS, with_e2e=False)
         extra["layer_7_separate_calls"] = {
             "value": round(sep["value"], 2), "unit": "GB/s",
