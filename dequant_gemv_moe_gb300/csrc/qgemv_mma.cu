@@ -192,13 +192,22 @@ struct B1Plan {
   int nstage, off_w, off_x, off_sx, off_inv, off_z, off_red, total;
 };
 
+// Per stage: activations (Q4_K: x and -x of the odd sub-blocks; Q6_K: x) and
+// the negated sums of its 8 (Q4_K) or 16 (Q6_K) sub-blocks.
+template <int FMT>
+struct B1Fmt {
+  static constexpr int kStageX = FMT == DQ_Q4_K ? Q4KB1::kStageX : 512;
+  static constexpr int kSubs = FMT == DQ_Q4_K ? 8 : 16;
+};
+
+template <int FMT>
 __host__ __device__ inline B1Plan b1_plan(int nstage, int ksplit) {
   B1Plan p;
   p.nstage = nstage;
   p.off_w = 1024;                                             // barriers below
-  p.off_x = p.off_w + nstage * Layout<DQ_Q4_K>::W_STAGE;      // 128-byte aligned
-  p.off_sx = p.off_x + nstage * Q4KB1::kStageX;
-  p.off_inv = p.off_sx + nstage * 32;
+  p.off_x = p.off_w + nstage * Layout<FMT>::W_STAGE;          // 128-byte aligned
+  p.off_sx = p.off_x + nstage * B1Fmt<FMT>::kStageX;
+  p.off_inv = p.off_sx + nstage * 4 * B1Fmt<FMT>::kSubs;
   p.off_z = (p.off_inv + nstage * 4 + 127) / 128 * 128;       // 16 zero bytes at +0
   p.off_red = p.off_z + 128;
   p.total = p.off_red + (ksplit > 1 ? (ksplit - 1) * kConsumerWarps * 32 * 16 : 0);
@@ -206,7 +215,7 @@ __host__ __device__ inline B1Plan b1_plan(int nstage, int ksplit) {
 }
 
 struct B1Params {
-  CUtensorMap tmap;  // W as [N rows][row_bytes/2] 16-bit elements, box 144 B x 64 rows
+  CUtensorMap tmap;  // W as [N rows][row_bytes/2] 16-bit elements, box BOX x 64 rows
   int N;
   int nsb;           // super-blocks per row
   const void* x;     // [K], fp16 or bf16
@@ -217,14 +226,15 @@ struct B1Params {
 
 // PAIR: each consumer iteration takes two stages (more independent work per
 // warp, more registers: three CTAs per SM instead of four).
-template <bool BF16, bool PAIR>
+template <int FMT, bool BF16, bool PAIR>
 __global__ void __launch_bounds__(kThreads, PAIR ? 3 : 4)
-    qgemv_q4k_b1_kernel(const __grid_constant__ B1Params p) {
+    qgemv_b1_kernel(const __grid_constant__ B1Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  using L = Layout<DQ_Q4_K>;
+  using L = Layout<FMT>;
+  constexpr int kStageX = B1Fmt<FMT>::kStageX, kSubs = B1Fmt<FMT>::kSubs;
   const int ksplit = (int)cluster_nctarank();
   const int rank = (int)cluster_ctarank();
-  const B1Plan plan = b1_plan(p.nstage, ksplit);
+  const B1Plan plan = b1_plan<FMT>(p.nstage, ksplit);
   uint64_t* full = (uint64_t*)smem;
   uint64_t* empty = full + plan.nstage;
   uint64_t* red_full = empty + plan.nstage;
@@ -250,8 +260,9 @@ __global__ void __launch_bounds__(kThreads, PAIR ? 3 : 4)
   const uint64_t pol = l2_evict_first_policy();
   auto issue = [&](int c, int s) {
     mbar_arrive_expect_tx(&full[s], L::W_STAGE);   // rows past N are zero-filled, still counted
-    tma_load_2d(wbuf + s * L::W_STAGE, &p.tmap, (int)(((int64_t)(sb0 + c) * L::SBB) >> 1), row0,
-                &full[s], pol);
+    // box start: the super-block's first byte rounded down to 16 bytes
+    tma_load_2d(wbuf + s * L::W_STAGE, &p.tmap,
+                (int)((((int64_t)(sb0 + c) * L::SBB) & ~(int64_t)15) >> 1), row0, &full[s], pol);
   };
   const int early = p.w_early ? min(plan.nstage, nsbl) : 0;
   if (threadIdx.x == 0) {
@@ -303,9 +314,9 @@ __global__ void __launch_bounds__(kThreads, PAIR ? 3 : 4)
             h[j] = h2_as_u32(__floats2half2_rn(__uint_as_float(h[j] << 16) * scale,
                                                __uint_as_float(h[j] & 0xFFFF0000u) * scale));
         }
-        uint8_t* xst = smem + plan.off_x + s * Q4KB1::kStageX;
+        uint8_t* xst = smem + plan.off_x + s * kStageX;
         *(uint4*)(xst + 16 * lane) = make_uint4(h[0], h[1], h[2], h[3]);
-        if (lane & 4)   // odd sub-block: its negation too
+        if (FMT == DQ_Q4_K && (lane & 4))   // odd sub-block: its negation too
           *(uint4*)(xst + 512 + 16 * lane) = make_uint4(h[0] ^ 0x80008000u, h[1] ^ 0x80008000u,
                                                         h[2] ^ 0x80008000u, h[3] ^ 0x80008000u);
         float sum = 0.f;
@@ -315,9 +326,12 @@ __global__ void __launch_bounds__(kThreads, PAIR ? 3 : 4)
           sum += f.x;
           sum += f.y;
         }
+        // sub-blocks of 32 (Q4_K: 4 lanes) or 16 (Q6_K: 2 lanes) activations
         sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-        if ((lane & 3) == 0) ((float*)(smem + plan.off_sx + s * 32))[lane >> 2] = -sum;
+        if (FMT == DQ_Q4_K) sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        constexpr int lanes_per_sub = 32 / kSubs;
+        if ((lane & (lanes_per_sub - 1)) == 0)
+          ((float*)(smem + plan.off_sx + s * 4 * kSubs))[lane / lanes_per_sub] = -sum;
         if (lane == 0) ((float*)(smem + plan.off_inv))[s] = inv;
         mbar_arrive(&full[s]);
         if (++s == plan.nstage) {
@@ -329,23 +343,42 @@ __global__ void __launch_bounds__(kThreads, PAIR ? 3 : 4)
   } else {
     // ------------------------------ consumers ------------------------------
     const int cw = warp - 1, g = lane >> 2, t = lane & 3;
-    // mma row g is weight row rg (and rg + 8) of the warp's 16: rows 0,2,4,6
-    // in the first half-warp, 1,3,5,7 in the second, so that the 8-byte quant
-    // loads of a half-warp fall on 32 distinct banks (row pitch 144 bytes)
-    const int rg = 2 * (g & 3) + (g >> 2);
+    // Q4_K: mma row g is weight row rg (and rg + 8) of the warp's 16: rows
+    // 0,2,4,6 in the first half-warp, 1,3,5,7 in the second, so that the
+    // 8-byte quant loads of a half-warp fall on 32 distinct banks (row pitch
+    // 144 bytes).  Q6_K's 4-byte loads at pitch 240 are conflict-free as is.
+    const int rg = FMT == DQ_Q4_K ? 2 * (g & 3) + (g >> 2) : g;
     const Q4KB1::Lane lc = Q4KB1::lane_consts(g, t);
+    uint32_t real6[8];
+#pragma unroll
+    for (int n = 0; n < 8; ++n) real6[n] = n == g ? 1u : 0u;
     const uint32_t wrow = smem_u32(wbuf) + (16 * cw + rg) * L::ROW_PITCH;
-    const uint32_t xg = smem_u32(smem + plan.off_x) + 64 * g + 16 * t;
-    const uint32_t sx = smem_u32(smem + plan.off_sx) + 8 * t;
+    const uint32_t xbase = smem_u32(smem + plan.off_x);
+    const uint32_t sxb = smem_u32(smem + plan.off_sx);
     const uint32_t zb = smem_u32(smem + plan.off_z);
     const float* invs = (const float*)(smem + plan.off_inv);
     float2 accp0 = make_float2(0.f, 0.f), accp8 = make_float2(0.f, 0.f);
     float2 accq0 = make_float2(0.f, 0.f), accq8 = make_float2(0.f, 0.f);
     int s = 0;
     uint32_t ph = 0;
-    auto stage = [&](int st, uint32_t o, float2& a0, float2& a8) {
-      Q4KB1::run(wrow + st * L::W_STAGE + o, 8 * L::ROW_PITCH, xg + Q4KB1::kStageX * st + o, zb,
-                 sx + 32 * st + o, BF16 ? invs[st] : 1.f, lc, a0, a8);
+    // super-block c of this CTA sits in stage st
+    auto stage = [&](int st, int c, uint32_t o, float2& a0, float2& a8) {
+      const float inv = BF16 ? invs[st] : 1.f;
+      if constexpr (FMT == DQ_Q4_K) {
+        Q4KB1::run(wrow + st * L::W_STAGE + o, 8 * L::ROW_PITCH,
+                   xbase + kStageX * st + 64 * g + 16 * t + o, zb, sxb + 4 * kSubs * st + 8 * t + o,
+                   inv, lc, a0, a8);
+      } else {
+        // the 210-byte super-block starts delta bytes into the 16-byte aligned box
+        const int delta = (int)(((int64_t)(sb0 + c) * L::SBB) & 15);
+        const uint32_t ra = wrow + st * L::W_STAGE + delta + o;
+        if (delta & 2)
+          Q6KB1::run<true>(ra, ra + 8 * L::ROW_PITCH, xbase + kStageX * st + o, zb,
+                           sxb + 4 * kSubs * st + o, inv, real6, t, a0, a8);
+        else
+          Q6KB1::run<false>(ra, ra + 8 * L::ROW_PITCH, xbase + kStageX * st + o, zb,
+                            sxb + 4 * kSubs * st + o, inv, real6, t, a0, a8);
+      }
     };
     auto advance = [&]() {
       if (++s == plan.nstage) {
@@ -364,8 +397,8 @@ __global__ void __launch_bounds__(kThreads, PAIR ? 3 : 4)
       if (!mbar_wait(&full[s], ph)) { ok = false; break; }
       advance();
       const uint32_t o = order_after_wait(0u);
-      stage(s0, o, accp0, accp8);
-      stage(s1, o, accq0, accq8);
+      stage(s0, c, o, accp0, accp8);
+      stage(s1, c + 1, o, accq0, accq8);
       keep_before_release(accp0.x, accp0.y, accp8.x, accp8.y);
       keep_before_release(accq0.x, accq0.y, accq8.x, accq8.y);
       __syncwarp();
@@ -377,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, PAIR ? 3 : 4)
     for (; ok && c < nsbl; ++c) {
       if (!mbar_wait(&full[s], ph)) break;
       const uint32_t o = order_after_wait(0u);
-      stage(s, o, accp0, accp8);
+      stage(s, c, o, accp0, accp8);
       keep_before_release(accp0.x, accp0.y, accp8.x, accp8.y);
       __syncwarp();
       if (lane == 0) mbar_arrive_relaxed(&empty[s]);
@@ -385,7 +418,8 @@ __global__ void __launch_bounds__(kThreads, PAIR ? 3 : 4)
     }
     float acc0 = (accp0.x + accp0.y) + (accq0.x + accq0.y);
     float acc8 = (accp8.x + accp8.y) + (accq8.x + accq8.y);
-    // the four lanes of a quad hold sub-blocks (2t, 2t+1): fixed-order sum
+    // the four lanes of a quad hold sub-blocks 2t, 2t+1 (Q6_K: of both
+    // halves): fixed-order sum
     acc0 += __shfl_xor_sync(0xffffffffu, acc0, 1);
     acc8 += __shfl_xor_sync(0xffffffffu, acc8, 1);
     acc0 += __shfl_xor_sync(0xffffffffu, acc0, 2);
@@ -491,10 +525,11 @@ int launch_qgemv_mma_fmt(const void* W, int64_t N, int64_t K, const void* x, int
   return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
 }
 
-// One fp16 / bf16 column of Q4_K: the block-diagonal kernel.
-int launch_qgemv_q4k_b1(const void* W, int64_t N, int64_t K, const void* x, int xdt, float* y,
-                        cudaStream_t stream, int force_ksplit, bool w_early) {
-  using L = Layout<DQ_Q4_K>;
+// One fp16 / bf16 column of Q4_K or Q6_K: the block-diagonal kernel.
+template <int FMT>
+int launch_qgemv_b1(const void* W, int64_t N, int64_t K, const void* x, int xdt, float* y,
+                    cudaStream_t stream, int force_ksplit, bool w_early) {
+  using L = Layout<FMT>;
   B1Params p;
   p.nsb = (int)(K / 256);
   const int tiles = (int)((N + kTileRows - 1) / kTileRows);
@@ -510,8 +545,8 @@ int launch_qgemv_q4k_b1(const void* W, int64_t N, int64_t K, const void* x, int 
   const bool pair = (long)tiles * ks <= 3L * sms;
   const int budget = pair ? 74 * 1024 : 56 * 1024;
   int nstage = 12;
-  while (nstage > 3 && b1_plan(nstage, ks).total > budget) --nstage;
-  const B1Plan plan = b1_plan(nstage, ks);
+  while (nstage > 3 && b1_plan<FMT>(nstage, ks).total > budget) --nstage;
+  const B1Plan plan = b1_plan<FMT>(nstage, ks);
   if (!make_weight_tmap(&p.tmap, W, (uint64_t)N, (uint64_t)p.nsb * L::SBB, L::BOX, kTileRows))
     return DQ_ERR_CUDA;
   p.N = (int)N;
@@ -519,10 +554,10 @@ int launch_qgemv_q4k_b1(const void* W, int64_t N, int64_t K, const void* x, int 
   p.y = y;
   p.nstage = nstage;
   p.w_early = w_early ? 1 : 0;
-  auto kern = xdt == DQ_BF16 ? (pair ? qgemv_q4k_b1_kernel<true, true>
-                                     : qgemv_q4k_b1_kernel<true, false>)
-                             : (pair ? qgemv_q4k_b1_kernel<false, true>
-                                     : qgemv_q4k_b1_kernel<false, false>);
+  auto kern = xdt == DQ_BF16 ? (pair ? qgemv_b1_kernel<FMT, true, true>
+                                     : qgemv_b1_kernel<FMT, true, false>)
+                             : (pair ? qgemv_b1_kernel<FMT, false, true>
+                                     : qgemv_b1_kernel<FMT, false, false>);
   static bool attr_set[4][64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -545,7 +580,9 @@ int launch_qgemv_q4k_b1(const void* W, int64_t N, int64_t K, const void* x, int 
 int launch_qgemv_mma(int fmt, const void* W, int64_t N, int64_t K, const void* x, int xdt,
                      int batch, float* y, cudaStream_t s, int force_ksplit, bool w_early) {
   if (fmt == DQ_Q4_K && batch == 1)
-    return launch_qgemv_q4k_b1(W, N, K, x, xdt, y, s, force_ksplit, w_early);
+    return launch_qgemv_b1<DQ_Q4_K>(W, N, K, x, xdt, y, s, force_ksplit, w_early);
+  if (fmt == DQ_Q6_K && batch == 1)
+    return launch_qgemv_b1<DQ_Q6_K>(W, N, K, x, xdt, y, s, force_ksplit, w_early);
   if (fmt == DQ_Q4_K)
     return launch_qgemv_mma_fmt<DQ_Q4_K>(W, N, K, x, xdt, batch, y, s, force_ksplit, w_early);
   if (fmt == DQ_Q6_K)

@@ -806,4 +806,103 @@ struct Q4KB1 {
   }
 };
 
+// ---------------------------------------------------------------------------
+// Q6_K with one activation column: the block-diagonal core for 16-weight
+// sub-blocks.  A super-block has 16 of them, so it takes two rounds of the 8
+// mma columns: round h carries sub-blocks 8h + n in column n, n = 2r + lh,
+// i.e. the 16 weights 128h + 32r + 16lh + [0, 16).  A holds q (6 bits) as
+// exact fp16 subnormals q * 2^-24; each sub-block is scaled once in fp32:
+//   y_row += d sc_j (sum_k q_k x_k - 32 sum_k x_k)               (j = 0..15)
+// Lane (g, t) supplies rows g and g+8 and weights l = 16lh + 4t + [0, 4) of
+// every sub-block: the low nibbles from ql[64h + 32(r&1) + l] (high nibbles
+// for r >= 2), bits 2r..2r+1 from qh[32h + l].  Its accumulators end with
+// sub-blocks 8h + 2t and 8h + 2t + 1 of both rows, h = 0, 1.
+// ---------------------------------------------------------------------------
+struct Q6KB1 {
+  // 32-bit word at a 2-byte aligned shared address whose misalignment
+  // (0 or 2 bytes, `mis`) is uniform for the stage
+  template <bool MIS>
+  __device__ __forceinline__ static uint32_t ldw(uint32_t a) {
+    if constexpr (!MIS) {
+      return lds_u32_nv(a);
+    } else {
+      const uint32_t lo = lds_u32_nv(a - 2), hi = lds_u32_nv(a + 2);
+      return __funnelshift_r(lo, hi, 16);
+    }
+  }
+
+  // q bytes (4 weights) of run r from the low-bit word (ql, run r&1) and the
+  // high-bit word (qh)
+  __device__ __forceinline__ static uint32_t q4(uint32_t ql, uint32_t qh, int r) {
+    const uint32_t lo = (r & 2) ? (ql >> 4) : ql;
+    const uint32_t hb = r == 0 ? (qh << 4) : r == 1 ? (qh << 2) : r == 2 ? qh : (qh >> 2);
+    return (lo & 0x0F0F0F0Fu) | (hb & 0x30303030u);
+  }
+
+  // one round (half h of the super-block) of rows g / g+8 (ra / rb: their
+  // super-block starts) into D[2][4]
+  template <bool MIS>
+  __device__ __forceinline__ static void round(uint32_t ra, uint32_t rb, int h, uint32_t xs,
+                                               uint32_t z, const uint32_t (&real)[8], int t,
+                                               float (&D)[2][4]) {
+    uint32_t Q[2][2][2], H[2][2];   // [row][run&1][lh], [row][lh]
+    const uint32_t rows[2] = {ra, rb};
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+      for (int lh = 0; lh < 2; ++lh) {
+        Q[rr][0][lh] = ldw<MIS>(rows[rr] + 64 * h + 16 * lh + 4 * t);
+        Q[rr][1][lh] = ldw<MIS>(rows[rr] + 64 * h + 32 + 16 * lh + 4 * t);
+        H[rr][lh] = ldw<MIS>(rows[rr] + 128 + 32 * h + 16 * lh + 4 * t);
+      }
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int lh = 0; lh < 2; ++lh) {
+        const int n = 2 * r + lh;   // column = sub-block 8h + n
+        const uint32_t w0 = q4(Q[0][r & 1][lh], H[0][lh], r);
+        const uint32_t w8 = q4(Q[1][r & 1][lh], H[1][lh], r);
+        const uint2 xv = lds_u64_nv(z + real[n] * (xs + 32 * (8 * h + n) - z));
+        // k slots (2t, 2t+1 | 2t+8, 2t+9) = weights l + (0, 1 | 2, 3)
+        mma_16816_nv(D[lh], __byte_perm(w0, 0, 0x4140), __byte_perm(w8, 0, 0x4140),
+                     __byte_perm(w0, 0, 0x4342), __byte_perm(w8, 0, 0x4342), xv.x, xv.y);
+      }
+  }
+
+  // The two rounds and their scales.  ra / rb: shared addresses of the
+  // super-block in rows g / g+8 (2-byte aligned; MIS: 2 mod 4), from
+  // order_after_wait() of the stage barrier.  xs: the stage's activations
+  // (fp16, natural order; this lane reads 8 bytes at xs + 32 j + 8 t);
+  // z: 8 zero bytes; nsx: the stage's 16 negated sub-block sums (fp32);
+  // inv: inverse activation scale.
+  template <bool MIS>
+  __device__ __forceinline__ static void run(uint32_t ra, uint32_t rb, uint32_t xs, uint32_t z,
+                                             uint32_t nsx, float inv, const uint32_t (&real)[8],
+                                             int t, float2& acc0, float2& acc8) {
+    const uint32_t xl = xs + 8 * t;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float D[2][4] = {};
+      round<MIS>(ra, rb, h, xl, z, real, t, D);
+      // sub-blocks j = 8h + 2t + (0, 1): scales, d, -sum x
+      const uint32_t s0 = lds_u16_nv(ra + 192 + 8 * h + 2 * t);
+      const uint32_t s8 = lds_u16_nv(rb + 192 + 8 * h + 2 * t);
+      const float d0 = __half2float(__ushort_as_half((unsigned short)lds_u16_nv(ra + 208))) * inv;
+      const float d8 = __half2float(__ushort_as_half((unsigned short)lds_u16_nv(rb + 208))) * inv;
+      const uint2 nsu = lds_u64_nv(nsx + 4 * (8 * h + 2 * t));
+      const float2 ns = make_float2(__uint_as_float(nsu.x), __uint_as_float(nsu.y));
+      const float2 sc0 = make_float2((float)(int8_t)(s0 & 0xFF), (float)(int8_t)(s0 >> 8));
+      const float2 sc8 = make_float2((float)(int8_t)(s8 & 0xFF), (float)(int8_t)(s8 >> 8));
+      // products in units of 2^-24; the -32 offset against the sums
+      const float2 c0 = fmul2(sc0, make_float2(d0 * 16777216.f, d0 * 16777216.f));
+      const float2 c8 = fmul2(sc8, make_float2(d8 * 16777216.f, d8 * 16777216.f));
+      const float2 k0 = fmul2(sc0, make_float2(32.f * d0, 32.f * d0));
+      const float2 k8 = fmul2(sc8, make_float2(32.f * d8, 32.f * d8));
+      // column 2t (even sub-block) accumulates in chain 0, 2t+1 in chain 1
+      acc0 = ffma2(ns, k0, ffma2(make_float2(D[0][0], D[1][1]), c0, acc0));
+      acc8 = ffma2(ns, k8, ffma2(make_float2(D[0][2], D[1][3]), c8, acc8));
+    }
+  }
+};
+
 }  // namespace dqmoe

@@ -187,14 +187,42 @@ def test_q4k_batch1_scale_regimes(dq, orc, xdt):
     assert rel.max() <= 1e-3, rel.max()
 
 
+@pytest.mark.parametrize("fmt", [Q4_K, Q6_K])
 @pytest.mark.parametrize("xdt", [1, 2])
 @pytest.mark.parametrize("ks", [1, 2, 3, 5, 8])
-def test_q4k_batch1_ksplit(dq, orc, xdt, ks):
-    # batch-1 kernel under every cluster split (uneven super-block ranges),
+def test_batch1_ksplit(dq, orc, fmt, xdt, ks):
+    # batch-1 kernels under every cluster split (uneven super-block ranges;
+    # Q6_K's 210-byte super-blocks alternate between 4- and 2-byte alignment),
     # ragged rows, rows of 32 and 64 super-blocks
     for N, K in [(130, 8192), (70, 16384)]:
-        err = _case(dq, orc, Q4_K, N, K, 1, xdt, seed=600 + ks * 10 + xdt + K, ksplit=ks)
+        err = _case(dq, orc, fmt, N, K, 1, xdt, seed=600 + ks * 10 + xdt + K + fmt, ksplit=ks)
         assert err <= TOL[xdt], (N, K, err)
+
+
+@pytest.mark.parametrize("xdt", [1, 2])
+def test_q6k_batch1_scales_and_extremes(dq, orc, xdt):
+    # every row's d over several decades and signs, int8 scales of both signs
+    # at their extremes, activations with huge and tiny sub-blocks
+    N, K = 96, 4096
+    g = synth.streams(4646 + xdt, 3)
+    W = synth.quant_matrix(g[0], Q6_K, N, K).reshape(N, K // 256, 210)
+    d = np.float16(np.geomspace(1e-6, 4.0, N) * np.where(np.arange(N) % 3 == 0, -1, 1))
+    W[:, :, 208:210] = d.view(np.uint8).reshape(N, 1, 2)
+    W[::5, :, 192:208] = np.array([127, -128] * 8, dtype=np.int8).view(np.uint8)
+    W = W.reshape(-1)
+    x = synth.activations(g[1], (1, K), 0)
+    x[0, :256] *= np.float32(1.0e4 if xdt == 1 else 3.0e6)
+    x[0, 256:512] *= np.float32(1e-5)
+    x[0, 512:528] = 0.0
+    x = x.astype(np.float16) if xdt == 1 else synth.f32_to_bf16_bits(x)
+    y = dq.qgemv(Q6_K, dev_bytes(W), N, K, dev_act(x, xdt)).cpu().numpy().astype(np.float64)
+    assert dq.device_status() == 0
+    ref = orc.qgemv(Q6_K, W, N, K, x, xdt, 1)
+    wabs = np.abs(orc.dequant(Q6_K, W, N * K).reshape(N, K).astype(np.float64))
+    xabs = np.abs(orc.act_to_f64(xdt, x).reshape(1, K))
+    scale = xabs @ wabs.T
+    rel = np.abs(y - ref) / scale
+    assert rel.max() <= 1e-3, rel.max()
 
 
 @pytest.mark.parametrize("xdt", [1, 2])
