@@ -905,4 +905,85 @@ struct Q6KB1 {
   }
 };
 
+// ---------------------------------------------------------------------------
+// Q8_0 with one activation column: the block-diagonal core.  The 8 blocks of
+// 32 weights of a super-block go to the 8 mma columns.  A holds q + 128 (the
+// int8 quant with its sign bit flipped) as exact fp16 subnormals, and each
+// block is scaled once in fp32:
+//   y_row += d_j (sum_k (q_k + 128) x_k - 128 sum_k x_k)            (j = 0..7)
+// Lane (g, t) supplies rows g and g+8 and weights 8t..8t+7 of every block
+// (bytes 34j + 2 + 8t ..: 4-byte aligned for odd j, 2 bytes off for even j,
+// both known at compile time); its accumulators end with blocks 2t and 2t+1.
+// ---------------------------------------------------------------------------
+struct Q80B1 {
+  // bytes q_{8t..8t+7} of block J of one row (super-block at `row`), as two
+  // words with the sign bits flipped
+  template <int J>
+  __device__ __forceinline__ static uint2 quants(uint32_t row, int t) {
+    const uint32_t a = row + 34 * J + 2 + 8 * t;
+    uint32_t w0, w1;
+    if constexpr (J & 1) {
+      w0 = lds_u32_nv(a);
+      w1 = lds_u32_nv(a + 4);
+    } else {
+      const uint32_t p = lds_u32_nv(a - 2), q = lds_u32_nv(a + 2), r = lds_u32_nv(a + 6);
+      w0 = __funnelshift_r(p, q, 16);
+      w1 = __funnelshift_r(q, r, 16);
+    }
+    return make_uint2(w0 ^ 0x80808080u, w1 ^ 0x80808080u);
+  }
+
+  template <int J>
+  __device__ __forceinline__ static void block(uint32_t ra, uint32_t rb, uint32_t xg, uint32_t z,
+                                               uint32_t real, int t, float (&D)[4]) {
+    const uint2 q0 = quants<J>(ra, t), q8 = quants<J>(rb, t);
+    const uint4 xv = lds_u128_nv(z + real * (xg - z));
+    // k slots (2t, 2t+1 | 2t+8, 2t+9) = weights (8t, 8t+1 | 8t+2, 8t+3), then +4
+    mma_16816_nv(D, __byte_perm(q0.x, 0, 0x4140), __byte_perm(q8.x, 0, 0x4140),
+                 __byte_perm(q0.x, 0, 0x4342), __byte_perm(q8.x, 0, 0x4342), xv.x, xv.y);
+    mma_16816_nv(D, __byte_perm(q0.y, 0, 0x4140), __byte_perm(q8.y, 0, 0x4140),
+                 __byte_perm(q0.y, 0, 0x4342), __byte_perm(q8.y, 0, 0x4342), xv.z, xv.w);
+  }
+
+  // ra / rb: shared addresses of the super-block (272 bytes, 16-byte aligned)
+  // in rows g / g+8, from order_after_wait() of the stage barrier; xg: this
+  // lane's 16 bytes of x (block g, weights 8t..8t+7); ze / zo: 16 zero bytes
+  // read in place of x for even / odd blocks; nsx: (-sum x of block 2t,
+  // -sum of 2t+1); real[j]: block j is this lane's own (j == g).
+  __device__ __forceinline__ static void run(uint32_t ra, uint32_t rb, uint32_t xg, uint32_t ze,
+                                             uint32_t zo, uint32_t nsx, float inv,
+                                             const uint32_t (&real)[8], int t, float2& acc0,
+                                             float2& acc8) {
+    float D[4][4] = {};   // four chains: blocks j, j + 4
+    block<0>(ra, rb, xg, ze, real[0], t, D[0]);
+    block<1>(ra, rb, xg, zo, real[1], t, D[1]);
+    block<2>(ra, rb, xg, ze, real[2], t, D[2]);
+    block<3>(ra, rb, xg, zo, real[3], t, D[3]);
+    block<4>(ra, rb, xg, ze, real[4], t, D[0]);
+    block<5>(ra, rb, xg, zo, real[5], t, D[1]);
+    block<6>(ra, rb, xg, ze, real[6], t, D[2]);
+    block<7>(ra, rb, xg, zo, real[7], t, D[3]);
+    // d of blocks 2t, 2t+1 of each row
+    const float d0a = __half2float(__ushort_as_half((unsigned short)lds_u16_nv(ra + 68 * t)));
+    const float d0b = __half2float(__ushort_as_half((unsigned short)lds_u16_nv(ra + 68 * t + 34)));
+    const float d8a = __half2float(__ushort_as_half((unsigned short)lds_u16_nv(rb + 68 * t)));
+    const float d8b = __half2float(__ushort_as_half((unsigned short)lds_u16_nv(rb + 68 * t + 34)));
+    const uint2 nsu = lds_u64_nv(nsx);
+    const float2 ns = make_float2(__uint_as_float(nsu.x), __uint_as_float(nsu.y));
+    const float2 dd0 = fmul2(make_float2(d0a, d0b), make_float2(inv, inv));
+    const float2 dd8 = fmul2(make_float2(d8a, d8b), make_float2(inv, inv));
+    // products in units of 2^-24; the +128 offset against the sums
+    const float2 c0 = fmul2(dd0, make_float2(16777216.f, 16777216.f));
+    const float2 c8 = fmul2(dd8, make_float2(16777216.f, 16777216.f));
+    const float2 k0 = fmul2(dd0, make_float2(128.f, 128.f));
+    const float2 k8 = fmul2(dd8, make_float2(128.f, 128.f));
+    const float2 s0 = fadd2(fadd2(make_float2(D[0][0], D[0][1]), make_float2(D[1][0], D[1][1])),
+                            fadd2(make_float2(D[2][0], D[2][1]), make_float2(D[3][0], D[3][1])));
+    const float2 s8 = fadd2(fadd2(make_float2(D[0][2], D[0][3]), make_float2(D[1][2], D[1][3])),
+                            fadd2(make_float2(D[2][2], D[2][3]), make_float2(D[3][2], D[3][3])));
+    acc0 = ffma2(ns, k0, ffma2(s0, c0, acc0));
+    acc8 = ffma2(ns, k8, ffma2(s8, c8, acc8));
+  }
+};
+
 }  // namespace dqmoe

@@ -187,7 +187,7 @@ def test_q4k_batch1_scale_regimes(dq, orc, xdt):
     assert rel.max() <= 1e-3, rel.max()
 
 
-@pytest.mark.parametrize("fmt", [Q4_K, Q6_K])
+@pytest.mark.parametrize("fmt", [Q4_K, Q6_K, Q8_0])
 @pytest.mark.parametrize("xdt", [1, 2])
 @pytest.mark.parametrize("ks", [1, 2, 3, 5, 8])
 def test_batch1_ksplit(dq, orc, fmt, xdt, ks):
@@ -242,6 +242,31 @@ def test_q4k_batch1_activation_extremes(dq, orc, xdt):
     ref = orc.qgemv(Q4_K, W, N, K, x, xdt, 1)
     assert np.isfinite(y).all()
     assert rel_err(y, ref) <= TOL[xdt]
+
+
+@pytest.mark.parametrize("xdt", [1, 2])
+def test_q80_batch1_scales_and_extremes(dq, orc, xdt):
+    # d over several decades and signs per block, quants at -127 / 127 and 0,
+    # activations with huge and tiny blocks
+    N, K = 96, 4096
+    g = synth.streams(4747 + xdt, 3)
+    W = synth.quant_matrix(g[0], Q8_0, N, K).reshape(N, K // 32, 34)
+    d = np.float16(np.geomspace(1e-6, 4.0, K // 32) * np.where(np.arange(K // 32) % 3 == 0, -1, 1))
+    W[:, :, 0:2] = d.view(np.uint8).reshape(1, K // 32, 2)
+    W[::7, :, 2:34] = np.array([127, -127, 0, 1] * 8, dtype=np.int8).view(np.uint8)
+    W = W.reshape(-1)
+    x = synth.activations(g[1], (1, K), 0)
+    x[0, :256] *= np.float32(1.0e4 if xdt == 1 else 3.0e6)
+    x[0, 256:512] *= np.float32(1e-5)
+    x[0, 512:544] = 0.0
+    x = x.astype(np.float16) if xdt == 1 else synth.f32_to_bf16_bits(x)
+    y = dq.qgemv(Q8_0, dev_bytes(W), N, K, dev_act(x, xdt)).cpu().numpy().astype(np.float64)
+    assert dq.device_status() == 0
+    ref = orc.qgemv(Q8_0, W, N, K, x, xdt, 1)
+    wabs = np.abs(orc.dequant(Q8_0, W, N * K).reshape(N, K).astype(np.float64))
+    xabs = np.abs(orc.act_to_f64(xdt, x).reshape(1, K))
+    rel = np.abs(y - ref) / (xabs @ wabs.T)
+    assert rel.max() <= 1e-3, rel.max()
 
 
 def test_qgemv_weights_early_and_chains(dq, orc):
