@@ -23,8 +23,11 @@ struct GemvParams {
   int w_early;      // 1: issue the first stages' weight copies before pdl_wait
 };
 
-template <int FMT>
-__global__ void __launch_bounds__(kThreads) qgemv_mma_kernel(const __grid_constant__ GemvParams p) {
+// PAIR: each consumer iteration takes two stages (more independent work per
+// warp and more registers: for grids of at most three CTAs per SM).
+template <int FMT, bool PAIR>
+__global__ void __launch_bounds__(kThreads, PAIR ? 3 : 1)
+    qgemv_mma_kernel(const __grid_constant__ GemvParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   using L = Layout<FMT>;
   const int ksplit = (int)cluster_nctarank();
@@ -110,37 +113,75 @@ __global__ void __launch_bounds__(kThreads) qgemv_mma_kernel(const __grid_consta
     bool ok = true;
     int s = 0;
     uint32_t ph = 0;
-    for (int c = 0; c < nchunk; ++c) {
-      ok = ok && mbar_wait(&full[s], ph);
-      if (ok) {
-        const uint32_t o = order_after_wait(0u);   // stage reads follow the wait
-        const int c0 = sb0 + c;
-        const uint32_t wst = wrow + s * L::W_STAGE + (uint32_t)(((int64_t)c0 * L::SBB) & 15) + o;
-        const uint32_t xcol[1] = {xcol0 + s * p.batch * L::XCOL + o};
-        if constexpr (SBDot<FMT>::kRowScale) {
-          float d[1][2][4] = {};
-          float r0, r8;
-          SBDot<FMT>::template run<1>(wst, 8 * L::ROW_PITCH, xcol, 0, t, d, r0, r8);
-          const float c0 = f16 ? 1.f : xinv[s * 8 + ((2 * t) & 7)];
-          const float c1 = f16 ? 1.f : xinv[s * 8 + ((2 * t + 1) & 7)];
-          fold_tile(acc, d[0], r0, r8, c0, c1);
-        } else if (f16) {
-          SBDot<FMT>::template run<1>(wst, 8 * L::ROW_PITCH, xcol, 0, t, accs);
-        } else {
-          float pt[1][2][4] = {};
-          SBDot<FMT>::template run<1>(wst, 8 * L::ROW_PITCH, xcol, 0, t, pt);
-          const float inv0 = xinv[s * 8 + ((2 * t) & 7)], inv1 = xinv[s * 8 + ((2 * t + 1) & 7)];
-          fold_tile(acc, pt[0], 1.f, 1.f, inv0, inv1);
-        }
-        keep_before_release<4>(acc);                // ... and finish before its release
-        keep_before_release<8>(&accs[0][0][0]);
-        __syncwarp();
-        if (lane == 0) mbar_arrive_relaxed(&empty[s]);
+    // super-block c of this CTA from stage st into (acc_, accs_)
+    auto compute = [&](int st, int c, uint32_t o, float (&acc_)[4], float (&accs_)[1][2][4]) {
+      const int c0 = sb0 + c;
+      const uint32_t wst = wrow + st * L::W_STAGE + (uint32_t)(((int64_t)c0 * L::SBB) & 15) + o;
+      const uint32_t xcol[1] = {xcol0 + st * p.batch * L::XCOL + o};
+      if constexpr (SBDot<FMT>::kRowScale) {
+        float d[1][2][4] = {};
+        float r0, r8;
+        SBDot<FMT>::template run<1>(wst, 8 * L::ROW_PITCH, xcol, 0, t, d, r0, r8);
+        const float c0s = f16 ? 1.f : xinv[st * 8 + ((2 * t) & 7)];
+        const float c1s = f16 ? 1.f : xinv[st * 8 + ((2 * t + 1) & 7)];
+        fold_tile(acc_, d[0], r0, r8, c0s, c1s);
+      } else if (f16) {
+        SBDot<FMT>::template run<1>(wst, 8 * L::ROW_PITCH, xcol, 0, t, accs_);
+      } else {
+        float pt[1][2][4] = {};
+        SBDot<FMT>::template run<1>(wst, 8 * L::ROW_PITCH, xcol, 0, t, pt);
+        const float inv0 = xinv[st * 8 + ((2 * t) & 7)], inv1 = xinv[st * 8 + ((2 * t + 1) & 7)];
+        fold_tile(acc_, pt[0], 1.f, 1.f, inv0, inv1);
       }
+    };
+    auto advance = [&]() {
       if (++s == plan.nstage) {
         s = 0;
         ph ^= 1;
       }
+    };
+    float accB[4] = {0.f, 0.f, 0.f, 0.f};
+    float accsB[1][2][4] = {};
+    int c = 0;
+    for (; PAIR && c + 1 < nchunk; c += 2) {
+      const int s0 = s;
+      const uint32_t p0 = ph;
+      advance();
+      const int s1 = s;
+      const uint32_t p1 = ph;
+      advance();
+      ok = ok && mbar_wait(&full[s0], p0) && mbar_wait(&full[s1], p1);
+      if (!ok) continue;   // after a timed-out wait: walk on without waits or reads
+      const uint32_t o = order_after_wait(0u);   // stage reads follow the waits
+      compute(s0, c, o, acc, accs);
+      compute(s1, c + 1, o, accB, accsB);
+      keep_before_release<4>(acc);              // ... and finish before their release
+      keep_before_release<8>(&accs[0][0][0]);
+      keep_before_release<4>(accB);
+      keep_before_release<8>(&accsB[0][0][0]);
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_relaxed(&empty[s0]);
+        mbar_arrive_relaxed(&empty[s1]);
+      }
+    }
+    for (; c < nchunk; ++c) {
+      const int s0 = s;
+      const uint32_t p0 = ph;
+      advance();
+      ok = ok && mbar_wait(&full[s0], p0);
+      if (!ok) continue;
+      const uint32_t o = order_after_wait(0u);
+      compute(s0, c, o, acc, accs);
+      keep_before_release<4>(acc);
+      keep_before_release<8>(&accs[0][0][0]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_relaxed(&empty[s0]);
+    }
+    for (int i = 0; i < 4; ++i) {
+      acc[i] += accB[i];
+      accs[0][0][i] += accsB[0][0][i];
+      accs[0][1][i] += accsB[0][1][i];
     }
     if (!SBDot<FMT>::kRowScale && f16)
       for (int i = 0; i < 4; ++i) acc[i] = accs[0][0][i] + accs[0][1][i];
@@ -505,26 +546,37 @@ int launch_qgemv_mma_fmt(const void* W, int64_t N, int64_t K, const void* x, int
   if (sms <= 0) return DQ_ERR_CUDA;
   // shared memory per CTA <= 56 KB so that four CTAs (20 warps) share an SM
   constexpr int kSmemBudget = 56 * 1024;
-  int ks = force_ksplit > 0 ? force_ksplit : choose_ksplit(tiles, p.nsb, sms);
+  // two or more tiles per SM: unsplit (28672 x 8192 at batch 8: Q4_K 34.5
+  // us paired against 38.3 us split in two, Q8_0 46.6 against 50.6 us,
+  // Q6_K even)
+  int ks = force_ksplit > 0 ? force_ksplit
+                            : (tiles >= 2 * sms ? 1 : choose_ksplit(tiles, p.nsb, sms));
   ks = std::max(1, std::min(ks, std::min(8, p.nsb)));
+  // Q4_K grids of at most three CTAs per SM take the paired kernel with
+  // deeper rings (28672 x 8192 at batch 8: 34.4 us against 38.2 us split in
+  // two); the heavier Q6_K / Q8_0 decodes measured slower paired (64.1 / 54.1
+  // us against 56.0 / 50.3 us)
+  const bool pair = FMT == DQ_Q4_K && (long)tiles * ks <= 3L * sms;
+  const int budget = pair ? 74 * 1024 : kSmemBudget;
   int nstage = 12;
-  while (nstage > 3 && make_plan<FMT>(nstage, batch, ks).total > kSmemBudget) --nstage;
+  while (nstage > 3 && make_plan<FMT>(nstage, batch, ks).total > budget) --nstage;
   p.nstage = nstage;
   const SmemPlan plan = make_plan<FMT>(nstage, batch, ks);
-  static bool attr_set[64] = {false};
+  auto kern = pair ? qgemv_mma_kernel<FMT, true> : qgemv_mma_kernel<FMT, false>;
+  static bool attr_set[2][64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 64 || !attr_set[dev]) {
-    if (cudaFuncSetAttribute(qgemv_mma_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             200 * 1024) != cudaSuccess)
+  if (dev >= 64 || !attr_set[pair][dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) !=
+        cudaSuccess)
       return DQ_ERR_CUDA;
-    if (cudaFuncSetAttribute(qgemv_mma_kernel<FMT>, cudaFuncAttributeNonPortableClusterSizeAllowed,
-                             1) != cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+        cudaSuccess)
       return DQ_ERR_CUDA;
-    if (dev < 64) attr_set[dev] = true;
+    if (dev < 64) attr_set[pair][dev] = true;
   }
-  if (launch_pdl(qgemv_mma_kernel<FMT>, dim3((unsigned)ks, (unsigned)tiles, 1), dim3(kThreads),
-                 (size_t)plan.total, stream, ks, p) != cudaSuccess)
+  if (launch_pdl(kern, dim3((unsigned)ks, (unsigned)tiles, 1), dim3(kThreads), (size_t)plan.total,
+                 stream, ks, p) != cudaSuccess)
     return DQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
 }
