@@ -504,18 +504,16 @@ int device_sms() {
 }
 
 // Pick the K-split (cluster size).  Measured on GB300 (graphs of back-to-back
-// launches): with two or more 64-row tiles per SM the unsplit grid (or a split
-// in two for long rows) is within a few percent of the best; with fewer, the
-// best split is the largest power of
-// two whose CTAs all fit at once (four per SM, the 56 KB shared-memory
-// budget).  Odd cluster sizes (3, 5, 6, 7) measured slower than the
-// neighbouring powers of two on every shape tried: a cluster's CTAs share one
-// GPC, and odd sizes leave SMs of it idle.
+// launches): with two or more 64-row tiles per SM the unsplit grid is best
+// (28672 x 8192: batch 1 23.8 us unsplit against 29.0 us split in two; batch
+// 8 Q4_K 34.5 against 38.3 us, Q8_0 46.6 against 50.6 us, Q6_K even); with
+// fewer, the best split is the largest power of two whose CTAs all fit at
+// once (four per SM, the 56 KB shared-memory budget).  Odd cluster sizes
+// (3, 5, 6, 7) measured slower than the neighbouring powers of two on every
+// shape tried: a cluster's CTAs share one GPC, and odd sizes leave SMs of it
+// idle.
 int choose_ksplit(int tiles, int nsb, int sms) {
-  // many tiles: unsplit, except long rows (>= 32 super-blocks), where halving
-  // each CTA's range measured 6-11% faster (28672 x 8192; at 28672 x 4096 the
-  // split gained nothing)
-  if (tiles >= 2 * sms) return (nsb >= 32 && (long)tiles * 2 <= 8L * sms) ? 2 : 1;
+  if (tiles >= 2 * sms) return 1;
   int s = 1;
   while (2 * s <= 8 && 2 * s <= nsb && (long)tiles * 2 * s <= 4L * sms) s *= 2;
   return s;
@@ -546,11 +544,7 @@ int launch_qgemv_mma_fmt(const void* W, int64_t N, int64_t K, const void* x, int
   if (sms <= 0) return DQ_ERR_CUDA;
   // shared memory per CTA <= 56 KB so that four CTAs (20 warps) share an SM
   constexpr int kSmemBudget = 56 * 1024;
-  // two or more tiles per SM: unsplit (28672 x 8192 at batch 8: Q4_K 34.5
-  // us paired against 38.3 us split in two, Q8_0 46.6 against 50.6 us,
-  // Q6_K even)
-  int ks = force_ksplit > 0 ? force_ksplit
-                            : (tiles >= 2 * sms ? 1 : choose_ksplit(tiles, p.nsb, sms));
+  int ks = force_ksplit > 0 ? force_ksplit : choose_ksplit(tiles, p.nsb, sms);
   ks = std::max(1, std::min(ks, std::min(8, p.nsb)));
   // Q4_K grids of at most three CTAs per SM take the paired kernel with
   // deeper rings (28672 x 8192 at batch 8: 34.4 us against 38.2 us split in
@@ -591,10 +585,7 @@ int launch_qgemv_b1(const void* W, int64_t N, int64_t K, const void* x, int xdt,
   const int tiles = (int)((N + kTileRows - 1) / kTileRows);
   const int sms = device_sms();
   if (sms <= 0) return DQ_ERR_CUDA;
-  // with two or more tiles per SM the unsplit grid measured best for this
-  // kernel (28672 x 8192: 29.0 us unsplit, 29.3 us split in two)
-  int ks = force_ksplit > 0 ? force_ksplit
-                            : (tiles >= 2 * sms ? 1 : choose_ksplit(tiles, p.nsb, sms));
+  int ks = force_ksplit > 0 ? force_ksplit : choose_ksplit(tiles, p.nsb, sms);
   ks = std::max(1, std::min(ks, std::min(8, p.nsb)));
   // grids that fit three CTAs per SM take the paired kernel with deeper rings
   // (28672 x 8192: 23.8 us against 28.2 us); larger ones four CTAs per SM
