@@ -712,7 +712,7 @@ def run_ours(args):
         return
     kern_bytes = (lay["weight_bytes"] + lay["act_bytes"]) / lay["n_linears"]
     achieved = kern_bytes / (lay["kern_ms"] / 1e3) / 1e9
-    tr = _traffic_record("qgemv_q4k_b1_kernel")
+    tr = _traffic_record("qgemv_b1_kernel<Q4_K>")
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
@@ -727,7 +727,7 @@ def run_ours(args):
                    "l2": "4 rotating weight copies, 491 MB > 3x L2",
                    "frac_of_hbm": round(value / world / peak, 4),
                    "parallelism": "replicas" if world > 1 else "single"},
-        "roofline": {"bound": "hbm", "kernel": "qgemv_q4k_b1_kernel",
+        "roofline": {"bound": "hbm", "kernel": "qgemv_b1_kernel<Q4_K>",
                      "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": peak_src + " hbm_gbs (MEASURED_PEAKS.json)",
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
