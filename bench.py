@@ -365,12 +365,16 @@ def bench_layer(torch, dq, args, lin, with_e2e=True):
         time.sleep(0.1)
     ms = start.elapsed_time(end)
     del graphs, rem
-    # timed region 2 (per-launch durations for the roofline): the same steps
-    # with an event before and after every launch, one graph per step so that
-    # every event keeps its own timestamp.  Events between launches serialise
-    # them, so these durations exclude the overlap the value above gets.
+    # the roofline's average launch duration: the timed region above (CUDA
+    # events around it, on the stream that replays the graphs) over its launches
+    kern_ms = ms / (K * nl)
+    kern_src = ("cuda events around the timed region / %d launches (back to back, as in the "
+                "value)" % (K * nl))
+    # for reference, timed region 2: the same steps with an event before and
+    # after every launch (one graph per step, so that every event keeps its own
+    # timestamp); events between launches serialise them and add their gaps
     ext_ok = make_event(torch, True) is not None
-    kern_ms, kern_src = None, "graph_step_time/%d" % nl
+    ser_ms = None
     if ext_ok and with_e2e:
         G = max(ROTATE, min(K, 400) - min(K, 400) % ROTATE)
         egraphs, evsets = [], []
@@ -391,14 +395,11 @@ def bench_layer(torch, dq, args, lin, with_e2e=True):
         tot = 0.0
         for e in evsets:
             tot += sum(e[j].elapsed_time(e[j + 1]) for j in range(len(lin)))
-        kern_ms = tot / (G * len(lin))
-        kern_src = ("cuda events around each launch, %d steps replayed after the timed region "
-                    "(launches serialised by the events)" % G)
+        ser_ms = tot / (G * len(lin))
         del egraphs
-    else:
-        kern_ms = ms / (K * len(lin))
     res = {"ms_per_step": ms / K, "weight_bytes": wbytes, "act_bytes": abytes,
            "value": wbytes * K / (ms / 1e3) / 1e9, "kern_ms": kern_ms, "kern_src": kern_src,
+           "serialised_launch_ms": ser_ms,
            "clocks": clk.summary(t0, t1), "launches": K * len(lin), "n_linears": nl}
     if not with_e2e:
         del Ws
@@ -733,6 +734,9 @@ def run_ours(args):
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": tr["dram_bytes_per_launch"] if tr else None,
                      "launch_time_source": lay["kern_src"],
+                     "achieved_serialised": (round(kern_bytes / (lay["serialised_launch_ms"] / 1e3)
+                                                   / 1e9, 1)
+                                             if lay.get("serialised_launch_ms") else None),
                      "alg_bytes_per_launch": kern_bytes},
         "cpu_baseline": cpu,
         "e2e": lay["e2e"],
