@@ -13,7 +13,7 @@ import numpy as np
 
 from . import build as _build
 
-OR_Q4_K, OR_Q6_K, OR_Q8_0, OR_Q4_0, OR_Q5_K, OR_NVFP4 = 1, 2, 3, 4, 5, 6
+OR_Q4_K, OR_Q6_K, OR_Q8_0, OR_Q4_0, OR_Q5_K, OR_NVFP4, OR_Q2_K, OR_Q3_K = 1, 2, 3, 4, 5, 6, 7, 8
 OR_F32, OR_F16, OR_BF16 = 0, 1, 2
 
 _lib = None

@@ -162,6 +162,49 @@ void decode_q5k(const uint8_t* b, double* w) {
   }
 }
 
+// Q2_K: 16 bytes of (scale | min << 4) for the sixteen 16-weight sub-blocks,
+// 64 bytes of 2-bit quants, fp16 d, fp16 dmin (84 bytes).  Weight
+// 128h + 32r + l (h = 0..1, r = 0..3, l = 0..31) takes bits 2r..2r+1 of
+// qs[32h + l]; sub-block j = weight / 16.  w = d*(sc_j & 15)*q - dmin*(sc_j >> 4).
+void decode_q2k(const uint8_t* b, double* w) {
+  const uint8_t* sc = b;
+  const uint8_t* qs = b + 16;
+  const double d = half_to_f64(rd16(b + 80));
+  const double dmin = half_to_f64(rd16(b + 82));
+  for (int h = 0; h < 2; ++h)
+    for (int r = 0; r < 4; ++r)
+      for (int l = 0; l < 32; ++l) {
+        const int i = 128 * h + 32 * r + l;
+        const int q = (qs[32 * h + l] >> (2 * r)) & 3;
+        const int j = i / 16;
+        w[i] = d * (sc[j] & 15) * q - dmin * (sc[j] >> 4);
+      }
+}
+
+// Q3_K: hmask[32] (high bits), 64 bytes of 2-bit low quants, 12 bytes of
+// sixteen 6-bit scales, fp16 d (110 bytes).  Weight 128h + 32r + l: low bits
+// 2r..2r+1 of qs[32h + l], high bit = bit 4h + r of hmask[l];
+// q = low - (high ? 0 : 4), in [-4, 3].  Scale j: low 4 bits = nibble j / 8 of
+// scales[j % 8], high 2 bits = bits 2(j / 4)..2(j / 4)+1 of scales[8 + j % 4];
+// w = d*(s_j - 32)*q, sub-block j = weight / 16.
+void decode_q3k(const uint8_t* b, double* w) {
+  const uint8_t* hm = b;
+  const uint8_t* qs = b + 32;
+  const uint8_t* s = b + 96;
+  const double d = half_to_f64(rd16(b + 108));
+  int sc[16];
+  for (int j = 0; j < 16; ++j)
+    sc[j] = (((s[j % 8] >> (4 * (j / 8))) & 15) | (((s[8 + j % 4] >> (2 * (j / 4))) & 3) << 4)) - 32;
+  for (int h = 0; h < 2; ++h)
+    for (int r = 0; r < 4; ++r)
+      for (int l = 0; l < 32; ++l) {
+        const int i = 128 * h + 32 * r + l;
+        const int low = (qs[32 * h + l] >> (2 * r)) & 3;
+        const int high = (hm[l] >> (4 * h + r)) & 1;
+        w[i] = d * sc[i / 16] * (low - (high ? 0 : 4));
+      }
+}
+
 // E2M1 (FP4): sign, 2-bit exponent (bias 1), 1-bit mantissa; exponent 0 is
 // subnormal (0 or 0.5).  Magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6.
 double e2m1_to_f64(int c) {
@@ -201,6 +244,8 @@ bool geometry(int fmt, int* qk, int* bytes) {
     case OR_Q4_0: *qk = 32; *bytes = 18; return true;
     case OR_Q5_K: *qk = 256; *bytes = 176; return true;
     case OR_NVFP4: *qk = 256; *bytes = 144; return true;
+    case OR_Q2_K: *qk = 256; *bytes = 84; return true;
+    case OR_Q3_K: *qk = 256; *bytes = 110; return true;
     default: return false;
   }
 }
@@ -211,6 +256,8 @@ void decode_block(int fmt, const uint8_t* b, double* w) {
   else if (fmt == OR_Q8_0) decode_q80(b, w);
   else if (fmt == OR_Q4_0) decode_q40(b, w);
   else if (fmt == OR_Q5_K) decode_q5k(b, w);
+  else if (fmt == OR_Q2_K) decode_q2k(b, w);
+  else if (fmt == OR_Q3_K) decode_q3k(b, w);
   else decode_nvfp4(b, w);
 }
 

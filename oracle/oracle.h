@@ -12,7 +12,8 @@
  *   [Titan Engine, §MoE 专家流式加载]  sparse activation, 2 of 8 experts
  *   [KTransformers, §支持的量化格式]  Q4_K_M / Q6_K / Q8_0
  *   [NTransformer (Show HN), §量化支持]  Q8_0 / Q4_K_M / Q6_K
- *   [KTransformers, §支持的量化格式]  Q4_0 / Q5_K (the other GGUF blocks)
+ *   [KTransformers, §支持的量化格式]  Q4_0 / Q5_K / Q2_K / Q3_K (the other GGUF
+ *                                    blocks the page lists)
  *   [Titan Engine, §激进量化策略 / §模型格式支持]  NVIDIA FP4 (Blackwell's
  *       native 4-bit float): E2M1 values with E4M3 scales per 16 weights
  *
@@ -29,7 +30,8 @@ extern "C" {
 
 /* format ids and activation dtype ids, same numbering as the public ABI but
  * declared independently */
-enum { OR_Q4_K = 1, OR_Q6_K = 2, OR_Q8_0 = 3, OR_Q4_0 = 4, OR_Q5_K = 5, OR_NVFP4 = 6 };
+enum { OR_Q4_K = 1, OR_Q6_K = 2, OR_Q8_0 = 3, OR_Q4_0 = 4, OR_Q5_K = 5, OR_NVFP4 = 6,
+       OR_Q2_K = 7, OR_Q3_K = 8 };
 enum { OR_F32 = 0, OR_F16 = 1, OR_BF16 = 2 };
 
 /* weights per block / bytes per block */

@@ -14,6 +14,9 @@ Recipe (the pages name no dataset; everything is synthetic):
   * Q8_0: d as Q4_K; the 32 int8 quants uniform over -127..127.
   * Q4_0: d as Q4_K; the 16 quant bytes uniform.  Q5_K: as Q4_K, plus the
     32 fifth-bit bytes uniform.
+  * Q2_K: the 16 scale/min bytes and 64 quant bytes uniform; d at 80 and
+    dmin at 82 as Q4_K.  Q3_K: hmask, quants and the 12 scale bytes uniform;
+    d at 108 as Q4_K.
   * NVFP4: the 128 code bytes uniform; the 16 E4M3 scale bytes positive with
     exponent field uniform over 1..6 and mantissa field uniform (scales
     2^-6 .. 2^-1 * 1.875: weights within +-0.7, the range of Q4_K's).
@@ -23,8 +26,9 @@ Recipe (the pages name no dataset; everything is synthetic):
 import numpy as np
 
 BLOCK = {1: (256, 144), 2: (256, 210), 3: (32, 34), 4: (32, 18), 5: (256, 176),
-         6: (256, 144)}  # fmt -> (weights, bytes)
-FMT_NAMES = {"q4_k": 1, "q6_k": 2, "q8_0": 3, "q4_0": 4, "q5_k": 5, "nvfp4": 6}
+         6: (256, 144), 7: (256, 84), 8: (256, 110)}  # fmt -> (weights, bytes)
+FMT_NAMES = {"q4_k": 1, "q6_k": 2, "q8_0": 3, "q4_0": 4, "q5_k": 5, "nvfp4": 6, "q2_k": 7,
+             "q3_k": 8}
 DT_NAMES = {"f32": 0, "f16": 1, "bf16": 2}
 BASE_SEED = 20261202
 
@@ -59,6 +63,11 @@ def quant_matrix(rng, fmt, rows, cols):
     elif fmt == 5:      # Q5_K: d at 0, dmin at 2 (as Q4_K)
         blk[:, 0:2] = _scale_f16(rng, nblk).view(np.uint8).reshape(nblk, 2)
         blk[:, 2:4] = _scale_f16(rng, nblk).view(np.uint8).reshape(nblk, 2)
+    elif fmt == 7:      # Q2_K: d at 80, dmin at 82
+        blk[:, 80:82] = _scale_f16(rng, nblk).view(np.uint8).reshape(nblk, 2)
+        blk[:, 82:84] = _scale_f16(rng, nblk).view(np.uint8).reshape(nblk, 2)
+    elif fmt == 8:      # Q3_K: d at 108
+        blk[:, 108:110] = _scale_f16(rng, nblk).view(np.uint8).reshape(nblk, 2)
     else:               # NVFP4: 16 positive E4M3 scale bytes with exponent field 1..6
         ef = rng.integers(1, 7, size=(nblk, 16), dtype=np.uint8)
         mf = rng.integers(0, 8, size=(nblk, 16), dtype=np.uint8)

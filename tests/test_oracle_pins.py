@@ -21,7 +21,7 @@ from scipy.special import softmax
 import synth
 from golden_io import read_block_cases
 
-Q4_K, Q6_K, Q8_0, Q4_0, Q5_K, NVFP4 = 1, 2, 3, 4, 5, 6
+Q4_K, Q6_K, Q8_0, Q4_0, Q5_K, NVFP4, Q2_K, Q3_K = 1, 2, 3, 4, 5, 6, 7, 8
 
 
 # ---------------------------------------------------------------------------
@@ -29,7 +29,9 @@ Q4_K, Q6_K, Q8_0, Q4_0, Q5_K, NVFP4 = 1, 2, 3, 4, 5, 6
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("fname,fmt,qk", [("q4_k_blocks.txt", Q4_K, 256),
                                           ("q6_k_blocks.txt", Q6_K, 256),
-                                          ("q8_0_blocks.txt", Q8_0, 32)])
+                                          ("q8_0_blocks.txt", Q8_0, 32),
+                                          ("q2_k_blocks.txt", Q2_K, 256),
+                                          ("q3_k_blocks.txt", Q3_K, 256)])
 def test_dequant_golden_blocks(orc, fname, fmt, qk):
     cases = read_block_cases(fname)
     assert len(cases) >= 3
@@ -42,8 +44,9 @@ def test_dequant_blocks_independent(orc):
     # decoding two blocks at once equals decoding each alone (no state leaks
     # across blocks; the block stride is the format's byte size)
     g = synth.streams(7, 3)
-    for fmt, qk, nb in [(Q4_K, 256, 144), (Q6_K, 256, 210), (Q8_0, 32, 34)]:
-        raw = synth.quant_matrix(g[fmt - 1], fmt, 3, qk)
+    for i, (fmt, qk, nb) in enumerate([(Q4_K, 256, 144), (Q6_K, 256, 210), (Q8_0, 32, 34),
+                                       (Q2_K, 256, 84), (Q3_K, 256, 110)]):
+        raw = synth.quant_matrix(g[i % 3], fmt, 3, qk)
         both = orc.dequant(fmt, raw, 3 * qk)
         for i in range(3):
             one = orc.dequant(fmt, raw[i * nb:(i + 1) * nb], qk)
@@ -211,6 +214,125 @@ def test_q5k_fifth_bit_walk(orc):
 
 
 # ---------------------------------------------------------------------------
+# Q2_K / Q3_K: bit walks, a reduction of one to the other
+# ---------------------------------------------------------------------------
+def _q2k_block(sc, qs, d, dmin):
+    b = np.zeros(84, dtype=np.uint8)
+    b[0:16] = sc
+    b[16:80] = qs
+    b[80:82] = np.array([d], dtype=np.float16).view(np.uint8)
+    b[82:84] = np.array([dmin], dtype=np.float16).view(np.uint8)
+    return b
+
+
+def _q3k_block(hm, qs, sc, d):
+    b = np.zeros(110, dtype=np.uint8)
+    b[0:32] = hm
+    b[32:96] = qs
+    b[96:108] = sc
+    b[108:110] = np.array([d], dtype=np.float16).view(np.uint8)
+    return b
+
+
+def test_q2k_quant_bits_each_feed_one_weight(orc):
+    # d = 1, every scale 1, min 0: each of the 512 quant bits moves exactly one
+    # weight, by 1 (low bit of its field) or 2 (high bit); every weight is
+    # reached by exactly two bits, one of each.
+    base = _q2k_block(np.full(16, 1), np.zeros(64), 1.0, 0.0)
+    assert np.all(orc.dequant(Q2_K, base, 256) == 0.0)
+    mags = [[] for _ in range(256)]
+    for byte in range(64):
+        for bit in range(8):
+            b = base.copy()
+            b[16 + byte] = 1 << bit
+            w = orc.dequant(Q2_K, b, 256).astype(np.float64)
+            nz = np.nonzero(w)[0]
+            assert nz.size == 1, (byte, bit)
+            mags[nz[0]].append(w[nz[0]])
+    assert all(sorted(m) == [1.0, 2.0] for m in mags)
+
+
+def test_q2k_scale_bits_each_feed_one_field(orc):
+    # q = 1 everywhere, d = dmin = 1: bit k of scale byte j changes exactly the
+    # 16 weights of sub-block j, by +2^k (scale nibble) or -2^(k-4) (min nibble)
+    base = _q2k_block(np.zeros(16), np.full(64, 0x55), 1.0, 1.0)
+    assert np.all(orc.dequant(Q2_K, base, 256) == 0.0)
+    for j in range(16):
+        for k in range(8):
+            b = base.copy()
+            b[j] = 1 << k
+            w = orc.dequant(Q2_K, b, 256).astype(np.float64)
+            want = np.zeros(256)
+            want[16 * j:16 * j + 16] = 2.0 ** k if k < 4 else -(2.0 ** (k - 4))
+            np.testing.assert_array_equal(w, want, err_msg=str((j, k)))
+
+
+def test_q3k_bits_each_feed_one_weight(orc):
+    # d = 1, every scale s = 33 (factor 1), all high bits set, low quants 0: all
+    # weights 0.  Each low-quant bit raises exactly one weight by 1 or 2 and
+    # each hmask bit, cleared, lowers exactly one weight by 4; every weight
+    # is reached by two low bits and one hmask bit.
+    sc = np.array([0x11] * 8 + [0xAA] * 4, dtype=np.uint8)
+    base = _q3k_block(np.full(32, 0xFF), np.zeros(64), sc, 1.0)
+    assert np.all(orc.dequant(Q3_K, base, 256) == 0.0)
+    mags = [[] for _ in range(256)]
+    for byte in range(64):
+        for bit in range(8):
+            b = base.copy()
+            b[32 + byte] = 1 << bit
+            w = orc.dequant(Q3_K, b, 256).astype(np.float64)
+            nz = np.nonzero(w)[0]
+            assert nz.size == 1, (byte, bit)
+            mags[nz[0]].append(w[nz[0]])
+    for byte in range(32):
+        for bit in range(8):
+            b = base.copy()
+            b[byte] = 0xFF ^ (1 << bit)
+            w = orc.dequant(Q3_K, b, 256).astype(np.float64)
+            nz = np.nonzero(w)[0]
+            assert nz.size == 1, (byte, bit)
+            mags[nz[0]].append(w[nz[0]])
+    assert all(sorted(m) == [-4.0, 1.0, 2.0] for m in mags)
+
+
+def test_q3k_scale_bits_each_feed_one_field(orc):
+    # q = 1 everywhere, d = 1, all scale bytes 0 (s = 0, w = -32): each of the
+    # 96 scale bits raises exactly one sub-block of 16 weights by a power of
+    # two from 1 to 32; the 96 bits make 16 sub-blocks x 6 distinct bits.
+    base = _q3k_block(np.full(32, 0xFF), np.full(64, 0x55), np.zeros(12), 1.0)
+    np.testing.assert_array_equal(orc.dequant(Q3_K, base, 256), -32.0)
+    seen = set()
+    for byte in range(12):
+        for bit in range(8):
+            b = base.copy()
+            b[96 + byte] = 1 << bit
+            diff = orc.dequant(Q3_K, b, 256).astype(np.float64) + 32.0
+            nz = np.nonzero(diff)[0]
+            assert nz.size == 16 and nz[0] % 16 == 0 and np.all(np.diff(nz) == 1), (byte, bit)
+            v = diff[nz[0]]
+            assert np.all(diff[nz] == v) and v == 2.0 ** round(np.log2(v)) and 1 <= v <= 32
+            field = (nz[0] // 16, int(np.log2(v)))
+            assert field not in seen
+            seen.add(field)
+            # the low nibbles (bytes 0..7) carry the four low scale bits
+            assert (byte < 8) == (v < 16)
+    assert len(seen) == 96
+
+
+def test_q3k_with_high_bits_set_is_q2k(orc):
+    # every hmask bit set and every 6-bit scale 33 (factor 1): Q3_K decodes as
+    # the Q2_K block of the same quant bytes and d with scale 1, min 0
+    rng = np.random.default_rng(707)
+    sc3 = np.array([0x11] * 8 + [0xAA] * 4, dtype=np.uint8)
+    for _ in range(4):
+        qs = rng.integers(0, 256, size=64)
+        d = float(np.float16(abs(rng.standard_normal()) * 0.01))
+        a = orc.dequant(Q3_K, _q3k_block(np.full(32, 0xFF), qs, sc3, d), 256)
+        b = orc.dequant(Q2_K, _q2k_block(np.full(16, 1), qs, d, 0.0), 256)
+        np.testing.assert_array_equal(a, b)
+
+
+# ---------------------------------------------------------------------------
 # NVFP4: the E2M1 and E4M3 value tables, a reduction to Q8_0, placement walks
 # ---------------------------------------------------------------------------
 E2M1_TABLE = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0,
@@ -286,7 +408,7 @@ def test_nvfp4_placement_walk(orc):
 # ---------------------------------------------------------------------------
 # qGEMV: brute force against numpy on tiny shapes; an exact integer case
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("fmt", [Q4_K, Q6_K, Q8_0, Q4_0, Q5_K, NVFP4])
+@pytest.mark.parametrize("fmt", [Q4_K, Q6_K, Q8_0, Q4_0, Q5_K, NVFP4, Q2_K, Q3_K])
 @pytest.mark.parametrize("xdt", [0, 1, 2])
 def test_qgemv_brute_force(orc, fmt, xdt):
     g = synth.streams(100 + fmt * 10 + xdt, 4)
