@@ -682,8 +682,9 @@ def run_ours(args):
         for v in f70.values():
             v["frac_of_hbm"] = round(v["weight_GBps"] / peak, 4)
         extra["gemv_70b_formats"] = f70
-        # the further block formats (Q4_0, Q5_K, NVFP4) on the gate shape
-        fx = bench_gemv_70b_formats(torch, dq, fmts=((4, "q4_0"), (5, "q5_k"), (6, "nvfp4")),
+        # the further block formats (Q4_0, Q5_K, NVFP4, Q2_K, Q3_K) on the gate shape
+        fx = bench_gemv_70b_formats(torch, dq, fmts=((4, "q4_0"), (5, "q5_k"), (6, "nvfp4"),
+                                                     (7, "q2_k"), (8, "q3_k")),
                                     shapes=[("up", 28672, 8192)])
         for v in fx.values():
             v["frac_of_hbm"] = round(v["weight_GBps"] / peak, 4)

@@ -28,7 +28,7 @@ using namespace dqmoe;
 
 namespace {
 
-bool fmt_ok(int fmt) { return fmt >= DQ_Q4_K && fmt <= DQ_NVFP4; }
+bool fmt_ok(int fmt) { return fmt >= DQ_Q4_K && fmt <= DQ_Q3_K; }
 // formats of the MoE layer's expert matrices
 bool moe_fmt_ok(int fmt) {
   return fmt == DQ_Q4_K || fmt == DQ_Q6_K || fmt == DQ_Q8_0 || fmt == DQ_NVFP4;
@@ -45,6 +45,8 @@ int block_bytes(int fmt) {
     case DQ_Q8_0: return DQ_Q8_0_BYTES;
     case DQ_Q4_0: return DQ_Q4_0_BYTES;
     case DQ_Q5_K: return DQ_Q5_K_BYTES;
+    case DQ_Q2_K: return DQ_Q2_K_BYTES;
+    case DQ_Q3_K: return DQ_Q3_K_BYTES;
     default: return DQ_NVFP4_BYTES;
   }
 }
@@ -57,7 +59,9 @@ int check_qgemv(int fmt, const void* W, int64_t N, int64_t K, const void* x, int
   if (batch < 1 || batch > DQ_MAX_BATCH) return DQ_ERR_ARG;
   // all kernels stream 256-weight super-block units
   if (K % 256) return DQ_ERR_ARG;
-  if (fmt == DQ_Q6_K && K % 2048) return DQ_ERR_ALIGN;   // 210-byte blocks: rows 16-B aligned
+  // rows 16-B aligned: 210- and 110-byte blocks in eights, 84-byte ones in fours
+  if ((fmt == DQ_Q6_K || fmt == DQ_Q3_K) && K % 2048) return DQ_ERR_ALIGN;
+  if (fmt == DQ_Q2_K && K % 1024) return DQ_ERR_ALIGN;
   if (!aligned(W, 16) || !aligned(x, 16) || !aligned(y, 4)) return DQ_ERR_ALIGN;
   if ((int64_t)((N + 63) / 64) > 65535) return DQ_ERR_UNSUPPORTED;
   return DQ_OK;

@@ -25,6 +25,8 @@ template <> struct Fmt<DQ_Q8_0> { static constexpr int SB_BYTES = 272; };
 template <> struct Fmt<DQ_Q4_0> { static constexpr int SB_BYTES = 144; };   // 8 blocks of 18
 template <> struct Fmt<DQ_Q5_K> { static constexpr int SB_BYTES = 176; };
 template <> struct Fmt<DQ_NVFP4> { static constexpr int SB_BYTES = 144; };
+template <> struct Fmt<DQ_Q2_K> { static constexpr int SB_BYTES = 84; };
+template <> struct Fmt<DQ_Q3_K> { static constexpr int SB_BYTES = 110; };
 
 // Hardware FP4/FP8 -> fp16 conversions (exact).  e2m1x8: the 8 E2M1 codes of
 // a word (byte j: codes 2j low nibble, 2j+1 high nibble) as 4 fp16 pairs in

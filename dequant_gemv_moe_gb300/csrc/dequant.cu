@@ -1,11 +1,12 @@
 // dequant.cu — step "block decode" on its own: packed blocks -> fp32.
 //
 // The pages name the formats (Titan Engine §激进量化策略: Q4_K; KTransformers
-// §支持的量化格式: Q4_K_M, Q6_K, Q8_0, Q4_0, Q5_K; NTransformer §量化支持: Q80, Q6K) but
-// print no layout; the GGUF/llama.cpp layouts declared in dqmoe.h are used.
-// Each output is the exact closed form rounded once to fp32: every product
-// below is exact in fp32 and the Q4_K difference is formed by one fused
-// multiply-add, so the result is bit-identical to any exact evaluation.
+// §支持的量化格式: Q4_K_M, Q6_K, Q8_0, Q4_0, Q5_K, Q2_K, Q3_K; NTransformer
+// §量化支持: Q80, Q6K) but print no layout; the GGUF/llama.cpp layouts
+// declared in dqmoe.h are used.  Each output is the exact closed form rounded
+// once to fp32: every product below is exact in fp32 and the Q4_K / Q5_K /
+// Q2_K differences are formed by one fused multiply-add, so the result is
+// bit-identical to any exact evaluation.
 //
 // One thread per output weight (coalesced fp32 stores); the block's few
 // header bytes are re-read by its threads through L1.  This kernel is for
@@ -118,6 +119,45 @@ __global__ void dequant_q5k_kernel(const uint8_t* __restrict__ blocks, int64_t n
   out[gid] = __fmaf_rn(d * (float)sc, (float)q, -(dmin * (float)m));
 }
 
+// Q2_K: weight i = 128h + 32r + l takes bits 2r..2r+1 of qs[32h + l];
+// w = d*sc*q - dmin*m of its 16-weight sub-block (both products exact in
+// fp32, the difference one fused multiply-add).
+__global__ void dequant_q2k_kernel(const uint8_t* __restrict__ blocks, int64_t nblk,
+                                   float* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t blk = gid >> 8;
+  if (blk >= nblk) return;
+  const int i = (int)(gid & 255);
+  const uint8_t* b = blocks + blk * 84;
+  const int h = i >> 7, r = (i >> 5) & 3, l = i & 31;
+  const int q = (b[16 + 32 * h + l] >> (2 * r)) & 3;
+  const int sm = b[i >> 4];
+  out[gid] = __fmaf_rn(h16(b + 80) * (float)(sm & 15), (float)q, -(h16(b + 82) * (float)(sm >> 4)));
+}
+
+// Q3_K: low bits 2r..2r+1 of qs[32h + l], high bit 4h + r of hmask[l]
+// (clear: q = low - 4); w = d*(s - 32)*q with the 6-bit scale s of the
+// 16-weight sub-block.  Every product is exact in fp32.
+__global__ void dequant_q3k_kernel(const uint8_t* __restrict__ blocks, int64_t nblk,
+                                   float* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t blk = gid >> 8;
+  if (blk >= nblk) return;
+  const int i = (int)(gid & 255);
+  const uint8_t* b = blocks + blk * 110;
+  const int h = i >> 7, r = (i >> 5) & 3, l = i & 31;
+  const int low = (b[32 + 32 * h + l] >> (2 * r)) & 3;
+  const int q = low - (((b[l] >> (4 * h + r)) & 1) ? 0 : 4);
+  const int j = i >> 4;
+  const int sc = ((b[96 + (j & 7)] >> (4 * (j >> 3))) & 15) |
+                 (((b[104 + (j & 3)] >> (2 * (j >> 2))) & 3) << 4);
+  out[gid] = h16(b + 108) * (float)(sc - 32) * (float)q;
+}
+
 // NVFP4: w = e2m1(code) * e4m3(scale of the 16-weight block); both
 // conversions by the hardware (exact), the product exact in fp32.  One thread
 // per 8 weights (one code word).
@@ -153,6 +193,8 @@ int launch_dequant(int fmt, const void* blocks, int64_t n, float* out, cudaStrea
   else if (fmt == DQ_Q8_0) launch_pdl(dequant_q80_kernel, dim3((unsigned)grid), dim3(threads), 0, s, 0, b, n / 32, out);
   else if (fmt == DQ_Q4_0) launch_pdl(dequant_q40_kernel, dim3((unsigned)grid), dim3(threads), 0, s, 0, b, n / 32, out);
   else if (fmt == DQ_Q5_K) launch_pdl(dequant_q5k_kernel, dim3((unsigned)grid), dim3(threads), 0, s, 0, b, n / 256, out);
+  else if (fmt == DQ_Q2_K) launch_pdl(dequant_q2k_kernel, dim3((unsigned)grid), dim3(threads), 0, s, 0, b, n / 256, out);
+  else if (fmt == DQ_Q3_K) launch_pdl(dequant_q3k_kernel, dim3((unsigned)grid), dim3(threads), 0, s, 0, b, n / 256, out);
   else launch_pdl(dequant_nvfp4_kernel, dim3((unsigned)((n / 8 + threads - 1) / threads)), dim3(threads), 0, s, 0, b, n / 256, out);
   return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
 }

@@ -131,6 +131,45 @@ __device__ __forceinline__ void lane_weights<DQ_Q5_K>(const uint8_t* b, int l, f
   }
 }
 
+// Q2_K / Q3_K: lane l owns bytes 2(l%16), +1 of qs half h = l/16: weights
+// 128h + 32r + 2(l%16) + {0, 1} for r = 0..3.
+template <>
+__device__ __forceinline__ void lane_weights<DQ_Q2_K>(const uint8_t* b, int l, float (&w)[8],
+                                                      int (&k)[8]) {
+  const float d = h16g(b + 80), dmin = h16g(b + 82);
+  const int h = l >> 4, li = 2 * (l & 15);
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int idx = 128 * h + 32 * r + li + i;
+      const int q = (b[16 + 32 * h + li + i] >> (2 * r)) & 3;
+      const int sm = b[idx >> 4];
+      w[2 * r + i] = __fmaf_rn(d * (float)(sm & 15), (float)q, -(dmin * (float)(sm >> 4)));
+      k[2 * r + i] = idx;
+    }
+}
+
+template <>
+__device__ __forceinline__ void lane_weights<DQ_Q3_K>(const uint8_t* b, int l, float (&w)[8],
+                                                      int (&k)[8]) {
+  const float d = h16g(b + 108);
+  const int h = l >> 4, li = 2 * (l & 15);
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int idx = 128 * h + 32 * r + li + i;
+      const int low = (b[32 + 32 * h + li + i] >> (2 * r)) & 3;
+      const int q = low - (((b[li + i] >> (4 * h + r)) & 1) ? 0 : 4);
+      const int j = idx >> 4;
+      const int sc = ((b[96 + (j & 7)] >> (4 * (j >> 3))) & 15) |
+                     (((b[104 + (j & 3)] >> (2 * (j >> 2))) & 3) << 4);
+      w[2 * r + i] = d * (float)(sc - 32) * (float)q;
+      k[2 * r + i] = idx;
+    }
+}
+
 template <>
 __device__ __forceinline__ void lane_weights<DQ_NVFP4>(const uint8_t* b, int l, float (&w)[8],
                                                        int (&k)[8]) {
@@ -213,6 +252,8 @@ int launch_qgemv_f32(int fmt, const void* W, int64_t N, int64_t K, const float* 
   if (fmt == DQ_Q8_0) return launch_f32_fmt<DQ_Q8_0>(W, N, K, x, batch, y, s);
   if (fmt == DQ_Q4_0) return launch_f32_fmt<DQ_Q4_0>(W, N, K, x, batch, y, s);
   if (fmt == DQ_Q5_K) return launch_f32_fmt<DQ_Q5_K>(W, N, K, x, batch, y, s);
+  if (fmt == DQ_Q2_K) return launch_f32_fmt<DQ_Q2_K>(W, N, K, x, batch, y, s);
+  if (fmt == DQ_Q3_K) return launch_f32_fmt<DQ_Q3_K>(W, N, K, x, batch, y, s);
   return launch_f32_fmt<DQ_NVFP4>(W, N, K, x, batch, y, s);
 }
 

@@ -642,6 +642,10 @@ int launch_qgemv_mma(int fmt, const void* W, int64_t N, int64_t K, const void* x
     return launch_qgemv_mma_fmt<DQ_Q4_0>(W, N, K, x, xdt, batch, y, s, force_ksplit, w_early);
   if (fmt == DQ_Q5_K)
     return launch_qgemv_mma_fmt<DQ_Q5_K>(W, N, K, x, xdt, batch, y, s, force_ksplit, w_early);
+  if (fmt == DQ_Q2_K)
+    return launch_qgemv_mma_fmt<DQ_Q2_K>(W, N, K, x, xdt, batch, y, s, force_ksplit, w_early);
+  if (fmt == DQ_Q3_K)
+    return launch_qgemv_mma_fmt<DQ_Q3_K>(W, N, K, x, xdt, batch, y, s, force_ksplit, w_early);
   return launch_qgemv_mma_fmt<DQ_NVFP4>(W, N, K, x, xdt, batch, y, s, force_ksplit, w_early);
 }
 

@@ -44,11 +44,14 @@ struct Layout {
   static constexpr int SBB = Fmt<FMT>::SB_BYTES;
   // one super-block (256 weights) per row per pipeline stage
   static constexpr int C = 1;
-  // bytes of a row's TMA box per stage: the super-block, for Q6_K a 16-byte
-  // aligned superset of its 210 bytes (starts up to 14 bytes early)
+  // bytes of a row's TMA box per stage: the super-block, for Q6_K / Q2_K /
+  // Q3_K a 16-byte aligned superset of its 210 / 84 / 110 bytes (starts up to
+  // 14 / 12 / 14 bytes early)
   static constexpr int BOX = (FMT == DQ_Q4_K || FMT == DQ_Q4_0 || FMT == DQ_NVFP4) ? 144
                              : (FMT == DQ_Q6_K)                   ? 240
                              : (FMT == DQ_Q5_K)                   ? 176
+                             : (FMT == DQ_Q2_K)                   ? 112
+                             : (FMT == DQ_Q3_K)                   ? 144
                                                                   : 272;
   // TMA writes box rows densely: pitch = BOX; BOX/16 is odd for every format,
   // so rows g and g+1 fall on different bank halves for 16-byte reads
@@ -623,6 +626,219 @@ struct SBDot<DQ_Q4_0> {
       mma_x<NT>(acc, 0, lo[0], lo[1], lo[2], lo[3], xcol, kb + 32 * s + 4 * t);
       mma_x<NT>(acc, 1, hi[0], hi[1], hi[2], hi[3], xcol, kb + 32 * s + 16 + 4 * t);
     }
+  }
+};
+
+// Q2_K / Q3_K: lane t owns the 16 quant bytes 16t..16t+15 of qs, i.e. half
+// hq = t/2 and positions l = 16(t&1) + [0, 16): weights 128hq + 32r + l of
+// the four 2-bit fields r, one 16-weight sub-block (8hq + 2r + (t&1)) per r.
+// Step i reads the lane's quant word w = (i + t) & 3 (bytes 4w..4w+3 of its
+// 16): with row pitches of an odd number of 16-byte units the 32 lanes of
+// each 4-byte load then fall on 32 distinct banks.  The k order inside an mma
+// is free, so each step's B fragment is read at the activations of its word.
+//
+// Decode: field r of each byte is masked in place (value q 4^r), the bytes
+// are spread to 16-bit lanes and read as exact fp16 subnormals q 4^r 2^-24,
+// and one HFMA2 with S/4^r and O yields the weight times a power of two per
+// row (undone in fp32 after the super-block, as Q4_K).
+
+// B fragments of one step at byte offset `off` from the lane's base xb.
+template <int NT>
+__device__ __forceinline__ void mma_xb(float (&acc)[NT][2][4], int ch, uint32_t a0, uint32_t a1,
+                                       uint32_t a2, uint32_t a3, const uint32_t (&xb)[NT],
+                                       int off) {
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const uint2 b = lds_u64_nv(xb[nt] + off);
+    mma_16816_nv(acc[nt][ch], a0, a1, a2, a3, b.x, b.y);
+  }
+}
+
+// Byte offset of field r's activations from those of field 0 of a word: the
+// word's positions sit below 32 inside their 64-activation group, so field r
+// is 32r further on and crosses r/2 group paddings of 8 halves.
+__device__ __forceinline__ constexpr int field_xoff(int r) { return 2 * (32 * r + 8 * (r >> 1)); }
+
+template <>
+struct SBDot<DQ_Q2_K> {
+  static constexpr bool kRowScale = true;
+
+  // S[r] = d sc F / 4^r and O[r] = -dmin m F 2^-24 of the lane's sub-block of
+  // field r (as broadcast pairs), F = 2^(26 - e) for e the larger exponent
+  // field of d and dmin: d F < 4096 and sc <= 15 keep S < 61440; rinv = 2^(e-2)
+  // undoes F 2^-24.  S is rounded once to fp16, O once from fp32.
+  __device__ __forceinline__ static void scales(uint32_t rb, int t, __half2 (&S)[4],
+                                                __half2 (&O)[4], float& rinv) {
+    const uint32_t dd = lds_u32_nv(rb + 80);   // d | dmin << 16
+    const uint32_t w0 = lds_u32_nv(rb + 8 * (t >> 1)), w1 = lds_u32_nv(rb + 8 * (t >> 1) + 4);
+    // scale bytes 8hq + 2r + (t&1): (r = 0, 1) from w0, (2, 3) from w1
+    const uint32_t tt = (uint32_t)(t & 1);
+    const uint32_t sel = tt | (4u << 4) | ((tt + 2u) << 8) | (4u << 12);
+    const uint32_t p0 = __byte_perm(w0, 0, sel), p1 = __byte_perm(w1, 0, sel);
+    const __half2 magic = u32_as_h2(0x64006400u);
+    const __half2 sc01 = __hsub2(u32_as_h2(lop3_and_or(p0, 0x000F000Fu, 0x64006400u)), magic);
+    const __half2 sc23 = __hsub2(u32_as_h2(lop3_and_or(p1, 0x000F000Fu, 0x64006400u)), magic);
+    const float2 m01 =
+        __half22float2(__hsub2(u32_as_h2(lop3_and_or(p0 >> 4, 0x000F000Fu, 0x64006400u)), magic));
+    const float2 m23 =
+        __half22float2(__hsub2(u32_as_h2(lop3_and_or(p1 >> 4, 0x000F000Fu, 0x64006400u)), magic));
+    const uint32_t e = max(dd & 0x7C00u, (dd >> 16) & 0x7C00u) >> 10;
+    const float F = __uint_as_float((153u - e) << 23);    // 2^(26 - e)
+    const float Fm = __uint_as_float((129u - e) << 23);   // 2^(2 - e) = F 2^-24
+    rinv = __uint_as_float((125u + e) << 23);             // 2^(e - 2)
+    const float df = __half2float(__ushort_as_half((unsigned short)(dd & 0xFFFF))) * F;
+    const float dm = -__half2float(__ushort_as_half((unsigned short)(dd >> 16))) * Fm;
+    const __half2 s01 = __hmul2(sc01, __floats2half2_rn(df, df * 0.25f));
+    const __half2 s23 = __hmul2(sc23, __floats2half2_rn(df * 0.0625f, df * 0.015625f));
+    const __half2 o01 = __floats2half2_rn(m01.x * dm, m01.y * dm);
+    const __half2 o23 = __floats2half2_rn(m23.x * dm, m23.y * dm);
+    S[0] = __low2half2(s01);
+    S[1] = __high2half2(s01);
+    S[2] = __low2half2(s23);
+    S[3] = __high2half2(s23);
+    O[0] = __low2half2(o01);
+    O[1] = __high2half2(o01);
+    O[2] = __low2half2(o23);
+    O[3] = __high2half2(o23);
+  }
+
+  template <int NT, bool PAIRX = false>
+  __device__ __forceinline__ static void run(uint32_t wrow, int pitch8,
+                                             const uint32_t (&xcol)[NT], int kb, int t,
+                                             float (&acc)[NT][2][4], float& r0, float& r8) {
+    __half2 S0[4], O0[4], S8[4], O8[4];
+    scales(wrow, t, S0, O0, r0);
+    scales(wrow + pitch8, t, S8, O8, r8);
+    const int kl = kb + 128 * (t >> 1) + 16 * (t & 1);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int w = (i + t) & 3;
+      const uint32_t qa = wrow + 16 + 16 * t + 4 * w;
+      const uint32_t q0 = lds_u32_nv(qa), q8 = lds_u32_nv(qa + pitch8);
+      // bytes (0, 1) and (2, 3) of each word in 16-bit lanes: weights (k, k+1), (k+2, k+3)
+      const uint32_t l0 = __byte_perm(q0, 0, 0x4140), h0 = __byte_perm(q0, 0, 0x4342);
+      const uint32_t l8 = __byte_perm(q8, 0, 0x4140), h8 = __byte_perm(q8, 0, 0x4342);
+      uint32_t xb[NT];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) xb[nt] = xcol[nt] + 2 * xoff(kl + 4 * w);
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const uint32_t m = 0x00030003u << (2 * r);
+        const uint32_t a0 = h2_as_u32(__hfma2(u32_as_h2(l0 & m), S0[r], O0[r]));
+        const uint32_t a1 = h2_as_u32(__hfma2(u32_as_h2(l8 & m), S8[r], O8[r]));
+        const uint32_t a2 = h2_as_u32(__hfma2(u32_as_h2(h0 & m), S0[r], O0[r]));
+        const uint32_t a3 = h2_as_u32(__hfma2(u32_as_h2(h8 & m), S8[r], O8[r]));
+        mma_xb<NT>(acc, r & 1, a0, a1, a2, a3, xb, field_xoff(r));
+      }
+    }
+  }
+};
+
+// Q3_K: Q2_K's quant placement plus the high bit of each weight from hmask[l]
+// (bit 4hq + r) and one signed 6-bit scale per sub-block.  With u = low + 4 *
+// high = q + 4 in 0..7, w = d (s - 32) (u - 4).  Per word and field the bytes
+// are assembled as u 2^b_r (b_r = 0, 2, 4, 5: the field's own position, and
+// for r = 3 one lower so that the high bit still fits the byte), then spread
+// and decoded as Q2_K's with S/2^b_r and O = -4 S 2^-24.  Blocks are 110
+// bytes, so every other one starts 2 bytes off a 4-byte boundary: each word
+// is then read as two aligned words and a funnel shift (MIS2).
+template <>
+struct SBDot<DQ_Q3_K> {
+  static constexpr bool kRowScale = true;
+
+  template <bool MIS2>
+  __device__ __forceinline__ static uint32_t ld(uint32_t a) {
+    if constexpr (MIS2) return __funnelshift_r(lds_u32_nv(a - 2), lds_u32_nv(a + 2), 16);
+    else return lds_u32_nv(a);
+  }
+
+  // S[r] = d F (s - 32) / 2^b_r, O[r] = -4 d F (s - 32) 2^-24 of the lane's
+  // sub-block of field r, F = 2^(25 - e) for e the exponent field of d:
+  // d F < 2048 and |s - 32| <= 32 keep |S| <= 65504; rinv = 2^(e - 1).
+  template <bool MIS2>
+  __device__ __forceinline__ static void scales(uint32_t rb, int t, __half2 (&S)[4],
+                                                __half2 (&O)[4], float& rinv) {
+    const uint32_t dh = lds_u16_nv(rb + 108);
+    const uint32_t s0 = ld<MIS2>(rb + 96), s1 = ld<MIS2>(rb + 100), s2 = ld<MIS2>(rb + 104);
+    const uint32_t tt = (uint32_t)(t & 1), sh = 4u * (uint32_t)(t >> 1);
+    const uint32_t sel = tt | (4u << 4) | ((tt + 2u) << 8) | (4u << 12);
+    // sub-block j = 8hq + 2r + tt: low four bits = nibble hq of scale byte
+    // 2r + tt (r = 0, 1 in s0, 2, 3 in s1); high two = field 2hq + r/2 of
+    // byte 8 + tt (r even) or 10 + tt (r odd), bytes tt, tt + 2 of s2
+    const uint32_t lo01 = __byte_perm(s0, 0, sel) >> sh, lo23 = __byte_perm(s1, 0, sel) >> sh;
+    const uint32_t hb = __byte_perm(s2, 0, sel) >> sh;
+    const uint32_t v01 =
+        lop3_and_or(hb << 4, 0x00300030u, lop3_and_or(lo01, 0x000F000Fu, 0x64006400u));
+    const uint32_t v23 =
+        lop3_and_or(hb << 2, 0x00300030u, lop3_and_or(lo23, 0x000F000Fu, 0x64006400u));
+    const __half2 bias = u32_as_h2(0x64206420u);   // 1024 + 32: s - 32, exact
+    const __half2 c01 = __hsub2(u32_as_h2(v01), bias), c23 = __hsub2(u32_as_h2(v23), bias);
+    const uint32_t e = (dh >> 10) & 31u;
+    const float F = __uint_as_float((152u - e) << 23);   // 2^(25 - e)
+    rinv = __uint_as_float((126u + e) << 23);            // 2^(e - 1)
+    const float df = __half2float(__ushort_as_half((unsigned short)dh)) * F;
+    const __half2 s01 = __hmul2(c01, __floats2half2_rn(df, df * 0.25f));
+    const __half2 s23 = __hmul2(c23, __floats2half2_rn(df * 0.0625f, df * 0.03125f));
+    // -4 S 2^-24 = -(S / 2^b_r) 2^(b_r - 22): exact power-of-two products
+    const __half2 o01 = __hmul2(s01, __floats2half2_rn(-0x1p-22f, -0x1p-20f));
+    const __half2 o23 = __hmul2(s23, __floats2half2_rn(-0x1p-18f, -0x1p-17f));
+    S[0] = __low2half2(s01);
+    S[1] = __high2half2(s01);
+    S[2] = __low2half2(s23);
+    S[3] = __high2half2(s23);
+    O[0] = __low2half2(o01);
+    O[1] = __high2half2(o01);
+    O[2] = __low2half2(o23);
+    O[3] = __high2half2(o23);
+  }
+
+  // u 2^b_r in each byte of a word, from its quant byte q and its hmask byte
+  // h already shifted down by 4hq (bit r = this half's high bit of field r)
+  __device__ __forceinline__ static uint32_t ubytes(uint32_t q, uint32_t h, int r) {
+    if (r < 3)
+      return lop3_and_or(h << (r + 2), 0x04040404u << (2 * r), q & (0x03030303u << (2 * r)));
+    return lop3_and_or(h << 4, 0x80808080u, (q >> 1) & 0x60606060u);
+  }
+
+  template <int NT, bool MIS2>
+  __device__ __forceinline__ static void run_impl(uint32_t wrow, int pitch8,
+                                                  const uint32_t (&xcol)[NT], int kb, int t,
+                                                  float (&acc)[NT][2][4], float& r0, float& r8) {
+    __half2 S0[4], O0[4], S8[4], O8[4];
+    scales<MIS2>(wrow, t, S0, O0, r0);
+    scales<MIS2>(wrow + pitch8, t, S8, O8, r8);
+    const uint32_t sh = 4u * (uint32_t)(t >> 1);
+    const int kl = kb + 128 * (t >> 1) + 16 * (t & 1);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int w = (i + t) & 3;
+      const uint32_t qa = wrow + 32 + 16 * t + 4 * w;      // qs[32hq + 16(t&1) + 4w]
+      const uint32_t ha = wrow + 16 * (t & 1) + 4 * w;     // hmask[16(t&1) + 4w]
+      const uint32_t q0 = ld<MIS2>(qa), q8 = ld<MIS2>(qa + pitch8);
+      const uint32_t e0 = ld<MIS2>(ha) >> sh, e8 = ld<MIS2>(ha + pitch8) >> sh;
+      uint32_t xb[NT];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) xb[nt] = xcol[nt] + 2 * xoff(kl + 4 * w);
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const uint32_t u0 = ubytes(q0, e0, r), u8 = ubytes(q8, e8, r);
+        const __half2 s0 = S0[r], o0 = O0[r], s8 = S8[r], o8 = O8[r];
+        const uint32_t a0 = h2_as_u32(__hfma2(u32_as_h2(__byte_perm(u0, 0, 0x4140)), s0, o0));
+        const uint32_t a1 = h2_as_u32(__hfma2(u32_as_h2(__byte_perm(u8, 0, 0x4140)), s8, o8));
+        const uint32_t a2 = h2_as_u32(__hfma2(u32_as_h2(__byte_perm(u0, 0, 0x4342)), s0, o0));
+        const uint32_t a3 = h2_as_u32(__hfma2(u32_as_h2(__byte_perm(u8, 0, 0x4342)), s8, o8));
+        mma_xb<NT>(acc, r & 1, a0, a1, a2, a3, xb, field_xoff(r));
+      }
+    }
+  }
+
+  template <int NT, bool PAIRX = false>
+  __device__ __forceinline__ static void run(uint32_t wrow, int pitch8,
+                                             const uint32_t (&xcol)[NT], int kb, int t,
+                                             float (&acc)[NT][2][4], float& r0, float& r8) {
+    // the block offset is the same for every row of a stage: a uniform branch
+    if (wrow & 2u) run_impl<NT, true>(wrow, pitch8, xcol, kb, t, acc, r0, r8);
+    else run_impl<NT, false>(wrow, pitch8, xcol, kb, t, acc, r0, r8);
   }
 };
 

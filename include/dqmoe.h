@@ -40,8 +40,8 @@
  *     of that row, consecutive, starting at byte n * row_bytes where
  *     row_bytes = (K/QK) * block_bytes.  Rows are consecutive.  W must be
  *     16-byte aligned and row_bytes a multiple of 16 (true for every shape
- *     with K a multiple of 256 for Q4_K, Q8_0, Q4_0, Q5_K and NVFP4, of 2048
- *     for Q6_K).
+ *     with K a multiple of 256 for Q4_K, Q8_0, Q4_0, Q5_K and NVFP4, of 1024
+ *     for Q2_K, of 2048 for Q6_K and Q3_K).
  *   - Activations x: [batch][K] row-major in x_dtype.  Outputs y: [batch][N]
  *     row-major, always fp32 (MoE activations reach ~1e7, beyond fp16).
  */
@@ -89,6 +89,22 @@ extern "C" {
 /*   w = d*sc_j*q - dmin*m_j as Q4_K.  Both are the other GGUF blocks the   */
 /*   [KTransformers, §支持的量化格式] list names beside Q4_K, Q6_K, Q8_0;    */
 /*   dq_dequant and dq_qgemv take them, the MoE layer does not.             */
+/* Q2_K super-block, 256 weights in 84 bytes:                               */
+/*   bytes 0-15  scales[16]: low nibble = scale sc_j, high nibble = min m_j */
+/*               of the sixteen 16-weight sub-blocks j                      */
+/*   bytes 16-79 qs[64] of 2-bit quants, bytes 80-81 fp16 d, 82-83 fp16 dmin */
+/*   weight 128h+32r+l (h = 0,1; r = 0..3; l = 0..31): bits 2r..2r+1 of     */
+/*   qs[32h+l]; sub-block j = weight/16; w = d*sc_j*q - dmin*m_j, q in 0..3. */
+/* Q3_K super-block, 256 weights in 110 bytes:                              */
+/*   bytes 0-31 hmask[32], 32-95 qs[64] (2-bit low quants as Q2_K's),       */
+/*   96-107 twelve bytes of sixteen 6-bit scales, 108-109 fp16 d.           */
+/*   weight 128h+32r+l: low = bits 2r..2r+1 of qs[32h+l], high bit = bit    */
+/*   4h+r of hmask[l]; q = low - 4 when the high bit is clear, else low     */
+/*   (q in -4..3).  Scale j: bits 0-3 = nibble j/8 of byte j%8, bits 4-5 =  */
+/*   bits 2(j/4)..2(j/4)+1 of byte 8 + j%4; w = d*(s_j - 32)*q.  Q2_K and   */
+/*   Q3_K are the low-bit blocks of the [KTransformers, §支持的量化格式] list  */
+/*   (Q2_K_L, Q2_K_XS, Q3_K_M mixes); dq_dequant and dq_qgemv take them, the */
+/*   MoE layer does not.                                                    */
 /* NVFP4 super-block, 256 weights in 144 bytes (the pages name NVIDIA's FP4 */
 /*   as Blackwell's native 4-bit float, [Titan Engine, §激进量化策略], and    */
 /*   print no layout; this is the library's):                               */
@@ -100,7 +116,7 @@ extern "C" {
 /*   bytes are out of contract.  dq_dequant, dq_qgemv and MoE experts.      */
 /* ------------------------------------------------------------------------ */
 typedef enum { DQ_Q4_K = 1, DQ_Q6_K = 2, DQ_Q8_0 = 3, DQ_Q4_0 = 4, DQ_Q5_K = 5,
-               DQ_NVFP4 = 6 } dq_fmt;
+               DQ_NVFP4 = 6, DQ_Q2_K = 7, DQ_Q3_K = 8 } dq_fmt;
 
 /* Activation element types accepted by the entry points. */
 typedef enum { DQ_F32 = 0, DQ_F16 = 1, DQ_BF16 = 2 } dq_dtype;
@@ -124,6 +140,8 @@ typedef enum {
 #define DQ_Q4_0_BYTES 18
 #define DQ_Q5_K_BYTES 176
 #define DQ_NVFP4_BYTES 144  /* per 256-weight super-block */
+#define DQ_Q2_K_BYTES 84
+#define DQ_Q3_K_BYTES 110
 #define DQ_MAX_BATCH 8      /* activation columns per dq_qgemv call */
 
 /* Weights per block and bytes per block of `fmt`.  Host-only, no CUDA.
@@ -134,9 +152,8 @@ int dq_block_geometry(int fmt, int* weights_per_block, int* bytes_per_block);
  * `fmt` into fp32.  Step "block decode" of the path; exposed so the decoded
  * values can be compared bit for bit (every closed form above is exact in
  * fp32 up to the final rounding of the Q4_K subtraction).
- *   blocks : device, n_weights/QK consecutive blocks, 16-byte aligned for
- *            Q4_K and Q5_K; 2-byte aligned for Q6_K/Q8_0/Q4_0 (their blocks
- *            are 210/34/18 B).
+ *   blocks : device, n_weights/QK consecutive blocks, 2-byte aligned (the
+ *            Q6_K/Q8_0/Q4_0/Q3_K blocks are 210/34/18/110 B).
  *   out    : device fp32 [n_weights], 4-byte aligned.
  * Errors: DQ_ERR_ARG (null, n_weights <= 0 or not a multiple of QK),
  *         DQ_ERR_ALIGN, DQ_ERR_CUDA. */
@@ -156,8 +173,9 @@ int dq_dequant(int fmt, const void* blocks, int64_t n_weights, float* out,
  * products in fp32).
  * Errors: DQ_ERR_ARG (null, N/K <= 0, K % 256 != 0 — every format is
  *         streamed in 256-weight units —, batch outside 1..8),
- *         DQ_ERR_ALIGN (W, x not 16-B aligned, y not 4-B aligned; Q6_K needs
- *         K % 2048 == 0 so that its 210-byte-block rows stay 16-B aligned),
+ *         DQ_ERR_ALIGN (W, x not 16-B aligned, y not 4-B aligned; rows must
+ *         stay 16-B aligned: Q2_K needs K % 1024 == 0 (84-byte blocks), Q6_K
+ *         and Q3_K K % 2048 == 0 (210- and 110-byte blocks)),
  *         DQ_ERR_UNSUPPORTED (N > 65535*64), DQ_ERR_CUDA. */
 int dq_qgemv(int fmt, const void* W, int64_t N, int64_t K, const void* x,
              int x_dtype, int batch, float* y, void* stream);

@@ -53,6 +53,8 @@ def test_qgemv_argument_errors_without_launch(so):
     assert f(1, a, 64, 256, a, 7, 1, a, None) == -1            # bad dtype
     assert f(1, P(4097), 64, 256, a, 1, 1, a, None) == -2      # misaligned W
     assert f(2, a, 64, 1024, a, 1, 1, a, None) == -2           # Q6_K needs K % 2048
+    assert f(7, a, 64, 512, a, 1, 1, a, None) == -2            # Q2_K needs K % 1024
+    assert f(8, a, 64, 1024, a, 1, 1, a, None) == -2           # Q3_K needs K % 2048
     assert f(1, a, 0, 256, a, 1, 1, a, None) == -1             # N = 0
 
 
@@ -80,12 +82,12 @@ def test_dequant_argument_errors(so):
 def test_block_geometry_all_formats(so):
     f = so.dq_block_geometry
     qk, nb = ctypes.c_int(), ctypes.c_int()
-    # Q4_K, Q6_K, Q8_0, Q4_0, Q5_K: the GGUF block sizes
+    # Q4_K, Q6_K, Q8_0, Q4_0, Q5_K, NVFP4, Q2_K, Q3_K: the block sizes
     for fmt, want in [(1, (256, 144)), (2, (256, 210)), (3, (32, 34)), (4, (32, 18)),
-                      (5, (256, 176)), (6, (256, 144))]:
+                      (5, (256, 176)), (6, (256, 144)), (7, (256, 84)), (8, (256, 110))]:
         assert f(fmt, ctypes.byref(qk), ctypes.byref(nb)) == 0
         assert (qk.value, nb.value) == want
-    assert f(7, ctypes.byref(qk), ctypes.byref(nb)) == -1
+    assert f(9, ctypes.byref(qk), ctypes.byref(nb)) == -1
     assert f(0, ctypes.byref(qk), ctypes.byref(nb)) == -1
 
 
@@ -103,7 +105,7 @@ def test_moe_rejects_gemv_only_formats(so):
     n = ctypes.c_size_t()
     f = so.dq_moe_workspace_size
     f.argtypes = [ctypes.POINTER(Desc), ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]
-    for fmt, rc in [(1, 0), (6, 0), (4, -3), (5, -3)]:
+    for fmt, rc in [(1, 0), (6, 0), (4, -3), (5, -3), (7, -3), (8, -3), (9, -1)]:
         d = Desc(8, 2, 512, 512, 0, fmt, a, a, a, a, None, None, None)
         assert f(ctypes.byref(d), 4, ctypes.byref(n)) == rc, fmt
 

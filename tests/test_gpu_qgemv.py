@@ -13,7 +13,7 @@ from gpu_util import TOL, dev_act, dev_bytes, rel_err
 
 pytestmark = pytest.mark.gpu
 
-Q4_K, Q6_K, Q8_0, Q4_0, Q5_K, NVFP4 = 1, 2, 3, 4, 5, 6
+Q4_K, Q6_K, Q8_0, Q4_0, Q5_K, NVFP4, Q2_K, Q3_K = 1, 2, 3, 4, 5, 6, 7, 8
 
 
 @pytest.fixture(scope="module")
@@ -24,7 +24,7 @@ def dq():
 
 
 @pytest.mark.parametrize("fmt,qk", [(Q4_K, 256), (Q6_K, 256), (Q8_0, 32), (Q4_0, 32),
-                                    (Q5_K, 256), (NVFP4, 256)])
+                                    (Q5_K, 256), (NVFP4, 256), (Q2_K, 256), (Q3_K, 256)])
 def test_dequant_bit_exact_random(dq, orc, fmt, qk):
     g = synth.streams(31 + fmt, 1)[0]
     raw = synth.quant_matrix(g, fmt, 37, 4096)
@@ -36,7 +36,9 @@ def test_dequant_bit_exact_random(dq, orc, fmt, qk):
 
 @pytest.mark.parametrize("fname,fmt,qk", [("q4_k_blocks.txt", Q4_K, 256),
                                           ("q6_k_blocks.txt", Q6_K, 256),
-                                          ("q8_0_blocks.txt", Q8_0, 32)])
+                                          ("q8_0_blocks.txt", Q8_0, 32),
+                                          ("q2_k_blocks.txt", Q2_K, 256),
+                                          ("q3_k_blocks.txt", Q3_K, 256)])
 def test_dequant_golden(dq, fname, fmt, qk):
     for c in read_block_cases(fname):
         got = dq.dequant(fmt, dev_bytes(c["bytes"]), qk).cpu().numpy().astype(np.float64)
@@ -64,7 +66,7 @@ def _case(dq, orc, fmt, N, K, B, xdt, seed, ksplit=None, rows=None, xscale=1.0):
     return rel_err(got, ref)
 
 
-@pytest.mark.parametrize("fmt", [Q4_K, Q6_K, Q8_0, Q4_0, Q5_K, NVFP4])
+@pytest.mark.parametrize("fmt", [Q4_K, Q6_K, Q8_0, Q4_0, Q5_K, NVFP4, Q2_K, Q3_K])
 @pytest.mark.parametrize("xdt", [0, 1, 2])
 @pytest.mark.parametrize("B", [1, 3, 8])
 def test_qgemv_small_ragged(dq, orc, fmt, xdt, B):
@@ -74,7 +76,7 @@ def test_qgemv_small_ragged(dq, orc, fmt, xdt, B):
     assert err <= TOL[xdt], err
 
 
-@pytest.mark.parametrize("fmt", [Q4_K, Q6_K, Q8_0, Q4_0, Q5_K, NVFP4])
+@pytest.mark.parametrize("fmt", [Q4_K, Q6_K, Q8_0, Q4_0, Q5_K, NVFP4, Q2_K, Q3_K])
 @pytest.mark.parametrize("ks", [1, 2, 3, 5, 8])
 def test_qgemv_cluster_ksplit(dq, orc, fmt, ks):
     N, K = 130, 8192
@@ -85,7 +87,8 @@ def test_qgemv_cluster_ksplit(dq, orc, fmt, ks):
 def test_qgemv_edge_shapes(dq, orc):
     # one row, one super-block, odd batch; Q6_K needs K % 2048 == 0
     for fmt, N, K in [(Q4_K, 1, 256), (Q8_0, 1, 256), (Q6_K, 1, 2048), (Q4_K, 65, 256),
-                      (Q8_0, 63, 512)]:
+                      (Q8_0, 63, 512), (Q2_K, 1, 1024), (Q3_K, 1, 2048), (Q2_K, 65, 1024),
+                      (Q3_K, 63, 2048)]:
         for xdt in (0, 1, 2):
             for B in (5, 1):
                 err = _case(dq, orc, fmt, N, K, B, xdt, seed=N + K + xdt + B)
@@ -295,8 +298,8 @@ def test_qgemv_weights_early_and_chains(dq, orc):
         assert rel_err(y3.cpu().numpy(), orc.qgemv(Q8_0, W3, N2, N1, x3h, 1, 2)) <= TOL[1]
 
 
-# ---------------------------------------------------------- Q4_0 and Q5_K
-@pytest.mark.parametrize("fmt", [Q4_0, Q5_K, NVFP4])
+# ------------------------------------------- Q4_0, Q5_K, NVFP4, Q2_K, Q3_K
+@pytest.mark.parametrize("fmt", [Q4_0, Q5_K, NVFP4, Q2_K, Q3_K])
 @pytest.mark.parametrize("B", [1, 8])
 def test_gemv_only_formats_70b_shape(dq, orc, fmt, B):
     # the 70B gate shape in the two qGEMV-only formats, sampled rows
@@ -339,3 +342,61 @@ def test_nvfp4_every_code_and_scale_on_gpu(dq, orc):
     got = dq.dequant(NVFP4, dev_bytes(raw), nsb * 256).cpu().numpy()
     ref = orc.dequant(NVFP4, raw, nsb * 256)
     assert got.view(np.uint32).tolist() == ref.view(np.uint32).tolist()
+
+
+def test_q3k_high_bits_matter_on_gpu(dq, orc):
+    # the same bytes with every hmask bit set and cleared differ, and each
+    # matches the oracle: the GPU decode reads the high bits
+    g = synth.streams(9300, 2)
+    N, K = 128, 4096
+    W = synth.quant_matrix(g[0], Q3_K, N, K)
+    Ws = []
+    for v in (0x00, 0xFF):
+        Wv = W.reshape(-1, 110).copy()
+        Wv[:, 0:32] = v
+        Ws.append(Wv.reshape(-1))
+    x = synth.activations(g[1], (3, K), 1)
+    ys = [dq.qgemv(Q3_K, dev_bytes(w), N, K, dev_act(x, 1)).cpu().numpy() for w in Ws]
+    refs = [orc.qgemv(Q3_K, w, N, K, x, 1, 3) for w in Ws]
+    for y, r in zip(ys, refs):
+        assert rel_err(y, r) <= TOL[1]
+    assert rel_err(ys[0], refs[1]) > 10 * TOL[1]
+
+
+def _set_fp16(W, nb, off, vals_per_row, N):
+    """Overwrite the fp16 field at byte `off` of every block of row r with vals_per_row[r]."""
+    blocks = W.reshape(N, -1, nb)
+    blocks[:, :, off:off + 2] = np.asarray(vals_per_row, dtype=np.float16).view(np.uint8).reshape(N, 1, 2)
+    return blocks.reshape(-1)
+
+
+@pytest.mark.parametrize("fmt", [Q2_K, Q3_K])
+@pytest.mark.parametrize("xdt", [1, 2])
+def test_low_bit_scale_regimes(dq, orc, fmt, xdt):
+    # rows whose super-block scales span the fp16 range (largest normal,
+    # 1, 2^-14, subnormal, zero) and, for Q2_K, dmin far above or below d:
+    # the per-row power-of-two folding must keep every row within tolerance
+    # of its own magnitude
+    N, K = 128, 4096
+    g = synth.streams(9400 + fmt * 10 + xdt, 2)
+    W = synth.quant_matrix(g[0], fmt, N, K)
+    regimes = [60000.0, 1.0, 2.0 ** -14, 2.0 ** -20, 0.0, 0.01, 3.5e-3, 1000.0]
+    d = np.array([regimes[r % len(regimes)] for r in range(N)])
+    if fmt == Q2_K:
+        W = _set_fp16(W, 84, 80, d, N)
+        dmin = np.array([[0.01, 1.0, 2.0 ** -20, 0.0][r % 4] for r in range(N)])
+        W = _set_fp16(W, 84, 82, dmin, N)
+    else:
+        W = _set_fp16(W, 110, 108, d, N)
+    x = synth.activations(g[1], (2, K), xdt)
+    y = dq.qgemv(fmt, dev_bytes(W), N, K, dev_act(x, xdt)).cpu().numpy()
+    assert dq.device_status() == 0
+    ref = orc.qgemv(fmt, W, N, K, x, xdt, 2)
+    assert np.isfinite(y).all()
+    for r in range(N):
+        scale = np.abs(ref[:, r]).max()
+        if scale == 0:
+            assert np.all(y[:, r] == 0), r
+            continue
+        err = np.abs(y[:, r] - ref[:, r]).max() / scale
+        assert err <= 4 * TOL[xdt], (r, d[r], err)
