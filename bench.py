@@ -444,34 +444,45 @@ def bench_layer(torch, dq, args, lin, with_e2e=True):
     return res
 
 
-def bench_gemv_70b(torch, dq, reps=50):
-    """North-star shape: batch-1 Q4_K 28672 x 8192 gate GEMV, 4 rotating copies."""
-    g = synth.streams(synth.BASE_SEED + 2, 2)
-    N, K = 28672, 8192
-    Ws = [torch.from_numpy(synth.quant_matrix(g[0], Q4_K, N, K)).cuda() for _ in range(ROTATE)]
-    x = torch.from_numpy(synth.activations(g[1], (1, K), 1)).cuda()
-    y = torch.empty(1, N, dtype=torch.float32, device="cuda")
-    for r in range(ROTATE):
-        dq.qgemv(Q4_K, Ws[r], N, K, x, y=y)
+def time_gemv(torch, dq, fmt, Ws, N, K, x, y, reps=30):
+    """Device time of one dq_qgemv launch, two ways, over the weight copies Ws
+    (together larger than L2):
+      isolated: each launch in its own CUDA graph between two events, the
+        graphs replayed one after another (no host gap inside the interval,
+        no overlap with a previous GEMV);
+      back to back: graphs of 8 launches over the copies, weights streamed
+        early, as a decode loop runs consecutive GEMVs (total / launches)."""
+    for W in Ws:
+        dq.qgemv(fmt, W, N, K, x, y=y)
     torch.cuda.synchronize()
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * reps)]
-    for i in range(reps):
-        evs[2 * i].record()
-        dq.qgemv(Q4_K, Ws[i % ROTATE], N, K, x, y=y)
-        evs[2 * i + 1].record()
-    torch.cuda.synchronize()
-    t = [evs[2 * i].elapsed_time(evs[2 * i + 1]) for i in range(reps)]
-    wb = weight_bytes(Q4_K, N, K)
-    us = float(np.median(t)) * 1e3
-    # back to back, as a decode loop runs consecutive GEMVs: one graph of 8
-    # launches over the rotating copies, weights streamed early
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
+    iso = None
+    if make_event(torch, True) is not None:
+        graphs, evs = [], []
+        with torch.cuda.stream(s):
+            for i in range(reps):
+                e = (make_event(torch, True), make_event(torch, True))
+                gr = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gr, stream=s):
+                    e[0].record()
+                    dq.qgemv(fmt, Ws[i % len(Ws)], N, K, x, y=y)
+                    e[1].record()
+                graphs.append(gr)
+                evs.append(e)
+        torch.cuda.current_stream().wait_stream(s)
+        for gr in graphs[:3]:
+            gr.replay()
+        for gr in graphs:
+            gr.replay()
+        torch.cuda.synchronize()
+        iso = [a.elapsed_time(b) * 1e3 for a, b in evs]
+        del graphs
     with torch.cuda.stream(s):
         gr = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gr, stream=s):
             for i in range(8):
-                dq.qgemv(Q4_K, Ws[i % ROTATE], N, K, x, y=y, weights_early=True)
+                dq.qgemv(fmt, Ws[i % len(Ws)], N, K, x, y=y, weights_early=True)
     torch.cuda.current_stream().wait_stream(s)
     for _ in range(3):
         gr.replay()
@@ -482,46 +493,59 @@ def bench_gemv_70b(torch, dq, reps=50):
         gr.replay()
     e1.record()
     torch.cuda.synchronize()
-    us_b2b = e0.elapsed_time(e1) * 1e3 / 160
-    del gr, Ws
+    b2b = e0.elapsed_time(e1) * 1e3 / 160
+    del gr
+    return iso, b2b
+
+
+def weight_copies(torch, W0, wb):
+    """W0 plus clones: at least ROTATE copies and at least 300 MB in all (> 2x L2)."""
+    n = max(ROTATE, -(-300_000_000 // wb))
+    return [W0] + [W0.clone() for _ in range(n - 1)]
+
+
+def bench_gemv_70b(torch, dq, reps=50):
+    """North-star shape: batch-1 Q4_K 28672 x 8192 gate GEMV, 4 rotating copies."""
+    g = synth.streams(synth.BASE_SEED + 2, 2)
+    N, K = 28672, 8192
+    wb = weight_bytes(Q4_K, N, K)
+    Ws = weight_copies(torch, torch.from_numpy(synth.quant_matrix(g[0], Q4_K, N, K)).cuda(), wb)
+    x = torch.from_numpy(synth.activations(g[1], (1, K), 1)).cuda()
+    y = torch.empty(1, N, dtype=torch.float32, device="cuda")
+    t, us_b2b = time_gemv(torch, dq, Q4_K, Ws, N, K, x, y, reps=reps)
+    del Ws
     torch.cuda.empty_cache()
+    us = float(np.median(t))
     return {"shape": "28672x8192 Q4_K batch 1 fp16", "us_median": us,
-            "us_p10": float(np.percentile(t, 10)) * 1e3, "us_p90": float(np.percentile(t, 90)) * 1e3,
+            "us_p10": float(np.percentile(t, 10)), "us_p90": float(np.percentile(t, 90)),
             "weight_GBps": wb / (us / 1e6) / 1e9, "bytes": wb + K * 2 + N * 4,
             "us_back_to_back": us_b2b, "weight_GBps_back_to_back": wb / (us_b2b / 1e6) / 1e9,
-            "note": "us_median: one launch between two events; back_to_back: 160 launches "
-                    "in graphs of 8 (4 rotating weight copies, 528 MB > L2)"}
+            "note": "us_median: each launch in its own graph between two events (no host "
+                    "gap, no overlap with a previous GEMV); back_to_back: 160 launches in "
+                    "graphs of 8 (4 rotating weight copies, 528 MB > L2)"}
 
 
 def bench_gemv_70b_formats(torch, dq, reps=30, fmts=((Q4_K, "q4_k"), (2, "q6_k"), (3, "q8_0")),
                            shapes=None):
     """The 70B-shaped linears (gate 28672x8192, down 8192x28672, q 8192x8192) in
-    Q4_K / Q6_K / Q8_0 at batch 1 and 8: one launch between two events, 4
-    rotating weight copies."""
+    Q4_K / Q6_K / Q8_0 at batch 1 and 8 (time_gemv: isolated and back to back)
+    over weight copies of at least 300 MB in all."""
     out = {}
     g = synth.streams(synth.BASE_SEED + 7, 2)
     for fmt, fname in fmts:
         for name, N, K in (shapes or synth.LLAMA70B_LINEARS[1:]):   # up (= gate shape), down, q
-            W0 = torch.from_numpy(synth.quant_matrix(g[0], fmt, N, K)).cuda()
-            Ws = [W0] + [W0.clone() for _ in range(ROTATE - 1)]
             wb = weight_bytes(fmt, N, K)
+            Ws = weight_copies(torch, torch.from_numpy(synth.quant_matrix(g[0], fmt, N, K)).cuda(), wb)
             for B in (1, 8):
                 x = torch.from_numpy(synth.activations(g[1], (B, K), 1)).cuda()
                 y = torch.empty(B, N, dtype=torch.float32, device="cuda")
-                for r in range(ROTATE):
-                    dq.qgemv(fmt, Ws[r], N, K, x, y=y)
-                torch.cuda.synchronize()
-                evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * reps)]
-                for i in range(reps):
-                    evs[2 * i].record()
-                    dq.qgemv(fmt, Ws[i % ROTATE], N, K, x, y=y)
-                    evs[2 * i + 1].record()
-                torch.cuda.synchronize()
-                us = float(np.median([evs[2 * i].elapsed_time(evs[2 * i + 1])
-                                      for i in range(reps)])) * 1e3
+                iso, b2b = time_gemv(torch, dq, fmt, Ws, N, K, x, y, reps=reps)
+                us = float(np.median(iso)) if iso else b2b
                 out["%s_%s_%dx%d_b%d" % (fname, "gate" if name == "up" else name, N, K, B)] = {
-                    "us": round(us, 2), "weight_GBps": round(wb / (us / 1e6) / 1e9, 1)}
-            del Ws, W0
+                    "us": round(us, 2), "weight_GBps": round(wb / (us / 1e6) / 1e9, 1),
+                    "us_back_to_back": round(b2b, 2),
+                    "weight_GBps_back_to_back": round(wb / (b2b / 1e6) / 1e9, 1)}
+            del Ws
             torch.cuda.empty_cache()
     return out
 
@@ -681,6 +705,7 @@ def run_ours(args):
         f70 = bench_gemv_70b_formats(torch, dq)
         for v in f70.values():
             v["frac_of_hbm"] = round(v["weight_GBps"] / peak, 4)
+            v["frac_of_hbm_back_to_back"] = round(v["weight_GBps_back_to_back"] / peak, 4)
         extra["gemv_70b_formats"] = f70
         # the further block formats (Q4_0, Q5_K, NVFP4, Q2_K, Q3_K) on the gate shape
         fx = bench_gemv_70b_formats(torch, dq, fmts=((4, "q4_0"), (5, "q5_k"), (6, "nvfp4"),
@@ -688,6 +713,7 @@ def run_ours(args):
                                     shapes=[("up", 28672, 8192)])
         for v in fx.values():
             v["frac_of_hbm"] = round(v["weight_GBps"] / peak, 4)
+            v["frac_of_hbm_back_to_back"] = round(v["weight_GBps_back_to_back"] / peak, 4)
         extra["gemv_70b_more_formats"] = fx
         if not args.no_moe:
             moe = {}

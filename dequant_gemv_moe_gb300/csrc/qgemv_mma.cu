@@ -503,19 +503,38 @@ int device_sms() {
   return sms;
 }
 
-// Pick the K-split (cluster size).  Measured on GB300 (graphs of back-to-back
-// launches): with two or more 64-row tiles per SM the unsplit grid is best
-// (28672 x 8192: batch 1 23.8 us unsplit against 29.0 us split in two; batch
-// 8 Q4_K 34.5 against 38.3 us, Q8_0 46.6 against 50.6 us, Q6_K even); with
-// fewer, the best split is the largest power of two whose CTAs all fit at
-// once (four per SM, the 56 KB shared-memory budget).  Odd cluster sizes
-// (3, 5, 6, 7) measured slower than the neighbouring powers of two on every
-// shape tried: a cluster's CTAs share one GPC, and odd sizes leave SMs of it
-// idle.
-int choose_ksplit(int tiles, int nsb, int sms) {
+// Early weight streaming (DQ_QGEMV_WEIGHTS_EARLY) only where a CTA's whole
+// K range fits its ring, so that all of its weights are in flight when the
+// previous kernel completes.  Measured on GB300 (graphs of back-to-back
+// launches of one Llama-3-8B linear, batch 1): early is faster for qkv 6144 x
+// 4096 (4 super-blocks per CTA, 5.94 against 6.32 us) and o 4096 x 4096 (2:
+// 4.89 against 5.47 us), slower for gate/up 28672 x 4096 (16: 14.6 against
+// 13.6 us) and down 4096 x 14336 (7 on a 5-stage ring: 10.6 against 9.5 us):
+// a partial prefetch competes with the previous kernel's last CTAs for HBM
+// and delays the completion every CTA of this one waits for.
+int early_weights(bool w_early, int nsb, int ks, int nstage) {
+  return (w_early && (nsb + ks - 1) / ks <= nstage) ? 1 : 0;
+}
+
+// Pick the K-split (cluster size) for `tiles` 64-row tiles when an SM holds
+// `per_sm` CTAs of the kernel.  Measured on GB300 (graphs of back-to-back
+// launches):
+//   * with two or more tiles per SM the unsplit grid is best (28672 x 8192:
+//     batch 1 23.8 us unsplit against 29.0 us split in two; batch 8 Q4_K 34.5
+//     against 38.3 us, Q8_0 46.6 against 50.6 us, Q6_K even);
+//   * with fewer, the split that fills the SMs' CTA slots in one wave:
+//     per_sm * sms / tiles, rounded down to 4 or 8 from 4 up.  Q4_K at
+//     8192 x 28672 / 8192 x 8192 (4 per SM): split 4 26.9 / 10.5 us, 3 27.8 /
+//     11.0, 6 (two waves) 35.1 / 14.9.  Kernels whose shared memory allows
+//     three per SM (the batch-8 Q6_K / Q8_0 rings, the batch-1 Q8_0 ring) take
+//     3: Q8_0 8192 x 28672 batch 8 54.1 us against 74.4 us at 4 (512 CTAs for
+//     456 slots: two waves) and 74.1 at 2; Q8_0 batch 1 45.9 against 56.3 us
+//     at 4 on the shallower 4-per-SM ring; Q6_K 8192 x 8192 batch 8 21.7
+//     against 24.6 us.
+int choose_ksplit(int tiles, int nsb, int sms, int per_sm) {
   if (tiles >= 2 * sms) return 1;
-  int s = 1;
-  while (2 * s <= 8 && 2 * s <= nsb && (long)tiles * 2 * s <= 4L * sms) s *= 2;
+  int s = std::min(8, std::min(nsb, std::max(1, per_sm * sms / tiles)));
+  if (s >= 4) s = s >= 8 ? 8 : 4;
   return s;
 }
 
@@ -538,13 +557,14 @@ int launch_qgemv_mma_fmt(const void* W, int64_t N, int64_t K, const void* x, int
   p.x.rows = nullptr;
   p.batch = batch;
   p.y = y;
-  p.w_early = w_early ? 1 : 0;
   const int tiles = (int)((N + kTileRows - 1) / kTileRows);
   const int sms = device_sms();
   if (sms <= 0) return DQ_ERR_CUDA;
   // shared memory per CTA <= 56 KB so that four CTAs (20 warps) share an SM
   constexpr int kSmemBudget = 56 * 1024;
-  int ks = force_ksplit > 0 ? force_ksplit : choose_ksplit(tiles, p.nsb, sms);
+  // CTAs per SM: four where a three-stage ring fits the 56 KB budget, else three
+  const int per_sm = make_plan<FMT>(3, batch, 4).total <= kSmemBudget ? 4 : 3;
+  int ks = force_ksplit > 0 ? force_ksplit : choose_ksplit(tiles, p.nsb, sms, per_sm);
   ks = std::max(1, std::min(ks, std::min(8, p.nsb)));
   // Q4_K grids of at most three CTAs per SM take the paired kernel with
   // deeper rings (28672 x 8192 at batch 8: 34.4 us against 38.2 us split in
@@ -555,6 +575,7 @@ int launch_qgemv_mma_fmt(const void* W, int64_t N, int64_t K, const void* x, int
   int nstage = 12;
   while (nstage > 3 && make_plan<FMT>(nstage, batch, ks).total > budget) --nstage;
   p.nstage = nstage;
+  p.w_early = early_weights(w_early, p.nsb, ks, nstage);
   const SmemPlan plan = make_plan<FMT>(nstage, batch, ks);
   auto kern = pair ? qgemv_mma_kernel<FMT, true> : qgemv_mma_kernel<FMT, false>;
   static bool attr_set[2][64] = {};
@@ -585,7 +606,10 @@ int launch_qgemv_b1(const void* W, int64_t N, int64_t K, const void* x, int xdt,
   const int tiles = (int)((N + kTileRows - 1) / kTileRows);
   const int sms = device_sms();
   if (sms <= 0) return DQ_ERR_CUDA;
-  int ks = force_ksplit > 0 ? force_ksplit : choose_ksplit(tiles, p.nsb, sms);
+  // CTAs per SM: four on the single-stage kernel; Q8_0, whose light decode
+  // needs the deeper rings of the paired kernel, three
+  const int per_sm = FMT == DQ_Q8_0 ? 3 : 4;
+  int ks = force_ksplit > 0 ? force_ksplit : choose_ksplit(tiles, p.nsb, sms, per_sm);
   ks = std::max(1, std::min(ks, std::min(8, p.nsb)));
   // grids that fit three CTAs per SM take the paired kernel with deeper rings
   // (28672 x 8192: 23.8 us against 28.2 us); larger ones four CTAs per SM
@@ -600,7 +624,7 @@ int launch_qgemv_b1(const void* W, int64_t N, int64_t K, const void* x, int xdt,
   p.x = x;
   p.y = y;
   p.nstage = nstage;
-  p.w_early = w_early ? 1 : 0;
+  p.w_early = early_weights(w_early, p.nsb, ks, nstage);
   auto kern = xdt == DQ_BF16 ? (pair ? qgemv_b1_kernel<FMT, true, true>
                                      : qgemv_b1_kernel<FMT, true, false>)
                              : (pair ? qgemv_b1_kernel<FMT, false, true>
