@@ -233,12 +233,13 @@ struct B1Plan {
   int nstage, off_w, off_x, off_sx, off_inv, off_z, off_red, total;
 };
 
-// Per stage: activations (Q4_K: x and -x of the odd sub-blocks; Q6_K, Q8_0:
-// x) and the negated sums of its 8 (Q4_K, Q8_0) or 16 (Q6_K) sub-blocks.
+// Per stage: activations (Q4_K: x and -x of the odd sub-blocks; the others:
+// x) and the negated sums of its 8 (Q4_K, Q8_0) or 16 (Q6_K, Q2_K, Q3_K)
+// sub-blocks.
 template <int FMT>
 struct B1Fmt {
   static constexpr int kStageX = FMT == DQ_Q4_K ? Q4KB1::kStageX : 512;
-  static constexpr int kSubs = FMT == DQ_Q6_K ? 16 : 8;
+  static constexpr int kSubs = (FMT == DQ_Q6_K || FMT == DQ_Q2_K || FMT == DQ_Q3_K) ? 16 : 8;
 };
 
 template <int FMT>
@@ -367,9 +368,9 @@ __global__ void __launch_bounds__(kThreads, PAIR ? 3 : 4)
           sum += f.x;
           sum += f.y;
         }
-        // sub-blocks of 32 (Q4_K: 4 lanes) or 16 (Q6_K: 2 lanes) activations
+        // sub-blocks of 32 (4 lanes) or 16 (2 lanes) activations
         sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-        if (FMT != DQ_Q6_K) sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        if (kSubs == 8) sum += __shfl_xor_sync(0xffffffffu, sum, 2);
         constexpr int lanes_per_sub = 32 / kSubs;
         if ((lane & (lanes_per_sub - 1)) == 0)
           ((float*)(smem + plan.off_sx + s * 4 * kSubs))[lane / lanes_per_sub] = -sum;
@@ -387,8 +388,12 @@ __global__ void __launch_bounds__(kThreads, PAIR ? 3 : 4)
     // Q4_K: mma row g is weight row rg (and rg + 8) of the warp's 16: rows
     // 0,2,4,6 in the first half-warp, 1,3,5,7 in the second, so that the
     // 8-byte quant loads of a half-warp fall on 32 distinct banks (row pitch
-    // 144 bytes).  Q6_K's 4-byte loads at pitch 240 are conflict-free as is.
-    const int rg = FMT == DQ_Q6_K ? g : 2 * (g & 3) + (g >> 2);
+    // 144 bytes).  The 4-byte loads of Q6_K, Q2_K and Q3_K (pitches 240, 112,
+    // 144: rows 4 banks apart) are conflict-free as is.
+    const int rg = kSubs == 16 ? g : 2 * (g & 3) + (g >> 2);
+    // Q2_K / Q3_K: 2^24 times the power of two of run r = t's in-place field
+    const float f23 = FMT == DQ_Q2_K ? 16777216.f / (float)(1 << (2 * t))
+                                     : 16777216.f / (float)(1 << (t == 3 ? 5 : 2 * t));
     const Q4KB1::Lane lc = Q4KB1::lane_consts(g, t);
     uint32_t real6[8];
 #pragma unroll
@@ -413,6 +418,21 @@ __global__ void __launch_bounds__(kThreads, PAIR ? 3 : 4)
         const uint32_t ra = wrow + st * L::W_STAGE + o;   // 272-byte super-blocks: aligned
         Q80B1::run(ra, ra + 8 * L::ROW_PITCH, xbase + kStageX * st + 64 * g + 16 * t + o,
                    zb + 64, zb, sxb + 4 * kSubs * st + 8 * t + o, inv, real6, t, a0, a8);
+      } else if constexpr (FMT == DQ_Q2_K) {
+        // 84-byte super-blocks: 4-byte aligned
+        const uint32_t ra = wrow + st * L::W_STAGE + (int)(((int64_t)(sb0 + c) * L::SBB) & 15) + o;
+        Q2KB1::run(ra, ra + 8 * L::ROW_PITCH, xbase + kStageX * st + o, zb,
+                   sxb + 4 * kSubs * st + o, inv, f23, real6, t, a0, a8);
+      } else if constexpr (FMT == DQ_Q3_K) {
+        // 110-byte super-blocks: 2-byte aligned, the offset uniform per stage
+        const int delta = (int)(((int64_t)(sb0 + c) * L::SBB) & 15);
+        const uint32_t ra = wrow + st * L::W_STAGE + delta + o;
+        if (delta & 2)
+          Q3KB1::run<true>(ra, ra + 8 * L::ROW_PITCH, xbase + kStageX * st + o, zb,
+                           sxb + 4 * kSubs * st + o, inv, f23, real6, t, a0, a8);
+        else
+          Q3KB1::run<false>(ra, ra + 8 * L::ROW_PITCH, xbase + kStageX * st + o, zb,
+                            sxb + 4 * kSubs * st + o, inv, f23, real6, t, a0, a8);
       } else {
         // the 210-byte super-block starts delta bytes into the 16-byte aligned box
         const int delta = (int)(((int64_t)(sb0 + c) * L::SBB) & 15);
@@ -596,7 +616,7 @@ int launch_qgemv_mma_fmt(const void* W, int64_t N, int64_t K, const void* x, int
   return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
 }
 
-// One fp16 / bf16 column of Q4_K, Q6_K or Q8_0: the block-diagonal kernel.
+// One fp16 / bf16 column of Q4_K, Q6_K, Q8_0, Q2_K or Q3_K: the block-diagonal kernel.
 template <int FMT>
 int launch_qgemv_b1(const void* W, int64_t N, int64_t K, const void* x, int xdt, float* y,
                     cudaStream_t stream, int force_ksplit, bool w_early) {
@@ -656,6 +676,10 @@ int launch_qgemv_mma(int fmt, const void* W, int64_t N, int64_t K, const void* x
     return launch_qgemv_b1<DQ_Q6_K>(W, N, K, x, xdt, y, s, force_ksplit, w_early);
   if (fmt == DQ_Q8_0 && batch == 1)
     return launch_qgemv_b1<DQ_Q8_0>(W, N, K, x, xdt, y, s, force_ksplit, w_early);
+  if (fmt == DQ_Q2_K && batch == 1)
+    return launch_qgemv_b1<DQ_Q2_K>(W, N, K, x, xdt, y, s, force_ksplit, w_early);
+  if (fmt == DQ_Q3_K && batch == 1)
+    return launch_qgemv_b1<DQ_Q3_K>(W, N, K, x, xdt, y, s, force_ksplit, w_early);
   if (fmt == DQ_Q4_K)
     return launch_qgemv_mma_fmt<DQ_Q4_K>(W, N, K, x, xdt, batch, y, s, force_ksplit, w_early);
   if (fmt == DQ_Q6_K)

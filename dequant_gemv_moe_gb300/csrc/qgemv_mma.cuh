@@ -1122,6 +1122,160 @@ struct Q6KB1 {
 };
 
 // ---------------------------------------------------------------------------
+// Q2_K and Q3_K with one activation column: Q6_K's two block-diagonal rounds
+// (round h: sub-block 8h + n in mma column n, n = 2r + lh; lane t supplies
+// weights 16lh + 4t + [0, 4) of run r, i.e. one quant word per (h, lh) serves
+// the four runs).  The 2-bit field r is masked in place, so column n sums
+// (q 4^r 2^-24) x (Q3_K: u = q + 4 assembled as u 2^b_r, b_r = 0, 2, 4, 5) and
+// every scale is applied per sub-block in fp32 after the products:
+//   Q2_K: y_row += d sc_j (sum q x) - dmin m_j (sum x)
+//   Q3_K: y_row += d (s_j - 32) (sum u x - 4 sum x)
+// The lane's columns 2t, 2t+1 both hold run r = t: one factor 4^-t (2^-b_t).
+// ---------------------------------------------------------------------------
+struct Q2KB1 {
+  // one round (half h) of rows g / g+8 (ra / rb: their super-block starts,
+  // 4-byte aligned) into D[2][4]
+  __device__ __forceinline__ static void round(uint32_t ra, uint32_t rb, int h, uint32_t xs,
+                                               uint32_t z, const uint32_t (&real)[8], int t,
+                                               float (&D)[2][4]) {
+    uint32_t L[2][2], H[2][2];   // [row][lh]: bytes (0, 1) and (2, 3) in 16-bit lanes
+    const uint32_t rows[2] = {ra, rb};
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+      for (int lh = 0; lh < 2; ++lh) {
+        const uint32_t q = lds_u32_nv(rows[rr] + 16 + 32 * h + 16 * lh + 4 * t);
+        L[rr][lh] = __byte_perm(q, 0, 0x4140);
+        H[rr][lh] = __byte_perm(q, 0, 0x4342);
+      }
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int lh = 0; lh < 2; ++lh) {
+        const int n = 2 * r + lh;
+        const uint32_t m = 0x00030003u << (2 * r);
+        const uint2 xv = lds_u64_nv(z + real[n] * (xs + 32 * (8 * h + n) - z));
+        mma_16816_nv(D[lh], L[0][lh] & m, L[1][lh] & m, H[0][lh] & m, H[1][lh] & m, xv.x, xv.y);
+      }
+  }
+
+  // ra / rb: shared addresses of the super-block in rows g / g+8 (from
+  // order_after_wait() of the stage barrier); xs: the stage's activations;
+  // z: 8 zero bytes; nsx: the stage's 16 negated sub-block sums; inv: inverse
+  // activation scale; f: 2^24 4^-t.
+  __device__ __forceinline__ static void run(uint32_t ra, uint32_t rb, uint32_t xs, uint32_t z,
+                                             uint32_t nsx, float inv, float f,
+                                             const uint32_t (&real)[8], int t, float2& acc0,
+                                             float2& acc8) {
+    const uint32_t xl = xs + 8 * t;
+    const uint32_t dd0 = lds_u32_nv(ra + 80), dd8 = lds_u32_nv(rb + 80);   // d | dmin << 16
+    const float d0 = __half2float(__ushort_as_half((unsigned short)(dd0 & 0xFFFF))) * inv;
+    const float m0 = __half2float(__ushort_as_half((unsigned short)(dd0 >> 16))) * inv;
+    const float d8 = __half2float(__ushort_as_half((unsigned short)(dd8 & 0xFFFF))) * inv;
+    const float m8 = __half2float(__ushort_as_half((unsigned short)(dd8 >> 16))) * inv;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float D[2][4] = {};
+      round(ra, rb, h, xl, z, real, t, D);
+      // sub-blocks j = 8h + 2t + (0, 1): scale | min << 4 bytes, -sum x
+      const uint32_t s0 = lds_u16_nv(ra + 8 * h + 2 * t), s8 = lds_u16_nv(rb + 8 * h + 2 * t);
+      const uint2 nsu = lds_u64_nv(nsx + 4 * (8 * h + 2 * t));
+      const float2 ns = make_float2(__uint_as_float(nsu.x), __uint_as_float(nsu.y));
+      const float2 sc0 = make_float2((float)(s0 & 15), (float)((s0 >> 8) & 15));
+      const float2 mn0 = make_float2((float)((s0 >> 4) & 15), (float)(s0 >> 12));
+      const float2 sc8 = make_float2((float)(s8 & 15), (float)((s8 >> 8) & 15));
+      const float2 mn8 = make_float2((float)((s8 >> 4) & 15), (float)(s8 >> 12));
+      const float2 c0 = fmul2(sc0, make_float2(d0 * f, d0 * f));
+      const float2 c8 = fmul2(sc8, make_float2(d8 * f, d8 * f));
+      const float2 k0 = fmul2(mn0, make_float2(m0, m0));
+      const float2 k8 = fmul2(mn8, make_float2(m8, m8));
+      // column 2t (even sub-block) accumulates in chain 0, 2t+1 in chain 1
+      acc0 = ffma2(ns, k0, ffma2(make_float2(D[0][0], D[1][1]), c0, acc0));
+      acc8 = ffma2(ns, k8, ffma2(make_float2(D[0][2], D[1][3]), c8, acc8));
+    }
+  }
+};
+
+struct Q3KB1 {
+  template <bool MIS>
+  __device__ __forceinline__ static uint32_t ldw(uint32_t a) {
+    if constexpr (!MIS) {
+      return lds_u32_nv(a);
+    } else {
+      const uint32_t lo = lds_u32_nv(a - 2), hi = lds_u32_nv(a + 2);
+      return __funnelshift_r(lo, hi, 16);
+    }
+  }
+
+  // u 2^b_r in each byte from the quant word q and the hmask word h shifted
+  // down by 4h (bit r = the high bit of run r)
+  __device__ __forceinline__ static uint32_t ubytes(uint32_t q, uint32_t h, int r) {
+    if (r < 3)
+      return lop3_and_or(h << (r + 2), 0x04040404u << (2 * r), q & (0x03030303u << (2 * r)));
+    return lop3_and_or(h << 4, 0x80808080u, (q >> 1) & 0x60606060u);
+  }
+
+  template <bool MIS>
+  __device__ __forceinline__ static void round(uint32_t ra, uint32_t rb, int h, uint32_t xs,
+                                               uint32_t z, const uint32_t (&real)[8], int t,
+                                               float (&D)[2][4]) {
+    uint32_t Q[2][2], E[2][2];   // [row][lh]: quant word, hmask word >> 4h
+    const uint32_t rows[2] = {ra, rb};
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+      for (int lh = 0; lh < 2; ++lh) {
+        Q[rr][lh] = ldw<MIS>(rows[rr] + 32 + 32 * h + 16 * lh + 4 * t);
+        E[rr][lh] = ldw<MIS>(rows[rr] + 16 * lh + 4 * t) >> (4 * h);
+      }
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int lh = 0; lh < 2; ++lh) {
+        const int n = 2 * r + lh;
+        const uint32_t w0 = ubytes(Q[0][lh], E[0][lh], r), w8 = ubytes(Q[1][lh], E[1][lh], r);
+        const uint2 xv = lds_u64_nv(z + real[n] * (xs + 32 * (8 * h + n) - z));
+        mma_16816_nv(D[lh], __byte_perm(w0, 0, 0x4140), __byte_perm(w8, 0, 0x4140),
+                     __byte_perm(w0, 0, 0x4342), __byte_perm(w8, 0, 0x4342), xv.x, xv.y);
+      }
+  }
+
+  // As Q2KB1::run; the super-block is 2-byte aligned (MIS: 2 mod 4);
+  // f: 2^24 2^-b_t.
+  template <bool MIS>
+  __device__ __forceinline__ static void run(uint32_t ra, uint32_t rb, uint32_t xs, uint32_t z,
+                                             uint32_t nsx, float inv, float f,
+                                             const uint32_t (&real)[8], int t, float2& acc0,
+                                             float2& acc8) {
+    const uint32_t xl = xs + 8 * t;
+    const float d0 = __half2float(__ushort_as_half((unsigned short)lds_u16_nv(ra + 108))) * inv;
+    const float d8 = __half2float(__ushort_as_half((unsigned short)lds_u16_nv(rb + 108))) * inv;
+    // sub-blocks j = 8h + 2t + (0, 1): low nibbles h of scale bytes 2t, 2t+1;
+    // top bits: field 2h + t/2 of bytes 8 + 2(t&1), +1
+    const uint32_t l0 = lds_u16_nv(ra + 96 + 2 * t), l8 = lds_u16_nv(rb + 96 + 2 * t);
+    const uint32_t u0 = lds_u16_nv(ra + 104 + 2 * (t & 1)), u8 = lds_u16_nv(rb + 104 + 2 * (t & 1));
+    const int hs = 2 * (t >> 1);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float D[2][4] = {};
+      round<MIS>(ra, rb, h, xl, z, real, t, D);
+      const uint32_t v0 = ((l0 >> (4 * h)) & 0x0F0Fu) | (((u0 >> (4 * h + hs)) & 0x0303u) << 4);
+      const uint32_t v8 = ((l8 >> (4 * h)) & 0x0F0Fu) | (((u8 >> (4 * h + hs)) & 0x0303u) << 4);
+      const float2 sc0 = make_float2((float)((int)(v0 & 63) - 32), (float)((int)(v0 >> 8) - 32));
+      const float2 sc8 = make_float2((float)((int)(v8 & 63) - 32), (float)((int)(v8 >> 8) - 32));
+      const uint2 nsu = lds_u64_nv(nsx + 4 * (8 * h + 2 * t));
+      const float2 ns = make_float2(__uint_as_float(nsu.x), __uint_as_float(nsu.y));
+      const float2 c0 = fmul2(sc0, make_float2(d0 * f, d0 * f));
+      const float2 c8 = fmul2(sc8, make_float2(d8 * f, d8 * f));
+      const float2 k0 = fmul2(sc0, make_float2(4.f * d0, 4.f * d0));
+      const float2 k8 = fmul2(sc8, make_float2(4.f * d8, 4.f * d8));
+      acc0 = ffma2(ns, k0, ffma2(make_float2(D[0][0], D[1][1]), c0, acc0));
+      acc8 = ffma2(ns, k8, ffma2(make_float2(D[0][2], D[1][3]), c8, acc8));
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
 // Q8_0 with one activation column: the block-diagonal core.  The 8 blocks of
 // 32 weights of a super-block go to the 8 mma columns.  A holds q + 128 (the
 // int8 quant with its sign bit flipped) as exact fp16 subnormals, and each

@@ -190,7 +190,7 @@ def test_q4k_batch1_scale_regimes(dq, orc, xdt):
     assert rel.max() <= 1e-3, rel.max()
 
 
-@pytest.mark.parametrize("fmt", [Q4_K, Q6_K, Q8_0])
+@pytest.mark.parametrize("fmt", [Q4_K, Q6_K, Q8_0, Q2_K, Q3_K])
 @pytest.mark.parametrize("xdt", [1, 2])
 @pytest.mark.parametrize("ks", [1, 2, 3, 5, 8])
 def test_batch1_ksplit(dq, orc, fmt, xdt, ks):
@@ -372,13 +372,15 @@ def _set_fp16(W, nb, off, vals_per_row, N):
 
 @pytest.mark.parametrize("fmt", [Q2_K, Q3_K])
 @pytest.mark.parametrize("xdt", [1, 2])
-def test_low_bit_scale_regimes(dq, orc, fmt, xdt):
+@pytest.mark.parametrize("B", [1, 2])
+def test_low_bit_scale_regimes(dq, orc, fmt, xdt, B):
     # rows whose super-block scales span the fp16 range (largest normal,
     # 1, 2^-14, subnormal, zero) and, for Q2_K, dmin far above or below d:
-    # the per-row power-of-two folding must keep every row within tolerance
-    # of its own magnitude
+    # every row within tolerance of its own magnitude, on the batch-1
+    # block-diagonal kernel (scales in fp32 after the products) and on the
+    # general one (per-row power-of-two folding)
     N, K = 128, 4096
-    g = synth.streams(9400 + fmt * 10 + xdt, 2)
+    g = synth.streams(9400 + fmt * 10 + xdt + 100 * B, 2)
     W = synth.quant_matrix(g[0], fmt, N, K)
     regimes = [60000.0, 1.0, 2.0 ** -14, 2.0 ** -20, 0.0, 0.01, 3.5e-3, 1000.0]
     d = np.array([regimes[r % len(regimes)] for r in range(N)])
@@ -388,10 +390,10 @@ def test_low_bit_scale_regimes(dq, orc, fmt, xdt):
         W = _set_fp16(W, 84, 82, dmin, N)
     else:
         W = _set_fp16(W, 110, 108, d, N)
-    x = synth.activations(g[1], (2, K), xdt)
+    x = synth.activations(g[1], (B, K), xdt)
     y = dq.qgemv(fmt, dev_bytes(W), N, K, dev_act(x, xdt)).cpu().numpy()
     assert dq.device_status() == 0
-    ref = orc.qgemv(fmt, W, N, K, x, xdt, 2)
+    ref = orc.qgemv(fmt, W, N, K, x, xdt, B)
     assert np.isfinite(y).all()
     for r in range(N):
         scale = np.abs(ref[:, r]).max()
@@ -400,3 +402,23 @@ def test_low_bit_scale_regimes(dq, orc, fmt, xdt):
             continue
         err = np.abs(y[:, r] - ref[:, r]).max() / scale
         assert err <= 4 * TOL[xdt], (r, d[r], err)
+
+
+@pytest.mark.parametrize("fmt", [Q2_K, Q3_K])
+@pytest.mark.parametrize("xdt", [1, 2])
+def test_low_bit_batch1_activation_extremes(dq, orc, fmt, xdt):
+    # one column with huge, tiny and all-zero 16-weight sub-blocks (bf16 far
+    # above the fp16 range: one power-of-two scale per stage)
+    N, K = 96, 4096
+    g = synth.streams(9500 + fmt * 10 + xdt, 3)
+    W = synth.quant_matrix(g[0], fmt, N, K)
+    x = synth.activations(g[1], (1, K), 0)
+    x[0, :256] *= np.float32(1.0e4 if xdt == 1 else 3.0e6)
+    x[0, 256:512] *= np.float32(1e-5)
+    x[0, 512:528] = 0.0
+    x = x.astype(np.float16) if xdt == 1 else synth.f32_to_bf16_bits(x)
+    y = dq.qgemv(fmt, dev_bytes(W), N, K, dev_act(x, xdt)).cpu().numpy()
+    assert dq.device_status() == 0
+    ref = orc.qgemv(fmt, W, N, K, x, xdt, 1)
+    assert np.isfinite(y).all()
+    assert rel_err(y, ref) <= TOL[xdt]
