@@ -18,7 +18,8 @@ int launch_qgemv_f32(int fmt, const void* W, int64_t N, int64_t K, const float* 
 int launch_qgemv_mma(int fmt, const void* W, int64_t N, int64_t K, const void* x, int xdt,
                      int batch, float* y, cudaStream_t s, int force_ksplit, bool w_early);
 int launch_router(const float* Wr, int E, int H, const void* x, int xdt, int T, int top_k,
-                  int KS, float* part, float* logits, int32_t* idx, float* gate, cudaStream_t s);
+                  int KS, float* part, float* logits, int32_t* idx, float* gate, cudaStream_t s,
+                  bool with_topk = true);
 int launch_permute(const int32_t* idx, int T, int k, int E, int32_t* offsets, int32_t* sorted,
                    cudaStream_t s);
 

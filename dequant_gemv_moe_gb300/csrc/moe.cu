@@ -200,15 +200,10 @@ __device__ __forceinline__ bool better(float a, int ia, float b, int ib) {
   return a > b || (a == b && ia < ib);
 }
 
-__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ part, int KS, int T,
-                                                   int E, int k, float* __restrict__ logits,
-                                                   int32_t* __restrict__ idx,
-                                                   float* __restrict__ gate) {
-  pdl_wait();
-  pdl_trigger();
-  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (t >= T) return;
+// Top-k of token t by one warp (lane: this thread's lane).
+__device__ __forceinline__ void topk_warp(const float* __restrict__ part, int KS, int T, int E,
+                                          int k, int t, int lane, float* __restrict__ logits,
+                                          int32_t* __restrict__ idx, float* __restrict__ gate) {
   float v[8];
   int id[8];
   // sum the KS partials of this lane's 8 experts in a fixed order (q
@@ -286,6 +281,16 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ par
   }
 }
 
+__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ part, int KS, int T,
+                                                   int E, int k, float* __restrict__ logits,
+                                                   int32_t* __restrict__ idx,
+                                                   float* __restrict__ gate) {
+  pdl_wait();
+  pdl_trigger();
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t < T) topk_warp(part, KS, T, E, k, t, threadIdx.x & 31, logits, idx, gate);
+}
+
 // ===========================================================================
 // 3. stable permute + work groups: one CTA of 1024 threads
 // ===========================================================================
@@ -346,7 +351,17 @@ __device__ __forceinline__ void x16_rows_cta(const void* x, int xdt, int T, int 
     if (threadIdx.x == 0) inv[row] = iv;
   }
 }
-__global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict__ idx, int T,
+// tk (nullable): top-k of the T <= 32 tokens first, one warp each, from the
+// router partials (tk->part, tk->KS), writing idx, gate and logits; the
+// permute then reads idx back (coherent loads: written by this CTA).
+struct TopkIn {
+  const float* part;
+  int KS;
+  float* logits;
+  float* gate;
+};
+
+__global__ void __launch_bounds__(1024) permute_kernel(int32_t* idx, int T,
                                                        int k, int E, int n_shared, int gw,
                                                        int32_t* __restrict__ offsets,
                                                        int32_t* __restrict__ sorted,
@@ -358,11 +373,17 @@ __global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict
                                                        int32_t* __restrict__ n_units,
                                                        const void* __restrict__ cx, int cxdt,
                                                        int cK, __half* __restrict__ cx16,
-                                                       float* __restrict__ cxinv) {
+                                                       float* __restrict__ cxinv, TopkIn tk) {
   pdl_wait();
   pdl_trigger();
   __shared__ float red[32];
   __shared__ int wsum[8];
+  if (tk.part) {
+    if ((int)(threadIdx.x >> 5) < T)
+      topk_warp(tk.part, tk.KS, T, E, k, threadIdx.x >> 5, threadIdx.x & 31, tk.logits, idx,
+                tk.gate);
+    __syncthreads();
+  }
   if (cx16) x16_rows_cta(cx, cxdt, T, cK, cx16, cxinv, red);
   __shared__ int cnt[256];
   __shared__ int off[257];
@@ -374,7 +395,7 @@ __global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict
   const int P = T * k;
   if (tid < 256) cnt[tid] = 0;
   __syncthreads();
-  for (int p = tid; p < P; p += 1024) atomicAdd(&cnt[idx[p]], 1);
+  for (int p = tid; p < P; p += 1024) atomicAdd(&cnt[__ldcg(idx + p)], 1);
   __syncthreads();
   // exclusive scan of counts (E <= 256)
   {
@@ -393,7 +414,7 @@ __global__ void __launch_bounds__(1024) permute_kernel(const int32_t* __restrict
     for (int i = tid; i < 32 * 256; i += 1024) (&cntw[0][0])[i] = 0;
     __syncthreads();
     const int p = base + tid;
-    const int e = (p < P) ? idx[p] : 256;
+    const int e = (p < P) ? __ldcg(idx + p) : 256;
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     const int rank = __popc(peers & ((1u << lane) - 1u));
     if (p < P && rank == 0) cntw[warp][e] = __popc(peers);
@@ -853,7 +874,8 @@ int launch_swiglu_wide(const int4* units, const int* n_units, int max_units, con
                        const float* U, int F, float* h, cudaStream_t s);
 
 int launch_router(const float* Wr, int E, int H, const void* x, int xdt, int T, int top_k,
-                  int KS, float* part, float* logits, int32_t* idx, float* gate, cudaStream_t s) {
+                  int KS, float* part, float* logits, int32_t* idx, float* gate, cudaStream_t s,
+                  bool with_topk) {
   if (T <= kRouterStreamT && KS == (H + kRouterChunk - 1) / kRouterChunk && KS > 1 &&
       ((uintptr_t)Wr & 15) == 0 && H % 4 == 0) {
     const dim3 g((unsigned)((E + 7) / 8), (unsigned)KS);
@@ -863,15 +885,16 @@ int launch_router(const float* Wr, int E, int H, const void* x, int xdt, int T, 
     launch_pdl(router_logits_kernel, dim3(g1), dim3(128), 0, s, 0, Wr, E, H, x, xdt, T, KS, part);
   }
   if (cudaGetLastError() != cudaSuccess) return DQ_ERR_CUDA;
+  if (!with_topk) return DQ_OK;
   launch_pdl(topk_kernel, dim3((unsigned)((T + 7) / 8)), dim3(256), 0, s, 0, part, KS, T, E, top_k, logits, idx, gate);
   return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
 }
 
 int launch_permute(const int32_t* idx, int T, int k, int E, int32_t* offsets, int32_t* sorted,
                    cudaStream_t s) {
-  launch_pdl(permute_kernel, dim3(1), dim3(1024), 0, s, 0, idx, T, k, E, 0, 8, offsets, sorted,
-             nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, 0, 0, nullptr,
-             nullptr);
+  launch_pdl(permute_kernel, dim3(1), dim3(1024), 0, s, 0, const_cast<int32_t*>(idx), T, k, E, 0,
+             8, offsets, sorted, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, 0,
+             0, nullptr, nullptr, TopkIn{nullptr, 0, nullptr, nullptr});
   return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
 }
 
@@ -896,9 +919,12 @@ int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, floa
   float* ypos = (float*)(w + pl.off_ypos);
 
   int rc = DQ_OK;
+  // up to 32 tokens in one call: the permute CTA takes the top-k too (one
+  // warp per token), one launch less on the decode path
+  const bool fuse_topk = (stages & 3) == 3 && T <= 32;
   if (stages & 1) {
     rc = launch_router(d.router_W, d.E, d.hidden, x, xdt, T, d.top_k, pl.KS, part, lg, idx, gate,
-                       s);
+                       s, !fuse_topk);
     if (rc != DQ_OK) return rc;
   }
   if (!(stages & 2)) return DQ_OK;
@@ -912,7 +938,8 @@ int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, floa
   launch_pdl(permute_kernel, dim3(1), dim3(1024), 0, s, 0, idx, T, d.top_k, d.E, d.n_shared,
              pl.GW, offsets, sorted, inv, tok, groups, ngroups, pl.wide ? units : nullptr, nunits,
              fuse_x16 ? x : nullptr, xdt, d.hidden, fuse_x16 ? x16t : nullptr,
-             fuse_x16 ? xinvt : nullptr);
+             fuse_x16 ? xinvt : nullptr,
+             fuse_topk ? TopkIn{part, pl.KS, lg, gate} : TopkIn{nullptr, 0, nullptr, nullptr});
   if (cudaGetLastError() != cudaSuccess) return DQ_ERR_CUDA;
 
   const int q = qk(d.fmt), bb = blk_bytes(d.fmt);
