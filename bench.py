@@ -178,10 +178,13 @@ def dist_setup(ngpus):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if world <= 1:
         return 0, 1, 0, None
+    import torch
     import torch.distributed as dist
     rank = int(os.environ["RANK"])
     local = int(os.environ.get("LOCAL_RANK", rank))
-    backend = "nccl"
+    # one GPU per rank over NCCL; gloo where no GPU is visible (the CPU tests
+    # of this plumbing)
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
     dist.init_process_group(backend=backend)
     return rank, world, local, dist
 
@@ -195,9 +198,16 @@ def max_over_ranks(dist, v):
     if dist is None:
         return v
     import torch
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_value(world, bytes_per_step, ms_per_step):
+    """Whole-job GB/s of `world` replicas, each moving bytes_per_step per step,
+    timed by the slowest rank (ms_per_step = max over ranks)."""
+    return world * bytes_per_step * 1e3 / ms_per_step / 1e9
 
 
 # ---------------------------------------------------------------------------
@@ -695,7 +705,7 @@ def run_ours(args):
     lay = bench_layer(torch, dq, args, synth.LLAMA8B_MERGED)
     barrier(dist)
     ms = max_over_ranks(dist, lay["ms_per_step"])
-    value = world * lay["weight_bytes"] * 1e3 / ms / 1e9
+    value = job_value(world, lay["weight_bytes"], ms)
     extra = {}
     if rank == 0:
         extra["gemv_70b_gate_b1"] = bench_gemv_70b(torch, dq)
