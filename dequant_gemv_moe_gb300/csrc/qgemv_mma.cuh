@@ -433,29 +433,64 @@ struct SBDot<DQ_Q4_K> {
 // Q6_K: lane t owns, in each half h, positions l in [8t, 8t+8) of the four
 // 32-weight runs r = 0..3: weights 128h + 32r + l, scale index 8h + 2r + t/2.
 // Blocks are 210 bytes, so every other block is only 2-byte aligned.
+//
+// Decode: q is assembled in place in each 16-bit lane (runs 0-1: the low
+// nibble at bits 0-3 and the two qh bits at 4-5, value q; runs 2-3: the high
+// nibble at bits 4-7 and the qh bits at 8-9, value 16 q), read as the exact
+// fp16 subnormal, and one HFMA2 with S = d sc F (runs 2-3: S / 16) and
+// O = -32 d sc F 2^-24 gives (q - 32) d sc F 2^-24: the weight times the
+// row's power of two F 2^-24 = 2^-(e+1), e the exponent field of d (undone in
+// fp32 after the super-block).  d F < 512 and |sc| <= 128 keep |S| <= 65504.
 template <>
 struct SBDot<DQ_Q6_K> {
-  static constexpr bool kRowScale = false;
+  static constexpr bool kRowScale = true;
+
+  // (q - 32) of two weights as an exact fp16 pair, for decoders that produce
+  // absolute weights (the tensor-core prefill slabs): nib holds 4-bit values
+  // in bits 0-3 of each 16-bit lane, hq 2-bit values already in bits 4-5
   __device__ __forceinline__ static uint32_t q6_pair(uint32_t nib, uint32_t hq) {
-    // nib: 4-bit values in bits 0-3 of each 16-bit lane; hq: 2-bit values
-    // already in bits 4-5.  Returns fp16 pair of (q - 32), exact.
     const uint32_t v = (nib & 0x000F000Fu) | (hq & 0x00300030u) | 0x64006400u;
     return h2_as_u32(__hsub2(u32_as_h2(v), u32_as_h2(0x64206420u)));   // 1024+q - 1056
   }
 
-  template <int NT>
+  // 32-bit word at a 2-byte aligned address whose misalignment (0 or 2
+  // bytes, MIS) is uniform for the stage
+  template <bool MIS>
+  __device__ __forceinline__ static uint32_t ldw(uint32_t a) {
+    if constexpr (MIS) return __funnelshift_r(lds_u32_nv(a - 2), lds_u32_nv(a + 2), 16);
+    else return lds_u32_nv(a);
+  }
+
+  template <int NT, bool PAIRX = false>
   __device__ __forceinline__ static void run(uint32_t wrow, int pitch8,
                                              const uint32_t (&xcol)[NT], int kb, int t,
-                                             float (&acc)[NT][2][4]) {
+                                             float (&acc)[NT][2][4], float& r0, float& r8) {
+    // the 210-byte super-blocks start 0 or 2 bytes off a word, the same for
+    // every row of a stage: a uniform branch
+    if (wrow & 2u) run_impl<NT, true>(wrow, pitch8, xcol, kb, t, acc, r0, r8);
+    else run_impl<NT, false>(wrow, pitch8, xcol, kb, t, acc, r0, r8);
+  }
+
+  template <int NT, bool MIS>
+  __device__ __forceinline__ static void run_impl(uint32_t wrow, int pitch8,
+                                                  const uint32_t (&xcol)[NT], int kb, int t,
+                                                  float (&acc)[NT][2][4], float& r0,
+                                                  float& r8) {
     const uint32_t rows[2] = {wrow, wrow + pitch8};
-    // d and this lane's 8 scales per row: sc[8h + 2r + t/2], h = 0..1, r = 0..3
-    __half2 scl[2][8];
+    // this lane's 8 scales per row, sc[8h + 2r + t/2] (h = 0..1, r = 0..3), as
+    // S and O pairs
+    __half2 S[2][8], O[2][8];
+    float rinv[2];
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
       const uint32_t rb = rows[rr];
-      const __half d = __ushort_as_half((unsigned short)lds_u16_nv(rb + 208));
-      const uint32_t s0 = lds_u32_a2_nv(rb + 192), s1 = lds_u32_a2_nv(rb + 196);
-      const uint32_t s2 = lds_u32_a2_nv(rb + 200), s3 = lds_u32_a2_nv(rb + 204);
+      const uint32_t dh = lds_u16_nv(rb + 208);
+      const uint32_t e = (dh >> 10) & 31u;
+      const float F = __uint_as_float((150u - e) << 23);   // 2^(23 - e)
+      rinv[rr] = __uint_as_float((128u + e) << 23);        // 2^(e + 1)
+      const float df = __half2float(__ushort_as_half((unsigned short)dh)) * F;   // exact
+      const uint32_t s0 = ldw<MIS>(rb + 192), s1 = ldw<MIS>(rb + 196);
+      const uint32_t s2 = ldw<MIS>(rb + 200), s3 = ldw<MIS>(rb + 204);
       const uint32_t sw[4] = {s0, s1, s2, s3};
 #pragma unroll
       for (int h = 0; h < 2; ++h)
@@ -465,39 +500,54 @@ struct SBDot<DQ_Q6_K> {
           const uint32_t word = sw[idx >> 2];
           const int byte = (idx & 3) + (t >> 1);
           const int sc = (int)(int8_t)((word >> (8 * byte)) & 0xFF);
-          scl[rr][4 * h + r] = __half2half2(__hmul(d, __int2half_rn(sc)));
+          // d F sc is exact in fp32 (11 + 8 bits); one rounding to fp16
+          const __half2 sv = __float2half2_rn(df * (float)sc * ((r & 2) ? 0.0625f : 1.f));
+          S[rr][4 * h + r] = sv;
+          O[rr][4 * h + r] = __hmul2(sv, __float2half2_rn((r & 2) ? -0x1p-15f : -0x1p-19f));
         }
     }
+    r0 = rinv[0];
+    r8 = rinv[1];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
 #pragma unroll
       for (int p = 0; p < 2; ++p) {
-        uint32_t A[2], B[2], H[2];
+        // per row: ql words of runs 0/2 (A) and 1/3 (B), the qh word (H), each
+        // as bytes (b0 b2 | b1 b3) in 16-bit lanes; the weights k+2, k+3 of
+        // each step come from the words shifted down by 8
+        uint32_t Q[2][2][2], H2[2][2], H4[2][2];   // [row][hi pair][run&1], [row][hi pair]
 #pragma unroll
         for (int rr = 0; rr < 2; ++rr) {
           const uint32_t rb = rows[rr];
-          A[rr] = __byte_perm(lds_u32_a2_nv(rb + 64 * h + 8 * t + 4 * p), 0, 0x3120);
-          B[rr] = __byte_perm(lds_u32_a2_nv(rb + 64 * h + 32 + 8 * t + 4 * p), 0, 0x3120);
-          H[rr] = __byte_perm(lds_u32_a2_nv(rb + 128 + 32 * h + 8 * t + 4 * p), 0, 0x3120);
+          const uint32_t A = __byte_perm(ldw<MIS>(rb + 64 * h + 8 * t + 4 * p), 0, 0x3120);
+          const uint32_t B = __byte_perm(ldw<MIS>(rb + 64 * h + 32 + 8 * t + 4 * p), 0, 0x3120);
+          const uint32_t H = __byte_perm(ldw<MIS>(rb + 128 + 32 * h + 8 * t + 4 * p), 0, 0x3120);
+          Q[rr][0][0] = A;
+          Q[rr][0][1] = B;
+          Q[rr][1][0] = A >> 8;
+          Q[rr][1][1] = B >> 8;
+          H4[rr][0] = H << 4;
+          H2[rr][0] = H << 2;
+          H4[rr][1] = (H >> 8) << 4;
+          H2[rr][1] = (H >> 8) << 2;
         }
         const int kbase = kb + 128 * h + 8 * t + 4 * p;
-        // run r: nibble source and the shift that brings qh bits 2r..2r+1 to 4..5
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
+          // qh bits 2r..2r+1 land at 4-5 (runs 0-1) or 8-9 (runs 2-3) after a
+          // left shift by 4 (r even) or 2 (r odd)
+          const uint32_t qm = (r & 2) ? 0x00F000F0u : 0x000F000Fu;
+          const uint32_t hm = (r & 2) ? 0x03000300u : 0x00300030u;
           uint32_t a[4];
 #pragma unroll
-          for (int rr = 0; rr < 2; ++rr) {
-            const uint32_t src = (r & 1) ? B[rr] : A[rr];
-            const uint32_t nlo = (r & 2) ? (src >> 4) : src;            // weights k, k+1
-            const uint32_t nhi = (r & 2) ? (src >> 12) : (src >> 8);    // weights k+2, k+3
-            // qh bits 2r..2r+1 of each byte moved to bits 4..5 of its 16-bit lane
-            const uint32_t hq = H[rr], hs = H[rr] >> 8;
-            const uint32_t hlo = (r <= 2) ? (hq << (4 - 2 * r)) : (hq >> (2 * r - 4));
-            const uint32_t hhi = (r <= 2) ? (hs << (4 - 2 * r)) : (hs >> (2 * r - 4));
-            const __half2 sc = scl[rr][4 * h + r];
-            a[rr] = h2_as_u32(__hmul2(u32_as_h2(q6_pair(nlo, hlo)), sc));
-            a[2 + rr] = h2_as_u32(__hmul2(u32_as_h2(q6_pair(nhi, hhi)), sc));
-          }
+          for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+            for (int hp = 0; hp < 2; ++hp) {
+              const uint32_t hq = (r & 1) ? H2[rr][hp] : H4[rr][hp];
+              const uint32_t u = lop3_and_or(hq, hm, Q[rr][hp][r & 1] & qm);
+              a[2 * hp + rr] =
+                  h2_as_u32(__hfma2(u32_as_h2(u), S[rr][4 * h + r], O[rr][4 * h + r]));
+            }
           mma_x<NT>(acc, r & 1, a[0], a[1], a[2], a[3], xcol, kbase + 32 * r);
         }
       }

@@ -229,6 +229,33 @@ def test_q6k_batch1_scales_and_extremes(dq, orc, xdt):
 
 
 @pytest.mark.parametrize("xdt", [1, 2])
+def test_q6k_batch3_scales_and_extremes(dq, orc, xdt):
+    # the general core folds d into a per-row power of two: d over several
+    # decades and signs (subnormal to 4), int8 scales at both extremes,
+    # three activation columns with huge, tiny and zero chunks
+    N, K, B = 96, 4096, 3
+    g = synth.streams(4848 + xdt, 3)
+    W = synth.quant_matrix(g[0], Q6_K, N, K).reshape(N, K // 256, 210)
+    d = np.float16(np.geomspace(3e-7, 4.0, N) * np.where(np.arange(N) % 3 == 0, -1, 1))
+    W[:, :, 208:210] = d.view(np.uint8).reshape(N, 1, 2)
+    W[::5, :, 192:208] = np.array([127, -128] * 8, dtype=np.int8).view(np.uint8)
+    W = W.reshape(-1)
+    x = synth.activations(g[1], (B, K), 0)
+    x[0, :256] *= np.float32(1.0e4 if xdt == 1 else 3.0e6)
+    x[1, 256:512] *= np.float32(1e-5)
+    x[2, 512:528] = 0.0
+    x = x.astype(np.float16) if xdt == 1 else synth.f32_to_bf16_bits(x)
+    y = dq.qgemv(Q6_K, dev_bytes(W), N, K, dev_act(x, xdt)).cpu().numpy().astype(np.float64)
+    assert dq.device_status() == 0
+    ref = orc.qgemv(Q6_K, W, N, K, x, xdt, B)
+    wabs = np.abs(orc.dequant(Q6_K, W, N * K).reshape(N, K).astype(np.float64))
+    xabs = np.abs(orc.act_to_f64(xdt, x).reshape(B, K))
+    scale = xabs @ wabs.T
+    rel = np.abs(y - ref) / scale
+    assert rel.max() <= 1e-3, rel.max()
+
+
+@pytest.mark.parametrize("xdt", [1, 2])
 def test_q4k_batch1_activation_extremes(dq, orc, xdt):
     # activations near the top of the fp16 range, tiny ones, and exact zeros in
     # whole sub-blocks (bf16 input far above fp16: one power-of-two scale)
