@@ -8,8 +8,9 @@ the previous one drains), replayed as one CUDA graph per step (one graph launch 
 step, the way the KTransformers page runs decode).  value = algorithmic weight
 bytes streamed per step / device time per step.  Inputs are resident in HBM before timing;
 L2 is defeated by rotating 4 copies of the layer's weights (491 MB > 3x L2).
-The same run also times the 70B-shaped batch-1 Q4_K gate GEMV (the north-star
-shape) and the two MoE layers (tokens/s), and the CPU oracle on a bounded
+The same run also times the 70B-shaped batch-1 Q4_K gate GEMV (28672 x 8192),
+the 70B-shaped linears in every block format, the two MoE layers (tokens/s),
+and the CPU oracle on a bounded
 sample of the same work.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -515,7 +516,7 @@ def weight_copies(torch, W0, wb):
 
 
 def bench_gemv_70b(torch, dq, reps=50):
-    """North-star shape: batch-1 Q4_K 28672 x 8192 gate GEMV, 4 rotating copies."""
+    """The Llama-70B gate shape: batch-1 Q4_K 28672 x 8192 GEMV, 4 rotating copies."""
     g = synth.streams(synth.BASE_SEED + 2, 2)
     N, K = 28672, 8192
     wb = weight_bytes(Q4_K, N, K)

@@ -8,7 +8,7 @@ mathematics or a library routine fix independently:
   * brute force with numpy's matmul on tiny shapes, plus an integer case that
     is exact in any precision;
   * numpy's stable sort for top-k / permute, scipy's softmax for k = E;
-  * the spec MoE invariant: the layer equals a dense all-experts
+  * the MoE invariant: the layer equals a dense all-experts
     compute masked to the selected experts.
 A plausible slip anywhere in the oracle (a swapped nibble, a wrong 6-bit
 field, a transposed operand, a dropped min term, a reversed tie-break, a
