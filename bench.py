@@ -34,7 +34,9 @@ import synth  # noqa: E402
 METRIC = "qGEMV weight GB/s (% of HBM peak); MoE-layer tokens/s at 1 GB300"
 Q4_K = 1
 ROTATE = 4
-LAYERS_PER_GRAPH = 8   # layer passes per captured graph (a decode step spans the layers)
+# layer passes per captured graph: one graph per decode step of the 32-layer
+# Llama-3-8B, whose step runs the same linears once per layer
+LAYERS_PER_GRAPH = 32
 
 
 def parse():
@@ -760,7 +762,7 @@ def run_ours(args):
         "config": {"workload": "llama3-8b decode-layer linears: q,k,v,o,gate,up,down Q4_K "
                                "(122.7 MB), fp16 x, batch 1, q|k|v and gate|up stored as "
                                "merged matrices (4 dq_qgemv launches per layer), weights "
-                               "read-only (early weight streaming); 8 layer passes per CUDA "
+                               "read-only (early weight streaming); 32 layer passes per CUDA "
                                "graph over 4 rotating weight copies, as a decode step's graph "
                                "spans the model's layers",
                    "l2": "4 rotating weight copies, 491 MB > 3x L2",
