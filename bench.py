@@ -244,6 +244,21 @@ def oracle_sample(budget_s=12.0, seed=synth.BASE_SEED + 1, threads=None):
                       "fp16 x, %.1f s of CPU time" % (rows_done, total_t)}
 
 
+LAYER_WEIGHT_BYTES = 122683392   # the seven Q4_K linears of one Llama-3-8B layer
+
+
+def layer_config(world):
+    """The headline workload, shared by both arms' JSON lines."""
+    return {"workload": "llama3-8b decode-layer linears: q,k,v,o,gate,up,down Q4_K "
+                        "(122.7 MB), fp16 x, batch 1, q|k|v and gate|up stored as "
+                        "merged matrices (4 dq_qgemv launches per layer), weights "
+                        "read-only (early weight streaming); 32 layer passes per CUDA "
+                        "graph over 4 rotating weight copies, as a decode step's graph "
+                        "spans the model's layers",
+            "l2": "4 rotating weight copies, 491 MB > 3x L2",
+            "parallelism": "replicas" if world > 1 else "single"}
+
+
 def run_reference(args):
     rank, world, local, dist = dist_setup(args.gpus)
     if rank != 0:
@@ -254,12 +269,14 @@ def run_reference(args):
     t0 = time.time()
     r = oracle_sample(budget_s=budget)
     wall = time.time() - t0
+    # one step = one layer's weight bytes at the oracle's measured rate on the
+    # sampled rows
     line = {"metric": METRIC, "impl": "reference", "value": r["value"], "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+            "ms_per_step": round(LAYER_WEIGHT_BYTES / (r["value"] * 1e9) * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "llama3-8b decode-layer linears, Q4_K, fp16 x, batch 1 "
-                                   "(oracle on sampled rows)"},
+            "config": layer_config(1),
             "cpu_baseline": r,
             "e2e": {"value": r["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
@@ -759,15 +776,7 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic",
-        "config": {"workload": "llama3-8b decode-layer linears: q,k,v,o,gate,up,down Q4_K "
-                               "(122.7 MB), fp16 x, batch 1, q|k|v and gate|up stored as "
-                               "merged matrices (4 dq_qgemv launches per layer), weights "
-                               "read-only (early weight streaming); 32 layer passes per CUDA "
-                               "graph over 4 rotating weight copies, as a decode step's graph "
-                               "spans the model's layers",
-                   "l2": "4 rotating weight copies, 491 MB > 3x L2",
-                   "frac_of_hbm": round(value / world / peak, 4),
-                   "parallelism": "replicas" if world > 1 else "single"},
+        "config": dict(layer_config(world), frac_of_hbm=round(value / world / peak, 4)),
         "roofline": {"bound": "hbm", "kernel": "qgemv_b1_kernel<Q4_K>",
                      "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": peak_src + " hbm_gbs (MEASURED_PEAKS.json)",
