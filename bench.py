@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-moe", action="store_true", help="skip the MoE-layer lines")
+    ap.add_argument("--oracle-sample", type=float, default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--oracle-threads", type=int, default=None, help=argparse.SUPPRESS)
     ap.add_argument("--case", default=None,
                     help="profiling aid: run only one workload a few times and exit "
                          "(gemv70b | layer8b | mixtral | deepseek1 | deepseek8 | deepseek256)")
@@ -217,31 +219,46 @@ def job_value(world, bytes_per_step, ms_per_step):
 # CPU oracle baseline (bounded sample of the same work)
 # ---------------------------------------------------------------------------
 def oracle_sample(budget_s=12.0, seed=synth.BASE_SEED + 1, threads=None):
+    """The oracle on the benchmark's own step: whole passes over the four
+    merged Llama-3-8B linears (122.7 MB of Q4_K weights, batch 1, fp16 x),
+    repeated until budget_s of CPU time has passed."""
     import oracle
     g = synth.streams(seed, 2)
-    x = synth.activations(g[1], (1, 14336), 1)
     threads = threads or oracle.default_threads()
-    total_bytes, total_t, rows_done = 0, 0.0, 0
-    rng = np.random.default_rng(0)
-    mats = {}
-    for name, N, K in synth.LLAMA8B_LINEARS:
-        key = (N, K)
-        if key not in mats:
-            mats[key] = synth.quant_matrix(g[0], Q4_K, 512, K)   # 512 sampled rows
-    t_end = time.time() + budget_s
-    while time.time() < t_end:
-        for name, N, K in synth.LLAMA8B_LINEARS:
-            W = mats[(N, K)]
-            rows = np.sort(rng.choice(512, 256, replace=False)).astype(np.int64)
+    mats = [(synth.quant_matrix(g[0], Q4_K, N, K), N, K) for (_, N, K) in synth.LLAMA8B_MERGED]
+    xs = [synth.activations(g[1], (1, K), 1) for (_, N, K) in synth.LLAMA8B_MERGED]
+    total_bytes, total_t, passes = 0, 0.0, 0
+    while total_t < budget_s or passes == 0:
+        for (W, N, K), x in zip(mats, xs):
             t0 = time.perf_counter()
-            oracle.qgemv(Q4_K, W, 512, K, x[:, :K], 1, 1, rows=rows, nthreads=threads)
+            oracle.qgemv(Q4_K, W, N, K, x, 1, 1, nthreads=threads)
             total_t += time.perf_counter() - t0
-            total_bytes += weight_bytes(Q4_K, len(rows), K)
-            rows_done += len(rows)
+            total_bytes += weight_bytes(Q4_K, N, K)
+        passes += 1
     return {"value": total_bytes / total_t / 1e9, "unit": "GB/s", "cores": threads,
             "kind": "oracle",
-            "sample": "%d rows of the 7 Llama-3-8B linears (256-row random samples), batch 1, "
-                      "fp16 x, %.1f s of CPU time" % (rows_done, total_t)}
+            "sample": "%d whole passes of the benchmark step (the four merged Llama-3-8B "
+                      "linears, 122.7 MB of Q4_K weights, every row), batch 1, fp16 x, %.1f s "
+                      "of CPU time" % (passes, total_t)}
+
+
+def oracle_sample_isolated(budget_s=12.0, threads=None):
+    """oracle_sample() in a fresh Python process that imports neither torch nor
+    CUDA (the GPU arm's own process holds a CUDA context and host threads of
+    its own), after one second of warm-up: the same conditions as the
+    reference arm."""
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-sample", str(budget_s)]
+    if threads:
+        cmd += ["--oracle-threads", str(threads)]
+    r = subprocess.run(cmd, capture_output=True, text=True, check=True)
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def oracle_sample_main(budget_s, threads):
+    oracle_sample(budget_s=1.0, threads=threads)      # warm-up
+    r = oracle_sample(budget_s=budget_s, threads=threads)
+    r["sample"] += " (own process, after 1 s of warm-up)"
+    print(json.dumps(r), flush=True)
 
 
 LAYER_WEIGHT_BYTES = 122683392   # the seven Q4_K linears of one Llama-3-8B layer
@@ -263,11 +280,11 @@ def run_reference(args):
     rank, world, local, dist = dist_setup(args.gpus)
     if rank != 0:
         return
-    for _ in range(args.warmup):
-        oracle_sample(budget_s=1.0)
+    oracle_sample(budget_s=1.0)      # warm-up, as oracle_sample_isolated
     budget = max(5.0, min(20.0, 2.0 * args.steps / 10.0))
     t0 = time.time()
     r = oracle_sample(budget_s=budget)
+    r["sample"] += " (own process, after 1 s of warm-up)"
     wall = time.time() - t0
     # one step = one layer's weight bytes at the oracle's measured rate on the
     # sampled rows
@@ -321,6 +338,39 @@ def make_event(torch, external):
         except TypeError:
             return None
     return torch.cuda.Event(enable_timing=True)
+
+
+MIN_TIMED_MS = 200.0
+MIN_REPS = 5
+
+
+def timed_reps(torch, run, min_ms=MIN_TIMED_MS, min_reps=MIN_REPS):
+    """Device time (ms) of repeated calls of run(), each bracketed by a
+    synchronize and CUDA events on the current stream, until at least min_ms
+    of device time and min_reps repetitions have been timed."""
+    out = []
+    while sum(out) < min_ms or len(out) < min_reps:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record()
+        run()
+        b.record()
+        torch.cuda.synchronize()
+        out.append(a.elapsed_time(b))
+    return out
+
+
+def rep_stats(reps, K, wbytes):
+    """Median / p10 / p90 of the repetitions, per step and as weight GB/s."""
+    r = np.asarray(reps, dtype=np.float64)
+    med, p10, p90 = (float(np.median(r)), float(np.percentile(r, 10)),
+                     float(np.percentile(r, 90)))
+    return {"repetitions": len(reps), "steps_per_repetition": K,
+            "timed_ms_total": round(float(r.sum()), 2),
+            "ms_per_step_median": med / K, "ms_per_step_p10": p10 / K, "ms_per_step_p90": p90 / K,
+            "GBps_median": wbytes * K / (med / 1e3) / 1e9,
+            "GBps_p10_time": wbytes * K / (p10 / 1e3) / 1e9,
+            "GBps_p90_time": wbytes * K / (p90 / 1e3) / 1e9}
 
 
 def layer_graphs(torch, s, step, K):
@@ -377,29 +427,29 @@ def bench_layer(torch, dq, args, lin, with_e2e=True):
     graphs, rem = layer_graphs(torch, s, step, K)
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(torch.cuda.current_device()) as clk:
-        time.sleep(0.3)   # let the sampler start
-        for i in range(-(-args.warmup // LAYERS_PER_GRAPH)):
-            graphs[0].replay()
-        torch.cuda.synchronize()
-        t0 = time.time()
-        start.record()
+
+    def k_steps():
         for i in range(K // LAYERS_PER_GRAPH):
             graphs[0].replay()
         if rem is not None:
             rem.replay()
-        end.record()
+
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        time.sleep(0.3)   # let the sampler start
+        for i in range(max(1, args.warmup)):
+            k_steps()
         torch.cuda.synchronize()
+        t0 = time.time()
+        reps = timed_reps(torch, k_steps)
         t1 = time.time()
         time.sleep(0.1)
-    ms = start.elapsed_time(end)
+    ms = float(np.median(reps))
     del graphs, rem
     # the roofline's average launch duration: the timed region above (CUDA
     # events around it, on the stream that replays the graphs) over its launches
     kern_ms = ms / (K * nl)
-    kern_src = ("cuda events around the timed region / %d launches (back to back, as in the "
-                "value)" % (K * nl))
+    kern_src = ("cuda events around each repetition of the timed region (median of %d) / %d "
+                "launches (back to back, as in the value)" % (len(reps), K * nl))
     # for reference, timed region 2: the same steps with an event before and
     # after every launch (one graph per step, so that every event keeps its own
     # timestamp); events between launches serialise them and add their gaps
@@ -430,6 +480,7 @@ def bench_layer(torch, dq, args, lin, with_e2e=True):
     res = {"ms_per_step": ms / K, "weight_bytes": wbytes, "act_bytes": abytes,
            "value": wbytes * K / (ms / 1e3) / 1e9, "kern_ms": kern_ms, "kern_src": kern_src,
            "serialised_launch_ms": ser_ms,
+           "timing": rep_stats(reps, K, wbytes),
            "clocks": clk.summary(t0, t1), "launches": K * len(lin), "n_linears": nl}
     if not with_e2e:
         del Ws
@@ -452,29 +503,31 @@ def bench_layer(torch, dq, args, lin, with_e2e=True):
 
     egr, erem = layer_graphs(torch, s, e2e_step, K)
     torch.cuda.synchronize()
-    for i in range(-(-args.warmup // LAYERS_PER_GRAPH)):
-        egr[0].replay()
+
+    def e2e_k_steps():
+        for i in range(K // LAYERS_PER_GRAPH):
+            egr[0].replay()
+        if erem is not None:
+            erem.replay()
+
+    for i in range(max(1, args.warmup)):
+        e2e_k_steps()
     torch.cuda.synchronize()
-    start.record()
-    for i in range(K // LAYERS_PER_GRAPH):
-        egr[0].replay()
-    if erem is not None:
-        erem.replay()
-    end.record()
-    torch.cuda.synchronize()
-    ems = start.elapsed_time(end)
+    ereps = timed_reps(torch, e2e_k_steps)
+    ems = float(np.median(ereps))
     res["e2e"] = {"value": wbytes * K / (ems / 1e3) / 1e9, "unit": "GB/s",
                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                   "ms_per_step": ems / K,
+                  "timing": rep_stats(ereps, K, wbytes),
                   "note": "x uploaded from pinned host memory and y read back in every step, "
-                          "captured with the step's %d dq_qgemv calls, %d steps per graph"
-                          % (nl, LAYERS_PER_GRAPH)}
+                          "captured with the step's %d dq_qgemv calls, %d steps per graph; "
+                          "median of the repetitions" % (nl, LAYERS_PER_GRAPH)}
     del egr, erem, Ws
     torch.cuda.empty_cache()
     return res
 
 
-def time_gemv(torch, dq, fmt, Ws, N, K, x, y, reps=30):
+def time_gemv(torch, dq, fmt, Ws, N, K, x, y, reps=30, b2b_ms=20.0, with_b2b_reps=False):
     """Device time of one dq_qgemv launch, two ways, over the weight copies Ws
     (together larger than L2):
       isolated: each launch in its own CUDA graph between two events, the
@@ -517,14 +570,17 @@ def time_gemv(torch, dq, fmt, Ws, N, K, x, y, reps=30):
     for _ in range(3):
         gr.replay()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(20):
-        gr.replay()
-    e1.record()
-    torch.cuda.synchronize()
-    b2b = e0.elapsed_time(e1) * 1e3 / 160
+
+    def twenty():
+        for _ in range(20):
+            gr.replay()
+
+    # repetitions of 160 back-to-back launches: median per launch
+    b2b_reps = [r * 1e3 / 160 for r in timed_reps(torch, twenty, min_ms=b2b_ms, min_reps=5)]
+    b2b = float(np.median(b2b_reps))
     del gr
+    if with_b2b_reps:
+        return iso, b2b, b2b_reps
     return iso, b2b
 
 
@@ -534,7 +590,7 @@ def weight_copies(torch, W0, wb):
     return [W0] + [W0.clone() for _ in range(n - 1)]
 
 
-def bench_gemv_70b(torch, dq, reps=50):
+def bench_gemv_70b(torch, dq, reps=200):
     """The Llama-70B gate shape: batch-1 Q4_K 28672 x 8192 GEMV, 4 rotating copies."""
     g = synth.streams(synth.BASE_SEED + 2, 2)
     N, K = 28672, 8192
@@ -542,17 +598,23 @@ def bench_gemv_70b(torch, dq, reps=50):
     Ws = weight_copies(torch, torch.from_numpy(synth.quant_matrix(g[0], Q4_K, N, K)).cuda(), wb)
     x = torch.from_numpy(synth.activations(g[1], (1, K), 1)).cuda()
     y = torch.empty(1, N, dtype=torch.float32, device="cuda")
-    t, us_b2b = time_gemv(torch, dq, Q4_K, Ws, N, K, x, y, reps=reps)
+    t, us_b2b, b2b_reps = time_gemv(torch, dq, Q4_K, Ws, N, K, x, y, reps=reps, b2b_ms=100.0,
+                                    with_b2b_reps=True)
     del Ws
     torch.cuda.empty_cache()
     us = float(np.median(t))
     return {"shape": "28672x8192 Q4_K batch 1 fp16", "us_median": us,
             "us_p10": float(np.percentile(t, 10)), "us_p90": float(np.percentile(t, 90)),
             "weight_GBps": wb / (us / 1e6) / 1e9, "bytes": wb + K * 2 + N * 4,
-            "us_back_to_back": us_b2b, "weight_GBps_back_to_back": wb / (us_b2b / 1e6) / 1e9,
-            "note": "us_median: each launch in its own graph between two events (no host "
-                    "gap, no overlap with a previous GEMV); back_to_back: 160 launches in "
-                    "graphs of 8 (4 rotating weight copies, 528 MB > L2)"}
+            "us_back_to_back": us_b2b,
+            "us_back_to_back_p10": float(np.percentile(b2b_reps, 10)),
+            "us_back_to_back_p90": float(np.percentile(b2b_reps, 90)),
+            "back_to_back_repetitions": len(b2b_reps),
+            "weight_GBps_back_to_back": wb / (us_b2b / 1e6) / 1e9,
+            "note": "us_median: %d launches, each in its own graph between two events (no host "
+                    "gap, no overlap with a previous GEMV); back_to_back: repetitions of 160 "
+                    "launches in graphs of 8 (4 rotating weight copies, 528 MB > L2), median "
+                    "per launch" % len(t)}
 
 
 def bench_gemv_70b_formats(torch, dq, reps=30, fmts=((Q4_K, "q4_k"), (2, "q6_k"), (3, "q8_0")),
@@ -728,7 +790,13 @@ def run_ours(args):
     value = job_value(world, lay["weight_bytes"], ms)
     extra = {}
     if rank == 0:
-        extra["gemv_70b_gate_b1"] = bench_gemv_70b(torch, dq)
+        with ClockSampler(torch.cuda.current_device()) as clk70:
+            time.sleep(0.3)
+            t70 = time.time()
+            extra["gemv_70b_gate_b1"] = bench_gemv_70b(torch, dq)
+            t71 = time.time()
+            time.sleep(0.1)
+        extra["gemv_70b_gate_b1"]["clocks"] = clk70.summary(t70, t71)
         g70 = extra["gemv_70b_gate_b1"]
         g70["frac_of_hbm"] = g70["weight_GBps"] / peak
         g70["frac_of_hbm_back_to_back"] = g70["weight_GBps_back_to_back"] / peak
@@ -762,12 +830,29 @@ def run_ours(args):
             "ms_per_step": round(sep["ms_per_step"], 5),
             "note": "the same layer with q, k, v, gate, up as five separate matrices: "
                     "seven dq_qgemv launches per step"}
-        cpu = oracle_sample()
-        one = oracle_sample(budget_s=4.0, threads=1)
+        cpu = oracle_sample_isolated()
+        one = oracle_sample_isolated(budget_s=4.0, threads=1)
         cpu["value_1_thread"] = one["value"]
         cpu["sample_1_thread"] = one["sample"]
     if rank != 0:
         return
+    g70 = extra["gemv_70b_gate_b1"]
+    # the 70B-shaped batch-1 Q4_K gate GEMV against the >= 80 % bar of the
+    # measured copy bandwidth
+    north_star = {
+        "kernel": "qgemv_b1_kernel<Q4_K>", "shape": g70["shape"],
+        "weight_bytes": weight_bytes(Q4_K, 28672, 8192),
+        "us_single_launch_median": round(g70["us_median"], 2),
+        "us_single_launch_p10": round(g70["us_p10"], 2),
+        "us_single_launch_p90": round(g70["us_p90"], 2),
+        "frac_single_launch": round(g70["frac_of_hbm"], 4),
+        "us_back_to_back_median": round(g70["us_back_to_back"], 2),
+        "us_back_to_back_p10": round(g70["us_back_to_back_p10"], 2),
+        "us_back_to_back_p90": round(g70["us_back_to_back_p90"], 2),
+        "frac_back_to_back": round(g70["frac_of_hbm_back_to_back"], 4),
+        "bar": 0.80, "meets_bar_back_to_back": g70["frac_of_hbm_back_to_back"] >= 0.80,
+        "meets_bar_single_launch": g70["frac_of_hbm"] >= 0.80,
+        "peak": peak, "clocks": g70.get("clocks")}
     kern_bytes = (lay["weight_bytes"] + lay["act_bytes"]) / lay["n_linears"]
     achieved = kern_bytes / (lay["kern_ms"] / 1e3) / 1e9
     tr = _traffic_record("qgemv_b1_kernel<Q4_K>")
@@ -776,7 +861,8 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic",
-        "config": dict(layer_config(world), frac_of_hbm=round(value / world / peak, 4)),
+        "config": layer_config(world),
+        "frac_of_hbm": round(value / world / peak, 4),
         "roofline": {"bound": "hbm", "kernel": "qgemv_b1_kernel<Q4_K>",
                      "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": peak_src + " hbm_gbs (MEASURED_PEAKS.json)",
@@ -786,10 +872,12 @@ def run_ours(args):
                      "achieved_serialised": (round(kern_bytes / (lay["serialised_launch_ms"] / 1e3)
                                                    / 1e9, 1)
                                              if lay.get("serialised_launch_ms") else None),
-                     "alg_bytes_per_launch": kern_bytes},
+                     "alg_bytes_per_launch": kern_bytes,
+                     "north_star": north_star},
         "cpu_baseline": cpu,
         "e2e": lay["e2e"],
-        "gpu_launches": lay["launches"],
+        "gpu_launches": lay["launches"] * lay["timing"]["repetitions"],
+        "timing": lay["timing"],
         "clocks": lay["clocks"],
     }
     line.update(extra)
@@ -798,7 +886,9 @@ def run_ours(args):
 
 def main():
     args = parse()
-    if args.case:
+    if args.oracle_sample is not None:
+        oracle_sample_main(args.oracle_sample, args.oracle_threads)
+    elif args.case:
         run_case(args)
     elif args.impl == "reference":
         run_reference(args)

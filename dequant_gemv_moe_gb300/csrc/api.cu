@@ -165,6 +165,9 @@ int dq_moe_forward(const dq_moe_desc* desc, const void* x, int x_dtype, int T, f
   int rc = check_desc(desc, T);
   if (rc != DQ_OK) return rc;
   if (!x || !y || !dtype_ok(x_dtype)) return DQ_ERR_ARG;
+  // the experts run on 16-bit tensor-core operands: fp32 activations would
+  // be held to a bar (1e-5) that path cannot meet, so they are refused
+  if (x_dtype == DQ_F32) return DQ_ERR_UNSUPPORTED;
   if (!aligned(x, 16) || !aligned(y, 16)) return DQ_ERR_ALIGN;
   if ((topk_idx && !aligned(topk_idx, 4)) || (topk_gate && !aligned(topk_gate, 4)) ||
       (logits && !aligned(logits, 4)))
@@ -226,6 +229,7 @@ int dq_moe_forward_streamed(dq_expert_cache* cache, const void* x, int x_dtype, 
                             void* ws, size_t ws_bytes, void* stream, void* copy_stream) {
   if (!cache || !x || !y || !dtype_ok(x_dtype) || T <= 0 || T > cache->max_tokens)
     return DQ_ERR_ARG;
+  if (x_dtype == DQ_F32) return DQ_ERR_UNSUPPORTED;   // as dq_moe_forward
   if (stream == copy_stream) return DQ_ERR_ARG;
   if (!aligned(x, 16) || !aligned(y, 16)) return DQ_ERR_ALIGN;
   if (!ws) return DQ_ERR_WORKSPACE;

@@ -57,7 +57,12 @@ __device__ __forceinline__ void report_timeout() {
 }
 
 // A wait that polls longer than this many SM clock cycles (~1 s) gives up.
-constexpr long long kWaitLimitCycles = 2000000000LL;
+// DQ_WAIT_LIMIT_CYCLES overrides it for a test build only (the library is
+// always built with the default).
+#ifndef DQ_WAIT_LIMIT_CYCLES
+#define DQ_WAIT_LIMIT_CYCLES 2000000000LL
+#endif
+constexpr long long kWaitLimitCycles = DQ_WAIT_LIMIT_CYCLES;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);

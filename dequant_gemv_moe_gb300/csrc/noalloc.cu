@@ -28,17 +28,24 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device (nullptr on error).
-void* scratch_on_current_device() {
+// Device address of the scratch array on the current device.  The address is
+// looked up once per device; the lookup is a runtime call that must not run
+// while `stream` is being captured, so a first call under capture is refused
+// (DQ_ERR_UNSUPPORTED) instead of calling into the runtime mid-capture.
+int scratch_on_current_device(cudaStream_t stream, void** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DQ_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_mu);
   if (!g_scratch_ptr[dev]) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return DQ_ERR_CUDA;
+    if (cs != cudaStreamCaptureStatusNone) return DQ_ERR_UNSUPPORTED;
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return DQ_ERR_CUDA;
     g_scratch_ptr[dev] = p;
   }
-  return g_scratch_ptr[dev];
+  *out = g_scratch_ptr[dev];
+  return DQ_OK;
 }
 
 }  // namespace
@@ -53,8 +60,9 @@ extern "C" int dq_moe_forward_noalloc(const dq_moe_desc* desc, const void* x, in
   const int rc = dq_moe_workspace_size(desc, T, &need);
   if (rc != DQ_OK) return rc;
   if (need > (size_t)DQ_NOALLOC_SCRATCH_BYTES) return DQ_ERR_WORKSPACE;
-  void* ws = scratch_on_current_device();
-  if (!ws) return DQ_ERR_CUDA;
+  void* ws = nullptr;
+  const int src = scratch_on_current_device((cudaStream_t)stream, &ws);
+  if (src != DQ_OK) return src;
   return dq_moe_forward(desc, x, x_dtype, T, y, ws, (size_t)DQ_NOALLOC_SCRATCH_BYTES, topk_idx,
                         topk_gate, logits, stream);
 }

@@ -24,9 +24,13 @@
  *     returns (calls are asynchronous on `stream`; the caller keeps buffers
  *     alive until the stream has passed the call).
  *   - `stream` is a cudaStream_t passed as void*; NULL means the legacy default
- *     stream.  No entry point synchronises the stream or the device, and no
- *     entry point allocates device memory: scratch is passed in by the caller.
- *     So a sequence of calls can be captured in a CUDA graph.
+ *     stream.  No entry point synchronises the stream or the device (except
+ *     dq_moe_forward_streamed and dq_device_status, which say so), and no
+ *     entry point allocates device memory: scratch is passed in by the
+ *     caller.  The one exception is the library's own fixed scratch array of
+ *     DQ_NOALLOC_SCRATCH_BYTES that dq_moe_forward_noalloc uses: it is
+ *     resident on every GPU that loads the library, whether or not that entry
+ *     point is called.
  *   - Return value: DQ_OK (0) or a negative dq_status.  Arguments are checked
  *     before anything is launched: on an argument error nothing is enqueued.
  *     DQ_ERR_CUDA means a launch reported an error (cudaGetLastError); the
@@ -171,6 +175,12 @@ int dq_dequant(int fmt, const void* blocks, int64_t n_weights, float* out,
  * fp16/bf16 activations run on the tensor-core path (weights decoded to fp16
  * in registers); fp32 activations run on an fp32 CUDA-core path (decode and
  * products in fp32).
+ * Range of the 16-bit path: Q4_K, Q5_K, Q6_K, Q2_K and Q3_K rows, and Q8_0
+ * at batch 1, are decoded in per-row or per-sub-block power-of-two units and
+ * take any finite fp16 d and dmin.  Q8_0 and Q4_0 at batch 2..8 and NVFP4
+ * decode to absolute fp16 weights: every decoded weight |w| must stay below
+ * 65504 (Q8_0: |d| < 515; Q4_0: |d| < 8187; NVFP4 always holds, |w| <= 2688).
+ * Beyond that the output is inf or NaN; the call cannot detect it. 
  * Errors: DQ_ERR_ARG (null, N/K <= 0, K % 256 != 0 — every format is
  *         streamed in 256-weight units —, batch outside 1..8),
  *         DQ_ERR_ALIGN (W, x not 16-B aligned, y not 4-B aligned; rows must
@@ -230,7 +240,13 @@ typedef struct {
   int32_t ffn;        /* F: rows of W_gate / W_up, columns of W_down */
   int32_t n_shared;   /* always-on shared experts, 0..4, weight 1 each */
   int32_t fmt;        /* dq_fmt of every expert matrix: DQ_Q4_K, DQ_Q6_K,
-                         DQ_Q8_0 or DQ_NVFP4 (others: DQ_ERR_UNSUPPORTED) */
+                         DQ_Q8_0 or DQ_NVFP4 (others: DQ_ERR_UNSUPPORTED).
+                         Range: experts with more than 32 tokens in a call
+                         (the tensor-core GEMM) and Q8_0 experts on any path
+                         decode to absolute fp16 weights, which must stay
+                         below 65504 in magnitude (Q4_K: 945|d| + 63|dmin|,
+                         Q6_K: 32|d||s|, Q8_0: 127|d|); beyond that the
+                         output is inf or NaN, undetected. */
   const float* router_W; /* device fp32 [E][H] */
   const void* w_gate; /* device, E stacked [F rows][H/QK blocks] matrices */
   const void* w_up;   /* device, E stacked [F][H/QK] */
@@ -269,7 +285,11 @@ int dq_moe_permute(const int32_t* topk_idx, int T, int top_k, int E,
 
 /* dq_moe_forward — the whole layer for T tokens (router, top-k, permute,
  * grouped gate/up with SwiGLU, grouped down, weighted combine + shared).
- *   x        : device [T][H] of x_dtype, 16-byte aligned.
+ *   x        : device [T][H] of x_dtype, 16-byte aligned; x_dtype DQ_F16 or
+ *              DQ_BF16.  The experts multiply 16-bit tensor-core operands,
+ *              which cannot meet the 1e-5 relative bar fp32 activations are
+ *              held to, so DQ_F32 is refused (DQ_ERR_UNSUPPORTED); a caller
+ *              with fp32 activations rounds them to bf16 first.
  *   y        : device fp32 [T][H], fully overwritten.
  *   ws       : device scratch of at least dq_moe_workspace_size bytes,
  *              256-byte aligned; contents on entry are ignored.
@@ -278,8 +298,8 @@ int dq_moe_permute(const int32_t* topk_idx, int T, int top_k, int E,
  * All launches go on `stream` with no host synchronisation, so the layer is
  * capturable in one CUDA graph ([KTransformers, §技术原理]: one graph call
  * per decode step).
- * Errors: DQ_ERR_ARG, DQ_ERR_ALIGN, DQ_ERR_UNSUPPORTED, DQ_ERR_WORKSPACE,
- *         DQ_ERR_CUDA. */
+ * Errors: DQ_ERR_ARG, DQ_ERR_ALIGN, DQ_ERR_UNSUPPORTED (also fp32 x),
+ *         DQ_ERR_WORKSPACE, DQ_ERR_CUDA. */
 int dq_moe_forward(const dq_moe_desc* desc, const void* x, int x_dtype, int T,
                    float* y, void* ws, size_t ws_bytes, int32_t* topk_idx,
                    float* topk_gate, float* logits, void* stream);
@@ -295,13 +315,15 @@ int dq_moe_forward(const dq_moe_desc* desc, const void* x, int x_dtype, int T,
  * device memory until the process exits.  No call allocates or frees memory.
  * The first call on a device (with that device current) looks up the array's
  * device address once (cudaGetSymbolAddress); make that first call before any
- * stream capture.  All calls on a device share the one array and each call
+ * stream capture: a first call made while `stream` is capturing is refused
+ * with DQ_ERR_UNSUPPORTED before anything is looked up or enqueued.  All calls on a device share the one array and each call
  * overwrites it, so calls that may overlap on the GPU (different streams
  * without ordering) race: order them.  Nothing needs to be zero on entry.
  * Arguments and outputs as dq_moe_forward (without ws / ws_bytes).
  * Errors: as dq_moe_forward; DQ_ERR_WORKSPACE when
  * dq_moe_workspace_size(desc, T) exceeds DQ_NOALLOC_SCRATCH_BYTES (decode-
  * sized T fits: e.g. 8 tokens of the 256-expert layer, 16 of the 8-expert one);
+ * DQ_ERR_UNSUPPORTED for a first call on a device under stream capture;
  * DQ_ERR_CUDA if the array's address cannot be obtained. */
 #define DQ_NOALLOC_SCRATCH_BYTES (32u << 20)
 int dq_moe_forward_noalloc(const dq_moe_desc* desc, const void* x, int x_dtype, int T,
@@ -359,7 +381,8 @@ int dq_expert_cache_workspace_size(const dq_expert_cache* cache, int T, size_t* 
  *   stream       : compute stream; copy_stream: the copies (a different
  *                  stream; NULL is the legacy default stream).
  * Returns once the work is enqueued (after the routing read-back).
- * Errors: DQ_ERR_ARG, DQ_ERR_ALIGN, DQ_ERR_WORKSPACE, DQ_ERR_CUDA. */
+ * Errors: DQ_ERR_ARG, DQ_ERR_ALIGN, DQ_ERR_UNSUPPORTED (fp32 x, as
+ *         dq_moe_forward), DQ_ERR_WORKSPACE, DQ_ERR_CUDA. */
 int dq_moe_forward_streamed(dq_expert_cache* cache, const void* x, int x_dtype, int T, float* y,
                             void* ws, size_t ws_bytes, void* stream, void* copy_stream);
 

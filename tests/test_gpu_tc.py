@@ -16,7 +16,7 @@ pytestmark = pytest.mark.gpu
     (Q4_K, 1, 1, 256, 256, 0, 33, 1),       # one unit of 33 tokens: N = 48, 2 boxes
     (Q4_K, 1, 1, 512, 512, 1, 40, 2),       # shared expert too; 4 row tiles
     (Q8_0, 1, 1, 256, 256, 0, 130, 1),      # > 128 tokens: two units (128 + 2)
-    (Q6_K, 1, 1, 2048, 2048, 0, 64, 0),     # Q6_K rows, fp32 activations
+    (Q6_K, 1, 1, 2048, 2048, 0, 64, 2),     # Q6_K rows, bf16 activations
     (NVFP4, 1, 1, 512, 256, 1, 150, 2),     # NVFP4 rows: two units, shared expert
 ])
 def test_tc_wide_units(dq, orc, fmt, E, k, H, F, ns, T, xdt):

@@ -603,3 +603,21 @@ def test_moe_single_expert_is_plain_ffn(orc):
     o = orc.expert_ffn(fmt, w["w_gate"], w["w_up"], w["w_down"], H, F,
                        orc.act_to_f64(1, x).ravel())
     np.testing.assert_array_equal(y[0], o.astype(np.float32))
+
+
+def test_ref_under_selection_reproduces_the_layer(orc):
+    # the parity tests' reference for a near-tie token (the oracle's expert
+    # FFNs and gates under a given selection) equals the oracle's layer when
+    # given the oracle's own selection, and differs under another one
+    from moe_layers import ref_under_selection
+    E, k, H, F, ns, T, fmt, xdt = 8, 2, 256, 512, 1, 4, 1, 1
+    w = synth.moe_weights(4100, E, H, F, ns, fmt)
+    x = synth.activations(synth.streams(4101, 1)[0], (T, H), xdt)
+    y, idx, gate, L = orc.moe_forward(fmt, E, k, H, F, ns, w["router_W"], w["w_gate"], w["w_up"],
+                                      w["w_down"], w["sh_gate"], w["sh_up"], w["sh_down"], x, xdt, T)
+    for t in range(T):
+        r = ref_under_selection(orc, fmt, w, E, k, H, F, ns, x, xdt, t, idx[t], L)
+        np.testing.assert_allclose(r, y[t], rtol=1e-6, atol=1e-6 * np.abs(y[t]).max())
+        other = np.array([e for e in range(E) if e not in idx[t]][:k])
+        r2 = ref_under_selection(orc, fmt, w, E, k, H, F, ns, x, xdt, t, other, L)
+        assert np.abs(r2 - y[t]).max() > 1e-3 * np.abs(y[t]).max()
