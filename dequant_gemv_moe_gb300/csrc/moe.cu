@@ -55,6 +55,11 @@ MoePlan moe_plan(const dq_moe_desc& d, int T, bool allow_wide) {
   // experts with more than kWide tokens go to the tensor-core GEMM in units of
   // <= 128 tokens: at most P/(kWide+1) such experts
   p.wide = allow_wide && T > kWide;
+  // one-token groups on the block-diagonal kernel when most touched experts
+  // see one token: every expert at T = 1, and while the picks are at most
+  // half the experts (DeepSeek-V3 shapes up to T = 16)
+  p.single = allow_wide && grouped_b1_supported(d.fmt) && (T == 1 || 2 * p.P <= d.E);
+  p.G1_max = p.single ? (int)std::min<int64_t>(d.E, p.P) + (T == 1 ? d.n_shared : 0) : 0;
   p.U_max = p.wide ? (int)(p.P / 128 + p.P / (kWide + 1) + 1 +
                            (int64_t)d.n_shared * ((T + 127) / 128))
                    : 0;
@@ -83,6 +88,8 @@ MoePlan moe_plan(const dq_moe_desc& d, int T, bool allow_wide) {
   p.off_xinv = o;    o = align256(o + npw * 4);
   p.off_g = o;       o = align256(o + npw * d.ffn * 4);
   p.off_u = o;       o = align256(o + npw * d.ffn * 4);
+  p.off_g1 = o;      o = align256(o + (size_t)std::max(p.G1_max, 1) * 16);
+  p.off_ng1 = o;     o = align256(o + 16);   // count, two work counters
   p.total = o;
   return p;
 }
@@ -200,7 +207,88 @@ __device__ __forceinline__ bool better(float a, int ia, float b, int ib) {
   return a > b || (a == b && ia < ib);
 }
 
-// Top-k of token t by one warp (lane: this thread's lane).
+// A float's bits as an unsigned key with the float's order (not NaN), and
+// back.
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float order_key_inv(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Compare-exchange of (value, index) pairs a, b into descending order.
+__device__ __forceinline__ void cas_desc(float& va, int& ia, float& vb, int& ib) {
+  if (better(vb, ib, va, ia)) {
+    const float tv = va;
+    const int ti = ia;
+    va = vb;
+    ia = ib;
+    vb = tv;
+    ib = ti;
+  }
+}
+
+// Selection of token t by one warp from its logits v (lane holds experts
+// lane + 32 j, j < 8; -inf / 0x7fffffff past E): each lane first sorts its 8
+// candidates (descending logit, lowest expert index first on ties) with a
+// sorting network, then k rounds take the best of the 32 lanes' heads (two
+// warp reductions) and advance the winning lane's head.  Lanes i < k compute the gate
+// of slot i (softmax over all E renormalised over the selection) and write
+// the index and the gate, and the index to sidx (nullable, shared memory).
+__device__ __forceinline__ void topk_select(float (&v)[8], int (&id)[8], int k, int t, int lane,
+                                            int32_t* __restrict__ idx, float* __restrict__ gate,
+                                            int* sidx) {
+  // Batcher's odd-even merge sort of 8 (19 compare-exchanges)
+#define DQ_CAS(a, b) cas_desc(v[a], id[a], v[b], id[b])
+  DQ_CAS(0, 1); DQ_CAS(2, 3); DQ_CAS(4, 5); DQ_CAS(6, 7);
+  DQ_CAS(0, 2); DQ_CAS(1, 3); DQ_CAS(4, 6); DQ_CAS(5, 7);
+  DQ_CAS(1, 2); DQ_CAS(5, 6);
+  DQ_CAS(0, 4); DQ_CAS(1, 5); DQ_CAS(2, 6); DQ_CAS(3, 7);
+  DQ_CAS(2, 4); DQ_CAS(3, 5);
+  DQ_CAS(1, 2); DQ_CAS(3, 4); DQ_CAS(5, 6);
+#undef DQ_CAS
+  float my_v = -INFINITY, top = -INFINITY;
+  int my_i = 0;
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    if (r >= k) break;
+    // the best head: the largest logit (as an order-preserving key), then the
+    // lowest expert index among the heads holding it (a lane's equal logits
+    // are in index order, so the lowest such index is a head)
+    const uint32_t key = order_key(v[0]);
+    const uint32_t mk = __reduce_max_sync(0xffffffffu, key);
+    const int bi = (int)__reduce_min_sync(0xffffffffu, key == mk ? (uint32_t)id[0] : 0xffffffffu);
+    const float bv = order_key_inv(mk);
+    if (r == 0) top = bv;
+    if (lane == r) {
+      my_v = bv;
+      my_i = bi;
+    }
+    if (id[0] == bi) {   // the winning lane's next candidate moves up
+#pragma unroll
+      for (int j = 0; j < 7; ++j) {
+        v[j] = v[j + 1];
+        id[j] = id[j + 1];
+      }
+      v[7] = -INFINITY;
+      id[7] = 0x7fffffff;
+    }
+  }
+  // softmax over all E renormalised over the selection
+  const float ex = lane < k ? expf(my_v - top) : 0.f;
+  float z = ex;
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+  if (lane < k) {
+    idx[(int64_t)t * k + lane] = my_i;
+    gate[(int64_t)t * k + lane] = ex / z;
+    if (sidx) sidx[t * k + lane] = my_i;
+  }
+}
+
+// Top-k of token t by one warp (lane: this thread's lane) from the router's
+// KS partial sums.
 __device__ __forceinline__ void topk_warp(const float* __restrict__ part, int KS, int T, int E,
                                           int k, int t, int lane, float* __restrict__ logits,
                                           int32_t* __restrict__ idx, float* __restrict__ gate) {
@@ -233,52 +321,7 @@ __device__ __forceinline__ void topk_warp(const float* __restrict__ part, int KS
       id[j] = 0x7fffffff;
     }
   }
-  float sv[8];
-  int si[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {             // k <= 8 rounds, registers only
-    sv[i] = -INFINITY;
-    si[i] = 0;
-    if (i >= k) continue;
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (better(v[j], id[j], bv, bi)) {
-        bv = v[j];
-        bi = id[j];
-      }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (better(ov, oi, bv, bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    sv[i] = bv;
-    si[i] = bi;
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (id[j] == bi) {   // remove the winner from further rounds
-        v[j] = -INFINITY;
-        id[j] = 0x7fffffff;
-      }
-  }
-  if (lane == 0) {
-    // softmax over all E renormalised over the selection
-    float z = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (i < k) z += expf(sv[i] - sv[0]);
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (i < k) {
-        idx[(int64_t)t * k + i] = si[i];
-        gate[(int64_t)t * k + i] = expf(sv[i] - sv[0]) / z;
-      }
-  }
+  topk_select(v, id, k, t, lane, idx, gate, nullptr);
 }
 
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ part, int KS, int T,
@@ -317,6 +360,42 @@ __device__ __forceinline__ int block_scan256(int v, int* wsum, int* total) {
   __syncthreads();   // wsum may be reused by the next call
   *total = all;
   return tid < 256 ? before + inc - v : 0;
+}
+
+// The same for three values at once (one pair of barriers).
+__device__ __forceinline__ int3 block_scan256x3(int3 v, int3* wsum3, int3* total) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int3 inc = tid < 256 ? v : make_int3(0, 0, 0);
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int nx = __shfl_up_sync(0xffffffffu, inc.x, o);
+    const int ny = __shfl_up_sync(0xffffffffu, inc.y, o);
+    const int nz = __shfl_up_sync(0xffffffffu, inc.z, o);
+    if (lane >= o) {
+      inc.x += nx;
+      inc.y += ny;
+      inc.z += nz;
+    }
+  }
+  if (tid < 256 && lane == 31) wsum3[warp] = inc;
+  __syncthreads();
+  int3 before = make_int3(0, 0, 0), all = make_int3(0, 0, 0);
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const int3 c = wsum3[w];
+    if (w < warp) {
+      before.x += c.x;
+      before.y += c.y;
+      before.z += c.z;
+    }
+    all.x += c.x;
+    all.y += c.y;
+    all.z += c.z;
+  }
+  __syncthreads();   // wsum3 may be reused by the next call
+  *total = all;
+  if (tid >= 256) return make_int3(0, 0, 0);
+  return make_int3(before.x + inc.x - v.x, before.y + inc.y - v.y, before.z + inc.z - v.z);
 }
 
 // Few tokens: the permute CTA also converts x to fp16 with a power-of-two
@@ -373,29 +452,66 @@ __global__ void __launch_bounds__(1024) permute_kernel(int32_t* idx, int T,
                                                        int32_t* __restrict__ n_units,
                                                        const void* __restrict__ cx, int cxdt,
                                                        int cK, __half* __restrict__ cx16,
-                                                       float* __restrict__ cxinv, TopkIn tk) {
+                                                       float* __restrict__ cxinv, TopkIn tk,
+                                                       int4* __restrict__ groups1,
+                                                       int32_t* __restrict__ n_groups1) {
   pdl_wait();
   pdl_trigger();
   __shared__ float red[32];
   __shared__ int wsum[8];
-  if (tk.part) {
-    if ((int)(threadIdx.x >> 5) < T)
-      topk_warp(tk.part, tk.KS, T, E, k, threadIdx.x >> 5, threadIdx.x & 31, tk.logits, idx,
-                tk.gate);
-    __syncthreads();
-  }
-  if (cx16) x16_rows_cta(cx, cxdt, T, cK, cx16, cxinv, red);
+  __shared__ int3 wsum3[8];
   __shared__ int cnt[256];
   __shared__ int off[257];
   __shared__ int run[256];
-  __shared__ int cntw[32][256];
+  __shared__ int cntw[32][256];   // per-warp counts; first the top-k's logits [T][E]
   __shared__ int gsc[257];
   __shared__ int usc[257];
+  __shared__ int osc[257];
+  __shared__ int sidx[256];       // the top-k's indices (T * k <= 256)
+  __shared__ int stok[256];       // the token of an expert's pair, for experts with one pair
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int P = T * k;
+  const bool own = tk.part != nullptr;   // the indices are chosen here: read them from sidx
+  if (own) {
+    // logits of the T <= 32 tokens: every thread sums the KS partials of its
+    // (token, expert) entries in a fixed order (q ascending), all loads in
+    // flight together; then one warp per token selects from shared memory
+    float* lg = (float*)&cntw[0][0];
+    const int n = T * E;
+    const int64_t qstride = (int64_t)T * E;
+    for (int i = tid; i < n; i += 1024) {
+      const float* pp = tk.part + i;
+      float v = 0.f;
+      for (int q0 = 0; q0 < tk.KS; q0 += 8) {
+        float a[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          a[j] = q0 + j < tk.KS ? __ldcg(pp + (q0 + j) * qstride) : 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (q0 + j < tk.KS) v += a[j];
+      }
+      lg[i] = v;
+      if (tk.logits) tk.logits[i] = v;
+    }
+    __syncthreads();
+    if (warp < T) {
+      float v[8];
+      int id[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int e = lane + 32 * j;
+        id[j] = e < E ? e : 0x7fffffff;
+        v[j] = e < E ? lg[warp * E + e] : -INFINITY;
+      }
+      topk_select(v, id, k, warp, lane, idx, tk.gate, sidx);
+    }
+    __syncthreads();
+  }
+  if (cx16) x16_rows_cta(cx, cxdt, T, cK, cx16, cxinv, red);
   if (tid < 256) cnt[tid] = 0;
   __syncthreads();
-  for (int p = tid; p < P; p += 1024) atomicAdd(&cnt[__ldcg(idx + p)], 1);
+  for (int p = tid; p < P; p += 1024) atomicAdd(&cnt[own ? sidx[p] : __ldcg(idx + p)], 1);
   __syncthreads();
   // exclusive scan of counts (E <= 256)
   {
@@ -411,17 +527,18 @@ __global__ void __launch_bounds__(1024) permute_kernel(int32_t* idx, int T,
   // stable scatter, 1024 pairs per round: rank inside the warp by match_any,
   // warps ordered through per-warp counts
   for (int base = 0; base < P; base += 1024) {
-    for (int i = tid; i < 32 * 256; i += 1024) (&cntw[0][0])[i] = 0;
+    const int nw = min(32, (P - base + 31) >> 5);   // warps holding pairs this round
+    for (int i = tid; i < nw * 256; i += 1024) (&cntw[0][0])[i] = 0;
     __syncthreads();
     const int p = base + tid;
-    const int e = (p < P) ? __ldcg(idx + p) : 256;
+    const int e = (p < P) ? (own ? sidx[p] : __ldcg(idx + p)) : 256;
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     const int rank = __popc(peers & ((1u << lane) - 1u));
     if (p < P && rank == 0) cntw[warp][e] = __popc(peers);
     __syncthreads();
     if (tid < E) {
       int s = run[tid];
-      for (int w = 0; w < 32; ++w) {
+      for (int w = 0; w < nw; ++w) {
         const int c = cntw[w][tid];
         cntw[w][tid] = s;
         s += c;
@@ -434,6 +551,7 @@ __global__ void __launch_bounds__(1024) permute_kernel(int32_t* idx, int T,
       sorted[pos] = p;
       if (inv) inv[p] = pos;
       if (tok) tok[pos] = p / k;
+      if (cnt[e] == 1) stok[e] = p / k;
     }
     __syncthreads();
   }
@@ -443,20 +561,28 @@ __global__ void __launch_bounds__(1024) permute_kernel(int32_t* idx, int T,
   // narrow groups of <= gw columns per expert (experts with <= kWide tokens),
   // wide units of <= 128 columns (more tokens); experts in order, then the
   // shared experts (all T tokens)
+  // with groups1, experts that received exactly one pair form the one-token
+  // list instead (expert, position, token), and so do the shared experts at
+  // T = 1
   const bool wide_ok = units != nullptr;
+  const bool one_ok = groups1 != nullptr;
   {
     const int n = (tid < E) ? cnt[tid] : 0;
     const bool w = wide_ok && n > kWide;
-    int gtot, utot;
-    const int gex = block_scan256(w ? 0 : (n + gw - 1) / gw, wsum, &gtot);
-    const int uex = block_scan256(w ? (n + 127) / 128 : 0, wsum, &utot);
+    const bool one = one_ok && n == 1;
+    int3 tot;
+    const int3 ex = block_scan256x3(
+        make_int3((w || one) ? 0 : (n + gw - 1) / gw, w ? (n + 127) / 128 : 0, one ? 1 : 0),
+        wsum3, &tot);
     if (tid < 256) {
-      gsc[tid] = gex;
-      usc[tid] = uex;
+      gsc[tid] = ex.x;
+      usc[tid] = ex.y;
+      osc[tid] = ex.z;
     }
     if (tid == 0) {
-      gsc[256] = gtot;
-      usc[256] = utot;
+      gsc[256] = tot.x;
+      usc[256] = tot.y;
+      osc[256] = tot.z;
     }
     __syncthreads();
   }
@@ -465,24 +591,34 @@ __global__ void __launch_bounds__(1024) permute_kernel(int32_t* idx, int T,
     if (wide_ok && n > kWide) {
       for (int j = 0; j * 128 < n; ++j)
         units[usc[tid] + j] = make_int4(tid, off[tid] + 128 * j, min(128, n - 128 * j), 0);
+    } else if (one_ok && n == 1) {
+      // the pair's token (recorded by the scatter above)
+      groups1[osc[tid]] = make_int4(tid, off[tid], stok[tid], 0);
     } else {
       for (int j = 0; j * gw < n; ++j)
         groups[gsc[tid] + j] = make_int4(tid, off[tid] + gw * j, min(gw, n - gw * j), 0);
     }
   }
-  const int nr = gsc[E], ur = usc[E];
+  const int nr = gsc[E], ur = usc[E], orr = osc[E];
+  const bool sh_one = one_ok && T == 1;
   const bool sh_wide = wide_ok && T > kWide;
   const int per = sh_wide ? (T + 127) / 128 : (T + gw - 1) / gw;
   const int width = sh_wide ? 128 : gw;
   for (int i = tid; i < n_shared * per; i += 1024) {
     const int s = i / per, j = i % per;
     const int4 g = make_int4(E + s, P + s * T + width * j, min(width, T - width * j), 0);
-    if (sh_wide) units[ur + i] = g;
+    if (sh_one) groups1[orr + s] = make_int4(E + s, P + s, 0, 0);
+    else if (sh_wide) units[ur + i] = g;
     else groups[nr + i] = g;
   }
   if (tid == 0) {
-    *n_groups = nr + (sh_wide ? 0 : n_shared * per);
+    *n_groups = nr + ((sh_wide || sh_one) ? 0 : n_shared * per);
     if (wide_ok) *n_units = ur + (sh_wide ? n_shared * per : 0);
+    if (one_ok) {
+      n_groups1[0] = orr + (sh_one ? n_shared : 0);
+      n_groups1[1] = 0;   // the one-token kernels' work counters
+      n_groups1[2] = 0;
+    }
   }
 }
 
@@ -894,7 +1030,7 @@ int launch_permute(const int32_t* idx, int T, int k, int E, int32_t* offsets, in
                    cudaStream_t s) {
   launch_pdl(permute_kernel, dim3(1), dim3(1024), 0, s, 0, const_cast<int32_t*>(idx), T, k, E, 0,
              8, offsets, sorted, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, 0,
-             0, nullptr, nullptr, TopkIn{nullptr, 0, nullptr, nullptr});
+             0, nullptr, nullptr, TopkIn{nullptr, 0, nullptr, nullptr}, nullptr, nullptr);
   return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
 }
 
@@ -932,14 +1068,21 @@ int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, floa
   int32_t* nunits = (int32_t*)(w + pl.off_nunits);
   __half* x16t = (__half*)(w + pl.off_x16t);
   float* xinvt = (float*)(w + pl.off_xinvt);
+  // one-token groups (pl.single) go to the block-diagonal kernels, which read
+  // x and h as they are; the grouped mma.sync kernels and their fp16 copies
+  // of x and h are needed only where a group can hold more tokens (T > 1)
+  int4* groups1 = (int4*)(w + pl.off_g1);
+  int32_t* ng1 = (int32_t*)(w + pl.off_ng1);
+  const bool general = !pl.single || T > 1;
   // one or two tokens of bf16/fp32 x: the permute CTA also makes their fp16
   // copy (measured: one launch less at T=1; at T=8 eight CTAs are faster)
-  const bool fuse_x16 = xdt != DQ_F16 && T <= 2 && d.hidden <= 8192;
+  const bool fuse_x16 = general && xdt != DQ_F16 && T <= 2 && d.hidden <= 8192;
   launch_pdl(permute_kernel, dim3(1), dim3(1024), 0, s, 0, idx, T, d.top_k, d.E, d.n_shared,
              pl.GW, offsets, sorted, inv, tok, groups, ngroups, pl.wide ? units : nullptr, nunits,
              fuse_x16 ? x : nullptr, xdt, d.hidden, fuse_x16 ? x16t : nullptr,
              fuse_x16 ? xinvt : nullptr,
-             fuse_topk ? TopkIn{part, pl.KS, lg, gate} : TopkIn{nullptr, 0, nullptr, nullptr});
+             fuse_topk ? TopkIn{part, pl.KS, lg, gate} : TopkIn{nullptr, 0, nullptr, nullptr},
+             pl.single ? groups1 : nullptr, pl.single ? ng1 : nullptr);
   if (cudaGetLastError() != cudaSuccess) return DQ_ERR_CUDA;
 
   const int q = qk(d.fmt), bb = blk_bytes(d.fmt);
@@ -953,7 +1096,7 @@ int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, floa
   // fp16 activations for the streaming kernels (fp16 input is used as is)
   const __half* xh = (const __half*)x;
   const float* xh_inv = nullptr;
-  if (xdt != DQ_F16) {
+  if (xdt != DQ_F16 && general) {
     if (!fuse_x16) {
       rc = launch_x16_rows(x, xdt, T, d.hidden, x16t, xinvt, s);
       if (rc != DQ_OK) return rc;
@@ -985,8 +1128,15 @@ int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, floa
   gu.tiles = d.ffn / 32;
   gu.rows_per_expert = d.ffn;
   if (!ms) {
-    rc = launch_grouped_fmt<true>(d.fmt, pl.NT, gu, pl.G_max * gu.tiles, s, d.E, d.n_shared);
-    if (rc != DQ_OK) return rc;
+    if (general) {
+      rc = launch_grouped_fmt<true>(d.fmt, pl.NT, gu, pl.G_max * gu.tiles, s, d.E, d.n_shared);
+      if (rc != DQ_OK) return rc;
+    }
+    if (pl.single) {
+      rc = launch_grouped_b1(true, d, groups1, ng1, pl.G1_max, ng1 + 1, x, xdt, d.hidden, h,
+                             d.ffn, s);
+      if (rc != DQ_OK) return rc;
+    }
   } else {
     // streamed: routed matrices from the slot cache, one launch per phase
     // once that phase's copies have landed
@@ -1018,9 +1168,12 @@ int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, floa
     if (rc != DQ_OK) return rc;
   }
 
-  // h -> fp16 with a power-of-two scale per position (all positions)
-  rc = launch_x16_rows(h, DQ_F32, (int)pl.NP, d.ffn, h16, hinv, s);
-  if (rc != DQ_OK) return rc;
+  // h -> fp16 with a power-of-two scale per position (all positions), for
+  // the grouped mma.sync kernels
+  if (general) {
+    rc = launch_x16_rows(h, DQ_F32, (int)pl.NP, d.ffn, h16, hinv, s);
+    if (rc != DQ_OK) return rc;
+  }
 
   GroupedParams dn;
   memset(&dn, 0, sizeof(dn));
@@ -1043,8 +1196,15 @@ int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, floa
   dn.tiles = d.hidden / 64;
   dn.rows_per_expert = d.hidden;
   if (!ms) {
-    rc = launch_grouped_fmt<false>(d.fmt, pl.NT, dn, pl.G_max * dn.tiles, s, d.E, d.n_shared);
-    if (rc != DQ_OK) return rc;
+    if (general) {
+      rc = launch_grouped_fmt<false>(d.fmt, pl.NT, dn, pl.G_max * dn.tiles, s, d.E, d.n_shared);
+      if (rc != DQ_OK) return rc;
+    }
+    if (pl.single) {
+      rc = launch_grouped_b1(false, d, groups1, ng1, pl.G1_max, ng1 + 2, h, DQ_F32, d.ffn, ypos,
+                             d.hidden, s);
+      if (rc != DQ_OK) return rc;
+    }
   } else {
     dn.Wa = (const uint8_t*)ms->slot_down;
     dn.slot_of = ms->slot_of;

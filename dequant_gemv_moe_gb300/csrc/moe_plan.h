@@ -19,9 +19,11 @@ struct MoePlan {
   int G_max;        // upper bound of narrow work groups (<= GW columns, mma.sync path)
   int U_max;        // upper bound of wide units (<= 128 columns, tcgen05 path)
   bool wide;        // wide units are possible (some expert may get > 32 tokens)
+  bool single;      // one-token groups run on the block-diagonal kernel (moe_b1.cu)
+  int G1_max;       // upper bound of one-token groups
   size_t off_part, off_logits, off_idx, off_gate, off_offsets, off_sorted, off_inv, off_tok,
       off_groups, off_ngroups, off_h, off_ypos, off_units, off_nunits, off_x16t, off_xinvt,
-      off_x16, off_xinv, off_g, off_u, off_h16, off_hinv, total;
+      off_x16, off_xinv, off_g, off_u, off_h16, off_hinv, off_g1, off_ng1, total;
 };
 
 // allow_wide = false keeps every expert on the grouped mma.sync kernel (the
@@ -43,6 +45,12 @@ struct MoeStream {
   const void* slot_down;
   int slots;
 };
+
+// The one-token expert kernels (moe_b1.cu).
+bool grouped_b1_supported(int fmt);
+int launch_grouped_b1(bool gateup, const dq_moe_desc& d, const int4* groups1,
+                      const int* n_groups1, int g1_max, int* claim, const void* x, int xdt,
+                      int64_t xstride, float* out, int64_t out_stride, cudaStream_t s);
 
 int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, float* y, void* ws,
                        int32_t* topk_idx, float* topk_gate, float* logits, cudaStream_t s,

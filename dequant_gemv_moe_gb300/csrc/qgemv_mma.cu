@@ -5,10 +5,15 @@
 // second pass and without scratch memory).
 #include <algorithm>
 
+#include "b1.cuh"
 #include "qgemv_mma.cuh"
 #include "tmap.h"
 
 namespace dqmoe {
+
+// stages of a CTA's weights prefetched into L2 before the wait when its K
+// range exceeds its ring (see early_weights)
+constexpr int kL2PrefetchStages = 2;
 
 struct GemvParams {
   CUtensorMap tmap;  // W as [N rows][row_bytes/2] 16-bit elements, box BOX x 64 rows
@@ -70,13 +75,19 @@ __global__ void __launch_bounds__(kThreads, PAIR ? 3 : 1)
     if (lane == 0) prefetch_tmap(&p.tmap);
     // weights are read-only inputs: with w_early their first stages stream in
     // while the previous kernel in the stream finishes
-    const int early = p.w_early ? min(plan.nstage, nchunk) : 0;
-    if (lane == 0)
+    const int early = p.w_early == 1 ? min(plan.nstage, nchunk) : 0;
+    if (lane == 0) {
       for (int c = 0; c < early; ++c) {
         const int64_t a = ((int64_t)(sb0 + c) * L::SBB) & ~(int64_t)15;
         mbar_arrive_expect_tx(&full[c], L::W_STAGE);
         tma_load_2d(wbuf + c * L::W_STAGE, &p.tmap, (int)(a >> 1), row0, &full[c], pol);
       }
+      // the range exceeds the ring: only its first stages, into L2
+      if (p.w_early == 2)
+        for (int c = 0; c < min(nchunk, kL2PrefetchStages); ++c)
+          tma_prefetch_l2_2d(&p.tmap, (int)((((int64_t)(sb0 + c) * L::SBB) & ~(int64_t)15) >> 1),
+                             row0);
+    }
     pdl_wait();
     bool ok = true;
     int s = 0;
@@ -227,35 +238,6 @@ __global__ void __launch_bounds__(kThreads, PAIR ? 3 : 1)
 // inverse scale.  The loader keeps the activation loads of the next
 // kB1Prefetch stages in flight in registers.
 // ---------------------------------------------------------------------------
-constexpr int kB1Prefetch = 4;
-
-struct B1Plan {
-  int nstage, off_w, off_x, off_sx, off_inv, off_z, off_red, total;
-};
-
-// Per stage: activations (Q4_K: x and -x of the odd sub-blocks; the others:
-// x) and the negated sums of its 8 (Q4_K, Q8_0) or 16 (Q6_K, Q2_K, Q3_K)
-// sub-blocks.
-template <int FMT>
-struct B1Fmt {
-  static constexpr int kStageX = FMT == DQ_Q4_K ? Q4KB1::kStageX : 512;
-  static constexpr int kSubs = (FMT == DQ_Q6_K || FMT == DQ_Q2_K || FMT == DQ_Q3_K) ? 16 : 8;
-};
-
-template <int FMT>
-__host__ __device__ inline B1Plan b1_plan(int nstage, int ksplit) {
-  B1Plan p;
-  p.nstage = nstage;
-  p.off_w = 1024;                                             // barriers below
-  p.off_x = p.off_w + nstage * Layout<FMT>::W_STAGE;          // 128-byte aligned
-  p.off_sx = p.off_x + nstage * B1Fmt<FMT>::kStageX;
-  p.off_inv = p.off_sx + nstage * 4 * B1Fmt<FMT>::kSubs;
-  p.off_z = (p.off_inv + nstage * 4 + 127) / 128 * 128;       // 16 zero bytes at +0
-  p.off_red = p.off_z + 128;
-  p.total = p.off_red + (ksplit > 1 ? (ksplit - 1) * kConsumerWarps * 32 * 16 : 0);
-  return p;
-}
-
 struct B1Params {
   CUtensorMap tmap;  // W as [N rows][row_bytes/2] 16-bit elements, box BOX x 64 rows
   int N;
@@ -306,12 +288,17 @@ __global__ void __launch_bounds__(kThreads, PAIR ? 3 : 4)
     tma_load_2d(wbuf + s * L::W_STAGE, &p.tmap,
                 (int)((((int64_t)(sb0 + c) * L::SBB) & ~(int64_t)15) >> 1), row0, &full[s], pol);
   };
-  const int early = p.w_early ? min(plan.nstage, nsbl) : 0;
+  const int early = p.w_early == 1 ? min(plan.nstage, nsbl) : 0;
   if (threadIdx.x == 0) {
     prefetch_tmap(&p.tmap);
     // weights are read-only: stream them in while the previous kernel ends
     // (and while the cluster forms)
     for (int c = 0; c < early; ++c) issue(c, c);
+    // the range exceeds the ring: only its first stages, into L2
+    if (p.w_early == 2)
+      for (int c = 0; c < min(nsbl, kL2PrefetchStages); ++c)
+        tma_prefetch_l2_2d(&p.tmap, (int)((((int64_t)(sb0 + c) * L::SBB) & ~(int64_t)15) >> 1),
+                           row0);
   }
   // the cluster's reduction barrier must be initialised before any peer
   // arrives on it, at the end of the kernel
@@ -321,11 +308,11 @@ __global__ void __launch_bounds__(kThreads, PAIR ? 3 : 4)
     // ------------------------------- loader --------------------------------
     pdl_wait();
     // lane covers activations 8*lane .. 8*lane+7 of a stage; sub-block = lane/4
-    const uint4* xsrc = (const uint4*)((const uint16_t*)p.x + (int64_t)sb0 * 256) + lane;
-    uint4 xr[kB1Prefetch];
+    constexpr int XDT = BF16 ? DQ_BF16 : DQ_F16;
+    B1X<XDT> xr[kB1Prefetch];
 #pragma unroll
     for (int u = 0; u < kB1Prefetch; ++u)
-      if (u < nsbl) xr[u] = __ldg(xsrc + 32 * u);
+      if (u < nsbl) xr[u] = b1_load_x<XDT>(p.x, sb0 + u, lane);
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
@@ -338,43 +325,11 @@ __global__ void __launch_bounds__(kThreads, PAIR ? 3 : 4)
           ok = __all_sync(0xffffffffu, mbar_wait(&empty[s], ph ^ 1));
         if (!ok || c >= nsbl) continue;
         if (lane == 0 && c >= early) issue(c, s);
-        uint32_t h[4] = {xr[u].x, xr[u].y, xr[u].z, xr[u].w};
-        if (c + kB1Prefetch < nsbl) xr[u] = __ldg(xsrc + 32 * (c + kB1Prefetch));
-        float inv = 1.f;
-        if constexpr (BF16) {
-          float amax = 0.f;
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(h[j] << 16)),
-                                     fabsf(__uint_as_float(h[j] & 0xFFFF0000u))));
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-          float scale;
-          pow2_scale(amax, scale, inv);
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            h[j] = h2_as_u32(__floats2half2_rn(__uint_as_float(h[j] << 16) * scale,
-                                               __uint_as_float(h[j] & 0xFFFF0000u) * scale));
-        }
-        uint8_t* xst = smem + plan.off_x + s * kStageX;
-        *(uint4*)(xst + 16 * lane) = make_uint4(h[0], h[1], h[2], h[3]);
-        if (FMT == DQ_Q4_K && (lane & 4))   // odd sub-block: its negation too
-          *(uint4*)(xst + 512 + 16 * lane) = make_uint4(h[0] ^ 0x80008000u, h[1] ^ 0x80008000u,
-                                                        h[2] ^ 0x80008000u, h[3] ^ 0x80008000u);
-        float sum = 0.f;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float2 f = __half22float2(u32_as_h2(h[j]));
-          sum += f.x;
-          sum += f.y;
-        }
-        // sub-blocks of 32 (4 lanes) or 16 (2 lanes) activations
-        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-        if (kSubs == 8) sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-        constexpr int lanes_per_sub = 32 / kSubs;
-        if ((lane & (lanes_per_sub - 1)) == 0)
-          ((float*)(smem + plan.off_sx + s * 4 * kSubs))[lane / lanes_per_sub] = -sum;
-        if (lane == 0) ((float*)(smem + plan.off_inv))[s] = inv;
+        const B1X<XDT> cur = xr[u];
+        if (c + kB1Prefetch < nsbl) xr[u] = b1_load_x<XDT>(p.x, sb0 + c + kB1Prefetch, lane);
+        b1_stage_x<FMT, XDT>(cur, smem + plan.off_x + s * kStageX,
+                             (float*)(smem + plan.off_sx + s * 4 * kSubs),
+                             (float*)(smem + plan.off_inv) + s, lane);
         mbar_arrive(&full[s]);
         if (++s == plan.nstage) {
           s = 0;
@@ -384,66 +339,15 @@ __global__ void __launch_bounds__(kThreads, PAIR ? 3 : 4)
     }
   } else {
     // ------------------------------ consumers ------------------------------
-    const int cw = warp - 1, g = lane >> 2, t = lane & 3;
-    // Q4_K: mma row g is weight row rg (and rg + 8) of the warp's 16: rows
-    // 0,2,4,6 in the first half-warp, 1,3,5,7 in the second, so that the
-    // 8-byte quant loads of a half-warp fall on 32 distinct banks (row pitch
-    // 144 bytes).  The 4-byte loads of Q6_K, Q2_K and Q3_K (pitches 240, 112,
-    // 144: rows 4 banks apart) are conflict-free as is.
-    const int rg = kSubs == 16 ? g : 2 * (g & 3) + (g >> 2);
-    // Q2_K / Q3_K: 2^24 times the power of two of run r = t's in-place field
-    const float f23 = FMT == DQ_Q2_K ? 16777216.f / (float)(1 << (2 * t))
-                                     : 16777216.f / (float)(1 << (t == 3 ? 5 : 2 * t));
-    const Q4KB1::Lane lc = Q4KB1::lane_consts(g, t);
-    uint32_t real6[8];
-#pragma unroll
-    for (int n = 0; n < 8; ++n) real6[n] = n == g ? 1u : 0u;
-    const uint32_t wrow = smem_u32(wbuf) + (16 * cw + rg) * L::ROW_PITCH;
-    const uint32_t xbase = smem_u32(smem + plan.off_x);
-    const uint32_t sxb = smem_u32(smem + plan.off_sx);
-    const uint32_t zb = smem_u32(smem + plan.off_z);
-    const float* invs = (const float*)(smem + plan.off_inv);
+    const int cw = warp - 1;
+    const B1Consumer<FMT, BF16, 8> cons(smem, plan, 16 * cw, lane);
     float2 accp0 = make_float2(0.f, 0.f), accp8 = make_float2(0.f, 0.f);
     float2 accq0 = make_float2(0.f, 0.f), accq8 = make_float2(0.f, 0.f);
     int s = 0;
     uint32_t ph = 0;
     // super-block c of this CTA sits in stage st
     auto stage = [&](int st, int c, uint32_t o, float2& a0, float2& a8) {
-      const float inv = BF16 ? invs[st] : 1.f;
-      if constexpr (FMT == DQ_Q4_K) {
-        Q4KB1::run(wrow + st * L::W_STAGE + o, 8 * L::ROW_PITCH,
-                   xbase + kStageX * st + 64 * g + 16 * t + o, zb, sxb + 4 * kSubs * st + 8 * t + o,
-                   inv, lc, a0, a8);
-      } else if constexpr (FMT == DQ_Q8_0) {
-        const uint32_t ra = wrow + st * L::W_STAGE + o;   // 272-byte super-blocks: aligned
-        Q80B1::run(ra, ra + 8 * L::ROW_PITCH, xbase + kStageX * st + 64 * g + 16 * t + o,
-                   zb + 64, zb, sxb + 4 * kSubs * st + 8 * t + o, inv, real6, t, a0, a8);
-      } else if constexpr (FMT == DQ_Q2_K) {
-        // 84-byte super-blocks: 4-byte aligned
-        const uint32_t ra = wrow + st * L::W_STAGE + (int)(((int64_t)(sb0 + c) * L::SBB) & 15) + o;
-        Q2KB1::run(ra, ra + 8 * L::ROW_PITCH, xbase + kStageX * st + o, zb,
-                   sxb + 4 * kSubs * st + o, inv, f23, real6, t, a0, a8);
-      } else if constexpr (FMT == DQ_Q3_K) {
-        // 110-byte super-blocks: 2-byte aligned, the offset uniform per stage
-        const int delta = (int)(((int64_t)(sb0 + c) * L::SBB) & 15);
-        const uint32_t ra = wrow + st * L::W_STAGE + delta + o;
-        if (delta & 2)
-          Q3KB1::run<true>(ra, ra + 8 * L::ROW_PITCH, xbase + kStageX * st + o, zb,
-                           sxb + 4 * kSubs * st + o, inv, f23, real6, t, a0, a8);
-        else
-          Q3KB1::run<false>(ra, ra + 8 * L::ROW_PITCH, xbase + kStageX * st + o, zb,
-                            sxb + 4 * kSubs * st + o, inv, f23, real6, t, a0, a8);
-      } else {
-        // the 210-byte super-block starts delta bytes into the 16-byte aligned box
-        const int delta = (int)(((int64_t)(sb0 + c) * L::SBB) & 15);
-        const uint32_t ra = wrow + st * L::W_STAGE + delta + o;
-        if (delta & 2)
-          Q6KB1::run<true>(ra, ra + 8 * L::ROW_PITCH, xbase + kStageX * st + o, zb,
-                           sxb + 4 * kSubs * st + o, inv, real6, t, a0, a8);
-        else
-          Q6KB1::run<false>(ra, ra + 8 * L::ROW_PITCH, xbase + kStageX * st + o, zb,
-                            sxb + 4 * kSubs * st + o, inv, real6, t, a0, a8);
-      }
+      cons.stage(st, (int64_t)sb0 + c, o, a0, a8);
     };
     auto advance = [&]() {
       if (++s == plan.nstage) {
@@ -483,12 +387,7 @@ __global__ void __launch_bounds__(kThreads, PAIR ? 3 : 4)
     }
     float acc0 = (accp0.x + accp0.y) + (accq0.x + accq0.y);
     float acc8 = (accp8.x + accp8.y) + (accq8.x + accq8.y);
-    // the four lanes of a quad hold sub-blocks 2t, 2t+1 (Q6_K: of both
-    // halves): fixed-order sum
-    acc0 += __shfl_xor_sync(0xffffffffu, acc0, 1);
-    acc8 += __shfl_xor_sync(0xffffffffu, acc8, 1);
-    acc0 += __shfl_xor_sync(0xffffffffu, acc0, 2);
-    acc8 += __shfl_xor_sync(0xffffffffu, acc8, 2);
+    b1_quad_sum(acc0, acc8);
     if (ksplit > 1) {
       if (rank != 0) {
         float* slot = red + (((rank - 1) * kConsumerWarps + cw) * 32 + lane) * 4;
@@ -502,8 +401,8 @@ __global__ void __launch_bounds__(kThreads, PAIR ? 3 : 4)
         }
       }
     }
-    if (rank == 0 && t == 0) {
-      const int ra = row0 + 16 * cw + rg, rb = ra + 8;
+    if (rank == 0 && cons.t == 0) {
+      const int ra = row0 + 16 * cw + cons.rg, rb = ra + 8;
       if (ra < p.N) p.y[ra] = acc0;
       if (rb < p.N) p.y[rb] = acc8;
     }
@@ -523,17 +422,22 @@ int device_sms() {
   return sms;
 }
 
-// Early weight streaming (DQ_QGEMV_WEIGHTS_EARLY) only where a CTA's whole
-// K range fits its ring, so that all of its weights are in flight when the
-// previous kernel completes.  Measured on GB300 (graphs of back-to-back
-// launches of one Llama-3-8B linear, batch 1): early is faster for qkv 6144 x
-// 4096 (4 super-blocks per CTA, 5.94 against 6.32 us) and o 4096 x 4096 (2:
-// 4.89 against 5.47 us), slower for gate/up 28672 x 4096 (16: 14.6 against
-// 13.6 us) and down 4096 x 14336 (7 on a 5-stage ring: 10.6 against 9.5 us):
-// a partial prefetch competes with the previous kernel's last CTAs for HBM
-// and delays the completion every CTA of this one waits for.
+// Early weight streaming (DQ_QGEMV_WEIGHTS_EARLY).  Where a CTA's whole K
+// range fits its ring (mode 1) every stage is copied into shared memory
+// before the wait, so all of its weights are in flight when the previous
+// kernel completes.  Measured on GB300 (graphs of back-to-back launches of one
+// Llama-3-8B linear, batch 1): faster for qkv 6144 x 4096 (4 super-blocks per
+// CTA, 5.94 against 6.32 us) and o 4096 x 4096 (2: 4.89 against 5.47 us).
+// Where it does not (mode 2) the first kL2PrefetchStages stages are only
+// prefetched into L2: copying a partial ring into shared memory early was
+// slower (gate/up 28672 x 4096: 14.6 against 13.6 us; down 4096 x 14336: 10.6
+// against 9.5 us), as it competes with the previous kernel's last CTAs for
+// HBM; an L2 prefetch of 2 stages gives 12.4 / 8.7 us (3 stages 12.3 / 8.8,
+// 4: 12.4 / 9.0, 6: 12.6 / 9.4, 8: 13.0 / 9.6, the whole range 15.1 / 9.6;
+// the 70B gate 28672 x 8192: 24.0 us without, 22.8 us with 2 stages).
 int early_weights(bool w_early, int nsb, int ks, int nstage) {
-  return (w_early && (nsb + ks - 1) / ks <= nstage) ? 1 : 0;
+  if (!w_early) return 0;
+  return (nsb + ks - 1) / ks <= nstage ? 1 : 2;
 }
 
 // Pick the K-split (cluster size) for `tiles` 64-row tiles when an SM holds

@@ -343,11 +343,11 @@ int dq_moe_forward_noalloc(const dq_moe_desc* desc, const void* x, int x_dtype, 
 /* up to phases-1 chunks (one cudaMemcpyAsync per matrix), and runs the      */
 /* grouped expert kernels chunk by chunk on `stream`, each after its chunk's */
 /* copies: the cached experts (and the shared ones) first, with no wait.     */
-/* Its result equals dq_moe_forward's on the same experts bit for bit when   */
-/* no expert receives more than 32 tokens (beyond that, the streamed layer   */
-/* keeps every expert on the grouped mma.sync kernel).  Not capturable in a  */
-/* CUDA graph (the host reads the routing).  A cache is used by one host     */
-/* thread at a time.                                                         */
+/* It keeps every expert on the grouped mma.sync kernel (dq_moe_forward runs */
+/* one-token experts on the block-diagonal kernel and experts with more than */
+/* 32 tokens on the tensor-core GEMM), so the two agree within the layer's   */
+/* tolerance, not bit for bit.  Not capturable in a CUDA graph (the host     */
+/* reads the routing).  A cache is used by one host thread at a time.        */
 /* ------------------------------------------------------------------------ */
 typedef struct dq_expert_cache dq_expert_cache;
 

@@ -1,8 +1,10 @@
 """Expert streaming (-m gpu): routed experts in page-locked host memory, a
 device cache of expert slots, copies in chunks overlapped with the grouped
-kernels.  The streamed layer runs the same kernels as the resident one, so
-with no expert above 32 tokens its output must equal dq_moe_forward's bit for
-bit; with more it is checked against the oracle.  The cache counters must
+kernels.  Every streamed output is compared with the oracle, and with
+dq_moe_forward's within the layer's tolerance (the streamed layer keeps every
+expert on the grouped mma.sync kernel; the resident one runs one-token experts
+on the block-diagonal kernel and experts above 32 tokens on the tensor-core
+GEMM).  The cache counters must
 account for every expert of every call."""
 import numpy as np
 import pytest
@@ -10,6 +12,7 @@ import torch
 
 import synth
 from gpu_util import dev_act, dev_bytes, rel_err
+from moe_layers import ref_under_selection
 from test_gpu_moe import MOE_TOL, NVFP4, Q4_K, Q8_0, dq  # noqa: F401
 
 pytestmark = pytest.mark.gpu
@@ -30,7 +33,7 @@ def _layer(seed, fmt, E, H, F, ns):
     (Q8_0, 8, 2, 768, 512, 1, 3, [3, 2, 3]),
     (NVFP4, 16, 2, 512, 512, 0, 2, [2, 2, 1]),
 ])
-def test_streamed_equals_resident(dq, fmt, E, k, H, F, ns, phases, Ts):
+def test_streamed_equals_resident(dq, orc, fmt, E, k, H, F, ns, phases, Ts):
     w, dev, host = _layer(9100 + E + F, fmt, E, H, F, ns)
     maxT = max(Ts)
     cache = dq.ExpertCache(E, k, H, F, ns, fmt, dev["router_W"], host["w_gate"], host["w_up"],
@@ -43,12 +46,26 @@ def test_streamed_equals_resident(dq, fmt, E, k, H, F, ns, phases, Ts):
     g = synth.streams(9200 + E, len(Ts))
     distinct = 0
     for i, T in enumerate(Ts):
-        x = dev_act(synth.activations(g[i], (T, H), 1), 1)
+        xh = synth.activations(g[i], (T, H), 1)
+        x = dev_act(xh, 1)
         y_s = cache.forward(x)
         y_r, idx, _, _ = dq.moe_forward(desc, x, want_routing=True)
         torch.cuda.synchronize()
         assert dq.device_status() == 0
-        np.testing.assert_array_equal(y_s.cpu().numpy(), y_r.cpu().numpy())
+        ys, yr = y_s.cpu().numpy(), y_r.cpu().numpy()
+        # the streamed layer keeps every expert on the grouped mma.sync kernel,
+        # the resident one runs one-token experts on the block-diagonal kernel:
+        # both match the oracle, and each other within the layer's tolerance
+        y_ref, idx_ref, _, L_ref = orc.moe_forward(fmt, E, k, H, F, ns, w["router_W"],
+                                                   w["w_gate"], w["w_up"], w["w_down"],
+                                                   w["sh_gate"], w["sh_up"], w["sh_down"], xh, 1, T)
+        ig = idx.cpu().numpy()
+        for t in range(T):   # a near-tie routed differently: the oracle under that selection
+            if not np.array_equal(ig[t], idx_ref[t]):
+                y_ref[t] = ref_under_selection(orc, fmt, w, E, k, H, F, ns, xh, 1, t, ig[t], L_ref)
+        assert rel_err(ys, y_ref) <= MOE_TOL
+        assert rel_err(yr, y_ref) <= MOE_TOL
+        assert rel_err(ys, yr) <= MOE_TOL
         distinct += len(np.unique(idx.cpu().numpy()))
     st = cache.stats()
     assert st["hits"] + st["misses"] == distinct
