@@ -74,11 +74,12 @@ def run_case(args):
         # 1.6 GB of weights (a small case for full captures of that kernel)
         cfg = dict(synth.MOE_DEEPSEEK, E=64)
         print(json.dumps(bench_moe(torch, dq, cfg, 64, reps=max(1, args.steps))))
-    elif args.case == "prefill32":
+    elif args.case in ("prefill32", "prefill32nvfp4"):
         # DeepSeek-V3 expert shapes with 32 routed experts (+1 shared), T = 256:
         # ~64 tokens per expert, every expert on the tcgen05 grouped GEMM; 0.8 GB
-        # of weights (a small case for full ncu captures of that kernel)
-        cfg = dict(synth.MOE_DEEPSEEK, E=32)
+        # of weights (a small case for full ncu captures of that kernel), Q4_K
+        # or NVFP4 expert weights
+        cfg = prefill_cfg(6 if args.case.endswith("nvfp4") else Q4_K)
         print(json.dumps(bench_moe(torch, dq, cfg, 256, reps=max(1, args.steps))))
     elif args.case == "streamed":
         print(json.dumps(bench_moe_streamed(torch, dq, synth.MOE_DEEPSEEK, 8, reps=max(3, args.steps))))
@@ -96,6 +97,16 @@ def peaks():
         return float(m["hbm_gbs"]), "measured"
     except Exception:
         return 6800.0, "fallback"
+
+
+def tensor_peak():
+    """Measured dense bf16 tensor throughput (TFLOP/s, burst) of this GPU type
+    (fp16 operands run at the same rate)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except Exception:
+        return 1900.0
 
 
 def weight_bytes(fmt, N, K):
@@ -642,6 +653,13 @@ def bench_gemv_70b_formats(torch, dq, reps=30, fmts=((Q4_K, "q4_k"), (2, "q6_k")
     return out
 
 
+def prefill_cfg(fmt):
+    """The prefill-chunk workload of the tensor-core expert GEMM: DeepSeek-V3
+    expert shapes (hidden 7168, FFN 2048, top-8 + 1 shared) with 32 routed
+    experts, so that a 256-token chunk gives each expert ~64 tokens."""
+    return dict(synth.MOE_DEEPSEEK, E=32, fmt=fmt)
+
+
 def bench_moe(torch, dq, cfg, T, reps=20):
     w = synth.moe_weights(synth.BASE_SEED + (3 if cfg is synth.MOE_MIXTRAL else 4), cfg["E"],
                           cfg["H"], cfg["F"], cfg["n_shared"], cfg["fmt"])
@@ -702,9 +720,11 @@ def bench_moe(torch, dq, cfg, T, reps=20):
     alg = exp_bytes + cfg["E"] * cfg["H"] * 4 + T * cfg["H"] * (2 + 4)
     del graphs, dev
     torch.cuda.empty_cache()
+    # expert products: gate, up and down of every routed slot and shared expert
+    flops = 2.0 * T * (cfg["top_k"] + cfg["n_shared"]) * 3 * cfg["F"] * cfg["H"]
     return {"T": T, "ms": ms, "tokens_per_s": T / (ms / 1e3),
             "experts_touched": float(np.mean(touched)), "alg_bytes": alg,
-            "GBps": alg / (ms / 1e3) / 1e9}
+            "GBps": alg / (ms / 1e3) / 1e9, "expert_tflops": flops / (ms / 1e3) / 1e12}
 
 
 def h2d_peak(torch, nbytes=1 << 30, reps=5):
@@ -818,6 +838,16 @@ def run_ours(args):
             moe["mixtral_T16"] = bench_moe(torch, dq, synth.MOE_MIXTRAL, 16)
             for T in synth.MOE_DEEPSEEK["T"]:
                 moe["deepseek_v3_T%d" % T] = bench_moe(torch, dq, synth.MOE_DEEPSEEK, T)
+            # prefill chunks on the tensor-core expert GEMM (~64 tokens per
+            # expert), Q4_K and NVFP4 weights: HBM and tensor-pipe fractions
+            tpk = tensor_peak()
+            for fmt, nm in ((Q4_K, "q4_k"), (6, "nvfp4")):
+                r = bench_moe(torch, dq, prefill_cfg(fmt), 256)
+                r["workload"] = ("DeepSeek-V3 expert shapes, 32 routed experts + 1 shared, "
+                                 "T=256 (~64 tokens per expert: tcgen05 grouped GEMM), %s" % nm)
+                r["frac_of_tensor_peak"] = r["expert_tflops"] / tpk
+                r["tensor_peak_tflops"] = tpk
+                moe["prefill_ds32e_T256_" + nm] = r
             for v in moe.values():
                 v["frac_of_hbm"] = v["GBps"] / peak
             extra["moe"] = moe

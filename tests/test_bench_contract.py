@@ -45,7 +45,8 @@ def test_gpu_arm_line_assembly(monkeypatch, capsys):
                                          "weight_GBps": 4000.0, "weight_GBps_back_to_back": 5500.0})
     monkeypatch.setattr(bench, "bench_gemv_70b_formats",
                         lambda *a, **k: {"f": {"weight_GBps": 1.0, "weight_GBps_back_to_back": 2.0}})
-    monkeypatch.setattr(bench, "bench_moe", lambda *a, **k: {"GBps": 100.0, "tokens_per_s": 1.0})
+    monkeypatch.setattr(bench, "bench_moe", lambda *a, **k: {"GBps": 100.0, "tokens_per_s": 1.0,
+                                                           "expert_tflops": 50.0})
     monkeypatch.setattr(bench, "bench_moe_streamed", lambda *a, **k: {})
     monkeypatch.setattr(bench, "oracle_sample_isolated",
                         lambda *a, **k: {"value": 0.8, "unit": "GB/s", "cores": 8, "kind": "oracle",
