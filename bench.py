@@ -46,11 +46,15 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-moe", action="store_true", help="skip the MoE-layer lines")
+    ap.add_argument("--min-timed-ms", type=float, default=200.0,
+                    help="device time each timed region is repeated for (median reported); "
+                         "a small value keeps launch-list profiling runs short")
     ap.add_argument("--oracle-sample", type=float, default=None, help=argparse.SUPPRESS)
     ap.add_argument("--oracle-threads", type=int, default=None, help=argparse.SUPPRESS)
     ap.add_argument("--case", default=None,
                     help="profiling aid: run only one workload a few times and exit "
-                         "(gemv70b | layer8b | mixtral | deepseek1 | deepseek8 | deepseek256)")
+                         "(gemv70b | layer8b | formats70b | mixtral | deepseek1 | deepseek8 | "
+                         "deepseek256 | ds64 | ds32t1 | prefill32 | prefill32nvfp4 | streamed)")
     return ap.parse_args()
 
 
@@ -81,6 +85,12 @@ def run_case(args):
         # or NVFP4 expert weights
         cfg = prefill_cfg(6 if args.case.endswith("nvfp4") else Q4_K)
         print(json.dumps(bench_moe(torch, dq, cfg, 256, reps=max(1, args.steps))))
+    elif args.case == "ds32t1":
+        # DeepSeek-V3 expert shapes with 32 routed experts (+1 shared), T = 1:
+        # the one-token expert kernels on 0.8 GB of weights (a small case for
+        # full ncu captures of them)
+        cfg = dict(synth.MOE_DEEPSEEK, E=32)
+        print(json.dumps(bench_moe(torch, dq, cfg, 1, reps=max(1, args.steps))))
     elif args.case == "streamed":
         print(json.dumps(bench_moe_streamed(torch, dq, synth.MOE_DEEPSEEK, 8, reps=max(3, args.steps))))
     elif args.case.startswith("deepseek"):
@@ -355,11 +365,13 @@ MIN_TIMED_MS = 200.0
 MIN_REPS = 5
 
 
-def timed_reps(torch, run, min_ms=MIN_TIMED_MS, min_reps=MIN_REPS):
+def timed_reps(torch, run, min_ms=None, min_reps=MIN_REPS):
     """Device time (ms) of repeated calls of run(), each bracketed by a
     synchronize and CUDA events on the current stream, until at least min_ms
     of device time and min_reps repetitions have been timed."""
     out = []
+    if min_ms is None:
+        min_ms = MIN_TIMED_MS
     while sum(out) < min_ms or len(out) < min_reps:
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
@@ -587,7 +599,8 @@ def time_gemv(torch, dq, fmt, Ws, N, K, x, y, reps=30, b2b_ms=20.0, with_b2b_rep
             gr.replay()
 
     # repetitions of 160 back-to-back launches: median per launch
-    b2b_reps = [r * 1e3 / 160 for r in timed_reps(torch, twenty, min_ms=b2b_ms, min_reps=5)]
+    b2b_reps = [r * 1e3 / 160 for r in timed_reps(torch, twenty, min_ms=min(b2b_ms, MIN_TIMED_MS),
+                                                  min_reps=5)]
     b2b = float(np.median(b2b_reps))
     del gr
     if with_b2b_reps:
@@ -915,7 +928,9 @@ def run_ours(args):
 
 
 def main():
+    global MIN_TIMED_MS
     args = parse()
+    MIN_TIMED_MS = args.min_timed_ms
     if args.oracle_sample is not None:
         oracle_sample_main(args.oracle_sample, args.oracle_threads)
     elif args.case:

@@ -28,24 +28,27 @@ namespace dqmoe {
 
 constexpr int kTcRows = 128;      // weight rows per tile (UMMA M)
 constexpr int kTcMaxN = 128;      // tokens per unit (UMMA N <= 128 here)
-// slab ring depth: two slabs keep the shared memory at ~103 KB (Q4_K /
-// NVFP4 rows), so that two CTAs share an SM and their decoder warps hide each
-// other's latency (DeepSeek-V3 expert shapes, 32 experts of ~64 tokens,
-// Q4_K: 0.81 -> 0.68 ms against four slabs at one CTA per SM)
-constexpr int kTcSlabs = 2;
+// Slab ring depth (a kernel parameter, SLABS): two slabs keep the shared
+// memory at ~103 KB (Q4_K / NVFP4 rows), so that two CTAs share an SM and
+// their decoder warps hide each other's latency.  Calls whose routed experts
+// are expected above the 32-token threshold (prefill chunks: many units) take
+// two (DeepSeek-V3 expert shapes, 32 experts of ~64 tokens, Q4_K: 0.81 ->
+// 0.68 ms against four); calls where only the shared experts reach this
+// kernel (a few units of 16 row tiles each, fewer CTAs than SMs) keep four:
+// a deeper ring per CTA.
 constexpr int kTcWStages = 2;     // packed super-block ring depth
 constexpr int kTcThreads = 192;   // 6 warps
 constexpr int kSlabA = kTcRows * 128;   // 16 KB: 128 rows x 64 fp16
 constexpr int kSlabB = kTcMaxN * 128;   // 16 KB: 128 tokens x 64 fp16
 
-template <int FMT>
+template <int FMT, int SLABS>
 struct TcLayout {
   static constexpr int BOX = Layout<FMT>::BOX;               // bytes per row per super-block
   static constexpr int W_STG = kTcRows * BOX;                // multiple of 1024
   static constexpr int OFF_W = 1024;
   static constexpr int OFF_A = OFF_W + kTcWStages * W_STG;
-  static constexpr int OFF_B = OFF_A + kTcSlabs * kSlabA;
-  static constexpr int TOTAL = OFF_B + kTcSlabs * kSlabB;
+  static constexpr int OFF_B = OFF_A + SLABS * kSlabA;
+  static constexpr int TOTAL = OFF_B + SLABS * kSlabB;
   static_assert(W_STG % 1024 == 0, "TMA / swizzle atoms need 1024-byte alignment");
 };
 
@@ -177,12 +180,14 @@ struct TcParams {
   int64_t out_stride;
 };
 
-template <int FMT>
-__global__ void __launch_bounds__(kTcThreads, 2) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+template <int FMT, int SLABS>
+__global__ void __launch_bounds__(kTcThreads, SLABS == 2 ? 2 : 1)
+    tc_gemm_kernel(const __grid_constant__ TcParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   pdl_wait();
   pdl_trigger();
-  using TL = TcLayout<FMT>;
+  using TL = TcLayout<FMT, SLABS>;
+  constexpr int kTcSlabs = SLABS;
   const int unit = blockIdx.y;
   if (unit >= __ldg(p.n_units)) return;            // uniform for the whole CTA
   // swizzle atoms and TMA boxes need a 1024-byte aligned window
@@ -333,12 +338,12 @@ __global__ void __launch_bounds__(kTcThreads, 2) tc_gemm_kernel(const __grid_con
 // ---------------------------------------------------------------------------
 // host
 // ---------------------------------------------------------------------------
-template <int FMT>
+template <int FMT, int SLABS>
 int launch_tc_fmt(const void* W, const void* Wsh, int E, int n_shared, int rows_per_expert,
                   int K, const int4* units, const int* n_units, int max_units, const __half* X16,
                   int64_t npos, const float* xinv, float* out, int64_t out_stride,
                   cudaStream_t s) {
-  using TL = TcLayout<FMT>;
+  using TL = TcLayout<FMT, SLABS>;
   TcParams p;
   memset(&p, 0, sizeof(p));
   const int qk = FMT == DQ_Q8_0 ? 32 : 256;
@@ -363,33 +368,38 @@ int launch_tc_fmt(const void* W, const void* Wsh, int E, int n_shared, int rows_
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 64 || !attr[dev]) {
-    if (cudaFuncSetAttribute(tc_gemm_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             TL::TOTAL) != cudaSuccess)
+    if (cudaFuncSetAttribute(tc_gemm_kernel<FMT, SLABS>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, TL::TOTAL) != cudaSuccess)
       return DQ_ERR_CUDA;
     if (dev < 64) attr[dev] = true;
   }
   dim3 grid((unsigned)(rows_per_expert / kTcRows), (unsigned)std::max(1, max_units));
-  if (launch_pdl(tc_gemm_kernel<FMT>, grid, dim3(kTcThreads), TL::TOTAL, s, 0, p) != cudaSuccess)
+  if (launch_pdl(tc_gemm_kernel<FMT, SLABS>, grid, dim3(kTcThreads), TL::TOTAL, s, 0, p) !=
+      cudaSuccess)
     return DQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
 }
 
+// many_units: routed experts are expected above the 32-token threshold (two
+// slabs, two CTAs per SM); otherwise four slabs, one CTA per SM.
 int launch_tc_gemm(int fmt, const void* W, const void* Wsh, int E, int n_shared,
                    int rows_per_expert, int K, const int4* units, const int* n_units,
                    int max_units, const __half* X16, int64_t npos, const float* xinv, float* out,
-                   int64_t out_stride, cudaStream_t s) {
+                   int64_t out_stride, bool many_units, cudaStream_t s) {
   if (rows_per_expert % kTcRows) return DQ_ERR_UNSUPPORTED;
-  if (fmt == DQ_Q4_K)
-    return launch_tc_fmt<DQ_Q4_K>(W, Wsh, E, n_shared, rows_per_expert, K, units, n_units,
-                                  max_units, X16, npos, xinv, out, out_stride, s);
-  if (fmt == DQ_Q6_K)
-    return launch_tc_fmt<DQ_Q6_K>(W, Wsh, E, n_shared, rows_per_expert, K, units, n_units,
-                                  max_units, X16, npos, xinv, out, out_stride, s);
-  if (fmt == DQ_Q8_0)
-    return launch_tc_fmt<DQ_Q8_0>(W, Wsh, E, n_shared, rows_per_expert, K, units, n_units,
-                                  max_units, X16, npos, xinv, out, out_stride, s);
-  return launch_tc_fmt<DQ_NVFP4>(W, Wsh, E, n_shared, rows_per_expert, K, units, n_units,
-                                 max_units, X16, npos, xinv, out, out_stride, s);
+  const bool deep = !many_units;
+#define DQ_TC(F)                                                                               \
+  if (fmt == F)                                                                                \
+    return deep ? launch_tc_fmt<F, 4>(W, Wsh, E, n_shared, rows_per_expert, K, units, n_units, \
+                                      max_units, X16, npos, xinv, out, out_stride, s)          \
+                : launch_tc_fmt<F, 2>(W, Wsh, E, n_shared, rows_per_expert, K, units, n_units, \
+                                      max_units, X16, npos, xinv, out, out_stride, s);
+  DQ_TC(DQ_Q4_K)
+  DQ_TC(DQ_Q6_K)
+  DQ_TC(DQ_Q8_0)
+  DQ_TC(DQ_NVFP4)
+#undef DQ_TC
+  return DQ_ERR_UNSUPPORTED;
 }
 
 }  // namespace dqmoe
