@@ -342,11 +342,17 @@ def _traffic_record(kernel):
     return r
 
 
+# the files the headline kernel (qgemv_b1_kernel) is compiled from
+KERNEL_SOURCES = ("dequant_gemv_moe_gb300/csrc/qgemv_mma.cu", "dequant_gemv_moe_gb300/csrc/qgemv_mma.cuh",
+                  "dequant_gemv_moe_gb300/csrc/b1.cuh", "dequant_gemv_moe_gb300/csrc/common.cuh",
+                  "dequant_gemv_moe_gb300/csrc/tmap.h", "dequant_gemv_moe_gb300/csrc/tmap.cu",
+                  "include/dqmoe.h")
+
+
 def csrc_hash():
     h = hashlib.sha1()
-    d = os.path.join(ROOT, "dequant_gemv_moe_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
-        with open(os.path.join(d, f), "rb") as fh:
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(f.encode())
             h.update(fh.read())
     return h.hexdigest()
