@@ -148,6 +148,13 @@ def _moe_case(dq, orc, fmt, E, k, H, F, ns, T, xdt, seed, tokens=None, cached=No
     (NVFP4, 8, 2, 512, 512, 0, 30, 1),
     (NVFP4, 4, 2, 768, 512, 1, 50, 2),
     (NVFP4, 2, 2, 512, 256, 1, 90, 1),
+    # one token with shared experts: the shared experts' products run before
+    # the router (hidden > 1024: the streaming router, which waits at its end;
+    # hidden 1024: the tiled router)
+    (Q4_K, 16, 4, 2048, 512, 2, 1, 2),
+    (Q8_0, 8, 2, 2048, 1024, 1, 1, 1),
+    (Q6_K, 4, 2, 4096, 2048, 1, 1, 2),
+    (Q4_K, 16, 4, 1024, 512, 1, 1, 1),
 ])
 def test_moe_forward_small(dq, orc, fmt, E, k, H, F, ns, T, xdt):
     err, _ = _moe_case(dq, orc, fmt, E, k, H, F, ns, T, xdt, seed=3000 + E * 7 + T)
