@@ -13,11 +13,11 @@
 // the fp32 SwiGLU output), converting each 256-value stage to fp16 with one
 // power-of-two scale in the loader: no separate conversion launch.
 //
-// Work: units of (one-token group, row tile).  CTA b takes units b and
-// b + grid first, then claims further units one at a time from a counter
-// (which balances the work across SMs); the loader makes each claim two units
-// ahead and reads its group record one unit ahead, so their latency hides
-// behind the current unit's stages.  Units are streamed as stages of one
+// Work: units of (one-token group, row tile).  CTA b takes unit b first, then
+// claims further units one at a time from a counter (which balances the work
+// across SMs); the loader makes each claim two units ahead and reads its group
+// record one unit ahead, so their latency hides behind the current unit's
+// stages.  Units are streamed as stages of one
 // super-block of 64 rows:
 //   gate/up: 32 rows of W_gate and the same 32 rows of W_up (two TMA boxes);
 //            consumer warp w holds gate rows 8w + r and the matching up rows,
@@ -49,7 +49,7 @@ struct GroupedB1Params {
                          //  position, activation row, 0)
   const int* n_groups;
   int* claim;            // work counter, zero when the kernel starts (counts the
-                         // claims beyond the first two units of every CTA)
+                         // claims beyond the first unit of every CTA)
   const void* x;         // gate/up: x [T][H] (row = the group's token); down: h [NP][F]
                          // (row = the group's position)
   int64_t xstride;       // elements per activation row
@@ -110,12 +110,15 @@ __global__ void __launch_bounds__(kThreads, 4)
     const int total = __ldcg(p.n_groups) * p.tiles;
     constexpr int kXBytes = XDT == DQ_F32 ? 4 : 2;
     // lane 0 holds the next unit u1 with its group record g1 and the unit
-    // after it, u2: units b and b + grid first, then claims from the counter;
-    // each claim is made two units ahead and its group record read one unit
-    // ahead, so neither load stalls the loader
-    int u1 = (int)blockIdx.x, u2 = (int)(blockIdx.x + gridDim.x);
+    // after it, u2: unit b first, then claims from the counter; each claim is
+    // made two units ahead and its group record read one unit ahead, so
+    // neither load stalls the loader
+    int u1 = (int)blockIdx.x, u2 = 0;
     int4 g1 = make_int4(0, 0, 0, 0);
-    if (lane == 0 && u1 < total) g1 = __ldcg(p.groups + u1 / p.tiles);
+    if (lane == 0) {
+      if (u1 < total) g1 = __ldcg(p.groups + u1 / p.tiles);
+      u2 = (int)gridDim.x + atomicAdd(p.claim, 1);
+    }
     // the current unit (enqueue side): activation row, first weight row (bit
     // 30: shared expert), output position
     const char* xrow = nullptr;
@@ -136,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 4)
       if (lane == 0) {
         u1 = u2;
         if (u1 < total) g1 = __ldcg(p.groups + u1 / p.tiles);
-        u2 = 2 * (int)gridDim.x + atomicAdd(p.claim, 1);
+        u2 = (int)gridDim.x + atomicAdd(p.claim, 1);
       }
       return u;
     };
