@@ -427,8 +427,15 @@ def bench_layer(torch, dq, args, lin, with_e2e=True):
     # weights: ROTATE copies of the layer
     Ws = [[torch.from_numpy(synth.quant_matrix(g[0], Q4_K, N, K)).cuda() for (_, N, K) in lin]
           for _ in range(ROTATE)]
-    xs = [torch.from_numpy(synth.activations(g[1], (1, K), 1)).cuda() for (_, N, K) in lin]
-    ys = [torch.empty(1, N, dtype=torch.float32, device="cuda") for (_, N, K) in lin]
+    # the step's activations and outputs each in one device buffer (slices
+    # per linear), so that the end-to-end pass moves them in one copy each way
+    kofs = np.cumsum([0] + [K for (_, N, K) in lin])
+    nofs = np.cumsum([0] + [N for (_, N, K) in lin])
+    x_all = torch.from_numpy(np.concatenate(
+        [synth.activations(g[1], (1, K), 1) for (_, N, K) in lin], axis=1)).cuda()
+    y_all = torch.empty(1, int(nofs[-1]), dtype=torch.float32, device="cuda")
+    xs = [x_all[:, kofs[i]:kofs[i + 1]] for i in range(len(lin))]
+    ys = [y_all[:, nofs[i]:nofs[i + 1]] for i in range(len(lin))]
     wbytes = sum(weight_bytes(Q4_K, N, K) for (_, N, K) in lin)
     abytes = sum(K * 2 + N * 4 for (_, N, K) in lin)
 
@@ -518,17 +525,20 @@ def bench_layer(torch, dq, args, lin, with_e2e=True):
 
     # e2e: the same step through the public call with host buffers — pinned
     # x uploaded and y read back every step inside the timed region
-    hx = [torch.from_numpy(synth.activations(g[2], (1, K_), 1)).pin_memory() for (_, N_, K_) in lin]
-    hy = [torch.empty(1, N_, dtype=torch.float32).pin_memory() for (_, N_, K_) in lin]
-    h2d = sum(t.numel() * 2 for t in hx)
-    d2h = sum(t.numel() * 4 for t in hy)
+    # pinned host buffers holding the whole step's activations / outputs:
+    # one upload and one read-back per step
+    hx = torch.from_numpy(np.concatenate(
+        [synth.activations(g[2], (1, K_), 1) for (_, N_, K_) in lin], axis=1)).pin_memory()
+    hy = torch.empty(1, int(nofs[-1]), dtype=torch.float32).pin_memory()
+    h2d = hx.numel() * 2
+    d2h = hy.numel() * 4
 
     def e2e_step(r):
-        for i, (_, N_, K_) in enumerate(lin):
-            xs[i].copy_(hx[i], non_blocking=True)
+        # the library's copy kernel (dq_stage): the upload, the four GEMVs and
+        # the read-back stay one chain of programmatic dependent launches
+        dq.stage(x_all, hx)
         step(r)
-        for i in range(len(lin)):
-            hy[i].copy_(ys[i], non_blocking=True)
+        dq.stage(hy, y_all)
 
     egr, erem = layer_graphs(torch, s, e2e_step, K)
     torch.cuda.synchronize()
@@ -548,9 +558,11 @@ def bench_layer(torch, dq, args, lin, with_e2e=True):
                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                   "ms_per_step": ems / K,
                   "timing": rep_stats(ereps, K, wbytes),
-                  "note": "x uploaded from pinned host memory and y read back in every step, "
-                          "captured with the step's %d dq_qgemv calls, %d steps per graph; "
-                          "median of the repetitions" % (nl, LAYERS_PER_GRAPH)}
+                  "note": "the step's activations uploaded from pinned host memory and its "
+                          "outputs read back in every step (one dq_stage copy each way: the "
+                          "%d linears' vectors sit in one buffer), captured with the step's "
+                          "%d dq_qgemv calls, %d steps per graph; median of the repetitions"
+                          % (nl, nl, LAYERS_PER_GRAPH)}
     del egr, erem, Ws
     torch.cuda.empty_cache()
     return res

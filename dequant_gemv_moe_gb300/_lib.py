@@ -40,6 +40,7 @@ _SIGS = {
     "dq_qgemv_ksplit": [_I, _P, _I64, _I64, _P, _I, _I, _P, _I, _P],
     "dq_qgemv_ex": [_I, _P, _I64, _I64, _P, _I, _I, _P, _I, ctypes.c_uint, _P],
     "dq_device_status": [_P],
+    "dq_stage": [_P, _P, _I64, _P],
 }
 _OPTIONAL_SIGS = {
     "dq_moe_workspace_size": [ctypes.POINTER(MoeDesc), _I, _P],

@@ -67,6 +67,16 @@ def qgemv(fmt, W, N, K, x, y=None, ksplit=None, weights_early=False):
     return y
 
 
+def stage(dst, src):
+    """Copy src into dst (same number of bytes; CUDA or page-locked CPU tensors)
+    with the library's copy kernel on the current stream (dq_stage)."""
+    nb = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != nb:
+        raise ValueError("stage: dst and src sizes differ")
+    _call("dq_stage", _ptr(dst), _ptr(src), nb, _stream())
+    return dst
+
+
 def device_status():
     v = ctypes.c_int()
     _call("dq_device_status", ctypes.byref(v))

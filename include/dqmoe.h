@@ -393,6 +393,23 @@ int dq_expert_cache_stats(const dq_expert_cache* cache, long long* hits, long lo
 /* Releases the host resources of the cache (not the caller's slot buffers). */
 int dq_expert_cache_destroy(dq_expert_cache* cache);
 
+/* dq_stage — copy `bytes` from src to dst with a kernel launched like every
+ * other kernel of this library (programmatic dependent launch on `stream`):
+ * for moving a decode step's activations in from page-locked host memory and
+ * its outputs back out without leaving the chain of launches, so that the
+ * GEMV after the copy is scheduled while the copy drains (a copy-engine copy
+ * between two kernels ends that chain).  The pages do not describe this call;
+ * it serves the host-buffer decode loop ([KTransformers, §技术原理]: one
+ * graph launch per decode step) and the benchmark's end-to-end measurement.
+ *   dst, src : device memory or page-locked (mapped) host memory the GPU can
+ *              address, 16-byte aligned, not overlapping.
+ *   bytes    : a positive multiple of 16.
+ * The copy waits for the kernel before it on `stream` (its source may be that
+ * kernel's output) and is asynchronous like every call.
+ * Errors: DQ_ERR_ARG (null pointer, bytes <= 0, overlapping ranges),
+ *         DQ_ERR_ALIGN (pointers or size not 16-byte multiples), DQ_ERR_CUDA. */
+int dq_stage(void* dst, const void* src, int64_t bytes, void* stream);
+
 /* Human-readable name of a dq_status value (static string, never NULL). */
 const char* dq_status_string(int status);
 
