@@ -34,15 +34,23 @@ static size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 constexpr int kWide = 32;
 
 // up to kRouterStreamT tokens the router streams W_r in hidden chunks of
-// kRouterChunk (one warp per expert row and chunk); beyond, it tiles
+// kRouterChunk (one warp per expert row and chunk), up to kRouterStreamT2 in
+// chunks of kRouterChunk2 (the chunk of every token's x stays at 32 KB of
+// shared memory); beyond, it tiles
 constexpr int kRouterStreamT = 8;
 constexpr int kRouterChunk = 1024;
+constexpr int kRouterStreamT2 = 32;
+constexpr int kRouterChunk2 = 256;
+
+int router_chunk(int T) {
+  return T <= kRouterStreamT ? kRouterChunk : T <= kRouterStreamT2 ? kRouterChunk2 : 0;
+}
 
 MoePlan moe_plan(const dq_moe_desc& d, int T, bool allow_wide) {
   MoePlan p;
   const int tiles = ((d.E + 63) / 64) * ((T + 31) / 32);
-  p.KS = T <= kRouterStreamT ? (d.hidden + kRouterChunk - 1) / kRouterChunk
-                             : std::max(1, std::min(d.hidden / 256, (320 + tiles - 1) / tiles));
+  p.KS = router_chunk(T) ? (d.hidden + router_chunk(T) - 1) / router_chunk(T)
+                         : std::max(1, std::min(d.hidden / 256, (320 + tiles - 1) / tiles));
   p.P = (int64_t)T * d.top_k;
   p.NP = p.P + (int64_t)d.n_shared * T;
   // group width from the expected tokens per routed expert (uniform routing):
@@ -63,6 +71,20 @@ MoePlan moe_plan(const dq_moe_desc& d, int T, bool allow_wide) {
   p.U_max = p.wide ? (int)(p.P / 128 + p.P / (kWide + 1) + 1 +
                            (int64_t)d.n_shared * ((T + 127) / 128))
                    : 0;
+  // Down products split over K (p.DS parts, summed in order by the combine)
+  // when the expected units (64-row tiles of the touched experts) are too few
+  // for the persistent grid (~3 CTAs on each of 152 SMs) to come out even:
+  // Mixtral shapes at T = 16 have 8 experts x 64 tiles = 512 units for 456
+  // CTAs, so 56 CTAs would stream a second unit alone.  Only where every
+  // position is produced by the grouped kernels (no one-token or tensor-core
+  // groups), each part keeps >= 4 super-blocks.
+  p.DS = 1;
+  if (allow_wide && !p.wide && !p.single) {
+    const int64_t units = (std::min<int64_t>(d.E, p.P) +
+                           (int64_t)d.n_shared * ((T + p.GW - 1) / p.GW)) * (d.hidden / 64);
+    constexpr int64_t kSlots = 3 * 152;
+    while (p.DS < 4 && units * p.DS < 4 * kSlots && d.ffn / 256 >= 8 * p.DS) p.DS *= 2;
+  }
   size_t o = 0;
   p.off_part = o;    o = align256(o + (size_t)p.KS * T * d.E * 4);
   p.off_logits = o;  o = align256(o + (size_t)T * d.E * 4);
@@ -75,7 +97,7 @@ MoePlan moe_plan(const dq_moe_desc& d, int T, bool allow_wide) {
   p.off_groups = o;  o = align256(o + (size_t)p.G_max * 16);
   p.off_ngroups = o; o = align256(o + 16);
   p.off_h = o;       o = align256(o + (size_t)p.NP * d.ffn * 4);
-  p.off_ypos = o;    o = align256(o + (size_t)p.NP * d.hidden * 4);
+  p.off_ypos = o;    o = align256(o + (size_t)p.DS * p.NP * d.hidden * 4);
   p.off_units = o;   o = align256(o + (size_t)std::max(p.U_max, 1) * 16);
   p.off_nunits = o;  o = align256(o + 16);
   // fp16 copies of the activations the streaming kernels read
@@ -110,34 +132,67 @@ __global__ void __launch_bounds__(128) router_logits_kernel(const float* __restr
                                                             float* __restrict__ part) {
   pdl_wait();
   pdl_trigger();
-  __shared__ __align__(16) float Ws[32][64 + 4];
-  __shared__ __align__(16) float Xs[32][32 + 4];
+  // two buffers: the next chunk's loads are in flight (in registers) while
+  // this chunk is multiplied.  Loader mapping: a warp covers 8 consecutive
+  // hidden indices of 4 consecutive experts (tokens), so that every global
+  // load instruction reads whole 32-byte sectors and the transposed stores
+  // hit 32 distinct banks (row pitches 68 and 36: 4 hh + e mod 32).
+  __shared__ __align__(16) float Ws[2][32][64 + 4];
+  __shared__ __align__(16) float Xs[2][32][32 + 4];
   const int e0 = blockIdx.x * 64, t0 = blockIdx.y * 32, ks = blockIdx.z;
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
   const int nch = H / 32;
   const int c_begin = (int)((int64_t)nch * ks / KS), c_end = (int)((int64_t)nch * (ks + 1) / KS);
-  float acc[4][4] = {};
-  for (int c = c_begin; c < c_end; ++c) {
+  float wr[16], xr[8];
+  auto load = [&](int c) {
     const int h0 = c * 32;
-    for (int i = tid; i < 64 * 32; i += 128) {
-      const int e = i >> 5, hh = i & 31;
-      Ws[hh][e] = (e0 + e < E) ? __ldg(Wr + (int64_t)(e0 + e) * H + h0 + hh) : 0.f;
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      const int i = tid + 128 * r;
+      const int hh = (i & 7) | ((i >> 9) << 3), e = (i >> 3) & 63;
+      wr[r] = (e0 + e < E) ? __ldg(Wr + (int64_t)(e0 + e) * H + h0 + hh) : 0.f;
     }
-    for (int i = tid; i < 32 * 32; i += 128) {
-      const int t = i >> 5, hh = i & 31;
-      Xs[hh][t] = (t0 + t < T) ? act_f32(x, xdt, (int64_t)(t0 + t) * H + h0 + hh) : 0.f;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const int i = tid + 128 * r;
+      const int hh = (i & 7) | ((i >> 8) << 3), t = (i >> 3) & 31;
+      xr[r] = (t0 + t < T) ? act_f32(x, xdt, (int64_t)(t0 + t) * H + h0 + hh) : 0.f;
     }
-    __syncthreads();
+  };
+  auto store = [&](int b) {
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      const int i = tid + 128 * r;
+      Ws[b][(i & 7) | ((i >> 9) << 3)][(i >> 3) & 63] = wr[r];
+    }
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const int i = tid + 128 * r;
+      Xs[b][(i & 7) | ((i >> 8) << 3)][(i >> 3) & 31] = xr[r];
+    }
+  };
+  float acc[4][4] = {};
+  if (c_begin < c_end) {
+    load(c_begin);
+    store(0);
+  }
+  __syncthreads();
+  for (int c = c_begin; c < c_end; ++c) {
+    const int b = (c - c_begin) & 1;
+    const bool more = c + 1 < c_end;
+    if (more) load(c + 1);
 #pragma unroll 8
     for (int hh = 0; hh < 32; ++hh) {
-      const float4 xv = *(const float4*)&Xs[hh][ty * 4];
-      const float4 wv = *(const float4*)&Ws[hh][tx * 4];
+      const float4 xv = *(const float4*)&Xs[b][hh][ty * 4];
+      const float4 wv = *(const float4*)&Ws[b][hh][tx * 4];
       const float xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
       for (int a = 0; a < 4; ++a)
 #pragma unroll
-        for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(xa[a], wa[b], acc[a][b]);
+        for (int q = 0; q < 4; ++q) acc[a][q] = fmaf(xa[a], wa[q], acc[a][q]);
     }
+    // the other buffer was last read before the previous barrier
+    if (more) store(b ^ 1);
     __syncthreads();
   }
 #pragma unroll
@@ -145,26 +200,28 @@ __global__ void __launch_bounds__(128) router_logits_kernel(const float* __restr
     const int t = t0 + ty * 4 + a;
     if (t >= T) continue;
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const int e = e0 + tx * 4 + b;
-      if (e < E) part[((int64_t)ks * T + t) * E + e] = acc[a][b];
+    for (int q = 0; q < 4; ++q) {
+      const int e = e0 + tx * 4 + q;
+      if (e < E) part[((int64_t)ks * T + t) * E + e] = acc[a][q];
     }
   }
 }
 
-// Few tokens (T <= 8): the router is a GEMV over the 7.3 MB of W_r (DeepSeek);
-// warp w of CTA (b, ks) streams expert row 8b + w over hidden chunk ks with
-// 16-byte loads against the chunk of every token's x, staged once per CTA in
-// shared memory, and writes part[ks][t][e] like the tiled kernel.
+// Few tokens (T <= 32): the router is a GEMV over the 7.3 MB of W_r
+// (DeepSeek); warp w of CTA (b, ks) streams expert row 8b + w over hidden
+// chunk ks with 16-byte loads against the chunk of every token's x, staged
+// once per CTA in shared memory, and writes part[ks][t][e] like the tiled
+// kernel.  TMAX tokens at most, CHUNK hidden values per chunk.
+template <int TMAX, int CHUNK>
 __global__ void __launch_bounds__(256) router_stream_kernel(const float* __restrict__ Wr, int E,
                                                             int H, const void* __restrict__ x,
                                                             int xdt, int T,
                                                             float* __restrict__ part) {
   pdl_wait();
   pdl_trigger();
-  __shared__ __align__(16) float xs[kRouterStreamT][kRouterChunk];
-  const int ks = blockIdx.y, h0 = ks * kRouterChunk;
-  const int n = min(kRouterChunk, H - h0);          // multiple of 32
+  __shared__ __align__(16) float xs[TMAX][CHUNK];
+  const int ks = blockIdx.y, h0 = ks * CHUNK;
+  const int n = min(CHUNK, H - h0);                 // multiple of 32
   for (int i = threadIdx.x; i < T * n; i += blockDim.x) {
     const int t = i / n, h = i - t * n;
     xs[t][h] = act_f32(x, xdt, (int64_t)t * H + h0 + h);
@@ -174,12 +231,12 @@ __global__ void __launch_bounds__(256) router_stream_kernel(const float* __restr
   const int e = blockIdx.x * 8 + warp;
   if (e >= E) return;
   const float4* w = (const float4*)(Wr + (int64_t)e * H + h0);
-  float acc[kRouterStreamT] = {};
+  float acc[TMAX] = {};
 #pragma unroll 8
-  for (int j = lane; j < n / 4; j += 32) {   // a full chunk: 8 loads in flight per lane
+  for (int j = lane; j < n / 4; j += 32) {   // a full chunk: all loads in flight per lane
     const float4 wv = __ldcs(w + j);
 #pragma unroll
-    for (int t = 0; t < kRouterStreamT; ++t) {
+    for (int t = 0; t < TMAX; ++t) {
       if (t < T) {
         const float4 xv = *(const float4*)&xs[t][4 * j];
         acc[t] = fmaf(wv.x, xv.x, acc[t]);
@@ -190,7 +247,7 @@ __global__ void __launch_bounds__(256) router_stream_kernel(const float* __restr
     }
   }
 #pragma unroll
-  for (int t = 0; t < kRouterStreamT; ++t) {
+  for (int t = 0; t < TMAX; ++t) {
     if (t < T) {
       float v = acc[t];
 #pragma unroll
@@ -650,6 +707,8 @@ struct GroupedParams {
   const float* colinv; // 1/scale of each column's fp16 activations (nullable: 1)
   const int* coltok;   // colinv index of position pos: coltok[pos] (nullable: pos)
   int tiles;           // tiles per group
+  int ksplit;          // down only: K parts per tile, part q written at out + q * part_stride
+  int64_t part_stride;
   int nstage;
   // expert streaming (both nullable): routed expert e's matrices sit in slot
   // slot_of[e] of the stacked maps; only units of experts with
@@ -688,7 +747,8 @@ __global__ void __launch_bounds__(kThreads) grouped_kernel(const __grid_constant
   float* ex = (float*)(smem + plan.off_red);   // [64][NC] gate/up exchange
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_units = __ldg(p.n_groups) * p.tiles;
+  const int per_group = p.tiles * p.ksplit;
+  const int n_units = __ldg(p.n_groups) * per_group;
   const int nchunk = (p.nsb + L::C - 1) / L::C;
 
   if (threadIdx.x == 0) {
@@ -708,8 +768,8 @@ __global__ void __launch_bounds__(kThreads) grouped_kernel(const __grid_constant
     uint32_t lph = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-      const int4 grp = __ldg(p.groups + u / p.tiles);
-      const int tile = u % p.tiles;
+      const int4 grp = __ldg(p.groups + u / per_group);
+      const int tile = (u % per_group) / p.ksplit, part = u % p.ksplit;
       const bool shared = grp.x >= p.E;
       int eid;
       if (!unit_in_phase(p, grp, eid)) continue;
@@ -727,7 +787,8 @@ __global__ void __launch_bounds__(kThreads) grouped_kernel(const __grid_constant
         xs.base = (const __half*)p.xbase + (int64_t)grp.y * p.xstride;
         xs.rows = nullptr;
       }
-      for (int c = 0; c < nchunk && ok; ++c, ++gc) {
+      const int c_end = (part + 1) * nchunk / p.ksplit;
+      for (int c = part * nchunk / p.ksplit; c < c_end && ok; ++c, ++gc) {
         if (gc >= plan.nstage) ok = mbar_wait(&empty[ls], lph ^ 1);
         if (!ok) break;
         const int s = ls;
@@ -760,15 +821,16 @@ __global__ void __launch_bounds__(kThreads) grouped_kernel(const __grid_constant
     uint32_t cph = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-      const int4 grp = __ldg(p.groups + u / p.tiles);
-      const int tile = u % p.tiles;
+      const int4 grp = __ldg(p.groups + u / per_group);
+      const int tile = (u % per_group) / p.ksplit, part = u % p.ksplit;
       const int ncols = grp.z;
       int mat_unused;
       if (!unit_in_phase(p, grp, mat_unused)) continue;   // the loader skips it too
       const bool f16 = p.xdt == DQ_F16;      // fp16 input carries no scale
       float acc[NT][4] = {};
       float accs[NT][2][4] = {};             // fp16 input: running accumulator pairs
-      for (int c = 0; c < nchunk; ++c) {
+      const int c_end = (part + 1) * nchunk / p.ksplit;
+      for (int c = part * nchunk / p.ksplit; c < c_end; ++c) {
         const int s = cs;
         const uint32_t par = cph;
         if (++cs == plan.nstage) {
@@ -844,7 +906,7 @@ __global__ void __launch_bounds__(kThreads) grouped_kernel(const __grid_constant
       }
       if (!GATEUP) {
         const int ra = tile * 64 + 16 * cw + g, rb = ra + 8;
-        float* o = p.out + (int64_t)grp.y * p.out_stride;
+        float* o = p.out + part * p.part_stride + (int64_t)grp.y * p.out_stride;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           const int c0 = 8 * nt + 2 * t, c1 = c0 + 1;
@@ -886,38 +948,69 @@ __global__ void __launch_bounds__(kThreads) grouped_kernel(const __grid_constant
 
 // ===========================================================================
 // 6. combine: y[t] = sum_i gate[t][i] * ypos[pos(t,i)] + sum_s ypos[P + sT + t]
+// where a position's value is the sum of its `parts` K-split parts (part q at
+// ypos + q * part_stride), added in part order.
 // ===========================================================================
+__device__ __forceinline__ float4 ypos_value(const float* __restrict__ ypos, int64_t pos, int H,
+                                             int h4, int parts, int64_t part_stride) {
+  float4 v = __ldg((const float4*)(ypos + pos * H) + h4);
+  for (int q = 1; q < parts; ++q) {
+    const float4 w = __ldg((const float4*)(ypos + q * part_stride + pos * H) + h4);
+    v.x += w.x;
+    v.y += w.y;
+    v.z += w.z;
+    v.w += w.w;
+  }
+  return v;
+}
+
+template <bool PARTS>
+__device__ __forceinline__ void combine_one(const float* __restrict__ ypos,
+                                            const int32_t* __restrict__ inv,
+                                            const float* __restrict__ gate, int T, int k, int H,
+                                            int n_shared, int parts, int64_t part_stride, int64_t i,
+                                            float* __restrict__ y) {
+  const int H4 = H / 4;
+  const int64_t P = (int64_t)T * k;
+  const int t = (int)(i / H4), h4 = (int)(i % H4);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s < k; ++s) {
+    const int pos = __ldg(inv + (int64_t)t * k + s);
+    const float g = __ldg(gate + (int64_t)t * k + s);
+    const float4 v = PARTS ? ypos_value(ypos, pos, H, h4, parts, part_stride)
+                           : __ldg((const float4*)(ypos + (int64_t)pos * H) + h4);
+    acc.x = fmaf(g, v.x, acc.x);
+    acc.y = fmaf(g, v.y, acc.y);
+    acc.z = fmaf(g, v.z, acc.z);
+    acc.w = fmaf(g, v.w, acc.w);
+  }
+  for (int s = 0; s < n_shared; ++s) {
+    const int64_t pos = P + (int64_t)s * T + t;
+    const float4 v = PARTS ? ypos_value(ypos, pos, H, h4, parts, part_stride)
+                           : __ldg((const float4*)(ypos + pos * H) + h4);
+    acc.x += v.x;
+    acc.y += v.y;
+    acc.z += v.z;
+    acc.w += v.w;
+  }
+  ((float4*)y)[i] = acc;
+}
+
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ ypos,
                                                       const int32_t* __restrict__ inv,
                                                       const float* __restrict__ gate, int T,
-                                                      int k, int H, int n_shared,
+                                                      int k, int H, int n_shared, int parts,
+                                                      int64_t part_stride,
                                                       float* __restrict__ y) {
   pdl_wait();
   pdl_trigger();
-  const int H4 = H / 4;
-  const int64_t total = (int64_t)T * H4;
-  const int64_t P = (int64_t)T * k;
+  const int64_t total = (int64_t)T * (H / 4);
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
-    const int t = (int)(i / H4), h4 = (int)(i % H4);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < k; ++s) {
-      const int pos = __ldg(inv + (int64_t)t * k + s);
-      const float g = __ldg(gate + (int64_t)t * k + s);
-      const float4 v = __ldg((const float4*)(ypos + (int64_t)pos * H) + h4);
-      acc.x = fmaf(g, v.x, acc.x);
-      acc.y = fmaf(g, v.y, acc.y);
-      acc.z = fmaf(g, v.z, acc.z);
-      acc.w = fmaf(g, v.w, acc.w);
-    }
-    for (int s = 0; s < n_shared; ++s) {
-      const float4 v = __ldg((const float4*)(ypos + (P + (int64_t)s * T + t) * H) + h4);
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
-    }
-    ((float4*)y)[i] = acc;
+    if (parts == 1)
+      combine_one<false>(ypos, inv, gate, T, k, H, n_shared, 1, 0, i, y);
+    else
+      combine_one<true>(ypos, inv, gate, T, k, H, n_shared, parts, part_stride, i, y);
   }
 }
 
@@ -1012,10 +1105,16 @@ int launch_swiglu_wide(const int4* units, const int* n_units, int max_units, con
 int launch_router(const float* Wr, int E, int H, const void* x, int xdt, int T, int top_k,
                   int KS, float* part, float* logits, int32_t* idx, float* gate, cudaStream_t s,
                   bool with_topk) {
-  if (T <= kRouterStreamT && KS == (H + kRouterChunk - 1) / kRouterChunk && KS > 1 &&
-      ((uintptr_t)Wr & 15) == 0 && H % 4 == 0) {
+  const int chunk = router_chunk(T);
+  if (chunk && KS == (H + chunk - 1) / chunk && KS > 1 && ((uintptr_t)Wr & 15) == 0 &&
+      H % 4 == 0) {
     const dim3 g((unsigned)((E + 7) / 8), (unsigned)KS);
-    launch_pdl(router_stream_kernel, g, dim3(256), 0, s, 0, Wr, E, H, x, xdt, T, part);
+    if (T <= kRouterStreamT)
+      launch_pdl(router_stream_kernel<kRouterStreamT, kRouterChunk>, g, dim3(256), 0, s, 0, Wr,
+                 E, H, x, xdt, T, part);
+    else
+      launch_pdl(router_stream_kernel<kRouterStreamT2, kRouterChunk2>, g, dim3(256), 0, s, 0, Wr,
+                 E, H, x, xdt, T, part);
   } else {
     dim3 g1((unsigned)((E + 63) / 64), (unsigned)((T + 31) / 32), (unsigned)KS);
     launch_pdl(router_logits_kernel, dim3(g1), dim3(128), 0, s, 0, Wr, E, H, x, xdt, T, KS, part);
@@ -1126,6 +1225,7 @@ int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, floa
   gu.colinv = xh_inv;
   gu.coltok = tok;
   gu.tiles = d.ffn / 32;
+  gu.ksplit = 1;
   gu.rows_per_expert = d.ffn;
   if (!ms) {
     if (general) {
@@ -1196,10 +1296,13 @@ int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, floa
   dn.colinv = hinv;
   dn.coltok = nullptr;
   dn.tiles = d.hidden / 64;
+  dn.ksplit = ms ? 1 : pl.DS;
+  dn.part_stride = (int64_t)pl.NP * d.hidden;
   dn.rows_per_expert = d.hidden;
   if (!ms) {
     if (general) {
-      rc = launch_grouped_fmt<false>(d.fmt, pl.NT, dn, pl.G_max * dn.tiles, s, d.E, d.n_shared);
+      rc = launch_grouped_fmt<false>(d.fmt, pl.NT, dn, pl.G_max * dn.tiles * dn.ksplit, s, d.E,
+                                     d.n_shared);
       if (rc != DQ_OK) return rc;
     }
     if (pl.single) {
@@ -1228,7 +1331,8 @@ int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, floa
 
   const int64_t n4 = (int64_t)T * d.hidden / 4;
   const int cgrid = (int)std::min<int64_t>((n4 + 255) / 256, 4096);
-  launch_pdl(combine_kernel, dim3(cgrid), dim3(256), 0, s, 0, ypos, inv, gate, T, d.top_k, d.hidden, d.n_shared, y);
+  launch_pdl(combine_kernel, dim3(cgrid), dim3(256), 0, s, 0, ypos, inv, gate, T, d.top_k,
+             d.hidden, d.n_shared, pl.DS, (int64_t)pl.NP * d.hidden, y);
   return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
 }
 

@@ -21,6 +21,7 @@ struct MoePlan {
   bool wide;        // wide units are possible (some expert may get > 32 tokens)
   bool single;      // one-token groups run on the block-diagonal kernel (moe_b1.cu)
   int G1_max;       // upper bound of one-token groups
+  int DS;           // K parts of the grouped down products (ypos holds DS copies)
   size_t off_part, off_logits, off_idx, off_gate, off_offsets, off_sorted, off_inv, off_tok,
       off_groups, off_ngroups, off_h, off_ypos, off_units, off_nunits, off_x16t, off_xinvt,
       off_x16, off_xinv, off_g, off_u, off_h16, off_hinv, off_g1, off_ng1, total;

@@ -30,35 +30,36 @@ __device__ __forceinline__ float act(const void* x, int xdt, int64_t i) {
 }
 }  // namespace
 
-// one CTA (256 threads) per row: out[row][k] = fp16(in[row][k] * 2^e),
-// inv[row] = 2^-e, with max|in[row]| * 2^e in [2^14, 2^15)
-__global__ void __launch_bounds__(256) x16_tokens_kernel(const void* __restrict__ x, int xdt,
-                                                         int rows, int K, __half* __restrict__ out,
-                                                         float* __restrict__ inv) {
+// one CTA per row: out[row][k] = fp16(in[row][k] * 2^e), inv[row] = 2^-e, with
+// max|in[row]| * 2^e in [2^14, 2^15).  256 threads, or 1024 for rows longer
+// than 256 * R values, so that a row of up to 1024 * R values is read once,
+// every load in flight before any is used.
+__global__ void __launch_bounds__(1024) x16_tokens_kernel(const void* __restrict__ x, int xdt,
+                                                          int rows, int K, __half* __restrict__ out,
+                                                          float* __restrict__ inv) {
   pdl_wait();
   pdl_trigger();
-  __shared__ float red[8];
+  __shared__ float red[32];
   constexpr int R = 32;                 // values kept in registers per thread
-  const int row = blockIdx.x;
+  const int row = blockIdx.x, nt = blockDim.x, nw = nt >> 5;
   const int64_t base = (int64_t)row * K;
-  const bool in_regs = K <= 256 * R;
+  const bool in_regs = K <= nt * R;
   float v[R];
   float amax = 0.f;
   if (in_regs) {
-    // every load of the row is issued before any is used
 #pragma unroll
     for (int i = 0; i < R; ++i) {
-      const int k = threadIdx.x + 256 * i;
+      const int k = threadIdx.x + nt * i;
       v[i] = k < K ? act(x, xdt, base + k) : 0.f;
     }
 #pragma unroll
     for (int i = 0; i < R; ++i) amax = fmaxf(amax, fabsf(v[i]));
   } else {
-    for (int k0 = threadIdx.x; k0 < K; k0 += 256 * 8) {
+    for (int k0 = threadIdx.x; k0 < K; k0 += nt * 8) {
       float a[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const int k = k0 + 256 * i;
+        const int k = k0 + nt * i;
         a[i] = k < K ? act(x, xdt, base + k) : 0.f;
       }
 #pragma unroll
@@ -69,27 +70,26 @@ __global__ void __launch_bounds__(256) x16_tokens_kernel(const void* __restrict_
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
   __syncthreads();
   amax = red[0];
-#pragma unroll
-  for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
+  for (int i = 1; i < nw; ++i) amax = fmaxf(amax, red[i]);
   float sc, iv;
   pow2_scale(amax, sc, iv);
   if (in_regs) {
 #pragma unroll
     for (int i = 0; i < R; ++i) {
-      const int k = threadIdx.x + 256 * i;
+      const int k = threadIdx.x + nt * i;
       if (k < K) out[base + k] = __float2half_rn(v[i] * sc);
     }
   } else {
-    for (int k0 = threadIdx.x; k0 < K; k0 += 256 * 8) {
+    for (int k0 = threadIdx.x; k0 < K; k0 += nt * 8) {
       float a[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const int k = k0 + 256 * i;
+        const int k = k0 + nt * i;
         a[i] = k < K ? act(x, xdt, base + k) : 0.f;
       }
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const int k = k0 + 256 * i;
+        const int k = k0 + nt * i;
         if (k < K) out[base + k] = __float2half_rn(a[i] * sc);
       }
     }
@@ -98,7 +98,10 @@ __global__ void __launch_bounds__(256) x16_tokens_kernel(const void* __restrict_
 }
 
 // X16[pos] = x16[tok[pos]], xinv[pos] = tinv[tok[pos]] (tinv null: 1) for the
-// positions of the wide units; one CTA per unit
+// positions of the wide units.  Grid (kGatherSplit, units): CTA (j, u) copies
+// the rows j * 8 + warp (+ 8 kGatherSplit ...) of unit u, one warp per row.
+constexpr int kGatherSplit = 8;
+
 __global__ void __launch_bounds__(256) gather_x16_kernel(const int4* __restrict__ units,
                                                          const int* __restrict__ n_units,
                                                          const int32_t* __restrict__ tok,
@@ -108,14 +111,15 @@ __global__ void __launch_bounds__(256) gather_x16_kernel(const int4* __restrict_
                                                          float* __restrict__ xinv) {
   pdl_wait();
   pdl_trigger();
-  if ((int)blockIdx.x >= __ldg(n_units)) return;
-  const int4 u = __ldg(units + blockIdx.x);
+  if ((int)blockIdx.y >= __ldg(n_units)) return;
+  const int4 u = __ldg(units + blockIdx.y);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int n = warp; n < u.z; n += 8) {
+  for (int n = blockIdx.x * 8 + warp; n < u.z; n += 8 * kGatherSplit) {
     const int pos = u.y + n;
     const int t = __ldg(tok + pos);
     const uint4* src = (const uint4*)(x16 + (int64_t)t * K);
     uint4* dst = (uint4*)(X16 + (int64_t)pos * K);
+#pragma unroll 4
     for (int k = lane; k < K / 8; k += 32) dst[k] = __ldg(src + k);
     if (lane == 0) xinv[pos] = tinv ? __ldg(tinv + t) : 1.f;
   }
@@ -142,7 +146,9 @@ __global__ void __launch_bounds__(256) swiglu_wide_kernel(const int4* __restrict
 
 int launch_x16_rows(const void* x, int xdt, int rows, int K, __half* out, float* inv,
                     cudaStream_t s) {
-  if (launch_pdl(x16_tokens_kernel, dim3(rows), dim3(256), 0, s, 0, x, xdt, rows, K, out, inv) !=
+  const int threads = K > 256 * 32 ? 1024 : 256;
+  if (launch_pdl(x16_tokens_kernel, dim3(rows), dim3(threads), 0, s, 0, x, xdt, rows, K, out,
+                 inv) !=
       cudaSuccess)
     return DQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
@@ -151,8 +157,8 @@ int launch_x16_rows(const void* x, int xdt, int rows, int K, __half* out, float*
 int launch_gather_x16(const int4* units, const int* n_units, int max_units, const int32_t* tok,
                       const __half* x16, const float* tinv, int K, __half* X16, float* xinv,
                       cudaStream_t s) {
-  const unsigned grid = (unsigned)(max_units > 0 ? max_units : 1);
-  if (launch_pdl(gather_x16_kernel, dim3(grid), dim3(256), 0, s, 0, units, n_units, tok, x16, tinv,
+  const dim3 grid((unsigned)kGatherSplit, (unsigned)(max_units > 0 ? max_units : 1));
+  if (launch_pdl(gather_x16_kernel, grid, dim3(256), 0, s, 0, units, n_units, tok, x16, tinv,
                  K, X16, xinv) != cudaSuccess)
     return DQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;

@@ -155,6 +155,11 @@ def _moe_case(dq, orc, fmt, E, k, H, F, ns, T, xdt, seed, tokens=None, cached=No
     (Q8_0, 8, 2, 2048, 1024, 1, 1, 1),
     (Q6_K, 4, 2, 4096, 2048, 1, 1, 2),
     (Q4_K, 16, 4, 1024, 512, 1, 1, 1),
+    # few down units for the grid: the down products split over K (two and
+    # four parts, shared expert included), summed in part order by the combine
+    (Q6_K, 4, 2, 2048, 2048, 1, 6, 2),
+    (Q8_0, 8, 2, 1024, 4096, 1, 12, 2),
+    (NVFP4, 8, 2, 1024, 4096, 0, 1, 1),
 ])
 def test_moe_forward_small(dq, orc, fmt, E, k, H, F, ns, T, xdt):
     err, _ = _moe_case(dq, orc, fmt, E, k, H, F, ns, T, xdt, seed=3000 + E * 7 + T)
