@@ -1093,7 +1093,7 @@ int launch_grouped_fmt(int fmt, int nt, const GroupedParams& gp, int units_max, 
 int launch_tc_gemm(int fmt, const void* W, const void* Wsh, int E, int n_shared,
                    int rows_per_expert, int K, const int4* units, const int* n_units,
                    int max_units, const __half* X16, int64_t npos, const float* xinv, float* out,
-                   int64_t out_stride, bool many_units, cudaStream_t s);
+                   int64_t out_stride, cudaStream_t s);
 int launch_x16_rows(const void* x, int xdt, int rows, int K, __half* out, float* inv,
                     cudaStream_t s);
 int launch_gather_x16(const int4* units, const int* n_units, int max_units, const int32_t* tok,
@@ -1254,17 +1254,15 @@ int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, floa
     }
   }
 
-  // wide units: gathered fp16 rows, tensor-core gate and up GEMMs, SwiGLU;
-  // many: routed experts are expected above the threshold (prefill chunks)
-  const bool many = pl.P > (int64_t)kWide * d.E;
+  // wide units: gathered fp16 rows, tensor-core gate and up GEMMs, SwiGLU
   if (pl.wide) {
     rc = launch_gather_x16(units, nunits, pl.U_max, tok, xh, xh_inv, d.hidden, x16, xinv, s);
     if (rc != DQ_OK) return rc;
     rc = launch_tc_gemm(d.fmt, d.w_gate, d.sh_gate, d.E, d.n_shared, d.ffn, d.hidden, units,
-                        nunits, pl.U_max, x16, pl.NP, xinv, G, d.ffn, many, s);
+                        nunits, pl.U_max, x16, pl.NP, xinv, G, d.ffn, s);
     if (rc != DQ_OK) return rc;
     rc = launch_tc_gemm(d.fmt, d.w_up, d.sh_up, d.E, d.n_shared, d.ffn, d.hidden, units, nunits,
-                        pl.U_max, x16, pl.NP, xinv, U, d.ffn, many, s);
+                        pl.U_max, x16, pl.NP, xinv, U, d.ffn, s);
     if (rc != DQ_OK) return rc;
     rc = launch_swiglu_wide(units, nunits, pl.U_max, G, U, d.ffn, h, s);
     if (rc != DQ_OK) return rc;
@@ -1325,7 +1323,7 @@ int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, floa
   }
   if (pl.wide) {
     rc = launch_tc_gemm(d.fmt, d.w_down, d.sh_down, d.E, d.n_shared, d.hidden, d.ffn, units,
-                        nunits, pl.U_max, h16, pl.NP, hinv, ypos, d.hidden, many, s);
+                        nunits, pl.U_max, h16, pl.NP, hinv, ypos, d.hidden, s);
     if (rc != DQ_OK) return rc;
   }
 
