@@ -126,9 +126,44 @@ __device__ __forceinline__ float act_f32(const void* x, int dtype, int64_t i) {
   return __half2float(__ushort_as_half(u));
 }
 
+// The same with the dtype fixed at compile time: loads in an unrolled loop
+// are all issued before the first is used (a run-time dtype branch around
+// each load keeps them one at a time).
+template <int XDT>
+__device__ __forceinline__ float act_t(const void* x, int64_t i) {
+  if (XDT == DQ_F32) return __ldg((const float*)x + i);
+  const unsigned short u = __ldg((const unsigned short*)x + i);
+  if (XDT == DQ_BF16) return __uint_as_float((uint32_t)u << 16);
+  return __half2float(__ushort_as_half(u));
+}
+
+// 16 bytes of activations (8 fp16 / bf16 or 4 fp32 values) as fp32.
+template <int XDT>
+__device__ __forceinline__ void act_vec(const uint4& r, float* f) {
+  const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+  if (XDT == DQ_F32) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) f[j] = __uint_as_float(w[j]);
+  } else if (XDT == DQ_BF16) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      f[2 * j] = __uint_as_float(w[j] << 16);
+      f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 v = __half22float2(u32_as_h2(w[j]));
+      f[2 * j] = v.x;
+      f[2 * j + 1] = v.y;
+    }
+  }
+}
+
+template <int XDT>
 __global__ void __launch_bounds__(128) router_logits_kernel(const float* __restrict__ Wr, int E,
                                                             int H, const void* __restrict__ x,
-                                                            int xdt, int T, int KS,
+                                                            int T, int KS,
                                                             float* __restrict__ part) {
   pdl_wait();
   pdl_trigger();
@@ -156,7 +191,7 @@ __global__ void __launch_bounds__(128) router_logits_kernel(const float* __restr
     for (int r = 0; r < 8; ++r) {
       const int i = tid + 128 * r;
       const int hh = (i & 7) | ((i >> 8) << 3), t = (i >> 3) & 31;
-      xr[r] = (t0 + t < T) ? act_f32(x, xdt, (int64_t)(t0 + t) * H + h0 + hh) : 0.f;
+      xr[r] = (t0 + t < T) ? act_t<XDT>(x, (int64_t)(t0 + t) * H + h0 + hh) : 0.f;
     }
   };
   auto store = [&](int b) {
@@ -212,37 +247,68 @@ __global__ void __launch_bounds__(128) router_logits_kernel(const float* __restr
 // chunk ks with 16-byte loads against the chunk of every token's x, staged
 // once per CTA in shared memory, and writes part[ks][t][e] like the tiled
 // kernel.  TMAX tokens at most, CHUNK hidden values per chunk.
-template <int TMAX, int CHUNK>
+template <int TMAX, int CHUNK, int XDT>
 __global__ void __launch_bounds__(256) router_stream_kernel(const float* __restrict__ Wr, int E,
                                                             int H, const void* __restrict__ x,
-                                                            int xdt, int T,
-                                                            float* __restrict__ part) {
+                                                            int T, float* __restrict__ part) {
   pdl_wait();
   pdl_trigger();
   __shared__ __align__(16) float xs[TMAX][CHUNK];
   const int ks = blockIdx.y, h0 = ks * CHUNK;
   const int n = min(CHUNK, H - h0);                 // multiple of 32
-  for (int i = threadIdx.x; i < T * n; i += blockDim.x) {
-    const int t = i / n, h = i - t * n;
-    xs[t][h] = act_f32(x, xdt, (int64_t)t * H + h0 + h);
+  // every load of the call is issued before any is used: the chunk of x
+  // (16-byte loads, at most kVec per thread) and this warp's row of W_r
+  constexpr int kES = XDT == DQ_F32 ? 4 : 2;        // bytes per activation
+  constexpr int kVE = 16 / kES;                     // activations per 16-byte load
+  constexpr int kVec = TMAX * CHUNK / kVE / 256;
+  const int nv = n / kVE, total = T * nv;
+  uint4 xr[kVec];
+#pragma unroll
+  for (int j = 0; j < kVec; ++j) {
+    const int i = threadIdx.x + 256 * j;
+    if (i < total) {
+      const int t = i / nv, v = i - t * nv;
+      xr[j] = __ldg((const uint4*)((const char*)x + ((int64_t)t * H + h0 + v * kVE) * kES));
+    }
   }
-  __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * 8 + warp;
-  if (e >= E) return;
-  const float4* w = (const float4*)(Wr + (int64_t)e * H + h0);
-  float acc[TMAX] = {};
-#pragma unroll 8
-  for (int j = lane; j < n / 4; j += 32) {   // a full chunk: all loads in flight per lane
-    const float4 wv = __ldcs(w + j);
+  constexpr int kW = CHUNK / 4 / 32;                // float4 of W_r per lane
+  float4 wv[kW];
+  if (e < E) {
+    const float4* w = (const float4*)(Wr + (int64_t)e * H + h0);
 #pragma unroll
-    for (int t = 0; t < TMAX; ++t) {
-      if (t < T) {
-        const float4 xv = *(const float4*)&xs[t][4 * j];
-        acc[t] = fmaf(wv.x, xv.x, acc[t]);
-        acc[t] = fmaf(wv.y, xv.y, acc[t]);
-        acc[t] = fmaf(wv.z, xv.z, acc[t]);
-        acc[t] = fmaf(wv.w, xv.w, acc[t]);
+    for (int j = 0; j < kW; ++j)
+      wv[j] = lane + 32 * j < n / 4 ? __ldcs(w + lane + 32 * j) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int j = 0; j < kVec; ++j) {
+    const int i = threadIdx.x + 256 * j;
+    if (i < total) {
+      const int t = i / nv, v = i - t * nv;
+      float f[kVE];
+      act_vec<XDT>(xr[j], f);
+#pragma unroll
+      for (int q = 0; q < kVE; q += 4)
+        *(float4*)&xs[t][v * kVE + q] = make_float4(f[q], f[q + 1], f[q + 2], f[q + 3]);
+    }
+  }
+  __syncthreads();
+  if (e >= E) return;
+  float acc[TMAX] = {};
+#pragma unroll
+  for (int j = 0; j < kW; ++j) {
+    if (lane + 32 * j < n / 4) {
+      const float4 w4 = wv[j];
+#pragma unroll
+      for (int t = 0; t < TMAX; ++t) {
+        if (t < T) {
+          const float4 xv = *(const float4*)&xs[t][4 * (lane + 32 * j)];
+          acc[t] = fmaf(w4.x, xv.x, acc[t]);
+          acc[t] = fmaf(w4.y, xv.y, acc[t]);
+          acc[t] = fmaf(w4.z, xv.z, acc[t]);
+          acc[t] = fmaf(w4.w, xv.w, acc[t]);
+        }
       }
     }
   }
@@ -1106,18 +1172,30 @@ int launch_router(const float* Wr, int E, int H, const void* x, int xdt, int T, 
                   int KS, float* part, float* logits, int32_t* idx, float* gate, cudaStream_t s,
                   bool with_topk) {
   const int chunk = router_chunk(T);
+  const bool vec_ok = ((uintptr_t)x & 15) == 0 && H % 8 == 0;
   if (chunk && KS == (H + chunk - 1) / chunk && KS > 1 && ((uintptr_t)Wr & 15) == 0 &&
-      H % 4 == 0) {
+      H % 4 == 0 && vec_ok) {
     const dim3 g((unsigned)((E + 7) / 8), (unsigned)KS);
-    if (T <= kRouterStreamT)
-      launch_pdl(router_stream_kernel<kRouterStreamT, kRouterChunk>, g, dim3(256), 0, s, 0, Wr,
-                 E, H, x, xdt, T, part);
-    else
-      launch_pdl(router_stream_kernel<kRouterStreamT2, kRouterChunk2>, g, dim3(256), 0, s, 0, Wr,
-                 E, H, x, xdt, T, part);
+#define DQ_RS(TM, CH, XD) \
+  launch_pdl(router_stream_kernel<TM, CH, XD>, g, dim3(256), 0, s, 0, Wr, E, H, x, T, part)
+    if (T <= kRouterStreamT) {
+      if (xdt == DQ_F32) DQ_RS(kRouterStreamT, kRouterChunk, DQ_F32);
+      else if (xdt == DQ_BF16) DQ_RS(kRouterStreamT, kRouterChunk, DQ_BF16);
+      else DQ_RS(kRouterStreamT, kRouterChunk, DQ_F16);
+    } else {
+      if (xdt == DQ_F32) DQ_RS(kRouterStreamT2, kRouterChunk2, DQ_F32);
+      else if (xdt == DQ_BF16) DQ_RS(kRouterStreamT2, kRouterChunk2, DQ_BF16);
+      else DQ_RS(kRouterStreamT2, kRouterChunk2, DQ_F16);
+    }
+#undef DQ_RS
   } else {
     dim3 g1((unsigned)((E + 63) / 64), (unsigned)((T + 31) / 32), (unsigned)KS);
-    launch_pdl(router_logits_kernel, dim3(g1), dim3(128), 0, s, 0, Wr, E, H, x, xdt, T, KS, part);
+    if (xdt == DQ_F32)
+      launch_pdl(router_logits_kernel<DQ_F32>, g1, dim3(128), 0, s, 0, Wr, E, H, x, T, KS, part);
+    else if (xdt == DQ_BF16)
+      launch_pdl(router_logits_kernel<DQ_BF16>, g1, dim3(128), 0, s, 0, Wr, E, H, x, T, KS, part);
+    else
+      launch_pdl(router_logits_kernel<DQ_F16>, g1, dim3(128), 0, s, 0, Wr, E, H, x, T, KS, part);
   }
   if (cudaGetLastError() != cudaSuccess) return DQ_ERR_CUDA;
   if (!with_topk) return DQ_OK;

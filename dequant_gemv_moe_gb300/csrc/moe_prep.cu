@@ -23,9 +23,12 @@ __device__ __forceinline__ float wmax(float v) {
   return v;
 }
 
-__device__ __forceinline__ float act(const void* x, int xdt, int64_t i) {
-  if (xdt == DQ_F32) return __ldg((const float*)x + i);
-  if (xdt == DQ_BF16) return __uint_as_float((uint32_t)__ldg((const unsigned short*)x + i) << 16);
+// the dtype is a compile-time constant, so that the loads of an unrolled
+// loop are all in flight before the first is used
+template <int XDT>
+__device__ __forceinline__ float act(const void* x, int64_t i) {
+  if (XDT == DQ_F32) return __ldg((const float*)x + i);
+  if (XDT == DQ_BF16) return __uint_as_float((uint32_t)__ldg((const unsigned short*)x + i) << 16);
   return __half2float(__ldg((const __half*)x + i));
 }
 }  // namespace
@@ -34,8 +37,9 @@ __device__ __forceinline__ float act(const void* x, int xdt, int64_t i) {
 // max|in[row]| * 2^e in [2^14, 2^15).  256 threads, or 1024 for rows longer
 // than 256 * R values, so that a row of up to 1024 * R values is read once,
 // every load in flight before any is used.
-__global__ void __launch_bounds__(1024) x16_tokens_kernel(const void* __restrict__ x, int xdt,
-                                                          int rows, int K, __half* __restrict__ out,
+template <int XDT>
+__global__ void __launch_bounds__(1024) x16_tokens_kernel(const void* __restrict__ x, int rows,
+                                                          int K, __half* __restrict__ out,
                                                           float* __restrict__ inv) {
   pdl_wait();
   pdl_trigger();
@@ -50,7 +54,7 @@ __global__ void __launch_bounds__(1024) x16_tokens_kernel(const void* __restrict
 #pragma unroll
     for (int i = 0; i < R; ++i) {
       const int k = threadIdx.x + nt * i;
-      v[i] = k < K ? act(x, xdt, base + k) : 0.f;
+      v[i] = k < K ? act<XDT>(x, base + k) : 0.f;
     }
 #pragma unroll
     for (int i = 0; i < R; ++i) amax = fmaxf(amax, fabsf(v[i]));
@@ -60,7 +64,7 @@ __global__ void __launch_bounds__(1024) x16_tokens_kernel(const void* __restrict
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int k = k0 + nt * i;
-        a[i] = k < K ? act(x, xdt, base + k) : 0.f;
+        a[i] = k < K ? act<XDT>(x, base + k) : 0.f;
       }
 #pragma unroll
       for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(a[i]));
@@ -85,7 +89,7 @@ __global__ void __launch_bounds__(1024) x16_tokens_kernel(const void* __restrict
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int k = k0 + nt * i;
-        a[i] = k < K ? act(x, xdt, base + k) : 0.f;
+        a[i] = k < K ? act<XDT>(x, base + k) : 0.f;
       }
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -147,10 +151,17 @@ __global__ void __launch_bounds__(256) swiglu_wide_kernel(const int4* __restrict
 int launch_x16_rows(const void* x, int xdt, int rows, int K, __half* out, float* inv,
                     cudaStream_t s) {
   const int threads = K > 256 * 32 ? 1024 : 256;
-  if (launch_pdl(x16_tokens_kernel, dim3(rows), dim3(threads), 0, s, 0, x, xdt, rows, K, out,
-                 inv) !=
-      cudaSuccess)
-    return DQ_ERR_CUDA;
+  cudaError_t e;
+  if (xdt == DQ_F32)
+    e = launch_pdl(x16_tokens_kernel<DQ_F32>, dim3(rows), dim3(threads), 0, s, 0, x, rows, K, out,
+                   inv);
+  else if (xdt == DQ_BF16)
+    e = launch_pdl(x16_tokens_kernel<DQ_BF16>, dim3(rows), dim3(threads), 0, s, 0, x, rows, K,
+                   out, inv);
+  else
+    e = launch_pdl(x16_tokens_kernel<DQ_F16>, dim3(rows), dim3(threads), 0, s, 0, x, rows, K, out,
+                   inv);
+  if (e != cudaSuccess) return DQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
 }
 
