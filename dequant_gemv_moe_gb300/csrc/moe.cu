@@ -595,6 +595,72 @@ __global__ void __launch_bounds__(1024) permute_kernel(int32_t* idx, int T,
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int P = T * k;
   const bool own = tk.part != nullptr;   // the indices are chosen here: read them from sidx
+  if (T == 1 && own && groups1 && !units && !cx16) {
+    // one token, every selected expert a one-token group (the decode step):
+    // the logits as below (every thread sums the partials of its experts in
+    // the same order: bit-identical), then warp 0 alone, no further block
+    // barriers; every output the general path writes for this case is
+    // written: an expert's position is its rank among the selected experts
+    // (expert order), its pair's token 0.
+    float* lg = (float*)&cntw[0][0];
+    for (int e = tid; e < E; e += 1024) {
+      const float* pp = tk.part + e;
+      float a = 0.f;
+      for (int q0 = 0; q0 < tk.KS; q0 += 8) {
+        float b[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) b[j] = q0 + j < tk.KS ? __ldcg(pp + (int64_t)(q0 + j) * E) : 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (q0 + j < tk.KS) a += b[j];
+      }
+      lg[e] = a;
+      if (tk.logits) tk.logits[e] = a;
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    float v[8];
+    int id[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int e = lane + 32 * j;
+      v[j] = e < E ? lg[e] : -INFINITY;
+      id[j] = e < E ? e : 0x7fffffff;
+    }
+    topk_select(v, id, k, 0, lane, idx, tk.gate, sidx);
+    __syncwarp();
+    int sel[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sel[i] = i < k ? sidx[i] : 0x7fffffff;
+    if (lane < k) {
+      const int e = sel[lane];
+      int rank = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) rank += sel[i] < e ? 1 : 0;
+      if (sorted) sorted[rank] = lane;
+      if (inv) inv[lane] = rank;
+      if (tok) tok[rank] = 0;
+      groups1[rank] = make_int4(e, rank, 0, 0);
+    }
+    for (int sh = lane; sh < n_shared; sh += 32) {
+      if (tok) tok[P + sh] = 0;
+      groups1[k + sh] = make_int4(E + sh, P + sh, 0, 0);
+    }
+    if (offsets)
+      for (int e = lane; e <= E; e += 32) {
+        int c = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) c += sel[i] < e ? 1 : 0;
+        offsets[e] = c;
+      }
+    if (lane == 0) {
+      if (groups) *n_groups = 0;
+      n_groups1[0] = k + n_shared;
+      n_groups1[1] = 0;   // the one-token kernels' work counters
+      n_groups1[2] = 0;
+    }
+    return;
+  }
   if (own) {
     // logits of the T <= 32 tokens: every thread sums the KS partials of its
     // (token, expert) entries in a fixed order (q ascending), all loads in
