@@ -70,9 +70,9 @@ def test_gpu_arm_line_assembly(monkeypatch, capsys):
     assert {"value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step"} <= set(line["e2e"])
     assert line["gpu_launches"] == 40 * 7
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(line["clocks"])
-    # the workload config carries no measurement; the spec GEMV sits in the roofline
+    # the workload config carries no measurement; the 70B gate GEMV sits in the roofline
     assert "frac_of_hbm" not in line["config"]
-    ns = rf["north_star"]
+    ns = rf["gemv_70b_gate_b1"]
     assert ns["bar"] == 0.8 and ns["meets_bar_back_to_back"] is True
     assert ns["frac_back_to_back"] == pytest.approx(5500.0 / rf["peak"], rel=1e-3)
     assert line["timing"]["repetitions"] == 7
