@@ -53,7 +53,7 @@ def parse():
     ap.add_argument("--oracle-threads", type=int, default=None, help=argparse.SUPPRESS)
     ap.add_argument("--case", default=None,
                     help="profiling aid: run only one workload a few times and exit "
-                         "(gemv70b | layer8b | formats70b | mixtral | deepseek1 | deepseek8 | "
+                         "(gemv70b | layer8b | formats70b | dequant70b | mixtral | deepseek1 | deepseek8 | "
                          "deepseek256 | ds64 | ds32t1 | prefill32 | prefill32nvfp4 | streamed)")
     return ap.parse_args()
 
@@ -70,6 +70,8 @@ def run_case(args):
                                                         with_e2e=False).items()}))
     elif args.case == "mixtral":
         print(json.dumps(bench_moe(torch, dq, synth.MOE_MIXTRAL, 16, reps=max(1, args.steps))))
+    elif args.case == "dequant70b":
+        print(json.dumps(bench_dequant(torch, dq, reps=max(1, args.steps))))
     elif args.case == "formats70b":
         print(json.dumps(bench_gemv_70b_formats(torch, dq, reps=max(1, args.steps))))
     elif args.case == "ds64":
@@ -684,6 +686,38 @@ def bench_gemv_70b_formats(torch, dq, reps=30, fmts=((Q4_K, "q4_k"), (2, "q6_k")
     return out
 
 
+def bench_dequant(torch, dq, reps=10, fmts=((Q4_K, "q4_k"), (2, "q6_k"), (3, "q8_0"))):
+    """The decode step on its own (dq_dequant: packed blocks -> fp32) on the 70B
+    gate matrix (28672 x 8192): bytes read + written per launch over the CUDA-
+    event time of `reps` launches back to back (inputs and outputs far above
+    L2)."""
+    N, K = 28672, 8192
+    n = N * K
+    out = {}
+    g = synth.streams(synth.BASE_SEED + 9, 1)
+    o = torch.empty(n, dtype=torch.float32, device="cuda")
+    for fmt, name in fmts:
+        W = torch.from_numpy(synth.quant_matrix(g[0], fmt, N, K)).cuda()
+        for _ in range(3):
+            dq.dequant(fmt, W, n, out=o)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            dq.dequant(fmt, W, n, out=o)
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / reps
+        nb = weight_bytes(fmt, N, K) + 4 * n
+        out["%s_%dx%d" % (name, N, K)] = {"us": round(us, 2), "bytes": nb,
+                                          "GBps": round(nb / (us / 1e6) / 1e9, 1)}
+        del W
+    del o
+    torch.cuda.empty_cache()
+    return out
+
+
 def prefill_cfg(fmt):
     """The prefill-chunk workload of the tensor-core expert GEMM: DeepSeek-V3
     expert shapes (hidden 7168, FFN 2048, top-8 + 1 shared) with 32 routed
@@ -887,6 +921,10 @@ def run_ours(args):
             v["frac_of_hbm"] = round(v["weight_GBps"] / peak, 4)
             v["frac_of_hbm_back_to_back"] = round(v["weight_GBps_back_to_back"] / peak, 4)
         extra["gemv_70b_more_formats"] = fx
+        dqt = bench_dequant(torch, dq)
+        for v in dqt.values():
+            v["frac_of_hbm"] = round(v["GBps"] / peak, 4)
+        extra["dequant_70b_gate"] = dqt
         if not args.no_moe:
             moe = {}
             moe["mixtral_T16"] = bench_moe(torch, dq, synth.MOE_MIXTRAL, 16)

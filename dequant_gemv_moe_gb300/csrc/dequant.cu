@@ -9,8 +9,12 @@
 // bit-identical to any exact evaluation.
 //
 // One thread per output weight (coalesced fp32 stores); the block's few
-// header bytes are re-read by its threads through L1.  This kernel is for
-// bit-exact checking, not for speed: the GEMV kernels never materialise W.
+// header bytes are re-read by its threads through L1.  Q4_K, Q6_K and Q8_0
+// also have a wide form (one thread per 16 / 16 / 8 consecutive weights: the
+// scale fields read once, the quant bytes as 16-bit loads, 16-byte stores),
+// taken when the output is 16-byte aligned; it evaluates every weight with
+// the same expression, so both forms give the same bits.  The GEMV kernels
+// never materialise W: this is the decode step on its own.
 #include "common.cuh"
 
 namespace dqmoe {
@@ -74,6 +78,104 @@ __global__ void dequant_q80_kernel(const uint8_t* __restrict__ blocks, int64_t n
   if (blk >= nblk) return;
   const uint8_t* b = blocks + blk * 34;
   out[gid] = h16(b) * (float)(int8_t)b[2 + (gid & 31)];
+}
+
+// N bytes at an even address as N/2 16-bit loads (blocks are 2-byte aligned).
+template <int N>
+__device__ __forceinline__ void bytesN(const uint8_t* p, uint8_t (&v)[N]) {
+#pragma unroll
+  for (int k = 0; k < N / 2; ++k) {
+    const unsigned short u = __ldg((const unsigned short*)p + k);
+    v[2 * k] = (uint8_t)(u & 0xFF);
+    v[2 * k + 1] = (uint8_t)(u >> 8);
+  }
+}
+__device__ __forceinline__ void bytes8(const uint8_t* p, uint8_t (&v)[8]) { bytesN<8>(p, v); }
+
+template <int N>
+__device__ __forceinline__ void storeN(float* o, const float (&v)[N]) {
+#pragma unroll
+  for (int k = 0; k < N / 4; ++k)
+    ((float4*)o)[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+}
+__device__ __forceinline__ void store8(float* o, const float (&v)[8]) { storeN<8>(o, v); }
+
+// Wide forms: thread g decodes weights NW g .. NW g + NW - 1 (Q4_K, Q6_K: 16,
+// within one 32-weight run; Q8_0: 8).
+constexpr int kNW = 16;
+__global__ void dequant8_q4k_kernel(const uint8_t* __restrict__ blocks, int64_t nblk,
+                                    float* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t blk = g / (256 / kNW);
+  if (blk >= nblk) return;
+  const int i0 = (int)(g % (256 / kNW)) * kNW;
+  const uint8_t* b = blocks + blk * 144;
+  const float d = h16(b), dmin = h16(b + 2);
+  const uint8_t* s = b + 4;
+  const int j = i0 >> 5;
+  int sc, m;
+  if (j < 4) {
+    sc = s[j] & 63;
+    m = s[j + 4] & 63;
+  } else {
+    sc = (s[j + 4] & 15) | ((s[j - 4] >> 6) << 4);
+    m = (s[j + 4] >> 4) | ((s[j] >> 6) << 4);
+  }
+  uint8_t q8[kNW];
+  bytesN<kNW>(b + 16 + 32 * (i0 >> 6) + (i0 & 31), q8);
+  float v[kNW];
+#pragma unroll
+  for (int k = 0; k < kNW; ++k) {
+    const int q = (i0 & 32) ? (q8[k] >> 4) : (q8[k] & 15);
+    v[k] = __fmaf_rn(d * (float)sc, (float)q, -(dmin * (float)m));
+  }
+  storeN<kNW>(out + g * kNW, v);
+}
+
+__global__ void dequant8_q6k_kernel(const uint8_t* __restrict__ blocks, int64_t nblk,
+                                    float* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t blk = g / (256 / kNW);
+  if (blk >= nblk) return;
+  const int i0 = (int)(g % (256 / kNW)) * kNW;
+  const uint8_t* b = blocks + blk * 210;
+  const int h = i0 >> 7, r = (i0 >> 5) & 3, l0 = i0 & 31;   // i = 128h + 32r + l
+  uint8_t ql[kNW], qh[kNW];
+  bytesN<kNW>(b + 64 * h + l0 + ((r & 1) ? 32 : 0), ql);
+  bytesN<kNW>(b + 128 + 32 * h + l0, qh);
+  const int sc = (int)(int8_t)b[192 + (i0 >> 4)];
+  const float d = h16(b + 208);
+  float v[kNW];
+#pragma unroll
+  for (int k = 0; k < kNW; ++k) {
+    const int lo = (r & 2) ? (ql[k] >> 4) : (ql[k] & 15);
+    const int hi = (qh[k] >> (2 * r)) & 3;
+    const int q = lo | (hi << 4);
+    v[k] = d * (float)sc * (float)(q - 32);
+  }
+  storeN<kNW>(out + g * kNW, v);
+}
+
+__global__ void dequant8_q80_kernel(const uint8_t* __restrict__ blocks, int64_t nblk,
+                                    float* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t blk = g >> 2;
+  if (blk >= nblk) return;
+  const int i0 = (int)(g & 3) * 8;
+  const uint8_t* b = blocks + blk * 34;
+  uint8_t q8[8];
+  bytes8(b + 2 + i0, q8);
+  const float d = h16(b);
+  float v[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) v[k] = d * (float)(int8_t)q8[k];
+  store8(out + g * 8, v);
 }
 
 // Q4_0: w = d*(q - 8); byte j of qs: weight j (low nibble), j+16 (high).
@@ -188,6 +290,14 @@ int launch_dequant(int fmt, const void* blocks, int64_t n, float* out, cudaStrea
   const int threads = 256;
   const int64_t grid = (n + threads - 1) / threads;
   const uint8_t* b = (const uint8_t*)blocks;
+  if (((uintptr_t)out & 15) == 0 && (fmt == DQ_Q4_K || fmt == DQ_Q6_K || fmt == DQ_Q8_0)) {
+    const dim3 g8((unsigned)((n / 8 + threads - 1) / threads));
+    const dim3 gw((unsigned)((n / kNW + threads - 1) / threads));
+    if (fmt == DQ_Q4_K) launch_pdl(dequant8_q4k_kernel, gw, dim3(threads), 0, s, 0, b, n / 256, out);
+    else if (fmt == DQ_Q6_K) launch_pdl(dequant8_q6k_kernel, gw, dim3(threads), 0, s, 0, b, n / 256, out);
+    else launch_pdl(dequant8_q80_kernel, g8, dim3(threads), 0, s, 0, b, n / 32, out);
+    return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
+  }
   if (fmt == DQ_Q4_K) launch_pdl(dequant_q4k_kernel, dim3((unsigned)grid), dim3(threads), 0, s, 0, b, n / 256, out);
   else if (fmt == DQ_Q6_K) launch_pdl(dequant_q6k_kernel, dim3((unsigned)grid), dim3(threads), 0, s, 0, b, n / 256, out);
   else if (fmt == DQ_Q8_0) launch_pdl(dequant_q80_kernel, dim3((unsigned)grid), dim3(threads), 0, s, 0, b, n / 32, out);

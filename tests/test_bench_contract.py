@@ -45,6 +45,9 @@ def test_gpu_arm_line_assembly(monkeypatch, capsys):
                                          "weight_GBps": 4000.0, "weight_GBps_back_to_back": 5500.0})
     monkeypatch.setattr(bench, "bench_gemv_70b_formats",
                         lambda *a, **k: {"f": {"weight_GBps": 1.0, "weight_GBps_back_to_back": 2.0}})
+    monkeypatch.setattr(bench, "bench_dequant",
+                        lambda *a, **k: {"q4_k_28672x8192": {"us": 200.0, "bytes": 1,
+                                                             "GBps": 5000.0}})
     monkeypatch.setattr(bench, "bench_moe", lambda *a, **k: {"GBps": 100.0, "tokens_per_s": 1.0,
                                                            "expert_tflops": 50.0})
     monkeypatch.setattr(bench, "bench_moe_streamed", lambda *a, **k: {})

@@ -34,6 +34,14 @@ def test_dequant_bit_exact_random(dq, orc, fmt, qk):
     got = dq.dequant(fmt, dev_bytes(raw), n).cpu().numpy()
     ref = orc.dequant(fmt, raw, n)
     assert got.view(np.uint32).tolist() == ref.view(np.uint32).tolist()
+    # an output 4 bytes past a 16-byte boundary: the one-weight-per-thread
+    # form (the 16-byte aligned output above takes the 8-wide form for Q4_K,
+    # Q6_K and Q8_0)
+    buf = torch.full((n + 4,), float("nan"), dtype=torch.float32, device="cuda")
+    dq.dequant(fmt, dev_bytes(raw), n, out=buf[1:n + 1])
+    got1 = buf[1:n + 1].cpu().numpy()
+    assert got1.view(np.uint32).tolist() == ref.view(np.uint32).tolist()
+    assert np.isnan(buf[0].item()) and np.isnan(buf[n + 1].item())
 
 
 @pytest.mark.parametrize("fname,fmt,qk", [("q4_k_blocks.txt", Q4_K, 256),
