@@ -42,6 +42,13 @@ def test_dequant_bit_exact_random(dq, orc, fmt, qk):
     got1 = buf[1:n + 1].cpu().numpy()
     assert got1.view(np.uint32).tolist() == ref.view(np.uint32).tolist()
     assert np.isnan(buf[0].item()) and np.isnan(buf[n + 1].item())
+    # blocks 2 bytes past a 16-byte boundary (Q4_K's wide form then reads
+    # 16-bit words instead of 16-byte vectors)
+    raw_t = torch.from_numpy(np.ascontiguousarray(raw).view(np.uint8).reshape(-1))
+    bb = torch.zeros(raw_t.numel() + 16, dtype=torch.uint8, device="cuda")
+    bb[2:2 + raw_t.numel()].copy_(raw_t)
+    got2 = dq.dequant(fmt, bb[2:2 + raw_t.numel()], n).cpu().numpy()
+    assert got2.view(np.uint32).tolist() == ref.view(np.uint32).tolist()
 
 
 @pytest.mark.parametrize("fname,fmt,qk", [("q4_k_blocks.txt", Q4_K, 256),
