@@ -119,16 +119,9 @@ MoePlan moe_plan(const dq_moe_desc& d, int T, bool allow_wide) {
 // ===========================================================================
 // 1. router logits (fp32 SIMT tile 64 experts x 32 tokens, 4x4 per thread)
 // ===========================================================================
-__device__ __forceinline__ float act_f32(const void* x, int dtype, int64_t i) {
-  if (dtype == DQ_F32) return __ldg((const float*)x + i);
-  const unsigned short u = __ldg((const unsigned short*)x + i);
-  if (dtype == DQ_BF16) return __uint_as_float((uint32_t)u << 16);
-  return __half2float(__ushort_as_half(u));
-}
-
-// The same with the dtype fixed at compile time: loads in an unrolled loop
-// are all issued before the first is used (a run-time dtype branch around
-// each load keeps them one at a time).
+// Activation i of x (fp32, bf16 or fp16) as fp32.  The dtype is fixed at
+// compile time: loads in an unrolled loop are all issued before the first is
+// used (a run-time dtype branch around each load keeps them one at a time).
 template <int XDT>
 __device__ __forceinline__ float act_t(const void* x, int64_t i) {
   if (XDT == DQ_F32) return __ldg((const float*)x + i);
@@ -524,8 +517,9 @@ __device__ __forceinline__ int3 block_scan256x3(int3 v, int3* wsum3, int3* total
 // Few tokens: the permute CTA also converts x to fp16 with a power-of-two
 // scale per token (the x16 prep of the expert kernels), saving a launch on
 // the decode path.  Rows of at most 8192 values.
-__device__ __forceinline__ void x16_rows_cta(const void* x, int xdt, int T, int K, __half* out,
-                                             float* inv, float* red) {
+template <int XDT>
+__device__ __forceinline__ void x16_rows_cta_t(const void* x, int T, int K, __half* out,
+                                               float* inv, float* red) {
   for (int row = 0; row < T; ++row) {
     const int64_t base = (int64_t)row * K;
     float v[8];
@@ -533,7 +527,7 @@ __device__ __forceinline__ void x16_rows_cta(const void* x, int xdt, int T, int 
 #pragma unroll
     for (int i = 0; i < 8; ++i) {                  // K <= 8192
       const int k = threadIdx.x + 1024 * i;
-      v[i] = k < K ? act_f32(x, xdt, base + k) : 0.f;
+      v[i] = k < K ? act_t<XDT>(x, base + k) : 0.f;
       amax = fmaxf(amax, fabsf(v[i]));
     }
 #pragma unroll
@@ -552,6 +546,12 @@ __device__ __forceinline__ void x16_rows_cta(const void* x, int xdt, int T, int 
     }
     if (threadIdx.x == 0) inv[row] = iv;
   }
+}
+__device__ __forceinline__ void x16_rows_cta(const void* x, int xdt, int T, int K, __half* out,
+                                             float* inv, float* red) {
+  if (xdt == DQ_F32) x16_rows_cta_t<DQ_F32>(x, T, K, out, inv, red);
+  else if (xdt == DQ_BF16) x16_rows_cta_t<DQ_BF16>(x, T, K, out, inv, red);
+  else x16_rows_cta_t<DQ_F16>(x, T, K, out, inv, red);
 }
 // tk (nullable): top-k of the T <= 32 tokens first, one warp each, from the
 // router partials (tk->part, tk->KS), writing idx, gate and logits; the

@@ -160,6 +160,8 @@ def _moe_case(dq, orc, fmt, E, k, H, F, ns, T, xdt, seed, tokens=None, cached=No
     (Q6_K, 4, 2, 2048, 2048, 1, 6, 2),
     (Q8_0, 8, 2, 1024, 4096, 1, 12, 2),
     (NVFP4, 8, 2, 1024, 4096, 0, 1, 1),
+    # two bf16 tokens: the permute CTA converts x to fp16 itself
+    (Q4_K, 32, 4, 2048, 512, 1, 2, 2),
 ])
 def test_moe_forward_small(dq, orc, fmt, E, k, H, F, ns, T, xdt):
     err, _ = _moe_case(dq, orc, fmt, E, k, H, F, ns, T, xdt, seed=3000 + E * 7 + T)
