@@ -28,10 +28,73 @@ struct GemvParams {
   int w_early;      // 1: issue the first stages' weight copies before pdl_wait
 };
 
+// bf16 activations of one stage for up to 8 columns: this loader lane's 8
+// values of each column (16 bytes) into registers.
+__device__ __forceinline__ void bf16_stage_load(const XSrc& xs, int ncols, int64_t k0, int lane,
+                                                uint4 (&r)[8]) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    if (j < ncols)
+      r[j] = __ldg((const uint4*)((const uint16_t*)xs.base + (int64_t)j * xs.col_stride + k0) +
+                   lane);
+}
+
+// ... converted to fp16 with one power-of-two scale per column (as stage_x
+// does for bf16: the same values and scales) and stored; arrives on `full`
+// like stage_x (two arrivals per lane).
+template <int FMT>
+__device__ __forceinline__ void bf16_stage_store(const uint4 (&r)[8], int ncols, uint8_t* xdst,
+                                                 float* xinv, int lane, uint64_t* full) {
+  float amax[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    amax[j] = 0.f;
+    if (j < ncols) {
+      const uint32_t w[4] = {r[j].x, r[j].y, r[j].z, r[j].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        amax[j] = fmaxf(amax[j], fabsf(__uint_as_float(w[i] << 16)));
+        amax[j] = fmaxf(amax[j], fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) amax[j] = fmaxf(amax[j], __shfl_xor_sync(0xffffffffu, amax[j], o));
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (j < ncols) {
+      float sc, inv;
+      pow2_scale(amax[j], sc, inv);
+      const uint32_t w[4] = {r[j].x, r[j].y, r[j].z, r[j].w};
+      uint32_t h[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        h[i] = h2_as_u32(__floats2half2_rn(__uint_as_float(w[i] << 16) * sc,
+                                           __uint_as_float(w[i] & 0xFFFF0000u) * sc));
+      *(uint4*)(xdst + j * Layout<FMT>::XCOL + 2 * xoff(8 * lane)) =
+          make_uint4(h[0], h[1], h[2], h[3]);
+      if (lane == 0) xinv[j] = inv;
+    }
+  }
+  cp_async_arrive_noinc(full);
+  mbar_arrive(full);
+}
+
 // PAIR: each consumer iteration takes two stages (more independent work per
 // warp and more registers: for grids of at most three CTAs per SM).
-template <int FMT, bool PAIR>
-__global__ void __launch_bounds__(kThreads, PAIR ? 3 : 1)
+// BF16X: bf16 activations at batch >= 4, whose next stage the loader holds in
+// registers while it converts the current one (its global load latency hidden
+// behind a stage); a separate instance, so that the extra registers stay out
+// of the fp16 kernels.  Capped at four CTAs per SM (96 registers) except for
+// Q6_K, whose decode measured faster uncapped at three.  Measured on the 70B
+// shapes at batch 8 (gate / down / q, us): Q4_K 103.5 / 99.5 / 29.8 -> 56.0 /
+// 54.4 / 18.2, Q6_K 104.7 / 135.6 / 41.1 -> 64.7 / 76.4 / 24.8, Q8_0 107.7 /
+// 126.9 / 40.2 -> 63.3 / 74.0 / 24.4; at batch 2 it was not faster for Q4_K
+// and Q8_0.
+template <int FMT, bool PAIR, bool BF16X>
+__global__ void __launch_bounds__(kThreads, PAIR ? 3 : ((BF16X && FMT != DQ_Q6_K) ? 4 : 1))
     qgemv_mma_kernel(const __grid_constant__ GemvParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   using L = Layout<FMT>;
@@ -92,6 +155,8 @@ __global__ void __launch_bounds__(kThreads, PAIR ? 3 : 1)
     bool ok = true;
     int s = 0;
     uint32_t ph = 0;            // phase parity of stage s in the current round
+    uint4 nxt[8];               // BF16X: the next stage's raw activations
+    if (BF16X && nchunk > 0) bf16_stage_load(p.x, p.batch, (int64_t)sb0 * 256, lane, nxt);
     for (int c = 0; c < nchunk && ok; ++c) {
       if (c >= plan.nstage) ok = mbar_wait(&empty[s], ph ^ 1);
       if (!ok) break;
@@ -103,8 +168,17 @@ __global__ void __launch_bounds__(kThreads, PAIR ? 3 : 1)
         mbar_arrive_expect_tx(&full[s], L::W_STAGE);   // rows past N are zero-filled, still counted
         tma_load_2d(wbuf + s * L::W_STAGE, &p.tmap, (int)(a >> 1), row0, &full[s], pol);
       }
-      stage_x<FMT>(p.x, p.batch, (int64_t)c0 * 256, 1, xbuf + s * p.batch * L::XCOL,
-                   xinv + s * 8, lane, &full[s]);
+      if constexpr (BF16X) {
+        uint4 cur[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
+        if (c + 1 < nchunk) bf16_stage_load(p.x, p.batch, (int64_t)(c0 + 1) * 256, lane, nxt);
+        bf16_stage_store<FMT>(cur, p.batch, xbuf + s * p.batch * L::XCOL, xinv + s * 8, lane,
+                              &full[s]);
+      } else {
+        stage_x<FMT>(p.x, p.batch, (int64_t)c0 * 256, 1, xbuf + s * p.batch * L::XCOL,
+                     xinv + s * 8, lane, &full[s]);
+      }
       if (++s == plan.nstage) {
         s = 0;
         ph ^= 1;
@@ -486,8 +560,11 @@ int launch_qgemv_mma_fmt(const void* W, int64_t N, int64_t K, const void* x, int
   if (sms <= 0) return DQ_ERR_CUDA;
   // shared memory per CTA <= 56 KB so that four CTAs (20 warps) share an SM
   constexpr int kSmemBudget = 56 * 1024;
-  // CTAs per SM: four where a three-stage ring fits the 56 KB budget, else three
-  const int per_sm = make_plan<FMT>(3, batch, 4).total <= kSmemBudget ? 4 : 3;
+  const bool bf16x = xdt == DQ_BF16 && batch >= 4;
+  // CTAs per SM: four where a three-stage ring fits the 56 KB budget, else
+  // three; three for the uncapped Q6_K bf16 instance
+  const int per_sm =
+      (!(bf16x && FMT == DQ_Q6_K) && make_plan<FMT>(3, batch, 4).total <= kSmemBudget) ? 4 : 3;
   int ks = force_ksplit > 0 ? force_ksplit : choose_ksplit(tiles, p.nsb, sms, per_sm);
   ks = std::max(1, std::min(ks, std::min(8, p.nsb)));
   // Q4_K grids of at most three CTAs per SM take the paired kernel with
@@ -501,18 +578,21 @@ int launch_qgemv_mma_fmt(const void* W, int64_t N, int64_t K, const void* x, int
   p.nstage = nstage;
   p.w_early = early_weights(w_early, p.nsb, ks, nstage);
   const SmemPlan plan = make_plan<FMT>(nstage, batch, ks);
-  auto kern = pair ? qgemv_mma_kernel<FMT, true> : qgemv_mma_kernel<FMT, false>;
-  static bool attr_set[2][64] = {};
+  auto kern = pair ? (bf16x ? qgemv_mma_kernel<FMT, true, true> : qgemv_mma_kernel<FMT, true, false>)
+                   : (bf16x ? qgemv_mma_kernel<FMT, false, true>
+                            : qgemv_mma_kernel<FMT, false, false>);
+  static bool attr_set[4][64] = {};
+  const int v = (pair ? 1 : 0) + (bf16x ? 2 : 0);
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 64 || !attr_set[pair][dev]) {
+  if (dev >= 64 || !attr_set[v][dev]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) !=
         cudaSuccess)
       return DQ_ERR_CUDA;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
         cudaSuccess)
       return DQ_ERR_CUDA;
-    if (dev < 64) attr_set[pair][dev] = true;
+    if (dev < 64) attr_set[v][dev] = true;
   }
   if (launch_pdl(kern, dim3((unsigned)ks, (unsigned)tiles, 1), dim3(kThreads), (size_t)plan.total,
                  stream, ks, p) != cudaSuccess)

@@ -177,16 +177,20 @@ __device__ __forceinline__ void stage_x(const XSrc& xs, int ncols, int64_t k0, i
     cp_async_arrive_noinc(full);
     return;
   }
-  // four columns at a time: their global loads are in flight together
+  // four columns at a time: their global loads are all issued before any
+  // value is used (a use inside the same branch as its load would wait for
+  // each load in turn)
   static_assert(Layout<FMT>::C == 1, "one super-block per stage");
   for (int c0 = 0; c0 < ncols; c0 += 4) {
     float v[4][8];
     float amax[4];
 #pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (c0 + j < ncols && nsb_stage > 0) load8_f32(xs, c0 + j, k0 + 8 * lane, v[j]);
+#pragma unroll
     for (int j = 0; j < 4; ++j) {
       amax[j] = 0.f;
       if (c0 + j < ncols && nsb_stage > 0) {
-        load8_f32(xs, c0 + j, k0 + 8 * lane, v[j]);
 #pragma unroll
         for (int i = 0; i < 8; ++i) amax[j] = fmaxf(amax[j], fabsf(v[j][i]));
       }
