@@ -87,9 +87,11 @@ def _case(dq, orc, fmt, N, K, B, xdt, seed, ksplit=None, xscale=1.0, cached=Fals
 
 @pytest.mark.parametrize("fmt", [Q4_K, Q6_K, Q8_0, Q4_0, Q5_K, NVFP4, Q2_K, Q3_K])
 @pytest.mark.parametrize("xdt", [0, 1, 2])
-@pytest.mark.parametrize("B", [1, 3, 8])
+@pytest.mark.parametrize("B", [1, 3, 5, 8])
 def test_qgemv_small_ragged(dq, orc, fmt, xdt, B):
     # several 64-row tiles plus a ragged tail; K spans several pipeline stages
+    # (bf16 at batch 5 and 8: the kernel instance that keeps the next stage's
+    # activations in registers, with a partial and a full set of columns)
     N, K = 200, 4096
     err = _case(dq, orc, fmt, N, K, B, xdt, seed=fmt * 100 + xdt * 10 + B)
     assert err <= TOL[xdt], err
