@@ -84,15 +84,16 @@ __device__ __forceinline__ void bf16_stage_store(const uint4 (&r)[8], int ncols,
 
 // PAIR: each consumer iteration takes two stages (more independent work per
 // warp and more registers: for grids of at most three CTAs per SM).
-// BF16X: bf16 activations at batch >= 4, whose next stage the loader holds in
-// registers while it converts the current one (its global load latency hidden
-// behind a stage); a separate instance, so that the extra registers stay out
-// of the fp16 kernels.  Capped at four CTAs per SM (96 registers) except for
-// Q6_K, whose decode measured faster uncapped at three.  Measured on the 70B
-// shapes at batch 8 (gate / down / q, us): Q4_K 103.5 / 99.5 / 29.8 -> 56.0 /
-// 54.4 / 18.2, Q6_K 104.7 / 135.6 / 41.1 -> 64.7 / 76.4 / 24.8, Q8_0 107.7 /
-// 126.9 / 40.2 -> 63.3 / 74.0 / 24.4; at batch 2 it was not faster for Q4_K
-// and Q8_0.
+// BF16X: bf16 activations at batch >= 4 (Q4_K and Q6_K: >= 2), whose next
+// stage the loader holds in registers while it converts the current one (its
+// global load latency hidden behind a stage); a separate instance, so that the
+// extra registers stay out of the fp16 kernels.  Capped at four CTAs per SM
+// (96 registers) except for Q6_K, whose decode measured faster uncapped at
+// three.  Measured on the 70B shapes (gate / down / q, us): batch 8 Q4_K
+// 103.5 / 99.5 / 29.8 -> 56.0 / 54.4 / 18.2, Q6_K 104.7 / 135.6 / 41.1 -> 64.7 /
+// 76.4 / 24.8, Q8_0 107.7 / 126.9 / 40.2 -> 63.3 / 74.0 / 24.4; batch 2 Q4_K
+// 47.4 / 50.9 / 17.0 -> 46.8 / 45.2 / 16.1, Q6_K 64.1 / 80.5 / 25.7 -> 55.6 /
+// 66.0 / 21.8, Q8_0 slower (61.7 -> 74.3 us on down).
 template <int FMT, bool PAIR, bool BF16X>
 __global__ void __launch_bounds__(kThreads, PAIR ? 3 : ((BF16X && FMT != DQ_Q6_K) ? 4 : 1))
     qgemv_mma_kernel(const __grid_constant__ GemvParams p) {
@@ -560,7 +561,8 @@ int launch_qgemv_mma_fmt(const void* W, int64_t N, int64_t K, const void* x, int
   if (sms <= 0) return DQ_ERR_CUDA;
   // shared memory per CTA <= 56 KB so that four CTAs (20 warps) share an SM
   constexpr int kSmemBudget = 56 * 1024;
-  const bool bf16x = xdt == DQ_BF16 && batch >= 4;
+  const bool bf16x =
+      xdt == DQ_BF16 && (batch >= 4 || (batch >= 2 && (FMT == DQ_Q4_K || FMT == DQ_Q6_K)));
   // CTAs per SM: four where a three-stage ring fits the 56 KB budget, else
   // three; three for the uncapped Q6_K bf16 instance
   const int per_sm =
