@@ -102,10 +102,10 @@ def moe_workspace_size(desc, T):
     return n.value
 
 
-def moe_router(router_W, E, H, x, top_k, logits=None, want_logits=True):
+def moe_router(router_W, E, H, x, top_k, logits=None):
     T = x.shape[0]
     dev = x.device
-    if logits is None and want_logits:
+    if logits is None:
         logits = torch.empty(T, E, dtype=torch.float32, device=dev)
     idx = torch.empty(T, top_k, dtype=torch.int32, device=dev)
     gate = torch.empty(T, top_k, dtype=torch.float32, device=dev)

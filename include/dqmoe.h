@@ -262,13 +262,17 @@ typedef struct {
 int dq_moe_workspace_size(const dq_moe_desc* desc, int T, size_t* bytes);
 
 /* dq_moe_router — steps "router" and "top-k + gates" alone.
- *   router_W : device fp32 [E][H];  x : device [T][H] of x_dtype.
- *   logits   : device fp32 [T][E] (nullable).
+ *   router_W : device fp32 [E][H];  x : device [T][H] of x_dtype; H % 32 == 0.
+ *   logits   : device fp32 [T][E], required: the logits are summed there
+ *              before the selection reads them (this entry point takes no
+ *              workspace).
  *   topk_idx : device int32 [T][top_k], slot order = descending logit,
  *              lowest expert index first among equal logits.
  *   topk_gate: device fp32 [T][top_k], renormalised softmax weights.
- * Errors: DQ_ERR_ARG, DQ_ERR_ALIGN (x, router_W not 16-B aligned),
- *         DQ_ERR_UNSUPPORTED (E > 256 or top_k > 8), DQ_ERR_CUDA. */
+ * Errors: DQ_ERR_ARG (a null pointer, H % 32 != 0, sizes <= 0, top_k > E),
+ *         DQ_ERR_ALIGN (router_W, x, logits, topk_idx or topk_gate not 4-byte
+ *         aligned), DQ_ERR_UNSUPPORTED (E > 256, top_k > 8 or T > 65536),
+ *         DQ_ERR_CUDA. */
 int dq_moe_router(const float* router_W, int E, int H, const void* x,
                   int x_dtype, int T, int top_k, float* logits,
                   int32_t* topk_idx, float* topk_gate, void* stream);

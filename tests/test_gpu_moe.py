@@ -67,6 +67,29 @@ def test_router_topk(dq, orc, E, k, H, T, xdt):
                   gate.cpu().numpy())
 
 
+def test_router_argument_errors(dq):
+    # the logits buffer is required (the sums are formed there); pointers need
+    # 4-byte alignment; nothing is launched on an error
+    import ctypes
+    E, k, H, T = 16, 2, 256, 2
+    Wr = torch.zeros(E, H, dtype=torch.float32, device="cuda")
+    x = torch.zeros(T, H, dtype=torch.float16, device="cuda")
+    lg = torch.full((T, E), 7.0, dtype=torch.float32, device="cuda")
+    idx = torch.full((T, k), -3, dtype=torch.int32, device="cuda")
+    gate = torch.full((T, k), 7.0, dtype=torch.float32, device="cuda")
+    P = ctypes.c_void_p
+    st = P(torch.cuda.current_stream().cuda_stream)
+    f = dq.lib.dq_moe_router
+    assert f(P(Wr.data_ptr()), E, H, P(x.data_ptr()), 1, T, k, None, P(idx.data_ptr()),
+             P(gate.data_ptr()), st) == -1
+    assert f(P(Wr.data_ptr() + 2), E, H, P(x.data_ptr()), 1, T, k, P(lg.data_ptr()),
+             P(idx.data_ptr()), P(gate.data_ptr()), st) == -2
+    assert f(P(Wr.data_ptr()), E, 100, P(x.data_ptr()), 1, T, k, P(lg.data_ptr()),
+             P(idx.data_ptr()), P(gate.data_ptr()), st) == -1
+    torch.cuda.synchronize()
+    assert bool((idx == -3).all()) and bool((lg == 7.0).all())
+
+
 def test_topk_ties_lowest_index(dq):
     # zero router weights: every logit is 0, the selection is experts 0..k-1
     E, k, H, T = 32, 4, 256, 3
