@@ -294,7 +294,7 @@ int dq_moe_permute(const int32_t* topk_idx, int T, int top_k, int E,
  *              which cannot meet the 1e-5 relative bar fp32 activations are
  *              held to, so DQ_F32 is refused (DQ_ERR_UNSUPPORTED); a caller
  *              with fp32 activations rounds them to bf16 first.
- *   y        : device fp32 [T][H], fully overwritten.
+ *   y        : device fp32 [T][H], 16-byte aligned, fully overwritten.
  *   ws       : device scratch of at least dq_moe_workspace_size bytes,
  *              256-byte aligned; contents on entry are ignored.
  *   topk_idx, topk_gate, logits : optional device outputs as in
@@ -302,8 +302,9 @@ int dq_moe_permute(const int32_t* topk_idx, int T, int top_k, int E,
  * All launches go on `stream` with no host synchronisation, so the layer is
  * capturable in one CUDA graph ([KTransformers, §技术原理]: one graph call
  * per decode step).
- * Errors: DQ_ERR_ARG, DQ_ERR_ALIGN, DQ_ERR_UNSUPPORTED (also fp32 x),
- *         DQ_ERR_WORKSPACE, DQ_ERR_CUDA. */
+ * Errors: DQ_ERR_ARG, DQ_ERR_ALIGN (x, y not 16-byte aligned, ws not 256-byte
+ *         aligned, an optional output not 4-byte aligned), DQ_ERR_UNSUPPORTED
+ *         (also fp32 x), DQ_ERR_WORKSPACE, DQ_ERR_CUDA. */
 int dq_moe_forward(const dq_moe_desc* desc, const void* x, int x_dtype, int T,
                    float* y, void* ws, size_t ws_bytes, int32_t* topk_idx,
                    float* topk_gate, float* logits, void* stream);
