@@ -243,68 +243,80 @@ __global__ void __launch_bounds__(128) router_logits_kernel(const float* __restr
 template <int TMAX, int CHUNK, int XDT>
 __global__ void __launch_bounds__(256) router_stream_kernel(const float* __restrict__ Wr, int E,
                                                             int H, const void* __restrict__ x,
-                                                            int T, float* __restrict__ part) {
+                                                            int T, float* __restrict__ part,
+                                                            int nc) {
   pdl_wait();
   pdl_trigger();
+  // CTA (b, ks) sums hidden chunks ks*nc .. ks*nc + nc - 1 (the layer: one
+  // chunk per CTA, partials summed by the top-k; dq_moe_router: every chunk,
+  // the partial is the logit)
   __shared__ __align__(16) float xs[TMAX][CHUNK];
-  const int ks = blockIdx.y, h0 = ks * CHUNK;
-  const int n = min(CHUNK, H - h0);                 // multiple of 32
-  // every load of the call is issued before any is used: the chunk of x
-  // (16-byte loads, at most kVec per thread) and this warp's row of W_r
+  const int ks = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 8 + warp;
+  const bool active = e < E;
   constexpr int kES = XDT == DQ_F32 ? 4 : 2;        // bytes per activation
   constexpr int kVE = 16 / kES;                     // activations per 16-byte load
   constexpr int kVec = TMAX * CHUNK / kVE / 256;
-  const int nv = n / kVE, total = T * nv;
-  uint4 xr[kVec];
-#pragma unroll
-  for (int j = 0; j < kVec; ++j) {
-    const int i = threadIdx.x + 256 * j;
-    if (i < total) {
-      const int t = i / nv, v = i - t * nv;
-      xr[j] = __ldg((const uint4*)((const char*)x + ((int64_t)t * H + h0 + v * kVE) * kES));
-    }
-  }
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e = blockIdx.x * 8 + warp;
   constexpr int kW = CHUNK / 4 / 32;                // float4 of W_r per lane
-  float4 wv[kW];
-  if (e < E) {
-    const float4* w = (const float4*)(Wr + (int64_t)e * H + h0);
-#pragma unroll
-    for (int j = 0; j < kW; ++j)
-      wv[j] = lane + 32 * j < n / 4 ? __ldcs(w + lane + 32 * j) : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-#pragma unroll
-  for (int j = 0; j < kVec; ++j) {
-    const int i = threadIdx.x + 256 * j;
-    if (i < total) {
-      const int t = i / nv, v = i - t * nv;
-      float f[kVE];
-      act_vec<XDT>(xr[j], f);
-#pragma unroll
-      for (int q = 0; q < kVE; q += 4)
-        *(float4*)&xs[t][v * kVE + q] = make_float4(f[q], f[q + 1], f[q + 2], f[q + 3]);
-    }
-  }
-  __syncthreads();
-  if (e >= E) return;
   float acc[TMAX] = {};
+  for (int ci = 0; ci < nc; ++ci) {
+    const int h0 = (ks * nc + ci) * CHUNK;
+    if (h0 >= H) break;                             // uniform over the CTA
+    const int n = min(CHUNK, H - h0);               // multiple of 32
+    // every load of the chunk is issued before any is used: the chunk of x
+    // (16-byte loads, at most kVec per thread) and this warp's row of W_r
+    const int nv = n / kVE, total = T * nv;
+    uint4 xr[kVec];
 #pragma unroll
-  for (int j = 0; j < kW; ++j) {
-    if (lane + 32 * j < n / 4) {
-      const float4 w4 = wv[j];
+    for (int j = 0; j < kVec; ++j) {
+      const int i = threadIdx.x + 256 * j;
+      if (i < total) {
+        const int t = i / nv, v = i - t * nv;
+        xr[j] = __ldg((const uint4*)((const char*)x + ((int64_t)t * H + h0 + v * kVE) * kES));
+      }
+    }
+    float4 wv[kW];
+    if (active) {
+      const float4* w = (const float4*)(Wr + (int64_t)e * H + h0);
 #pragma unroll
-      for (int t = 0; t < TMAX; ++t) {
-        if (t < T) {
-          const float4 xv = *(const float4*)&xs[t][4 * (lane + 32 * j)];
-          acc[t] = fmaf(w4.x, xv.x, acc[t]);
-          acc[t] = fmaf(w4.y, xv.y, acc[t]);
-          acc[t] = fmaf(w4.z, xv.z, acc[t]);
-          acc[t] = fmaf(w4.w, xv.w, acc[t]);
+      for (int j = 0; j < kW; ++j)
+        wv[j] = lane + 32 * j < n / 4 ? __ldcs(w + lane + 32 * j) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (ci > 0) __syncthreads();                    // the previous chunk's reads of xs
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) {
+      const int i = threadIdx.x + 256 * j;
+      if (i < total) {
+        const int t = i / nv, v = i - t * nv;
+        float f[kVE];
+        act_vec<XDT>(xr[j], f);
+#pragma unroll
+        for (int q = 0; q < kVE; q += 4)
+          *(float4*)&xs[t][v * kVE + q] = make_float4(f[q], f[q + 1], f[q + 2], f[q + 3]);
+      }
+    }
+    __syncthreads();
+    if (active) {
+#pragma unroll
+      for (int j = 0; j < kW; ++j) {
+        if (lane + 32 * j < n / 4) {
+          const float4 w4 = wv[j];
+#pragma unroll
+          for (int t = 0; t < TMAX; ++t) {
+            if (t < T) {
+              const float4 xv = *(const float4*)&xs[t][4 * (lane + 32 * j)];
+              acc[t] = fmaf(w4.x, xv.x, acc[t]);
+              acc[t] = fmaf(w4.y, xv.y, acc[t]);
+              acc[t] = fmaf(w4.z, xv.z, acc[t]);
+              acc[t] = fmaf(w4.w, xv.w, acc[t]);
+            }
+          }
         }
       }
     }
   }
+  if (!active) return;
 #pragma unroll
   for (int t = 0; t < TMAX; ++t) {
     if (t < T) {
@@ -1238,12 +1250,16 @@ int launch_router(const float* Wr, int E, int H, const void* x, int xdt, int T, 
                   int KS, float* part, float* logits, int32_t* idx, float* gate, cudaStream_t s,
                   bool with_topk) {
   const int chunk = router_chunk(T);
+  const int nchunks = chunk ? (H + chunk - 1) / chunk : 0;
   const bool vec_ok = ((uintptr_t)x & 15) == 0 && H % 8 == 0;
-  if (chunk && KS == (H + chunk - 1) / chunk && KS > 1 && ((uintptr_t)Wr & 15) == 0 &&
-      H % 4 == 0 && vec_ok) {
+  // the streaming kernel: one chunk per CTA (KS partials), or every chunk in
+  // each CTA when one partial is asked for (dq_moe_router)
+  if (chunk && (KS == nchunks || KS == 1) && ((uintptr_t)Wr & 15) == 0 && H % 4 == 0 &&
+      vec_ok) {
+    const int nc = KS == 1 ? nchunks : 1;
     const dim3 g((unsigned)((E + 7) / 8), (unsigned)KS);
 #define DQ_RS(TM, CH, XD) \
-  launch_pdl(router_stream_kernel<TM, CH, XD>, g, dim3(256), 0, s, 0, Wr, E, H, x, T, part)
+  launch_pdl(router_stream_kernel<TM, CH, XD>, g, dim3(256), 0, s, 0, Wr, E, H, x, T, part, nc)
     if (T <= kRouterStreamT) {
       if (xdt == DQ_F32) DQ_RS(kRouterStreamT, kRouterChunk, DQ_F32);
       else if (xdt == DQ_BF16) DQ_RS(kRouterStreamT, kRouterChunk, DQ_BF16);
