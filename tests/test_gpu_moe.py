@@ -185,6 +185,14 @@ def _moe_case(dq, orc, fmt, E, k, H, F, ns, T, xdt, seed, tokens=None, cached=No
     (NVFP4, 8, 2, 1024, 4096, 0, 1, 1),
     # two bf16 tokens: the permute CTA converts x to fp16 itself
     (Q4_K, 32, 4, 2048, 512, 1, 2, 2),
+    # Q6_K / Q8_0 one-token experts at T > 1 beside experts with two tokens
+    # (each seed's routing gives 1-4 of them; the last case also one 3-token
+    # expert), which run on the general kernel in the same layer
+    (Q6_K, 16, 2, 2048, 2048, 1, 3, 1),
+    (Q6_K, 32, 8, 2048, 2048, 0, 2, 2),
+    (Q8_0, 16, 2, 1024, 1024, 0, 4, 2),
+    (Q4_K, 32, 4, 2048, 512, 1, 4, 1),
+    (Q8_0, 64, 4, 1024, 512, 1, 8, 1),
 ])
 def test_moe_forward_small(dq, orc, fmt, E, k, H, F, ns, T, xdt):
     err, _ = _moe_case(dq, orc, fmt, E, k, H, F, ns, T, xdt, seed=3000 + E * 7 + T)
