@@ -71,7 +71,7 @@ def run_case(args):
     elif args.case == "mixtral":
         print(json.dumps(bench_moe(torch, dq, synth.MOE_MIXTRAL, 16, reps=max(1, args.steps))))
     elif args.case == "dequant70b":
-        print(json.dumps(bench_dequant(torch, dq, reps=max(1, args.steps))))
+        print(json.dumps(bench_dequant(torch, dq, reps=max(1, args.steps), fmts=ALL_DEQUANT_FMTS)))
     elif args.case == "formats70b":
         print(json.dumps(bench_gemv_70b_formats(torch, dq, reps=max(1, args.steps))))
     elif args.case == "ds64":
@@ -686,7 +686,11 @@ def bench_gemv_70b_formats(torch, dq, reps=30, fmts=((Q4_K, "q4_k"), (2, "q6_k")
     return out
 
 
-def bench_dequant(torch, dq, reps=10, fmts=((Q4_K, "q4_k"), (2, "q6_k"), (3, "q8_0"))):
+ALL_DEQUANT_FMTS = ((Q4_K, "q4_k"), (2, "q6_k"), (3, "q8_0"), (4, "q4_0"), (5, "q5_k"),
+                    (6, "nvfp4"), (7, "q2_k"), (8, "q3_k"))
+
+
+def bench_dequant(torch, dq, reps=10, fmts=ALL_DEQUANT_FMTS[:3]):
     """The decode step on its own (dq_dequant: packed blocks -> fp32) on the 70B
     gate matrix (28672 x 8192): bytes read + written per launch over the CUDA-
     event time of `reps` launches back to back (inputs and outputs far above

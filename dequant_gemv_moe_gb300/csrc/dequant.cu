@@ -9,12 +9,14 @@
 // bit-identical to any exact evaluation.
 //
 // One thread per output weight (coalesced fp32 stores); the block's few
-// header bytes are re-read by its threads through L1.  Q4_K, Q6_K and Q8_0
-// also have a wide form (one thread per 16 / 16 / 8 consecutive weights: the
-// scale fields read once, the quant bytes as 16-bit loads, 16-byte stores),
-// taken when the output is 16-byte aligned; it evaluates every weight with
-// the same expression, so both forms give the same bits.  The GEMV kernels
-// never materialise W: this is the decode step on its own.
+// header bytes are re-read by its threads through L1.  Every format also has
+// a wide form, taken when the output is 16-byte aligned: a warp per 512
+// weights, each lane decoding runs of 4 (the scale fields read once per run,
+// the quant bytes as 16-bit loads) into 16-byte stores that cover 512
+// contiguous bytes per warp instruction (Q8_0: a thread per 8 weights).  It
+// evaluates every weight with the same expression, so both forms give the same
+// bits.  The GEMV kernels never materialise W: this is the decode step on its
+// own.
 #include "common.cuh"
 
 namespace dqmoe {
@@ -80,86 +82,164 @@ __global__ void dequant_q80_kernel(const uint8_t* __restrict__ blocks, int64_t n
   out[gid] = h16(b) * (float)(int8_t)b[2 + (gid & 31)];
 }
 
-// N bytes at an even address as N/2 16-bit loads (blocks are 2-byte aligned).
-template <int N>
-__device__ __forceinline__ void bytesN(const uint8_t* p, uint8_t (&v)[N]) {
+// Four bytes at an even address (blocks are 2-byte aligned) as two 16-bit
+// loads, byte 0 in bits 0..7.
+__device__ __forceinline__ uint32_t bytes4(const uint8_t* p) {
+  return (uint32_t)__ldg((const unsigned short*)p) |
+         ((uint32_t)__ldg((const unsigned short*)p + 1) << 16);
+}
+__device__ __forceinline__ void store4(float* o, float a, float b, float c, float d) {
+  *(float4*)o = make_float4(a, b, c, d);
+}
+
+// Wide forms: weights i .. i + 3 (i % 4 == 0) of one block at b, each by
+// the same expression as the one-weight form (so both give the same bits).
+template <int FMT> struct DQW;
+
+template <> struct DQW<DQ_Q4_K> {
+  static constexpr int QK = 256, BB = 144;
+  __device__ __forceinline__ static void run(const uint8_t* b, int i, float (&v)[4]) {
+    const float d = h16(b), dmin = h16(b + 2);
+    const uint8_t* s = b + 4;
+    const int j = i >> 5;
+    int sc, m;
+    if (j < 4) {
+      sc = s[j] & 63;
+      m = s[j + 4] & 63;
+    } else {
+      sc = (s[j + 4] & 15) | ((s[j - 4] >> 6) << 4);
+      m = (s[j + 4] >> 4) | ((s[j] >> 6) << 4);
+    }
+    // byte 16 + 32 (i >> 6) + (i & 31): weight i (low nibble) and i + 32
+    uint32_t q = bytes4(b + 16 + 32 * (i >> 6) + (i & 31));
+    if (i & 32) q >>= 4;
+    const float ds = d * (float)sc, dm = -(dmin * (float)m);
 #pragma unroll
-  for (int k = 0; k < N / 2; ++k) {
-    const unsigned short u = __ldg((const unsigned short*)p + k);
-    v[2 * k] = (uint8_t)(u & 0xFF);
-    v[2 * k + 1] = (uint8_t)(u >> 8);
+    for (int e = 0; e < 4; ++e) v[e] = __fmaf_rn(ds, (float)((q >> (8 * e)) & 15), dm);
   }
-}
-__device__ __forceinline__ void bytes8(const uint8_t* p, uint8_t (&v)[8]) { bytesN<8>(p, v); }
+};
 
-template <int N>
-__device__ __forceinline__ void storeN(float* o, const float (&v)[N]) {
+template <> struct DQW<DQ_Q6_K> {
+  static constexpr int QK = 256, BB = 210;
+  __device__ __forceinline__ static void run(const uint8_t* b, int i, float (&v)[4]) {
+    const int h = i >> 7, r = (i >> 5) & 3, l = i & 31;   // i = 128h + 32r + l
+    uint32_t lo = bytes4(b + 64 * h + l + ((r & 1) ? 32 : 0));
+    if (r & 2) lo >>= 4;
+    const uint32_t hi = bytes4(b + 128 + 32 * h + l) >> (2 * r);
+    const float ds = h16(b + 208) * (float)(int)(int8_t)b[192 + (i >> 4)];
 #pragma unroll
-  for (int k = 0; k < N / 4; ++k)
-    ((float4*)o)[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
-}
-__device__ __forceinline__ void store8(float* o, const float (&v)[8]) { storeN<8>(o, v); }
+    for (int e = 0; e < 4; ++e) {
+      const int q = (int)((lo >> (8 * e)) & 15) | (int)(((hi >> (8 * e)) & 3) << 4);
+      v[e] = ds * (float)(q - 32);
+    }
+  }
+};
 
-// Wide forms: thread g decodes weights NW g .. NW g + NW - 1 (Q4_K, Q6_K: 16,
-// within one 32-weight run; Q8_0: 8).
-constexpr int kNW = 16;
-__global__ void dequant8_q4k_kernel(const uint8_t* __restrict__ blocks, int64_t nblk,
-                                    float* __restrict__ out) {
+template <> struct DQW<DQ_Q5_K> {
+  static constexpr int QK = 256, BB = 176;
+  __device__ __forceinline__ static void run(const uint8_t* b, int i, float (&v)[4]) {
+    const float d = h16(b), dmin = h16(b + 2);
+    const uint8_t* s = b + 4;
+    const int j = i >> 5;
+    int sc, m;
+    if (j < 4) {
+      sc = s[j] & 63;
+      m = s[j + 4] & 63;
+    } else {
+      sc = (s[j + 4] & 15) | ((s[j - 4] >> 6) << 4);
+      m = (s[j + 4] >> 4) | ((s[j] >> 6) << 4);
+    }
+    const int c = i >> 6, l = i & 31;
+    uint32_t q = bytes4(b + 48 + 32 * c + l);
+    if (i & 32) q >>= 4;
+    const uint32_t hb = bytes4(b + 16 + l) >> j;   // bit j of qh[l]: bit 4 of q
+    const float ds = d * (float)sc, dm = -(dmin * (float)m);
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      v[e] = __fmaf_rn(ds, (float)(((q >> (8 * e)) & 15) | (((hb >> (8 * e)) & 1) << 4)), dm);
+  }
+};
+
+template <> struct DQW<DQ_Q4_0> {
+  static constexpr int QK = 32, BB = 18;
+  __device__ __forceinline__ static void run(const uint8_t* b, int i, float (&v)[4]) {
+    uint32_t q = bytes4(b + 2 + (i & 15));
+    if (i & 16) q >>= 4;
+    const float d = h16(b);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) v[e] = d * (float)((int)((q >> (8 * e)) & 15) - 8);
+  }
+};
+
+template <> struct DQW<DQ_Q2_K> {
+  static constexpr int QK = 256, BB = 84;
+  __device__ __forceinline__ static void run(const uint8_t* b, int i, float (&v)[4]) {
+    const int h = i >> 7, r = (i >> 5) & 3, l = i & 31;
+    const uint32_t q = bytes4(b + 16 + 32 * h + l) >> (2 * r);
+    const int sm = b[i >> 4];
+    const float ds = h16(b + 80) * (float)(sm & 15), dm = -(h16(b + 82) * (float)(sm >> 4));
+#pragma unroll
+    for (int e = 0; e < 4; ++e) v[e] = __fmaf_rn(ds, (float)((q >> (8 * e)) & 3), dm);
+  }
+};
+
+template <> struct DQW<DQ_Q3_K> {
+  static constexpr int QK = 256, BB = 110;
+  __device__ __forceinline__ static void run(const uint8_t* b, int i, float (&v)[4]) {
+    const int h = i >> 7, r = (i >> 5) & 3, l = i & 31;
+    const uint32_t low = bytes4(b + 32 + 32 * h + l) >> (2 * r);
+    const uint32_t hm = bytes4(b + l) >> (4 * h + r);
+    const int j = i >> 4;
+    const int sc = ((b[96 + (j & 7)] >> (4 * (j >> 3))) & 15) |
+                   (((b[104 + (j & 3)] >> (2 * (j >> 2))) & 3) << 4);
+    const float ds = h16(b + 108) * (float)(sc - 32);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int q = (int)((low >> (8 * e)) & 3) - (((hm >> (8 * e)) & 1) ? 0 : 4);
+      v[e] = ds * (float)q;
+    }
+  }
+};
+
+template <> struct DQW<DQ_NVFP4> {
+  static constexpr int QK = 256, BB = 144;
+  __device__ __forceinline__ static void run(const uint8_t* b, int i, float (&v)[4]) {
+    // codes of weights i .. i + 3: bytes 16 + i / 2, + 1 (low nibble first)
+    uint32_t h[4];
+    e2m1x8_to_h2x4((uint32_t)__ldg((const unsigned short*)(b + 16 + i / 2)), h);
+    const float s = __low2float(u32_as_h2(e4m3x2_to_h2((uint16_t)b[i >> 4])));
+    const float2 a = __half22float2(u32_as_h2(h[0])), c = __half22float2(u32_as_h2(h[1]));
+    v[0] = a.x * s;
+    v[1] = a.y * s;
+    v[2] = c.x * s;
+    v[3] = c.y * s;
+  }
+};
+
+// Warp w decodes the 512 weights 512 w .. 512 w + 511, 16 per lane in four
+// rounds; in round k lane l takes weights 128 k + 4 l .. + 3, so that each
+// round's 16-byte stores cover 512 contiguous bytes of the output.
+template <int FMT>
+__global__ void dequantw_kernel(const uint8_t* __restrict__ blocks, int64_t n,
+                                float* __restrict__ out) {
+  using D = DQW<FMT>;
   pdl_wait();
   pdl_trigger();
   const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t blk = g / (256 / kNW);
-  if (blk >= nblk) return;
-  const int i0 = (int)(g % (256 / kNW)) * kNW;
-  const uint8_t* b = blocks + blk * 144;
-  const float d = h16(b), dmin = h16(b + 2);
-  const uint8_t* s = b + 4;
-  const int j = i0 >> 5;
-  int sc, m;
-  if (j < 4) {
-    sc = s[j] & 63;
-    m = s[j + 4] & 63;
-  } else {
-    sc = (s[j + 4] & 15) | ((s[j - 4] >> 6) << 4);
-    m = (s[j + 4] >> 4) | ((s[j] >> 6) << 4);
-  }
-  uint8_t q8[kNW];
-  bytesN<kNW>(b + 16 + 32 * (i0 >> 6) + (i0 & 31), q8);
-  float v[kNW];
+  const int l = (int)(g & 31);
+  const int64_t w0 = (g >> 5) * 512;
 #pragma unroll
-  for (int k = 0; k < kNW; ++k) {
-    const int q = (i0 & 32) ? (q8[k] >> 4) : (q8[k] & 15);
-    v[k] = __fmaf_rn(d * (float)sc, (float)q, -(dmin * (float)m));
+  for (int k = 0; k < 4; ++k) {
+    const int64_t w = w0 + 128 * k + 4 * l;
+    if (w >= n) break;
+    float v[4];
+    D::run(blocks + (w / D::QK) * D::BB, (int)(w % D::QK), v);
+    store4(out + w, v[0], v[1], v[2], v[3]);
   }
-  storeN<kNW>(out + g * kNW, v);
 }
 
-__global__ void dequant8_q6k_kernel(const uint8_t* __restrict__ blocks, int64_t nblk,
-                                    float* __restrict__ out) {
-  pdl_wait();
-  pdl_trigger();
-  const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t blk = g / (256 / kNW);
-  if (blk >= nblk) return;
-  const int i0 = (int)(g % (256 / kNW)) * kNW;
-  const uint8_t* b = blocks + blk * 210;
-  const int h = i0 >> 7, r = (i0 >> 5) & 3, l0 = i0 & 31;   // i = 128h + 32r + l
-  uint8_t ql[kNW], qh[kNW];
-  bytesN<kNW>(b + 64 * h + l0 + ((r & 1) ? 32 : 0), ql);
-  bytesN<kNW>(b + 128 + 32 * h + l0, qh);
-  const int sc = (int)(int8_t)b[192 + (i0 >> 4)];
-  const float d = h16(b + 208);
-  float v[kNW];
-#pragma unroll
-  for (int k = 0; k < kNW; ++k) {
-    const int lo = (r & 2) ? (ql[k] >> 4) : (ql[k] & 15);
-    const int hi = (qh[k] >> (2 * r)) & 3;
-    const int q = lo | (hi << 4);
-    v[k] = d * (float)sc * (float)(q - 32);
-  }
-  storeN<kNW>(out + g * kNW, v);
-}
-
+// Q8_0: thread g decodes weights 8g .. 8g + 7 (a quarter block), two 16-byte
+// stores (measured faster for this format than the warp-interleaved form).
 __global__ void dequant8_q80_kernel(const uint8_t* __restrict__ blocks, int64_t nblk,
                                     float* __restrict__ out) {
   pdl_wait();
@@ -167,15 +247,14 @@ __global__ void dequant8_q80_kernel(const uint8_t* __restrict__ blocks, int64_t 
   const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t blk = g >> 2;
   if (blk >= nblk) return;
-  const int i0 = (int)(g & 3) * 8;
   const uint8_t* b = blocks + blk * 34;
-  uint8_t q8[8];
-  bytes8(b + 2 + i0, q8);
+  const int i0 = (int)(g & 3) * 8;
+  const uint32_t q0 = bytes4(b + 2 + i0), q1 = bytes4(b + 6 + i0);
   const float d = h16(b);
-  float v[8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) v[k] = d * (float)(int8_t)q8[k];
-  store8(out + g * 8, v);
+  store4(out + g * 8, d * (float)(int8_t)(q0 & 0xFF), d * (float)(int8_t)((q0 >> 8) & 0xFF),
+         d * (float)(int8_t)((q0 >> 16) & 0xFF), d * (float)(int8_t)(q0 >> 24));
+  store4(out + g * 8 + 4, d * (float)(int8_t)(q1 & 0xFF), d * (float)(int8_t)((q1 >> 8) & 0xFF),
+         d * (float)(int8_t)((q1 >> 16) & 0xFF), d * (float)(int8_t)(q1 >> 24));
 }
 
 // Q4_0: w = d*(q - 8); byte j of qs: weight j (low nibble), j+16 (high).
@@ -290,12 +369,18 @@ int launch_dequant(int fmt, const void* blocks, int64_t n, float* out, cudaStrea
   const int threads = 256;
   const int64_t grid = (n + threads - 1) / threads;
   const uint8_t* b = (const uint8_t*)blocks;
-  if (((uintptr_t)out & 15) == 0 && (fmt == DQ_Q4_K || fmt == DQ_Q6_K || fmt == DQ_Q8_0)) {
-    const dim3 g8((unsigned)((n / 8 + threads - 1) / threads));
-    const dim3 gw((unsigned)((n / kNW + threads - 1) / threads));
-    if (fmt == DQ_Q4_K) launch_pdl(dequant8_q4k_kernel, gw, dim3(threads), 0, s, 0, b, n / 256, out);
-    else if (fmt == DQ_Q6_K) launch_pdl(dequant8_q6k_kernel, gw, dim3(threads), 0, s, 0, b, n / 256, out);
-    else launch_pdl(dequant8_q80_kernel, g8, dim3(threads), 0, s, 0, b, n / 32, out);
+  if (((uintptr_t)out & 15) == 0) {
+    // the wide forms: one warp per 512 weights (Q8_0: one thread per 8)
+    const dim3 gw((unsigned)(((n + 511) / 512 * 32 + threads - 1) / threads));
+    if (fmt == DQ_Q4_K) launch_pdl(dequantw_kernel<DQ_Q4_K>, gw, dim3(threads), 0, s, 0, b, n, out);
+    else if (fmt == DQ_Q6_K) launch_pdl(dequantw_kernel<DQ_Q6_K>, gw, dim3(threads), 0, s, 0, b, n, out);
+    else if (fmt == DQ_Q5_K) launch_pdl(dequantw_kernel<DQ_Q5_K>, gw, dim3(threads), 0, s, 0, b, n, out);
+    else if (fmt == DQ_Q4_0) launch_pdl(dequantw_kernel<DQ_Q4_0>, gw, dim3(threads), 0, s, 0, b, n, out);
+    else if (fmt == DQ_Q2_K) launch_pdl(dequantw_kernel<DQ_Q2_K>, gw, dim3(threads), 0, s, 0, b, n, out);
+    else if (fmt == DQ_Q3_K) launch_pdl(dequantw_kernel<DQ_Q3_K>, gw, dim3(threads), 0, s, 0, b, n, out);
+    else if (fmt == DQ_NVFP4) launch_pdl(dequantw_kernel<DQ_NVFP4>, gw, dim3(threads), 0, s, 0, b, n, out);
+    else launch_pdl(dequant8_q80_kernel, dim3((unsigned)((n / 8 + threads - 1) / threads)),
+                    dim3(threads), 0, s, 0, b, n / 32, out);
     return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
   }
   if (fmt == DQ_Q4_K) launch_pdl(dequant_q4k_kernel, dim3((unsigned)grid), dim3(threads), 0, s, 0, b, n / 256, out);

@@ -35,20 +35,25 @@ def test_dequant_bit_exact_random(dq, orc, fmt, qk):
     ref = orc.dequant(fmt, raw, n)
     assert got.view(np.uint32).tolist() == ref.view(np.uint32).tolist()
     # an output 4 bytes past a 16-byte boundary: the one-weight-per-thread
-    # form (the 16-byte aligned output above takes the 8-wide form for Q4_K,
-    # Q6_K and Q8_0)
+    # form (the 16-byte aligned output above takes the wide form for Q4_K,
+    # Q6_K and Q8_0: one warp per 512 weights)
     buf = torch.full((n + 4,), float("nan"), dtype=torch.float32, device="cuda")
     dq.dequant(fmt, dev_bytes(raw), n, out=buf[1:n + 1])
     got1 = buf[1:n + 1].cpu().numpy()
     assert got1.view(np.uint32).tolist() == ref.view(np.uint32).tolist()
     assert np.isnan(buf[0].item()) and np.isnan(buf[n + 1].item())
-    # blocks 2 bytes past a 16-byte boundary (Q4_K's wide form then reads
-    # 16-bit words instead of 16-byte vectors)
+    # blocks 2 bytes past a 16-byte boundary (the wide forms read 16-bit
+    # words)
     raw_t = torch.from_numpy(np.ascontiguousarray(raw).view(np.uint8).reshape(-1))
     bb = torch.zeros(raw_t.numel() + 16, dtype=torch.uint8, device="cuda")
     bb[2:2 + raw_t.numel()].copy_(raw_t)
     got2 = dq.dequant(fmt, bb[2:2 + raw_t.numel()], n).cpu().numpy()
     assert got2.view(np.uint32).tolist() == ref.view(np.uint32).tolist()
+    # three blocks fewer: the last warp's 512 weights end part-way (the
+    # blocks' prefix decodes to the weights' prefix)
+    n3 = n - 3 * qk
+    got3 = dq.dequant(fmt, dev_bytes(raw.reshape(-1)[:raw.size * n3 // n]), n3).cpu().numpy()
+    assert got3.view(np.uint32).tolist() == ref[:n3].view(np.uint32).tolist()
 
 
 @pytest.mark.parametrize("fname,fmt,qk", [("q4_k_blocks.txt", Q4_K, 256),
