@@ -767,6 +767,8 @@ def bench_moe(torch, dq, cfg, T, reps=20):
     s.wait_stream(torch.cuda.current_stream())
     graphs = []
     with torch.cuda.stream(s):
+        fwd(0)   # once on the capture stream outside capture (sets up its side stream)
+        torch.cuda.synchronize()
         for r in range(ROTATE):
             gr = torch.cuda.CUDAGraph()
             with torch.cuda.graph(gr, stream=s):

@@ -92,6 +92,26 @@ int check_desc(const dq_moe_desc* d, int T) {
 
 }  // namespace
 
+int dqmoe::moe_forward_checked(const dq_moe_desc* desc, const void* x, int x_dtype, int T,
+                               float* y, void* ws, size_t ws_bytes, int32_t* topk_idx,
+                               float* topk_gate, float* logits, void* stream, bool side) {
+  int rc = check_desc(desc, T);
+  if (rc != DQ_OK) return rc;
+  if (!x || !y || !dtype_ok(x_dtype)) return DQ_ERR_ARG;
+  // the experts run on 16-bit tensor-core operands: fp32 activations would
+  // be held to a bar (1e-5) that path cannot meet, so they are refused
+  if (x_dtype == DQ_F32) return DQ_ERR_UNSUPPORTED;
+  if (!aligned(x, 16) || !aligned(y, 16)) return DQ_ERR_ALIGN;
+  if ((topk_idx && !aligned(topk_idx, 4)) || (topk_gate && !aligned(topk_gate, 4)) ||
+      (logits && !aligned(logits, 4)))
+    return DQ_ERR_ALIGN;
+  if (!ws) return DQ_ERR_WORKSPACE;
+  if (!aligned(ws, 256)) return DQ_ERR_ALIGN;
+  if (ws_bytes < moe_plan(*desc, T).total) return DQ_ERR_WORKSPACE;
+  return launch_moe_forward(*desc, x, x_dtype, T, y, ws, topk_idx, topk_gate, logits,
+                            (cudaStream_t)stream, nullptr, 3, side);
+}
+
 extern "C" {
 
 int dq_block_geometry(int fmt, int* weights_per_block, int* bytes_per_block) {
@@ -162,22 +182,10 @@ int dq_moe_permute(const int32_t* topk_idx, int T, int top_k, int E, int32_t* of
 int dq_moe_forward(const dq_moe_desc* desc, const void* x, int x_dtype, int T, float* y, void* ws,
                    size_t ws_bytes, int32_t* topk_idx, float* topk_gate, float* logits,
                    void* stream) {
-  int rc = check_desc(desc, T);
-  if (rc != DQ_OK) return rc;
-  if (!x || !y || !dtype_ok(x_dtype)) return DQ_ERR_ARG;
-  // the experts run on 16-bit tensor-core operands: fp32 activations would
-  // be held to a bar (1e-5) that path cannot meet, so they are refused
-  if (x_dtype == DQ_F32) return DQ_ERR_UNSUPPORTED;
-  if (!aligned(x, 16) || !aligned(y, 16)) return DQ_ERR_ALIGN;
-  if ((topk_idx && !aligned(topk_idx, 4)) || (topk_gate && !aligned(topk_gate, 4)) ||
-      (logits && !aligned(logits, 4)))
-    return DQ_ERR_ALIGN;
-  if (!ws) return DQ_ERR_WORKSPACE;
-  if (!aligned(ws, 256)) return DQ_ERR_ALIGN;
-  if (ws_bytes < moe_plan(*desc, T).total) return DQ_ERR_WORKSPACE;
-  return launch_moe_forward(*desc, x, x_dtype, T, y, ws, topk_idx, topk_gate, logits,
-                            (cudaStream_t)stream);
+  return dqmoe::moe_forward_checked(desc, x, x_dtype, T, y, ws, ws_bytes, topk_idx, topk_gate,
+                                    logits, stream, true);
 }
+
 
 int dq_expert_cache_create(const dq_moe_desc* d, int slots, void* slot_gate, void* slot_up,
                            void* slot_down, int max_tokens, int phases, dq_expert_cache** cache) {

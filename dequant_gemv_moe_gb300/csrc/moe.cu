@@ -18,6 +18,9 @@
 // so only the touched experts' packed weights are streamed from HBM.
 #include <algorithm>
 #include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "moe_plan.h"
 #include "qgemv_mma.cuh"
@@ -1293,11 +1296,72 @@ int launch_permute(const int32_t* idx, int T, int k, int E, int32_t* offsets, in
   return cudaGetLastError() == cudaSuccess ? DQ_OK : DQ_ERR_CUDA;
 }
 
+namespace {
+
+// A second stream per (device, caller stream), of the device's highest
+// priority, for the general expert kernels that run beside the one-token
+// ones; forked from and joined back into the caller's stream with events.
+// Created on first use outside stream capture and kept until the process
+// exits; `mu` orders the fork, the launches and the join of concurrent calls
+// on the same caller stream.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  std::mutex mu;
+};
+std::mutex g_side_mu;
+std::map<std::pair<int, cudaStream_t>, SideStream*> g_side;
+
+// The side stream of `s` on the current device, or null (none yet and `s` is
+// being captured, or creation failed): the caller then stays on `s`.
+SideStream* side_stream(cudaStream_t s) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  std::lock_guard<std::mutex> lock(g_side_mu);
+  auto it = g_side.find({dev, s});
+  if (it != g_side.end()) return it->second;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
+    return nullptr;
+  int least = 0, greatest = 0;
+  if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return nullptr;
+  SideStream* ss = new SideStream;
+  if (cudaStreamCreateWithPriority(&ss->s, cudaStreamNonBlocking, greatest) != cudaSuccess ||
+      cudaEventCreateWithFlags(&ss->fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&ss->join, cudaEventDisableTiming) != cudaSuccess) {
+    cudaGetLastError();
+    delete ss;   // handles created before the failure stay with the process
+    return nullptr;
+  }
+  g_side[{dev, s}] = ss;
+  return ss;
+}
+
+// Joins the side stream back into the caller's stream when the layer's
+// launches are enqueued (also on an early error return), then releases the
+// side stream's lock.
+struct ForkJoin {
+  SideStream* ss = nullptr;
+  cudaStream_t main = nullptr;
+  std::unique_lock<std::mutex> lock;
+  int join() {
+    if (!ss) return DQ_OK;
+    const bool ok = cudaEventRecord(ss->join, ss->s) == cudaSuccess &&
+                    cudaStreamWaitEvent(main, ss->join, 0) == cudaSuccess;
+    ss = nullptr;
+    if (lock.owns_lock()) lock.unlock();
+    return ok ? DQ_OK : DQ_ERR_CUDA;
+  }
+  ~ForkJoin() { join(); }
+};
+
+}  // namespace
+
 // stages: 1 = router and top-k, 2 = the rest (permute, experts, combine), 3 = both.
 // ms (nullable): the streamed layer's slot cache and copy/compute phases.
 int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, float* y, void* ws,
                        int32_t* topk_idx, float* topk_gate, float* logits, cudaStream_t s,
-                       const MoeStream* ms, int stages) {
+                       const MoeStream* ms, int stages, bool side) {
   const MoePlan pl = moe_plan(d, T, ms == nullptr);
   uint8_t* w = (uint8_t*)ws;
   float* part = (float*)(w + pl.off_part);
@@ -1364,6 +1428,26 @@ int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, floa
     xh_inv = xinvt;
   }
 
+  // one-token groups beside the general kernels (T > 1): the general and
+  // tensor-core kernels run on a side stream of higher priority, so that
+  // their CTAs are placed first, concurrently with the one-token kernels on
+  // `s` (both read the same inputs and write different positions of h and
+  // ypos)
+  cudaStream_t sg = s;
+  ForkJoin fj;
+  if (side && !ms && general && pl.single) {
+    SideStream* ss = side_stream(s);
+    if (ss) {
+      fj.lock = std::unique_lock<std::mutex>(ss->mu);
+      if (cudaEventRecord(ss->fork, s) != cudaSuccess ||
+          cudaStreamWaitEvent(ss->s, ss->fork, 0) != cudaSuccess)
+        return DQ_ERR_CUDA;
+      fj.ss = ss;
+      fj.main = s;
+      sg = ss->s;
+    }
+  }
+
   GroupedParams gu;
   memset(&gu, 0, sizeof(gu));
   gu.Wa = (const uint8_t*)d.w_gate;
@@ -1389,7 +1473,7 @@ int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, floa
   gu.rows_per_expert = d.ffn;
   if (!ms) {
     if (general) {
-      rc = launch_grouped_fmt<true>(d.fmt, pl.NT, gu, pl.G_max * gu.tiles, s, d.E, d.n_shared);
+      rc = launch_grouped_fmt<true>(d.fmt, pl.NT, gu, pl.G_max * gu.tiles, sg, d.E, d.n_shared);
       if (rc != DQ_OK) return rc;
     }
     if (pl.single) {
@@ -1416,22 +1500,22 @@ int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, floa
 
   // wide units: gathered fp16 rows, tensor-core gate and up GEMMs, SwiGLU
   if (pl.wide) {
-    rc = launch_gather_x16(units, nunits, pl.U_max, tok, xh, xh_inv, d.hidden, x16, xinv, s);
+    rc = launch_gather_x16(units, nunits, pl.U_max, tok, xh, xh_inv, d.hidden, x16, xinv, sg);
     if (rc != DQ_OK) return rc;
     rc = launch_tc_gemm(d.fmt, d.w_gate, d.sh_gate, d.E, d.n_shared, d.ffn, d.hidden, units,
-                        nunits, pl.U_max, x16, pl.NP, xinv, G, d.ffn, s);
+                        nunits, pl.U_max, x16, pl.NP, xinv, G, d.ffn, sg);
     if (rc != DQ_OK) return rc;
     rc = launch_tc_gemm(d.fmt, d.w_up, d.sh_up, d.E, d.n_shared, d.ffn, d.hidden, units, nunits,
-                        pl.U_max, x16, pl.NP, xinv, U, d.ffn, s);
+                        pl.U_max, x16, pl.NP, xinv, U, d.ffn, sg);
     if (rc != DQ_OK) return rc;
-    rc = launch_swiglu_wide(units, nunits, pl.U_max, G, U, d.ffn, h, s);
+    rc = launch_swiglu_wide(units, nunits, pl.U_max, G, U, d.ffn, h, sg);
     if (rc != DQ_OK) return rc;
   }
 
   // h -> fp16 with a power-of-two scale per position (all positions), for
   // the grouped mma.sync kernels
   if (general) {
-    rc = launch_x16_rows(h, DQ_F32, (int)pl.NP, d.ffn, h16, hinv, s);
+    rc = launch_x16_rows(h, DQ_F32, (int)pl.NP, d.ffn, h16, hinv, sg);
     if (rc != DQ_OK) return rc;
   }
 
@@ -1459,7 +1543,7 @@ int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, floa
   dn.rows_per_expert = d.hidden;
   if (!ms) {
     if (general) {
-      rc = launch_grouped_fmt<false>(d.fmt, pl.NT, dn, pl.G_max * dn.tiles * dn.ksplit, s, d.E,
+      rc = launch_grouped_fmt<false>(d.fmt, pl.NT, dn, pl.G_max * dn.tiles * dn.ksplit, sg, d.E,
                                      d.n_shared);
       if (rc != DQ_OK) return rc;
     }
@@ -1483,10 +1567,13 @@ int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, floa
   }
   if (pl.wide) {
     rc = launch_tc_gemm(d.fmt, d.w_down, d.sh_down, d.E, d.n_shared, d.hidden, d.ffn, units,
-                        nunits, pl.U_max, h16, pl.NP, hinv, ypos, d.hidden, s);
+                        nunits, pl.U_max, h16, pl.NP, hinv, ypos, d.hidden, sg);
     if (rc != DQ_OK) return rc;
   }
 
+  // the join, before the combine reads every position
+  rc = fj.join();
+  if (rc != DQ_OK) return rc;
   const int64_t n4 = (int64_t)T * d.hidden / 4;
   const int cgrid = (int)std::min<int64_t>((n4 + 255) / 256, 4096);
   launch_pdl(combine_kernel, dim3(cgrid), dim3(256), 0, s, 0, ypos, inv, gate, T, d.top_k,

@@ -53,9 +53,16 @@ int launch_grouped_b1(bool gateup, const dq_moe_desc& d, const int4* groups1,
                       const int* n_groups1, int g1_max, int* claim, const void* x, int xdt,
                       int64_t xstride, float* out, int64_t out_stride, cudaStream_t s);
 
+// side: the general expert kernels may run on a second stream beside the
+// one-token ones (created on first use; dq_moe_forward_noalloc passes false).
 int launch_moe_forward(const dq_moe_desc& d, const void* x, int xdt, int T, float* y, void* ws,
                        int32_t* topk_idx, float* topk_gate, float* logits, cudaStream_t s,
-                       const MoeStream* ms = nullptr, int stages = 3);
+                       const MoeStream* ms = nullptr, int stages = 3, bool side = true);
+
+// dq_moe_forward's argument checks and launch, with the side-stream choice.
+int moe_forward_checked(const dq_moe_desc* desc, const void* x, int x_dtype, int T, float* y,
+                        void* ws, size_t ws_bytes, int32_t* topk_idx, float* topk_gate,
+                        float* logits, void* stream, bool side);
 
 }  // namespace dqmoe
 

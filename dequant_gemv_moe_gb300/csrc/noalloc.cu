@@ -17,6 +17,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "moe_plan.h"
 
 namespace dqmoe {
 
@@ -63,6 +64,7 @@ extern "C" int dq_moe_forward_noalloc(const dq_moe_desc* desc, const void* x, in
   void* ws = nullptr;
   const int src = scratch_on_current_device((cudaStream_t)stream, &ws);
   if (src != DQ_OK) return src;
-  return dq_moe_forward(desc, x, x_dtype, T, y, ws, (size_t)DQ_NOALLOC_SCRATCH_BYTES, topk_idx,
-                        topk_gate, logits, stream);
+  // one stream only: the layer's second stream would be created on first use
+  return moe_forward_checked(desc, x, x_dtype, T, y, ws, (size_t)DQ_NOALLOC_SCRATCH_BYTES,
+                             topk_idx, topk_gate, logits, stream, false);
 }

@@ -299,9 +299,17 @@ int dq_moe_permute(const int32_t* topk_idx, int T, int top_k, int E,
  *              256-byte aligned; contents on entry are ignored.
  *   topk_idx, topk_gate, logits : optional device outputs as in
  *              dq_moe_router (NULL to skip).
- * All launches go on `stream` with no host synchronisation, so the layer is
+ * The launches go on `stream` with no host synchronisation, so the layer is
  * capturable in one CUDA graph ([KTransformers, §技术原理]: one graph call
- * per decode step).
+ * per decode step).  When experts with one token sit beside experts with
+ * more (T > 1 and at most E/2 picks), the kernels of the larger groups run
+ * on a second stream of the library's (highest priority), forked from
+ * `stream` and joined back into it before the layer's last kernel, so the
+ * call is ordered on `stream` exactly as one stream would be; the results do
+ * not depend on it.  That stream (one per device and caller stream) is
+ * created by the first such call made outside stream capture and kept until
+ * the process exits; such a call captured on a stream that has not run one
+ * outside capture stays on `stream`.
  * Errors: DQ_ERR_ARG, DQ_ERR_ALIGN (x, y not 16-byte aligned, ws not 256-byte
  *         aligned, an optional output not 4-byte aligned), DQ_ERR_UNSUPPORTED
  *         (also fp32 x), DQ_ERR_WORKSPACE, DQ_ERR_CUDA. */
@@ -317,7 +325,9 @@ int dq_moe_forward(const dq_moe_desc* desc, const void* x, int x_dtype, int T,
  * counterpart; it exists for such callers only.
  * Scratch comes from one fixed array of DQ_NOALLOC_SCRATCH_BYTES (32 MiB)
  * inside the library: every GPU that loads the library keeps that much
- * device memory until the process exits.  No call allocates or frees memory.
+ * device memory until the process exits.  No call allocates or frees memory,
+ * and none creates the second stream dq_moe_forward may use: every launch
+ * goes on `stream`.
  * The first call on a device (with that device current) looks up the array's
  * device address once (cudaGetSymbolAddress); make that first call before any
  * stream capture: a first call made while `stream` is capturing is refused

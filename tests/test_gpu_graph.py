@@ -31,11 +31,17 @@ def dq():
     return dq
 
 
-def _capture(fn):
+def _capture(fn, warm=False):
+    """fn captured on a new stream; warm: fn runs once on that stream first,
+    outside capture (a layer with one-token experts beside the general kernels
+    then also captures its side stream's branch)."""
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(s):
+        if warm:
+            fn()
+            torch.cuda.synchronize()
         with torch.cuda.graph(g, stream=s):
             fn()
     torch.cuda.current_stream().wait_stream(s)
@@ -46,6 +52,9 @@ def _capture(fn):
     (16, 4, 1024, 512, 1, 1, 2),     # decode, one token, shared expert
     (16, 4, 1024, 512, 1, 8, 1),
     (4, 2, 512, 512, 0, 80, 1),      # ~40 tokens per expert: tcgen05 path inside
+    # one-token experts (side stream) beside the general kernels (shared
+    # expert, experts with two tokens), forked and joined inside the graph
+    (64, 2, 1024, 512, 1, 4, 2),
 ])
 def test_moe_layer_graph_replay(dq, orc, E, k, H, F, ns, T, xdt):
     w = synth.moe_weights(7700 + E + T, E, H, F, ns, 1)
@@ -63,7 +72,7 @@ def test_moe_layer_graph_replay(dq, orc, E, k, H, F, ns, T, xdt):
     xbuf = xs[0].clone()
     ybuf = torch.empty(T, H, dtype=torch.float32, device="cuda")
     ws = torch.empty(dq.moe_workspace_size(desc, T), dtype=torch.uint8, device="cuda")
-    graph = _capture(lambda: dq.moe_forward(desc, xbuf, y=ybuf, ws=ws))
+    graph = _capture(lambda: dq.moe_forward(desc, xbuf, y=ybuf, ws=ws), warm=True)
     for i in (1, 2, 0, 1):
         xbuf.copy_(xs[i])
         graph.replay()

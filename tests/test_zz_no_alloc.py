@@ -44,6 +44,9 @@ def _noalloc(dq, desc, x, xdt, T, y, idx):
 @pytest.mark.parametrize("fmt,E,k,H,F,ns,T,xdt", [
     (1, 8, 2, 512, 1024, 1, 5, 1),
     (3, 16, 4, 1024, 512, 0, 16, 2),
+    # one-token experts beside the shared expert's group: dq_moe_forward may
+    # fork a second stream here, the allocation-free entry stays on one
+    (1, 64, 2, 1024, 512, 1, 4, 2),
 ])
 def test_noalloc_matches_workspace_entry(fmt, E, k, H, F, ns, T, xdt):
     assert torch.cuda.is_available(), "GPU test"
