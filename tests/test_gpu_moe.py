@@ -171,8 +171,7 @@ def _moe_case(dq, orc, fmt, E, k, H, F, ns, T, xdt, seed, tokens=None, cached=No
     (NVFP4, 8, 2, 512, 512, 0, 30, 1),
     (NVFP4, 4, 2, 768, 512, 1, 50, 2),
     (NVFP4, 2, 2, 512, 256, 1, 90, 1),
-    # one token with shared experts: the shared experts' products run before
-    # the router (hidden > 1024: the streaming router, which waits at its end;
+    # one token with shared experts (hidden > 1024: the streaming router;
     # hidden 1024: the tiled router)
     (Q4_K, 16, 4, 2048, 512, 2, 1, 2),
     (Q8_0, 8, 2, 2048, 1024, 1, 1, 1),
