@@ -431,7 +431,11 @@ def test_low_bit_scale_regimes(dq, orc, fmt, xdt, B):
     # 1, 2^-14, subnormal, zero) and, for Q2_K, dmin far above or below d:
     # every row within tolerance of its own magnitude, on the batch-1
     # block-diagonal kernel (scales in fp32 after the products) and on the
-    # general one (per-row power-of-two folding)
+    # general one (per-row power-of-two folding).  Each row's error is taken
+    # over its own largest |y| (stricter than the max-normalised bar of the
+    # other tests for a row whose sum cancels), hence 4 x TOL; measured worst
+    # on GB300: 1.9 x TOL (Q3_K, fp16 x, batch 2, general kernel), at most
+    # 0.11 x TOL at batch 1
     N, K = 128, 4096
     g = synth.streams(9400 + fmt * 10 + xdt + 100 * B, 2)
     W = synth.quant_matrix(g[0], fmt, N, K)
