@@ -422,7 +422,9 @@ __device__ __forceinline__ void pdl_trigger() {
 }
 
 // Launch with programmatic stream serialization and, for cluster > 0, a
-// thread-block cluster of `cluster` CTAs along x.
+// thread-block cluster of `cluster` CTAs along x, placed by the load-balancing
+// policy (measured on the Llama-3-8B layer step, whose o and down GEMVs run
+// in clusters of 8: 32.72 -> 32.24 us; the spread policy equals the default).
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
                               cudaStream_t s, int cluster, Args&&... args) {
@@ -431,7 +433,7 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[3];
   int n = 0;
   attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[n].val.programmaticStreamSerializationAllowed = 1;
@@ -441,6 +443,9 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
     attr[n].val.clusterDim.x = (unsigned)cluster;
     attr[n].val.clusterDim.y = 1;
     attr[n].val.clusterDim.z = 1;
+    ++n;
+    attr[n].id = cudaLaunchAttributeClusterSchedulingPolicyPreference;
+    attr[n].val.clusterSchedulingPolicyPreference = cudaClusterSchedulingPolicyLoadBalancing;
     ++n;
   }
   cfg.attrs = attr;
